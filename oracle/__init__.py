@@ -1,0 +1,170 @@
+"""Oracle for the paged-KV decode step (fp64, CPU).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers. The product library does
+not import, link or execute anything under ``oracle/``, and nothing here imports
+the product package.
+
+``oracle.c`` holds the arithmetic (bf16 conversion, RoPE table and rotation,
+append, paged and contiguous attention); this module compiles it with gcc into
+``oracle/_build/liboracle.so`` and wraps it with ctypes over numpy arrays.
+``pool.py`` is a plain-Python model of the block pool. Sources of each function
+are cited in ``oracle.c`` and ``pool.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (no fast-math, no FP contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.or_double_from_bf16.argtypes = [ctypes.c_uint16]
+            lib.or_double_from_bf16.restype = f64
+            lib.or_bf16_from_double.argtypes = [f64]
+            lib.or_bf16_from_double.restype = ctypes.c_uint16
+            lib.or_bf16_from_double_array.argtypes = [P, i64, P]
+            lib.or_double_from_bf16_array.argtypes = [P, i64, P]
+            lib.or_rope_table.argtypes = [f64, i32, i32, P]
+            lib.or_rope_rotate.argtypes = [P, i32, i32, P, i32, P]
+            lib.or_slot_mapping.argtypes = [i32, P, i32, P, P]
+            lib.or_slot_mapping.restype = i32
+            lib.or_append.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P]
+            lib.or_append.restype = i32
+            lib.or_paged_attention.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, f64, P, i32]
+            lib.or_paged_attention.restype = i32
+            lib.or_contiguous_attention.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, f64, P]
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# --------------------------------------------------------------- bf16 ------
+
+def bf16_to_f64(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exact."""
+    h = _c(h, np.uint16)
+    out = np.empty(h.shape, np.float64)
+    _load().or_double_from_bf16_array(_p(h), h.size, _p(out))
+    return out
+
+
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 -> bf16 bit patterns, one rounding to nearest-even."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().or_bf16_from_double_array(_p(x), x.size, _p(out))
+    return out
+
+
+def bf16_from_double_scalar(x: float) -> int:
+    return int(_load().or_bf16_from_double(float(x)))
+
+
+# --------------------------------------------------------------- RoPE ------
+
+def rope_table(theta: float, head_dim: int, max_pos: int) -> np.ndarray:
+    """float32 [max_pos][head_dim/2][2] of (cos, sin)."""
+    out = np.empty((max_pos, head_dim // 2, 2), np.float32)
+    _load().or_rope_table(float(theta), head_dim, max_pos, _p(out))
+    return out
+
+
+def rope_rotate(x: np.ndarray, table: np.ndarray, pos: int) -> np.ndarray:
+    """Rotate bf16 vectors x[..., d] (uint16 bits), all at position pos."""
+    x = _c(x, np.uint16)
+    d = x.shape[-1]
+    table = _c(table, np.float32)
+    assert 0 <= pos < table.shape[0] and table.shape[1] * 2 == d
+    y = np.empty_like(x)
+    _load().or_rope_rotate(_p(x), x.size // d, d, _p(table), int(pos), _p(y))
+    return y
+
+
+# ------------------------------------------------------ slots / append ------
+
+def slot_mapping(block_tables: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    bt = _c(block_tables, np.int32)
+    pos = _c(positions, np.int32)
+    out = np.empty(pos.shape, np.int32)
+    _load().or_slot_mapping(pos.shape[0], _p(bt), bt.shape[1], _p(pos), _p(out))
+    return out
+
+
+def append(q, k, v, positions, slot_mapping_, table, k_cache, v_cache):
+    """Returns q_out; writes k_cache / v_cache (uint16 arrays [nb][Hkv][16][d]) in place."""
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k.shape[1]
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+    pos = _c(positions, np.int32); sm = _c(slot_mapping_, np.int32)
+    table = _c(table, np.float32)
+    q_out = np.empty_like(q)
+    st = _load().or_append(B, Hq, Hkv, d, k_cache.shape[0], _p(q), _p(k), _p(v), _p(pos), _p(sm),
+                           _p(table), table.shape[0], _p(q_out), _p(k_cache), _p(v_cache))
+    return q_out, st
+
+
+# ---------------------------------------------------------- attention ------
+
+def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale, nthreads=1):
+    """q uint16 [B][Hq][d]; caches uint16 [nb][Hkv][16][d]; returns float64 [B][Hq][d]."""
+    q = _c(q, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    kc = _c(k_cache, np.uint16); vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32)
+    out = np.empty((B, Hq, d), np.float64)
+    used = _load().or_paged_attention(B, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1],
+                                      _p(cl), float(scale), _p(out), int(nthreads))
+    paged_attention.threads_used = used
+    return out
+
+
+def contiguous_attention(q, K, V, lens, scale):
+    """q uint16 [B][Hq][d]; K, V uint16 [B][Hkv][n_max][d]; returns float64 [B][Hq][d]."""
+    q = _c(q, np.uint16); K = _c(K, np.uint16); V = _c(V, np.uint16)
+    B, Hq, d = q.shape
+    Hkv, n_max = K.shape[1], K.shape[2]
+    ln = _c(lens, np.int32)
+    out = np.empty((B, Hq, d), np.float64)
+    _load().or_contiguous_attention(B, Hq, Hkv, d, n_max, _p(q), _p(K), _p(V), _p(ln), float(scale),
+                                    _p(out))
+    return out

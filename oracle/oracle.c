@@ -1,0 +1,312 @@
+/*
+ * Oracle for the paged-KV decode step: plain, slow, fp64 C on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark load this file. The product library never
+ * links, includes or calls it, and it shares no code, header, table or helper
+ * with the CUDA path.
+ *
+ * What it computes, and where the pages define it:
+ *  - bf16 <-> double conversion from the IEEE-754 binary16-brain definition
+ *    (1 sign, 8 exponent, 7 stored mantissa bits; round to nearest, ties to
+ *    even; overflow to infinity).
+ *  - RoPE table and rotation: "Rotary Position Embedding (RoPE) construction
+ *    and application" in the NJU course brief "端侧大模型推理框架", §2.1
+ *    (components to implement). Pairing (i, i+d/2), angle p * theta^(-2i/d).
+ *  - Append (write_decode_kv): mini-infer README, "decode_batch 关键步骤",
+ *    step 4: the new token's K/V are written back into the block tensor.
+ *  - Slot of a token from the block table: mini-infer README, "项目概述"
+ *    (Paged KV Cache = BlockTable + free-block pool), and the nxmr.cn article,
+ *    §2.1 "KV缓存的内存革命" (logical pages mapped to physical pages).
+ *  - Decode attention with GQA: NJU course brief §2.1, "QKV projection and
+ *    Grouped-Query Attention" (query head j reads KV head j / G, the
+ *    repeat_interleave convention), computed as the plain definition
+ *    softmax(scale * q K^T) V over the request's paged history, in double.
+ *  - Brute-force contiguous attention: the preallocated contiguous per-layer
+ *    KV of the lnwmold.com InferLLM article, §3.4 "KV Cache的优化实现"; used to
+ *    pin the paged walk.
+ *
+ * Every parity function here is pinned by the tests in tests/test_oracle_*.py
+ * against closed forms, brute force and invariants that do not reuse this code.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BLOCK 16
+
+/* ---------------------------------------------------------------- bf16 ---- */
+
+/* bf16 bits -> double. Exact: every bf16 value is a double. */
+double or_double_from_bf16(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> bf16 bits, one rounding, to nearest with ties to even.
+ * The quantum is 2^(E-7) for a value in [2^E, 2^(E+1)), E clamped below at
+ * -126 (the subnormal range has the fixed quantum 2^-133). The value is scaled
+ * so the quantum becomes 1, rounded to an integer in the default rounding mode
+ * (nearest-even), and scaled back; the result is a bf16 value, so converting it
+ * to float is exact and its top 16 bits are the answer. NaN gives the quiet NaN
+ * 0x7FC0 with the input's sign; values at or beyond 2^128 after rounding give
+ * infinity. */
+uint16_t or_bf16_from_double(double x) {
+    if (isnan(x)) return (uint16_t)(signbit(x) ? 0xFFC0u : 0x7FC0u);
+    const uint16_t sgn = (uint16_t)(signbit(x) ? 0x8000u : 0u);
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sgn | 0x7F80u);
+    if (a == 0.0) return sgn;
+    int e2;
+    (void)frexp(a, &e2); /* a = f * 2^e2 with f in [0.5, 1) */
+    int E = e2 - 1;      /* a in [2^E, 2^(E+1)) */
+    if (E < -126) E = -126;
+    const double n = nearbyint(ldexp(a, 7 - E));
+    const double r = ldexp(n, E - 7);
+    if (r >= 0x1p128) return (uint16_t)(sgn | 0x7F80u);
+    const float f = (float)r; /* exact */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sgn | (uint16_t)(u >> 16));
+}
+
+void or_bf16_from_double_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_from_double(x[i]);
+}
+
+void or_double_from_bf16_array(const uint16_t* h, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_double_from_bf16(h[i]);
+}
+
+/* ---------------------------------------------------------------- RoPE ---- */
+
+/* cos/sin table, layout [max_pos][d/2][2] fp32: entry (p, i) holds
+ * cos(p * theta^(-2i/d)) and sin(...) evaluated in double and rounded once to
+ * fp32. */
+void or_rope_table(double theta, int32_t d, int32_t max_pos, float* out) {
+    const int32_t half = d / 2;
+    for (int32_t p = 0; p < max_pos; ++p) {
+        for (int32_t i = 0; i < half; ++i) {
+            const double inv_freq = 1.0 / pow(theta, (2.0 * (double)i) / (double)d);
+            const double ang = (double)p * inv_freq;
+            out[((int64_t)p * half + i) * 2 + 0] = (float)cos(ang);
+            out[((int64_t)p * half + i) * 2 + 1] = (float)sin(ang);
+        }
+    }
+}
+
+/* Rotate one head vector x[d] (bf16 bits) with the table row cs[d/2][2]:
+ *   y[i]       = x[i]       * cos_i - x[i+d/2] * sin_i
+ *   y[i + d/2] = x[i + d/2] * cos_i + x[i]     * sin_i
+ * in double (each product of a bf16 and an fp32 value is exact in double, so
+ * the only rounding before the final one is the add), then one rounding to
+ * bf16. */
+static void rope_rotate_vec(const uint16_t* x, int32_t d, const float* cs, uint16_t* y) {
+    const int32_t half = d / 2;
+    for (int32_t i = 0; i < half; ++i) {
+        const double x1 = or_double_from_bf16(x[i]);
+        const double x2 = or_double_from_bf16(x[i + half]);
+        const double c = (double)cs[2 * i + 0];
+        const double s = (double)cs[2 * i + 1];
+        const double p1 = x1 * c;
+        const double p2 = x2 * s;
+        const double p3 = x2 * c;
+        const double p4 = x1 * s;
+        y[i] = or_bf16_from_double(p1 - p2);
+        y[i + half] = or_bf16_from_double(p3 + p4);
+    }
+}
+
+/* Rotate n_vec head vectors of length d, all at position pos. */
+void or_rope_rotate(const uint16_t* x, int32_t n_vec, int32_t d, const float* table,
+                    int32_t pos, uint16_t* y) {
+    const float* cs = table + (int64_t)pos * (d / 2) * 2;
+    for (int32_t v = 0; v < n_vec; ++v) rope_rotate_vec(x + (int64_t)v * d, d, cs, y + (int64_t)v * d);
+}
+
+/* ------------------------------------------------------ slots and append ---- */
+
+/* Slot of token `pos` of request b through its block table row:
+ *   slot = table[b][pos / 16] * 16 + pos % 16.
+ * Returns 0, or -1 when pos is outside the table row or the block id is < 0. */
+int32_t or_slot_mapping(int32_t B, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* pos, int32_t* slot_out) {
+    int32_t bad = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t p = pos[b];
+        if (p < 0 || p / OR_BLOCK >= max_blocks_per_seq) { slot_out[b] = -1; bad = -1; continue; }
+        const int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + p / OR_BLOCK];
+        if (blk < 0) { slot_out[b] = -1; bad = -1; continue; }
+        slot_out[b] = blk * OR_BLOCK + p % OR_BLOCK;
+    }
+    return bad;
+}
+
+/* Append one new token per request:
+ *   q_out[b][j]   = RoPE(q[b][j], positions[b])            for every query head j
+ *   k_cache[slot] = RoPE(k[b][h], positions[b])            for every KV head h
+ *   v_cache[slot] = v[b][h]                                (not rotated)
+ * with the cache layout [num_blocks][Hkv][16][d], slot = slot_mapping[b]
+ * (block slot/16, offset slot%16). No other byte of the caches changes.
+ * Returns 0, or -1 if some slot or position is out of range (that request's
+ * cache write is skipped, its q_out row is still written when the position is
+ * valid). */
+int32_t or_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks,
+                  const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* positions, const int32_t* slot_mapping,
+                  const float* table, int32_t max_pos,
+                  uint16_t* q_out, uint16_t* k_cache, uint16_t* v_cache) {
+    int32_t status = 0;
+    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t p = positions[b];
+        if (p < 0 || p >= max_pos) { status = -1; continue; }
+        or_rope_rotate(q + (int64_t)b * Hq * d, Hq, d, table, p, q_out + (int64_t)b * Hq * d);
+        const int32_t slot = slot_mapping[b];
+        if (slot < 0 || slot / OR_BLOCK >= num_blocks) { status = -1; continue; }
+        const int64_t blk = slot / OR_BLOCK, off = slot % OR_BLOCK;
+        for (int32_t h = 0; h < Hkv; ++h) {
+            const int64_t dst = ((blk * Hkv + h) * OR_BLOCK + off) * d;
+            or_rope_rotate(k + ((int64_t)b * Hkv + h) * d, 1, d, table, p, tmp);
+            memcpy(k_cache + dst, tmp, sizeof(uint16_t) * (size_t)d);
+            memcpy(v_cache + dst, v + ((int64_t)b * Hkv + h) * d, sizeof(uint16_t) * (size_t)d);
+        }
+    }
+    free(tmp);
+    return status;
+}
+
+/* ------------------------------------------------------------ attention ---- */
+
+typedef struct {
+    int32_t B, Hq, Hkv, d, max_blocks_per_seq;
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    double scale;
+    double* out;
+    int64_t row_begin, row_end; /* rows are (b, j) pairs, b-major */
+} or_attn_job;
+
+/* One output row: request b, query head j, KV head h = j / G. Walks the block
+ * table token by token: K_t and V_t live in block table[b][t/16] at offset
+ * t%16. s_t = scale * <q, K_t>; out = sum_t exp(s_t - max s) V_t / sum_t
+ * exp(s_t - max s). Context length <= 0 gives a zero row. */
+static void attn_row(const or_attn_job* a, int32_t b, int32_t j, double* s) {
+    const int32_t d = a->d, G = a->Hq / a->Hkv, h = j / G;
+    double* o = a->out + ((int64_t)b * a->Hq + j) * d;
+    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+    const int32_t n = a->context_lens[b];
+    if (n <= 0) return;
+    const uint16_t* qr = a->q + ((int64_t)b * a->Hq + j) * d;
+    double m = -INFINITY;
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint16_t* kt = a->k_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        double acc = 0.0;
+        for (int32_t i = 0; i < d; ++i) acc += or_double_from_bf16(qr[i]) * or_double_from_bf16(kt[i]);
+        s[t] = a->scale * acc;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int32_t t = 0; t < n; ++t) {
+        const double w = exp(s[t] - m);
+        l += w;
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint16_t* vt = a->v_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        for (int32_t i = 0; i < d; ++i) o[i] += w * or_double_from_bf16(vt[i]);
+    }
+    for (int32_t i = 0; i < d; ++i) o[i] /= l;
+}
+
+static void* attn_worker(void* arg) {
+    const or_attn_job* a = (const or_attn_job*)arg;
+    int32_t nmax = 1;
+    for (int32_t b = 0; b < a->B; ++b)
+        if (a->context_lens[b] > nmax) nmax = a->context_lens[b];
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    for (int64_t r = a->row_begin; r < a->row_end; ++r)
+        attn_row(a, (int32_t)(r / a->Hq), (int32_t)(r % a->Hq), s);
+    free(s);
+    return NULL;
+}
+
+/* Paged decode attention over rows (b, j) for b < B, j < Hq; out is double
+ * [B][Hq][d]. Rows are independent; nthreads > 1 splits them into contiguous
+ * ranges run on POSIX threads, which leaves every row's arithmetic unchanged.
+ * Returns the number of threads used. */
+int32_t or_paged_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                           const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, double scale, double* out,
+                           int32_t nthreads) {
+    const int64_t rows = (int64_t)B * Hq;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = (int32_t)(rows > 0 ? rows : 1);
+    or_attn_job* jobs = (or_attn_job*)malloc(sizeof(or_attn_job) * (size_t)nthreads);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int32_t t = 0; t < nthreads; ++t) {
+        or_attn_job* a = &jobs[t];
+        a->B = B; a->Hq = Hq; a->Hkv = Hkv; a->d = d; a->max_blocks_per_seq = max_blocks_per_seq;
+        a->q = q; a->k_cache = k_cache; a->v_cache = v_cache;
+        a->block_tables = block_tables; a->context_lens = context_lens;
+        a->scale = scale; a->out = out;
+        a->row_begin = rows * t / nthreads;
+        a->row_end = rows * (t + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        attn_worker(&jobs[0]);
+    } else {
+        for (int32_t t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, attn_worker, &jobs[t]);
+        for (int32_t t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    free(th);
+    free(jobs);
+    return nthreads;
+}
+
+/* Brute force over a contiguous cache: K and V are [B][Hkv][n_max][d] with
+ * request b's tokens at positions 0..lens[b]-1 (the non-paged layout). Builds
+ * the score vector, subtracts its max, exponentiates, normalises the weights
+ * first and then sums weight * V. Used only to pin or_paged_attention. */
+void or_contiguous_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t n_max,
+                             const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                             const int32_t* lens, double scale, double* out) {
+    const int32_t G = Hq / Hkv;
+    double* w = (double*)malloc(sizeof(double) * (size_t)(n_max > 0 ? n_max : 1));
+    for (int32_t b = 0; b < B; ++b) {
+        for (int32_t j = 0; j < Hq; ++j) {
+            double* o = out + ((int64_t)b * Hq + j) * d;
+            memset(o, 0, sizeof(double) * (size_t)d);
+            const int32_t n = lens[b];
+            if (n <= 0) continue;
+            const int32_t h = j / G;
+            const uint16_t* qr = q + ((int64_t)b * Hq + j) * d;
+            const uint16_t* Kb = K + ((int64_t)b * Hkv + h) * n_max * d;
+            const uint16_t* Vb = V + ((int64_t)b * Hkv + h) * n_max * d;
+            double mx = -INFINITY;
+            for (int32_t t = 0; t < n; ++t) {
+                double acc = 0.0;
+                for (int32_t i = 0; i < d; ++i)
+                    acc += or_double_from_bf16(qr[i]) * or_double_from_bf16(Kb[(int64_t)t * d + i]);
+                w[t] = acc * scale;
+                mx = w[t] > mx ? w[t] : mx;
+            }
+            double z = 0.0;
+            for (int32_t t = 0; t < n; ++t) { w[t] = exp(w[t] - mx); z += w[t]; }
+            for (int32_t t = 0; t < n; ++t) w[t] /= z;
+            for (int32_t i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int32_t t = 0; t < n; ++t) acc += w[t] * or_double_from_bf16(Vb[(int64_t)t * d + i]);
+                o[i] = acc;
+            }
+        }
+    }
+    free(w);
+}

@@ -1,0 +1,229 @@
+"""Seeded synthetic workloads for the paged-KV decode step.
+
+This module only makes inputs: shapes, context lengths, pool operation
+sequences and random bf16 values. It holds none of the method's arithmetic (no
+RoPE, no slot arithmetic, no attention) and imports neither the product package
+nor the oracle, so both sides can be fed from it.
+
+The five workloads follow the shapes the pages work with: Qwen3-1.7B / Qwen3-8B
+layers (NJU course brief "端侧大模型推理框架", §2.1 and §2.2), Qwen2.5-7B at
+mini-infer's batch 8 with 128 new tokens (mini-infer README, "性能数据"), 16-token
+KV blocks in a fixed pool (mini-infer README, "项目概述"), plus a tiny case and a
+skewed long-context batch.
+
+Values are N(0,1) drawn with numpy's PCG64 (stream-stable across platforms)
+and rounded to bf16 by torch (round to nearest even). The big serving workload
+fills its caches on the device with torch's seeded CUDA generator instead; the
+tests copy back the blocks they check.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK = 16
+CANARY_BF16 = 0x7FA5  # a NaN pattern: slots no request owns, and block tails
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int                  # 1-based position in the workload list (seed = 1000 + index)
+    layers: int
+    B: int
+    Hq: int
+    Hkv: int
+    head_dim: int
+    num_blocks: int             # physical blocks per layer
+    max_seqs: int
+    theta: float = 1.0e6
+    ctx_kind: str = "fixed"     # fixed | uniform | loguniform | skewed | sweep
+    ctx_args: tuple = ()
+    permuted_pool: bool = True  # pool handed out in a seeded random order
+    churn: bool = False         # fragment the pool first (serving workload)
+    sweep_steps: int = 1        # decode steps in one pass (128 for the sweep)
+    device_fill: bool = False   # caches filled on the device
+
+    @property
+    def G(self):
+        return self.Hq // self.Hkv
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def seed(self):
+        return 1000 + self.index
+
+    def max_context(self):
+        """Largest post-append length any request reaches in one pass."""
+        if self.ctx_kind == "fixed":
+            return max(self.ctx_args) + 1
+        if self.ctx_kind in ("uniform", "loguniform"):
+            return self.ctx_args[1] + 1
+        if self.ctx_kind == "skewed":
+            return self.ctx_args[0] + 1
+        if self.ctx_kind == "sweep":
+            return self.ctx_args[0] + self.sweep_steps
+        raise ValueError(self.ctx_kind)
+
+    @property
+    def max_blocks_per_seq(self):
+        return -(-self.max_context() // BLOCK)
+
+    @property
+    def max_pos(self):
+        return self.max_context()
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, layers=1, B=2, Hq=4, Hkv=2, head_dim=64, num_blocks=64,
+                     max_seqs=2, ctx_kind="fixed", ctx_args=(17, 40)),
+    "qwen3_1p7b": Workload("qwen3_1p7b", 2, layers=1, B=8, Hq=16, Hkv=8, head_dim=128,
+                           num_blocks=1024, max_seqs=8, ctx_kind="uniform", ctx_args=(128, 2048)),
+    "qwen25_7b_sweep": Workload("qwen25_7b_sweep", 3, layers=28, B=8, Hq=28, Hkv=4, head_dim=128,
+                                num_blocks=4096, max_seqs=8, ctx_kind="sweep", ctx_args=(128,),
+                                sweep_steps=128),
+    "qwen3_8b": Workload("qwen3_8b", 4, layers=36, B=64, Hq=32, Hkv=8, head_dim=128,
+                         num_blocks=24576, max_seqs=4096, ctx_kind="loguniform",
+                         ctx_args=(512, 8192), permuted_pool=False, churn=True, device_fill=True),
+    "skewed": Workload("skewed", 5, layers=1, B=256, Hq=32, Hkv=8, head_dim=128, num_blocks=16384,
+                       max_seqs=256, ctx_kind="skewed", ctx_args=(32768, 16, 1024)),
+}
+
+
+def rng_for(w: Workload, stream: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64([w.seed, stream]))
+
+
+def context_lengths(w: Workload) -> np.ndarray:
+    """Tokens already cached per request before the first appended token."""
+    r = rng_for(w, 1)
+    if w.ctx_kind == "fixed":
+        c = np.array(w.ctx_args, np.int64)
+    elif w.ctx_kind == "uniform":
+        c = r.integers(w.ctx_args[0], w.ctx_args[1] + 1, size=w.B)
+    elif w.ctx_kind == "loguniform":
+        lo, hi = w.ctx_args
+        c = np.floor(np.exp(r.uniform(math.log(lo), math.log(hi), size=w.B))).astype(np.int64)
+        c = np.clip(c, lo, hi)
+    elif w.ctx_kind == "skewed":
+        long_len, lo, hi = w.ctx_args
+        c = r.integers(lo, hi + 1, size=w.B)
+        c[int(r.integers(0, w.B))] = long_len
+    elif w.ctx_kind == "sweep":
+        c = np.full(w.B, w.ctx_args[0], np.int64)
+    else:
+        raise ValueError(w.ctx_kind)
+    return c.astype(np.int32)
+
+
+def initial_free_order(w: Workload):
+    """Pop order of a fresh pool: a seeded permutation, or None for 0, 1, 2, ..."""
+    if not w.permuted_pool:
+        return None
+    return rng_for(w, 2).permutation(w.num_blocks).astype(np.int32)
+
+
+def churn(w: Workload, pool, first_dummy_id: int) -> int:
+    """Fragment the free pool with allocate/free rounds of dummy sequences.
+
+    Eight rounds of: allocate dummies of U{1..256} blocks until fewer than half
+    the blocks are free, then free each live dummy with probability 1/2. Then
+    free random dummies until at most 8192 dummy blocks remain. ``pool`` needs
+    alloc(seq, tokens) -> status, free(seq) -> status and num_free().
+    Returns the number of dummy blocks left allocated.
+    """
+    r = rng_for(w, 3)
+    live = {}  # dummy id -> blocks
+    nxt = first_dummy_id
+    for _ in range(8):
+        while pool.num_free() >= w.num_blocks // 2:
+            nb = int(r.integers(1, 257))
+            if nb > pool.num_free():
+                break
+            assert pool.alloc(nxt, nb * BLOCK) == 0
+            live[nxt] = nb
+            nxt += 1
+            assert nxt < w.max_seqs
+        for s in sorted(live):
+            if r.random() < 0.5:
+                assert pool.free(s) == 0
+                del live[s]
+    while sum(live.values()) > 8192:
+        ids = sorted(live)
+        s = ids[int(r.integers(0, len(ids)))]
+        assert pool.free(s) == 0
+        del live[s]
+    return sum(live.values())
+
+
+def setup_pool(w: Workload, pool, ctx: np.ndarray) -> None:
+    """Run the workload's pool history on ``pool``: churn (if any), then give
+    request b (sequence id b) ``ctx[b]`` tokens."""
+    if w.churn:
+        churn(w, pool, first_dummy_id=w.B)
+    for b in range(w.B):
+        st = pool.alloc(b, int(ctx[b]))
+        assert st == 0, f"request {b} does not fit the pool (status {st})"
+
+
+# --------------------------------------------------------------- values ------
+
+def bf16_normal(r: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1) values rounded to bf16, returned as uint16 bit patterns."""
+    import torch
+    x = r.standard_normal(size=shape, dtype=np.float32)
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def new_token_values(w: Workload, layer: int, step: int = 0):
+    """q [B][Hq][d], k [B][Hkv][d], v [B][Hkv][d] (bf16 bits) for one layer and step."""
+    r = np.random.Generator(np.random.PCG64([w.seed, 100, step, layer]))
+    q = bf16_normal(r, (w.B, w.Hq, w.head_dim))
+    k = bf16_normal(r, (w.B, w.Hkv, w.head_dim))
+    v = bf16_normal(r, (w.B, w.Hkv, w.head_dim))
+    return q, k, v
+
+
+def history_cache(w: Workload, layer: int, block_tables: np.ndarray, ctx: np.ndarray):
+    """Host K/V caches [num_blocks][Hkv][16][d] (bf16 bits) for one layer: the
+    slots of tokens 0..ctx[b]-1 of every request hold N(0,1) values (taken as
+    already rotated keys), every other slot holds the NaN canary."""
+    r = np.random.Generator(np.random.PCG64([w.seed, 200, layer]))
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    kc = np.full(shape, CANARY_BF16, np.uint16)
+    vc = np.full(shape, CANARY_BF16, np.uint16)
+    for b in range(w.B):
+        n = int(ctx[b])
+        if n <= 0:
+            continue
+        nblk = -(-n // BLOCK)
+        blks = block_tables[b, :nblk].astype(np.int64)
+        kv = bf16_normal(r, (2, nblk, w.Hkv, BLOCK, w.head_dim))
+        full = n // BLOCK
+        kc[blks[:full]] = kv[0, :full]
+        vc[blks[:full]] = kv[1, :full]
+        rem = n - full * BLOCK
+        if rem:
+            kc[blks[full], :, :rem] = kv[0, full, :, :rem]
+            vc[blks[full], :, :rem] = kv[1, full, :, :rem]
+    return kc, vc
+
+
+def device_fill_cache(w: Workload, layer: int, k_cache, v_cache) -> None:
+    """Fill a layer's device caches (torch bf16 tensors) with N(0,1) values
+    from torch's seeded CUDA generator (every slot, no canary)."""
+    import torch
+    g = torch.Generator(device=k_cache.device)
+    g.manual_seed(w.seed * 1000 + layer)
+    for t in (k_cache, v_cache):
+        flat = t.view(-1)
+        chunk = 1 << 28
+        for s in range(0, flat.numel(), chunk):
+            e = min(flat.numel(), s + chunk)
+            flat[s:e].copy_(torch.randn(e - s, generator=g, device=t.device, dtype=torch.float32))
