@@ -1,0 +1,437 @@
+"""Benchmark of the paged-KV decode step on one GB300 (or N replicas).
+
+One step = the whole hot path over one decode batch of the Qwen3-8B-shaped
+serving workload: for each of 36 layers, RoPE append of the new token
+(mi_paged_kv_append) and paged GQA decode attention (mi_paged_decode_attention)
+over 64 requests with log-uniform contexts in [512, 8192] whose blocks come
+from a churned 24,576-block pool. Every layer reads its own 727 MB of K/V, far
+more than the 129 MB L2, so no flush is needed between steps.
+
+Printed: one JSON line (rank 0). ``value`` = algorithmic bytes of the step (K/V
+of valid tokens, q, out, live table entries, lengths, append traffic) over the
+device-timed step, inputs resident in HBM. ``e2e`` = the same metric for real
+decode steps driven through the C ABI from host buffers: host pool growth and
+metadata, H2D of metadata and new q/k/v from pinned memory, 36 layers, D2H of
+the outputs. ``roofline`` = the attention call (split-KV kernel + LSE combine)
+against the measured HBM copy bandwidth. ``cpu_baseline`` = the fp64 oracle on
+the host cores on a bounded sample.
+
+``--impl reference`` times the oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import (BLOCK, WORKLOADS, context_lengths, device_fill_cache, history_cache,  # noqa: E402
+                       initial_free_order, new_token_values, setup_pool)
+
+METRIC = "paged decode-attention KV GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- bytes ----
+
+def attention_bytes(w, lens):
+    """Algorithmic bytes of one attention call (one layer)."""
+    lens = np.maximum(np.asarray(lens, np.int64), 0)
+    kv = int(lens.sum()) * w.Hkv * w.head_dim * 2 * 2
+    qo = 2 * w.B * w.Hq * w.head_dim * 2
+    tables = 4 * int(np.sum(-(-lens // BLOCK))) + 4 * w.B
+    return kv + qo + tables
+
+
+def append_bytes(w):
+    """Algorithmic bytes of one append call (one layer)."""
+    new = w.B * (w.Hq + 2 * w.Hkv) * w.head_dim * 2
+    rope_rows = w.B * (w.head_dim // 2) * 8
+    return 2 * new + rope_rows + 8 * w.B
+
+
+def describe(w):
+    return {"workload": w.name, "layers": w.layers, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+            "head_dim": w.head_dim, "block_size": BLOCK, "pool_blocks_per_layer": w.num_blocks,
+            "contexts": "log-uniform [512, 8192] + 1 appended" if w.ctx_kind == "loguniform" else w.ctx_kind,
+            "pool": "fragmented by seeded alloc/free churn" if w.churn else "seeded permutation",
+            "l2": "no flush: every layer reads its own K/V (> L2) once per step",
+            "parallelism": "replicas"}
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_decode_25_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, when it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
+    try:
+        kv = dict(tok.split("=", 1) for tok in open(path).read().split())
+    except Exception:
+        return None
+    if kv.get("source") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    return float(kv["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- oracle timing --
+
+def oracle_sample(w, nthreads, rank_seed=0):
+    """Host inputs for one layer of the step, and a callable that runs the
+    oracle's append + attention on them (test infrastructure only)."""
+    import oracle
+    from oracle.pool import PoolModel
+    ctx = context_lengths(w)
+    model = PoolModel(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+    setup_pool(w, model, ctx)
+    bt_hist, _, _ = model.batch_meta(range(w.B))
+    for b in range(w.B):
+        assert model.alloc(b, int(ctx[b]) + 1) == 0
+    bt, cl, sl = model.batch_meta(range(w.B))
+    kc, vc = history_cache(w, 0, bt_hist, ctx)
+    q, k, v = new_token_values(w, 0)
+    table = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    pos = (cl - 1).astype(np.int32)
+
+    def run():
+        q_out, _ = oracle.append(q, k, v, pos, sl, table, kc, vc)
+        oracle.paged_attention(q_out, kc, vc, bt, cl, w.scale, nthreads=nthreads)
+        return oracle.paged_attention.threads_used
+
+    return run, attention_bytes(w, cl) + append_bytes(w)
+
+
+def time_oracle(w, budget_s=12.0):
+    nthreads = os.cpu_count() or 1
+    run, nbytes = oracle_sample(w, nthreads)
+    t0 = time.perf_counter()
+    used = run()
+    n = 1
+    while time.perf_counter() - t0 < budget_s and n < 50:
+        run()
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": int(used), "kind": "oracle",
+            "sample": f"one layer of the step (append + attention, all {w.B} requests, {w.Hq} heads), "
+                      f"repeated {n}x, fp64 C on {used} POSIX threads; seconds per layer {dt:.3f}",
+            "s_per_layer": dt}
+
+
+# ------------------------------------------------------------ reference ----
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    nthreads = os.cpu_count() or 1
+    run, nbytes = oracle_sample(w, nthreads)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    used = nthreads
+    for _ in range(args.steps):
+        used = run()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    val = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(describe(w), sample="one of the 36 layers per step (append + attention)"),
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": int(used), "kind": "oracle",
+                             "sample": "one layer per step: append + attention, all requests and heads"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- main -----
+
+def dist_setup(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b", choices=list(WORKLOADS))
+    ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 0 and args.steps >= 1
+    w = WORKLOADS[args.workload]
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import paged_kv_decode_25_gb300 as mi
+    mi.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    variant = {"default": mi.MI_ATTN_DEFAULT, "mma": mi.MI_ATTN_MMA, "fma": mi.MI_ATTN_FMA}[args.variant]
+
+    # ---- workload: pool history, caches, new-token values (one replica per rank)
+    ctx = context_lengths(w)
+    pool = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+    setup_pool(w, pool, ctx)
+    seqs = list(range(w.B))
+    for b in seqs:
+        mi.check(pool.alloc(b, int(ctx[b]) + 1), "alloc")
+    bt, cl, sl = pool.batch_meta(seqs)
+    pos = (cl - 1).astype(np.int32)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    caches = []
+    for layer in range(w.layers):
+        kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        vc = torch.empty_like(kc)
+        if w.device_fill:
+            device_fill_cache(w, layer + 1000 * rank, kc, vc)
+        else:
+            hk, hv = history_cache(w, layer, bt, ctx)
+            kc.copy_(torch.from_numpy(hk.view(np.int16)).view(torch.bfloat16))
+            vc.copy_(torch.from_numpy(hv.view(np.int16)).view(torch.bfloat16))
+        caches.append((kc, vc))
+    st, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos + 4096)
+    mi.check(st, "rope table")
+    rope = torch.from_numpy(table).to(device)
+    max_pos = table.shape[0]
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    qkv_host = [new_token_values(w, layer) for layer in range(w.layers)]
+    q_all = torch.stack([u16(x[0]) for x in qkv_host]).to(device)   # [L][B][Hq][d]
+    k_all = torch.stack([u16(x[1]) for x in qkv_host]).to(device)
+    v_all = torch.stack([u16(x[2]) for x in qkv_host]).to(device)
+    qo_all = torch.empty_like(q_all)
+    out_all = torch.empty_like(q_all)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
+    bt_d, cl_d, sl_d, pos_d = i32(bt), i32(cl), i32(sl), i32(pos)
+    ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        for layer in range(w.layers):
+            kc, vc = caches[layer]
+            mi.check(mi.mi_paged_kv_append(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
+                                           max_pos, qo_all[layer], kc, vc, err, stream), "append")
+            if ev is not None:
+                ev[layer][0].record(stream)
+            mi.check(mi.mi_paged_decode_attention_variant(d, qo_all[layer], kc, vc, bt_d, cl_d, w.scale,
+                                                          out_all[layer], ws, variant=variant, dev_err=err,
+                                                          stream=stream), "attention")
+            if ev is not None:
+                ev[layer][1].record(stream)
+
+    # ---- device-timed steps (fixed step replayed; inputs resident)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    step_ms_local = t_start.elapsed_time(t_end) / args.steps
+    step_ms = max_over_ranks(step_ms_local, world, device)
+    attn_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
+               for layer in range(w.layers)]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    a_bytes = attention_bytes(w, cl)
+    step_bytes = w.layers * (a_bytes + append_bytes(w))
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = a_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name)
+
+    # ---- end to end: real decode steps from host buffers through the C ABI
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
+    ctx_now = cl.copy()
+    h_bt = torch.empty((w.B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory()
+    h_cl = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_sl = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_pos = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_q = torch.stack([u16(x[0]) for x in qkv_host]).pin_memory()
+    h_k = torch.stack([u16(x[1]) for x in qkv_host]).pin_memory()
+    h_v = torch.stack([u16(x[2]) for x in qkv_host]).pin_memory()
+    h_out = torch.empty(out_all.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_bytes = 0.0
+
+    def e2e_step():
+        nonlocal ctx_now, e2e_bytes
+        ctx_now = ctx_now + 1
+        for b in seqs:
+            mi.check(pool.alloc(b, int(ctx_now[b])), "alloc")
+        st_, _, _, _ = mi.mi_kv_pool_batch_meta(pool.handle, seqs, w.max_blocks_per_seq, h_bt.numpy(),
+                                                h_cl.numpy(), h_sl.numpy())
+        mi.check(st_, "batch_meta")
+        h_pos.numpy()[:] = h_cl.numpy() - 1
+        for src, dst in ((h_bt, bt_d), (h_cl, cl_d), (h_sl, sl_d), (h_pos, pos_d), (h_q, q_all), (h_k, k_all),
+                         (h_v, v_all)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        h_out.copy_(out_all, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy()) + append_bytes(w))
+
+    for _ in range(min(args.warmup, 2)):
+        e2e_step()
+    e2e_bytes = 0.0
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_cl, h_sl, h_pos, h_q, h_k, h_v))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_val = world * (e2e_bytes / e2e_steps) / (e2e_s / e2e_steps) / 1e9
+
+    if rank != 0:
+        barrier(world)
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = time_oracle(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(describe(w), variant=args.variant),
+        "steps_per_s": 1e3 / step_ms * world,
+        "hbm_frac_step": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "paged decode attention (split-KV kernel + LSE combine), per layer",
+                     "algorithmic_bytes_per_launch": a_bytes, "avg_launch_ms": attn_avg_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
+        "gpu_launches": args.steps * w.layers * 3,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * mi.h - paged KV cache decode step for one NVIDIA GB300 (sm_103a).
+ *
+ * One decode step per layer is: grow each request's block table on the host
+ * (mi_kv_pool_*), apply RoPE to the new token's q/k and scatter k/v into the
+ * paged cache (mi_paged_kv_append), then Grouped-Query decode attention over
+ * every request's paged history (mi_paged_decode_attention).
+ *
+ * The step follows mini-infer's decode_batch (mini-infer README, "架构设计",
+ * "decode_batch 关键步骤": gather_batch_kv -> model_forward -> write_decode_kv)
+ * over its Paged KV Cache ("项目概述": BlockTable + free-block pool), with GQA
+ * and RoPE as the NJU course brief "端侧大模型推理框架" §2.1 lists them for the
+ * Qwen models. The gather is not materialised: the attention kernel reads each
+ * block in place.
+ *
+ * Conventions for every entry point:
+ *  - All sizes are int32 unless stated. bf16 tensors are passed as void*.
+ *  - Device pointers are caller-owned memory on the current CUDA device, and
+ *    must stay valid until the work queued on `stream` has finished. The
+ *    library allocates no device memory and keeps no device pointer.
+ *  - Every device entry point is asynchronous on `stream` (NULL = the legacy
+ *    default stream). Host-side argument checks return synchronously, before
+ *    anything is queued; a rejected call queues nothing.
+ *  - Data-dependent faults found on the device (a block id outside
+ *    [0, num_blocks), a slot outside the cache, a position outside the RoPE
+ *    table, a context longer than a table row) never trap: the kernel skips the
+ *    offending entry and ORs an MI_DEVERR_* bit into *dev_err (when dev_err is
+ *    not NULL). The caller reads the word after synchronising; the library
+ *    never clears it.
+ *  - Thread safety: device entry points are reentrant. A pool handle must be
+ *    used by one host thread at a time.
+ */
+#ifndef MI_H
+#define MI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream), without the CUDA headers. */
+typedef struct CUstream_st* mi_stream_t;
+
+typedef enum mi_status {
+    MI_OK = 0,
+    MI_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned buffer */
+    MI_ERR_OUT_OF_BLOCKS = 2,  /* the pool cannot grow the sequence; nothing changed */
+    MI_ERR_UNKNOWN_SEQ = 3,    /* sequence id not allocated */
+    MI_ERR_UNSUPPORTED = 4,    /* head_dim, block_size or GQA group outside what is built */
+    MI_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+    MI_ERR_DEVICE_BOUNDS = 6,  /* reserved: a caller may map a nonzero *dev_err to it */
+    MI_ERR_TIMEOUT = 7         /* reserved for bounded device-side waits */
+} mi_status;
+
+/* Bits ORed into *dev_err by the kernels. */
+#define MI_DEVERR_BAD_BLOCK    0x1 /* block table entry outside [0, num_blocks) */
+#define MI_DEVERR_BAD_SLOT     0x2 /* slot_mapping entry outside the cache */
+#define MI_DEVERR_BAD_POS      0x4 /* position outside [0, max_pos) */
+#define MI_DEVERR_BAD_CONTEXT  0x8 /* context length above max_blocks_per_seq * block_size */
+#define MI_DEVERR_TIMEOUT      0x10 /* a staged copy did not land within the wait limit */
+
+/* Short human-readable name of a status. */
+const char* mi_status_string(mi_status s);
+
+/* ------------------------------------------------------------------------ */
+/* Host block pool (mini-infer README "项目概述" / "架构设计" KVCacheManager;
+ * nxmr.cn article §2.1 "KV缓存的内存革命" allocate sketch: pages_needed =
+ * ceil(seq_len / PAGE_SIZE), each popped from the free list). The pool is
+ * fixed: when the free list is empty a request fails instead of growing it.
+ *
+ * Semantics (exact, so that a model of the pool can reproduce every table):
+ *  - The free list is a stack. On creation successive pops return
+ *    initial_free_order[0], [1], ... (or 0, 1, 2, ... when it is NULL).
+ *  - mi_kv_pool_alloc(seq, n) grows seq's table to ceil(n / block_size) blocks
+ *    by popping the missing ones in order and appending them. All or nothing.
+ *  - mi_kv_pool_free(seq) pushes seq's blocks in table order (so the next pop
+ *    returns its last block) and forgets seq.
+ * The pool is host memory only and never touches the GPU.
+ * ------------------------------------------------------------------------ */
+typedef struct mi_kv_pool mi_kv_pool; /* opaque; owned by the library */
+
+/* num_blocks >= 1; block_size must be 16; max_seqs >= 1 (ids are 0..max_seqs-1);
+ * max_blocks_per_seq >= 1 is the width of one block-table row.
+ * initial_free_order: NULL or a permutation of [0, num_blocks) (checked).
+ * On MI_OK *out holds a new pool; release it with mi_kv_pool_destroy. */
+mi_status mi_kv_pool_create(int32_t num_blocks, int32_t block_size, int32_t max_seqs,
+                            int32_t max_blocks_per_seq, const int32_t* initial_free_order,
+                            mi_kv_pool** out);
+
+/* Frees the pool and every table. NULL is ignored. */
+void mi_kv_pool_destroy(mi_kv_pool* pool);
+
+/* Grow sequence seq_id to hold num_tokens tokens (creating it if new).
+ * MI_ERR_INVALID_ARG: seq_id outside [0, max_seqs), num_tokens < 0, fewer tokens
+ * than the sequence already holds, or more blocks than a table row.
+ * MI_ERR_OUT_OF_BLOCKS: not enough free blocks; the pool is unchanged. */
+mi_status mi_kv_pool_alloc(mi_kv_pool* pool, int32_t seq_id, int32_t num_tokens);
+
+/* Return all blocks of seq_id to the free list. MI_ERR_UNKNOWN_SEQ if seq_id
+ * holds no allocation. */
+mi_status mi_kv_pool_free(mi_kv_pool* pool, int32_t seq_id);
+
+/* Number of free blocks, or -1 for a NULL pool. */
+int32_t mi_kv_pool_num_free(const mi_kv_pool* pool);
+
+/* Host metadata for a decode batch of B sequences (host buffers, caller-owned):
+ *  block_tables  [B][max_blocks_per_seq] int32: physical block ids, padded with -1;
+ *  context_lens  [B] int32: tokens held (the post-append length in a decode step);
+ *  slot_mapping  [B] int32: slot of the sequence's last token,
+ *                table[(n-1)/16]*16 + (n-1)%16, or -1 when n == 0.
+ * Any output pointer may be NULL to skip it. MI_ERR_UNKNOWN_SEQ if a sequence
+ * is not allocated (outputs then undefined). */
+mi_status mi_kv_pool_batch_meta(const mi_kv_pool* pool, const int32_t* seq_ids, int32_t B,
+                                int32_t* block_tables, int32_t* context_lens,
+                                int32_t* slot_mapping);
+
+/* Copy of one sequence's table into out[0..max_out) (host); returns the
+ * number of blocks it holds, or -1 if unknown. */
+int32_t mi_kv_pool_seq_blocks(const mi_kv_pool* pool, int32_t seq_id, int32_t* out,
+                              int32_t max_out);
+
+/* ------------------------------------------------------------------------ */
+/* Shapes shared by the device entry points.
+ *   B                   requests in the batch (1 .. 65535)
+ *   Hq, Hkv             query / KV heads; Hq % Hkv == 0, G = Hq/Hkv in 1..8
+ *   head_dim            64 or 128
+ *   block_size          16
+ *   num_blocks          physical blocks in k_cache / v_cache
+ *   max_blocks_per_seq  width of a block-table row
+ * Cache layout (both caches, bf16, contiguous, 16-byte aligned):
+ *   [num_blocks][Hkv][block_size][head_dim]
+ * so one (block, KV head) tile of 16 tokens is contiguous (4 KB at d = 128).
+ * ------------------------------------------------------------------------ */
+typedef struct mi_dims {
+    int32_t B, Hq, Hkv, head_dim, block_size, num_blocks, max_blocks_per_seq;
+} mi_dims;
+
+/* RoPE table on the host: out[max_pos][head_dim/2][2] fp32 holds
+ * (cos, sin) of p * theta^(-2i/head_dim), each evaluated in double and rounded
+ * once to fp32 (NJU course brief §2.1, "RoPE construction and application";
+ * theta = 1e6 for Qwen2.5/Qwen3). The caller copies it to the device for
+ * mi_paged_kv_append. head_dim even and >= 2, max_pos >= 1, theta > 0. */
+mi_status mi_rope_table(double theta, int32_t head_dim, int32_t max_pos, float* host_out);
+
+/* Append one new token per request (mini-infer README "decode_batch 关键步骤",
+ * write_decode_kv, with RoPE applied first as in NJU course brief §2.1).
+ * For request b at position p = positions[b]:
+ *   q_out[b][j]                    = RoPE_p(q[b][j])   for j < Hq
+ *   k_cache[blk][h][off][:]        = RoPE_p(k[b][h])   for h < Hkv
+ *   v_cache[blk][h][off][:]        = v[b][h]
+ * with blk = slot_mapping[b] / 16, off = slot_mapping[b] % 16. RoPE rotates the
+ * pairs (i, i + d/2) by the table angle (rotate-half pairing):
+ *   y[i] = x[i] c - x[i+d/2] s,  y[i+d/2] = x[i+d/2] c + x[i] s
+ * computed in double from the bf16 inputs and fp32 table values, then rounded
+ * once to bf16 (nearest, ties to even). No other cache byte is written.
+ * Device buffers: q [B][Hq][d], k, v [B][Hkv][d], q_out [B][Hq][d] (bf16;
+ * q_out may equal q), positions, slot_mapping [B] int32, rope_cos_sin
+ * [max_pos][d/2][2] fp32 (from mi_rope_table), dev_err int32 or NULL.
+ * A bad position skips the whole request (MI_DEVERR_BAD_POS); a bad slot skips
+ * its cache writes (MI_DEVERR_BAD_SLOT). */
+mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, const void* k, const void* v,
+                             const int32_t* positions, const int32_t* slot_mapping,
+                             const float* rope_cos_sin, int32_t max_pos, void* q_out,
+                             void* k_cache, void* v_cache, int32_t* dev_err, mi_stream_t stream);
+
+/* Device workspace the attention call needs for these dims on the current
+ * device (split-KV partials of the persistent grid): a size in bytes, or 0 when
+ * the dims are not supported. */
+size_t mi_paged_decode_workspace_bytes(const mi_dims* dims);
+
+/* Paged GQA decode attention (mini-infer README "decode_batch 关键步骤": the
+ * attention of model_forward over the KV that gather_batch_kv would collect,
+ * read in place; NJU course brief §2.1 GQA: query head j uses KV head j / G).
+ * For every request b and query head j, with n = context_lens[b] (the length
+ * after append) and K_t, V_t read from block block_tables[b][t/16], offset t%16:
+ *   out[b][j] = sum_t softmax_t(scale * <q[b][j], K_t>) V_t,   t < n
+ * computed as a split-KV online softmax in fp32 followed by a log-sum-exp
+ * combine of the splits, rounded to bf16. n <= 0 gives a zero row.
+ * Device buffers: q [B][Hq][d] bf16 (RoPE already applied), k_cache, v_cache
+ * (layout above), block_tables [B][max_blocks_per_seq] int32, context_lens [B]
+ * int32, out [B][Hq][d] bf16, workspace of mi_paged_decode_workspace_bytes()
+ * bytes (16-byte aligned; contents need no initialisation and are overwritten),
+ * dev_err int32 or NULL. Only the first ceil(n/16) entries of a table row are
+ * read. Tokens past n in the last block are never used (they may hold any bits,
+ * NaN included). Results are bitwise independent of where blocks sit in the
+ * cache. */
+mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, float scale, void* out,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                    mi_stream_t stream);
+
+/* Kernel variant used by mi_paged_decode_attention_variant:
+ *   MI_ATTN_MMA  bf16 tensor-core tiles (mma.sync m16n8k16: 16 tokens x 8 heads),
+ *   MI_ATTN_FMA  fp32 CUDA-core FMA tiles.
+ * Both share the staging pipeline, split plan and combine, and return results
+ * within the same tolerance; mi_paged_decode_attention uses the default. */
+typedef enum mi_attn_variant { MI_ATTN_DEFAULT = 0, MI_ATTN_MMA = 1, MI_ATTN_FMA = 2 } mi_attn_variant;
+
+/* mi_paged_decode_attention with an explicit kernel variant and grid size:
+ * ctas = 0 picks the persistent grid (all SMs at full occupancy); a positive
+ * value caps the number of CTAs (and thus KV splits), which changes only the
+ * fp32 rounding of the result. The workspace must be sized for ctas = 0. */
+mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables,
+                                            const int32_t* context_lens, float scale, void* out,
+                                            void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_err, mi_stream_t stream,
+                                            mi_attn_variant variant, int32_t ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MI_H */

@@ -1,0 +1,245 @@
+"""Python binding of the paged-KV decode library (libmi.so).
+
+Argument marshalling only: every function here forwards to the C ABI of
+include/mi.h with the same name, passing device pointers of torch tensors (or
+host numpy buffers for the pool) and the current CUDA stream. All arithmetic of
+the decode step runs in the library's CUDA kernels; nothing here computes a
+result. The library must have been built (``build.build()``); calling any entry
+point without it raises RuntimeError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmi.so")
+_lock = threading.Lock()
+_lib = None
+
+MI_OK, MI_ERR_INVALID_ARG, MI_ERR_OUT_OF_BLOCKS, MI_ERR_UNKNOWN_SEQ = 0, 1, 2, 3
+MI_ERR_UNSUPPORTED, MI_ERR_CUDA, MI_ERR_DEVICE_BOUNDS, MI_ERR_TIMEOUT = 4, 5, 6, 7
+MI_DEVERR_BAD_BLOCK, MI_DEVERR_BAD_SLOT, MI_DEVERR_BAD_POS = 0x1, 0x2, 0x4
+MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT = 0x8, 0x10
+MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
+
+# every symbol include/mi.h declares
+EXPORTS = (
+    "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc",
+    "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_seq_blocks",
+    "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
+    "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
+)
+
+
+class MiDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("B", "Hq", "Hkv", "head_dim", "block_size", "num_blocks", "max_blocks_per_seq")]
+
+
+class MIError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+def load():
+    """Load libmi.so (raises RuntimeError when it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmi.so is not built at %s; run paged_kv_decode_25_gb300/build.py"
+                               % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, f32, f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_double
+        dims_p = ctypes.POINTER(MiDims)
+        sig = {
+            "mi_status_string": ([i32], ctypes.c_char_p),
+            "mi_kv_pool_create": ([i32, i32, i32, i32, P, ctypes.POINTER(P)], i32),
+            "mi_kv_pool_destroy": ([P], None),
+            "mi_kv_pool_alloc": ([P, i32, i32], i32),
+            "mi_kv_pool_free": ([P, i32], i32),
+            "mi_kv_pool_num_free": ([P], i32),
+            "mi_kv_pool_batch_meta": ([P, P, i32, P, P, P], i32),
+            "mi_kv_pool_seq_blocks": ([P, i32, P, i32], i32),
+            "mi_rope_table": ([f64, i32, i32, P], i32),
+            "mi_paged_kv_append": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P], i32),
+            "mi_paged_decode_workspace_bytes": ([dims_p], ctypes.c_size_t),
+            "mi_paged_decode_attention": ([dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
+            "mi_paged_decode_attention_variant": (
+                [dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P, i32, i32], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(s: int) -> str:
+    return load().mi_status_string(int(s)).decode()
+
+
+def check(status: int, what: str = "mi call") -> None:
+    if status != MI_OK:
+        raise MIError(status, what)
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _ptr(x):
+    """Device/host address of a torch tensor or numpy array (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        assert x.flags.c_contiguous
+        return x.ctypes.data
+    assert x.is_contiguous(), "tensors must be contiguous"
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dims(B, Hq, Hkv, head_dim, num_blocks, max_blocks_per_seq, block_size=16) -> MiDims:
+    return MiDims(B, Hq, Hkv, head_dim, block_size, num_blocks, max_blocks_per_seq)
+
+
+# ------------------------------------------------------------------ pool ---
+
+def mi_kv_pool_create(num_blocks, block_size, max_seqs, max_blocks_per_seq, initial_free_order=None):
+    """Returns (status, handle)."""
+    order = None
+    if initial_free_order is not None:
+        order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+        assert order.shape == (num_blocks,)
+    h = ctypes.c_void_p()
+    st = load().mi_kv_pool_create(num_blocks, block_size, max_seqs, max_blocks_per_seq,
+                                  _ptr(order), ctypes.byref(h))
+    return st, h.value
+
+
+def mi_kv_pool_destroy(handle):
+    load().mi_kv_pool_destroy(handle)
+
+
+def mi_kv_pool_alloc(handle, seq_id, num_tokens):
+    return load().mi_kv_pool_alloc(handle, int(seq_id), int(num_tokens))
+
+
+def mi_kv_pool_free(handle, seq_id):
+    return load().mi_kv_pool_free(handle, int(seq_id))
+
+
+def mi_kv_pool_num_free(handle):
+    return load().mi_kv_pool_num_free(handle)
+
+
+def mi_kv_pool_batch_meta(handle, seq_ids, max_blocks_per_seq, block_tables=None, context_lens=None,
+                          slot_mapping=None):
+    """Fills (or allocates) host int32 outputs; returns (status, block_tables, context_lens, slot_mapping)."""
+    ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    B = ids.shape[0]
+    bt = np.empty((B, max_blocks_per_seq), np.int32) if block_tables is None else block_tables
+    cl = np.empty(B, np.int32) if context_lens is None else context_lens
+    sl = np.empty(B, np.int32) if slot_mapping is None else slot_mapping
+    st = load().mi_kv_pool_batch_meta(handle, _ptr(ids), B, _ptr(bt), _ptr(cl), _ptr(sl))
+    return st, bt, cl, sl
+
+
+def mi_kv_pool_seq_blocks(handle, seq_id, max_out=1 << 20):
+    n = load().mi_kv_pool_seq_blocks(handle, int(seq_id), None, 0)
+    if n < 0:
+        return None
+    out = np.empty(max(n, 1), np.int32)
+    load().mi_kv_pool_seq_blocks(handle, int(seq_id), _ptr(out), n)
+    return out[:n]
+
+
+class Pool:
+    """Owner of a library pool handle, with the alloc/free/num_free/batch_meta
+    calls the workloads expect (each returns the library's status)."""
+
+    def __init__(self, num_blocks, max_seqs, max_blocks_per_seq, initial_order=None, block_size=16):
+        st, self.handle = mi_kv_pool_create(num_blocks, block_size, max_seqs, max_blocks_per_seq,
+                                            initial_order)
+        check(st, "mi_kv_pool_create")
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def alloc(self, seq, num_tokens):
+        return mi_kv_pool_alloc(self.handle, seq, num_tokens)
+
+    def free(self, seq):
+        return mi_kv_pool_free(self.handle, seq)
+
+    def num_free(self):
+        return mi_kv_pool_num_free(self.handle)
+
+    def batch_meta(self, seq_ids):
+        st, bt, cl, sl = mi_kv_pool_batch_meta(self.handle, seq_ids, self.max_blocks_per_seq)
+        check(st, "mi_kv_pool_batch_meta")
+        return bt, cl, sl
+
+    def close(self):
+        if self.handle:
+            mi_kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------ device ops ---
+
+def mi_rope_table(theta, head_dim, max_pos):
+    """Returns (status, float32 [max_pos][head_dim/2][2] host array)."""
+    out = np.empty((max_pos, head_dim // 2, 2), np.float32)
+    st = load().mi_rope_table(float(theta), int(head_dim), int(max_pos), _ptr(out))
+    return st, out
+
+
+def mi_paged_kv_append(d: MiDims, q, k, v, positions, slot_mapping, rope_cos_sin, max_pos, q_out,
+                       k_cache, v_cache, dev_err=None, stream=None):
+    return load().mi_paged_kv_append(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(positions),
+                                     _ptr(slot_mapping), _ptr(rope_cos_sin), int(max_pos), _ptr(q_out),
+                                     _ptr(k_cache), _ptr(v_cache), _ptr(dev_err), _stream(stream))
+
+
+def mi_paged_decode_workspace_bytes(d: MiDims) -> int:
+    return int(load().mi_paged_decode_workspace_bytes(ctypes.byref(d)))
+
+
+def mi_paged_decode_attention(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                              workspace, workspace_bytes=None, dev_err=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return load().mi_paged_decode_attention(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(block_tables), _ptr(context_lens), float(scale),
+                                            _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err),
+                                            _stream(stream))
+
+
+def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                      out, workspace, variant=MI_ATTN_DEFAULT, ctas=0,
+                                      workspace_bytes=None, dev_err=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return load().mi_paged_decode_attention_variant(
+        ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream),
+        int(variant), int(ctas))

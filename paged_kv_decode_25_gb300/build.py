@@ -1,0 +1,84 @@
+"""Build libmi.so in-tree for sm_103a.
+
+Compiles the host pool (g++) and the CUDA translation units (nvcc, one
+-gencode for compute_103a/sm_103a) in parallel, then links one shared library
+next to this file. Run as a script or call build().
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libmi.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-ffp-contract=off",
+              "-I" + INCLUDE] + ARCH
+CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-I" + INCLUDE]
+CU_SOURCES = ["append.cu", "decode.cu"]
+CPP_SOURCES = ["pool.cpp"]
+
+
+def _nvcc():
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found")
+    return cand
+
+
+def _inputs():
+    srcs = [os.path.join(CSRC, f) for f in CU_SOURCES + CPP_SOURCES]
+    hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    hdrs.append(os.path.join(INCLUDE, "mi.h"))
+    return srcs, hdrs
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    srcs, hdrs = _inputs()
+    return any(os.path.getmtime(f) > t for f in srcs + hdrs + [os.path.abspath(__file__)])
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and not _stale():
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    jobs = []
+    objs = []
+    for f in CU_SOURCES:
+        o = os.path.join(OUT_DIR, f + ".o")
+        jobs.append([nvcc] + NVCC_FLAGS + ["-c", os.path.join(CSRC, f), "-o", o])
+        objs.append(o)
+    for f in CPP_SOURCES:
+        o = os.path.join(OUT_DIR, f + ".o")
+        jobs.append(["g++"] + CXX_FLAGS + ["-c", os.path.join(CSRC, f), "-o", o])
+        objs.append(o)
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("build failed: %s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
+        if verbose and (r.stdout or r.stderr):
+            print(r.stdout + r.stderr, file=sys.stderr)
+
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        list(ex.map(run, jobs))
+    tmp = LIB + ".tmp.%d" % os.getpid()
+    run([nvcc, "-shared"] + ARCH + ["-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

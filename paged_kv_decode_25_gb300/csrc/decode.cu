@@ -1,0 +1,905 @@
+// mi_paged_decode_attention: GQA decode attention over the paged KV cache.
+//
+// What it computes is the attention inside mini-infer's decode_batch
+// model_forward (mini-infer README, "decode_batch 关键步骤"), over the history
+// its gather_batch_kv would collect from the block tensor, with GQA as in the
+// NJU course brief "端侧大模型推理框架" §2.1 (query head j reads KV head j / G).
+// The gather is never materialised: blocks are read in place.
+//
+// Work decomposition (split-KV, flash-decoding style, balanced):
+//   * A "unit" is one (request b, KV head h) pair; it owns ceil(n_b / 16) KV
+//     blocks. Units are laid end to end in (b, h) order into one flat sequence
+//     of blocks, of total length TB.
+//   * A persistent grid of P CTAs cuts that sequence into P contiguous ranges
+//     of (almost) equal block counts, so every CTA streams the same number of
+//     bytes however skewed the context lengths are.
+//   * Inside a CTA, warp w takes every W-th block of the range. Each warp owns
+//     a ring of S shared-memory stages fed by 2-D TMA tensor copies (128-byte
+//     swizzle) on its own mbarriers, so loads for later blocks are in flight
+//     while the current block is computed.
+//   * One 16-token K/V tile serves all G query heads of the KV head: scores
+//     are 16 tokens x G heads, with an fp32 online softmax (base-2 exponent,
+//     scale * log2(e) folded into one multiply).
+//   * At every unit boundary the warps merge their (max, sum, output) states in
+//     shared memory. A unit wholly inside the range is written as bf16 output;
+//     a unit cut by the range edge leaves a normalised fp32 partial and its
+//     log-sum-exp in the workspace, and the combine kernel merges the pieces.
+// The split plan depends only on the context lengths, so results are bitwise
+// independent of which physical blocks a request holds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace mi {
+namespace {
+
+constexpr int kMaxG = 8;
+constexpr float kNegInf = -INFINITY;
+
+struct AttnParams {
+    const uint16_t* q;             // [B][Hq][HD]
+    const int32_t* block_tables;   // [B][mbps]
+    const int32_t* context_lens;   // [B]
+    uint16_t* out;                 // [B][Hq][HD]
+    float* part;                   // partial slots [P][2][slot_floats]
+    int32_t* dev_err;
+    int B, Hq, Hkv, G, num_blocks, mbps, stages, slot_floats;
+    float sl2;                     // scale * log2(e)
+};
+
+// ------------------------------------------------------------- the plan ---
+
+__device__ __forceinline__ int ctx_clamped(const AttnParams& p, int b) {
+    int n = __ldg(p.context_lens + b);
+    n = n < 0 ? 0 : n;
+    const int cap = p.mbps * kBlock;
+    return n > cap ? cap : n;
+}
+
+__device__ __forceinline__ int unit_blocks(const AttnParams& p, int b) {
+    return b < p.B ? (ctx_clamped(p, b) + kBlock - 1) / kBlock : 0;
+}
+
+// A position in the flat unit sequence: unit (b, h) covers flat blocks
+// [start, start + len).
+struct Cursor {
+    int b, h, len;
+    long long start;
+    __device__ __forceinline__ void next(const AttnParams& p) {
+        start += len;
+        if (++h == p.Hkv) {
+            h = 0;
+            ++b;
+            len = unit_blocks(p, b);
+            while (len == 0 && b < p.B) len = unit_blocks(p, ++b);
+        }
+    }
+    __device__ __forceinline__ void advance_to(const AttnParams& p, long long x) {
+        while (x >= start + len && b < p.B) next(p);
+    }
+};
+
+__device__ __forceinline__ long long range_start(long long TB, int P, int i) {
+    return (long long)(((unsigned long long)TB * (unsigned long long)i) / (unsigned long long)P);
+}
+
+// Block-wide exclusive scan of the per-thread values v (one per thread).
+// Writes scratch[tid] = sum of v over threads < tid and scratch[nt] = total.
+// `scratch` holds blockDim.x + 1 long longs plus 32 more for warp totals.
+__device__ void block_exclusive_scan(long long v, long long* scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    long long* wsum = scratch + blockDim.x + 1;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        long long t = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) wsum[lane] = t;  // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    const long long before = (wid ? wsum[wid - 1] : 0) + x - v;
+    scratch[tid] = before;
+    if (tid == blockDim.x - 1) scratch[blockDim.x] = before + v;
+    __syncthreads();
+}
+
+// The plan, computed identically by every CTA of both kernels. Each thread
+// sums the unit lengths of a contiguous chunk of requests; the scan of those
+// sums gives the total number of flat blocks TB = Hkv * sum_b ceil(n_b / 16).
+struct Plan {
+    int b0, b1;      // this thread's request chunk
+    long long TB;
+};
+
+__device__ __forceinline__ Plan plan_scan(const AttnParams& p, long long* scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (p.B + nt - 1) / nt;
+    Plan pl;
+    pl.b0 = min(p.B, tid * per);
+    pl.b1 = min(p.B, pl.b0 + per);
+    long long s = 0;
+    for (int b = pl.b0; b < pl.b1; ++b) s += unit_blocks(p, b);
+    block_exclusive_scan(s, scratch);
+    pl.TB = scratch[nt] * p.Hkv;
+    return pl;
+}
+
+// Locate the unit holding flat block x (0 <= x < TB) after plan_scan: the
+// thread whose chunk spans x walks it. found = {b, h, unit start, unit length}.
+__device__ __forceinline__ void plan_find(const AttnParams& p, const Plan& pl, long long x,
+                                          const long long* scratch, long long* found) {
+    const int tid = threadIdx.x;
+    const long long lo = scratch[tid] * p.Hkv, hi = scratch[tid + 1] * p.Hkv;
+    if (x >= lo && x < hi) {
+        long long acc = scratch[tid];
+        for (int b = pl.b0; b < pl.b1; ++b) {
+            const int L = unit_blocks(p, b);
+            if (x < (acc + L) * p.Hkv) {
+                const int h = (int)((x - acc * p.Hkv) / L);
+                found[0] = b;
+                found[1] = h;
+                found[2] = acc * p.Hkv + (long long)h * L;
+                found[3] = L;
+                break;
+            }
+            acc += L;
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------- smem layout ------
+
+template <int HD>
+struct Tile {
+    static constexpr int kBytes = kBlock * HD * 2;  // one 16-token K or V tile
+    static constexpr int kHalves = HD / 64;         // 128-byte swizzle spans 64 bf16 columns
+};
+
+// Physical byte offset of 16-byte chunk `chunk` (0 .. HD/8-1) of row `row`
+// inside a tile written by the 128-byte-swizzled TMA copy: the tile is
+// [HD/64 halves][16 rows][128 bytes] and chunk c of a row sits at c ^ (row & 7).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+struct SmemPlan {
+    int tiles, bars, mbuf, lbuf, obuf, xbuf, scan, found, fac, total;
+};
+
+__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G) {
+    SmemPlan s;
+    int off = 0;
+    s.tiles = off; off += W * S * 2 * kBlock * HD * 2;
+    s.bars = off;  off += W * S * 8;
+    s.mbuf = off;  off += W * kMaxG * 4;
+    s.lbuf = off;  off += W * kMaxG * 4;
+    s.fac = off;   off += (W + 3) * kMaxG * 4;
+    s.obuf = off;  off += W * G * HD * 4;
+    s.xbuf = off;  off += W * (kBlock * kMaxG + kMaxG) * 4;
+    off = (off + 15) & ~15;
+    s.scan = off;  off += (W * 32 + 1 + 32) * 8;
+    s.found = off; off += 4 * 8;
+    s.total = off + 1024;  // slack to align the tiles to 1024 bytes
+    return s;
+}
+
+// ---------------------------------------------------- per-warp compute ----
+
+// Tensor-core tile: S^T[16 tokens x 8 heads] = K[16 x HD] . Q^T[HD x 8] with
+// mma.sync m16n8k16 (heads beyond G are zero columns), online softmax on the
+// fragments, then O^T[HD x 8] += V^T[HD x 16] . P^T[16 x 8] (V^T by
+// ldmatrix.trans, P^T by movmatrix.trans of the score fragments).
+template <int HD>
+struct MmaState {
+    static constexpr int kK = HD / 16;
+    uint32_t qb[kK][2];
+    float o[kK][4];
+    float m[2], l[2];
+
+    __device__ __forceinline__ void begin_unit(const AttnParams& p, int b, int h, int lane) {
+        const int n = lane >> 2;
+        const bool ok = n < p.G;
+        const uint16_t* qrow = p.q + ((long long)b * p.Hq + (long long)h * p.G + (ok ? n : 0)) * HD;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const int dcol = kk * 16 + (lane & 3) * 2;
+            qb[kk][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol)) : 0u;
+            qb[kk][1] = ok ? __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol + 8)) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float sl2, int lane) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int csel = lane >> 4;
+#pragma unroll
+            for (int kk = 0; kk < kK; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kt + swz(tok, kk * 2 + csel), a0, a1, a2, a3);
+                mma_bf16_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            }
+        }
+        const int t0 = lane >> 2, t1 = t0 + 8;
+        float s0 = t0 < valid ? c[0] * sl2 : kNegInf;  // head 2*(lane&3),   token t0
+        float s1 = t0 < valid ? c[1] * sl2 : kNegInf;  // head 2*(lane&3)+1, token t0
+        float s2 = t1 < valid ? c[2] * sl2 : kNegInf;  // head 2*(lane&3),   token t1
+        float s3 = t1 < valid ? c[3] * sl2 : kNegInf;  // head 2*(lane&3)+1, token t1
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float r0 = mn0 == kNegInf ? 0.f : mn0, r1 = mn1 == kNegInf ? 0.f : mn1;
+        const float al0 = exp2f(m[0] - r0), al1 = exp2f(m[1] - r1);
+        m[0] = mn0;
+        m[1] = mn1;
+        const uint32_t x0 = pack_bf16x2(exp2f(s0 - r0), exp2f(s1 - r1));
+        const uint32_t x1 = pack_bf16x2(exp2f(s2 - r0), exp2f(s3 - r1));
+        // the sums use the same bf16-rounded weights the PV product uses
+        l[0] = l[0] * al0 + (bf16_lo(x0) + bf16_lo(x1));
+        l[1] = l[1] * al1 + (bf16_hi(x0) + bf16_hi(x1));
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
+        {
+            const int qd = lane >> 3;
+            const int tok = (lane & 7) + (qd >> 1) * 8;
+            const int csel = qd & 1;
+#pragma unroll
+            for (int mt = 0; mt < kK; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(vt + swz(tok, mt * 2 + csel), a0, a1, a2, a3);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+            }
+        }
+    }
+
+    // Reduce the per-thread sums and write (m, l, O) of this warp to smem.
+    __device__ __forceinline__ void store(float* mbuf, float* lbuf, float* obuf, int G, int lane) {
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], sh);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], sh);
+        }
+        const int h0 = (lane & 3) * 2, h1 = h0 + 1;
+        if (lane < 4) {
+            if (h0 < G) { mbuf[h0] = m[0]; lbuf[h0] = l[0]; }
+            if (h1 < G) { mbuf[h1] = m[1]; lbuf[h1] = l[1]; }
+        }
+        const int r = lane >> 2;
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) {
+            if (h0 < G) {
+                obuf[h0 * HD + mt * 16 + r] = o[mt][0];
+                obuf[h0 * HD + mt * 16 + r + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+                obuf[h1 * HD + mt * 16 + r] = o[mt][1];
+                obuf[h1 * HD + mt * 16 + r + 8] = o[mt][3];
+            }
+        }
+    }
+};
+
+// CUDA-core tile. Lane (r, c): c = lane % LPR picks a 16-byte chunk (8 dims)
+// of a K/V row, r = lane / LPR a row group; the lane handles tokens r + RG*i.
+// Partial dot products (TPL tokens x GP heads per lane) are summed over the
+// LPR lanes of a row by a transposing butterfly that halves the values each
+// lane carries at every step; afterwards lane c holds token r + RG*(c/2) for
+// heads (c%2)*GP/2 .. +GP/2. Weights go through a per-warp smem exchange to
+// the lanes that own each token's V chunk.
+template <int HD, int GP>
+struct FmaState {
+    static constexpr int LPR = HD / 8;     // lanes per K/V row
+    static constexpr int RG = 32 / LPR;    // row groups
+    static constexpr int TPL = kBlock / RG;  // tokens per lane
+    static constexpr int R = GP / 2;       // reduced values per lane
+    static_assert(TPL * GP % LPR == 0 && TPL * GP / LPR == R, "layout");
+    float q[GP][8];
+    float o[GP][8];
+    float m[R], l[R];
+
+    __device__ __forceinline__ void begin_unit(const AttnParams& p, int b, int h, int lane) {
+        const int c = lane % LPR;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            if (g < p.G) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+                    p.q + ((long long)b * p.Hq + (long long)h * p.G + g) * HD + c * 8));
+                q[g][0] = bf16_lo(w.x); q[g][1] = bf16_hi(w.x);
+                q[g][2] = bf16_lo(w.y); q[g][3] = bf16_hi(w.y);
+                q[g][4] = bf16_lo(w.z); q[g][5] = bf16_hi(w.z);
+                q[g][6] = bf16_lo(w.w); q[g][7] = bf16_hi(w.w);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[g][e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < R; ++k) { m[k] = kNegInf; l[k] = 0.f; }
+    }
+
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float sl2, int lane,
+                                          float* xp, int G) {
+        const int c = lane % LPR, r = lane / LPR;
+        float val[TPL * GP];
+#pragma unroll
+        for (int i = 0; i < TPL; ++i) {
+            const int t = r + RG * i;
+            uint32_t w0, w1, w2, w3;
+            lds128(kt + swz(t, c), w0, w1, w2, w3);
+            const float kf[8] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1),
+                                 bf16_lo(w2), bf16_hi(w2), bf16_lo(w3), bf16_hi(w3)};
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(q[g][e], kf[e], acc);
+                val[i * GP + g] = acc;
+            }
+        }
+        // transposing butterfly over the LPR lanes of a row
+#pragma unroll
+        for (int msk = LPR / 2, n = TPL * GP; msk >= 1; msk >>= 1, n >>= 1) {
+            const bool up = (lane & msk) != 0;
+#pragma unroll
+            for (int k = 0; k < n / 2; ++k) {
+                const float lo = val[k], hi = val[k + n / 2];
+                const float send = up ? lo : hi;
+                const float keep = up ? hi : lo;
+                val[k] = keep + __shfl_xor_sync(0xffffffffu, send, msk);
+            }
+        }
+        const int t = r + RG * (c >> 1);
+        const int g0 = (c & 1) * R;
+        float s[R], al[R];
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            s[k] = (t < valid && g0 + k < G) ? val[k] * sl2 : kNegInf;
+            float mx = s[k];
+#pragma unroll
+            for (int sh = 2; sh < 32; sh <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+            const float mn = fmaxf(m[k], mx);
+            const float ref = mn == kNegInf ? 0.f : mn;
+            al[k] = exp2f(m[k] - ref);
+            const float pk = exp2f(s[k] - ref);
+            l[k] = l[k] * al[k] + pk;
+            m[k] = mn;
+            xp[t * GP + g0 + k] = pk;
+        }
+        if (lane < 2) {
+#pragma unroll
+            for (int k = 0; k < R; ++k) xp[kBlock * GP + g0 + k] = al[k];
+        }
+        __syncwarp();
+        float alpha[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) alpha[g] = xp[kBlock * GP + g];
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[g][e] *= alpha[g];
+#pragma unroll
+        for (int i = 0; i < TPL; ++i) {
+            const int tt = r + RG * i;
+            if (tt < valid) {
+                uint32_t w0, w1, w2, w3;
+                lds128(vt + swz(tt, c), w0, w1, w2, w3);
+                const float vf[8] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1),
+                                     bf16_lo(w2), bf16_hi(w2), bf16_lo(w3), bf16_hi(w3)};
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    const float pw = xp[tt * GP + g];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[g][e] = fmaf(pw, vf[e], o[g][e]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void store(float* mbuf, float* lbuf, float* obuf, int G, int lane) {
+        const int c = lane % LPR;
+#pragma unroll
+        for (int k = 0; k < R; ++k)
+#pragma unroll
+            for (int sh = 2; sh < 32; sh <<= 1) l[k] += __shfl_xor_sync(0xffffffffu, l[k], sh);
+#pragma unroll
+        for (int sh = LPR; sh < 32; sh <<= 1)
+#pragma unroll
+            for (int g = 0; g < GP; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], sh);
+        if (lane < 2) {
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const int g = (lane & 1) * R + k;
+                if (g < G) { mbuf[g] = m[k]; lbuf[g] = l[k]; }
+            }
+        }
+        if (lane < LPR) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g)
+                if (g < G)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) obuf[g * HD + c * 8 + e] = o[g][e];
+        }
+    }
+};
+
+// ------------------------------------------------------ the main kernel ---
+
+enum { kVarMma = 1, kVarFma = 2 };
+
+template <int HD, int VAR, int GP>
+struct StateOf;
+template <int HD, int GP>
+struct StateOf<HD, kVarMma, GP> { using T = MmaState<HD>; };
+template <int HD, int GP>
+struct StateOf<HD, kVarFma, GP> { using T = FmaState<HD, GP>; };
+
+template <int HD, int VAR, int GP, int W>
+__global__ void __launch_bounds__(W * 32, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = p.stages;
+    const SmemPlan sp = smem_plan(W, S, HD, p.G);
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t* base = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    float* mbuf = reinterpret_cast<float*>(base + sp.mbuf);
+    float* lbuf = reinterpret_cast<float*>(base + sp.lbuf);
+    float* fac = reinterpret_cast<float*>(base + sp.fac);
+    float* obuf = reinterpret_cast<float*>(base + sp.obuf);
+    float* xbuf = reinterpret_cast<float*>(base + sp.xbuf) + warp * (kBlock * kMaxG + kMaxG);
+    long long* scan = reinterpret_cast<long long*>(base + sp.scan);
+    long long* found = reinterpret_cast<long long*>(base + sp.found);
+    constexpr int kTile = Tile<HD>::kBytes;
+    const uint32_t my_tiles = sbase + sp.tiles + (uint32_t)(warp * S * 2 * kTile);
+    const uint32_t my_bars = sbase + sp.bars + (uint32_t)(warp * S * 8);
+
+    // Rows of requests with no tokens are zero; CTA i owns b = i mod gridDim.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        const int n = __ldg(p.context_lens + b);
+        if (n > p.mbps * kBlock && tid == 0) raise_err(p.dev_err, MI_DEVERR_BAD_CONTEXT);
+        if (n <= 0) {
+            uint4* row = reinterpret_cast<uint4*>(p.out + (long long)b * p.Hq * HD);
+            for (int i = tid; i < p.Hq * HD / 8; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // The plan: total blocks, this CTA's range, the unit holding its start.
+    const Plan pl = plan_scan(p, scan);
+    const long long TB = pl.TB;
+    const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
+    if ((int)blockIdx.x >= P) return;
+    const long long ra = range_start(TB, P, blockIdx.x), rb = range_start(TB, P, blockIdx.x + 1);
+    plan_find(p, pl, ra, scan, found);
+    Cursor cu;
+    cu.b = (int)found[0];
+    cu.h = (int)found[1];
+    cu.start = found[2];
+    cu.len = (int)found[3];
+
+    if (tid < W * S) mbar_init(sbase + sp.bars + tid * 8, 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    // Producer state (lane 0 of each warp): its own cursor over the unit sequence.
+    const long long nmine = (rb - ra > warp) ? (rb - ra - warp + W - 1) / W : 0;
+    Cursor pc = cu;
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](long long k) {
+        const long long x = ra + warp + k * W;
+        pc.advance_to(p, x);
+        const int j = (int)(x - pc.start);
+        const int blk = __ldg(p.block_tables + (long long)pc.b * p.mbps + j);
+        const uint32_t bar = my_bars + (uint32_t)((k % S) * 8);
+        if (blk < 0 || blk >= p.num_blocks) {
+            raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
+            mbar_arrive(bar);
+            return;
+        }
+        const uint32_t dst = my_tiles + (uint32_t)((k % S) * 2 * kTile);
+        mbar_arrive_expect_tx(bar, 2 * kTile);
+        const int y = (blk * p.Hkv + pc.h) * kBlock;
+#pragma unroll
+        for (int hf = 0; hf < Tile<HD>::kHalves; ++hf) {
+            tma_load_2d(dst + hf * 2048, &tmk, bar, hf * 64, y, policy);
+            tma_load_2d(dst + kTile + hf * 2048, &tmv, bar, hf * 64, y, policy);
+        }
+    };
+    if (lane == 0)
+        for (long long k = 0; k < nmine && k < S; ++k) issue(k);
+
+    using State = typename StateOf<HD, VAR, GP>::T;
+    State st;
+    bool dead = false;     // a wait timed out: stop touching the pipeline
+    long long k = 0;       // blocks of this warp consumed so far
+    long long k_dead = 0;  // first block whose wait timed out
+    float* res = fac + W * kMaxG;  // rows: 1/L, M, L per head
+
+    while (cu.start < rb && cu.b < p.B) {
+        const long long sa = cu.start > ra ? cu.start : ra;
+        const long long se = (cu.start + cu.len) < rb ? (cu.start + cu.len) : rb;
+        const int nvalid = ctx_clamped(p, cu.b);
+        st.begin_unit(p, cu.b, cu.h, lane);
+        long long x = sa + (((warp - (sa - ra)) % W) + W) % W;
+        for (; x < se; x += W) {
+            const uint32_t stage = (uint32_t)(k % S);
+            const uint32_t par = (uint32_t)((k / S) & 1);
+            if (!dead) {
+                const bool ok = mbar_wait_bounded(my_bars + stage * 8, par);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    dead = true;
+                    k_dead = k;
+                    if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+                }
+            }
+            const int j = (int)(x - cu.start);
+            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
+            const int valid = min(kBlock, nvalid - j * kBlock);
+            if (!dead && blk >= 0 && blk < p.num_blocks) {
+                const uint32_t kt = my_tiles + stage * 2 * kTile, vt = kt + kTile;
+                if (VAR == kVarMma && valid < kBlock) {
+                    // rows past the context may hold any bits: zero V there
+                    for (int i = lane; i < (kBlock - valid) * (HD / 8); i += 32) {
+                        const int row = valid + i / (HD / 8), ch = i % (HD / 8);
+                        st_shared_zero16(vt + swz(row, ch));
+                    }
+                    __syncwarp();
+                }
+                if constexpr (VAR == kVarMma) {
+                    st.block(kt, vt, valid, p.sl2, lane);
+                } else {
+                    st.block(kt, vt, valid, p.sl2, lane, xbuf, p.G);
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && !dead && k + S < nmine) {
+                fence_proxy_async_smem();
+                issue(k + S);
+            }
+            ++k;
+        }
+        // merge the warps' states for this unit (a warp without a block in it
+        // stores its initial state: max -inf, sum 0, output 0)
+        st.store(mbuf + warp * kMaxG, lbuf + warp * kMaxG, obuf + warp * p.G * HD, p.G, lane);
+        __syncthreads();
+        if (tid < p.G) {
+            float M = kNegInf;
+            for (int w = 0; w < W; ++w) M = fmaxf(M, mbuf[w * kMaxG + tid]);
+            float L = 0.f;
+            for (int w = 0; w < W; ++w) {
+                const float f = (M == kNegInf) ? 0.f : exp2f(mbuf[w * kMaxG + tid] - M);
+                fac[w * kMaxG + tid] = f;
+                L += f * lbuf[w * kMaxG + tid];
+            }
+            res[tid] = L > 0.f ? 1.f / L : 0.f;
+            res[kMaxG + tid] = M;
+            res[2 * kMaxG + tid] = L;
+        }
+        __syncthreads();
+        const bool whole = (sa == cu.start) && (se == cu.start + cu.len);
+        const int slot = (sa == ra) ? 0 : 1;
+        float* part = p.part + ((long long)blockIdx.x * 2 + slot) * p.slot_floats;
+        for (int idx = tid; idx < p.G * HD; idx += blockDim.x) {
+            const int g = idx / HD, dcol = idx - g * HD;
+            float acc = 0.f;
+            for (int w = 0; w < W; ++w) {
+                const float f = fac[w * kMaxG + g];
+                if (f != 0.f) acc += f * obuf[(w * p.G + g) * HD + dcol];
+            }
+            const float v = acc * res[g];
+            if (whole) {
+                p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + dcol] = f32_to_bf16(v);
+            } else {
+                part[idx] = v;
+                if (dcol == 0) {
+                    const float L = res[2 * kMaxG + g];
+                    part[p.G * HD + g] = L > 0.f ? res[kMaxG + g] + log2f(L) : kNegInf;
+                }
+            }
+        }
+        __syncthreads();
+        cu.next(p);
+    }
+    // After a timed-out wait, let the copies this warp still has in flight
+    // land (each wait bounded again) before the CTA's shared memory goes away.
+    if (dead) {
+        for (long long kk = k_dead; kk < k_dead + S && kk < nmine; ++kk)
+            (void)mbar_wait_bounded(my_bars + (uint32_t)((kk % S) * 8), (uint32_t)((kk / S) & 1));
+    }
+}
+
+// Merge the partials of every unit that a range boundary cut. Boundary i
+// (between CTA i-1 and CTA i) handles the unit holding flat block ra(i) when
+// this is the unit's first cut.
+template <int HD>
+__global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
+    __shared__ long long scan[256 + 1 + 32];
+    __shared__ long long found[4];
+    const Plan pl = plan_scan(p, scan);
+    const long long TB = pl.TB;
+    const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
+    const int i = blockIdx.x;
+    if (i == 0 || i >= P) return;
+    const long long x = range_start(TB, P, i);
+    plan_find(p, pl, x, scan, found);
+    const int b = (int)found[0], h = (int)found[1];
+    const long long us = found[2];
+    const int len = (int)found[3];
+    if (us == x) return;                              // not cut here
+    const long long prev = range_start(TB, P, i - 1);
+    if (us < prev) return;                            // cut earlier; handled there
+    const long long ue = us + len;                    // unit end
+    int last = i;
+    while (last + 1 < P && range_start(TB, P, last + 1) < ue) ++last;
+    const int first_slot = (us == prev) ? 0 : 1;
+    const int G = p.G;
+    for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+        const int g = idx / HD;
+        float M = kNegInf;
+        for (int c = i - 1; c <= last; ++c) {
+            const int s = (c == i - 1) ? first_slot : 0;
+            M = fmaxf(M, p.part[((long long)c * 2 + s) * p.slot_floats + G * HD + g]);
+        }
+        float num = 0.f, den = 0.f;
+        if (M != kNegInf) {
+            for (int c = i - 1; c <= last; ++c) {
+                const int s = (c == i - 1) ? first_slot : 0;
+                const float* sl = p.part + ((long long)c * 2 + s) * p.slot_floats;
+                const float wgt = exp2f(sl[G * HD + g] - M);
+                num += wgt * sl[idx];
+                den += wgt;
+            }
+        }
+        const float v = den > 0.f ? num / den : 0.f;
+        p.out[((long long)b * p.Hq + (long long)h * G + g) * HD + (idx - g * HD)] = f32_to_bf16(v);
+    }
+}
+
+// ------------------------------------------------------------- host side --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult qr;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)HD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)HD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr int kWarps = 8;
+constexpr int kMaxStages = 4;
+constexpr int kSmemLimit = 227 * 1024;
+
+int pick_stages(int HD, int G) {
+    for (int S = kMaxStages; S >= 1; --S)
+        if (smem_plan(kWarps, S, HD, G).total <= kSmemLimit) return S;
+    return 0;
+}
+
+int gp_of(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : 8); }
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, AttnParams);
+
+template <int HD>
+KernelFn fma_kernel_for(int GP) {
+    switch (GP) {
+        case 2: return attn_kernel<HD, kVarFma, 2, kWarps>;
+        case 4: return attn_kernel<HD, kVarFma, 4, kWarps>;
+        default: return attn_kernel<HD, kVarFma, 8, kWarps>;
+    }
+}
+
+KernelFn pick_kernel(int HD, int var, int G) {
+    // the MMA tile always spans 8 head columns; the FMA tile is sized to G
+    if (var == kVarMma) return HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps> : attn_kernel<128, kVarMma, 8, kWarps>;
+    return HD == 64 ? fma_kernel_for<64>(gp_of(G)) : fma_kernel_for<128>(gp_of(G));
+}
+
+struct GridKey {
+    int dev;
+    KernelFn fn;
+    int smem;
+};
+
+// Persistent grid: SMs x resident CTAs of this kernel at this smem size.
+// Queried once per (device, kernel, smem) and cached; the query also raises
+// the kernel's dynamic shared-memory limit on that device.
+int grid_for(KernelFn fn, int smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static GridKey keys[64];
+    static int vals[64];
+    static int nkeys = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < nkeys; ++i)
+            if (keys[i].dev == dev && keys[i].fn == fn && keys[i].smem == smem) return vals[i];
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+        return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), kWarps * 32,
+                                                      smem) != cudaSuccess)
+        return 0;
+    const int g = sms * (occ > 0 ? occ : 1);
+    std::lock_guard<std::mutex> lk(mu);
+    if (nkeys < 64) {
+        keys[nkeys] = GridKey{dev, fn, smem};
+        vals[nkeys] = g;
+        ++nkeys;
+    }
+    return g;
+}
+
+mi_status check_dims(const mi_dims* dims) {
+    if (!dims) return MI_ERR_INVALID_ARG;
+    const mi_dims& D = *dims;
+    if (D.B < 0 || D.B > 65535 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1)
+        return MI_ERR_INVALID_ARG;
+    if (D.block_size != kBlock || (D.head_dim != 64 && D.head_dim != 128) || D.Hq % D.Hkv != 0 ||
+        D.Hq / D.Hkv > kMaxG)
+        return MI_ERR_UNSUPPORTED;
+    if ((long long)D.num_blocks * D.Hkv * kBlock > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
+    if ((long long)D.max_blocks_per_seq * kBlock > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
+    return MI_OK;
+}
+
+int slot_floats(const mi_dims& D) { return (D.Hq / D.Hkv) * D.head_dim + 8; }
+
+int max_grid(const mi_dims& D) {
+    const int G = D.Hq / D.Hkv;
+    const int S = pick_stages(D.head_dim, G);
+    if (!S) return 0;
+    const int smem = smem_plan(kWarps, S, D.head_dim, G).total;
+    int g = 0;
+    for (int var : {kVarMma, kVarFma}) {
+        const int n = grid_for(pick_kernel(D.head_dim, var, G), smem);
+        if (n <= 0) return 0;
+        g = n > g ? n : g;
+    }
+    return g;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace mi
+
+extern "C" size_t mi_paged_decode_workspace_bytes(const mi_dims* dims) {
+    using namespace mi;
+    if (check_dims(dims) != MI_OK) return 0;
+    const int g = max_grid(*dims);
+    if (g <= 0) return 0;
+    return (size_t)g * 2 * (size_t)slot_floats(*dims) * sizeof(float);
+}
+
+extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
+                                                       const void* k_cache, const void* v_cache,
+                                                       const int32_t* block_tables,
+                                                       const int32_t* context_lens, float scale,
+                                                       void* out, void* workspace,
+                                                       size_t workspace_bytes, int32_t* dev_err,
+                                                       mi_stream_t stream, mi_attn_variant variant,
+                                                       int32_t ctas) {
+    using namespace mi;
+    const mi_status ds = check_dims(dims);
+    if (ds != MI_OK) return ds;
+    const mi_dims D = *dims;
+    if (D.B == 0) return MI_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return MI_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
+        !aligned16(workspace))
+        return MI_ERR_INVALID_ARG;
+    if (ctas < 0 || !std::isfinite(scale)) return MI_ERR_INVALID_ARG;
+    const int var = variant == MI_ATTN_FMA ? kVarFma : kVarMma;
+    if (variant != MI_ATTN_DEFAULT && variant != MI_ATTN_MMA && variant != MI_ATTN_FMA)
+        return MI_ERR_INVALID_ARG;
+    const int G = D.Hq / D.Hkv, HD = D.head_dim;
+    const int S = pick_stages(HD, G);
+    const int smem = smem_plan(kWarps, S, HD, G).total;
+    const int gmax = max_grid(D);
+    if (gmax <= 0) return MI_ERR_CUDA;
+    const size_t need = (size_t)gmax * 2 * (size_t)slot_floats(D) * sizeof(float);
+    if (workspace_bytes < need) return MI_ERR_INVALID_ARG;
+    const int grid = ctas > 0 && ctas < gmax ? ctas : gmax;
+
+    CUtensorMap tk, tv;
+    const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
+    if (!make_tmap(&tk, k_cache, rows, HD) || !make_tmap(&tv, v_cache, rows, HD)) return MI_ERR_CUDA;
+
+    AttnParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<uint16_t*>(out);
+    p.part = static_cast<float*>(workspace);
+    p.dev_err = dev_err;
+    p.B = D.B;
+    p.Hq = D.Hq;
+    p.Hkv = D.Hkv;
+    p.G = G;
+    p.num_blocks = D.num_blocks;
+    p.mbps = D.max_blocks_per_seq;
+    p.stages = S;
+    p.slot_floats = slot_floats(D);
+    p.sl2 = scale * 1.4426950408889634f;
+
+    KernelFn fn = pick_kernel(HD, var, G);
+    cudaStream_t s = (cudaStream_t)stream;
+    fn<<<grid, kWarps * 32, smem, s>>>(tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return MI_ERR_CUDA;
+    if (HD == 64)
+        combine_kernel<64><<<grid, 256, 0, s>>>(p);
+    else
+        combine_kernel<128><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}
+
+extern "C" mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,
+                                               const void* v_cache, const int32_t* block_tables,
+                                               const int32_t* context_lens, float scale, void* out,
+                                               void* workspace, size_t workspace_bytes,
+                                               int32_t* dev_err, mi_stream_t stream) {
+    return mi_paged_decode_attention_variant(dims, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                             out, workspace, workspace_bytes, dev_err, stream,
+                                             MI_ATTN_DEFAULT, 0);
+}

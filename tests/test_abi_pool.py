@@ -1,0 +1,158 @@
+"""CPU tests of the C ABI: the library loads and exports every symbol the
+header declares; the host block pool matches the oracle's pool model table for
+table under each workload's history and random churn; host-side argument checks
+reject bad calls without touching a GPU; the host RoPE table matches the
+oracle's bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.pool import PoolModel
+from workloads import WORKLOADS, context_lengths, initial_free_order, setup_pool
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mi():
+    import paged_kv_decode_25_gb300 as mi
+    from paged_kv_decode_25_gb300 import build
+    build.build()
+    mi.load()
+    return mi
+
+
+def _declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mi_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol(mi):
+    declared = _declared_symbols()
+    assert declared, "no declarations found"
+    lib = mi.load()
+    for n in declared:
+        assert hasattr(lib, n), n
+    assert declared == set(mi.EXPORTS)
+
+
+def _compare(lib, model, seqs, mbps):
+    bt1, cl1, sl1 = lib.batch_meta(seqs)
+    bt2, cl2, sl2 = model.batch_meta(seqs)
+    assert np.array_equal(bt1, bt2) and np.array_equal(cl1, cl2) and np.array_equal(sl1, sl2)
+    assert lib.num_free() == model.num_free()
+    return bt1, cl1, sl1
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_pool_matches_model_on_workload_history(mi, name):
+    w = WORKLOADS[name]
+    ctx = context_lengths(w)
+    order = initial_free_order(w)
+    lib = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, order)
+    model = PoolModel(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, order)
+    setup_pool(w, lib, ctx)
+    setup_pool(w, model, ctx)
+    seqs = list(range(w.B))
+    _compare(lib, model, seqs, w.max_blocks_per_seq)
+    steps = min(w.sweep_steps, 20)
+    for s in range(steps):
+        for b in seqs:
+            assert lib.alloc(b, int(ctx[b]) + s + 1) == 0
+            assert model.alloc(b, int(ctx[b]) + s + 1) == 0
+        bt, cl, sl = _compare(lib, model, seqs, w.max_blocks_per_seq)
+        # the slot of the newest token, from the oracle's own slot arithmetic
+        assert np.array_equal(sl, oracle.slot_mapping(bt, cl - 1))
+    if w.churn:  # the churned pool hands out blocks out of order
+        bt, _, _ = lib.batch_meta(seqs)
+        assert np.any(np.diff(bt[0][bt[0] >= 0]) != 1)
+
+
+def test_pool_random_churn_matches_model(mi):
+    r = np.random.Generator(np.random.PCG64(31))
+    N, S, W = 500, 64, 40
+    order = r.permutation(N)
+    lib = mi.Pool(N, S, W, order)
+    model = PoolModel(N, S, W, order)
+    for it in range(4000):
+        s = int(r.integers(0, S))
+        if r.random() < 0.25:
+            assert lib.free(s) == model.free(s)
+        else:
+            n = max(0, model.tokens.get(s, 0) + int(r.integers(-3, 80)))
+            assert lib.alloc(s, n) == model.alloc(s, n)
+        if it % 97 == 0:
+            live = sorted(model.tables)
+            if live:
+                _compare(lib, model, live, W)
+    for s in sorted(model.tables):
+        got = mi.mi_kv_pool_seq_blocks(lib.handle, s)
+        assert list(got) == model.tables[s]
+
+
+def test_pool_errors(mi):
+    st, h = mi.mi_kv_pool_create(8, 16, 2, 2)
+    assert st == mi.MI_OK
+    assert mi.mi_kv_pool_alloc(h, 2, 1) == mi.MI_ERR_INVALID_ARG      # seq id out of range
+    assert mi.mi_kv_pool_alloc(h, 0, -1) == mi.MI_ERR_INVALID_ARG     # negative tokens
+    assert mi.mi_kv_pool_alloc(h, 0, 33) == mi.MI_ERR_INVALID_ARG     # wider than a row
+    assert mi.mi_kv_pool_free(h, 1) == mi.MI_ERR_UNKNOWN_SEQ
+    assert mi.mi_kv_pool_alloc(h, 0, 20) == mi.MI_OK
+    assert mi.mi_kv_pool_alloc(h, 0, 10) == mi.MI_ERR_INVALID_ARG     # shrinking
+    st, bt, cl, sl = mi.mi_kv_pool_batch_meta(h, [0, 1], 2)
+    assert st == mi.MI_ERR_UNKNOWN_SEQ
+    mi.mi_kv_pool_destroy(h)
+    assert mi.mi_kv_pool_create(8, 32, 2, 2)[0] == mi.MI_ERR_UNSUPPORTED
+    assert mi.mi_kv_pool_create(0, 16, 2, 2)[0] == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_kv_pool_create(4, 16, 2, 2, [0, 1, 1, 3])[0] == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_kv_pool_num_free(None) == -1
+
+
+def test_pool_exhaustion_is_all_or_nothing(mi):
+    lib = mi.Pool(6, 4, 8)
+    assert lib.alloc(0, 16 * 4) == 0
+    before = mi.mi_kv_pool_seq_blocks(lib.handle, 0).tolist(), lib.num_free()
+    assert lib.alloc(0, 16 * 7) == mi.MI_ERR_OUT_OF_BLOCKS
+    assert (mi.mi_kv_pool_seq_blocks(lib.handle, 0).tolist(), lib.num_free()) == before
+    assert lib.alloc(1, 16 * 3) == mi.MI_ERR_OUT_OF_BLOCKS
+    assert mi.mi_kv_pool_seq_blocks(lib.handle, 1) is None
+
+
+@pytest.mark.parametrize("d,theta,max_pos", [(64, 1e6, 100), (128, 1e6, 9000), (128, 1e4, 33)])
+def test_rope_table_matches_oracle_bits(mi, d, theta, max_pos):
+    st, t = mi.mi_rope_table(theta, d, max_pos)
+    assert st == mi.MI_OK
+    ref = oracle.rope_table(theta, d, max_pos)
+    assert np.array_equal(t.view(np.uint32), ref.view(np.uint32))
+
+
+def test_device_entry_points_reject_bad_args_without_a_gpu(mi):
+    d = mi.dims(2, 4, 2, 64, 8, 4)
+    bad = mi.dims(2, 4, 3, 64, 8, 4)  # Hq % Hkv != 0
+    assert mi.mi_paged_decode_workspace_bytes(bad) == 0
+    assert mi.mi_paged_kv_append(bad, 16, 16, 16, 16, 16, 16, 4, 16, 16, 16, stream=0) == mi.MI_ERR_UNSUPPORTED
+    odd = mi.dims(2, 4, 2, 96, 8, 4)
+    assert mi.mi_paged_kv_append(odd, 16, 16, 16, 16, 16, 16, 4, 16, 16, 16, stream=0) == mi.MI_ERR_UNSUPPORTED
+    wide = mi.dims(2, 18, 2, 64, 8, 4)  # G = 9
+    assert mi.load().mi_paged_decode_attention_variant(
+        __import__("ctypes").byref(wide), 16, 16, 16, 16, 16, 1.0, 16, 16, 1 << 20, None, 0, 0, 0
+    ) == mi.MI_ERR_UNSUPPORTED
+    # null pointers are caught before any CUDA call
+    assert mi.mi_paged_kv_append(d, None, 16, 16, 16, 16, 16, 4, 16, 16, 16, stream=0) == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_paged_decode_attention(d, None, 16, 16, 16, 16, 1.0, 16, 16, workspace_bytes=1 << 20,
+                                        stream=0) == mi.MI_ERR_INVALID_ARG
+    # misaligned caches are rejected
+    assert mi.mi_paged_decode_attention(d, 16, 18, 16, 16, 16, 1.0, 16, 16, workspace_bytes=1 << 20,
+                                        stream=0) == mi.MI_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    zero = mi.dims(0, 4, 2, 64, 8, 4)
+    assert mi.mi_paged_kv_append(zero, None, None, None, None, None, None, 4, None, None, None,
+                                 stream=0) == mi.MI_OK

@@ -1,0 +1,150 @@
+"""GPU parity of mi_paged_kv_append against the oracle: bit-exact q_out and
+cache contents, every byte the append must not touch left as it was (the
+caches start filled with a NaN canary outside the live history)."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import from_dev_u16, grow, pools_for, to_dev_i32, to_dev_u16
+from workloads import WORKLOADS, device_fill_cache, history_cache, new_token_values
+
+pytestmark = pytest.mark.gpu
+
+
+def _mi():
+    import paged_kv_decode_25_gb300 as mi
+    return mi
+
+
+@pytest.mark.parametrize("name,layers", [("tiny", [0]), ("qwen3_1p7b", [0]), ("skewed", [0]),
+                                         ("qwen25_7b_sweep", [0, 27])])
+def test_append_bit_exact(cuda_device, name, layers):
+    import torch
+    mi = _mi()
+    w = WORKLOADS[name]
+    lib, model, ctx = pools_for(w)
+    bt_hist, _, _ = lib.batch_meta(range(w.B))
+    grow(lib, w.B, ctx + 1)
+    grow(model, w.B, ctx + 1)
+    bt, cl, sl = lib.batch_meta(range(w.B))
+    bt_m, cl_m, sl_m = model.batch_meta(range(w.B))
+    assert np.array_equal(bt, bt_m) and np.array_equal(sl, sl_m)
+    pos = (cl - 1).astype(np.int32)
+    assert np.array_equal(oracle.slot_mapping(bt_m, pos), sl)
+    st, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    assert st == 0
+    table_ref = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    rope_d = torch.from_numpy(table).to(cuda_device)
+    pos_d, sl_d = to_dev_i32(pos, cuda_device), to_dev_i32(sl, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for layer in layers:
+        kc, vc = history_cache(w, layer, bt_hist, ctx)
+        q, k, v = new_token_values(w, layer)
+        kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(vc, cuda_device)
+        q_d, k_d, v_d = (to_dev_u16(a, cuda_device) for a in (q, k, v))
+        qo_d = torch.empty_like(q_d)
+        assert mi.mi_paged_kv_append(d, q_d, k_d, v_d, pos_d, sl_d, rope_d, w.max_pos, qo_d, kc_d, vc_d,
+                                     err) == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        q_ref, st = oracle.append(q, k, v, pos, sl_m, table_ref, kc, vc)
+        assert st == 0
+        assert np.array_equal(from_dev_u16(qo_d), q_ref)
+        assert np.array_equal(from_dev_u16(kc_d), kc)
+        assert np.array_equal(from_dev_u16(vc_d), vc)
+
+
+def test_append_in_place_q(cuda_device):
+    import torch
+    mi = _mi()
+    w = WORKLOADS["tiny"]
+    lib, model, ctx = pools_for(w)
+    grow(lib, w.B, ctx + 1)
+    bt, cl, sl = lib.batch_meta(range(w.B))
+    pos = (cl - 1).astype(np.int32)
+    _, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    q, k, v = new_token_values(w, 0)
+    kc = np.zeros((w.num_blocks, w.Hkv, 16, w.head_dim), np.uint16)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    q_d = to_dev_u16(q, cuda_device)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(kc, cuda_device)
+    assert mi.mi_paged_kv_append(d, q_d, to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                 to_dev_i32(pos, cuda_device), to_dev_i32(sl, cuda_device),
+                                 torch.from_numpy(table).to(cuda_device), w.max_pos, q_d, kc_d, vc_d) == 0
+    torch.cuda.synchronize()
+    q_ref, _ = oracle.append(q, k, v, pos, sl, oracle.rope_table(w.theta, w.head_dim, w.max_pos), kc, kc.copy())
+    assert np.array_equal(from_dev_u16(q_d), q_ref)
+
+
+def test_append_full_size_serving_layer(cuda_device):
+    """Qwen3-8B-shaped layer at full size (24,576-block pool after churn): every
+    written slot equals the oracle's rotation, nothing else in the 1.6 GB of
+    cache changes."""
+    import torch
+    mi = _mi()
+    w = WORKLOADS["qwen3_8b"]
+    lib, model, ctx = pools_for(w)
+    grow(lib, w.B, ctx + 1)
+    grow(model, w.B, ctx + 1)
+    bt, cl, sl = lib.batch_meta(range(w.B))
+    assert np.array_equal(sl, model.batch_meta(range(w.B))[2])
+    pos = (cl - 1).astype(np.int32)
+    _, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    table_ref = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    shape = (w.num_blocks, w.Hkv, 16, w.head_dim)
+    kc_d = torch.empty(shape, dtype=torch.bfloat16, device=cuda_device)
+    vc_d = torch.empty_like(kc_d)
+    device_fill_cache(w, 0, kc_d, vc_d)
+    k0, v0 = kc_d.clone(), vc_d.clone()
+    q, k, v = new_token_values(w, 0)
+    q_d = to_dev_u16(q, cuda_device)
+    qo_d = torch.empty_like(q_d)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    assert mi.mi_paged_kv_append(d, q_d, to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                 to_dev_i32(pos, cuda_device), to_dev_i32(sl, cuda_device),
+                                 torch.from_numpy(table).to(cuda_device), w.max_pos, qo_d, kc_d, vc_d,
+                                 err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    blk = torch.from_numpy((sl // 16).astype(np.int64)).to(cuda_device)
+    off = torch.from_numpy((sl % 16).astype(np.int64)).to(cuda_device)
+    got_k = from_dev_u16(kc_d[blk, :, off])  # [B][Hkv][d]
+    got_v = from_dev_u16(vc_d[blk, :, off])
+    for b in range(w.B):
+        assert np.array_equal(got_k[b], oracle.rope_rotate(k[b], table_ref, int(pos[b])))
+        assert np.array_equal(got_v[b], v[b])
+        assert np.array_equal(from_dev_u16(qo_d[b]), oracle.rope_rotate(q[b], table_ref, int(pos[b])))
+    kc_d[blk, :, off] = k0[blk, :, off]
+    vc_d[blk, :, off] = v0[blk, :, off]
+    assert torch.equal(kc_d.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(vc_d.view(torch.int16), v0.view(torch.int16))
+
+
+def test_append_bad_slot_and_position_flagged(cuda_device):
+    import torch
+    mi = _mi()
+    B, Hq, Hkv, dd, nb = 3, 4, 2, 64, 4
+    r = np.random.Generator(np.random.PCG64(5))
+    from workloads import bf16_normal
+    q = bf16_normal(r, (B, Hq, dd)); k = bf16_normal(r, (B, Hkv, dd)); v = bf16_normal(r, (B, Hkv, dd))
+    _, table = mi.mi_rope_table(1e6, dd, 8)
+    kc = np.full((nb, Hkv, 16, dd), 0x1234, np.uint16)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(kc, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    d = mi.dims(B, Hq, Hkv, dd, nb, 4)
+    pos = np.array([1, 9, 2], np.int32)          # 9 is past the table
+    slots = np.array([5, 3, nb * 16], np.int32)  # nb*16 is past the cache
+    qo_d = torch.zeros_like(to_dev_u16(q, cuda_device))
+    assert mi.mi_paged_kv_append(d, to_dev_u16(q, cuda_device), to_dev_u16(k, cuda_device),
+                                 to_dev_u16(v, cuda_device), to_dev_i32(pos, cuda_device),
+                                 to_dev_i32(slots, cuda_device), torch.from_numpy(table).to(cuda_device), 8,
+                                 qo_d, kc_d, vc_d, err) == 0
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & mi.MI_DEVERR_BAD_POS and e & mi.MI_DEVERR_BAD_SLOT
+    # request 0 was written, request 1 (bad position) and 2's cache (bad slot) were not
+    kc_ref = kc.copy()
+    kc_ref[0, :, 5] = oracle.rope_rotate(k[0], oracle.rope_table(1e6, dd, 8), 1)
+    assert np.array_equal(from_dev_u16(kc_d), kc_ref)
