@@ -256,10 +256,15 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(WORKLOADS))
     ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers per step (default: the workload's); fewer only for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     assert args.warmup >= 0 and args.steps >= 1
     w = WORKLOADS[args.workload]
+    if args.layers is not None:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.layers)
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
@@ -337,8 +342,8 @@ def main():
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
            for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(int(vis[local]) if len(vis) > local and vis[local].isdigit() else local)
     clocks.start()
     time.sleep(0.3)
     barrier(world)

@@ -756,32 +756,30 @@ struct GridKey {
 };
 
 // Persistent grid: SMs x resident CTAs of this kernel at this smem size.
-// Queried once per (device, kernel, smem) and cached; the query also raises
-// the kernel's dynamic shared-memory limit on that device.
+// The first query for a (device, kernel) raises the kernel's dynamic
+// shared-memory limit to the largest plan any shape uses, so a launch never
+// depends on which shape was seen last; the grid is cached per smem size.
 int grid_for(KernelFn fn, int smem) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     static std::mutex mu;
-    static GridKey keys[64];
-    static int vals[64];
+    static GridKey keys[128];
+    static int vals[128];
     static int nkeys = 0;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        for (int i = 0; i < nkeys; ++i)
-            if (keys[i].dev == dev && keys[i].fn == fn && keys[i].smem == smem) return vals[i];
-    }
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < nkeys; ++i)
+        if (keys[i].dev == dev && keys[i].fn == fn && keys[i].smem == smem) return vals[i];
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemLimit) != cudaSuccess)
+        return 0;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-        return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), kWarps * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const int g = sms * (occ > 0 ? occ : 1);
-    std::lock_guard<std::mutex> lk(mu);
-    if (nkeys < 64) {
+    if (nkeys < 128) {
         keys[nkeys] = GridKey{dev, fn, smem};
         vals[nkeys] = g;
         ++nkeys;
