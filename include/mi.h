@@ -211,6 +211,36 @@ mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
                                             int32_t* dev_err, mi_stream_t stream,
                                             mi_attn_variant variant, int32_t ctas);
 
+/* ------------------------------------------------------------------------ */
+/* Allocation-free attention. The pages have no counterpart to this entry
+ * point: it serves callers of this library that cannot call cudaMalloc (a
+ * plugin whose host framework owns all device memory, a serving loop that
+ * forbids allocator calls because they can synchronise the device, a process
+ * held to a fixed device-memory budget). */
+
+/* Size of the library's own scratch array (16 MiB, per GPU that loads the
+ * library, held until the process exits). */
+#define MI_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* mi_paged_decode_attention without a workspace argument: the split-KV
+ * partials go to a fixed device array inside the library
+ * (MI_NOALLOC_SCRATCH_BYTES). Same inputs, outputs, results and device error
+ * bits as mi_paged_decode_attention. It calls no allocator.
+ * Returns MI_ERR_UNSUPPORTED when the dims are not supported or need more
+ * scratch than the array holds (mi_paged_decode_workspace_bytes(dims) >
+ * MI_NOALLOC_SCRATCH_BYTES), before anything is queued.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call on a device shares the one array and
+ * it keeps the last call's contents (nothing in it needs to start at zero):
+ * calls whose work overlaps on the GPU (other streams, other threads) race on
+ * it, so order them, e.g. on one stream. */
+mi_status mi_paged_decode_attention_noalloc(const mi_dims* dims, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables,
+                                            const int32_t* context_lens, float scale, void* out,
+                                            int32_t* dev_err, mi_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,9 @@ EXPORTS = (
     "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
+    "mi_paged_decode_attention_noalloc",
 )
+MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class MiDims(ctypes.Structure):
@@ -73,6 +75,7 @@ def load():
             "mi_paged_decode_attention": ([dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_attention_variant": (
                 [dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P, i32, i32], i32),
+            "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -243,3 +246,12 @@ def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tabl
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream),
         int(variant), int(ctas))
+
+
+def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                      dev_err=None, stream=None):
+    """Attention with the library's own fixed scratch array (no workspace
+    argument, no allocation). See include/mi.h for the sharing rules."""
+    return load().mi_paged_decode_attention_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                    _ptr(block_tables), _ptr(context_lens), float(scale),
+                                                    _ptr(out), _ptr(dev_err), _stream(stream))
