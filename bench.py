@@ -13,7 +13,8 @@ device-timed step, inputs resident in HBM. ``e2e`` = the same metric for real
 decode steps driven through the C ABI from host buffers: host pool growth and
 metadata, H2D of metadata and new q/k/v from pinned memory, 36 layers, D2H of
 the outputs. ``roofline`` = the attention call (split-KV kernel + LSE combine)
-against the measured HBM copy bandwidth. ``cpu_baseline`` = the fp64 oracle on
+against the measured HBM copy bandwidth (one kernel per layer: the log-sum-exp
+combine of split units runs inside it). ``cpu_baseline`` = the fp64 oracle on
 the host cores on a bounded sample.
 
 ``--impl reference`` times the oracle alone (the reference arm).
@@ -426,12 +427,12 @@ def main():
         "hbm_frac_step": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "paged decode attention (split-KV kernel + LSE combine), per layer",
+                     "kernel": "paged decode attention (split-KV kernel with the LSE combine of cut units fused), per layer",
                      "algorithmic_bytes_per_launch": a_bytes, "avg_launch_ms": attn_avg_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
-        "gpu_launches": args.steps * w.layers * 3,
+        "gpu_launches": args.steps * w.layers * 2,  # append + attention per layer
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

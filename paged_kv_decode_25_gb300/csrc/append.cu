@@ -9,6 +9,33 @@
 namespace mi {
 namespace {
 
+// Exact widening to double built from the bit fields (integer work only);
+// zero, subnormal, infinite and NaN inputs take the hardware conversion.
+__device__ __forceinline__ double bf16_bits_to_f64(uint32_t h) {
+    const uint32_t e = (h >> 7) & 0xFFu;
+    if (e == 0u || e == 0xFFu) return (double)__uint_as_float(h << 16);
+    const uint32_t hi = ((h & 0x8000u) << 16) | ((e + 896u) << 20) | ((h & 0x7Fu) << 13);
+    return __hiloint2double((int)hi, 0);
+}
+
+__device__ __forceinline__ double f32_to_f64_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t e = (u >> 23) & 0xFFu;
+    if (e == 0u || e == 0xFFu) return (double)f;
+    const uint32_t m = u & 0x7FFFFFu;
+    const uint32_t hi = (u & 0x80000000u) | ((e + 896u) << 20) | (m >> 3);
+    return __hiloint2double((int)hi, (int)(m << 29));
+}
+
+// y = RN_bf16(RN_double(a*b - c*d)) with every product exact in double: the
+// fma forms a*b - (c*d) exactly and rounds once, as the two-step form does.
+__device__ __forceinline__ uint32_t rot_lo(double a, double b, double c, double d) {
+    return f64_to_bf16(fma(a, b, -(c * d)));
+}
+__device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double d) {
+    return f64_to_bf16(fma(a, b, c * d));
+}
+
 struct AppendParams {
     const uint16_t* q;
     const uint16_t* k;
@@ -23,49 +50,87 @@ struct AppendParams {
     int Hq, Hkv, d, num_blocks, max_pos;
 };
 
-// One CTA per request. Threads walk (head, pair) items: heads 0..Hq-1 are
-// query heads (to q_out), heads Hq..Hq+Hkv-1 are key heads (to the cache);
-// then 16-byte chunks of v are copied.
-__global__ void __launch_bounds__(256) append_kernel(AppendParams a) {
-    const int b = blockIdx.x;
-    const int p = a.positions[b];
-    if (p < 0 || p >= a.max_pos) {
-        if (threadIdx.x == 0) raise_err(a.dev_err, MI_DEVERR_BAD_POS);
-        return;
-    }
-    const int slot = a.slot_mapping[b];
-    const bool slot_ok = slot >= 0 && slot < a.num_blocks * kBlock;
-    if (!slot_ok && threadIdx.x == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SLOT);
-    const long long blk = slot_ok ? slot / kBlock : 0;
-    const int off = slot_ok ? slot % kBlock : 0;
+// One thread per (request, head, group of 8 rotation pairs): heads 0..Hq-1 are
+// query heads (to q_out), heads Hq..Hq+Hkv-1 key heads (to the cache). Each
+// thread loads its two 16-byte halves and its 8 (cos, sin) pairs before it
+// computes or stores anything, so q_out may alias q. Threads past the
+// rotation items copy 16-byte chunks of v into the cache.
+__global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
+    // inputs may come from the kernel just before this one in the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int half = a.d / 2;
-    const float2* cs = a.rope + (long long)p * half;
-    const int items = (a.Hq + a.Hkv) * half;
-    for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
-        const int head = idx / half;
-        const int i = idx - head * half;
+    const int groups = half / 8;  // 8-pair groups per head
+    const long long n_rot = (long long)B * (a.Hq + a.Hkv) * groups;
+    const long long n_cpy = (long long)B * a.Hkv * (a.d / 8);
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < n_rot) {
+        const int grp = (int)(t % groups);
+        const long long bh = t / groups;
+        const int head = (int)(bh % (a.Hq + a.Hkv));
+        const int b = (int)(bh / (a.Hq + a.Hkv));
         const bool is_q = head < a.Hq;
-        if (!is_q && !slot_ok) continue;
         const uint16_t* src = is_q ? a.q + ((long long)b * a.Hq + head) * a.d
                                    : a.k + ((long long)b * a.Hkv + (head - a.Hq)) * a.d;
-        const double x1 = (double)bf16_to_f32(src[i]);
-        const double x2 = (double)bf16_to_f32(src[i + half]);
-        const float2 t = cs[i];
-        const double c = (double)t.x, s = (double)t.y;
-        const double y1 = x1 * c - x2 * s;  // products are exact in double
-        const double y2 = x2 * c + x1 * s;
-        uint16_t* dst = is_q ? a.q_out + ((long long)b * a.Hq + head) * a.d
-                             : a.k_cache + ((blk * a.Hkv + (head - a.Hq)) * kBlock + off) * a.d;
-        dst[i] = f64_to_bf16(y1);
-        dst[i + half] = f64_to_bf16(y2);
+        const int i0 = grp * 8;
+        // issue the independent loads first
+        const uint4 lo = *reinterpret_cast<const uint4*>(src + i0);
+        const uint4 hi = *reinterpret_cast<const uint4*>(src + i0 + half);
+        const int p = a.positions[b];
+        const int slot = is_q ? 0 : a.slot_mapping[b];
+        if (p < 0 || p >= a.max_pos) {
+            if (head == 0 && grp == 0) raise_err(a.dev_err, MI_DEVERR_BAD_POS);  // once per request
+            return;
+        }
+        long long dst_off;
+        if (is_q) {
+            dst_off = ((long long)b * a.Hq + head) * a.d;
+        } else {
+            if (slot < 0 || slot >= a.num_blocks * kBlock) {
+                if (head == a.Hq && grp == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SLOT);
+                return;
+            }
+            dst_off = (((long long)(slot / kBlock) * a.Hkv + (head - a.Hq)) * kBlock + slot % kBlock) * a.d;
+        }
+        const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (long long)p * half + i0);
+        float4 cs[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cs[j] = cs4[j];
+        const uint32_t xl[4] = {lo.x, lo.y, lo.z, lo.w};
+        const uint32_t xh[4] = {hi.x, hi.y, hi.z, hi.w};
+        uint32_t yl[4], yh[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // pairs 2j and 2j+1 of the group: (cos, sin) = cs[j].xy and cs[j].zw
+            const double a0 = bf16_bits_to_f64(xl[j] & 0xFFFFu), a1 = bf16_bits_to_f64(xl[j] >> 16);
+            const double b0 = bf16_bits_to_f64(xh[j] & 0xFFFFu), b1 = bf16_bits_to_f64(xh[j] >> 16);
+            const double c0 = f32_to_f64_bits(cs[j].x), s0 = f32_to_f64_bits(cs[j].y);
+            const double c1 = f32_to_f64_bits(cs[j].z), s1 = f32_to_f64_bits(cs[j].w);
+            const uint32_t r0 = rot_lo(a0, c0, b0, s0);
+            const uint32_t r1 = rot_lo(a1, c1, b1, s1);
+            const uint32_t r2 = rot_hi(b0, c0, a0, s0);
+            const uint32_t r3 = rot_hi(b1, c1, a1, s1);
+            yl[j] = r0 | (r1 << 16);
+            yh[j] = r2 | (r3 << 16);
+        }
+        uint16_t* dst = (is_q ? a.q_out : a.k_cache) + dst_off;
+        *reinterpret_cast<uint4*>(dst + i0) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
+        *reinterpret_cast<uint4*>(dst + i0 + half) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+        return;
     }
-    if (!slot_ok) return;
-    const int chunks = a.d / 8;  // 16-byte chunks per head vector
-    for (int idx = threadIdx.x; idx < a.Hkv * chunks; idx += blockDim.x) {
-        const int h = idx / chunks, c = idx - h * chunks;
-        const uint4 val = reinterpret_cast<const uint4*>(a.v + ((long long)b * a.Hkv + h) * a.d)[c];
-        reinterpret_cast<uint4*>(a.v_cache + ((blk * a.Hkv + h) * kBlock + off) * a.d)[c] = val;
-    }
+    const long long c = t - n_rot;
+    if (c >= n_cpy) return;
+    const int chunks = a.d / 8;
+    const int ch = (int)(c % chunks);
+    const long long bh = c / chunks;
+    const int h = (int)(bh % a.Hkv);
+    const int b = (int)(bh / a.Hkv);
+    const int p = a.positions[b];
+    const int slot = a.slot_mapping[b];
+    if (p < 0 || p >= a.max_pos || slot < 0 || slot >= a.num_blocks * kBlock) return;
+    const uint4 val = reinterpret_cast<const uint4*>(a.v + ((long long)b * a.Hkv + h) * a.d)[ch];
+    reinterpret_cast<uint4*>(a.v_cache + (((long long)(slot / kBlock) * a.Hkv + h) * kBlock + slot % kBlock) *
+                             a.d)[ch] = val;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -89,7 +154,9 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     if (D.B == 0) return MI_OK;
     if (!q || !k || !v || !positions || !slot_mapping || !rope_cos_sin || !q_out || !k_cache || !v_cache)
         return MI_ERR_INVALID_ARG;
-    if (!aligned16(v) || !aligned16(v_cache) || !aligned16(rope_cos_sin)) return MI_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(rope_cos_sin))
+        return MI_ERR_INVALID_ARG;
     AppendParams a;
     a.q = static_cast<const uint16_t*>(q);
     a.k = static_cast<const uint16_t*>(k);
@@ -106,6 +173,18 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     a.d = D.head_dim;
     a.num_blocks = D.num_blocks;
     a.max_pos = max_pos;
-    append_kernel<<<D.B, 256, 0, (cudaStream_t)stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+    const long long threads = (long long)D.B * (D.Hq + D.Hkv) * (D.head_dim / 16) +
+                              (long long)D.B * D.Hkv * (D.head_dim / 8);
+    // programmatic dependent launch: the kernel may be scheduled while the
+    // previous kernel in the stream drains, and waits for it before any load
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + 127) / 128));
+    cfg.blockDim = dim3(128);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, a, (int)D.B) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }

@@ -6,32 +6,42 @@
 // NJU course brief "端侧大模型推理框架" §2.1 (query head j reads KV head j / G).
 // The gather is never materialised: blocks are read in place.
 //
-// Work decomposition (split-KV, flash-decoding style, balanced):
+// Work decomposition (split-KV, flash-decoding style):
 //   * A "unit" is one (request b, KV head h) pair; it owns ceil(n_b / 16) KV
 //     blocks. Units are laid end to end in (b, h) order into one flat sequence
-//     of blocks, of total length TB.
-//   * A persistent grid of P CTAs cuts that sequence into P contiguous ranges
-//     of (almost) equal block counts, so every CTA streams the same number of
+//     of TB blocks.
+//   * A persistent grid (two CTAs per SM) cuts that sequence into equal
+//     contiguous ranges, one per CTA, so every CTA streams the same number of
 //     bytes however skewed the context lengths are.
-//   * Inside a CTA, warp w takes every W-th block of the range. Each warp owns
-//     a ring of S shared-memory stages fed by 2-D TMA tensor copies (128-byte
-//     swizzle) on its own mbarriers, so loads for later blocks are in flight
-//     while the current block is computed.
+//   * Warp specialisation: in each CTA one producer warp walks the block table
+//     and issues 2-D TMA tensor copies (128-byte swizzle, one 4 KB box per K
+//     or V tile) into a ring of shared-memory stages per consumer warp
+//     (full/empty mbarriers); consumer warp w takes blocks w, w+W, ... of the
+//     range. The producer never joins the consumers' barriers, so their merges
+//     do not interrupt the stream.
 //   * One 16-token K/V tile serves all G query heads of the KV head: scores
-//     are 16 tokens x G heads, with an fp32 online softmax (base-2 exponent,
-//     scale * log2(e) folded into one multiply).
-//   * At every unit boundary the warps merge their (max, sum, output) states in
-//     shared memory. A unit wholly inside the range is written as bf16 output;
-//     a unit cut by the range edge leaves a normalised fp32 partial and its
-//     log-sum-exp in the workspace, and the combine kernel merges the pieces.
-// The split plan depends only on the context lengths, so results are bitwise
-// independent of which physical blocks a request holds.
+//     are 16 tokens x G heads on tensor cores (or fp32 FMAs), with an fp32
+//     online softmax (base-2 exponent, scale * log2(e) folded into one
+//     multiply).
+//   * At every unit boundary the consumer warps merge their (max, sum, output)
+//     states in shared memory. A unit wholly inside the range is written as
+//     bf16 output; a unit cut by range edges leaves a normalised fp32 partial
+//     and its log-sum-exp per piece in the workspace, then bumps the unit's
+//     counter word (tagged with the call's epoch, so it never needs clearing);
+//     the CTA that stores the last piece merges the unit (log-sum-exp
+//     combine). Each CTA streams the cut unit at its range end first, so
+//     these merges happen early rather than at the end of the kernel.
+// The split depends only on the context lengths and the grid size, so results
+// are bitwise independent of which physical blocks a request holds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
+#include <random>
 
 #include "common.cuh"
 
@@ -46,9 +56,12 @@ struct AttnParams {
     const int32_t* block_tables;   // [B][mbps]
     const int32_t* context_lens;   // [B]
     uint16_t* out;                 // [B][Hq][HD]
-    float* part;                   // partial slots [P][2][slot_floats]
+    float* part;                   // partial slots [CTAs][2][slot_floats]
+    unsigned long long* unit_word; // [CTAs]: per cut unit (at its first piece's CTA): epoch | pieces stored
+    unsigned long long epoch;      // distinct per call
     int32_t* dev_err;
     int B, Hq, Hkv, G, num_blocks, mbps, stages, slot_floats;
+    int grid;                      // CTAs of the attention kernel
     float sl2;                     // scale * log2(e)
 };
 
@@ -84,10 +97,6 @@ struct Cursor {
     }
 };
 
-__device__ __forceinline__ long long range_start(long long TB, int P, int i) {
-    return (long long)(((unsigned long long)TB * (unsigned long long)i) / (unsigned long long)P);
-}
-
 // Block-wide exclusive scan of the per-thread values v (one per thread).
 // Writes scratch[tid] = sum of v over threads < tid and scratch[nt] = total.
 // `scratch` holds blockDim.x + 1 long longs plus 32 more for warp totals.
@@ -118,83 +127,96 @@ __device__ void block_exclusive_scan(long long v, long long* scratch) {
     __syncthreads();
 }
 
-// The plan, computed identically by every CTA of both kernels. Each thread
-// sums the unit lengths of a contiguous chunk of requests; the scan of those
-// sums gives the total number of flat blocks TB = Hkv * sum_b ceil(n_b / 16).
-struct Plan {
-    int b0, b1;      // this thread's request chunk
-    long long TB;
-};
-
-__device__ __forceinline__ Plan plan_scan(const AttnParams& p, long long* scratch) {
+// Each thread sums the unit lengths of a contiguous chunk of requests; after
+// the scan, scan[t] is the number of request blocks before chunk t and
+// scan[nt] their total. Returns TB = Hkv * total.
+__device__ __forceinline__ long long plan_scan(const AttnParams& p, long long* scan) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (p.B + nt - 1) / nt;
-    Plan pl;
-    pl.b0 = min(p.B, tid * per);
-    pl.b1 = min(p.B, pl.b0 + per);
+    const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     long long s = 0;
-    for (int b = pl.b0; b < pl.b1; ++b) s += unit_blocks(p, b);
-    block_exclusive_scan(s, scratch);
-    pl.TB = scratch[nt] * p.Hkv;
-    return pl;
+    for (int b = b0; b < b1; ++b) s += unit_blocks(p, b);
+    block_exclusive_scan(s, scan);
+    return scan[nt] * p.Hkv;
 }
 
-// Locate the unit holding flat block x (0 <= x < TB) after plan_scan: the
-// thread whose chunk spans x walks it. found = {b, h, unit start, unit length}.
-__device__ __forceinline__ void plan_find(const AttnParams& p, const Plan& pl, long long x,
-                                          const long long* scratch, long long* found) {
-    const int tid = threadIdx.x;
-    const long long lo = scratch[tid] * p.Hkv, hi = scratch[tid + 1] * p.Hkv;
-    if (x >= lo && x < hi) {
-        long long acc = scratch[tid];
-        for (int b = pl.b0; b < pl.b1; ++b) {
-            const int L = unit_blocks(p, b);
-            if (x < (acc + L) * p.Hkv) {
-                const int h = (int)((x - acc * p.Hkv) / L);
-                found[0] = b;
-                found[1] = h;
-                found[2] = acc * p.Hkv + (long long)h * L;
-                found[3] = L;
-                break;
-            }
-            acc += L;
-        }
+// The unit holding flat block x (0 <= x < TB), by one thread: binary search
+// of the chunk sums, then a walk through that chunk's requests.
+__device__ Cursor locate(const AttnParams& p, const long long* scan, int nt, long long x) {
+    int lo = 0, hi = nt;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (scan[mid] * p.Hkv <= x) lo = mid; else hi = mid;
     }
-    __syncthreads();
+    const int per = (p.B + nt - 1) / nt;
+    int b = lo * per;
+    long long acc = scan[lo];
+    int L = unit_blocks(p, b);
+    while (x >= (acc + L) * p.Hkv) {
+        acc += L;
+        L = unit_blocks(p, ++b);
+    }
+    Cursor c;
+    c.b = b;
+    c.len = L;
+    c.h = (int)((x - acc * p.Hkv) / L);
+    c.start = acc * p.Hkv + (long long)c.h * L;
+    return c;
 }
+
+// Range of CTA i of P over TB flat blocks.
+__device__ __forceinline__ long long range_start(long long TB, int P, int i) {
+    return (long long)(((unsigned long long)TB * (unsigned long long)i) / (unsigned long long)P);
+}
+
+// The CTA whose range holds flat block x (0 <= x < TB).
+__device__ __forceinline__ int cta_of(long long TB, int P, long long x) {
+    int c = (int)(((unsigned long long)x * (unsigned long long)P) / (unsigned long long)TB);
+    while (c > 0 && range_start(TB, P, c) > x) --c;
+    while (c + 1 < P && range_start(TB, P, c + 1) <= x) ++c;
+    return c;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------- smem layout ------
 
 template <int HD>
 struct Tile {
     static constexpr int kBytes = kBlock * HD * 2;  // one 16-token K or V tile
-    static constexpr int kHalves = HD / 64;         // 128-byte swizzle spans 64 bf16 columns
 };
 
-// Physical byte offset of 16-byte chunk `chunk` (0 .. HD/8-1) of row `row`
-// inside a tile written by the 128-byte-swizzled TMA copy: the tile is
-// [HD/64 halves][16 rows][128 bytes] and chunk c of a row sits at c ^ (row & 7).
+// Physical byte offset of 16-byte chunk `chunk` (0 .. HD/8-1) of token row
+// `row` inside a tile written by one 128-byte-swizzled TMA box. The cache is
+// viewed as 128-byte lines (HD/64 per token), so a 16-token tile is one
+// contiguous box of 16*HD/64 lines; chunk c of line l sits at c ^ (l & 7).
+template <int HD>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+    const int line = row * (HD / 64) + (chunk >> 3);
+    return (uint32_t)(line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
 }
 
 struct SmemPlan {
-    int tiles, bars, mbuf, lbuf, obuf, xbuf, scan, found, fac, total;
+    int tiles, full, empty, mbuf, lbuf, obuf, xbuf, scan, fac, flag, total;
 };
 
-__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G) {
+// W consumer warps plus one producer warp; S stages per consumer warp. The
+// weight-exchange buffer is only needed by the CUDA-core tile.
+__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma) {
     SmemPlan s;
     int off = 0;
     s.tiles = off; off += W * S * 2 * kBlock * HD * 2;
-    s.bars = off;  off += W * S * 8;
+    s.full = off;  off += W * S * 8;
+    s.empty = off; off += W * S * 8;
     s.mbuf = off;  off += W * kMaxG * 4;
     s.lbuf = off;  off += W * kMaxG * 4;
     s.fac = off;   off += (W + 3) * kMaxG * 4;
     s.obuf = off;  off += W * G * HD * 4;
-    s.xbuf = off;  off += W * (kBlock * kMaxG + kMaxG) * 4;
+    s.xbuf = off;  off += fma ? W * (kBlock * kMaxG + kMaxG) * 4 : 0;
     off = (off + 15) & ~15;
-    s.scan = off;  off += (W * 32 + 1 + 32) * 8;
-    s.found = off; off += 4 * 8;
+    s.scan = off;  off += ((W + 1) * 32 + 1 + 32) * 8;
+    s.flag = off;  off += 16;
     s.total = off + 1024;  // slack to align the tiles to 1024 bytes
     return s;
 }
@@ -236,7 +258,7 @@ struct MmaState {
 #pragma unroll
             for (int kk = 0; kk < kK; ++kk) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(kt + swz(tok, kk * 2 + csel), a0, a1, a2, a3);
+                ldsm_x4(kt + swz<HD>(tok, kk * 2 + csel), a0, a1, a2, a3);
                 mma_bf16_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
         }
@@ -261,12 +283,16 @@ struct MmaState {
         // the sums use the same bf16-rounded weights the PV product uses
         l[0] = l[0] * al0 + (bf16_lo(x0) + bf16_lo(x1));
         l[1] = l[1] * al1 + (bf16_hi(x0) + bf16_hi(x1));
+        // the running max rarely moves once a few blocks are in: skip the
+        // rescale when no lane's factor differs from 1
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-        for (int mt = 0; mt < kK; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int mt = 0; mt < kK; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
         }
         const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
         {
@@ -276,7 +302,7 @@ struct MmaState {
 #pragma unroll
             for (int mt = 0; mt < kK; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(vt + swz(tok, mt * 2 + csel), a0, a1, a2, a3);
+                ldsm_x4_trans(vt + swz<HD>(tok, mt * 2 + csel), a0, a1, a2, a3);
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
             }
         }
@@ -357,7 +383,7 @@ struct FmaState {
         for (int i = 0; i < TPL; ++i) {
             const int t = r + RG * i;
             uint32_t w0, w1, w2, w3;
-            lds128(kt + swz(t, c), w0, w1, w2, w3);
+            lds128(kt + swz<HD>(t, c), w0, w1, w2, w3);
             const float kf[8] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1),
                                  bf16_lo(w2), bf16_hi(w2), bf16_lo(w3), bf16_hi(w3)};
 #pragma unroll
@@ -414,7 +440,7 @@ struct FmaState {
             const int tt = r + RG * i;
             if (tt < valid) {
                 uint32_t w0, w1, w2, w3;
-                lds128(vt + swz(tt, c), w0, w1, w2, w3);
+                lds128(vt + swz<HD>(tt, c), w0, w1, w2, w3);
                 const float vf[8] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1),
                                      bf16_lo(w2), bf16_hi(w2), bf16_lo(w3), bf16_hi(w3)};
 #pragma unroll
@@ -456,6 +482,8 @@ struct FmaState {
     }
 };
 
+
+
 // ------------------------------------------------------ the main kernel ---
 
 enum { kVarMma = 1, kVarFma = 2 };
@@ -467,117 +495,153 @@ struct StateOf<HD, kVarMma, GP> { using T = MmaState<HD>; };
 template <int HD, int GP>
 struct StateOf<HD, kVarFma, GP> { using T = FmaState<HD, GP>; };
 
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// W consumer warps (compute, merge) and one producer warp (block-table walk
+// and TMA issue in lanes 0..W-1, zero rows for empty requests in the rest).
+// Consumers synchronise among themselves on named barrier 1.
 template <int HD, int VAR, int GP, int W>
-__global__ void __launch_bounds__(W * 32, 1)
+__global__ void __launch_bounds__((W + 1) * 32, 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
-    const SmemPlan sp = smem_plan(W, S, HD, p.G);
+    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma);
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t* base = smem_raw + pad;
     const uint32_t sbase = raw + pad;
+    long long* scan = reinterpret_cast<long long*>(base + sp.scan);
+    constexpr int kTile = Tile<HD>::kBytes;
+    const uint32_t full0 = sbase + sp.full, empty0 = sbase + sp.empty;
+
+    if (tid < W * S) {
+        mbar_init(full0 + tid * 8, 1);
+        mbar_init(empty0 + tid * 8, 1);
+    }
+    fence_mbar_init();
+    // Inputs may come from the kernel just before this one in the stream.
+    pdl_wait();
+    pdl_trigger();
+
+    const long long TB = plan_scan(p, scan);  // (ends with a barrier of all warps)
+    const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
+    const int cta = blockIdx.x;
+    const long long ra = cta < P ? range_start(TB, P, cta) : 0;
+    const long long rb = cta < P ? range_start(TB, P, cta + 1) : 0;
+    // The range's last unit, when it starts inside the range and continues
+    // past rb, is streamed first ("part 0" = [sl, rb), then "part 1" =
+    // [ra, sl)): both pieces of every cut unit are then written early and
+    // their merge does not land at the end of the kernel.
+    long long sl = rb;
+    if (rb > ra) {
+        const Cursor cl = locate(p, scan, blockDim.x, rb - 1);
+        if (cl.start > ra && cl.start + cl.len > rb) sl = cl.start;
+    }
+
+    if (warp == W) {
+        // ------------------------------------------------ producer warp --
+        if (lane >= W) {
+            // Rows of requests with no tokens are zero; CTA i owns b = i mod
+            // gridDim (these rows belong to no unit, so nobody else writes them).
+            const int nl = 32 - W;
+            for (int b = cta; b < p.B; b += gridDim.x) {
+                const int n = __ldg(p.context_lens + b);
+                if (n > p.mbps * kBlock && lane == W) raise_err(p.dev_err, MI_DEVERR_BAD_CONTEXT);
+                if (n <= 0) {
+                    uint4* row = reinterpret_cast<uint4*>(p.out + (long long)b * p.Hq * HD);
+                    for (int i = lane - W; i < p.Hq * HD / 8; i += nl) row[i] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            return;
+        }
+        // Lane w < W feeds consumer warp w: blocks ps + w, ps + w + W, ... of
+        // each part [ps, pe) of this CTA's range. For each it waits for a free
+        // stage of the warp's ring, looks the block up in the table and issues
+        // the two copies.
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t stg = 0, ph = 1;  // a fresh barrier reads as having completed the phase before 0
+        const uint32_t my_full = full0 + (uint32_t)(lane * S) * 8, my_empty = empty0 + (uint32_t)(lane * S) * 8;
+        const uint32_t my_tiles = sbase + sp.tiles + (uint32_t)(lane * S) * (2 * kTile);
+        for (int part = 0; part < 2; ++part) {
+        const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
+        long long x = ps + lane;
+        if (x >= pe) continue;
+        Cursor cu = locate(p, scan, blockDim.x, x);
+        for (; x < pe; x += W) {
+            if (!mbar_wait_bounded(my_empty + stg * 8, ph)) {
+                // the consumer stopped taking stages (it timed out itself)
+                raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+                return;
+            }
+            cu.advance_to(p, x);
+            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
+            const uint32_t bar = my_full + stg * 8;
+            if (blk < 0 || blk >= p.num_blocks) {
+                raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
+                mbar_arrive(bar);  // the consumer skips the block (it checks the table itself)
+            } else {
+                const uint32_t dst = my_tiles + stg * (2 * kTile);
+                mbar_arrive_expect_tx(bar, 2 * kTile);
+                const int y = ((blk * p.Hkv + cu.h) * kBlock) * (HD / 64);
+                tma_load_2d(dst, &tmk, bar, 0, y, policy);
+                tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
+            }
+            if (++stg == (uint32_t)S) {
+                stg = 0;
+                ph ^= 1u;
+            }
+        }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps --
+    if (cta >= P) return;
     float* mbuf = reinterpret_cast<float*>(base + sp.mbuf);
     float* lbuf = reinterpret_cast<float*>(base + sp.lbuf);
     float* fac = reinterpret_cast<float*>(base + sp.fac);
+    float* res = fac + W * kMaxG;  // rows: 1/L, M, L per head
     float* obuf = reinterpret_cast<float*>(base + sp.obuf);
     float* xbuf = reinterpret_cast<float*>(base + sp.xbuf) + warp * (kBlock * kMaxG + kMaxG);
-    long long* scan = reinterpret_cast<long long*>(base + sp.scan);
-    long long* found = reinterpret_cast<long long*>(base + sp.found);
-    constexpr int kTile = Tile<HD>::kBytes;
-    const uint32_t my_tiles = sbase + sp.tiles + (uint32_t)(warp * S * 2 * kTile);
-    const uint32_t my_bars = sbase + sp.bars + (uint32_t)(warp * S * 8);
-
-    // Rows of requests with no tokens are zero; CTA i owns b = i mod gridDim.
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        const int n = __ldg(p.context_lens + b);
-        if (n > p.mbps * kBlock && tid == 0) raise_err(p.dev_err, MI_DEVERR_BAD_CONTEXT);
-        if (n <= 0) {
-            uint4* row = reinterpret_cast<uint4*>(p.out + (long long)b * p.Hq * HD);
-            for (int i = tid; i < p.Hq * HD / 8; i += blockDim.x) row[i] = make_uint4(0, 0, 0, 0);
-        }
-    }
-
-    // The plan: total blocks, this CTA's range, the unit holding its start.
-    const Plan pl = plan_scan(p, scan);
-    const long long TB = pl.TB;
-    const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
-    if ((int)blockIdx.x >= P) return;
-    const long long ra = range_start(TB, P, blockIdx.x), rb = range_start(TB, P, blockIdx.x + 1);
-    plan_find(p, pl, ra, scan, found);
-    Cursor cu;
-    cu.b = (int)found[0];
-    cu.h = (int)found[1];
-    cu.start = found[2];
-    cu.len = (int)found[3];
-
-    if (tid < W * S) mbar_init(sbase + sp.bars + tid * 8, 1);
-    fence_mbar_init();
-    __syncthreads();
-
-    // Producer state (lane 0 of each warp): its own cursor over the unit sequence.
-    const long long nmine = (rb - ra > warp) ? (rb - ra - warp + W - 1) / W : 0;
-    Cursor pc = cu;
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](long long k) {
-        const long long x = ra + warp + k * W;
-        pc.advance_to(p, x);
-        const int j = (int)(x - pc.start);
-        const int blk = __ldg(p.block_tables + (long long)pc.b * p.mbps + j);
-        const uint32_t bar = my_bars + (uint32_t)((k % S) * 8);
-        if (blk < 0 || blk >= p.num_blocks) {
-            raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
-            mbar_arrive(bar);
-            return;
-        }
-        const uint32_t dst = my_tiles + (uint32_t)((k % S) * 2 * kTile);
-        mbar_arrive_expect_tx(bar, 2 * kTile);
-        const int y = (blk * p.Hkv + pc.h) * kBlock;
-#pragma unroll
-        for (int hf = 0; hf < Tile<HD>::kHalves; ++hf) {
-            tma_load_2d(dst + hf * 2048, &tmk, bar, hf * 64, y, policy);
-            tma_load_2d(dst + kTile + hf * 2048, &tmv, bar, hf * 64, y, policy);
-        }
-    };
-    if (lane == 0)
-        for (long long k = 0; k < nmine && k < S; ++k) issue(k);
-
+    const int nc = W * 32;
     using State = typename StateOf<HD, VAR, GP>::T;
     State st;
-    bool dead = false;     // a wait timed out: stop touching the pipeline
-    long long k = 0;       // blocks of this warp consumed so far
-    long long k_dead = 0;  // first block whose wait timed out
-    float* res = fac + W * kMaxG;  // rows: 1/L, M, L per head
+    bool dead = false;  // a wait timed out: stop touching the pipeline
+    uint32_t cstage = 0, cphase = 0;
 
-    while (cu.start < rb && cu.b < p.B) {
-        const long long sa = cu.start > ra ? cu.start : ra;
-        const long long se = (cu.start + cu.len) < rb ? (cu.start + cu.len) : rb;
+    for (int part = 0; part < 2; ++part) {
+    const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
+    if (ps >= pe) continue;
+    Cursor cu = locate(p, scan, blockDim.x, ps);
+    while (cu.start < pe && cu.b < p.B) {
+        const long long sa = cu.start > ps ? cu.start : ps;
+        const long long se = (cu.start + cu.len) < pe ? (cu.start + cu.len) : pe;
         const int nvalid = ctx_clamped(p, cu.b);
         st.begin_unit(p, cu.b, cu.h, lane);
-        long long x = sa + (((warp - (sa - ra)) % W) + W) % W;
+        long long x = sa + (((warp - (sa - ps)) % W) + W) % W;
         for (; x < se; x += W) {
-            const uint32_t stage = (uint32_t)(k % S);
-            const uint32_t par = (uint32_t)((k / S) & 1);
+            const uint32_t si = (uint32_t)(warp * S) + cstage;
             if (!dead) {
-                const bool ok = mbar_wait_bounded(my_bars + stage * 8, par);
-                if (__any_sync(0xffffffffu, !ok)) {
+                const bool okw = mbar_wait_bounded(full0 + si * 8, cphase);
+                if (__any_sync(0xffffffffu, !okw)) {
                     dead = true;
-                    k_dead = k;
                     if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                 }
             }
             const int j = (int)(x - cu.start);
-            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
             const int valid = min(kBlock, nvalid - j * kBlock);
+            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
             if (!dead && blk >= 0 && blk < p.num_blocks) {
-                const uint32_t kt = my_tiles + stage * 2 * kTile, vt = kt + kTile;
+                const uint32_t kt = sbase + sp.tiles + si * (2 * kTile), vt = kt + kTile;
                 if (VAR == kVarMma && valid < kBlock) {
                     // rows past the context may hold any bits: zero V there
                     for (int i = lane; i < (kBlock - valid) * (HD / 8); i += 32) {
                         const int row = valid + i / (HD / 8), ch = i % (HD / 8);
-                        st_shared_zero16(vt + swz(row, ch));
+                        st_shared_zero16(vt + swz<HD>(row, ch));
                     }
                     __syncwarp();
                 }
@@ -588,16 +652,20 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0 && !dead && k + S < nmine) {
+            if (lane == 0 && !dead) {
+                // this warp's reads of the stage are done: hand it back
                 fence_proxy_async_smem();
-                issue(k + S);
+                mbar_arrive(empty0 + si * 8);
             }
-            ++k;
+            if (++cstage == (uint32_t)S) {
+                cstage = 0;
+                cphase ^= 1u;
+            }
         }
-        // merge the warps' states for this unit (a warp without a block in it
-        // stores its initial state: max -inf, sum 0, output 0)
+        // merge the warps' states for this unit (a warp without a block in
+        // it stores its initial state: max -inf, sum 0, output 0)
         st.store(mbuf + warp * kMaxG, lbuf + warp * kMaxG, obuf + warp * p.G * HD, p.G, lane);
-        __syncthreads();
+        consumer_sync(nc);
         if (tid < p.G) {
             float M = kNegInf;
             for (int w = 0; w < W; ++w) M = fmaxf(M, mbuf[w * kMaxG + tid]);
@@ -611,11 +679,11 @@ __global__ void __launch_bounds__(W * 32, 1)
             res[kMaxG + tid] = M;
             res[2 * kMaxG + tid] = L;
         }
-        __syncthreads();
+        consumer_sync(nc);
         const bool whole = (sa == cu.start) && (se == cu.start + cu.len);
         const int slot = (sa == ra) ? 0 : 1;
-        float* part = p.part + ((long long)blockIdx.x * 2 + slot) * p.slot_floats;
-        for (int idx = tid; idx < p.G * HD; idx += blockDim.x) {
+        float* part = p.part + ((long long)cta * 2 + slot) * p.slot_floats;
+        for (int idx = tid; idx < p.G * HD; idx += nc) {
             const int g = idx / HD, dcol = idx - g * HD;
             float acc = 0.f;
             for (int w = 0; w < W; ++w) {
@@ -633,61 +701,93 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
             }
         }
-        __syncthreads();
-        cu.next(p);
-    }
-    // After a timed-out wait, let the copies this warp still has in flight
-    // land (each wait bounded again) before the CTA's shared memory goes away.
-    if (dead) {
-        for (long long kk = k_dead; kk < k_dead + S && kk < nmine; ++kk)
-            (void)mbar_wait_bounded(my_bars + (uint32_t)((kk % S) * 8), (uint32_t)((kk / S) & 1));
-    }
-}
-
-// Merge the partials of every unit that a range boundary cut. Boundary i
-// (between CTA i-1 and CTA i) handles the unit holding flat block ra(i) when
-// this is the unit's first cut.
-template <int HD>
-__global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
-    __shared__ long long scan[256 + 1 + 32];
-    __shared__ long long found[4];
-    const Plan pl = plan_scan(p, scan);
-    const long long TB = pl.TB;
-    const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
-    const int i = blockIdx.x;
-    if (i == 0 || i >= P) return;
-    const long long x = range_start(TB, P, i);
-    plan_find(p, pl, x, scan, found);
-    const int b = (int)found[0], h = (int)found[1];
-    const long long us = found[2];
-    const int len = (int)found[3];
-    if (us == x) return;                              // not cut here
-    const long long prev = range_start(TB, P, i - 1);
-    if (us < prev) return;                            // cut earlier; handled there
-    const long long ue = us + len;                    // unit end
-    int last = i;
-    while (last + 1 < P && range_start(TB, P, last + 1) < ue) ++last;
-    const int first_slot = (us == prev) ? 0 : 1;
-    const int G = p.G;
-    for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
-        const int g = idx / HD;
-        float M = kNegInf;
-        for (int c = i - 1; c <= last; ++c) {
-            const int s = (c == i - 1) ? first_slot : 0;
-            M = fmaxf(M, p.part[((long long)c * 2 + s) * p.slot_floats + G * HD + g]);
-        }
-        float num = 0.f, den = 0.f;
-        if (M != kNegInf) {
-            for (int c = i - 1; c <= last; ++c) {
-                const int s = (c == i - 1) ? first_slot : 0;
-                const float* sl = p.part + ((long long)c * 2 + s) * p.slot_floats;
-                const float wgt = exp2f(sl[G * HD + g] - M);
-                num += wgt * sl[idx];
-                den += wgt;
+        if (!whole) {
+            // pieces of this unit: CTAs cf..cl; the first one's slot is 1 when
+            // the unit starts inside its range, every other piece is slot 0
+            const int cf = cta_of(TB, P, cu.start), cl = cta_of(TB, P, cu.start + cu.len - 1);
+            const int fs = (cu.start == range_start(TB, P, cf)) ? 0 : 1;
+            const int ns = cl - cf + 1;
+            volatile int* mflag = reinterpret_cast<volatile int*>(base + sp.flag);
+            consumer_sync(nc);  // this CTA's partial is stored
+            if (tid == 0) {
+                // one counter word per cut unit, at its first piece's CTA:
+                // high 48 bits = the call's epoch, low 16 = pieces stored. A
+                // word from another call counts as zero, so nothing needs
+                // clearing. acq_rel: this CTA's partial is published before
+                // the count, the others' partials are visible after it.
+                unsigned long long* wd = p.unit_word + cf;
+                const unsigned long long e48 = p.epoch & 0xFFFFFFFFFFFFull;
+                unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(wd), nw, got;
+                for (;;) {
+                    nw = ((old >> 16) == e48) ? old + 1 : ((e48 << 16) | 1ull);
+                    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                                 : "=l"(got) : "l"(wd), "l"(old), "l"(nw) : "memory");
+                    if (got == old) break;
+                    old = got;
+                }
+                *mflag = (int)(nw & 0xFFFFull) == ns;
+            }
+            consumer_sync(nc);
+            if (*mflag) {
+                // M = max lse, out = sum 2^(lse-M) o / sum 2^(lse-M), pieces in order
+                auto slot_of = [&](int c) {
+                    return p.part + ((long long)c * 2 + (c == cf ? fs : 0)) * p.slot_floats;
+                };
+                if (ns <= W * HD) {
+                    float* wts = obuf;  // [ns][G] log-sum-exps, then weights
+                    for (int i = tid; i < ns * p.G; i += nc)
+                        wts[i] = __ldcg(slot_of(cf + i / p.G) + p.G * HD + i % p.G);
+                    consumer_sync(nc);
+                    if (tid < p.G) {
+                        float M = kNegInf;
+                        for (int c = 0; c < ns; ++c) M = fmaxf(M, wts[c * p.G + tid]);
+                        float den = 0.f;
+                        for (int c = 0; c < ns; ++c) {
+                            const float wgt = M == kNegInf ? 0.f : exp2f(wts[c * p.G + tid] - M);
+                            wts[c * p.G + tid] = wgt;
+                            den += wgt;
+                        }
+                        res[tid] = den > 0.f ? 1.f / den : 0.f;
+                    }
+                    consumer_sync(nc);
+                    for (int idx = tid; idx < p.G * HD; idx += nc) {
+                        const int g = idx / HD;
+                        float num = 0.f;
+#pragma unroll 4
+                        for (int c = 0; c < ns; ++c) num += wts[c * p.G + g] * __ldcg(slot_of(cf + c) + idx);
+                        p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + (idx - g * HD)] =
+                            f32_to_bf16(num * res[g]);
+                    }
+                } else {
+                    // more pieces than the weight buffer holds: two passes per output
+                    for (int idx = tid; idx < p.G * HD; idx += nc) {
+                        const int g = idx / HD;
+                        float M = kNegInf;
+                        for (int c = cf; c <= cl; ++c) M = fmaxf(M, __ldcg(slot_of(c) + p.G * HD + g));
+                        float num = 0.f, den = 0.f;
+                        if (M != kNegInf)
+                            for (int c = cf; c <= cl; ++c) {
+                                const float wgt = exp2f(__ldcg(slot_of(c) + p.G * HD + g) - M);
+                                num += wgt * __ldcg(slot_of(c) + idx);
+                                den += wgt;
+                            }
+                        p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + (idx - g * HD)] =
+                            f32_to_bf16(den > 0.f ? num / den : 0.f);
+                    }
+                }
             }
         }
-        const float v = den > 0.f ? num / den : 0.f;
-        p.out[((long long)b * p.Hq + (long long)h * G + g) * HD + (idx - g * HD)] = f32_to_bf16(v);
+        consumer_sync(nc);
+        cu.next(p);
+    }
+    }
+    // After a timed-out wait, let the copies still in flight for this warp's
+    // stages land (each wait bounded again) before shared memory goes away.
+    if (dead && lane == 0) {
+        for (int s2 = 0; s2 < S; ++s2) {
+            const uint32_t si = (uint32_t)(warp * S) + (uint32_t)s2;
+            (void)mbar_wait_bounded(full0 + si * 8, s2 < (int)cstage ? cphase ^ 1u : cphase);
+        }
     }
 }
 
@@ -707,12 +807,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// 2-D map over a cache viewed as 128-byte lines: [rows * HD/64][64] bf16,
+// box = one 16-token tile (16 * HD/64 lines x 64 columns), 128-byte swizzle.
 bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)HD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)HD * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows * (HD / 64)};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, (cuuint32_t)(kBlock * HD / 64)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -720,13 +822,18 @@ bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) {
     return r == CUDA_SUCCESS;
 }
 
-constexpr int kWarps = 8;
-constexpr int kMaxStages = 4;
-constexpr int kSmemLimit = 227 * 1024;
+constexpr int kWarps = 4;                 // consumer warps; one producer warp more
+constexpr int kMaxStages = 3;
+constexpr int kSmemLimit = 227 * 1024;    // per CTA
+constexpr int kSmemTwoPerSm = 115712;     // per CTA so that two fit in an SM's 228 KB
 
-int pick_stages(int HD, int G) {
+// Stages per consumer warp: as many as fit with two CTAs per SM, else (very
+// wide GQA groups) as many as fit one CTA.
+int pick_stages(int HD, int G, bool fma) {
     for (int S = kMaxStages; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G).total <= kSmemLimit) return S;
+        if (smem_plan(kWarps, S, HD, G, fma).total <= kSmemTwoPerSm) return S;
+    for (int S = kMaxStages; S >= 1; --S)
+        if (smem_plan(kWarps, S, HD, G, fma).total <= kSmemLimit) return S;
     return 0;
 }
 
@@ -775,7 +882,7 @@ int grid_for(KernelFn fn, int smem) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), kWarps * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), (kWarps + 1) * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const int g = sms * (occ > 0 ? occ : 1);
@@ -804,19 +911,59 @@ int slot_floats(const mi_dims& D) { return (D.Hq / D.Hkv) * D.head_dim + 8; }
 
 int max_grid(const mi_dims& D) {
     const int G = D.Hq / D.Hkv;
-    const int S = pick_stages(D.head_dim, G);
-    if (!S) return 0;
-    const int smem = smem_plan(kWarps, S, D.head_dim, G).total;
     int g = 0;
     for (int var : {kVarMma, kVarFma}) {
-        const int n = grid_for(pick_kernel(D.head_dim, var, G), smem);
+        const bool fma = var == kVarFma;
+        const int S = pick_stages(D.head_dim, G, fma);
+        if (!S) return 0;
+        const int n = grid_for(pick_kernel(D.head_dim, var, G), smem_plan(kWarps, S, D.head_dim, G, fma).total);
         if (n <= 0) return 0;
         g = n > g ? n : g;
     }
     return g;
 }
 
+// Workspace: [unit counter words, one per CTA | partial slots, two per CTA].
+// The words carry the epoch of the call that wrote them, so nothing needs
+// clearing between calls.
+size_t word_bytes(int grid) { return (((size_t)grid * 8) + 255) / 256 * 256; }
+
+size_t workspace_for(const mi_dims& D, int grid) {
+    return word_bytes(grid) + (size_t)grid * 2 * (size_t)slot_floats(D) * sizeof(float);
+}
+
+// A distinct value per call (in this process): a random start, then a
+// counter, so a word left by earlier work in the buffer is never mistaken for
+// this call's (the kernel compares the low 48 bits).
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> ctr{0};
+    static const unsigned long long start = [] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd() ^
+               (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+    }();
+    return start + 2 * ctr.fetch_add(1) + 1;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel in the stream finishes, and waits for it
+// (griddepcontrol.wait) before touching memory that kernel may write.
+template <typename... Args>
+cudaError_t launch_pdl(void (*fn)(Args...), int grid, int block, int smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
 
 }  // namespace
 }  // namespace mi
@@ -826,7 +973,7 @@ extern "C" size_t mi_paged_decode_workspace_bytes(const mi_dims* dims) {
     if (check_dims(dims) != MI_OK) return 0;
     const int g = max_grid(*dims);
     if (g <= 0) return 0;
-    return (size_t)g * 2 * (size_t)slot_floats(*dims) * sizeof(float);
+    return workspace_for(*dims, g);
 }
 
 extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
@@ -848,16 +995,15 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
         !aligned16(workspace))
         return MI_ERR_INVALID_ARG;
     if (ctas < 0 || !std::isfinite(scale)) return MI_ERR_INVALID_ARG;
-    const int var = variant == MI_ATTN_FMA ? kVarFma : kVarMma;
     if (variant != MI_ATTN_DEFAULT && variant != MI_ATTN_MMA && variant != MI_ATTN_FMA)
         return MI_ERR_INVALID_ARG;
+    const int var = variant == MI_ATTN_FMA ? kVarFma : kVarMma;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
-    const int S = pick_stages(HD, G);
-    const int smem = smem_plan(kWarps, S, HD, G).total;
+    const int S = pick_stages(HD, G, var == kVarFma);
+    const int smem = smem_plan(kWarps, S, HD, G, var == kVarFma).total;
     const int gmax = max_grid(D);
     if (gmax <= 0) return MI_ERR_CUDA;
-    const size_t need = (size_t)gmax * 2 * (size_t)slot_floats(D) * sizeof(float);
-    if (workspace_bytes < need) return MI_ERR_INVALID_ARG;
+    if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
     const int grid = ctas > 0 && ctas < gmax ? ctas : gmax;
 
     CUtensorMap tk, tv;
@@ -869,7 +1015,9 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = static_cast<uint16_t*>(out);
-    p.part = static_cast<float*>(workspace);
+    p.unit_word = static_cast<unsigned long long*>(workspace);
+    p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + word_bytes(gmax));
+    p.epoch = next_epoch();
     p.dev_err = dev_err;
     p.B = D.B;
     p.Hq = D.Hq;
@@ -879,17 +1027,12 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
     p.mbps = D.max_blocks_per_seq;
     p.stages = S;
     p.slot_floats = slot_floats(D);
+    p.grid = grid;
     p.sl2 = scale * 1.4426950408889634f;
 
-    KernelFn fn = pick_kernel(HD, var, G);
     cudaStream_t s = (cudaStream_t)stream;
-    fn<<<grid, kWarps * 32, smem, s>>>(tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) return MI_ERR_CUDA;
-    if (HD == 64)
-        combine_kernel<64><<<grid, 256, 0, s>>>(p);
-    else
-        combine_kernel<128><<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+    KernelFn fn = pick_kernel(HD, var, G);
+    return launch_pdl(fn, grid, (kWarps + 1) * 32, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }
 
 extern "C" mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,

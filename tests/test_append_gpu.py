@@ -148,3 +148,43 @@ def test_append_bad_slot_and_position_flagged(cuda_device):
     kc_ref = kc.copy()
     kc_ref[0, :, 5] = oracle.rope_rotate(k[0], oracle.rope_table(1e6, dd, 8), 1)
     assert np.array_equal(from_dev_u16(kc_d), kc_ref)
+
+
+def test_append_bit_exact_on_extreme_values(cuda_device):
+    """Finite bf16 inputs over the whole exponent range (subnormals, signed
+    zeros, values near the largest finite bf16, pairs that nearly cancel)
+    rotate to the oracle's bits."""
+    import torch
+    mi = _mi()
+    r = np.random.Generator(np.random.PCG64(77))
+    B, Hq, Hkv, dd, nb, max_pos = 16, 8, 2, 128, 4, 4096
+    n = B * (Hq + 2 * Hkv) * dd
+    sign = r.integers(0, 2, n).astype(np.uint16) << 15
+    expo = r.integers(0, 255, n).astype(np.uint16)      # 0 = zero/subnormal, 254 = largest finite binade
+    mant = r.integers(0, 128, n).astype(np.uint16)
+    bits = (sign | (expo << 7) | mant).astype(np.uint16)
+    bits[: n // 8] &= 0x807F                              # a block of subnormals and signed zeros
+    q = bits[: B * Hq * dd].reshape(B, Hq, dd).copy()
+    k = bits[B * Hq * dd: B * (Hq + Hkv) * dd].reshape(B, Hkv, dd).copy()
+    v = bits[B * (Hq + Hkv) * dd:].reshape(B, Hkv, dd).copy()
+    k[0, 0, : dd // 2] = k[0, 0, dd // 2:]                # x1 == x2: the rotation nearly cancels
+    pos = r.integers(0, max_pos, B).astype(np.int32)
+    slots = (r.permutation(nb * 16)[:B]).astype(np.int32)
+    st, table = mi.mi_rope_table(1e6, dd, max_pos)
+    assert st == 0
+    kc = np.full((nb, Hkv, 16, dd), 0x7FA5, np.uint16)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(kc, cuda_device)
+    qo_d = torch.empty((B, Hq, dd), dtype=torch.bfloat16, device=cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    d = mi.dims(B, Hq, Hkv, dd, nb, 1)
+    assert mi.mi_paged_kv_append(d, to_dev_u16(q, cuda_device), to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                 to_dev_i32(pos, cuda_device), to_dev_i32(slots, cuda_device),
+                                 torch.from_numpy(table).to(cuda_device), max_pos, qo_d, kc_d, vc_d, err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kc_ref, vc_ref = kc.copy(), kc.copy()
+    q_ref, st = oracle.append(q, k, v, pos, slots, oracle.rope_table(1e6, dd, max_pos), kc_ref, vc_ref)
+    assert st == 0
+    assert np.array_equal(from_dev_u16(qo_d), q_ref)
+    assert np.array_equal(from_dev_u16(kc_d), kc_ref)
+    assert np.array_equal(from_dev_u16(vc_d), vc_ref)

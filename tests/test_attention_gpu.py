@@ -292,3 +292,4 @@ def test_workspace_too_small_is_rejected(cuda_device):
     z = torch.zeros(16, dtype=torch.int32, device=cuda_device)
     st = mi.mi_paged_decode_attention(d, z, z, z, z, z, 1.0, z, ws, workspace_bytes=n - 16)
     assert st == mi.MI_ERR_INVALID_ARG
+
