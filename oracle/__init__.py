@@ -6,7 +6,7 @@ not import, link or execute anything under ``oracle/``, and nothing here imports
 the product package.
 
 ``oracle.c`` holds the arithmetic (bf16 conversion, RoPE table and rotation,
-append, paged and contiguous attention); this module compiles it with gcc into
+append, paged decode, causal paged prefill and contiguous attention); this module compiles it with gcc into
 ``oracle/_build/liboracle.so`` and wraps it with ctypes over numpy arrays.
 ``pool.py`` is a plain-Python model of the block pool. Sources of each function
 are cited in ``oracle.c`` and ``pool.py``.
@@ -62,6 +62,8 @@ def _load():
             lib.or_paged_attention.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, f64, P, i32]
             lib.or_paged_attention.restype = i32
             lib.or_contiguous_attention.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, f64, P]
+            lib.or_paged_prefill_attention.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, f64, P, i32]
+            lib.or_paged_prefill_attention.restype = i32
             _lib = lib
     return _lib
 
@@ -167,4 +169,20 @@ def contiguous_attention(q, K, V, lens, scale):
     out = np.empty((B, Hq, d), np.float64)
     _load().or_contiguous_attention(B, Hq, Hkv, d, n_max, _p(q), _p(K), _p(V), _p(ln), float(scale),
                                     _p(out))
+    return out
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, nthreads=1):
+    """Causal attention of each request's new tokens (rows query_start[r] ..
+    query_start[r+1]-1 of q uint16 [T][Hq][d]); returns float64 [T][Hq][d]."""
+    q = _c(q, np.uint16)
+    T, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    kc = _c(k_cache, np.uint16); vc = _c(v_cache, np.uint16)
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32); qs = _c(query_start, np.int32)
+    R = cl.shape[0]
+    assert qs.shape == (R + 1,) and qs[R] == T
+    out = np.empty((T, Hq, d), np.float64)
+    _load().or_paged_prefill_attention(R, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), _p(qs),
+                                       float(scale), _p(out), int(nthreads))
     return out

@@ -310,3 +310,100 @@ void or_contiguous_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int3
     }
     free(w);
 }
+
+/* ------------------------------------------------------ prefill attention -- */
+
+typedef struct {
+    int32_t R, Hq, Hkv, d, max_blocks_per_seq;
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start;
+    double scale;
+    double* out;
+    int64_t row_begin, row_end; /* rows are (query token, head) pairs */
+} or_prefill_job;
+
+/* Query token qi (a row of q) of request r is the token at position
+ * p = n_r - m_r + i (its i-th new token, n_r = context_lens[r] counting the new
+ * tokens, m_r = query_start[r+1] - query_start[r]); it attends causally to the
+ * cached tokens t <= p (prefill / chunked prefill of the course brief's
+ * prefill + decode loop, §2.1, over mini-infer's paged cache, "项目概述"). */
+static void prefill_row(const or_prefill_job* a, int32_t qi, int32_t j, double* s) {
+    const int32_t d = a->d, G = a->Hq / a->Hkv, h = j / G;
+    double* o = a->out + ((int64_t)qi * a->Hq + j) * d;
+    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+    int32_t r = 0;
+    while (r < a->R && a->query_start[r + 1] <= qi) ++r;
+    if (r >= a->R) return;
+    const int32_t m = a->query_start[r + 1] - a->query_start[r];
+    const int32_t n = a->context_lens[r];
+    const int32_t pos = n - m + (qi - a->query_start[r]);
+    if (pos < 0) return;
+    const uint16_t* qr = a->q + ((int64_t)qi * a->Hq + j) * d;
+    double mx = -INFINITY;
+    for (int32_t t = 0; t <= pos; ++t) {
+        const int64_t blk = a->block_tables[(int64_t)r * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint16_t* kt = a->k_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        double acc = 0.0;
+        for (int32_t i = 0; i < d; ++i) acc += or_double_from_bf16(qr[i]) * or_double_from_bf16(kt[i]);
+        s[t] = a->scale * acc;
+        if (s[t] > mx) mx = s[t];
+    }
+    double l = 0.0;
+    for (int32_t t = 0; t <= pos; ++t) {
+        const double w = exp(s[t] - mx);
+        l += w;
+        const int64_t blk = a->block_tables[(int64_t)r * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint16_t* vt = a->v_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        for (int32_t i = 0; i < d; ++i) o[i] += w * or_double_from_bf16(vt[i]);
+    }
+    for (int32_t i = 0; i < d; ++i) o[i] /= l;
+}
+
+static void* prefill_worker(void* arg) {
+    const or_prefill_job* a = (const or_prefill_job*)arg;
+    int32_t nmax = 1;
+    for (int32_t r = 0; r < a->R; ++r)
+        if (a->context_lens[r] > nmax) nmax = a->context_lens[r];
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    for (int64_t row = a->row_begin; row < a->row_end; ++row)
+        prefill_row(a, (int32_t)(row / a->Hq), (int32_t)(row % a->Hq), s);
+    free(s);
+    return NULL;
+}
+
+/* Causal paged attention for T = query_start[R] new tokens; out is double
+ * [T][Hq][d]. Rows are independent; nthreads > 1 runs contiguous row ranges on
+ * POSIX threads without changing any row's arithmetic. Returns threads used. */
+int32_t or_paged_prefill_attention(int32_t R, int32_t Hq, int32_t Hkv, int32_t d, const uint16_t* q,
+                                   const uint16_t* k_cache, const uint16_t* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start,
+                                   double scale, double* out, int32_t nthreads) {
+    const int64_t rows = (int64_t)query_start[R] * Hq;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = (int32_t)(rows > 0 ? rows : 1);
+    or_prefill_job* jobs = (or_prefill_job*)malloc(sizeof(or_prefill_job) * (size_t)nthreads);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int32_t t = 0; t < nthreads; ++t) {
+        or_prefill_job* a = &jobs[t];
+        a->R = R; a->Hq = Hq; a->Hkv = Hkv; a->d = d; a->max_blocks_per_seq = max_blocks_per_seq;
+        a->q = q; a->k_cache = k_cache; a->v_cache = v_cache;
+        a->block_tables = block_tables; a->context_lens = context_lens; a->query_start = query_start;
+        a->scale = scale; a->out = out;
+        a->row_begin = rows * t / nthreads;
+        a->row_end = rows * (t + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        prefill_worker(&jobs[0]);
+    } else {
+        for (int32_t t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, prefill_worker, &jobs[t]);
+        for (int32_t t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    free(th);
+    free(jobs);
+    return nthreads;
+}

@@ -81,3 +81,8 @@ class PoolModel:
             if n > 0:
                 sl[i] = t[(n - 1) // BLOCK] * BLOCK + (n - 1) % BLOCK
         return bt, cl, sl
+
+    def token_slots(self, seq, first, count):
+        """Slots of tokens first .. first+count-1 of a sequence (must be held)."""
+        t = self.tables[seq]
+        return np.array([t[(i) // BLOCK] * BLOCK + i % BLOCK for i in range(first, first + count)], np.int32)
