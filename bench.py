@@ -37,10 +37,12 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import (BLOCK, WORKLOADS, context_lengths, device_fill_cache, history_cache,  # noqa: E402
-                       initial_free_order, new_token_values, setup_pool)
+from workloads import (BLOCK, PREFILL_WORKLOADS, WORKLOADS, context_lengths, device_fill_cache,  # noqa: E402
+                       history_cache, initial_free_order, new_token_values, prefill_new_values,
+                       prefill_setup_pool, setup_pool)
 
 METRIC = "paged decode-attention KV GB/s"
+PREFILL_METRIC = "paged prefill-attention TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -71,17 +73,28 @@ def describe(w):
             "parallelism": "replicas"}
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs"):
+    fallback = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback[key], "fallback"
+
+
+def prefill_flops(w, hist, new):
+    """Algorithmic FLOPs of one prefill attention call: new token i of request
+    r at position hist[r] + i attends to hist[r] + i + 1 keys; per key and query
+    head, 2*d for q.k and 2*d for p*v."""
+    h = np.asarray(hist, np.float64)
+    m = np.asarray(new, np.float64)
+    keys = float(np.sum(m * h + m * (m + 1) / 2))
+    return 4.0 * w.head_dim * w.Hq * keys
 
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh"):
+    for f in ("decode.cu", "common.cuh", "tma.cuh"):
         with open(os.path.join(ROOT, "paged_kv_decode_25_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -197,6 +210,46 @@ def time_oracle(w, budget_s=12.0):
             "s_per_layer": dt}
 
 
+def prefill_oracle_sample(w, nthreads, rows_per_request=2):
+    """Host inputs for a bounded sample of one prefill layer (the first and a
+    random new token of every request, each as a one-token request over its
+    causal prefix) and a callable running the oracle's chunked append of all
+    new tokens plus causal attention of the sampled rows (test infrastructure
+    only). Returns (run, flops of the sampled rows)."""
+    import oracle
+    from oracle.pool import PoolModel
+    model = PoolModel(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, None)
+    prefill_setup_pool(w, model)
+    bt, _, _ = model.batch_meta(range(w.B))
+    h, m = w.lengths()
+    kc, vc = history_cache(w, 0, bt, h)
+    q, k, v = prefill_new_values(w, 0)
+    table = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    pos = np.concatenate([np.arange(h[r], h[r] + m[r]) for r in range(w.B)]).astype(np.int32)
+    slots = np.concatenate([model.token_slots(r, int(h[r]), int(m[r])) for r in range(w.B)])
+    qs = np.concatenate([[0], np.cumsum(m)]).astype(np.int64)
+    rng = np.random.Generator(np.random.PCG64(5))
+    rows, lens, tabs = [], [], []
+    for r in range(w.B):
+        for i in [0] + [int(rng.integers(0, m[r])) for _ in range(rows_per_request - 1)]:
+            rows.append(int(qs[r]) + i)
+            lens.append(int(h[r]) + i + 1)
+            tabs.append(bt[r])
+    rows = np.array(rows)
+    lens = np.array(lens, np.int32)
+    tabs = np.stack(tabs)
+    qs1 = np.arange(len(rows) + 1, dtype=np.int32)
+    flops = 4.0 * w.head_dim * w.Hq * float(lens.sum())
+
+    def run():
+        # the append writes the same values to the same slots on every call
+        q_out, _ = oracle.append(q, k, v, pos, slots, table, kc, vc)
+        oracle.paged_prefill_attention(q_out[rows], kc, vc, tabs, lens, qs1, w.scale, nthreads=nthreads)
+        return nthreads
+
+    return run, flops, len(rows)
+
+
 # ------------------------------------------------------------ reference ----
 
 def run_reference(args, w, rank, world):
@@ -221,6 +274,181 @@ def run_reference(args, w, rank, world):
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
+
+
+def run_prefill(args, w, rank, world):
+    """Prefill step: for each layer, the chunked append of every new token
+    (RoPE, scatter through mi_kv_pool_token_slots slots) and the causal paged
+    prefill attention. Prints one JSON line on rank 0."""
+    import dataclasses
+    layers = args.layers if args.layers is not None else 36
+    w = dataclasses.replace(w, layers=layers)
+    h, m = w.lengths()
+    n = (h + m).astype(np.int32)
+    R, T = w.B, int(m.sum())
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run, flops, nrows = prefill_oracle_sample(w, os.cpu_count() or 1)
+        for _ in range(args.warmup):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            used = run()
+        dt = (time.perf_counter() - t0) / args.steps
+        val = flops / dt / 1e12
+        cores = min(int(used), nrows * w.Hq)
+        sample = f"append of all {T} new tokens + causal attention of {nrows} sampled new tokens, one layer"
+        print(json.dumps({
+            "impl": "reference", "metric": PREFILL_METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "requests": R, "new_tokens": T, "Hq": w.Hq, "Hkv": w.Hkv,
+                       "head_dim": w.head_dim, "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
+
+    import torch
+    import paged_kv_decode_25_gb300 as mi
+    mi.load()
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    pool = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, None)
+    prefill_setup_pool(w, pool)
+    bt, _, _ = pool.batch_meta(range(R))
+    slots = np.concatenate([pool.token_slots(r, int(h[r]), int(m[r])) for r in range(R)]).astype(np.int32)
+    pos = np.concatenate([np.arange(h[r], h[r] + m[r]) for r in range(R)]).astype(np.int32)
+    qs = np.concatenate([[0], np.cumsum(m)]).astype(np.int32)
+    d_app = mi.dims(T, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    d_att = mi.dims(R, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    caches = []
+    for layer in range(layers):
+        kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        vc = torch.empty_like(kc)
+        device_fill_cache(w, layer + 1000 * rank, kc, vc)
+        caches.append((kc, vc))
+    st, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    mi.check(st, "rope table")
+    rope = torch.from_numpy(table).to(device)
+
+    def u16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    q_h, k_h, v_h = (u16(a) for a in prefill_new_values(w, 0))  # one set of new-token values, every layer
+    q_d, k_d, v_d = q_h.to(device), k_h.to(device), v_h.to(device)
+    qo_d, out_d = torch.empty_like(q_d), torch.empty_like(q_d)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
+    bt_d, n_d, qs_d, sl_d, pos_d = i32(bt), i32(n), i32(qs), i32(slots), i32(pos)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    max_q = int(m.max())
+
+    def step(ev=None):
+        for layer in range(layers):
+            kc, vc = caches[layer]
+            mi.check(mi.mi_paged_kv_append(d_app, q_d, k_d, v_d, pos_d, sl_d, rope, w.max_pos, qo_d, kc, vc,
+                                           err, stream), "append")
+            if ev is not None:
+                ev[layer][0].record(stream)
+            mi.check(mi.mi_paged_prefill_attention(d_att, T, max_q, qo_d, kc, vc, bt_d, n_d, qs_d, w.scale,
+                                                   out_d, err, stream), "prefill attention")
+            if ev is not None:
+                ev[layer][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s_ in range(args.steps):
+        step(evs[s_])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    step_ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, device)
+    attn_ms = [evs[s_][l_][0].elapsed_time(evs[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    fl = prefill_flops(w, h, m)
+    value = world * layers * fl / (step_ms * 1e-3) / 1e12
+    peak, peak_kind = measured_peak("bf16_tflops_sustained")
+    achieved = fl / (attn_avg_ms * 1e-3) / 1e12
+
+    # end to end: new-token values and metadata from pinned host memory, outputs back
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 10))
+    pin = lambda t: t.clone().pin_memory()  # noqa: E731
+    hq, hk, hv = pin(q_h), pin(k_h), pin(v_h)
+    meta = [(pin(torch.from_numpy(np.ascontiguousarray(a, np.int32))), dst)
+            for a, dst in ((bt, bt_d), (n, n_d), (qs, qs_d), (slots, sl_d), (pos, pos_d))]
+    h_out = torch.empty(out_d.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for src, dst in meta + [(hq, q_d), (hk, k_d), (hv, v_d)]:
+            dst.copy_(src, non_blocking=True)
+        step()
+        h_out.copy_(out_d, non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t, _ in meta) + sum(
+        t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = h_out.numel() * h_out.element_size()
+    if rank != 0:
+        barrier(world)
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        run, flops, nrows = prefill_oracle_sample(w, os.cpu_count() or 1)
+        t0 = time.perf_counter()
+        run()
+        reps = 1
+        while time.perf_counter() - t0 < 12.0 and reps < 20:
+            run()
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": min(os.cpu_count() or 1, nrows * w.Hq),
+               "kind": "oracle",
+               "sample": f"append of all {T} new tokens + causal attention of {nrows} sampled new tokens "
+                         f"(one layer), fp64 C, repeated {reps}x; seconds per sample {dt:.3f}"}
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": layers, "requests": R, "new_tokens": T,
+                   "history": "8 fresh prompts U[512, 2048]; 8 chunks of 512 over log-uniform [1024, 8192]",
+                   "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.head_dim, "block_size": BLOCK,
+                   "l2": "no flush: every layer reads its own caches", "parallelism": "replicas"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind + " (sustained bf16)",
+                     "kernel": "paged prefill attention (mma.sync m16n8k16 bf16), per layer",
+                     "algorithmic_flops_per_launch": fl, "avg_launch_ms": attn_avg_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * layers * fl / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * layers * 2,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
 
 
 # ---------------------------------------------------------------- main -----
@@ -254,7 +482,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--workload", default="qwen3_8b", choices=list(WORKLOADS))
+    ap.add_argument("--workload", default="qwen3_8b", choices=list(WORKLOADS) + list(PREFILL_WORKLOADS))
     ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
@@ -262,11 +490,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     assert args.warmup >= 0 and args.steps >= 1
+    rank, world, local = dist_setup(args)
+    if args.workload in PREFILL_WORKLOADS:
+        run_prefill(args, PREFILL_WORKLOADS[args.workload], rank, world)
+        return
     w = WORKLOADS[args.workload]
     if args.layers is not None:
         import dataclasses
         w = dataclasses.replace(w, layers=args.layers)
-    rank, world, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

@@ -60,6 +60,9 @@ typedef enum mi_status {
 #define MI_DEVERR_BAD_POS      0x4 /* position outside [0, max_pos) */
 #define MI_DEVERR_BAD_CONTEXT  0x8 /* context length above max_blocks_per_seq * block_size */
 #define MI_DEVERR_TIMEOUT      0x10 /* a staged copy did not land within the wait limit */
+#define MI_DEVERR_BAD_QUERY    0x20 /* prefill: query_start not within [0, total_q] and ascending,
+                                       a request longer than max_query_len, or more
+                                       new tokens than context */
 
 /* Short human-readable name of a status. */
 const char* mi_status_string(mi_status s);
@@ -116,6 +119,16 @@ mi_status mi_kv_pool_batch_meta(const mi_kv_pool* pool, const int32_t* seq_ids, 
                                 int32_t* block_tables, int32_t* context_lens,
                                 int32_t* slot_mapping);
 
+/* Slots of tokens first_token .. first_token+count-1 of sequence seq_id, in
+ * order, into slots_out[0..count) (host): slot = table[t/16]*16 + t%16. This
+ * is the slot_mapping of a chunked append (prefill of many tokens per
+ * request; mini-infer README "项目概述", prefill and decode as separate
+ * passes). MI_ERR_UNKNOWN_SEQ if seq_id holds no allocation;
+ * MI_ERR_INVALID_ARG if first_token < 0, count < 0 or the range passes the
+ * tokens the sequence holds. */
+mi_status mi_kv_pool_token_slots(const mi_kv_pool* pool, int32_t seq_id, int32_t first_token,
+                                 int32_t count, int32_t* slots_out);
+
 /* Copy of one sequence's table into out[0..max_out) (host); returns the
  * number of blocks it holds, or -1 if unknown. */
 int32_t mi_kv_pool_seq_blocks(const mi_kv_pool* pool, int32_t seq_id, int32_t* out,
@@ -123,7 +136,9 @@ int32_t mi_kv_pool_seq_blocks(const mi_kv_pool* pool, int32_t seq_id, int32_t* o
 
 /* ------------------------------------------------------------------------ */
 /* Shapes shared by the device entry points.
- *   B                   requests in the batch (1 .. 65535)
+ *   B                   requests in the batch (decode attention: up to 65535;
+ *                       prefill attention: any); for mi_paged_kv_append the
+ *                       number of new-token rows (up to 2^24)
  *   Hq, Hkv             query / KV heads; Hq % Hkv == 0, G = Hq/Hkv in 1..8
  *   head_dim            64 or 128
  *   block_size          16
@@ -146,7 +161,10 @@ mi_status mi_rope_table(double theta, int32_t head_dim, int32_t max_pos, float* 
 
 /* Append one new token per request (mini-infer README "decode_batch 关键步骤",
  * write_decode_kv, with RoPE applied first as in NJU course brief §2.1).
- * For request b at position p = positions[b]:
+ * Rows are independent, so the same call appends a prefill chunk: make each
+ * new token a row b (dims.B = total new tokens) with its own position and
+ * slot (mi_kv_pool_token_slots).
+ * For row b at position p = positions[b]:
  *   q_out[b][j]                    = RoPE_p(q[b][j])   for j < Hq
  *   k_cache[blk][h][off][:]        = RoPE_p(k[b][h])   for h < Hkv
  *   v_cache[blk][h][off][:]        = v[b][h]
@@ -210,6 +228,35 @@ mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
                                             void* workspace, size_t workspace_bytes,
                                             int32_t* dev_err, mi_stream_t stream,
                                             mi_attn_variant variant, int32_t ctas);
+
+/* Causal paged GQA attention for a prefill or chunked-prefill batch (NJU
+ * course brief §2.1, the prefill stage of the prefill + decode loop; mini-infer
+ * README "项目概述", prefill as its own pass). dims.B = R requests. Request r
+ * contributes m_r = query_start[r+1] - query_start[r] new tokens, rows
+ * query_start[r] .. query_start[r+1]-1 of q, and holds n_r = context_lens[r]
+ * tokens counting them, so its new token i sits at position n_r - m_r + i:
+ *   out[row][j] = sum_t softmax_t(scale * <q[row][j], K_t>) V_t,
+ *                 t <= n_r - m_r + i,  K_t, V_t of KV head j / G
+ * read through block_tables[r] as in mi_paged_decode_attention; fp32 online
+ * softmax on bf16 tensor-core products, rounded to bf16.
+ * Host arguments: total_q = query_start[R] (rows of q and out), max_query_len
+ * >= every m_r (sizes the grid; 0 queues nothing).
+ * Device buffers: q, out [total_q][Hq][d] bf16 (16-byte aligned; q with RoPE
+ * applied), k_cache, v_cache, block_tables [R][max_blocks_per_seq] int32,
+ * context_lens [R] int32, query_start [R+1] int32, dev_err int32 or NULL.
+ * No workspace. Only the table entries covering positions < n_r are read;
+ * cache tokens past n_r may hold any bits.
+ * Device errors (MI_DEVERR_*): a bad query_start entry or m_r > max_query_len
+ * skips request r (BAD_QUERY; its rows are left as they were); m_r > n_r gives
+ * zero rows for the new tokens at negative positions (BAD_QUERY); n_r above a
+ * table row clamps to it (BAD_CONTEXT); a bad block id drops that block's
+ * keys (BAD_BLOCK). A request with m_r = 1 computes what
+ * mi_paged_decode_attention computes for it. */
+mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
+                                     const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     const int32_t* query_start, float scale, void* out,
+                                     int32_t* dev_err, mi_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Allocation-free attention. The pages have no counterpart to this entry

@@ -23,16 +23,17 @@ _lib = None
 MI_OK, MI_ERR_INVALID_ARG, MI_ERR_OUT_OF_BLOCKS, MI_ERR_UNKNOWN_SEQ = 0, 1, 2, 3
 MI_ERR_UNSUPPORTED, MI_ERR_CUDA, MI_ERR_DEVICE_BOUNDS, MI_ERR_TIMEOUT = 4, 5, 6, 7
 MI_DEVERR_BAD_BLOCK, MI_DEVERR_BAD_SLOT, MI_DEVERR_BAD_POS = 0x1, 0x2, 0x4
-MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT = 0x8, 0x10
+MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT, MI_DEVERR_BAD_QUERY = 0x8, 0x10, 0x20
 MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
 
 # every symbol include/mi.h declares
 EXPORTS = (
     "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc",
-    "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_seq_blocks",
+    "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_token_slots",
+    "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
-    "mi_paged_decode_attention_noalloc",
+    "mi_paged_prefill_attention", "mi_paged_decode_attention_noalloc",
 )
 MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -68,6 +69,7 @@ def load():
             "mi_kv_pool_free": ([P, i32], i32),
             "mi_kv_pool_num_free": ([P], i32),
             "mi_kv_pool_batch_meta": ([P, P, i32, P, P, P], i32),
+            "mi_kv_pool_token_slots": ([P, i32, i32, i32, P], i32),
             "mi_kv_pool_seq_blocks": ([P, i32, P, i32], i32),
             "mi_rope_table": ([f64, i32, i32, P], i32),
             "mi_paged_kv_append": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P], i32),
@@ -75,6 +77,7 @@ def load():
             "mi_paged_decode_attention": ([dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_attention_variant": (
                 [dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P, i32, i32], i32),
+            "mi_paged_prefill_attention": ([dims_p, i32, i32, P, P, P, P, P, P, f32, P, P, P], i32),
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
@@ -164,6 +167,13 @@ def mi_kv_pool_batch_meta(handle, seq_ids, max_blocks_per_seq, block_tables=None
     return st, bt, cl, sl
 
 
+def mi_kv_pool_token_slots(handle, seq_id, first_token, count):
+    """Returns (status, int32 [count] host array of slots)."""
+    out = np.empty(max(int(count), 1), np.int32)
+    st = load().mi_kv_pool_token_slots(handle, int(seq_id), int(first_token), int(count), _ptr(out))
+    return st, out[:max(int(count), 0)]
+
+
 def mi_kv_pool_seq_blocks(handle, seq_id, max_out=1 << 20):
     n = load().mi_kv_pool_seq_blocks(handle, int(seq_id), None, 0)
     if n < 0:
@@ -191,6 +201,11 @@ class Pool:
 
     def num_free(self):
         return mi_kv_pool_num_free(self.handle)
+
+    def token_slots(self, seq, first_token, count):
+        st, slots = mi_kv_pool_token_slots(self.handle, seq, first_token, count)
+        check(st, "mi_kv_pool_token_slots")
+        return slots
 
     def batch_meta(self, seq_ids):
         st, bt, cl, sl = mi_kv_pool_batch_meta(self.handle, seq_ids, self.max_blocks_per_seq)
@@ -246,6 +261,14 @@ def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tabl
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream),
         int(variant), int(ctas))
+
+
+def mi_paged_prefill_attention(d: MiDims, total_q, max_query_len, q, k_cache, v_cache, block_tables,
+                               context_lens, query_start, scale, out, dev_err=None, stream=None):
+    return load().mi_paged_prefill_attention(ctypes.byref(d), int(total_q), int(max_query_len), _ptr(q),
+                                             _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                             _ptr(context_lens), _ptr(query_start), float(scale), _ptr(out),
+                                             _ptr(dev_err), _stream(stream))
 
 
 def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale, out,

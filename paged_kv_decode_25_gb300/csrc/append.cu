@@ -57,8 +57,8 @@ struct AppendParams {
 // rotation items copy 16-byte chunks of v into the cache.
 __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     // inputs may come from the kernel just before this one in the stream
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_wait();
+    pdl_trigger();
     const int half = a.d / 2;
     const int groups = half / 8;  // 8-pair groups per head
     const long long n_rot = (long long)B * (a.Hq + a.Hkv) * groups;
@@ -146,7 +146,7 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     using namespace mi;
     if (!dims) return MI_ERR_INVALID_ARG;
     const mi_dims D = *dims;
-    if (D.B < 0 || D.B > 65535 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || max_pos < 1)
+    if (D.B < 0 || D.B > (1 << 24) || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || max_pos < 1)
         return MI_ERR_INVALID_ARG;
     if (D.block_size != kBlock || (D.head_dim != 64 && D.head_dim != 128) || D.Hq % D.Hkv != 0)
         return MI_ERR_UNSUPPORTED;
@@ -175,16 +175,9 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     a.max_pos = max_pos;
     const long long threads = (long long)D.B * (D.Hq + D.Hkv) * (D.head_dim / 16) +
                               (long long)D.B * D.Hkv * (D.head_dim / 8);
-    // programmatic dependent launch: the kernel may be scheduled while the
-    // previous kernel in the stream drains, and waits for it before any load
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((threads + 127) / 128));
-    cfg.blockDim = dim3(128);
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, append_kernel, a, (int)D.B) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+    const long long grid = (threads + 127) / 128;
+    if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
+    return launch_pdl(append_kernel, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B) == cudaSuccess
+               ? MI_OK
+               : MI_ERR_CUDA;
 }

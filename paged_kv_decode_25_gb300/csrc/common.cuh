@@ -176,4 +176,28 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
 }
 
+// ----------------------------------------------- programmatic launch -------
+
+// A kernel launched with launch_pdl may start while the previous kernel in
+// the stream is still running; it calls pdl_wait() before touching memory
+// that kernel may write, and pdl_trigger() to let the next kernel start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Args>
+inline cudaError_t launch_pdl(void (*fn)(Args...), int grid, int block, int smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 }  // namespace mi

@@ -44,6 +44,7 @@
 #include <random>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace mi {
 namespace {
@@ -177,8 +178,6 @@ __device__ __forceinline__ int cta_of(long long TB, int P, long long x) {
     return c;
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------- smem layout ------
 
@@ -186,16 +185,6 @@ template <int HD>
 struct Tile {
     static constexpr int kBytes = kBlock * HD * 2;  // one 16-token K or V tile
 };
-
-// Physical byte offset of 16-byte chunk `chunk` (0 .. HD/8-1) of token row
-// `row` inside a tile written by one 128-byte-swizzled TMA box. The cache is
-// viewed as 128-byte lines (HD/64 per token), so a 16-token tile is one
-// contiguous box of 16*HD/64 lines; chunk c of line l sits at c ^ (l & 7).
-template <int HD>
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    const int line = row * (HD / 64) + (chunk >> 3);
-    return (uint32_t)(line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
-}
 
 struct SmemPlan {
     int tiles, full, empty, mbuf, lbuf, obuf, xbuf, scan, fac, flag, total;
@@ -793,35 +782,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
 
 // ------------------------------------------------------------- host side --
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult qr;
-        void* f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// 2-D map over a cache viewed as 128-byte lines: [rows * HD/64][64] bf16,
-// box = one 16-token tile (16 * HD/64 lines x 64 columns), 128-byte swizzle.
-bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {64, (cuuint64_t)rows * (HD / 64)};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {64, (cuuint32_t)(kBlock * HD / 64)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 constexpr int kWarps = 4;                 // consumer warps; one producer warp more
 constexpr int kMaxStages = 3;
 constexpr int kSmemLimit = 227 * 1024;    // per CTA
@@ -946,24 +906,6 @@ unsigned long long next_epoch() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Launch with programmatic dependent launch allowed: the kernel may be
-// scheduled while the previous kernel in the stream finishes, and waits for it
-// (griddepcontrol.wait) before touching memory that kernel may write.
-template <typename... Args>
-cudaError_t launch_pdl(void (*fn)(Args...), int grid, int block, int smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, args...);
-}
 
 }  // namespace
 }  // namespace mi

@@ -158,3 +158,17 @@ extern "C" mi_status mi_rope_table(double theta, int32_t head_dim, int32_t max_p
     }
     return MI_OK;
 }
+
+extern "C" mi_status mi_kv_pool_token_slots(const mi_kv_pool* p, int32_t seq, int32_t first_token,
+                                            int32_t count, int32_t* slots_out) {
+    if (!p || first_token < 0 || count < 0 || (count > 0 && !slots_out)) return MI_ERR_INVALID_ARG;
+    if (seq < 0 || (size_t)seq >= p->tables.size() || !p->live[(size_t)seq]) return MI_ERR_UNKNOWN_SEQ;
+    if ((int64_t)first_token + count > p->tokens[(size_t)seq]) return MI_ERR_INVALID_ARG;
+    const std::vector<int32_t>& t = p->tables[(size_t)seq];
+    const int32_t BS = p->block_size;
+    for (int32_t i = 0; i < count; ++i) {
+        const int32_t tok = first_token + i;
+        slots_out[i] = t[(size_t)(tok / BS)] * BS + tok % BS;
+    }
+    return MI_OK;
+}

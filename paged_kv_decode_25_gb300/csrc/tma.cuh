@@ -1,0 +1,59 @@
+// Staging of 16-token KV tiles by TMA, shared by the decode and prefill
+// attention kernels: the host-side tensor map over a paged cache and the
+// device-side address of a 16-byte chunk inside a staged, 128-byte-swizzled
+// tile.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace mi {
+
+// Physical byte offset of 16-byte chunk `chunk` (0 .. HD/8-1) of token row
+// `row` inside a tile written by one 128-byte-swizzled TMA box. The cache is
+// viewed as 128-byte lines (HD/64 per token), so a 16-token tile is one
+// contiguous box of 16*HD/64 lines; chunk c of line l sits at c ^ (l & 7).
+// The tile must start on a 1024-byte boundary.
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    const int line = row * (HD / 64) + (chunk >> 3);
+    return (uint32_t)(line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda); nullptr when the driver does not provide it.
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult qr;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D map over a cache viewed as 128-byte lines: [rows * HD/64][64] bf16,
+// box = one 16-token tile (16 * HD/64 lines x 64 columns), 128-byte swizzle.
+// `rows` counts token rows of all blocks and KV heads (num_blocks * Hkv * 16).
+inline bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows * (HD / 64)};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, (cuuint32_t)(kBlock * HD / 64)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace mi

@@ -156,3 +156,60 @@ def test_device_entry_points_reject_bad_args_without_a_gpu(mi):
     zero = mi.dims(0, 4, 2, 64, 8, 4)
     assert mi.mi_paged_kv_append(zero, None, None, None, None, None, None, 4, None, None, None,
                                  stream=0) == mi.MI_OK
+
+
+def test_token_slots_match_model_after_churn(mi):
+    from workloads import PREFILL_WORKLOADS, prefill_setup_pool
+    w = WORKLOADS["qwen3_8b"]
+    order = initial_free_order(w)
+    lib = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, order)
+    model = PoolModel(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, order)
+    ctx = context_lengths(w)
+    setup_pool(w, lib, ctx)
+    setup_pool(w, model, ctx)
+    r = np.random.Generator(np.random.PCG64(11))
+    for b in range(0, w.B, 5):
+        n = int(ctx[b])
+        first = int(r.integers(0, n))
+        count = int(r.integers(0, n - first + 1))
+        assert np.array_equal(lib.token_slots(b, first, count), model.token_slots(b, first, count))
+    pw = PREFILL_WORKLOADS["prefill_small"]
+    lib2 = mi.Pool(pw.num_blocks, pw.max_seqs, pw.max_blocks_per_seq, None)
+    model2 = PoolModel(pw.num_blocks, pw.max_seqs, pw.max_blocks_per_seq, None)
+    prefill_setup_pool(pw, lib2)
+    prefill_setup_pool(pw, model2)
+    h, m = pw.lengths()
+    for b in range(pw.B):
+        assert np.array_equal(lib2.token_slots(b, int(h[b]), int(m[b])),
+                              model2.token_slots(b, int(h[b]), int(m[b])))
+
+
+def test_token_slots_errors(mi):
+    p = mi.Pool(8, 2, 4)
+    assert p.alloc(0, 20) == 0
+    st, _ = mi.mi_kv_pool_token_slots(p.handle, 1, 0, 1)
+    assert st == mi.MI_ERR_UNKNOWN_SEQ
+    assert mi.mi_kv_pool_token_slots(p.handle, 0, 15, 6)[0] == mi.MI_ERR_INVALID_ARG  # past token 20
+    assert mi.mi_kv_pool_token_slots(p.handle, 0, -1, 2)[0] == mi.MI_ERR_INVALID_ARG
+    st, s = mi.mi_kv_pool_token_slots(p.handle, 0, 14, 6)
+    assert st == mi.MI_OK and len(s) == 6
+    st, s = mi.mi_kv_pool_token_slots(p.handle, 0, 20, 0)
+    assert st == mi.MI_OK and len(s) == 0
+
+
+def test_prefill_rejects_bad_args_without_a_gpu(mi):
+    d = mi.dims(2, 4, 2, 64, 8, 4)
+    P = dict(q=16, k_cache=16, v_cache=16, block_tables=16, context_lens=16, query_start=16, scale=1.0,
+             out=16, stream=0)
+    odd = mi.dims(2, 4, 2, 96, 8, 4)
+    assert mi.mi_paged_prefill_attention(odd, 4, 2, **P) == mi.MI_ERR_UNSUPPORTED
+    wide = mi.dims(2, 18, 2, 64, 8, 4)  # G = 9
+    assert mi.mi_paged_prefill_attention(wide, 4, 2, **P) == mi.MI_ERR_UNSUPPORTED
+    assert mi.mi_paged_prefill_attention(d, -1, 2, **P) == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_paged_prefill_attention(d, 4, -2, **P) == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_paged_prefill_attention(d, 4, 2, **dict(P, scale=float("nan"))) == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_paged_prefill_attention(d, 4, 2, **dict(P, query_start=None)) == mi.MI_ERR_INVALID_ARG
+    assert mi.mi_paged_prefill_attention(d, 4, 2, **dict(P, out=24)) == mi.MI_ERR_INVALID_ARG  # misaligned
+    # nothing to do: no call reaches the GPU
+    assert mi.mi_paged_prefill_attention(d, 0, 0, **dict(P, q=None, out=None)) == mi.MI_OK
+    assert mi.mi_paged_prefill_attention(mi.dims(0, 4, 2, 64, 8, 4), 0, 0, **P) == mi.MI_OK

@@ -227,3 +227,109 @@ def device_fill_cache(w: Workload, layer: int, k_cache, v_cache) -> None:
         for s in range(0, flat.numel(), chunk):
             e = min(flat.numel(), s + chunk)
             flat[s:e].copy_(torch.randn(e - s, generator=g, device=t.device, dtype=torch.float32))
+
+
+# ------------------------------------------------------------- prefill -------
+
+@dataclass(frozen=True)
+class PrefillWorkload:
+    """A prefill / chunked-prefill batch of one layer: request r holds
+    history[r] cached tokens and appends new[r] tokens at positions
+    history[r] .. history[r] + new[r] - 1 (NJU course brief §2.1, the prefill
+    stage; mini-infer README "项目概述", prefill as its own pass).
+
+    kind "explicit": ``args`` = (history tuple, new tuple).
+    kind "mixed": ``args`` = (fresh, fresh_lo, fresh_hi, cont, cont_lo, cont_hi,
+    chunk): ``fresh`` whole prompts of U[fresh_lo, fresh_hi] tokens with no
+    history, then ``cont`` continuations with log-uniform [cont_lo, cont_hi]
+    history and a ``chunk``-token chunk each."""
+    name: str
+    index: int
+    Hq: int
+    Hkv: int
+    head_dim: int
+    num_blocks: int
+    kind: str
+    args: tuple
+    theta: float = 1.0e6
+    layers: int = 1
+
+    @property
+    def G(self):
+        return self.Hq // self.Hkv
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def seed(self):
+        return 1000 + self.index
+
+    @property
+    def B(self):
+        return len(self.lengths()[0])
+
+    def lengths(self):
+        """(history, new) int32 arrays, one entry per request."""
+        if self.kind == "explicit":
+            h, n = self.args
+            return np.array(h, np.int32), np.array(n, np.int32)
+        if self.kind == "mixed":
+            fresh, flo, fhi, cont, clo, chi, chunk = self.args
+            r = np.random.Generator(np.random.PCG64([self.seed, 1]))
+            fn = r.integers(flo, fhi + 1, size=fresh)
+            ch = np.floor(np.exp(r.uniform(math.log(clo), math.log(chi), size=cont))).astype(np.int64)
+            h = np.concatenate([np.zeros(fresh, np.int64), np.clip(ch, clo, chi)])
+            n = np.concatenate([fn, np.full(cont, chunk, np.int64)])
+            return h.astype(np.int32), n.astype(np.int32)
+        raise ValueError(self.kind)
+
+    def max_context(self):
+        h, n = self.lengths()
+        return int((h + n).max())
+
+    @property
+    def max_blocks_per_seq(self):
+        return -(-self.max_context() // BLOCK)
+
+    @property
+    def max_pos(self):
+        return self.max_context()
+
+    @property
+    def max_seqs(self):
+        return self.B
+
+
+PREFILL_WORKLOADS = {
+    # small enough for the oracle to check every row: several tiles, ragged
+    # tails, a one-token request, a request with no history
+    "prefill_small": PrefillWorkload("prefill_small", 6, Hq=8, Hkv=2, head_dim=128, num_blocks=256,
+                                     kind="explicit",
+                                     args=((0, 0, 37, 100, 300, 16), (1, 70, 16, 129, 33, 47))),
+    # Qwen3-8B layer shape (Hq 32, Hkv 8, d 128): 8 fresh prompts of 512..2048
+    # tokens and 8 chunked continuations (512-token chunks over 1k..8k history)
+    "qwen3_8b_prefill": PrefillWorkload("qwen3_8b_prefill", 7, Hq=32, Hkv=8, head_dim=128,
+                                        num_blocks=4096, kind="mixed",
+                                        args=(8, 512, 2048, 8, 1024, 8192, 512)),
+}
+
+
+def prefill_setup_pool(w: PrefillWorkload, pool) -> None:
+    """Give request r (sequence id r) history[r] + new[r] tokens, in order."""
+    h, n = w.lengths()
+    for r in range(w.B):
+        st = pool.alloc(r, int(h[r] + n[r]))
+        assert st == 0, f"request {r} does not fit the pool (status {st})"
+
+
+def prefill_new_values(w: PrefillWorkload, layer: int = 0):
+    """q [T][Hq][d], k [T][Hkv][d], v [T][Hkv][d] (bf16 bits) of the new
+    tokens, request after request."""
+    T = int(w.lengths()[1].sum())
+    r = np.random.Generator(np.random.PCG64([w.seed, 300, layer]))
+    q = bf16_normal(r, (T, w.Hq, w.head_dim))
+    k = bf16_normal(r, (T, w.Hkv, w.head_dim))
+    v = bf16_normal(r, (T, w.Hkv, w.head_dim))
+    return q, k, v
