@@ -129,6 +129,28 @@ mi_status mi_kv_pool_batch_meta(const mi_kv_pool* pool, const int32_t* seq_ids, 
 mi_status mi_kv_pool_token_slots(const mi_kv_pool* pool, int32_t seq_id, int32_t first_token,
                                  int32_t count, int32_t* slots_out);
 
+/* Admission of a new prefill request from the pool's free space: the
+ * three-level brake of the GitLink project report "mxdyymxgxtlkjdxtjyhysx"
+ * (section "我们的解决方案：SLO感知与KV Cache保护调度器"):
+ *   MI_ADMIT_HARD_BRAKE  free share of the pool below hard_bp / 10000
+ *                        (report's example: 10%), whatever is running;
+ *   MI_ADMIT_SOFT_BRAKE  running_decodes > 0 and free share below
+ *                        soft_bp / 10000 (example: 30%);
+ *   MI_ADMIT_PROCEED     otherwise.
+ * "Below" is strict; the shares are compared exactly in integers
+ * (free * 10000 < bp * num_blocks). Thresholds in basis points, 0..10000.
+ * MI_ERR_INVALID_ARG for a NULL pool or out, running_decodes < 0 or a
+ * threshold outside 0..10000. Host only; the pool is not changed. */
+typedef enum mi_admit_decision {
+    MI_ADMIT_PROCEED = 0,
+    MI_ADMIT_SOFT_BRAKE = 1,
+    MI_ADMIT_HARD_BRAKE = 2
+} mi_admit_decision;
+#define MI_ADMIT_HARD_BP_DEFAULT 1000
+#define MI_ADMIT_SOFT_BP_DEFAULT 3000
+mi_status mi_kv_pool_admission(const mi_kv_pool* pool, int32_t running_decodes, int32_t hard_bp,
+                               int32_t soft_bp, mi_admit_decision* out);
+
 /* Copy of one sequence's table into out[0..max_out) (host); returns the
  * number of blocks it holds, or -1 if unknown. */
 int32_t mi_kv_pool_seq_blocks(const mi_kv_pool* pool, int32_t seq_id, int32_t* out,

@@ -33,12 +33,19 @@ class PoolModel:
         assert sorted(order) == list(range(num_blocks))
         self.free_stack = order[::-1]          # pop() returns order[0] first
         self.max_seqs = max_seqs
+        self.num_blocks = num_blocks
         self.max_blocks_per_seq = max_blocks_per_seq
         self.tables = {}                       # seq id -> list of block ids
         self.tokens = {}                       # seq id -> token count
 
     def num_free(self):
         return len(self.free_stack)
+
+    def admission(self, running_decodes, hard_bp=None, soft_bp=None):
+        """Brake level for a new prefill request (oracle.admission)."""
+        from oracle import admission as A
+        return A.admission(len(self.free_stack), self.num_blocks, running_decodes,
+                           A.HARD_BP if hard_bp is None else hard_bp, A.SOFT_BP if soft_bp is None else soft_bp)
 
     def alloc(self, seq, num_tokens):
         if not (0 <= seq < self.max_seqs) or num_tokens < 0:

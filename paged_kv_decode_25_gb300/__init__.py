@@ -25,11 +25,14 @@ MI_ERR_UNSUPPORTED, MI_ERR_CUDA, MI_ERR_DEVICE_BOUNDS, MI_ERR_TIMEOUT = 4, 5, 6,
 MI_DEVERR_BAD_BLOCK, MI_DEVERR_BAD_SLOT, MI_DEVERR_BAD_POS = 0x1, 0x2, 0x4
 MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT, MI_DEVERR_BAD_QUERY = 0x8, 0x10, 0x20
 MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
+MI_ADMIT_PROCEED, MI_ADMIT_SOFT_BRAKE, MI_ADMIT_HARD_BRAKE = 0, 1, 2
+MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
 
 # every symbol include/mi.h declares
 EXPORTS = (
     "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc",
     "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_token_slots",
+    "mi_kv_pool_admission",
     "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
@@ -70,6 +73,7 @@ def load():
             "mi_kv_pool_num_free": ([P], i32),
             "mi_kv_pool_batch_meta": ([P, P, i32, P, P, P], i32),
             "mi_kv_pool_token_slots": ([P, i32, i32, i32, P], i32),
+            "mi_kv_pool_admission": ([P, i32, i32, i32, P], i32),
             "mi_kv_pool_seq_blocks": ([P, i32, P, i32], i32),
             "mi_rope_table": ([f64, i32, i32, P], i32),
             "mi_paged_kv_append": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P], i32),
@@ -174,6 +178,15 @@ def mi_kv_pool_token_slots(handle, seq_id, first_token, count):
     return st, out[:max(int(count), 0)]
 
 
+def mi_kv_pool_admission(handle, running_decodes, hard_bp=MI_ADMIT_HARD_BP_DEFAULT,
+                         soft_bp=MI_ADMIT_SOFT_BP_DEFAULT):
+    """Returns (status, decision)."""
+    out = ctypes.c_int32(-1)
+    st = load().mi_kv_pool_admission(handle, int(running_decodes), int(hard_bp), int(soft_bp),
+                                     ctypes.byref(out))
+    return st, int(out.value)
+
+
 def mi_kv_pool_seq_blocks(handle, seq_id, max_out=1 << 20):
     n = load().mi_kv_pool_seq_blocks(handle, int(seq_id), None, 0)
     if n < 0:
@@ -206,6 +219,11 @@ class Pool:
         st, slots = mi_kv_pool_token_slots(self.handle, seq, first_token, count)
         check(st, "mi_kv_pool_token_slots")
         return slots
+
+    def admission(self, running_decodes, hard_bp=MI_ADMIT_HARD_BP_DEFAULT, soft_bp=MI_ADMIT_SOFT_BP_DEFAULT):
+        st, dec = mi_kv_pool_admission(self.handle, running_decodes, hard_bp, soft_bp)
+        check(st, "mi_kv_pool_admission")
+        return dec
 
     def batch_meta(self, seq_ids):
         st, bt, cl, sl = mi_kv_pool_batch_meta(self.handle, seq_ids, self.max_blocks_per_seq)

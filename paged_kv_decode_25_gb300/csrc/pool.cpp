@@ -172,3 +172,19 @@ extern "C" mi_status mi_kv_pool_token_slots(const mi_kv_pool* p, int32_t seq, in
     }
     return MI_OK;
 }
+
+extern "C" mi_status mi_kv_pool_admission(const mi_kv_pool* p, int32_t running_decodes, int32_t hard_bp,
+                                          int32_t soft_bp, mi_admit_decision* out) {
+    if (!p || !out || running_decodes < 0 || hard_bp < 0 || hard_bp > 10000 || soft_bp < 0 || soft_bp > 10000)
+        return MI_ERR_INVALID_ARG;
+    // free / total < bp / 10000, compared exactly in 64-bit integers
+    const int64_t free_scaled = (int64_t)p->free_stack.size() * 10000;
+    const int64_t total = p->num_blocks;
+    if (free_scaled < (int64_t)hard_bp * total)
+        *out = MI_ADMIT_HARD_BRAKE;
+    else if (running_decodes > 0 && free_scaled < (int64_t)soft_bp * total)
+        *out = MI_ADMIT_SOFT_BRAKE;
+    else
+        *out = MI_ADMIT_PROCEED;
+    return MI_OK;
+}

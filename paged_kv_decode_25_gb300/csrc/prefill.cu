@@ -22,9 +22,11 @@
 //     softmax on the accumulator fragments; the probabilities are repacked in
 //     place as bf16 A fragments and O[16 x HD] += P . V with V read by
 //     ldmatrix.trans.
-//   * Grid: one CTA per (row tile from the end k, request r, KV head h), k the
-//     slowest index, so the hardware dispatches the tiles with the most keys
-//     first; tiles past a request's last row exit at once.
+//   * Grid: one CTA per (request r, KV head h, row tile from the end k), k the
+//     fastest index: the CTAs resident at any time share the K/V of a few
+//     (request, head) pairs through L2, and each pair's tiles start with the
+//     one that reads the most keys. Tiles past a request's last row exit at
+//     once.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -50,6 +52,7 @@ struct PrefillParams {
     uint16_t* out;                 // [T][Hq][HD]
     int32_t* dev_err;
     int R, Hq, Hkv, G, num_blocks, mbps, T, max_q;
+    int tiles_max;                 // row tiles of the longest request
     float sl2;                     // scale * log2(e)
 };
 
@@ -97,10 +100,10 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
     pdl_trigger();
 
     // ------------------------------------------------------- work item ----
-    const int h = blockIdx.x % p.Hkv;
-    const int rest = blockIdx.x / p.Hkv;
-    const int r = rest % p.R;
-    const int k = rest / p.R;
+    const int k = blockIdx.x % p.tiles_max;
+    const int rest = blockIdx.x / p.tiles_max;
+    const int h = rest % p.Hkv;
+    const int r = rest / p.Hkv;
     const bool reporter = k == 0 && h == 0 && threadIdx.x == 0;  // one error report per request
     const int q0 = __ldg(p.query_start + r), q1 = __ldg(p.query_start + r + 1);
     const int m = q1 - q0;
@@ -449,6 +452,7 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
     p.mbps = D.max_blocks_per_seq;
     p.T = total_q;
     p.max_q = max_query_len;
+    p.tiles_max = (int)tiles_max;
     p.sl2 = scale * 1.4426950408889634f;
     const cudaError_t e =
         HD == 64 ? launch_pdl(prefill_kernel<64>, (int)grid, (kPWarps + 1) * 32, smem, (cudaStream_t)stream, tk, tv, p)

@@ -333,3 +333,63 @@ def prefill_new_values(w: PrefillWorkload, layer: int = 0):
     k = bf16_normal(r, (T, w.Hkv, w.head_dim))
     v = bf16_normal(r, (T, w.Hkv, w.head_dim))
     return q, k, v
+
+
+# ------------------------------------------------- continuous batching -------
+
+def serving_churn(pool, steps: int, seed: int, use_brakes: bool = True, arrival_max: int = 4,
+                  prompt=(64, 1024), gen=(16, 512), max_seqs: int = 4096, hard_bp=None, soft_bp=None):
+    """Drive a pool through a continuous-batching schedule (mini-infer README
+    "项目概述": every step admits what it can and decodes the running batch)
+    and return the trace of pool events.
+
+    Each step: 0..arrival_max new requests arrive (prompt U[prompt], output
+    U[gen] tokens, seeded); waiting requests are admitted in arrival order
+    while ``pool.admission(len(running))`` says proceed (or always, when
+    use_brakes is False) and their prompt fits; every running request then
+    grows by one token, and one that finds no free block is preempted (freed,
+    back to the head of the queue, its tokens to be recomputed); finished
+    requests are freed. ``pool`` needs alloc, free, num_free and admission.
+    Returns a list of per-step tuples (admitted ids, preempted ids, finished
+    ids, free blocks after the step)."""
+    r = np.random.Generator(np.random.PCG64([seed, 400]))
+    waiting, running, trace = [], [], []
+    target = {}  # request -> (prompt tokens, total tokens)
+    held = {}    # running request -> tokens in the pool
+    nxt = 0
+    kw = {} if hard_bp is None else {"hard_bp": hard_bp, "soft_bp": soft_bp}
+    for _ in range(steps):
+        for _ in range(int(r.integers(0, arrival_max + 1))):
+            if nxt < max_seqs:
+                p_len = int(r.integers(prompt[0], prompt[1] + 1))
+                target[nxt] = (p_len, p_len + int(r.integers(gen[0], gen[1] + 1)))
+                waiting.append(nxt)
+                nxt += 1
+        admitted, preempted, finished = [], [], []
+        while waiting:
+            if use_brakes and pool.admission(len(running), **kw) != 0:
+                break
+            s = waiting[0]
+            if pool.alloc(s, target[s][0]) != 0:
+                break
+            waiting.pop(0)
+            running.append(s)
+            held[s] = target[s][0]
+            admitted.append(s)
+        for s in list(running):
+            n = held[s] + 1
+            if pool.alloc(s, n) != 0:
+                assert pool.free(s) == 0
+                running.remove(s)
+                del held[s]
+                waiting.insert(0, s)
+                preempted.append(s)
+                continue
+            held[s] = n
+            if n >= target[s][1]:
+                assert pool.free(s) == 0
+                running.remove(s)
+                del held[s]
+                finished.append(s)
+        trace.append((tuple(admitted), tuple(preempted), tuple(finished), pool.num_free()))
+    return trace
