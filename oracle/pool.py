@@ -35,8 +35,11 @@ class PoolModel:
         self.max_seqs = max_seqs
         self.num_blocks = num_blocks
         self.max_blocks_per_seq = max_blocks_per_seq
-        self.tables = {}                       # seq id -> list of block ids
-        self.tokens = {}                       # seq id -> token count
+        self.tables = {}                       # seq id -> list of block ids (resident sequences)
+        self.tokens = {}                       # seq id -> token count (resident or swapped out)
+        self.swapped = set()                   # sequences whose blocks are swapped out
+        self.clock = 0                         # use counter for LRU eviction
+        self.last_use = {}                     # resident seq id -> clock of its last use
 
     def num_free(self):
         return len(self.free_stack)
@@ -48,7 +51,7 @@ class PoolModel:
                            A.HARD_BP if hard_bp is None else hard_bp, A.SOFT_BP if soft_bp is None else soft_bp)
 
     def alloc(self, seq, num_tokens):
-        if not (0 <= seq < self.max_seqs) or num_tokens < 0:
+        if not (0 <= seq < self.max_seqs) or num_tokens < 0 or seq in self.swapped:
             return INVALID_ARG
         have = self.tables.get(seq, [])
         if num_tokens < self.tokens.get(seq, 0):
@@ -64,15 +67,69 @@ class PoolModel:
             table.append(self.free_stack.pop())
         self.tables[seq] = table
         self.tokens[seq] = num_tokens
+        self._use([seq])
         return OK
 
     def free(self, seq):
+        if seq in self.swapped:
+            self.swapped.discard(seq)
+            del self.tokens[seq]
+            return OK
         if seq not in self.tables:
             return UNKNOWN_SEQ
         for blk in self.tables.pop(seq):
             self.free_stack.append(blk)
         del self.tokens[seq]
+        self.last_use.pop(seq, None)
         return OK
+
+    # ---- swap to host memory with LRU eviction (NJU course brief, optional
+    # task 3 "KV Cache Offloading": inactive KV blocks go to CPU memory and come
+    # back when needed, under an eviction policy such as LRU)
+
+    def _use(self, seqs):
+        self.clock += 1
+        for s in seqs:
+            self.last_use[s] = self.clock
+
+    def touch(self, seqs):
+        """Mark resident sequences as used now (one clock tick for the call)."""
+        if any(s not in self.tables for s in seqs):
+            return UNKNOWN_SEQ
+        self._use(seqs)
+        return OK
+
+    def lru_victim(self, exclude=()):
+        """Least recently used resident sequence holding a block, not in
+        exclude (ties: lower id); -1 when there is none."""
+        cand = [(self.last_use.get(s, 0), s) for s, t in self.tables.items() if t and s not in set(exclude)]
+        return min(cand)[1] if cand else -1
+
+    def swap_out(self, seq):
+        """Release a resident sequence's blocks (pushed as free() pushes them)
+        and keep its token count; returns (status, its former table)."""
+        if seq not in self.tables:
+            return UNKNOWN_SEQ, []
+        table = self.tables.pop(seq)
+        for blk in table:
+            self.free_stack.append(blk)
+        self.swapped.add(seq)
+        self.last_use.pop(seq, None)
+        return OK, table
+
+    def swap_in(self, seq):
+        """Give a swapped-out sequence ceil(tokens/16) fresh blocks in pop
+        order; returns (status, its new table). Out of blocks: unchanged."""
+        if seq not in self.swapped:
+            return UNKNOWN_SEQ, []
+        need = -(-self.tokens[seq] // BLOCK)
+        if need > len(self.free_stack):
+            return OUT_OF_BLOCKS, []
+        table = [self.free_stack.pop() for _ in range(need)]
+        self.tables[seq] = table
+        self.swapped.discard(seq)
+        self._use([seq])
+        return OK, list(table)
 
     def batch_meta(self, seq_ids):
         """block_tables [B][max_blocks_per_seq] (pad -1), context_lens [B], slot of the last token [B]."""
