@@ -64,6 +64,12 @@ def _load():
             lib.or_contiguous_attention.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, f64, P]
             lib.or_paged_prefill_attention.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, f64, P, i32]
             lib.or_paged_prefill_attention.restype = i32
+            lib.or_e4m3_from_double_array.argtypes = [P, ctypes.c_int64, P]
+            lib.or_double_from_e4m3_array.argtypes = [P, ctypes.c_int64, P]
+            lib.or_append_fp8.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P, P]
+            lib.or_append_fp8.restype = i32
+            lib.or_paged_attention_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, i32, P, f64, P, i32]
+            lib.or_paged_attention_fp8.restype = i32
             _lib = lib
     return _lib
 
@@ -185,4 +191,54 @@ def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, que
     out = np.empty((T, Hq, d), np.float64)
     _load().or_paged_prefill_attention(R, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl), _p(qs),
                                        float(scale), _p(out), int(nthreads))
+    return out
+
+
+# ------------------------------------------------------------- FP8 KV ------
+
+def e4m3_from_f64(x: np.ndarray) -> np.ndarray:
+    """float64 -> e4m3 codes (uint8): nearest-even, saturating to +-448."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint8)
+    _load().or_e4m3_from_double_array(_p(x), x.size, _p(out))
+    return out
+
+
+def e4m3_to_f64(c: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) -> float64, exact."""
+    c = _c(c, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().or_double_from_e4m3_array(_p(c), c.size, _p(out))
+    return out
+
+
+def append_fp8(q, k, v, positions, slot_mapping_, table, k_scale, v_scale, k_cache, v_cache):
+    """As append, into uint8 e4m3 caches with fp32 per-KV-head scales.
+    Returns (q_out, status)."""
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k.shape[1]
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    pos = _c(positions, np.int32); sm = _c(slot_mapping_, np.int32)
+    table = _c(table, np.float32)
+    ks = _c(k_scale, np.float32); vs = _c(v_scale, np.float32)
+    q_out = np.empty_like(q)
+    st = _load().or_append_fp8(B, Hq, Hkv, d, k_cache.shape[0], _p(q), _p(k), _p(v), _p(pos), _p(sm),
+                               _p(table), table.shape[0], _p(ks), _p(vs), _p(q_out), _p(k_cache), _p(v_cache))
+    return q_out, st
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, nthreads=1):
+    """q uint16 [B][Hq][d]; caches uint8 e4m3 [nb][Hkv][16][d]; per-KV-head
+    fp32 scales; returns float64 [B][Hq][d]."""
+    q = _c(q, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    kc = _c(k_cache, np.uint8); vc = _c(v_cache, np.uint8)
+    ks = _c(k_scale, np.float32); vs = _c(v_scale, np.float32)
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32)
+    out = np.empty((B, Hq, d), np.float64)
+    used = _load().or_paged_attention_fp8(B, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
+                                          bt.shape[1], _p(cl), float(scale), _p(out), int(nthreads))
+    paged_attention_fp8.threads_used = used
     return out

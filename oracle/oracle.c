@@ -407,3 +407,180 @@ int32_t or_paged_prefill_attention(int32_t R, int32_t Hq, int32_t Hkv, int32_t d
     free(jobs);
     return nthreads;
 }
+
+/* ------------------------------------------------------------- FP8 KV ---- */
+/* FP8 KV cache (GitLink project report "mxdyymxgxtlkjdxtjyhysx", section
+ * "技术探索：FP8 KV Cache量化效果分析": the KV cache stored as FP8 to cut the
+ * bytes moved). The pages name no format or scaling; the reading taken here:
+ * the e4m3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 holds subnormals m/8 * 2^-6; the all-ones code S.1111.111
+ * is NaN; no infinities; largest finite 448) with one fp32 scale per KV head,
+ * symmetric (no zero point, as the nxmr.cn article's §2.2 "量化压缩的实战选择"
+ * advises for 8-bit KV): stored code = e4m3(x / scale[h]), value = code value *
+ * scale[h]. */
+
+/* e4m3 code -> double, from the format definition. */
+double or_double_from_e4m3(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return s ? -NAN : NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);              /* m/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + (double)m, e - 10);    /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* double -> e4m3 code, rounding to nearest with ties to even and saturating
+ * to +-448 (no code means infinity). The quantum is 2^(E-3) for |x| in
+ * [2^E, 2^(E+1)), E clamped below at -6 (the subnormal range has quantum
+ * 2^-9); |x| is scaled so the quantum is 1, rounded to an integer in the
+ * default rounding mode (nearest-even) and scaled back, then encoded. */
+uint8_t or_e4m3_from_double(double x) {
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x)) return (uint8_t)(sgn | 0x7F);
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sgn | 0x7E);          /* 1.75 * 2^8 */
+    if (a == 0.0) return sgn;
+    int E;
+    (void)frexp(a, &E);                                    /* a = f * 2^E, f in [0.5, 1) */
+    E -= 1;                                                /* a in [2^E, 2^(E+1)) */
+    if (E < -6) E = -6;
+    const double q = nearbyint(ldexp(a, 3 - E));           /* a / 2^(E-3), rounded */
+    const double r = ldexp(q, E - 3);                      /* the rounded magnitude */
+    if (r >= 448.0) return (uint8_t)(sgn | 0x7E);
+    if (r < ldexp(1.0, -6)) return (uint8_t)(sgn | (uint8_t)ldexp(r, 9));   /* subnormal */
+    int Er;
+    const double fr = frexp(r, &Er);                       /* r = fr * 2^Er */
+    const int e = Er - 1 + 7;                              /* biased exponent */
+    const int m = (int)(ldexp(fr, 4)) - 8;                 /* fr * 16 = 8 + m */
+    return (uint8_t)(sgn | (uint8_t)(e << 3) | (uint8_t)m);
+}
+
+void or_e4m3_from_double_array(const double* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_e4m3_from_double(x[i]);
+}
+
+void or_double_from_e4m3_array(const uint8_t* c, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = or_double_from_e4m3(c[i]);
+}
+
+/* Append into FP8 caches: as or_append, but the cache rows hold
+ *   k8 = e4m3(bf16(RoPE(k)) / k_scale[h]),  v8 = e4m3(v / v_scale[h])
+ * (the bf16 value the bf16 cache would hold, divided in double by the head's
+ * fp32 scale, then one rounding to e4m3). q_out is the bf16 RoPE(q). */
+int32_t or_append_fp8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks,
+                      const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const int32_t* positions, const int32_t* slot_mapping,
+                      const float* table, int32_t max_pos, const float* k_scale, const float* v_scale,
+                      uint16_t* q_out, uint8_t* k_cache, uint8_t* v_cache) {
+    int32_t status = 0;
+    uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t p = positions[b];
+        if (p < 0 || p >= max_pos) { status = -1; continue; }
+        or_rope_rotate(q + (int64_t)b * Hq * d, Hq, d, table, p, q_out + (int64_t)b * Hq * d);
+        const int32_t slot = slot_mapping[b];
+        if (slot < 0 || slot / OR_BLOCK >= num_blocks) { status = -1; continue; }
+        const int64_t blk = slot / OR_BLOCK, off = slot % OR_BLOCK;
+        for (int32_t h = 0; h < Hkv; ++h) {
+            const int64_t dst = ((blk * Hkv + h) * OR_BLOCK + off) * d;
+            or_rope_rotate(k + ((int64_t)b * Hkv + h) * d, 1, d, table, p, tmp);
+            const uint16_t* vr = v + ((int64_t)b * Hkv + h) * d;
+            for (int32_t i = 0; i < d; ++i) {
+                k_cache[dst + i] = or_e4m3_from_double(or_double_from_bf16(tmp[i]) / (double)k_scale[h]);
+                v_cache[dst + i] = or_e4m3_from_double(or_double_from_bf16(vr[i]) / (double)v_scale[h]);
+            }
+        }
+    }
+    free(tmp);
+    return status;
+}
+
+typedef struct {
+    int32_t B, Hq, Hkv, d, max_blocks_per_seq;
+    const uint16_t* q;
+    const uint8_t* k_cache;
+    const uint8_t* v_cache;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    double scale;
+    double* out;
+    int64_t row_begin, row_end;
+} or_attn8_job;
+
+/* Decode attention over FP8 caches: the definition of attn_row with
+ * K_t = value(k8) * k_scale[h] and V_t = value(v8) * v_scale[h], in double. */
+static void attn8_row(const or_attn8_job* a, int32_t b, int32_t j, double* s) {
+    const int32_t d = a->d, G = a->Hq / a->Hkv, h = j / G;
+    double* o = a->out + ((int64_t)b * a->Hq + j) * d;
+    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+    const int32_t n = a->context_lens[b];
+    if (n <= 0) return;
+    const uint16_t* qr = a->q + ((int64_t)b * a->Hq + j) * d;
+    const double ks = (double)a->k_scale[h], vs = (double)a->v_scale[h];
+    double m = -INFINITY;
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint8_t* kt = a->k_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        double acc = 0.0;
+        for (int32_t i = 0; i < d; ++i) acc += or_double_from_bf16(qr[i]) * (or_double_from_e4m3(kt[i]) * ks);
+        s[t] = a->scale * acc;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int32_t t = 0; t < n; ++t) {
+        const double w = exp(s[t] - m);
+        l += w;
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const uint8_t* vt = a->v_cache + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        for (int32_t i = 0; i < d; ++i) o[i] += w * (or_double_from_e4m3(vt[i]) * vs);
+    }
+    for (int32_t i = 0; i < d; ++i) o[i] /= l;
+}
+
+static void* attn8_worker(void* arg) {
+    const or_attn8_job* a = (const or_attn8_job*)arg;
+    int32_t nmax = 1;
+    for (int32_t b = 0; b < a->B; ++b)
+        if (a->context_lens[b] > nmax) nmax = a->context_lens[b];
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    for (int64_t r = a->row_begin; r < a->row_end; ++r)
+        attn8_row(a, (int32_t)(r / a->Hq), (int32_t)(r % a->Hq), s);
+    free(s);
+    return NULL;
+}
+
+/* FP8 paged decode attention, rows (b, j) on nthreads POSIX threads as in
+ * or_paged_attention. Returns the number of threads used. */
+int32_t or_paged_attention_fp8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, const uint16_t* q,
+                               const uint8_t* k_cache, const uint8_t* v_cache, const float* k_scale,
+                               const float* v_scale, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens, double scale,
+                               double* out, int32_t nthreads) {
+    const int64_t rows = (int64_t)B * Hq;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = (int32_t)(rows > 0 ? rows : 1);
+    or_attn8_job* jobs = (or_attn8_job*)malloc(sizeof(or_attn8_job) * (size_t)nthreads);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int32_t t = 0; t < nthreads; ++t) {
+        or_attn8_job* a = &jobs[t];
+        a->B = B; a->Hq = Hq; a->Hkv = Hkv; a->d = d; a->max_blocks_per_seq = max_blocks_per_seq;
+        a->q = q; a->k_cache = k_cache; a->v_cache = v_cache; a->k_scale = k_scale; a->v_scale = v_scale;
+        a->block_tables = block_tables; a->context_lens = context_lens;
+        a->scale = scale; a->out = out;
+        a->row_begin = rows * t / nthreads;
+        a->row_end = rows * (t + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        attn8_worker(&jobs[0]);
+    } else {
+        for (int32_t t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, attn8_worker, &jobs[t]);
+        for (int32_t t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    free(th);
+    free(jobs);
+    return nthreads;
+}
