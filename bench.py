@@ -451,6 +451,153 @@ def run_prefill(args, w, rank, world):
     barrier(world)
 
 
+def run_swap(args, rank, world):
+    """KV swap step on the Qwen3-8B serving pool (one layer's caches): the 16
+    least recently used sequences are swapped out to a pinned host cache and
+    back in, each direction one mi_kv_copy_blocks launch. Prints one
+    JSON line on rank 0; the reference rate is a contiguous pinned
+    cudaMemcpyAsync of the same bytes, each direction, timed in the same run."""
+    import torch
+    import paged_kv_decode_25_gb300 as mi
+    w = WORKLOADS["qwen3_8b"]
+    name = "qwen3_8b_swap"
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle.swap as osw
+        r = np.random.Generator(np.random.PCG64(1))
+        nb = 4096
+        src = r.integers(0, 1 << 16, size=(nb, w.Hkv, BLOCK, w.head_dim), dtype=np.uint16)
+        dst = np.zeros((nb, w.Hkv, BLOCK, w.head_dim), np.uint16)
+        ids = r.permutation(nb)
+        for _ in range(args.warmup):
+            osw.copy_blocks(src, ids, dst, np.arange(nb))
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            osw.copy_blocks(src, ids, dst, np.arange(nb))
+        dt = (time.perf_counter() - t0) / args.steps
+        val = 2 * src.nbytes / dt / 1e9  # K and V counted as in the GPU arm: one cache copied twice
+        sample = f"{nb} scattered blocks of one cache copied block by block with numpy, one thread"
+        print(json.dumps({
+            "impl": "reference", "metric": "KV swap GB/s", "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": name, "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
+    mi.load()
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    ctx = context_lengths(w)
+    pool = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+    setup_pool(w, pool, ctx)
+    seqs = list(range(w.B))
+    assert pool.touch(seqs[16:]) == 0  # the batch's last 48 requests were just used
+    victims = []  # LRU order: idle sequences left by the churn first, then requests 0..15
+    for _ in range(16):
+        v = pool.lru_victim(victims)
+        victims.append(v)
+    host = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq)
+    src_blocks, host_blocks = [], []
+    for v in victims:
+        st, blocks = pool.swap_out(v)
+        mi.check(st, "swap_out")
+        mi.check(host.alloc(v, len(blocks) * BLOCK), "host alloc")
+        src_blocks += blocks
+        host_blocks += [int(x) for x in mi.mi_kv_pool_seq_blocks(host.handle, v)]
+    back_blocks = []
+    for v in victims:
+        st, blocks = pool.swap_in(v)
+        mi.check(st, "swap_in")
+        back_blocks += blocks
+    n = len(src_blocks)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    device_fill_cache(w, 0, kc, vc)
+    nh = max(host_blocks) + 1
+    hk = torch.empty((nh,) + shape[1:], dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
+    s_d, h_d, b_d = i32(src_blocks), i32(host_blocks), i32(back_blocks)
+    dims = mi.dims(1, w.Hkv, w.Hkv, w.head_dim, 1, 1)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    block_bytes = w.Hkv * BLOCK * w.head_dim * 2
+    moved = 2 * 2 * n * block_bytes  # K and V, out and back
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mi.check(mi.mi_kv_copy_blocks(dims, kc, vc, w.num_blocks, s_d, hk, hv, nh, h_d, n, err, stream), "out")
+        if ev is not None:
+            ev[1].record(stream)
+        mi.check(mi.mi_kv_copy_blocks(dims, hk, hv, nh, h_d, kc, vc, w.num_blocks, b_d, n, err, stream), "in")
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    out_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    in_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    step_ms = out_ms + in_ms
+    # reference: the same bytes as one contiguous pinned copy per direction and cache
+    half = n * block_bytes
+    dflat = kc.view(-1)[: half // 2]
+    hflat = hk.view(-1)[: half // 2]
+    ce = []
+    for _ in range(3 + args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        hflat.copy_(dflat, non_blocking=True)
+        hflat.copy_(dflat, non_blocking=True)
+        e[1].record(stream)
+        dflat.copy_(hflat, non_blocking=True)
+        dflat.copy_(hflat, non_blocking=True)
+        e[2].record(stream)
+        ce.append(e)
+    torch.cuda.synchronize()
+    ce = ce[3:]
+    ce_out = sum(e[0].elapsed_time(e[1]) for e in ce) / len(ce)
+    ce_in = sum(e[1].elapsed_time(e[2]) for e in ce) / len(ce)
+    gbs = lambda ms: 2 * half / (ms * 1e-3) / 1e9  # noqa: E731
+    value = moved / (step_ms * 1e-3) / 1e9
+    peak = moved / ((ce_out + ce_in) * 1e-3) / 1e9
+    line = {
+        "metric": "KV swap GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "victims": 16, "blocks": n, "bytes_per_direction": 2 * half,
+                   "from": "qwen3_8b pool after churn: the 16 least recently used sequences, one layer",
+                   "host": "pinned (cudaHostAlloc through torch), read and written in place by the kernel"},
+        "swap_out_gbs": gbs(out_ms), "swap_in_gbs": gbs(in_ms),
+        "roofline": {"bound": "link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "peak_kind": "measured in this run: contiguous pinned cudaMemcpyAsync "
+                                                  "of the same bytes, each direction",
+                     "peak_out_gbs": gbs(ce_out), "peak_in_gbs": gbs(ce_in)},
+        "cpu_baseline": None,
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": moved // 2, "d2h_bytes_per_step": moved // 2,
+                "note": "the swap is itself host<->device traffic"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- main -----
 
 def dist_setup(args):
@@ -482,7 +629,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--workload", default="qwen3_8b", choices=list(WORKLOADS) + list(PREFILL_WORKLOADS))
+    ap.add_argument("--workload", default="qwen3_8b",
+                    choices=list(WORKLOADS) + list(PREFILL_WORKLOADS) + ["qwen3_8b_swap"])
     ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
@@ -493,6 +641,9 @@ def main():
     rank, world, local = dist_setup(args)
     if args.workload in PREFILL_WORKLOADS:
         run_prefill(args, PREFILL_WORKLOADS[args.workload], rank, world)
+        return
+    if args.workload == "qwen3_8b_swap":
+        run_swap(args, rank, world)
         return
     w = WORKLOADS[args.workload]
     if args.layers is not None:

@@ -151,6 +151,39 @@ typedef enum mi_admit_decision {
 mi_status mi_kv_pool_admission(const mi_kv_pool* pool, int32_t running_decodes, int32_t hard_bp,
                                int32_t soft_bp, mi_admit_decision* out);
 
+/* ---- KV swap to host memory with LRU eviction (NJU course brief, optional
+ * task 3 "KV Cache Offloading": inactive KV blocks move to CPU memory and come
+ * back when needed, under an eviction policy such as LRU).
+ * A sequence is resident (it holds a table) or swapped out (it holds no
+ * block; its token count is kept). Swapped-out sequences are unknown to
+ * batch_meta, token_slots and seq_blocks (MI_ERR_UNKNOWN_SEQ / -1), rejected
+ * by alloc (MI_ERR_INVALID_ARG) and forgotten by free. The pool keeps a use
+ * clock: every successful alloc, swap_in and touch call advances it by one
+ * and stamps the sequences it names. */
+
+/* Mark n resident sequences as used now. MI_ERR_UNKNOWN_SEQ (and no change)
+ * if one is not resident. */
+mi_status mi_kv_pool_touch(mi_kv_pool* pool, const int32_t* seq_ids, int32_t n);
+
+/* The resident sequence with the oldest use stamp that holds at least one
+ * block and is not among exclude[0..n_exclude) (ties: lower id), or -1. */
+int32_t mi_kv_pool_lru_victim(const mi_kv_pool* pool, const int32_t* exclude, int32_t n_exclude);
+
+/* Swap out a resident sequence: its table (in order) goes to
+ * blocks_out[0..*n_out) and its blocks return to the free list as
+ * mi_kv_pool_free returns them. The caller copies those blocks' contents
+ * out (mi_kv_copy_blocks) before anything can reuse them. MI_ERR_INVALID_ARG
+ * (no change) if max_out is below the block count. */
+mi_status mi_kv_pool_swap_out(mi_kv_pool* pool, int32_t seq_id, int32_t* blocks_out, int32_t max_out,
+                              int32_t* n_out);
+
+/* Swap a sequence back in: pop ceil(tokens/16) blocks (as alloc pops them)
+ * into its table and blocks_out[0..*n_out); the caller copies its contents
+ * back into them. MI_ERR_OUT_OF_BLOCKS leaves the pool unchanged;
+ * MI_ERR_UNKNOWN_SEQ if it is not swapped out. */
+mi_status mi_kv_pool_swap_in(mi_kv_pool* pool, int32_t seq_id, int32_t* blocks_out, int32_t max_out,
+                             int32_t* n_out);
+
 /* Copy of one sequence's table into out[0..max_out) (host); returns the
  * number of blocks it holds, or -1 if unknown. */
 int32_t mi_kv_pool_seq_blocks(const mi_kv_pool* pool, int32_t seq_id, int32_t* out,
@@ -279,6 +312,26 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
                                      const int32_t* block_tables, const int32_t* context_lens,
                                      const int32_t* query_start, float scale, void* out,
                                      int32_t* dev_err, mi_stream_t stream);
+
+/* Block copies between two paged caches (the data movement of a swap):
+ *   dst_k[dst_blocks[i]] = src_k[src_blocks[i]],
+ *   dst_v[dst_blocks[i]] = src_v[src_blocks[i]]     for i < n,
+ * a block being all Hkv heads' 16 token rows ([Hkv][16][head_dim] bf16; dims
+ * supplies Hkv, head_dim and block_size; its other fields are not used).
+ * src_* hold src_num_blocks blocks, dst_* dst_num_blocks. Each of the four
+ * caches may be device memory or pinned host memory (cudaHostAlloc or
+ * cudaHostRegister: the kernel reads and writes it in place); all 16-byte
+ * aligned. src_blocks and dst_blocks are int32 [n] arrays the device can read
+ * (device or pinned host). Pinned host pointers are translated to their
+ * device addresses; pageable host memory is refused (MI_ERR_INVALID_ARG).
+ * Destination blocks must be distinct and must not overlap the source
+ * blocks. A pair with an id out of range is skipped (MI_DEVERR_BAD_BLOCK).
+ * One kernel launch on `stream`; host buffers must stay pinned and untouched
+ * by the host until it completes. */
+mi_status mi_kv_copy_blocks(const mi_dims* dims, const void* src_k, const void* src_v,
+                            int32_t src_num_blocks, const int32_t* src_blocks, void* dst_k, void* dst_v,
+                            int32_t dst_num_blocks, const int32_t* dst_blocks, int32_t n,
+                            int32_t* dev_err, mi_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Allocation-free attention. The pages have no counterpart to this entry

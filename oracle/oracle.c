@@ -466,9 +466,10 @@ void or_double_from_e4m3_array(const uint8_t* c, int64_t n, double* out) {
 }
 
 /* Append into FP8 caches: as or_append, but the cache rows hold
- *   k8 = e4m3(bf16(RoPE(k)) / k_scale[h]),  v8 = e4m3(v / v_scale[h])
- * (the bf16 value the bf16 cache would hold, divided in double by the head's
- * fp32 scale, then one rounding to e4m3). q_out is the bf16 RoPE(q). */
+ *   k8 = e4m3(fp32(bf16(RoPE(k)) / k_scale[h])),  v8 = e4m3(fp32(v / v_scale[h]))
+ * (the bf16 value the bf16 cache would hold, divided by the head's fp32 scale
+ * in IEEE single precision, then rounded to e4m3). q_out is the bf16
+ * RoPE(q). */
 int32_t or_append_fp8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks,
                       const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       const int32_t* positions, const int32_t* slot_mapping,
@@ -488,8 +489,10 @@ int32_t or_append_fp8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num
             or_rope_rotate(k + ((int64_t)b * Hkv + h) * d, 1, d, table, p, tmp);
             const uint16_t* vr = v + ((int64_t)b * Hkv + h) * d;
             for (int32_t i = 0; i < d; ++i) {
-                k_cache[dst + i] = or_e4m3_from_double(or_double_from_bf16(tmp[i]) / (double)k_scale[h]);
-                v_cache[dst + i] = or_e4m3_from_double(or_double_from_bf16(vr[i]) / (double)v_scale[h]);
+                const float yk = (float)or_double_from_bf16(tmp[i]) / k_scale[h];
+                const float yv = (float)or_double_from_bf16(vr[i]) / v_scale[h];
+                k_cache[dst + i] = or_e4m3_from_double((double)yk);
+                v_cache[dst + i] = or_e4m3_from_double((double)yv);
             }
         }
     }

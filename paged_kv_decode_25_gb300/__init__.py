@@ -32,7 +32,8 @@ MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
 EXPORTS = (
     "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc",
     "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_token_slots",
-    "mi_kv_pool_admission",
+    "mi_kv_pool_admission", "mi_kv_pool_touch", "mi_kv_pool_lru_victim", "mi_kv_pool_swap_out",
+    "mi_kv_pool_swap_in", "mi_kv_copy_blocks",
     "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
@@ -74,6 +75,11 @@ def load():
             "mi_kv_pool_batch_meta": ([P, P, i32, P, P, P], i32),
             "mi_kv_pool_token_slots": ([P, i32, i32, i32, P], i32),
             "mi_kv_pool_admission": ([P, i32, i32, i32, P], i32),
+            "mi_kv_pool_touch": ([P, P, i32], i32),
+            "mi_kv_pool_lru_victim": ([P, P, i32], i32),
+            "mi_kv_pool_swap_out": ([P, i32, P, i32, P], i32),
+            "mi_kv_pool_swap_in": ([P, i32, P, i32, P], i32),
+            "mi_kv_copy_blocks": ([dims_p, P, P, i32, P, P, P, i32, P, i32, P, P], i32),
             "mi_kv_pool_seq_blocks": ([P, i32, P, i32], i32),
             "mi_rope_table": ([f64, i32, i32, P], i32),
             "mi_paged_kv_append": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P], i32),
@@ -187,6 +193,33 @@ def mi_kv_pool_admission(handle, running_decodes, hard_bp=MI_ADMIT_HARD_BP_DEFAU
     return st, int(out.value)
 
 
+def mi_kv_pool_touch(handle, seq_ids):
+    ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    return load().mi_kv_pool_touch(handle, _ptr(ids), int(ids.shape[0]))
+
+
+def mi_kv_pool_lru_victim(handle, exclude=()):
+    ex = np.ascontiguousarray(exclude, dtype=np.int32)
+    return int(load().mi_kv_pool_lru_victim(handle, _ptr(ex) if ex.size else None, int(ex.size)))
+
+
+def _swap(fn, handle, seq_id, max_out):
+    out = np.empty(max(int(max_out), 1), np.int32)
+    n = ctypes.c_int32(0)
+    st = fn(handle, int(seq_id), _ptr(out), int(max_out), ctypes.byref(n))
+    return st, out[:n.value].copy()
+
+
+def mi_kv_pool_swap_out(handle, seq_id, max_out=1 << 20):
+    """Returns (status, the sequence's former blocks)."""
+    return _swap(load().mi_kv_pool_swap_out, handle, seq_id, max_out)
+
+
+def mi_kv_pool_swap_in(handle, seq_id, max_out=1 << 20):
+    """Returns (status, the sequence's new blocks)."""
+    return _swap(load().mi_kv_pool_swap_in, handle, seq_id, max_out)
+
+
 def mi_kv_pool_seq_blocks(handle, seq_id, max_out=1 << 20):
     n = load().mi_kv_pool_seq_blocks(handle, int(seq_id), None, 0)
     if n < 0:
@@ -224,6 +257,20 @@ class Pool:
         st, dec = mi_kv_pool_admission(self.handle, running_decodes, hard_bp, soft_bp)
         check(st, "mi_kv_pool_admission")
         return dec
+
+    def touch(self, seq_ids):
+        return mi_kv_pool_touch(self.handle, seq_ids)
+
+    def lru_victim(self, exclude=()):
+        return mi_kv_pool_lru_victim(self.handle, exclude)
+
+    def swap_out(self, seq):
+        st, blocks = mi_kv_pool_swap_out(self.handle, seq)
+        return st, [int(b) for b in blocks]
+
+    def swap_in(self, seq):
+        st, blocks = mi_kv_pool_swap_in(self.handle, seq)
+        return st, [int(b) for b in blocks]
 
     def batch_meta(self, seq_ids):
         st, bt, cl, sl = mi_kv_pool_batch_meta(self.handle, seq_ids, self.max_blocks_per_seq)
@@ -287,6 +334,13 @@ def mi_paged_prefill_attention(d: MiDims, total_q, max_query_len, q, k_cache, v_
                                              _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                              _ptr(context_lens), _ptr(query_start), float(scale), _ptr(out),
                                              _ptr(dev_err), _stream(stream))
+
+
+def mi_kv_copy_blocks(d: MiDims, src_k, src_v, src_num_blocks, src_blocks, dst_k, dst_v, dst_num_blocks,
+                      dst_blocks, n, dev_err=None, stream=None):
+    return load().mi_kv_copy_blocks(ctypes.byref(d), _ptr(src_k), _ptr(src_v), int(src_num_blocks),
+                                    _ptr(src_blocks), _ptr(dst_k), _ptr(dst_v), int(dst_num_blocks),
+                                    _ptr(dst_blocks), int(n), _ptr(dev_err), _stream(stream))
 
 
 def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale, out,

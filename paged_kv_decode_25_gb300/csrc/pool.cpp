@@ -21,7 +21,12 @@ struct mi_kv_pool {
     std::vector<int32_t> free_stack;            // back() is the next block handed out
     std::vector<std::vector<int32_t>> tables;   // per sequence id
     std::vector<int32_t> tokens;                // per sequence id
-    std::vector<uint8_t> live;                  // per sequence id
+    std::vector<uint8_t> live;                  // per sequence id: resident (holds its table)
+    std::vector<uint8_t> swapped;               // per sequence id: blocks swapped out, tokens kept
+    std::vector<int64_t> last_use;              // per sequence id: clock of the last use
+    int64_t clock = 0;                          // LRU use counter
+
+    void use(int32_t seq) { last_use[(size_t)seq] = clock; }
 };
 
 extern "C" const char* mi_status_string(mi_status s) {
@@ -68,6 +73,8 @@ extern "C" mi_status mi_kv_pool_create(int32_t num_blocks, int32_t block_size, i
         p->tables.resize((size_t)max_seqs);
         p->tokens.assign((size_t)max_seqs, 0);
         p->live.assign((size_t)max_seqs, 0);
+        p->swapped.assign((size_t)max_seqs, 0);
+        p->last_use.assign((size_t)max_seqs, 0);
     } catch (...) {
         delete p;
         return MI_ERR_INVALID_ARG;
@@ -80,6 +87,7 @@ extern "C" void mi_kv_pool_destroy(mi_kv_pool* pool) { delete pool; }
 
 extern "C" mi_status mi_kv_pool_alloc(mi_kv_pool* p, int32_t seq, int32_t num_tokens) {
     if (!p || seq < 0 || (size_t)seq >= p->tables.size() || num_tokens < 0) return MI_ERR_INVALID_ARG;
+    if (p->swapped[(size_t)seq]) return MI_ERR_INVALID_ARG;  // swap it in first
     std::vector<int32_t>& t = p->tables[(size_t)seq];
     if (p->live[(size_t)seq] && num_tokens < p->tokens[(size_t)seq]) return MI_ERR_INVALID_ARG;
     const int64_t need = ((int64_t)num_tokens + p->block_size - 1) / p->block_size;
@@ -92,11 +100,18 @@ extern "C" mi_status mi_kv_pool_alloc(mi_kv_pool* p, int32_t seq, int32_t num_to
     }
     p->tokens[(size_t)seq] = num_tokens;
     p->live[(size_t)seq] = 1;
+    ++p->clock;
+    p->use(seq);
     return MI_OK;
 }
 
 extern "C" mi_status mi_kv_pool_free(mi_kv_pool* p, int32_t seq) {
     if (!p) return MI_ERR_INVALID_ARG;
+    if (seq >= 0 && (size_t)seq < p->tables.size() && p->swapped[(size_t)seq]) {
+        p->swapped[(size_t)seq] = 0;  // nothing on the device: just forget it
+        p->tokens[(size_t)seq] = 0;
+        return MI_OK;
+    }
     if (seq < 0 || (size_t)seq >= p->tables.size() || !p->live[(size_t)seq]) return MI_ERR_UNKNOWN_SEQ;
     std::vector<int32_t>& t = p->tables[(size_t)seq];
     for (int32_t b : t) p->free_stack.push_back(b);
@@ -186,5 +201,69 @@ extern "C" mi_status mi_kv_pool_admission(const mi_kv_pool* p, int32_t running_d
         *out = MI_ADMIT_SOFT_BRAKE;
     else
         *out = MI_ADMIT_PROCEED;
+    return MI_OK;
+}
+
+// ---------------------------------------------------------------- swap ----
+
+extern "C" mi_status mi_kv_pool_touch(mi_kv_pool* p, const int32_t* seq_ids, int32_t n) {
+    if (!p || n < 0 || (n > 0 && !seq_ids)) return MI_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t s = seq_ids[i];
+        if (s < 0 || (size_t)s >= p->tables.size() || !p->live[(size_t)s]) return MI_ERR_UNKNOWN_SEQ;
+    }
+    ++p->clock;
+    for (int32_t i = 0; i < n; ++i) p->use(seq_ids[i]);
+    return MI_OK;
+}
+
+extern "C" int32_t mi_kv_pool_lru_victim(const mi_kv_pool* p, const int32_t* exclude, int32_t n_exclude) {
+    if (!p || n_exclude < 0 || (n_exclude > 0 && !exclude)) return -1;
+    int32_t best = -1;
+    for (size_t s = 0; s < p->tables.size(); ++s) {
+        if (!p->live[s] || p->tables[s].empty()) continue;
+        bool skip = false;
+        for (int32_t i = 0; i < n_exclude && !skip; ++i) skip = exclude[i] == (int32_t)s;
+        if (skip) continue;
+        if (best < 0 || p->last_use[s] < p->last_use[(size_t)best]) best = (int32_t)s;  // ties: lower id
+    }
+    return best;
+}
+
+extern "C" mi_status mi_kv_pool_swap_out(mi_kv_pool* p, int32_t seq, int32_t* blocks_out, int32_t max_out,
+                                         int32_t* n_out) {
+    if (!p || max_out < 0) return MI_ERR_INVALID_ARG;
+    if (seq < 0 || (size_t)seq >= p->tables.size() || !p->live[(size_t)seq]) return MI_ERR_UNKNOWN_SEQ;
+    std::vector<int32_t>& t = p->tables[(size_t)seq];
+    if ((int64_t)t.size() > max_out || (!t.empty() && !blocks_out)) return MI_ERR_INVALID_ARG;
+    for (size_t i = 0; i < t.size(); ++i) {
+        blocks_out[i] = t[i];
+        p->free_stack.push_back(t[i]);
+    }
+    if (n_out) *n_out = (int32_t)t.size();
+    t.clear();
+    p->live[(size_t)seq] = 0;
+    p->swapped[(size_t)seq] = 1;
+    return MI_OK;
+}
+
+extern "C" mi_status mi_kv_pool_swap_in(mi_kv_pool* p, int32_t seq, int32_t* blocks_out, int32_t max_out,
+                                        int32_t* n_out) {
+    if (!p || max_out < 0) return MI_ERR_INVALID_ARG;
+    if (seq < 0 || (size_t)seq >= p->tables.size() || !p->swapped[(size_t)seq]) return MI_ERR_UNKNOWN_SEQ;
+    const int64_t need = ((int64_t)p->tokens[(size_t)seq] + p->block_size - 1) / p->block_size;
+    if (need > max_out || (need > 0 && !blocks_out)) return MI_ERR_INVALID_ARG;
+    if (need > (int64_t)p->free_stack.size()) return MI_ERR_OUT_OF_BLOCKS;
+    std::vector<int32_t>& t = p->tables[(size_t)seq];
+    for (int64_t i = 0; i < need; ++i) {
+        t.push_back(p->free_stack.back());
+        p->free_stack.pop_back();
+        blocks_out[i] = t.back();
+    }
+    if (n_out) *n_out = (int32_t)need;
+    p->swapped[(size_t)seq] = 0;
+    p->live[(size_t)seq] = 1;
+    ++p->clock;
+    p->use(seq);
     return MI_OK;
 }

@@ -22,11 +22,12 @@
 //     softmax on the accumulator fragments; the probabilities are repacked in
 //     place as bf16 A fragments and O[16 x HD] += P . V with V read by
 //     ldmatrix.trans.
-//   * Grid: one CTA per (request r, KV head h, row tile from the end k), k the
-//     fastest index: the CTAs resident at any time share the K/V of a few
-//     (request, head) pairs through L2, and each pair's tiles start with the
-//     one that reads the most keys. Tiles past a request's last row exit at
-//     once.
+//   * Grid: one CTA per (request r, KV head h, row tile k counted from the
+//     request's end). Tiles come in groups of 8 consecutive k per (r, h), and
+//     the groups run k-group by k-group over all (r, h): the hardware starts
+//     the tiles with the most keys first, as a longest-first schedule wants,
+//     while the 8 tiles of a group read the same K/V through L2 at about the
+//     same time. Tiles past a request's last row exit at once.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -43,6 +44,7 @@ constexpr int kStageBlocks = 4;                 // 16-token blocks per stage: 64
 constexpr int kSubBlocks = 2;                   // blocks per softmax sub-step: 32 keys
 constexpr int kPStages = 3;
 constexpr int kMaxGroup = 8;
+constexpr int kTileGroup = 8;                   // row tiles of one (request, head) launched together
 
 struct PrefillParams {
     const uint16_t* q;             // [T][Hq][HD], RoPE applied
@@ -52,7 +54,6 @@ struct PrefillParams {
     uint16_t* out;                 // [T][Hq][HD]
     int32_t* dev_err;
     int R, Hq, Hkv, G, num_blocks, mbps, T, max_q;
-    int tiles_max;                 // row tiles of the longest request
     float sl2;                     // scale * log2(e)
 };
 
@@ -100,10 +101,12 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
     pdl_trigger();
 
     // ------------------------------------------------------- work item ----
-    const int k = blockIdx.x % p.tiles_max;
-    const int rest = blockIdx.x / p.tiles_max;
-    const int h = rest % p.Hkv;
-    const int r = rest / p.Hkv;
+    const int kw = blockIdx.x % kTileGroup;
+    const int rest0 = blockIdx.x / kTileGroup;
+    const int h = rest0 % p.Hkv;
+    const int rest = rest0 / p.Hkv;
+    const int r = rest % p.R;
+    const int k = (rest / p.R) * kTileGroup + kw;
     const bool reporter = k == 0 && h == 0 && threadIdx.x == 0;  // one error report per request
     const int q0 = __ldg(p.query_start + r), q1 = __ldg(p.query_start + r + 1);
     const int m = q1 - q0;
@@ -428,7 +431,7 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
         return MI_ERR_INVALID_ARG;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     const long long tiles_max = ((long long)max_query_len * G + kPRows - 1) / kPRows;
-    const long long grid = tiles_max * D.B * D.Hkv;
+    const long long grid = (tiles_max + kTileGroup - 1) / kTileGroup * kTileGroup * D.B * D.Hkv;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
 
     int smem = 0;
@@ -452,7 +455,6 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
     p.mbps = D.max_blocks_per_seq;
     p.T = total_q;
     p.max_q = max_query_len;
-    p.tiles_max = (int)tiles_max;
     p.sl2 = scale * 1.4426950408889634f;
     const cudaError_t e =
         HD == 64 ? launch_pdl(prefill_kernel<64>, (int)grid, (kPWarps + 1) * 32, smem, (cudaStream_t)stream, tk, tv, p)

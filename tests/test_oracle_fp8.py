@@ -84,8 +84,11 @@ def test_append_fp8_is_bf16_append_then_quantise():
     kc8 = np.zeros((nb, Hkv, BS, d), np.uint8); vc8 = kc8.copy()
     q8, st8 = oracle.append_fp8(q, k, v, pos, slots, table, ks, vs, kc8, vc8)
     assert st == st8 == 0 and np.array_equal(q16, q8)
-    want_k = oracle.e4m3_from_f64(oracle.bf16_to_f64(kc16) / ks[None, :, None, None].astype(np.float64))
-    want_v = oracle.e4m3_from_f64(oracle.bf16_to_f64(vc16) / vs[None, :, None, None].astype(np.float64))
+    # the quotient is taken in IEEE single precision (numpy float32 division)
+    want_k = oracle.e4m3_from_f64((oracle.bf16_to_f64(kc16).astype(np.float32) / ks[None, :, None, None])
+                                  .astype(np.float64))
+    want_v = oracle.e4m3_from_f64((oracle.bf16_to_f64(vc16).astype(np.float32) / vs[None, :, None, None])
+                                  .astype(np.float64))
     touched = np.zeros(nb * BS, bool); touched[slots] = True
     touched = touched.reshape(nb, BS)[:, None, :, None]
     assert np.array_equal(np.where(touched, kc8, 0), np.where(touched, want_k, 0))
