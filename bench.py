@@ -48,20 +48,47 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ---------------------------------------------------------------- bytes ----
 
-def attention_bytes(w, lens):
-    """Algorithmic bytes of one attention call (one layer)."""
+def attention_bytes(w, lens, kvb=2):
+    """Algorithmic bytes of one attention call (one layer); kvb = bytes per
+    cached element (2 for bf16, 1 for e4m3)."""
     lens = np.maximum(np.asarray(lens, np.int64), 0)
-    kv = int(lens.sum()) * w.Hkv * w.head_dim * 2 * 2
+    kv = int(lens.sum()) * w.Hkv * w.head_dim * kvb * 2
     qo = 2 * w.B * w.Hq * w.head_dim * 2
     tables = 4 * int(np.sum(-(-lens // BLOCK))) + 4 * w.B
     return kv + qo + tables
 
 
-def append_bytes(w):
-    """Algorithmic bytes of one append call (one layer)."""
+def append_bytes(w, kvb=2):
+    """Algorithmic bytes of one append call (one layer): new q, k, v read;
+    q_out and the cache rows (kvb bytes per element) written; table rows,
+    positions and slots read."""
     new = w.B * (w.Hq + 2 * w.Hkv) * w.head_dim * 2
+    written = w.B * w.Hq * w.head_dim * 2 + w.B * 2 * w.Hkv * w.head_dim * kvb
     rope_rows = w.B * (w.head_dim // 2) * 8
-    return 2 * new + rope_rows + 8 * w.B
+    return new + written + rope_rows + 8 * w.B
+
+
+def fp8_scales(w):
+    """Per-KV-head e4m3 scales: about 3..6 standard deviations of the N(0,1)
+    values at e4m3's largest finite value, 448 (seeded)."""
+    r = np.random.Generator(np.random.PCG64([w.seed, 500]))
+    return (((3.0 + 3.0 * r.random(w.Hkv)) / 448.0).astype(np.float32),
+            ((3.0 + 3.0 * r.random(w.Hkv)) / 448.0).astype(np.float32))
+
+
+def device_fill_fp8(w, layer, k_cache, v_cache, ks, vs):
+    """e4m3 caches (uint8 tensors) of N(0,1) values over the per-head scales,
+    clamped to +-448 (torch's e4m3 cast turns overflow into NaN)."""
+    import torch
+    g = torch.Generator(device=k_cache.device)
+    g.manual_seed(w.seed * 1000 + layer)
+    for t, sc in ((k_cache, ks), (v_cache, vs)):
+        inv = torch.from_numpy(1.0 / sc).to(t.device)
+        for blk in range(0, t.shape[0], 4096):
+            e = min(t.shape[0], blk + 4096)
+            x = torch.randn((e - blk,) + tuple(t.shape[1:]), generator=g, device=t.device)
+            x.mul_(inv[None, :, None, None]).clamp_(-448.0, 448.0)
+            t[blk:e].copy_(x.to(torch.float8_e4m3fn).view(torch.uint8))
 
 
 def describe(w):
@@ -632,6 +659,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b",
                     choices=list(WORKLOADS) + list(PREFILL_WORKLOADS) + ["qwen3_8b_swap"])
     ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV cache element type of the decode step (fp8: e4m3 with per-head scales)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default: the workload's); fewer only for small profiling runs")
@@ -662,6 +691,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     variant = {"default": mi.MI_ATTN_DEFAULT, "mma": mi.MI_ATTN_MMA, "fma": mi.MI_ATTN_FMA}[args.variant]
+    fp8 = args.kv == "fp8"
+    kvb = 1 if fp8 else 2
+    if fp8 and not w.device_fill:
+        raise SystemExit("--kv fp8 is measured on the device-filled serving workload")
 
     # ---- workload: pool history, caches, new-token values (one replica per rank)
     ctx = context_lengths(w)
@@ -675,10 +708,14 @@ def main():
     d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
     shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
     caches = []
+    ks_h, vs_h = fp8_scales(w)
+    ks_d, vs_d = torch.from_numpy(ks_h).to(device), torch.from_numpy(vs_h).to(device)
     for layer in range(w.layers):
-        kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        kc = torch.empty(shape, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
         vc = torch.empty_like(kc)
-        if w.device_fill:
+        if fp8:
+            device_fill_fp8(w, layer + 1000 * rank, kc, vc, ks_h, vs_h)
+        elif w.device_fill:
             device_fill_cache(w, layer + 1000 * rank, kc, vc)
         else:
             hk, hv = history_cache(w, layer, bt, ctx)
@@ -708,13 +745,23 @@ def main():
     def step(ev=None):
         for layer in range(w.layers):
             kc, vc = caches[layer]
-            mi.check(mi.mi_paged_kv_append(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
-                                           max_pos, qo_all[layer], kc, vc, err, stream), "append")
+            if fp8:
+                mi.check(mi.mi_paged_kv_append_fp8(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
+                                                   max_pos, qo_all[layer], kc, vc, ks_d, vs_d, err, stream),
+                         "append")
+            else:
+                mi.check(mi.mi_paged_kv_append(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
+                                               max_pos, qo_all[layer], kc, vc, err, stream), "append")
             if ev is not None:
                 ev[layer][0].record(stream)
-            mi.check(mi.mi_paged_decode_attention_variant(d, qo_all[layer], kc, vc, bt_d, cl_d, w.scale,
-                                                          out_all[layer], ws, variant=variant, dev_err=err,
-                                                          stream=stream), "attention")
+            if fp8:
+                mi.check(mi.mi_paged_decode_attention_fp8(d, qo_all[layer], kc, vc, ks_d, vs_d, bt_d, cl_d, w.scale,
+                                                          out_all[layer], ws, dev_err=err, stream=stream),
+                         "attention")
+            else:
+                mi.check(mi.mi_paged_decode_attention_variant(d, qo_all[layer], kc, vc, bt_d, cl_d, w.scale,
+                                                              out_all[layer], ws, variant=variant, dev_err=err,
+                                                              stream=stream), "attention")
             if ev is not None:
                 ev[layer][1].record(stream)
 
@@ -744,12 +791,12 @@ def main():
     attn_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
                for layer in range(w.layers)]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    a_bytes = attention_bytes(w, cl)
-    step_bytes = w.layers * (a_bytes + append_bytes(w))
+    a_bytes = attention_bytes(w, cl, kvb)
+    step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     achieved = a_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name + ("_fp8" if fp8 else ""))
 
     # ---- end to end: real decode steps from host buffers through the C ABI
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
@@ -779,7 +826,7 @@ def main():
         step()
         h_out.copy_(out_all, non_blocking=True)
         torch.cuda.synchronize()
-        e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy()) + append_bytes(w))
+        e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy(), kvb) + append_bytes(w, kvb))
 
     for _ in range(min(args.warmup, 2)):
         e2e_step()
@@ -803,8 +850,9 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(describe(w), variant=args.variant),
+        "vs_baseline": None, "dtype": "fp8e4m3 KV, bf16 q/out" if fp8 else "bf16", "data": "synthetic",
+        "config": dict(describe(w), variant=args.variant if not fp8 else "fp8 tensor-core tile",
+                       kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16"),
         "steps_per_s": 1e3 / step_ms * world,
         "hbm_frac_step": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -60,6 +60,7 @@ typedef enum mi_status {
 #define MI_DEVERR_BAD_POS      0x4 /* position outside [0, max_pos) */
 #define MI_DEVERR_BAD_CONTEXT  0x8 /* context length above max_blocks_per_seq * block_size */
 #define MI_DEVERR_TIMEOUT      0x10 /* a staged copy did not land within the wait limit */
+#define MI_DEVERR_BAD_SCALE    0x40 /* FP8 append: a KV head's scale is not a positive finite number */
 #define MI_DEVERR_BAD_QUERY    0x20 /* prefill: query_start not within [0, total_q] and ascending,
                                        a request longer than max_query_len, or more
                                        new tokens than context */
@@ -283,6 +284,40 @@ mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
                                             void* workspace, size_t workspace_bytes,
                                             int32_t* dev_err, mi_stream_t stream,
                                             mi_attn_variant variant, int32_t ctas);
+
+/* ---- FP8 (e4m3) KV cache (GitLink project report "mxdyymxgxtlkjdxtjyhysx",
+ * section "技术探索：FP8 KV Cache量化效果分析": the KV cache held in FP8 to cut
+ * the bytes each decode step moves). Layout as the bf16 caches with one byte
+ * per element: [num_blocks][Hkv][16][head_dim] e4m3 (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111 = NaN,
+ * largest finite 448). Each KV head h has fp32 scales k_scale[h], v_scale[h]
+ * (device arrays [Hkv]): a cached code c stands for value(c) * scale[h]. */
+
+/* mi_paged_kv_append into FP8 caches. q_out is as in mi_paged_kv_append; the
+ * cache rows of the new token hold, for every element,
+ *   k8 = e4m3(fp32(bf16(RoPE(k)) / k_scale[h])),  v8 = e4m3(fp32(v / v_scale[h]))
+ * where bf16(RoPE(k)) is exactly what mi_paged_kv_append would store, the
+ * quotient is an IEEE single-precision division, and e4m3() rounds to nearest
+ * with ties to even, values beyond +-448 saturating to +-448. A scale that is
+ * not a positive finite number skips that head's cache writes
+ * (MI_DEVERR_BAD_SCALE). */
+mi_status mi_paged_kv_append_fp8(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                 const int32_t* positions, const int32_t* slot_mapping,
+                                 const float* rope_cos_sin, int32_t max_pos, void* q_out, void* k_cache,
+                                 void* v_cache, const float* k_scale, const float* v_scale,
+                                 int32_t* dev_err, mi_stream_t stream);
+
+/* mi_paged_decode_attention over FP8 caches: the same definition with
+ * K_t = value(k8_t) * k_scale[h] and V_t = value(v8_t) * v_scale[h]. The
+ * products run on tensor cores in f16 (every e4m3 value is an f16 value; q is
+ * converted to f16 with one rounding, so |q| must stay below 65504), with an
+ * fp32 online softmax, as the bf16 call. Same workspace
+ * (mi_paged_decode_workspace_bytes), errors and guarantees. */
+mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, const void* k_cache,
+                                        const void* v_cache, const float* k_scale, const float* v_scale,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        float scale, void* out, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_err, mi_stream_t stream);
 
 /* Causal paged GQA attention for a prefill or chunked-prefill batch (NJU
  * course brief §2.1, the prefill stage of the prefill + decode loop; mini-infer

@@ -23,7 +23,7 @@ _lib = None
 MI_OK, MI_ERR_INVALID_ARG, MI_ERR_OUT_OF_BLOCKS, MI_ERR_UNKNOWN_SEQ = 0, 1, 2, 3
 MI_ERR_UNSUPPORTED, MI_ERR_CUDA, MI_ERR_DEVICE_BOUNDS, MI_ERR_TIMEOUT = 4, 5, 6, 7
 MI_DEVERR_BAD_BLOCK, MI_DEVERR_BAD_SLOT, MI_DEVERR_BAD_POS = 0x1, 0x2, 0x4
-MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT, MI_DEVERR_BAD_QUERY = 0x8, 0x10, 0x20
+MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT, MI_DEVERR_BAD_QUERY, MI_DEVERR_BAD_SCALE = 0x8, 0x10, 0x20, 0x40
 MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
 MI_ADMIT_PROCEED, MI_ADMIT_SOFT_BRAKE, MI_ADMIT_HARD_BRAKE = 0, 1, 2
 MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
@@ -37,6 +37,7 @@ EXPORTS = (
     "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
+    "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
     "mi_paged_prefill_attention", "mi_paged_decode_attention_noalloc",
 )
 MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -88,6 +89,9 @@ def load():
             "mi_paged_decode_attention_variant": (
                 [dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P, i32, i32], i32),
             "mi_paged_prefill_attention": ([dims_p, i32, i32, P, P, P, P, P, P, f32, P, P, P], i32),
+            "mi_paged_kv_append_fp8": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P, P, P], i32),
+            "mi_paged_decode_attention_fp8": (
+                [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
@@ -326,6 +330,23 @@ def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tabl
         ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream),
         int(variant), int(ctas))
+
+
+def mi_paged_kv_append_fp8(d: MiDims, q, k, v, positions, slot_mapping, rope_cos_sin, max_pos, q_out,
+                           k_cache, v_cache, k_scale, v_scale, dev_err=None, stream=None):
+    return load().mi_paged_kv_append_fp8(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(positions),
+                                         _ptr(slot_mapping), _ptr(rope_cos_sin), int(max_pos), _ptr(q_out),
+                                         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(dev_err), _stream(stream))
+
+
+def mi_paged_decode_attention_fp8(d: MiDims, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                  scale, out, workspace, workspace_bytes=None, dev_err=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return load().mi_paged_decode_attention_fp8(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                                _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
+                                                int(wb), _ptr(dev_err), _stream(stream))
 
 
 def mi_paged_prefill_attention(d: MiDims, total_q, max_query_len, q, k_cache, v_cache, block_tables,

@@ -44,17 +44,34 @@ struct AppendParams {
     const int32_t* slot_mapping;
     const float2* rope;  // [max_pos][d/2] (cos, sin)
     uint16_t* q_out;
-    uint16_t* k_cache;
+    uint16_t* k_cache;             // bf16 caches
     uint16_t* v_cache;
+    uint8_t* k_cache8;             // e4m3 caches (FP8 append)
+    uint8_t* v_cache8;
+    const float* k_scale;          // [Hkv] e4m3 quantisation scales
+    const float* v_scale;
     int32_t* dev_err;
     int Hq, Hkv, d, num_blocks, max_pos;
 };
+
+// Eight bf16 values (packed pairs) / scale in IEEE single precision, then to
+// e4m3 (nearest-even, saturating): eight codes, first value in the low byte.
+__device__ __forceinline__ uint2 quantize8(const uint32_t (&x)[4], float scale) {
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        c[j] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(x[j]), scale), __fdiv_rn(bf16_hi(x[j]), scale));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+__device__ __forceinline__ bool scale_ok(float s) { return s > 0.f && s <= 3.0e38f; }
 
 // One thread per (request, head, group of 8 rotation pairs): heads 0..Hq-1 are
 // query heads (to q_out), heads Hq..Hq+Hkv-1 key heads (to the cache). Each
 // thread loads its two 16-byte halves and its 8 (cos, sin) pairs before it
 // computes or stores anything, so q_out may alias q. Threads past the
 // rotation items copy 16-byte chunks of v into the cache.
+template <bool FP8>
 __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     // inputs may come from the kernel just before this one in the stream
     pdl_wait();
@@ -113,6 +130,17 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
             yl[j] = r0 | (r1 << 16);
             yh[j] = r2 | (r3 << 16);
         }
+        if (FP8 && !is_q) {
+            const float ks = a.k_scale[head - a.Hq];
+            if (!scale_ok(ks)) {
+                if (grp == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SCALE);
+                return;
+            }
+            uint8_t* dst8 = a.k_cache8 + dst_off;
+            *reinterpret_cast<uint2*>(dst8 + i0) = quantize8(yl, ks);
+            *reinterpret_cast<uint2*>(dst8 + i0 + half) = quantize8(yh, ks);
+            return;
+        }
         uint16_t* dst = (is_q ? a.q_out : a.k_cache) + dst_off;
         *reinterpret_cast<uint4*>(dst + i0) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
         *reinterpret_cast<uint4*>(dst + i0 + half) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
@@ -129,8 +157,15 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     const int slot = a.slot_mapping[b];
     if (p < 0 || p >= a.max_pos || slot < 0 || slot >= a.num_blocks * kBlock) return;
     const uint4 val = reinterpret_cast<const uint4*>(a.v + ((long long)b * a.Hkv + h) * a.d)[ch];
-    reinterpret_cast<uint4*>(a.v_cache + (((long long)(slot / kBlock) * a.Hkv + h) * kBlock + slot % kBlock) *
-                             a.d)[ch] = val;
+    const long long row = (((long long)(slot / kBlock) * a.Hkv + h) * kBlock + slot % kBlock) * a.d;
+    if (FP8) {
+        const float vs = a.v_scale[h];
+        if (!scale_ok(vs)) return;  // reported by the key threads
+        const uint32_t x[4] = {val.x, val.y, val.z, val.w};
+        reinterpret_cast<uint2*>(a.v_cache8 + row)[ch] = quantize8(x, vs);
+    } else {
+        reinterpret_cast<uint4*>(a.v_cache + row)[ch] = val;
+    }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -138,12 +173,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 }  // namespace mi
 
-extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, const void* k,
-                                        const void* v, const int32_t* positions,
-                                        const int32_t* slot_mapping, const float* rope_cos_sin,
-                                        int32_t max_pos, void* q_out, void* k_cache, void* v_cache,
-                                        int32_t* dev_err, mi_stream_t stream) {
-    using namespace mi;
+namespace mi {
+namespace {
+
+mi_status append(const mi_dims* dims, const void* q, const void* k, const void* v, const int32_t* positions,
+                 const int32_t* slot_mapping, const float* rope_cos_sin, int32_t max_pos, void* q_out,
+                 void* k_cache, void* v_cache, const float* k_scale, const float* v_scale, bool fp8,
+                 int32_t* dev_err, mi_stream_t stream) {
     if (!dims) return MI_ERR_INVALID_ARG;
     const mi_dims D = *dims;
     if (D.B < 0 || D.B > (1 << 24) || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || max_pos < 1)
@@ -154,6 +190,7 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     if (D.B == 0) return MI_OK;
     if (!q || !k || !v || !positions || !slot_mapping || !rope_cos_sin || !q_out || !k_cache || !v_cache)
         return MI_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return MI_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(rope_cos_sin))
         return MI_ERR_INVALID_ARG;
@@ -165,8 +202,12 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
     a.slot_mapping = slot_mapping;
     a.rope = reinterpret_cast<const float2*>(rope_cos_sin);
     a.q_out = static_cast<uint16_t*>(q_out);
-    a.k_cache = static_cast<uint16_t*>(k_cache);
-    a.v_cache = static_cast<uint16_t*>(v_cache);
+    a.k_cache = fp8 ? nullptr : static_cast<uint16_t*>(k_cache);
+    a.v_cache = fp8 ? nullptr : static_cast<uint16_t*>(v_cache);
+    a.k_cache8 = fp8 ? static_cast<uint8_t*>(k_cache) : nullptr;
+    a.v_cache8 = fp8 ? static_cast<uint8_t*>(v_cache) : nullptr;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.dev_err = dev_err;
     a.Hq = D.Hq;
     a.Hkv = D.Hkv;
@@ -177,7 +218,29 @@ extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, cons
                               (long long)D.B * D.Hkv * (D.head_dim / 8);
     const long long grid = (threads + 127) / 128;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
-    return launch_pdl(append_kernel, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B) == cudaSuccess
-               ? MI_OK
-               : MI_ERR_CUDA;
+    const cudaError_t e = fp8 ? launch_pdl(append_kernel<true>, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B)
+                              : launch_pdl(append_kernel<false>, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B);
+    return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mi
+
+extern "C" mi_status mi_paged_kv_append(const mi_dims* dims, const void* q, const void* k,
+                                        const void* v, const int32_t* positions,
+                                        const int32_t* slot_mapping, const float* rope_cos_sin,
+                                        int32_t max_pos, void* q_out, void* k_cache, void* v_cache,
+                                        int32_t* dev_err, mi_stream_t stream) {
+    return mi::append(dims, q, k, v, positions, slot_mapping, rope_cos_sin, max_pos, q_out, k_cache, v_cache,
+                      nullptr, nullptr, false, dev_err, stream);
+}
+
+extern "C" mi_status mi_paged_kv_append_fp8(const mi_dims* dims, const void* q, const void* k,
+                                            const void* v, const int32_t* positions,
+                                            const int32_t* slot_mapping, const float* rope_cos_sin,
+                                            int32_t max_pos, void* q_out, void* k_cache, void* v_cache,
+                                            const float* k_scale, const float* v_scale, int32_t* dev_err,
+                                            mi_stream_t stream) {
+    return mi::append(dims, q, k, v, positions, slot_mapping, rope_cos_sin, max_pos, q_out, k_cache, v_cache,
+                      k_scale, v_scale, true, dev_err, stream);
 }

@@ -64,6 +64,8 @@ struct AttnParams {
     int B, Hq, Hkv, G, num_blocks, mbps, stages, slot_floats;
     int grid;                      // CTAs of the attention kernel
     float sl2;                     // scale * log2(e)
+    const float* k_scale;          // [Hkv] e4m3 caches: per-head dequantisation scales
+    const float* v_scale;          // [Hkv]
 };
 
 // ------------------------------------------------------------- the plan ---
@@ -181,9 +183,14 @@ __device__ __forceinline__ int cta_of(long long TB, int P, long long x) {
 
 // ------------------------------------------------------- smem layout ------
 
-template <int HD>
+enum { kVarMma = 1, kVarFma = 2, kVarFp8 = 3 };
+
+// Bytes of one cache element: bf16, or e4m3 for the FP8 variant.
+__host__ __device__ constexpr int elem_bytes(int var) { return var == kVarFp8 ? 1 : 2; }
+
+template <int HD, int EB>
 struct Tile {
-    static constexpr int kBytes = kBlock * HD * 2;  // one 16-token K or V tile
+    static constexpr int kBytes = kBlock * HD * EB;  // one 16-token K or V tile
 };
 
 struct SmemPlan {
@@ -192,10 +199,10 @@ struct SmemPlan {
 
 // W consumer warps plus one producer warp; S stages per consumer warp. The
 // weight-exchange buffer is only needed by the CUDA-core tile.
-__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma) {
+__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma, int eb = 2) {
     SmemPlan s;
     int off = 0;
-    s.tiles = off; off += W * S * 2 * kBlock * HD * 2;
+    s.tiles = off; off += W * S * 2 * kBlock * HD * eb;
     s.full = off;  off += W * S * 8;
     s.empty = off; off += W * S * 8;
     s.mbuf = off;  off += W * kMaxG * 4;
@@ -319,6 +326,140 @@ struct MmaState {
             if (h1 < G) {
                 obuf[h1 * HD + mt * 16 + r] = o[mt][1];
                 obuf[h1 * HD + mt * 16 + r + 8] = o[mt][3];
+            }
+        }
+    }
+};
+
+// Tensor-core tile over e4m3 (FP8) K/V tiles, the MMA tile's arithmetic in
+// f16 (every e4m3 value is an f16 value, and f16 keeps 11 bits of the
+// probabilities). S^T = K . Q^T: ldmatrix hands each lane four consecutive K
+// bytes of a token row, which convert to two f16 pairs; within every 16-dim
+// k-slice the lane's k slots (2c, 2c+1) and (2c+8, 2c+9) are taken to be dims
+// (4c, 4c+1) and (4c+2, 4c+3), and Q's fragments are loaded in the same order,
+// so the dot products are unchanged. O^T = V^T . P^T: each lane reads four
+// bytes (dims 4j..4j+3) of token rows 2c, 2c+1, 2c+8, 2c+9, byte-permutes
+// them into (token pair, dim) pairs and converts; the 16 O^T rows of a tile
+// pair are dims 4(8t + r) + {0, 1} (even tile) and + {2, 3} (odd tile).
+// K's per-head scale folds into the exponent scale, V's into the output.
+template <int HD>
+struct Fp8State {
+    static constexpr int kK = HD / 16;
+    uint32_t qb[kK][2];
+    float o[kK][4];
+    float m[2], l[2];
+    float sl2, vsc;
+
+    __device__ __forceinline__ void begin_unit(const AttnParams& p, int b, int h, int lane) {
+        const int n = lane >> 2, c = lane & 3;
+        const bool ok = n < p.G;
+        const uint16_t* qrow = p.q + ((long long)b * p.Hq + (long long)h * p.G + (ok ? n : 0)) * HD;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c)) : make_uint2(0, 0);
+            qb[kk][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));  // dims 4c, 4c+1
+            qb[kk][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));  // dims 4c+2, 4c+3
+        }
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
+        sl2 = p.sl2 * __ldg(p.k_scale + h);
+        vsc = __ldg(p.v_scale + h);
+    }
+
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float /*sl2 of bf16*/, int lane) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mi = lane >> 3;
+            const int tok = (lane & 7) + (mi & 1) * 8;
+#pragma unroll
+            for (int kp = 0; kp < kK / 2; ++kp) {
+                uint32_t r0, r1, r2, r3;  // tokens g / g+8 of k-slices 2kp / 2kp+1
+                ldsm_x4(kt + swz8<HD>(tok, 2 * kp + (mi >> 1)), r0, r1, r2, r3);
+                mma_f16_16816(c, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                              e4m3x2_to_f16x2(r1 >> 16), qb[2 * kp][0], qb[2 * kp][1]);
+                mma_f16_16816(c, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                              e4m3x2_to_f16x2(r3 >> 16), qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+            }
+        }
+        const int t0 = lane >> 2, t1 = t0 + 8;
+        float s0 = t0 < valid ? c[0] * sl2 : kNegInf;
+        float s1 = t0 < valid ? c[1] * sl2 : kNegInf;
+        float s2 = t1 < valid ? c[2] * sl2 : kNegInf;
+        float s3 = t1 < valid ? c[3] * sl2 : kNegInf;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float r0 = mn0 == kNegInf ? 0.f : mn0, r1 = mn1 == kNegInf ? 0.f : mn1;
+        const float al0 = exp2f(m[0] - r0), al1 = exp2f(m[1] - r1);
+        m[0] = mn0;
+        m[1] = mn1;
+        const uint32_t x0 = pack_f16x2(exp2f(s0 - r0), exp2f(s1 - r1));
+        const uint32_t x1 = pack_f16x2(exp2f(s2 - r0), exp2f(s3 - r1));
+        l[0] = l[0] * al0 + (f16_lo(x0) + f16_lo(x1));
+        l[1] = l[1] * al1 + (f16_hi(x0) + f16_hi(x1));
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < kK; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
+        {
+            const int g = lane >> 2, cc = lane & 3;
+#pragma unroll
+            for (int t = 0; t < kK / 2; ++t) {
+                // dims 4j .. 4j+3, j = 8t + g, of token rows 2cc, 2cc+1, 2cc+8, 2cc+9
+                const int chunk = 2 * t + (g >> 2), inb = (g & 3) * 4;
+                const uint32_t w0 = lds32(vt + swz8<HD>(2 * cc, chunk) + inb);
+                const uint32_t w1 = lds32(vt + swz8<HD>(2 * cc + 1, chunk) + inb);
+                const uint32_t w2 = lds32(vt + swz8<HD>(2 * cc + 8, chunk) + inb);
+                const uint32_t w3 = lds32(vt + swz8<HD>(2 * cc + 9, chunk) + inb);
+                const uint32_t lo01 = __byte_perm(w0, w1, 0x5140), hi01 = __byte_perm(w0, w1, 0x7362);
+                const uint32_t lo89 = __byte_perm(w2, w3, 0x5140), hi89 = __byte_perm(w2, w3, 0x7362);
+                mma_f16_16816(o[2 * t], e4m3x2_to_f16x2(lo01), e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(lo89),
+                              e4m3x2_to_f16x2(lo89 >> 16), b0, b1);
+                mma_f16_16816(o[2 * t + 1], e4m3x2_to_f16x2(hi01), e4m3x2_to_f16x2(hi01 >> 16),
+                              e4m3x2_to_f16x2(hi89), e4m3x2_to_f16x2(hi89 >> 16), b0, b1);
+            }
+        }
+    }
+
+    // Reduce the per-thread sums and write (m, l, O * v_scale) of this warp to smem.
+    __device__ __forceinline__ void store(float* mbuf, float* lbuf, float* obuf, int G, int lane) {
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], sh);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], sh);
+        }
+        const int h0 = (lane & 3) * 2, h1 = h0 + 1;
+        if (lane < 4) {
+            if (h0 < G) { mbuf[h0] = m[0]; lbuf[h0] = l[0]; }
+            if (h1 < G) { mbuf[h1] = m[1]; lbuf[h1] = l[1]; }
+        }
+        const int r = lane >> 2;
+#pragma unroll
+        for (int t = 0; t < kK / 2; ++t) {
+            const int d0 = 4 * (8 * t + r);
+            if (h0 < G) {
+                obuf[h0 * HD + d0] = o[2 * t][0] * vsc;
+                obuf[h0 * HD + d0 + 1] = o[2 * t][2] * vsc;
+                obuf[h0 * HD + d0 + 2] = o[2 * t + 1][0] * vsc;
+                obuf[h0 * HD + d0 + 3] = o[2 * t + 1][2] * vsc;
+            }
+            if (h1 < G) {
+                obuf[h1 * HD + d0] = o[2 * t][1] * vsc;
+                obuf[h1 * HD + d0 + 1] = o[2 * t][3] * vsc;
+                obuf[h1 * HD + d0 + 2] = o[2 * t + 1][1] * vsc;
+                obuf[h1 * HD + d0 + 3] = o[2 * t + 1][3] * vsc;
             }
         }
     }
@@ -475,14 +616,14 @@ struct FmaState {
 
 // ------------------------------------------------------ the main kernel ---
 
-enum { kVarMma = 1, kVarFma = 2 };
-
 template <int HD, int VAR, int GP>
 struct StateOf;
 template <int HD, int GP>
 struct StateOf<HD, kVarMma, GP> { using T = MmaState<HD>; };
 template <int HD, int GP>
 struct StateOf<HD, kVarFma, GP> { using T = FmaState<HD, GP>; };
+template <int HD, int GP>
+struct StateOf<HD, kVarFp8, GP> { using T = Fp8State<HD>; };
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -498,13 +639,13 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
-    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma);
+    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma, elem_bytes(VAR));
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t* base = smem_raw + pad;
     const uint32_t sbase = raw + pad;
     long long* scan = reinterpret_cast<long long*>(base + sp.scan);
-    constexpr int kTile = Tile<HD>::kBytes;
+    constexpr int kTile = Tile<HD, elem_bytes(VAR)>::kBytes;
     const uint32_t full0 = sbase + sp.full, empty0 = sbase + sp.empty;
 
     if (tid < W * S) {
@@ -575,7 +716,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
             } else {
                 const uint32_t dst = my_tiles + stg * (2 * kTile);
                 mbar_arrive_expect_tx(bar, 2 * kTile);
-                const int y = ((blk * p.Hkv + cu.h) * kBlock) * (HD / 64);
+                const int y = (blk * p.Hkv + cu.h) * (kTile / 128);  // the tile's first 128-byte line
                 tma_load_2d(dst, &tmk, bar, 0, y, policy);
                 tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
             }
@@ -626,15 +767,16 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
             const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
             if (!dead && blk >= 0 && blk < p.num_blocks) {
                 const uint32_t kt = sbase + sp.tiles + si * (2 * kTile), vt = kt + kTile;
-                if (VAR == kVarMma && valid < kBlock) {
+                if (VAR != kVarFma && valid < kBlock) {
                     // rows past the context may hold any bits: zero V there
-                    for (int i = lane; i < (kBlock - valid) * (HD / 8); i += 32) {
-                        const int row = valid + i / (HD / 8), ch = i % (HD / 8);
-                        st_shared_zero16(vt + swz<HD>(row, ch));
+                    constexpr int kChunks = HD * elem_bytes(VAR) / 16;  // 16-byte chunks per token row
+                    for (int i = lane; i < (kBlock - valid) * kChunks; i += 32) {
+                        const int row = valid + i / kChunks, ch = i % kChunks;
+                        st_shared_zero16(vt + (VAR == kVarFp8 ? swz8<HD>(row, ch) : swz<HD>(row, ch)));
                     }
                     __syncwarp();
                 }
-                if constexpr (VAR == kVarMma) {
+                if constexpr (VAR != kVarFma) {
                     st.block(kt, vt, valid, p.sl2, lane);
                 } else {
                     st.block(kt, vt, valid, p.sl2, lane, xbuf, p.G);
@@ -783,18 +925,25 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
 // ------------------------------------------------------------- host side --
 
 constexpr int kWarps = 4;                 // consumer warps; one producer warp more
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 3;             // bf16 tiles; e4m3 tiles take twice as many
 constexpr int kSmemLimit = 227 * 1024;    // per CTA
 constexpr int kSmemTwoPerSm = 115712;     // per CTA so that two fit in an SM's 228 KB
 
 // Stages per consumer warp: as many as fit with two CTAs per SM, else (very
-// wide GQA groups) as many as fit one CTA.
-int pick_stages(int HD, int G, bool fma) {
-    for (int S = kMaxStages; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma).total <= kSmemTwoPerSm) return S;
-    for (int S = kMaxStages; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma).total <= kSmemLimit) return S;
+// wide GQA groups) as many as fit one CTA. e4m3 tiles are half the size, so
+// twice the stages keep the same bytes in flight.
+int pick_stages(int HD, int G, int var) {
+    const bool fma = var == kVarFma;
+    const int eb = elem_bytes(var), top = kMaxStages * 2 / eb;
+    for (int S = top; S >= 1; --S)
+        if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemTwoPerSm) return S;
+    for (int S = top; S >= 1; --S)
+        if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemLimit) return S;
     return 0;
+}
+
+int smem_of(int HD, int G, int var) {
+    return smem_plan(kWarps, pick_stages(HD, G, var), HD, G, var == kVarFma, elem_bytes(var)).total;
 }
 
 int gp_of(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : 8); }
@@ -811,8 +960,9 @@ KernelFn fma_kernel_for(int GP) {
 }
 
 KernelFn pick_kernel(int HD, int var, int G) {
-    // the MMA tile always spans 8 head columns; the FMA tile is sized to G
+    // the MMA tiles always span 8 head columns; the FMA tile is sized to G
     if (var == kVarMma) return HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps> : attn_kernel<128, kVarMma, 8, kWarps>;
+    if (var == kVarFp8) return HD == 64 ? attn_kernel<64, kVarFp8, 8, kWarps> : attn_kernel<128, kVarFp8, 8, kWarps>;
     return HD == 64 ? fma_kernel_for<64>(gp_of(G)) : fma_kernel_for<128>(gp_of(G));
 }
 
@@ -872,11 +1022,9 @@ int slot_floats(const mi_dims& D) { return (D.Hq / D.Hkv) * D.head_dim + 8; }
 int max_grid(const mi_dims& D) {
     const int G = D.Hq / D.Hkv;
     int g = 0;
-    for (int var : {kVarMma, kVarFma}) {
-        const bool fma = var == kVarFma;
-        const int S = pick_stages(D.head_dim, G, fma);
-        if (!S) return 0;
-        const int n = grid_for(pick_kernel(D.head_dim, var, G), smem_plan(kWarps, S, D.head_dim, G, fma).total);
+    for (int var : {kVarMma, kVarFma, kVarFp8}) {
+        if (!pick_stages(D.head_dim, G, var)) return 0;
+        const int n = grid_for(pick_kernel(D.head_dim, var, G), smem_of(D.head_dim, G, var));
         if (n <= 0) return 0;
         g = n > g ? n : g;
     }
@@ -918,31 +1066,29 @@ extern "C" size_t mi_paged_decode_workspace_bytes(const mi_dims* dims) {
     return workspace_for(*dims, g);
 }
 
-extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
-                                                       const void* k_cache, const void* v_cache,
-                                                       const int32_t* block_tables,
-                                                       const int32_t* context_lens, float scale,
-                                                       void* out, void* workspace,
-                                                       size_t workspace_bytes, int32_t* dev_err,
-                                                       mi_stream_t stream, mi_attn_variant variant,
-                                                       int32_t ctas) {
-    using namespace mi;
+namespace mi {
+namespace {
+
+// Checks, plans and launches one attention call of variant `var` (bf16 caches
+// for kVarMma / kVarFma, e4m3 caches with per-head scales for kVarFp8).
+mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                    const int32_t* context_lens, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream, int var, int32_t ctas) {
     const mi_status ds = check_dims(dims);
     if (ds != MI_OK) return ds;
     const mi_dims D = *dims;
     if (D.B == 0) return MI_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return MI_ERR_INVALID_ARG;
+    if (var == kVarFp8 && (!k_scale || !v_scale)) return MI_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
         !aligned16(workspace))
         return MI_ERR_INVALID_ARG;
     if (ctas < 0 || !std::isfinite(scale)) return MI_ERR_INVALID_ARG;
-    if (variant != MI_ATTN_DEFAULT && variant != MI_ATTN_MMA && variant != MI_ATTN_FMA)
-        return MI_ERR_INVALID_ARG;
-    const int var = variant == MI_ATTN_FMA ? kVarFma : kVarMma;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
-    const int S = pick_stages(HD, G, var == kVarFma);
-    const int smem = smem_plan(kWarps, S, HD, G, var == kVarFma).total;
+    const int S = pick_stages(HD, G, var);
+    const int smem = smem_of(HD, G, var);
     const int gmax = max_grid(D);
     if (gmax <= 0) return MI_ERR_CUDA;
     if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
@@ -950,7 +1096,9 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
 
     CUtensorMap tk, tv;
     const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
-    if (!make_tmap(&tk, k_cache, rows, HD) || !make_tmap(&tv, v_cache, rows, HD)) return MI_ERR_CUDA;
+    const bool maps = var == kVarFp8 ? make_tmap8(&tk, k_cache, rows, HD) && make_tmap8(&tv, v_cache, rows, HD)
+                                     : make_tmap(&tk, k_cache, rows, HD) && make_tmap(&tv, v_cache, rows, HD);
+    if (!maps) return MI_ERR_CUDA;
 
     AttnParams p;
     p.q = static_cast<const uint16_t*>(q);
@@ -971,10 +1119,42 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
     p.slot_floats = slot_floats(D);
     p.grid = grid;
     p.sl2 = scale * 1.4426950408889634f;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
 
     cudaStream_t s = (cudaStream_t)stream;
     KernelFn fn = pick_kernel(HD, var, G);
     return launch_pdl(fn, grid, (kWarps + 1) * 32, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mi
+
+extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
+                                                       const void* k_cache, const void* v_cache,
+                                                       const int32_t* block_tables,
+                                                       const int32_t* context_lens, float scale,
+                                                       void* out, void* workspace,
+                                                       size_t workspace_bytes, int32_t* dev_err,
+                                                       mi_stream_t stream, mi_attn_variant variant,
+                                                       int32_t ctas) {
+    using namespace mi;
+    if (variant != MI_ATTN_DEFAULT && variant != MI_ATTN_MMA && variant != MI_ATTN_FMA)
+        return MI_ERR_INVALID_ARG;
+    return attention(dims, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, dev_err, stream, variant == MI_ATTN_FMA ? kVarFma : kVarMma,
+                     ctas);
+}
+
+extern "C" mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, const void* k_cache,
+                                                   const void* v_cache, const float* k_scale,
+                                                   const float* v_scale, const int32_t* block_tables,
+                                                   const int32_t* context_lens, float scale, void* out,
+                                                   void* workspace, size_t workspace_bytes,
+                                                   int32_t* dev_err, mi_stream_t stream) {
+    using namespace mi;
+    return attention(dims, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, dev_err, stream, kVarFp8, 0);
 }
 
 extern "C" mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,

@@ -24,6 +24,16 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(line * 128 + (((chunk & 7) ^ (line & 7)) << 4));
 }
 
+// The same for a tile of one-byte (e4m3) elements: a token row is HD bytes,
+// so a 128-byte line holds 128/HD token rows; chunk c (0 .. HD/16-1) of row r
+// is byte r*HD + 16c of the tile before the swizzle.
+template <int HD>
+__device__ __forceinline__ uint32_t swz8(int row, int chunk) {
+    const int byte = row * HD + chunk * 16;
+    const int line = byte >> 7, cil = (byte >> 4) & 7;
+    return (uint32_t)(line * 128 + ((cil ^ (line & 7)) << 4));
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against libcuda); nullptr when the driver does not provide it.
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -52,6 +62,22 @@ inline bool make_tmap(CUtensorMap* m, const void* base, long long rows, int HD) 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D map over a one-byte (e4m3) cache viewed as 128-byte lines:
+// [rows * HD/128][128] u8, box = one 16-token tile (16 * HD/128 lines), 128-byte
+// swizzle.
+inline bool make_tmap8(CUtensorMap* m, const void* base, long long rows, int HD) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128, (cuuint64_t)rows * HD / 128};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, (cuuint32_t)(kBlock * HD / 128)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
