@@ -132,12 +132,14 @@ def recorded_traffic(workload):
     was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
     try:
-        kv = dict(tok.split("=", 1) for tok in open(path).read().split())
+        lines = open(path).read().splitlines()
     except Exception:
         return None
-    if kv.get("source") != kernel_source_hash() or kv.get("workload") != workload:
-        return None
-    return float(kv["dram_bytes_per_launch"])
+    for line in lines:
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("source") == kernel_source_hash() and kv.get("workload") == workload:
+            return float(kv["dram_bytes_per_launch"])
+    return None
 
 
 # ---------------------------------------------------------------- clocks ---

@@ -194,7 +194,7 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, mbuf, lbuf, obuf, xbuf, scan, fac, flag, total;
+    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, fac, flag, total;
 };
 
 // W consumer warps plus one producer warp; S stages per consumer warp. The
@@ -205,6 +205,7 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.tiles = off; off += W * S * 2 * kBlock * HD * eb;
     s.full = off;  off += W * S * 8;
     s.empty = off; off += W * S * 8;
+    s.okf = off;   off += W * S * 4;  // per stage: 1 when its block id was valid and copied
     s.mbuf = off;  off += W * kMaxG * 4;
     s.lbuf = off;  off += W * kMaxG * 4;
     s.fac = off;   off += (W + 3) * kMaxG * 4;
@@ -249,14 +250,19 @@ struct MmaState {
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float sl2, int lane) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            // two accumulation chains (even / odd k-slices) halve the
+            // dependent MMA latency
+            float c1[4] = {0.f, 0.f, 0.f, 0.f};
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int csel = lane >> 4;
 #pragma unroll
             for (int kk = 0; kk < kK; ++kk) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(kt + swz<HD>(tok, kk * 2 + csel), a0, a1, a2, a3);
-                mma_bf16_16816(c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                mma_bf16_16816(kk & 1 ? c1 : c, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] += c1[i];
         }
         const int t0 = lane >> 2, t1 = t0 + 8;
         float s0 = t0 < valid ? c[0] * sl2 : kNegInf;  // head 2*(lane&3),   token t0
@@ -371,6 +377,7 @@ struct Fp8State {
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float /*sl2 of bf16*/, int lane) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            float c1[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulation chain (odd k-slices)
             const int mi = lane >> 3;
             const int tok = (lane & 7) + (mi & 1) * 8;
 #pragma unroll
@@ -379,9 +386,11 @@ struct Fp8State {
                 ldsm_x4(kt + swz8<HD>(tok, 2 * kp + (mi >> 1)), r0, r1, r2, r3);
                 mma_f16_16816(c, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
                               e4m3x2_to_f16x2(r1 >> 16), qb[2 * kp][0], qb[2 * kp][1]);
-                mma_f16_16816(c, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                mma_f16_16816(c1, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
                               e4m3x2_to_f16x2(r3 >> 16), qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] += c1[i];
         }
         const int t0 = lane >> 2, t1 = t0 + 8;
         float s0 = t0 < valid ? c[0] * sl2 : kNegInf;
@@ -710,11 +719,14 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
             cu.advance_to(p, x);
             const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
             const uint32_t bar = my_full + stg * 8;
+            const uint32_t okf = sbase + sp.okf + ((uint32_t)(lane * S) + stg) * 4;
             if (blk < 0 || blk >= p.num_blocks) {
                 raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
-                mbar_arrive(bar);  // the consumer skips the block (it checks the table itself)
+                sts32(okf, 0u);
+                mbar_arrive(bar);  // the consumer skips the block
             } else {
                 const uint32_t dst = my_tiles + stg * (2 * kTile);
+                sts32(okf, 1u);
                 mbar_arrive_expect_tx(bar, 2 * kTile);
                 const int y = (blk * p.Hkv + cu.h) * (kTile / 128);  // the tile's first 128-byte line
                 tma_load_2d(dst, &tmk, bar, 0, y, policy);
@@ -764,8 +776,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 2)
             }
             const int j = (int)(x - cu.start);
             const int valid = min(kBlock, nvalid - j * kBlock);
-            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
-            if (!dead && blk >= 0 && blk < p.num_blocks) {
+            // the producer's flag (published by its arrive) says whether the block was copied
+            if (!dead && lds32(sbase + sp.okf + si * 4) != 0u) {
                 const uint32_t kt = sbase + sp.tiles + si * (2 * kTile), vt = kt + kTile;
                 if (VAR != kVarFma && valid < kBlock) {
                     // rows past the context may hold any bits: zero V there

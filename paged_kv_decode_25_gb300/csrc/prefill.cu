@@ -19,7 +19,7 @@
 //   * Consumer warp tile (mma.sync m16n8k16, bf16 in, fp32 accumulate):
 //     S[16 rows x 64 keys] = Q . K^T with Q held in registers as A fragments
 //     and K read by ldmatrix as B fragments; causal mask and base-2 online
-//     softmax on the accumulator fragments; the probabilities are repacked in
+//     softmax on the accumulator fragments, one 16-key block at a time; the probabilities are repacked in
 //     place as bf16 A fragments and O[16 x HD] += P . V with V read by
 //     ldmatrix.trans.
 //   * Grid: one CTA per (request r, KV head h, row tile k counted from the
@@ -39,9 +39,9 @@ namespace mi {
 namespace {
 
 constexpr int kPWarps = 4;                      // consumer warps
-constexpr int kPRows = kPWarps * 16;            // rows per CTA
+constexpr int kMT = 1;                          // 16-row m-tiles per consumer warp
+constexpr int kPRows = kPWarps * 16 * kMT;      // rows per CTA
 constexpr int kStageBlocks = 4;                 // 16-token blocks per stage: 64 keys
-constexpr int kSubBlocks = 2;                   // blocks per softmax sub-step: 32 keys
 constexpr int kPStages = 3;
 constexpr int kMaxGroup = 8;
 constexpr int kTileGroup = 8;                   // row tiles of one (request, head) launched together
@@ -84,7 +84,7 @@ __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
+__global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    PrefillParams p) {
     using SM = PrefillSmem<HD>;
@@ -192,14 +192,24 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
     }
 
     // --------------------------------------------------- consumer warps ----
+    // A warp owns kMT 16-row m-tiles; a thread holds rows lane/4 and lane/4 + 8
+    // of each (index [mt][0] and [mt][1]).
     const int c = lane & 3;
-    const int wr0 = rho0 + warp * 16;                  // first row of this warp
-    const int rA = wr0 + (lane >> 2), rB = rA + 8;     // this thread's two rows
-    const bool vA = rA < nrows, vB = rB < nrows;
-    const int iA = rA / p.G, iB = rB / p.G;
-    const int posA = vA ? first + iA : p_hi, posB = vB ? first + iB : p_hi;
-    const int mposA = posA < 0 ? 0 : posA, mposB = posB < 0 ? 0 : posB;  // masking positions
-    const int w_last = min(wr0 + 15, rho0 + rows_here - 1);
+    const int wr0 = rho0 + warp * 16 * kMT;            // first row of this warp
+    int ridx[kMT][2], tok[kMT][2], pos[kMT][2], mpos[kMT][2];
+    bool vrow[kMT][2];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = wr0 + mt * 16 + (lane >> 2) + 8 * hf;
+            ridx[mt][hf] = r;
+            vrow[mt][hf] = r < nrows;
+            tok[mt][hf] = r / p.G;
+            pos[mt][hf] = vrow[mt][hf] ? first + tok[mt][hf] : p_hi;
+            mpos[mt][hf] = pos[mt][hf] < 0 ? 0 : pos[mt][hf];  // masking position
+        }
+    const int w_last = min(wr0 + 16 * kMT - 1, rho0 + rows_here - 1);
     const int pw_hi = w_last >= wr0 ? first + w_last / p.G : -1;
     const int pw_lo = first + wr0 / p.G;
     const int nblk_w = pw_hi >= 0 ? pw_hi / kBlock + 1 : 0;  // blocks this warp reads
@@ -207,25 +217,34 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
     const int tail = n - (nb_ctx - 1) * kBlock;              // valid tokens in the context's last block
 
     // Q rows as A fragments (zero for rows past the request's last token)
-    uint32_t qa[kK][4];
-    {
-        const long long headA = (long long)(q0 + (vA ? iA : 0)) * p.Hq + (long long)h * p.G + rA % p.G;
-        const long long headB = (long long)(q0 + (vB ? iB : 0)) * p.Hq + (long long)h * p.G + rB % p.G;
-        const uint32_t* qA = reinterpret_cast<const uint32_t*>(p.q + headA * HD);
-        const uint32_t* qB = reinterpret_cast<const uint32_t*>(p.q + headB * HD);
+    uint32_t qa[kMT][kK][4];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+        const uint32_t* qr[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const long long head = (long long)(q0 + (vrow[mt][hf] ? tok[mt][hf] : 0)) * p.Hq +
+                                   (long long)h * p.G + ridx[mt][hf] % p.G;
+            qr[hf] = reinterpret_cast<const uint32_t*>(p.q + head * HD);
+        }
 #pragma unroll
         for (int ks = 0; ks < kK; ++ks) {
-            qa[ks][0] = vA ? __ldg(qA + ks * 8 + c) : 0u;
-            qa[ks][1] = vB ? __ldg(qB + ks * 8 + c) : 0u;
-            qa[ks][2] = vA ? __ldg(qA + ks * 8 + 4 + c) : 0u;
-            qa[ks][3] = vB ? __ldg(qB + ks * 8 + 4 + c) : 0u;
+            qa[mt][ks][0] = vrow[mt][0] ? __ldg(qr[0] + ks * 8 + c) : 0u;
+            qa[mt][ks][1] = vrow[mt][1] ? __ldg(qr[1] + ks * 8 + c) : 0u;
+            qa[mt][ks][2] = vrow[mt][0] ? __ldg(qr[0] + ks * 8 + 4 + c) : 0u;
+            qa[mt][ks][3] = vrow[mt][1] ? __ldg(qr[1] + ks * 8 + 4 + c) : 0u;
         }
     }
 
-    float o[kN][4];
+    float o[kMT][kN][4];
+    float mrow[kMT][2], lrow[kMT][2];
 #pragma unroll
-    for (int t = 0; t < kN; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    for (int mt = 0; mt < kMT; ++mt) {
+#pragma unroll
+        for (int t = 0; t < kN; ++t) o[mt][t][0] = o[mt][t][1] = o[mt][t][2] = o[mt][t][3] = 0.f;
+        mrow[mt][0] = mrow[mt][1] = -INFINITY;
+        lrow[mt][0] = lrow[mt][1] = 0.f;
+    }
 
     // ldmatrix lane addressing inside a staged tile
     const int k_key = ((lane >> 4) << 3) + (lane & 7), k_chk = (lane >> 3) & 1;   // K as B of Q.K^T
@@ -240,114 +259,99 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
             break;
         }
         const uint32_t present = lds_u32(mask0 + stg * 4);
-        uint32_t used = 0;  // blocks of the stage this warp multiplies
+        // the stage is taken one 16-key block at a time, each block's K and V
+        // fragments feeding every m-tile of the warp
 #pragma unroll
-        for (int l = 0; l < kStageBlocks; ++l)
-            if (((present >> l) & 1u) && j * kStageBlocks + l < nblk_w) used |= 1u << l;
-        // two 32-key sub-steps per stage keep the score and probability
-        // fragments of only two blocks live at a time
+        for (int l = 0; l < kStageBlocks; ++l) {
+            const int jb = j * kStageBlocks + l;  // request block index
+            if (!((present >> l) & 1u) || jb >= nblk_w) continue;
+            const uint32_t kt = sbase + stg * SM::kStage + (uint32_t)l * 2u * kTile, vt = kt + kTile;
+            float s[kMT][2][4];
 #pragma unroll
-        for (int hs = 0; hs < kStageBlocks / kSubBlocks; ++hs) {
-            const uint32_t sub = (used >> (hs * kSubBlocks)) & ((1u << kSubBlocks) - 1u);
-            if (!sub) continue;
-            const int jb = j * kStageBlocks + hs * kSubBlocks;  // request block index of the first block
-            const uint32_t sub_base = sbase + stg * SM::kStage + (uint32_t)(hs * kSubBlocks) * 2u * kTile;
-            float s[kSubBlocks][2][4];
+            for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-            for (int l = 0; l < kSubBlocks; ++l) {
+                for (int e = 0; e < 4; ++e) s[mt][0][e] = s[mt][1][e] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s[l][0][e] = s[l][1][e] = 0.f;
-                if (sub & (1u << l)) {
-                    const uint32_t kt = sub_base + (uint32_t)l * 2u * kTile;
+            for (int ks = 0; ks < kK; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(kt + swz<HD>(k_key, 2 * ks + k_chk), b00, b01, b10, b11);
 #pragma unroll
-                    for (int ks = 0; ks < kK; ++ks) {
-                        uint32_t b00, b01, b10, b11;
-                        ldsm_x4(kt + swz<HD>(k_key, 2 * ks + k_chk), b00, b01, b10, b11);
-                        mma_bf16_16816(s[l][0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-                        mma_bf16_16816(s[l][1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
-                    }
+                for (int mt = 0; mt < kMT; ++mt) {
+                    mma_bf16_16816(s[mt][0], qa[mt][ks][0], qa[mt][ks][1], qa[mt][ks][2], qa[mt][ks][3], b00, b01);
+                    mma_bf16_16816(s[mt][1], qa[mt][ks][0], qa[mt][ks][1], qa[mt][ks][2], qa[mt][ks][3], b10, b11);
                 }
             }
-            // scale to base 2, mask (blocks not multiplied, keys after a row's position)
+            // scale to base 2, mask keys after a row's position, online softmax
             const int kbase = jb * kBlock;
-            const bool causal = kbase + kSubBlocks * kBlock - 1 > pw_lo;
-            float xA = -INFINITY, xB = -INFINITY;
+            const bool causal = kbase + kBlock - 1 > pw_lo;
+            uint32_t pa[kMT][4];
 #pragma unroll
-            for (int l = 0; l < kSubBlocks; ++l) {
-                const bool on = (sub >> l) & 1u;
+            for (int mt = 0; mt < kMT; ++mt) {
+                float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int key = kbase + l * kBlock + t * 8 + 2 * c + (e & 1);
-                        const int pos = e < 2 ? mposA : mposB;
-                        const bool keep = on && (!causal || key <= pos);
-                        s[l][t][e] = keep ? s[l][t][e] * p.sl2 : -INFINITY;
+                        const int key = kbase + t * 8 + 2 * c + (e & 1);
+                        const bool keep = !causal || key <= mpos[mt][e >> 1];
+                        s[mt][t][e] = keep ? s[mt][t][e] * p.sl2 : -INFINITY;
                     }
-                    xA = fmaxf(xA, fmaxf(s[l][t][0], s[l][t][1]));
-                    xB = fmaxf(xB, fmaxf(s[l][t][2], s[l][t][3]));
+                    x0 = fmaxf(x0, fmaxf(s[mt][t][0], s[mt][t][1]));
+                    x1 = fmaxf(x1, fmaxf(s[mt][t][2], s[mt][t][3]));
                 }
-            }
-            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 1));
-            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 2));
-            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 1));
-            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 2));
-            const float nA = fmaxf(mA, xA), nB = fmaxf(mB, xB);
-            const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
-            const float aA = exp2f(mA - uA), aB = exp2f(mB - uB);
-            mA = nA;
-            mB = nB;
-            if (__any_sync(0xffffffffu, aA != 1.f || aB != 1.f)) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+                const float n0 = fmaxf(mrow[mt][0], x0), n1 = fmaxf(mrow[mt][1], x1);
+                const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+                const float a0 = exp2f(mrow[mt][0] - u0), a1 = exp2f(mrow[mt][1] - u1);
+                mrow[mt][0] = n0;
+                mrow[mt][1] = n1;
+                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-                for (int t = 0; t < kN; ++t) {
-                    o[t][0] *= aA;
-                    o[t][1] *= aA;
-                    o[t][2] *= aB;
-                    o[t][3] *= aB;
+                    for (int t = 0; t < kN; ++t) {
+                        o[mt][t][0] *= a0;
+                        o[mt][t][1] *= a0;
+                        o[mt][t][2] *= a1;
+                        o[mt][t][3] *= a1;
+                    }
                 }
-            }
-            lA *= aA;
-            lB *= aB;
-            // probabilities, repacked as the A fragments of P . V (16 keys per block)
-            uint32_t pa[kSubBlocks][4];
-#pragma unroll
-            for (int l = 0; l < kSubBlocks; ++l) {
                 float e[2][4];
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    e[t][0] = exp2f(s[l][t][0] - uA);
-                    e[t][1] = exp2f(s[l][t][1] - uA);
-                    e[t][2] = exp2f(s[l][t][2] - uB);
-                    e[t][3] = exp2f(s[l][t][3] - uB);
-                    lA += e[t][0] + e[t][1];
-                    lB += e[t][2] + e[t][3];
+                    e[t][0] = exp2f(s[mt][t][0] - u0);
+                    e[t][1] = exp2f(s[mt][t][1] - u0);
+                    e[t][2] = exp2f(s[mt][t][2] - u1);
+                    e[t][3] = exp2f(s[mt][t][3] - u1);
                 }
-                pa[l][0] = pack_bf16x2(e[0][0], e[0][1]);
-                pa[l][1] = pack_bf16x2(e[0][2], e[0][3]);
-                pa[l][2] = pack_bf16x2(e[1][0], e[1][1]);
-                pa[l][3] = pack_bf16x2(e[1][2], e[1][3]);
+                lrow[mt][0] = lrow[mt][0] * a0 + (e[0][0] + e[0][1] + e[1][0] + e[1][1]);
+                lrow[mt][1] = lrow[mt][1] * a1 + (e[0][2] + e[0][3] + e[1][2] + e[1][3]);
+                // probabilities, repacked as the A fragment of P . V (16 keys)
+                pa[mt][0] = pack_bf16x2(e[0][0], e[0][1]);
+                pa[mt][1] = pack_bf16x2(e[0][2], e[0][3]);
+                pa[mt][2] = pack_bf16x2(e[1][0], e[1][1]);
+                pa[mt][3] = pack_bf16x2(e[1][2], e[1][3]);
+            }
+            // keys past the context in its last block may hold any bits: zero them
+            uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
+            if (jb == nb_ctx - 1 && tail < kBlock) {
+                const int k0 = 2 * c;
+                zlo = (k0 < tail ? 0x0000FFFFu : 0u) | (k0 + 1 < tail ? 0xFFFF0000u : 0u);
+                zhi = (k0 + 8 < tail ? 0x0000FFFFu : 0u) | (k0 + 9 < tail ? 0xFFFF0000u : 0u);
             }
 #pragma unroll
-            for (int l = 0; l < kSubBlocks; ++l) {
-                if (!(sub & (1u << l))) continue;
-                const uint32_t vt = sub_base + (uint32_t)l * 2u * kTile + kTile;
-                // keys past the context in its last block may hold any bits: zero them
-                uint32_t zlo = 0xFFFFFFFFu, zhi = 0xFFFFFFFFu;
-                if (jb + l == nb_ctx - 1 && tail < kBlock) {
-                    const int k0 = 2 * c;
-                    zlo = (k0 < tail ? 0x0000FFFFu : 0u) | (k0 + 1 < tail ? 0xFFFF0000u : 0u);
-                    zhi = (k0 + 8 < tail ? 0x0000FFFFu : 0u) | (k0 + 9 < tail ? 0xFFFF0000u : 0u);
-                }
+            for (int dp = 0; dp < kN / 2; ++dp) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_trans(vt + swz<HD>(v_key, 2 * dp + v_chk), v0, v1, v2, v3);
+                v0 &= zlo;
+                v2 &= zlo;
+                v1 &= zhi;
+                v3 &= zhi;
 #pragma unroll
-                for (int dp = 0; dp < kN / 2; ++dp) {
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(vt + swz<HD>(v_key, 2 * dp + v_chk), v0, v1, v2, v3);
-                    v0 &= zlo;
-                    v2 &= zlo;
-                    v1 &= zhi;
-                    v3 &= zhi;
-                    mma_bf16_16816(o[2 * dp], pa[l][0], pa[l][1], pa[l][2], pa[l][3], v0, v1);
-                    mma_bf16_16816(o[2 * dp + 1], pa[l][0], pa[l][1], pa[l][2], pa[l][3], v2, v3);
+                for (int mt = 0; mt < kMT; ++mt) {
+                    mma_bf16_16816(o[mt][2 * dp], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
+                    mma_bf16_16816(o[mt][2 * dp + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
                 }
             }
         }
@@ -360,26 +364,23 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, 2)
     }
     if (dead) return;
 
-    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    // rows before position 0 (more new tokens than context) are +0
-    const uint32_t keepA = posA >= 0 ? 0xFFFFFFFFu : 0u, keepB = posB >= 0 ? 0xFFFFFFFFu : 0u;
-    const float invA = lA > 0.f ? 1.f / lA : 0.f;
-    const float invB = lB > 0.f ? 1.f / lB : 0.f;
-    if (vA) {
-        uint32_t* row = reinterpret_cast<uint32_t*>(
-            p.out + ((long long)(q0 + iA) * p.Hq + (long long)h * p.G + rA % p.G) * HD);
 #pragma unroll
-        for (int t = 0; t < kN; ++t) row[t * 4 + c] = pack_bf16x2(o[t][0] * invA, o[t][1] * invA) & keepA;
-    }
-    if (vB) {
-        uint32_t* row = reinterpret_cast<uint32_t*>(
-            p.out + ((long long)(q0 + iB) * p.Hq + (long long)h * p.G + rB % p.G) * HD);
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-        for (int t = 0; t < kN; ++t) row[t * 4 + c] = pack_bf16x2(o[t][2] * invB, o[t][3] * invB) & keepB;
-    }
+        for (int hf = 0; hf < 2; ++hf) {
+            float l = lrow[mt][hf];
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (!vrow[mt][hf]) continue;
+            // rows before position 0 (more new tokens than context) are +0
+            const uint32_t keep = pos[mt][hf] >= 0 ? 0xFFFFFFFFu : 0u;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint32_t* row = reinterpret_cast<uint32_t*>(
+                p.out + ((long long)(q0 + tok[mt][hf]) * p.Hq + (long long)h * p.G + ridx[mt][hf] % p.G) * HD);
+#pragma unroll
+            for (int t = 0; t < kN; ++t)
+                row[t * 4 + c] = pack_bf16x2(o[mt][t][2 * hf] * inv, o[mt][t][2 * hf + 1] * inv) & keep;
+        }
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
