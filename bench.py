@@ -642,6 +642,12 @@ def barrier(world):
         dist.barrier()
 
 
+def whole_job_rate(units_per_rank, seconds_max, world):
+    """Whole-job throughput of `world` replicas that each process
+    units_per_rank units, timed as the slowest rank's seconds."""
+    return world * units_per_rank / seconds_max
+
+
 def max_over_ranks(x, world, device):
     if world == 1:
         return x
@@ -795,7 +801,7 @@ def main():
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     a_bytes = attention_bytes(w, cl, kvb)
     step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
-    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
     peak, peak_kind = measured_peak()
     achieved = a_bytes / (attn_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(w.name + ("_fp8" if fp8 else ""))
