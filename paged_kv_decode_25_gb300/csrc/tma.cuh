@@ -82,4 +82,36 @@ inline bool make_tmap8(CUtensorMap* m, const void* base, long long rows, int HD)
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a bf16 cache for canonical K-major tiles: dims {64, HD/64,
+// rows} (a token row split into 128-byte halves), box {64, 1, 16}: one
+// 128-byte half of 16 token rows, landing as [16][128 B] with 128-byte swizzle.
+inline bool make_tmap_kv_halves(CUtensorMap* m, const void* base, long long rows, int HD) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)(HD / 64), (cuuint64_t)rows};
+    cuuint64_t strides[2] = {128, (cuuint64_t)HD * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlock};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 4-D map over q [T][Hq][HD] bf16: dims {64, HD/64, Hq, T}, box {64, 1, G,
+// rows / G}: one 128-byte half of `rows` (token, head) rows of a GQA group,
+// landing as [rows][128 B] with 128-byte swizzle; tokens past T read as zero.
+inline bool make_tmap_q_group(CUtensorMap* m, const void* q, int T, int Hq, int HD, int G, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)(HD / 64), (cuuint64_t)Hq, (cuuint64_t)T};
+    cuuint64_t strides[3] = {128, (cuuint64_t)HD * 2, (cuuint64_t)Hq * HD * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)G, (cuuint32_t)(rows / G)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace mi
