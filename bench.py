@@ -377,6 +377,9 @@ def run_prefill(args, w, rank, world):
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
     max_q = int(m.max())
+    pvar = mi.MI_PREFILL_MMA if args.variant == "mma" else mi.MI_PREFILL_DEFAULT
+    kernel_name = ("paged prefill attention (mma.sync m16n8k16 bf16), per layer" if args.variant == "mma" else
+                   "paged prefill attention (tcgen05.mma, tensor-memory accumulators), per layer")
 
     def step(ev=None):
         for layer in range(layers):
@@ -385,8 +388,9 @@ def run_prefill(args, w, rank, world):
                                            err, stream), "append")
             if ev is not None:
                 ev[layer][0].record(stream)
-            mi.check(mi.mi_paged_prefill_attention(d_att, T, max_q, qo_d, kc, vc, bt_d, n_d, qs_d, w.scale,
-                                                   out_d, err, stream), "prefill attention")
+            mi.check(mi.mi_paged_prefill_attention_variant(d_att, T, max_q, qo_d, kc, vc, bt_d, n_d, qs_d, w.scale,
+                                                           out_d, variant=pvar, dev_err=err, stream=stream),
+                     "prefill attention")
             if ev is not None:
                 ev[layer][1].record(stream)
 
@@ -468,7 +472,7 @@ def run_prefill(args, w, rank, world):
                    "l2": "no flush: every layer reads its own caches", "parallelism": "replicas"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind + " (sustained bf16)",
-                     "kernel": "paged prefill attention (mma.sync m16n8k16 bf16), per layer",
+                     "kernel": kernel_name,
                      "algorithmic_flops_per_launch": fl, "avg_launch_ms": attn_avg_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * layers * fl / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -61,6 +61,7 @@ typedef enum mi_status {
 #define MI_DEVERR_BAD_CONTEXT  0x8 /* context length above max_blocks_per_seq * block_size */
 #define MI_DEVERR_TIMEOUT      0x10 /* a staged copy did not land within the wait limit */
 #define MI_DEVERR_BAD_SCALE    0x40 /* FP8 append: a KV head's scale is not a positive finite number */
+#define MI_DEVERR_INTERNAL     0x80 /* a kernel could not lay out its shared memory (the call did nothing) */
 #define MI_DEVERR_BAD_QUERY    0x20 /* prefill: query_start not within [0, total_q] and ascending,
                                        a request longer than max_query_len, or more
                                        new tokens than context */
@@ -347,6 +348,22 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
                                      const int32_t* block_tables, const int32_t* context_lens,
                                      const int32_t* query_start, float scale, void* out,
                                      int32_t* dev_err, mi_stream_t stream);
+
+/* Kernel of mi_paged_prefill_attention_variant:
+ *   MI_PREFILL_MMA      warp-level mma.sync tiles (64 rows per CTA; any G),
+ *   MI_PREFILL_TCGEN05  fifth-generation tensor cores (tcgen05.mma with
+ *                       tensor-memory accumulators, 128 rows per CTA; G must
+ *                       divide 128, else MI_ERR_UNSUPPORTED).
+ * MI_PREFILL_DEFAULT takes the tcgen05 kernel when G divides 128, else the
+ * mma.sync one. Both compute the same definition within the same tolerance. */
+#define MI_PREFILL_DEFAULT 0
+#define MI_PREFILL_MMA 1
+#define MI_PREFILL_TCGEN05 2
+mi_status mi_paged_prefill_attention_variant(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
+                                             const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             const int32_t* query_start, float scale, void* out,
+                                             int32_t* dev_err, mi_stream_t stream, int32_t variant);
 
 /* Block copies between two paged caches (the data movement of a swap):
  *   dst_k[dst_blocks[i]] = src_k[src_blocks[i]],

@@ -27,6 +27,8 @@ MI_DEVERR_BAD_CONTEXT, MI_DEVERR_TIMEOUT, MI_DEVERR_BAD_QUERY, MI_DEVERR_BAD_SCA
 MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
 MI_ADMIT_PROCEED, MI_ADMIT_SOFT_BRAKE, MI_ADMIT_HARD_BRAKE = 0, 1, 2
 MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
+MI_PREFILL_DEFAULT, MI_PREFILL_MMA, MI_PREFILL_TCGEN05 = 0, 1, 2
+MI_DEVERR_INTERNAL = 0x80
 
 # every symbol include/mi.h declares
 EXPORTS = (
@@ -38,7 +40,7 @@ EXPORTS = (
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
     "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
-    "mi_paged_prefill_attention", "mi_paged_decode_attention_noalloc",
+    "mi_paged_prefill_attention", "mi_paged_prefill_attention_variant", "mi_paged_decode_attention_noalloc",
 )
 MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -89,6 +91,7 @@ def load():
             "mi_paged_decode_attention_variant": (
                 [dims_p, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P, i32, i32], i32),
             "mi_paged_prefill_attention": ([dims_p, i32, i32, P, P, P, P, P, P, f32, P, P, P], i32),
+            "mi_paged_prefill_attention_variant": ([dims_p, i32, i32, P, P, P, P, P, P, f32, P, P, P, i32], i32),
             "mi_paged_kv_append_fp8": ([dims_p, P, P, P, P, P, P, i32, P, P, P, P, P, P, P], i32),
             "mi_paged_decode_attention_fp8": (
                 [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
@@ -362,6 +365,15 @@ def mi_kv_copy_blocks(d: MiDims, src_k, src_v, src_num_blocks, src_blocks, dst_k
     return load().mi_kv_copy_blocks(ctypes.byref(d), _ptr(src_k), _ptr(src_v), int(src_num_blocks),
                                     _ptr(src_blocks), _ptr(dst_k), _ptr(dst_v), int(dst_num_blocks),
                                     _ptr(dst_blocks), int(n), _ptr(dev_err), _stream(stream))
+
+
+def mi_paged_prefill_attention_variant(d: MiDims, total_q, max_query_len, q, k_cache, v_cache, block_tables,
+                                       context_lens, query_start, scale, out, variant=MI_PREFILL_DEFAULT,
+                                       dev_err=None, stream=None):
+    return load().mi_paged_prefill_attention_variant(ctypes.byref(d), int(total_q), int(max_query_len), _ptr(q),
+                                                     _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                     _ptr(context_lens), _ptr(query_start), float(scale),
+                                                     _ptr(out), _ptr(dev_err), _stream(stream), int(variant))
 
 
 def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tables, context_lens, scale, out,

@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc.cuh"
 #include "tma.cuh"
 
 namespace mi {
@@ -56,6 +57,47 @@ struct PrefillParams {
     int R, Hq, Hkv, G, num_blocks, mbps, T, max_q;
     float sl2;                     // scale * log2(e)
 };
+
+// The work item of a CTA: row tile k (counted from the request's end) of
+// (request r, KV head h), with `tile_rows` (token, head) rows per tile.
+// Returns false when the CTA has nothing to do (past the request's last row,
+// or a bad request, which is reported once).
+struct Item {
+    int r, h, q0, m, n, first, nrows, rho0, rows_here, p_hi, nblk;
+};
+
+__device__ __forceinline__ bool work_item(const PrefillParams& p, int tile_rows, Item& it) {
+    const int kw = blockIdx.x % kTileGroup;
+    const int rest0 = blockIdx.x / kTileGroup;
+    it.h = rest0 % p.Hkv;
+    const int rest = rest0 / p.Hkv;
+    it.r = rest % p.R;
+    const int k = (rest / p.R) * kTileGroup + kw;
+    const bool reporter = k == 0 && it.h == 0 && threadIdx.x == 0;  // one error report per request
+    it.q0 = __ldg(p.query_start + it.r);
+    const int q1 = __ldg(p.query_start + it.r + 1);
+    it.m = q1 - it.q0;
+    if (it.q0 < 0 || q1 > p.T || it.m < 0 || it.m > p.max_q) {
+        if (reporter) raise_err(p.dev_err, MI_DEVERR_BAD_QUERY);
+        return false;
+    }
+    it.nrows = it.m * p.G;
+    const int tiles = (it.nrows + tile_rows - 1) / tile_rows;
+    if (k >= tiles) return false;
+    int n = __ldg(p.context_lens + it.r);
+    if (n > p.mbps * kBlock) {
+        if (reporter) raise_err(p.dev_err, MI_DEVERR_BAD_CONTEXT);
+        n = p.mbps * kBlock;
+    }
+    if (it.m > n && reporter) raise_err(p.dev_err, MI_DEVERR_BAD_QUERY);
+    it.n = n;
+    it.first = n - it.m;  // position of new token 0 (negative only when m > n)
+    it.rho0 = (tiles - 1 - k) * tile_rows;
+    it.rows_here = min(tile_rows, it.nrows - it.rho0);
+    it.p_hi = it.first + (it.rho0 + it.rows_here - 1) / p.G;  // position of the CTA's last row
+    it.nblk = it.p_hi >= 0 ? it.p_hi / kBlock + 1 : 0;        // blocks any row of the CTA reads
+    return true;
+}
 
 template <int HD>
 struct PrefillSmem {
@@ -101,33 +143,10 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
     pdl_trigger();
 
     // ------------------------------------------------------- work item ----
-    const int kw = blockIdx.x % kTileGroup;
-    const int rest0 = blockIdx.x / kTileGroup;
-    const int h = rest0 % p.Hkv;
-    const int rest = rest0 / p.Hkv;
-    const int r = rest % p.R;
-    const int k = (rest / p.R) * kTileGroup + kw;
-    const bool reporter = k == 0 && h == 0 && threadIdx.x == 0;  // one error report per request
-    const int q0 = __ldg(p.query_start + r), q1 = __ldg(p.query_start + r + 1);
-    const int m = q1 - q0;
-    if (q0 < 0 || q1 > p.T || m < 0 || m > p.max_q) {
-        if (reporter) raise_err(p.dev_err, MI_DEVERR_BAD_QUERY);
-        return;
-    }
-    const int nrows = m * p.G;
-    const int tiles = (nrows + kPRows - 1) / kPRows;
-    if (k >= tiles) return;
-    int n = __ldg(p.context_lens + r);
-    if (n > p.mbps * kBlock) {
-        if (reporter) raise_err(p.dev_err, MI_DEVERR_BAD_CONTEXT);
-        n = p.mbps * kBlock;
-    }
-    if (m > n && reporter) raise_err(p.dev_err, MI_DEVERR_BAD_QUERY);
-    const int first = n - m;  // position of new token 0 (negative only when m > n)
-    const int rho0 = (tiles - 1 - k) * kPRows;
-    const int rows_here = min(kPRows, nrows - rho0);
-    const int p_hi = first + (rho0 + rows_here - 1) / p.G;  // position of the CTA's last row
-    const int nblk = p_hi >= 0 ? p_hi / kBlock + 1 : 0;    // blocks any row of the CTA reads
+    Item it;
+    if (!work_item(p, kPRows, it)) return;
+    const int h = it.h, r = it.r, q0 = it.q0, n = it.n, first = it.first, nrows = it.nrows;
+    const int rho0 = it.rho0, rows_here = it.rows_here, p_hi = it.p_hi, nblk = it.nblk;
     const int nst = (nblk + kStageBlocks - 1) / kStageBlocks;
 
     if (threadIdx.x == 0) {
@@ -383,7 +402,337 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
         }
 }
 
+// ------------------------------------------------- tcgen05 prefill kernel --
+//
+// 128 (token, head) rows per CTA on the fifth-generation tensor cores:
+//   * warp 5 (producer) loads the Q tile once and streams 64-key stages (four
+//     16-token blocks, each as two 128-byte-wide TMA boxes for K and two for
+//     V) through a 2-stage ring, in the canonical 128-byte-swizzled layouts:
+//     Q [HD/64][128 rows][128 B], K and V [HD/64][64 keys][128 B];
+//   * one thread of warp 4 issues the UMMAs: S_j = Q . K_j^T (M 128, N 64,
+//     K-major A and B) into one of two tensor-memory score buffers, then,
+//     once the softmax has written P_j, O += P_j . V_j (M 128, N HD, A K-major
+//     from shared memory, B = V MN-major) into the tensor-memory accumulator;
+//     tcgen05.commit signals the mbarriers;
+//   * warps 0-3 (softmax): thread t owns row t, i.e. tensor-memory lane t. It
+//     loads its 64 scores, masks (causal, missing blocks), updates the
+//     running max and sum, rescales its O row in tensor memory when the max
+//     moved, and writes its probabilities as bf16 into the P tile; warp 0
+//     zeroes V rows of keys that are not in the context. After the last
+//     stage each thread reads its O row, normalises it and stores it.
+// Tensor memory: 256 columns per CTA (O in columns 0..HD-1, the two score
+// buffers at 128 and 192); two CTAs per SM.
+
+constexpr int kTcRows = 128;
+constexpr int kTcStages = 2;
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTcCols = 256;
+
+template <int HD>
+struct TcSmem {
+    static constexpr int kH = HD / 64;                    // 128-byte column blocks of a row
+    static constexpr int kQ = 0;                           // Q: kH x [128 rows][128 B]
+    static constexpr int kRing = kQ + kH * kTcRows * 128;
+    static constexpr int kKV = kH * 64 * 128;              // K (or V) of one stage: kH x [64 keys][128 B]
+    static constexpr int kStage = 2 * kKV;
+    static constexpr int kP = kRing + kTcStages * kStage;  // P: [128 rows][64 keys] bf16
+    static constexpr int kBar = kP + kTcRows * 128;
+    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full, o_done, fin
+    static constexpr int kNBar = 1 + 2 * kTcStages + 2 + 2 + 3;
+    static constexpr int kMask = kBar + kNBar * 8;
+    static constexpr int kTmem = kMask + kTcStages * 4;
+    static constexpr int kUsed = kTmem + 16;
+    static constexpr int kSlack = 896;                     // the base is aligned up to 1024 B at run time
+    static constexpr int kTotal = kUsed + kSlack;
+};
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, PrefillParams p) {
+    using SM = TcSmem<HD>;
+    constexpr int kH = SM::kH;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    pdl_wait();
+    pdl_trigger();
+
+    Item it;
+    if (!work_item(p, kTcRows, it)) return;
+    if (sbase - raw > (uint32_t)SM::kSlack) {  // no room to align the tiles
+        if (threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_INTERNAL);
+        return;
+    }
+    const int nst = (it.nblk + kStageBlocks - 1) / kStageBlocks;
+    const uint32_t bar = sbase + SM::kBar;
+    const uint32_t q_full = bar, kv_full0 = bar + 8, kv_empty0 = bar + 8 + 8 * kTcStages;
+    const uint32_t s_full0 = bar + 8 + 16 * kTcStages, s_free0 = s_full0 + 16, p_full = s_free0 + 16;
+    const uint32_t o_done = p_full + 8, fin = o_done + 8;
+    const uint32_t mask0 = sbase + SM::kMask;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(kv_full0 + s * 8, 1);
+            mbar_init(kv_empty0 + s * 8, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full0 + b * 8, 1);
+            mbar_init(s_free0 + b * 8, 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(fin, 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tc::alloc(sbase + SM::kTmem, kTcCols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tbase = lds_u32(sbase + SM::kTmem);
+
+    if (warp == 5) {
+        // ------------------------------------------------ producer warp --
+        const uint64_t policy = l2_policy_evict_normal();
+        if (lane == 0 && nst > 0) {
+            mbar_arrive_expect_tx(q_full, kH * kTcRows * 128);
+            for (int hh = 0; hh < kH; ++hh)
+                tma_load_4d(sbase + SM::kQ + hh * kTcRows * 128, &tmq, q_full, 0, hh, it.h * p.G,
+                            it.q0 + it.rho0 / p.G, policy);
+        }
+        for (int j = 0; j < nst; ++j) {
+            const int sl = j % kTcStages, u = j / kTcStages;
+            if (!wait_all(kv_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) {
+                if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+                break;
+            }
+            const int x = j * kStageBlocks + lane;
+            int blk = -1;
+            bool ok = false;
+            if (lane < kStageBlocks && x < it.nblk) {
+                blk = __ldg(p.block_tables + (long long)it.r * p.mbps + x);
+                ok = blk >= 0 && blk < p.num_blocks;
+                if (!ok) raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
+            }
+            const uint32_t msk = __ballot_sync(0xffffffffu, ok);
+            const uint32_t fb = kv_full0 + sl * 8;
+            if (lane == 0) {
+                sts32(mask0 + sl * 4, msk);
+                mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * 2u * kH * kBlock * 128u);
+            }
+            __syncwarp();
+            if (ok) {
+                const uint32_t kd = sbase + SM::kRing + sl * SM::kStage + lane * kBlock * 128;
+                const int row0 = (blk * p.Hkv + it.h) * kBlock;
+                for (int hh = 0; hh < kH; ++hh) {
+                    tma_load_3d(kd + hh * 64 * 128, &tmk, fb, 0, hh, row0, policy);
+                    tma_load_3d(kd + SM::kKV + hh * 64 * 128, &tmv, fb, 0, hh, row0, policy);
+                }
+            }
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------- MMA issuer ----
+        if (lane == 0 && nst > 0) {
+            constexpr uint32_t idS = tc::idesc_bf16(kTcRows, 64, false);
+            constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
+            bool ok = mbar_wait_bounded(q_full, 0);
+            auto issue_s = [&](int jj) {
+                const int sl = jj % kTcStages, b = jj & 1;
+                const uint32_t kbase = sbase + SM::kRing + sl * SM::kStage;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;  // 16 bf16 of the 128-byte row
+                    const uint64_t a = tc::sdesc_sw128(sbase + SM::kQ + (kk >> 2) * kTcRows * 128 + off, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(kbase + (kk >> 2) * 64 * 128 + off, 16, 1024);
+                    tc::mma_ss(tbase + 128u + 64u * b, a, bd, idS, kk > 0);
+                }
+                tc::commit(s_full0 + b * 8);
+            };
+            if (ok) ok = mbar_wait_bounded(kv_full0, 0);
+            if (ok) {
+                tc::fence_after();
+                issue_s(0);
+            }
+            for (int j = 0; ok && j < nst; ++j) {
+                if (j + 1 < nst) {
+                    const int j1 = j + 1, u1 = j1 >> 1;
+                    ok = mbar_wait_bounded(kv_full0 + (j1 % kTcStages) * 8, (uint32_t)((j1 / kTcStages) & 1));
+                    if (ok && u1 >= 1) ok = mbar_wait_bounded(s_free0 + (j1 & 1) * 8, (uint32_t)((u1 - 1) & 1));
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_s(j1);
+                }
+                if (!(ok = mbar_wait_bounded(p_full, (uint32_t)(j & 1)))) break;
+                tc::fence_after();
+                const uint32_t vbase = sbase + SM::kRing + (j % kTcStages) * SM::kStage + SM::kKV;
+#pragma unroll
+                for (int l = 0; l < kStageBlocks; ++l) {
+                    const uint64_t a = tc::sdesc_sw128(sbase + SM::kP + l * 32, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(vbase + l * kBlock * 128, 64 * 128, 1024);
+                    tc::mma_ss(tbase, a, bd, idO, j > 0 || l > 0);
+                }
+                tc::commit(o_done);
+                tc::commit(kv_empty0 + (j % kTcStages) * 8);
+            }
+            if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            // every MMA issued has finished before tensor memory is released
+            tc::commit(fin);
+            (void)mbar_wait_bounded(fin, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- softmax ----
+        const int t = threadIdx.x;  // row of the tile, tensor-memory lane
+        const int rr = it.rho0 + t;
+        const bool vrow = rr < it.nrows;
+        const int tok = rr / p.G;
+        const int pos = vrow ? it.first + tok : it.p_hi;
+        const int mpos = pos < 0 ? 0 : pos;
+        const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
+        const int nb_ctx = (it.n + kBlock - 1) / kBlock;
+        const int tail = it.n - (nb_ctx - 1) * kBlock;
+        float mrow = -INFINITY, lrow = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nst; ++j) {
+            const int sl = j % kTcStages, b = j & 1;
+            ok = wait_all(kv_full0 + sl * 8, (uint32_t)((j / kTcStages) & 1)) &&
+                 wait_all(s_full0 + b * 8, (uint32_t)((j >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after();
+            uint32_t x[64];
+            tc::ld32(tl + 128u + 64u * b, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tc::ld32(tl + 128u + 64u * b + 32u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tc::wait_ld();
+            tc::fence_before();
+            mbar_arrive(s_free0 + b * 8);
+            const uint32_t present = lds_u32(mask0 + sl * 4);
+            const int kbase = j * kStageBlocks * kBlock;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
+                const float v = keep ? __uint_as_float(x[c]) * p.sl2 : -INFINITY;
+                x[c] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
+            }
+            const float mn = fmaxf(mrow, mx);
+            const float un = mn == -INFINITY ? 0.f : mn;
+            const float alpha = exp2f(mrow - un);
+            mrow = mn;
+            // P and O are free once the previous P . V has finished
+            if (j > 0) {
+                if (!(ok = wait_all(o_done, (uint32_t)((j - 1) & 1)))) break;
+                tc::fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < HD / 32; ++ch) {
+                        uint32_t y[32];
+                        tc::ld32(tl + 32u * ch, y);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
+                        tc::st32(tl + 32u * ch, y);
+                    }
+                    tc::wait_st();
+                }
+            }
+            lrow *= alpha;
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float e0 = exp2f(__uint_as_float(x[2 * c]) - un);
+                const float e1 = exp2f(__uint_as_float(x[2 * c + 1]) - un);
+                lrow += e0 + e1;
+                w[c] = pack_bf16x2(e0, e1);
+            }
+            const uint32_t prow = sbase + SM::kP + t * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((ch ^ (t & 7)) << 4)),
+                             "r"(w[4 * ch]), "r"(w[4 * ch + 1]), "r"(w[4 * ch + 2]), "r"(w[4 * ch + 3])
+                             : "memory");
+            if (warp == 0) {
+                // V rows of keys outside the context (missing blocks, the
+                // last block's tail) may hold any bits: zero them
+                const uint32_t vbase = sbase + SM::kRing + sl * SM::kStage + SM::kKV;
+                for (int l = 0; l < kStageBlocks; ++l) {
+                    const int blk = j * kStageBlocks + l;
+                    const int from = !((present >> l) & 1u) ? 0 : (blk == nb_ctx - 1 && tail < kBlock ? tail : kBlock);
+                    for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
+                        const int key = l * kBlock + from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
+                        st_shared_zero16(vbase + hh * 64 * 128 + key * 128 + ch * 16);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before();
+            mbar_arrive(p_full);
+        }
+        if (!ok && threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+        if (ok && nst > 0) ok = wait_all(o_done, (uint32_t)((nst - 1) & 1));
+        tc::fence_after();
+        const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+        const uint32_t keep = pos >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
+        uint16_t* orow = p.out + ((long long)(it.q0 + tok) * p.Hq + (long long)it.h * p.G + rr % p.G) * HD;
+#pragma unroll 1
+        for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t y[32];
+            if (nst > 0 && ok) {
+                tc::ld32(tl + 32u * ch, y);
+                tc::wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) y[i] = 0u;
+            }
+            if (vrow && ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(y[8 * q4 + 2 * i]) * inv,
+                                            __uint_as_float(y[8 * q4 + 2 * i + 1]) * inv) & keep;
+                    dst[q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc::fence_after();
+        tc::dealloc(tbase, kTcCols);
+    }
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+template <int HD>
+bool prepare_tc() {
+    static std::mutex mu;
+    static bool done[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(prefill_tc_kernel<HD>),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<HD>::kTotal) != cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
+}
 
 template <int HD>
 bool prepare(int* smem) {
@@ -406,13 +755,15 @@ bool prepare(int* smem) {
 }  // namespace
 }  // namespace mi
 
-extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
-                                                const void* q, const void* k_cache, const void* v_cache,
-                                                const int32_t* block_tables, const int32_t* context_lens,
-                                                const int32_t* query_start, float scale, void* out,
-                                                int32_t* dev_err, mi_stream_t stream) {
-    using namespace mi;
+namespace mi {
+namespace {
+
+mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, const void* q, const void* k_cache,
+                  const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                  const int32_t* query_start, float scale, void* out, int32_t* dev_err, mi_stream_t stream,
+                  int32_t variant) {
     if (!dims) return MI_ERR_INVALID_ARG;
+    if (variant < MI_PREFILL_DEFAULT || variant > MI_PREFILL_TCGEN05) return MI_ERR_INVALID_ARG;
     const mi_dims D = *dims;
     if (D.B < 0 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1 || total_q < 0 ||
         max_query_len < 0)
@@ -420,6 +771,11 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
     if (D.block_size != kBlock || (D.head_dim != 64 && D.head_dim != 128) || D.Hq % D.Hkv != 0 ||
         D.Hq / D.Hkv > kMaxGroup)
         return MI_ERR_UNSUPPORTED;
+    const int G = D.Hq / D.Hkv, HD = D.head_dim;
+    // the tcgen05 tile stacks 128 / G tokens of a group: G must divide 128
+    const bool tc_ok = (kTcRows % G) == 0;
+    if (variant == MI_PREFILL_TCGEN05 && !tc_ok) return MI_ERR_UNSUPPORTED;
+    const bool use_tc = variant == MI_PREFILL_TCGEN05 || (variant == MI_PREFILL_DEFAULT && tc_ok);
     if ((long long)D.num_blocks * D.Hkv * kBlock * (D.head_dim / 64) > 0x7FFFFFFFLL ||
         (long long)D.max_blocks_per_seq * kBlock > 0x7FFFFFFFLL || (long long)total_q * D.Hq > 0x7FFFFFFFLL ||
         (long long)max_query_len * D.Hq > 0x7FFFFFFFLL)
@@ -430,16 +786,10 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
         return MI_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return MI_ERR_INVALID_ARG;
-    const int G = D.Hq / D.Hkv, HD = D.head_dim;
-    const long long tiles_max = ((long long)max_query_len * G + kPRows - 1) / kPRows;
+    const int rows_per_tile = use_tc ? kTcRows : kPRows;
+    const long long tiles_max = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
     const long long grid = (tiles_max + kTileGroup - 1) / kTileGroup * kTileGroup * D.B * D.Hkv;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
-
-    int smem = 0;
-    if (!(HD == 64 ? prepare<64>(&smem) : prepare<128>(&smem))) return MI_ERR_CUDA;
-    CUtensorMap tk, tv;
-    const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
-    if (!make_tmap(&tk, k_cache, rows, HD) || !make_tmap(&tv, v_cache, rows, HD)) return MI_ERR_CUDA;
 
     PrefillParams p;
     p.q = static_cast<const uint16_t*>(q);
@@ -457,8 +807,47 @@ extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t tot
     p.T = total_q;
     p.max_q = max_query_len;
     p.sl2 = scale * 1.4426950408889634f;
-    const cudaError_t e =
-        HD == 64 ? launch_pdl(prefill_kernel<64>, (int)grid, (kPWarps + 1) * 32, smem, (cudaStream_t)stream, tk, tv, p)
-                 : launch_pdl(prefill_kernel<128>, (int)grid, (kPWarps + 1) * 32, smem, (cudaStream_t)stream, tk, tv, p);
+    const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (use_tc) {
+        if (!(HD == 64 ? prepare_tc<64>() : prepare_tc<128>())) return MI_ERR_CUDA;
+        CUtensorMap tq, tk, tv;
+        if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, kTcRows) ||
+            !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_halves(&tv, v_cache, rows, HD))
+            return MI_ERR_CUDA;
+        e = HD == 64 ? launch_pdl(prefill_tc_kernel<64>, (int)grid, kTcThreads, TcSmem<64>::kTotal, st, tq, tk, tv, p)
+                     : launch_pdl(prefill_tc_kernel<128>, (int)grid, kTcThreads, TcSmem<128>::kTotal, st, tq, tk, tv,
+                                  p);
+    } else {
+        int smem = 0;
+        if (!(HD == 64 ? prepare<64>(&smem) : prepare<128>(&smem))) return MI_ERR_CUDA;
+        CUtensorMap tk, tv;
+        if (!make_tmap(&tk, k_cache, rows, HD) || !make_tmap(&tv, v_cache, rows, HD)) return MI_ERR_CUDA;
+        e = HD == 64 ? launch_pdl(prefill_kernel<64>, (int)grid, (kPWarps + 1) * 32, smem, st, tk, tv, p)
+                     : launch_pdl(prefill_kernel<128>, (int)grid, (kPWarps + 1) * 32, smem, st, tk, tv, p);
+    }
     return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mi
+
+extern "C" mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
+                                                const void* q, const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                const int32_t* query_start, float scale, void* out,
+                                                int32_t* dev_err, mi_stream_t stream) {
+    return mi::prefill(dims, total_q, max_query_len, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                       scale, out, dev_err, stream, MI_PREFILL_DEFAULT);
+}
+
+extern "C" mi_status mi_paged_prefill_attention_variant(const mi_dims* dims, int32_t total_q,
+                                                        int32_t max_query_len, const void* q, const void* k_cache,
+                                                        const void* v_cache, const int32_t* block_tables,
+                                                        const int32_t* context_lens, const int32_t* query_start,
+                                                        float scale, void* out, int32_t* dev_err,
+                                                        mi_stream_t stream, int32_t variant) {
+    return mi::prefill(dims, total_q, max_query_len, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                       scale, out, dev_err, stream, variant);
 }

@@ -16,13 +16,15 @@ from workloads import (BLOCK, PREFILL_WORKLOADS, bf16_normal, history_cache,
 
 pytestmark = pytest.mark.gpu
 
+VARIANTS = [1, 2]  # MI_PREFILL_MMA (mma.sync tiles), MI_PREFILL_TCGEN05 (tcgen05 + tensor memory)
+
 
 def _mi():
     import paged_kv_decode_25_gb300 as mi
     return mi
 
 
-def _run_prefill(w, device, layer=0, order_seed=None):
+def _run_prefill(w, device, layer=0, order_seed=None, variant=0):
     """Chunked append + prefill attention on the device; returns everything the
     checks need (host copies of the oracle's inputs and the device outputs)."""
     import torch
@@ -60,8 +62,8 @@ def _run_prefill(w, device, layer=0, order_seed=None):
     assert mi.mi_paged_kv_append(d_app, q_d, k_d, v_d, to_dev_i32(pos, device), to_dev_i32(slots, device),
                                  rope_d, w.max_pos, qo_d, kc_d, vc_d, err) == 0
     bt_d, n_d, qs_d = (to_dev_i32(a, device) for a in (bt, n, qs))
-    assert mi.mi_paged_prefill_attention(d_att, T, int(m.max()), qo_d, kc_d, vc_d, bt_d, n_d, qs_d,
-                                         w.scale, out_d, err) == 0
+    assert mi.mi_paged_prefill_attention_variant(d_att, T, int(m.max()), qo_d, kc_d, vc_d, bt_d, n_d, qs_d,
+                                                 w.scale, out_d, variant=variant, dev_err=err) == 0
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # the oracle's append on the host copies
@@ -72,9 +74,10 @@ def _run_prefill(w, device, layer=0, order_seed=None):
                 vc_d=vc_d, out_d=out_d, v_new=v)
 
 
-def test_prefill_small_full_parity(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_small_full_parity(cuda_device, variant):
     w = PREFILL_WORKLOADS["prefill_small"]
-    x = _run_prefill(w, cuda_device, order_seed=3)
+    x = _run_prefill(w, cuda_device, order_seed=3, variant=variant)
     assert np.array_equal(from_dev_u16(x["qo_d"]), x["q_ref"])
     assert np.array_equal(from_dev_u16(x["kc_d"]), x["kc"])
     assert np.array_equal(from_dev_u16(x["vc_d"]), x["vc"])
@@ -88,9 +91,10 @@ def test_prefill_small_full_parity(cuda_device):
         assert np.array_equal(got[0, j], x["v_new"][0, j // G])
 
 
-def test_prefill_qwen3_8b_sampled(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_qwen3_8b_sampled(cuda_device, variant):
     w = PREFILL_WORKLOADS["qwen3_8b_prefill"]
-    x = _run_prefill(w, cuda_device)
+    x = _run_prefill(w, cuda_device, variant=variant)
     # append: the new tokens' rows and slots, bit-exact
     assert np.array_equal(from_dev_u16(x["qo_d"]), x["q_ref"])
     kc_got, vc_got = from_dev_u16(x["kc_d"]), from_dev_u16(x["vc_d"])
@@ -141,7 +145,7 @@ def _random_case(seed, Hq, Hkv, d, hist, new, nb_extra=5):
     return q, kc, vc, bt, n.astype(np.int32), qs
 
 
-def _attend(device, q, kc, vc, bt, n, qs, scale, max_q=None):
+def _attend(device, q, kc, vc, bt, n, qs, scale, max_q=None, variant=0):
     import torch
     mi = _mi()
     T, Hq, d = q.shape
@@ -150,67 +154,72 @@ def _attend(device, q, kc, vc, bt, n, qs, scale, max_q=None):
     out = torch.full((max(T, 1), Hq, d), 7.0, dtype=torch.bfloat16, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     mq = int(np.diff(qs).max()) if max_q is None else max_q
-    st = mi.mi_paged_prefill_attention(dm, T, mq, to_dev_u16(q, device), to_dev_u16(kc, device),
-                                       to_dev_u16(vc, device), to_dev_i32(bt, device), to_dev_i32(n, device),
-                                       to_dev_i32(qs, device), scale, out, err)
+    st = mi.mi_paged_prefill_attention_variant(dm, T, mq, to_dev_u16(q, device), to_dev_u16(kc, device),
+                                               to_dev_u16(vc, device), to_dev_i32(bt, device), to_dev_i32(n, device),
+                                               to_dev_i32(qs, device), scale, out, variant=variant, dev_err=err)
     assert st == 0
     torch.cuda.synchronize()
     return from_dev_u16(out)[:T], int(err.item())
 
 
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 64), (8, 4, 128), (8, 2, 64), (16, 2, 128), (32, 8, 128)])
-def test_prefill_group_and_head_dim(cuda_device, Hq, Hkv, d):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_group_and_head_dim(cuda_device, Hq, Hkv, d, variant):
     hist = [0, 5, 64, 200, 31, 0]
     new = [3, 64, 1, 77, 130, 16]
     q, kc, vc, bt, n, qs = _random_case(Hq * 100 + d, Hq, Hkv, d, hist, new)
     scale = 1.0 / np.sqrt(d)
-    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, scale)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, scale, variant=variant)
     assert err == 0
     ref = oracle.paged_prefill_attention(q, kc, vc, bt, n, qs, scale, nthreads=8)
     assert_attention_close(got, ref, f"G={Hq // Hkv} d={d}")
 
 
-def test_prefill_one_token_requests_match_decode_oracle(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_one_token_requests_match_decode_oracle(cuda_device, variant):
     # m = 1 everywhere: the prefill kernel computes decode attention
     q, kc, vc, bt, n, qs = _random_case(5, 8, 2, 128, [0, 15, 16, 17, 500, 1023], [1] * 6)
-    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.09)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.09, variant=variant)
     assert err == 0
     ref = oracle.paged_attention(q, kc, vc, bt, n, 0.09)
     assert_attention_close(got, ref, "one-token prefill")
 
 
-def test_prefill_paging_invariance_bitwise(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_paging_invariance_bitwise(cuda_device, variant):
     hist, new = [40, 0, 123], [50, 97, 33]
     q, kc, vc, bt, n, qs = _random_case(9, 8, 2, 128, hist, new)
-    a, _ = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.1)
+    a, _ = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.1, variant=variant)
     # move every block to another physical id
     r = np.random.Generator(np.random.PCG64(10))
     perm = r.permutation(kc.shape[0])
     kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
     kc2[perm], vc2[perm] = kc, vc
     bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
-    b, _ = _attend(cuda_device, q, kc2, vc2, bt2, n, qs, 0.1)
+    b, _ = _attend(cuda_device, q, kc2, vc2, bt2, n, qs, 0.1, variant=variant)
     assert np.array_equal(a, b)
 
 
-def test_prefill_edge_lengths(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_edge_lengths(cuda_device, variant):
     # zero-token requests, block-aligned and ragged contexts, one long chunk
     hist = [0, 16, 0, 1, 47, 0, 255]
     new = [0, 16, 32, 0, 1, 65, 1]
     q, kc, vc, bt, n, qs = _random_case(12, 8, 4, 64, hist, new)
-    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.125)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.125, variant=variant)
     assert err == 0
     ref = oracle.paged_prefill_attention(q, kc, vc, bt, n, qs, 0.125)
     assert_attention_close(got, ref, "edge lengths")
 
 
-def test_prefill_error_bits(cuda_device):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_error_bits(cuda_device, variant):
     mi = _mi()
     q, kc, vc, bt, n, qs = _random_case(13, 4, 2, 64, [10, 20], [6, 12])
     # more new tokens than context: rows at negative positions are zero
     n_bad = n.copy()
     n_bad[0] = 4  # 6 new tokens, context 4: tokens 0, 1 at positions -2, -1
-    got, err = _attend(cuda_device, q, kc, vc, bt, n_bad, qs, 0.125)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n_bad, qs, 0.125, variant=variant)
     assert err & mi.MI_DEVERR_BAD_QUERY
     assert np.all(got[:2] == 0)
     ref = oracle.paged_prefill_attention(q, kc, vc, bt, n_bad, qs, 0.125)
@@ -218,11 +227,11 @@ def test_prefill_error_bits(cuda_device):
     # a bad block id: flagged, and the output stays finite
     bt_bad = bt.copy()
     bt_bad[1, 0] = kc.shape[0] + 3
-    got, err = _attend(cuda_device, q, kc, vc, bt_bad, n, qs, 0.125)
+    got, err = _attend(cuda_device, q, kc, vc, bt_bad, n, qs, 0.125, variant=variant)
     assert err & mi.MI_DEVERR_BAD_BLOCK
     assert np.all(np.isfinite(oracle.bf16_to_f64(got)))
     # a request longer than max_query_len is skipped (its rows untouched)
-    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.125, max_q=8)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, 0.125, max_q=8, variant=variant)
     assert err & mi.MI_DEVERR_BAD_QUERY
     assert np.all(oracle.bf16_to_f64(got[6:]) == 7.0)
     ref = oracle.paged_prefill_attention(q, kc, vc, bt, n, qs, 0.125)
@@ -230,9 +239,9 @@ def test_prefill_error_bits(cuda_device):
     # a context longer than a table row
     n_long = n.copy()
     n_long[1] = bt.shape[1] * BLOCK + 5
-    _, err = _attend(cuda_device, q, kc, vc, bt, n_long, qs, 0.125)
+    _, err = _attend(cuda_device, q, kc, vc, bt, n_long, qs, 0.125, variant=variant)
     assert err & mi.MI_DEVERR_BAD_CONTEXT
     # query_start out of order
     qs_bad = np.array([0, 12, 6], np.int32)
-    _, err = _attend(cuda_device, q[:6], kc, vc, bt, n, qs_bad, 0.125, max_q=12)
+    _, err = _attend(cuda_device, q[:6], kc, vc, bt, n, qs_bad, 0.125, max_q=12, variant=variant)
     assert err & mi.MI_DEVERR_BAD_QUERY
