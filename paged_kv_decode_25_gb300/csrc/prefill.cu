@@ -618,17 +618,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const uint32_t present = lds_u32(mask0 + sl * 4);
             const int kbase = j * kStageBlocks * kBlock;
             float mx = -INFINITY;
+            // stages wholly below every row's position with all blocks
+            // present need no mask
+            if (__all_sync(0xffffffffu, present == 0xFu && kbase + kStageBlocks * kBlock - 1 <= mpos)) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
-                const float v = keep ? __uint_as_float(x[c]) * p.sl2 : -INFINITY;
-                x[c] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 64; ++c) {
+                    const float v = __uint_as_float(x[c]) * p.sl2;
+                    x[c] = __float_as_uint(v);
+                    mx = fmaxf(mx, v);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
+                    const float v = keep ? __uint_as_float(x[c]) * p.sl2 : -INFINITY;
+                    x[c] = __float_as_uint(v);
+                    mx = fmaxf(mx, v);
+                }
             }
             const float mn = fmaxf(mrow, mx);
             const float un = mn == -INFINITY ? 0.f : mn;
             const float alpha = exp2f(mrow - un);
             mrow = mn;
+            // probabilities first: they overlap the previous P . V
+            float psum = 0.f;
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float e0 = exp2f(__uint_as_float(x[2 * c]) - un);
+                const float e1 = exp2f(__uint_as_float(x[2 * c + 1]) - un);
+                psum += e0 + e1;
+                w[c] = pack_bf16x2(e0, e1);
+            }
+            lrow = lrow * alpha + psum;
             // P and O are free once the previous P . V has finished
             if (j > 0) {
                 if (!(ok = wait_all(o_done, (uint32_t)((j - 1) & 1)))) break;
@@ -645,15 +667,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     }
                     tc::wait_st();
                 }
-            }
-            lrow *= alpha;
-            uint32_t w[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float e0 = exp2f(__uint_as_float(x[2 * c]) - un);
-                const float e1 = exp2f(__uint_as_float(x[2 * c + 1]) - un);
-                lrow += e0 + e1;
-                w[c] = pack_bf16x2(e0, e1);
             }
             const uint32_t prow = sbase + SM::kP + t * 128;
 #pragma unroll
