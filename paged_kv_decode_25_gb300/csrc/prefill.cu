@@ -435,10 +435,9 @@ struct TcSmem {
     static constexpr int kRing = kQ + kH * kTcRows * 128;
     static constexpr int kKV = kH * 64 * 128;              // K (or V) of one stage: kH x [64 keys][128 B]
     static constexpr int kStage = 2 * kKV;
-    static constexpr int kP = kRing + kTcStages * kStage;  // P: [128 rows][64 keys] bf16
-    static constexpr int kBar = kP + kTcRows * 128;
-    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full, o_done, fin
-    static constexpr int kNBar = 1 + 2 * kTcStages + 2 + 2 + 3;
+    static constexpr int kBar = kRing + kTcStages * kStage;
+    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full, o_done[2], fin
+    static constexpr int kNBar = 1 + 2 * kTcStages + 2 + 2 + 4;
     static constexpr int kMask = kBar + kNBar * 8;
     static constexpr int kTmem = kMask + kTcStages * 4;
     static constexpr int kUsed = kTmem + 16;
@@ -474,7 +473,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const uint32_t bar = sbase + SM::kBar;
     const uint32_t q_full = bar, kv_full0 = bar + 8, kv_empty0 = bar + 8 + 8 * kTcStages;
     const uint32_t s_full0 = bar + 8 + 16 * kTcStages, s_free0 = s_full0 + 16, p_full = s_free0 + 16;
-    const uint32_t o_done = p_full + 8, fin = o_done + 8;
+    // o_done[b] completes when P . V of a stage with parity b has finished: one
+    // barrier per parity keeps every wait within one phase of the barrier,
+    // although softmax warps may run a stage apart
+    const uint32_t o_done0 = p_full + 8, fin = o_done0 + 16;
     const uint32_t mask0 = sbase + SM::kMask;
 
     if (threadIdx.x == 0) {
@@ -485,10 +487,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full0 + b * 8, 1);
-            mbar_init(s_free0 + b * 8, 128);
+            mbar_init(s_free0 + b * 8, 1);
         }
         mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
+        mbar_init(o_done0, 1);
+        mbar_init(o_done0 + 8, 1);
         mbar_init(fin, 1);
         fence_mbar_init();
     }
@@ -575,13 +578,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (!(ok = mbar_wait_bounded(p_full, (uint32_t)(j & 1)))) break;
                 tc::fence_after();
                 const uint32_t vbase = sbase + SM::kRing + (j % kTcStages) * SM::kStage + SM::kKV;
+                // P_j sits in the first 32 columns of its score buffer (bf16 pairs)
+                const uint32_t pcol = tbase + 128u + 64u * (j & 1);
 #pragma unroll
                 for (int l = 0; l < kStageBlocks; ++l) {
-                    const uint64_t a = tc::sdesc_sw128(sbase + SM::kP + l * 32, 16, 1024);
                     const uint64_t bd = tc::sdesc_sw128(vbase + l * kBlock * 128, 64 * 128, 1024);
-                    tc::mma_ss(tbase, a, bd, idO, j > 0 || l > 0);
+                    tc::mma_ts(tbase, pcol + 8u * l, bd, idO, j > 0 || l > 0);
                 }
-                tc::commit(o_done);
+                tc::commit(o_done0 + (j & 1) * 8);
+                tc::commit(s_free0 + (j & 1) * 8);  // the buffer's P has been read
                 tc::commit(kv_empty0 + (j % kTcStages) * 8);
             }
             if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
@@ -613,8 +618,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc::ld32(tl + 128u + 64u * b, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
             tc::ld32(tl + 128u + 64u * b + 32u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
             tc::wait_ld();
-            tc::fence_before();
-            mbar_arrive(s_free0 + b * 8);
             const uint32_t present = lds_u32(mask0 + sl * 4);
             const int kbase = j * kStageBlocks * kBlock;
             float mx = -INFINITY;
@@ -636,11 +639,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     mx = fmaxf(mx, v);
                 }
             }
-            const float mn = fmaxf(mrow, mx);
-            const float un = mn == -INFINITY ? 0.f : mn;
-            const float alpha = exp2f(mrow - un);
-            mrow = mn;
-            // probabilities first: they overlap the previous P . V
+            // Lazy rescaling: the reference max only moves when the new max
+            // exceeds it by more than 2^8 (weights stay <= 256); O and l are
+            // rescaled together, so the normalised result is unchanged.
+            float alpha = 1.f;
+            bool need = false;
+            if (mrow == -INFINITY) {
+                mrow = mx;  // nothing accumulated yet: O row and l are zero
+            } else if (mx > mrow + 8.f) {
+                alpha = exp2f(mrow - mx);
+                mrow = mx;
+                need = true;
+            }
+            const float un = mrow == -INFINITY ? 0.f : mrow;
             float psum = 0.f;
             uint32_t w[32];
 #pragma unroll
@@ -651,29 +662,23 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 w[c] = pack_bf16x2(e0, e1);
             }
             lrow = lrow * alpha + psum;
-            // P and O are free once the previous P . V has finished
-            if (j > 0) {
-                if (!(ok = wait_all(o_done, (uint32_t)((j - 1) & 1)))) break;
+            if (__any_sync(0xffffffffu, need)) {
+                // O may be touched once the previous P . V has finished
+                if (!(ok = wait_all(o_done0 + ((j - 1) & 1) * 8, (uint32_t)(((j - 1) >> 1) & 1)))) break;
                 tc::fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int ch = 0; ch < HD / 32; ++ch) {
-                        uint32_t y[32];
-                        tc::ld32(tl + 32u * ch, y);
-                        tc::wait_ld();
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    uint32_t y[32];
+                    tc::ld32(tl + 32u * ch, y);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
-                        tc::st32(tl + 32u * ch, y);
-                    }
-                    tc::wait_st();
+                    for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
+                    tc::st32(tl + 32u * ch, y);
                 }
             }
-            const uint32_t prow = sbase + SM::kP + t * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((ch ^ (t & 7)) << 4)),
-                             "r"(w[4 * ch]), "r"(w[4 * ch + 1]), "r"(w[4 * ch + 2]), "r"(w[4 * ch + 3])
-                             : "memory");
+            // P over the consumed scores: the A operand of O += P . V
+            tc::st32(tl + 128u + 64u * b, w);
+            tc::wait_st();
             if (warp == 0) {
                 // V rows of keys outside the context (missing blocks, the
                 // last block's tail) may hold any bits: zero them
@@ -692,7 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_arrive(p_full);
         }
         if (!ok && threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
-        if (ok && nst > 0) ok = wait_all(o_done, (uint32_t)((nst - 1) & 1));
+        if (ok && nst > 0) ok = wait_all(o_done0 + ((nst - 1) & 1) * 8, (uint32_t)(((nst - 1) >> 1) & 1));
         tc::fence_after();
         const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
         const uint32_t keep = pos >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
