@@ -1,9 +1,11 @@
 // mi_paged_kv_append: RoPE on the new token's q/k, then scatter k/v into the
 // paged cache through slot_mapping (mini-infer README, "decode_batch 关键步骤",
 // write_decode_kv; RoPE as the NJU course brief "端侧大模型推理框架" §2.1 lists
-// it). The rotation is done in double from bf16 inputs and fp32 table values
-// (each product exact), then rounded once to bf16, so the result is a fixed
-// function of the inputs.
+// it). The rotation is defined in double from bf16 inputs and fp32 table
+// values (each product exact), then rounded once to bf16, so the result is a
+// fixed function of the inputs; it is computed in single precision with
+// error-free transformations when that provably gives the same bits, else in
+// double.
 #include "common.cuh"
 
 namespace mi {
@@ -34,6 +36,36 @@ __device__ __forceinline__ uint32_t rot_lo(double a, double b, double c, double 
 }
 __device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double d) {
     return f64_to_bf16(fma(a, b, c * d));
+}
+
+// RN_bf16(RN_double(a*b + c*d)) for bf16 a, c and fp32 b, d, in single
+// precision when that decides it. Both products are split exactly (the fma
+// recovers each rounding error, exact above the underflow range) and their sum
+// is split exactly (two-sum), so exact = s + t + pe + qe with s the rounded
+// sum. When no bf16 rounding boundary (a midpoint between neighbouring bf16
+// values, or one across a binade below) lies within the bound on |exact - s|
+// plus the double rounding's 2^-52 |s| of s, the answer is RN_bf16(s).
+// Otherwise (a boundary within reach, zero, tiny, infinite or NaN values)
+// `slow` is set and the caller takes the double-precision route.
+// The _rn intrinsics keep the compiler from contracting the transforms into
+// fused multiply-adds, which would break their exactness.
+__device__ __forceinline__ uint32_t rot_fast(float a, float b, float c, float d, bool& slow) {
+    const float p = __fmul_rn(a, b), q = __fmul_rn(c, d);
+    const float pe = fmaf(a, b, -p), qe = fmaf(c, d, -q);
+    const float s = __fadd_rn(p, q);
+    const float bb = __fsub_rn(s, p);
+    const float t = __fadd_rn(__fsub_rn(p, __fsub_rn(s, bb)), __fsub_rn(q, bb));
+    const float err = __fadd_rn(__fmul_rn(__fadd_rn(__fadd_rn(fabsf(t), fabsf(pe)), fabsf(qe)), 1.0001f),
+                                __fmul_rn(fabsf(s), 0x1p-50f));
+    const uint32_t S = __float_as_uint(fabsf(s));
+    const int L = (int)(S & 0xFFFFu);
+    const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L) - 2;
+    const float ulp = __uint_as_float((S & 0x7F800000u) - (23u << 23));
+    const float tiny = 0x1p-100f;
+    const bool ok = isfinite(s) && (p == 0.f || fabsf(p) >= tiny) && (q == 0.f || fabsf(q) >= tiny) &&
+                    fabsf(s) >= tiny && err < __fmul_rn((float)dist, ulp);
+    slow |= !ok;
+    return f32_to_bf16(s);
 }
 
 struct AppendParams {
@@ -119,14 +151,24 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             // pairs 2j and 2j+1 of the group: (cos, sin) = cs[j].xy and cs[j].zw
-            const double a0 = bf16_bits_to_f64(xl[j] & 0xFFFFu), a1 = bf16_bits_to_f64(xl[j] >> 16);
-            const double b0 = bf16_bits_to_f64(xh[j] & 0xFFFFu), b1 = bf16_bits_to_f64(xh[j] >> 16);
-            const double c0 = f32_to_f64_bits(cs[j].x), s0 = f32_to_f64_bits(cs[j].y);
-            const double c1 = f32_to_f64_bits(cs[j].z), s1 = f32_to_f64_bits(cs[j].w);
-            const uint32_t r0 = rot_lo(a0, c0, b0, s0);
-            const uint32_t r1 = rot_lo(a1, c1, b1, s1);
-            const uint32_t r2 = rot_hi(b0, c0, a0, s0);
-            const uint32_t r3 = rot_hi(b1, c1, a1, s1);
+            const float fa0 = bf16_lo(xl[j]), fa1 = bf16_hi(xl[j]);
+            const float fb0 = bf16_lo(xh[j]), fb1 = bf16_hi(xh[j]);
+            bool slow = false;
+            uint32_t r0 = rot_fast(fa0, cs[j].x, -fb0, cs[j].y, slow);
+            uint32_t r1 = rot_fast(fa1, cs[j].z, -fb1, cs[j].w, slow);
+            uint32_t r2 = rot_fast(fb0, cs[j].x, fa0, cs[j].y, slow);
+            uint32_t r3 = rot_fast(fb1, cs[j].z, fa1, cs[j].w, slow);
+            if (slow) {
+                // rare: the exact products and one double rounding decide it
+                const double a0 = bf16_bits_to_f64(xl[j] & 0xFFFFu), a1 = bf16_bits_to_f64(xl[j] >> 16);
+                const double b0 = bf16_bits_to_f64(xh[j] & 0xFFFFu), b1 = bf16_bits_to_f64(xh[j] >> 16);
+                const double c0 = f32_to_f64_bits(cs[j].x), s0 = f32_to_f64_bits(cs[j].y);
+                const double c1 = f32_to_f64_bits(cs[j].z), s1 = f32_to_f64_bits(cs[j].w);
+                r0 = rot_lo(a0, c0, b0, s0);
+                r1 = rot_lo(a1, c1, b1, s1);
+                r2 = rot_hi(b0, c0, a0, s0);
+                r3 = rot_hi(b1, c1, a1, s1);
+            }
             yl[j] = r0 | (r1 << 16);
             yh[j] = r2 | (r3 << 16);
         }

@@ -188,3 +188,44 @@ def test_append_bit_exact_on_extreme_values(cuda_device):
     assert np.array_equal(from_dev_u16(qo_d), q_ref)
     assert np.array_equal(from_dev_u16(kc_d), kc_ref)
     assert np.array_equal(from_dev_u16(vc_d), vc_ref)
+
+
+def test_append_rotation_bit_exact_on_wide_values(cuda_device):
+    """4,096 rows of q (32 heads) and k (8 heads) at positions spread over a
+    32k table, values over many binades (with zeros of both signs and the
+    bf16 extremes): every rotated output equals the oracle's bit for bit,
+    whichever internal route (single precision with exact transforms, or
+    double) a kernel thread takes."""
+    import torch
+    mi = _mi()
+    r = np.random.Generator(np.random.PCG64(31))
+    B, Hq, Hkv, d, max_pos, nb = 4096, 32, 8, 128, 32768, 300
+    def wide(shape):
+        x = r.standard_normal(shape) * 2.0 ** r.integers(-40, 40, shape)
+        x[r.random(shape) < 0.01] = 0.0
+        x[r.random(shape) < 0.01] = -0.0
+        x[r.random(shape) < 0.001] = 3.3e38
+        x[r.random(shape) < 0.001] = -1e-38
+        return oracle.f64_to_bf16(x)
+    q, k, v = wide((B, Hq, d)), wide((B, Hkv, d)), wide((B, Hkv, d))
+    pos = r.integers(0, max_pos, B).astype(np.int32)
+    slots = r.permutation(nb * 16)[:B].astype(np.int32)
+    _, table = mi.mi_rope_table(1e6, d, max_pos)
+    table_ref = oracle.rope_table(1e6, d, max_pos)
+    kc = np.zeros((nb, Hkv, 16, d), np.uint16)
+    vc = kc.copy()
+    dm = mi.dims(B, Hq, Hkv, d, nb, 1)
+    q_d = to_dev_u16(q, cuda_device)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(vc, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    qo_d = torch.empty_like(q_d)
+    assert mi.mi_paged_kv_append(dm, q_d, to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                 to_dev_i32(pos, cuda_device), to_dev_i32(slots, cuda_device),
+                                 torch.from_numpy(table).to(cuda_device), max_pos, qo_d, kc_d, vc_d, err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q_ref, st = oracle.append(q, k, v, pos, slots, table_ref, kc, vc)
+    assert st == 0
+    assert np.array_equal(from_dev_u16(qo_d), q_ref)
+    assert np.array_equal(from_dev_u16(kc_d), kc)
+    assert np.array_equal(from_dev_u16(vc_d), vc)
