@@ -620,7 +620,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc::wait_ld();
             const uint32_t present = lds_u32(mask0 + sl * 4);
             const int kbase = j * kStageBlocks * kBlock;
-            float mx = -INFINITY;
+            // eight independent partial maxima keep the dependency chains short
+            float mp[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
             // stages wholly below every row's position with all blocks
             // present need no mask
             if (__all_sync(0xffffffffu, present == 0xFu && kbase + kStageBlocks * kBlock - 1 <= mpos)) {
@@ -628,7 +631,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 for (int c = 0; c < 64; ++c) {
                     const float v = __uint_as_float(x[c]) * p.sl2;
                     x[c] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
+                    mp[c & 7] = fmaxf(mp[c & 7], v);
                 }
             } else {
 #pragma unroll
@@ -636,9 +639,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
                     const float v = keep ? __uint_as_float(x[c]) * p.sl2 : -INFINITY;
                     x[c] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
+                    mp[c & 7] = fmaxf(mp[c & 7], v);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             // Lazy rescaling: the reference max only moves when the new max
             // exceeds it by more than 2^8 (weights stay <= 256); O and l are
             // rescaled together, so the normalised result is unchanged.
@@ -652,15 +657,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 need = true;
             }
             const float un = mrow == -INFINITY ? 0.f : mrow;
-            float psum = 0.f;
+            float ps[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float e0 = exp2f(__uint_as_float(x[2 * c]) - un);
                 const float e1 = exp2f(__uint_as_float(x[2 * c + 1]) - un);
-                psum += e0 + e1;
+                ps[c & 7] += e0 + e1;
                 w[c] = pack_bf16x2(e0, e1);
             }
+            const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             lrow = lrow * alpha + psum;
             if (__any_sync(0xffffffffu, need)) {
                 // O may be touched once the previous P . V has finished
