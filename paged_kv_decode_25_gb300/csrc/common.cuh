@@ -59,6 +59,14 @@ __device__ __forceinline__ uint16_t f64_to_bf16(double x) {
     return (uint16_t)(sign | (uint16_t)bits);
 }
 
+// 2^x on the special-function unit (results below 2^-126 flush to zero,
+// which for attention weights relative to the row max is immaterial).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------- errors ------
 
 __device__ __forceinline__ void raise_err(int32_t* dev_err, int bit) {

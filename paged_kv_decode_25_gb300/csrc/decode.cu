@@ -277,11 +277,11 @@ struct MmaState {
         }
         const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
         const float r0 = mn0 == kNegInf ? 0.f : mn0, r1 = mn1 == kNegInf ? 0.f : mn1;
-        const float al0 = exp2f(m[0] - r0), al1 = exp2f(m[1] - r1);
+        const float al0 = ex2(m[0] - r0), al1 = ex2(m[1] - r1);
         m[0] = mn0;
         m[1] = mn1;
-        const uint32_t x0 = pack_bf16x2(exp2f(s0 - r0), exp2f(s1 - r1));
-        const uint32_t x1 = pack_bf16x2(exp2f(s2 - r0), exp2f(s3 - r1));
+        const uint32_t x0 = pack_bf16x2(ex2(s0 - r0), ex2(s1 - r1));
+        const uint32_t x1 = pack_bf16x2(ex2(s2 - r0), ex2(s3 - r1));
         // the sums use the same bf16-rounded weights the PV product uses
         l[0] = l[0] * al0 + (bf16_lo(x0) + bf16_lo(x1));
         l[1] = l[1] * al1 + (bf16_hi(x0) + bf16_hi(x1));
@@ -405,11 +405,11 @@ struct Fp8State {
         }
         const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
         const float r0 = mn0 == kNegInf ? 0.f : mn0, r1 = mn1 == kNegInf ? 0.f : mn1;
-        const float al0 = exp2f(m[0] - r0), al1 = exp2f(m[1] - r1);
+        const float al0 = ex2(m[0] - r0), al1 = ex2(m[1] - r1);
         m[0] = mn0;
         m[1] = mn1;
-        const uint32_t x0 = pack_f16x2(exp2f(s0 - r0), exp2f(s1 - r1));
-        const uint32_t x1 = pack_f16x2(exp2f(s2 - r0), exp2f(s3 - r1));
+        const uint32_t x0 = pack_f16x2(ex2(s0 - r0), ex2(s1 - r1));
+        const uint32_t x1 = pack_f16x2(ex2(s2 - r0), ex2(s3 - r1));
         l[0] = l[0] * al0 + (f16_lo(x0) + f16_lo(x1));
         l[1] = l[1] * al1 + (f16_hi(x0) + f16_hi(x1));
         if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {

@@ -445,14 +445,6 @@ struct TcSmem {
     static constexpr int kTotal = kUsed + kSlack;
 };
 
-// 2^x on the special-function unit (results below 2^-126 flush to zero,
-// which for attention weights relative to the row max is immaterial).
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
 }
