@@ -803,6 +803,10 @@ def main():
     attn_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
                for layer in range(w.layers)]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    # append of layer l runs between the end of layer l-1's attention and its own end event
+    app_ms = [evs[s][layer - 1][1].elapsed_time(evs[s][layer][0]) for s in range(args.steps)
+              for layer in range(1, w.layers)]
+    app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
     a_bytes = attention_bytes(w, cl, kvb)
     step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
     value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
@@ -867,6 +871,8 @@ def main():
                        kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16"),
         "steps_per_s": 1e3 / step_ms * world,
         "hbm_frac_step": value / world / peak,
+        "per_layer_ms": {"append": app_avg_ms, "attention": attn_avg_ms, "append+attention": step_ms / w.layers,
+                         "append_bytes": append_bytes(w, kvb), "attention_bytes": a_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "paged decode attention (split-KV kernel with the LSE combine of cut units fused), per layer",

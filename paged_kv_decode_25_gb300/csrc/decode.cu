@@ -640,9 +640,12 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 
 // W consumer warps (compute, merge) and one producer warp (block-table walk
 // and TMA issue in lanes 0..W-1, zero rows for empty requests in the rest).
-// Consumers synchronise among themselves on named barrier 1.
+// Consumers synchronise among themselves on named barrier 1. The e4m3 tile
+// runs three CTAs per SM (its per-block conversions make it latency-bound,
+// so more resident warps pay; its tiles are half the size, so the stages
+// still fit), the others two.
 template <int HD, int VAR, int GP, int W>
-__global__ void __launch_bounds__((W + 1) * 32, 2)
+__global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -940,13 +943,18 @@ constexpr int kWarps = 4;                 // consumer warps; one producer warp m
 constexpr int kMaxStages = 3;             // bf16 tiles; e4m3 tiles take twice as many
 constexpr int kSmemLimit = 227 * 1024;    // per CTA
 constexpr int kSmemTwoPerSm = 115712;     // per CTA so that two fit in an SM's 228 KB
+constexpr int kSmemThreePerSm = 76800;    // per CTA so that three fit
 
 // Stages per consumer warp: as many as fit with two CTAs per SM, else (very
 // wide GQA groups) as many as fit one CTA. e4m3 tiles are half the size, so
-// twice the stages keep the same bytes in flight.
+// they take up to twice the stages, and first try for three CTAs per SM with
+// at least two stages each.
 int pick_stages(int HD, int G, int var) {
     const bool fma = var == kVarFma;
     const int eb = elem_bytes(var), top = kMaxStages * 2 / eb;
+    if (var == kVarFp8)
+        for (int S = top; S >= 2; --S)
+            if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemThreePerSm) return S;
     for (int S = top; S >= 1; --S)
         if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemTwoPerSm) return S;
     for (int S = top; S >= 1; --S)
