@@ -1109,10 +1109,15 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     const int S = pick_stages(HD, G, var);
     const int smem = smem_of(HD, G, var);
+    // the workspace is sized for the widest grid of any variant; this
+    // kernel's own persistent grid is its SMs x resident CTAs
     const int gmax = max_grid(D);
     if (gmax <= 0) return MI_ERR_CUDA;
     if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
-    const int grid = ctas > 0 && ctas < gmax ? ctas : gmax;
+    KernelFn fn = pick_kernel(HD, var, G);
+    const int gown = grid_for(fn, smem);
+    if (gown <= 0 || gown > gmax) return MI_ERR_CUDA;
+    const int grid = ctas > 0 && ctas < gown ? ctas : gown;
 
     CUtensorMap tk, tv;
     const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
@@ -1143,7 +1148,6 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.v_scale = v_scale;
 
     cudaStream_t s = (cudaStream_t)stream;
-    KernelFn fn = pick_kernel(HD, var, G);
     return launch_pdl(fn, grid, (kWarps + 1) * 32, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }
 
