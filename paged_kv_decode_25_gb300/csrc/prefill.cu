@@ -406,9 +406,13 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
 //
 // 128 (token, head) rows per CTA on the fifth-generation tensor cores:
 //   * warp 5 (producer) loads the Q tile once and streams 64-key stages (four
-//     16-token blocks, each as two 128-byte-wide TMA boxes for K and two for
-//     V) through a 2-stage ring, in the canonical 128-byte-swizzled layouts:
-//     Q [HD/64][128 rows][128 B], K and V [HD/64][64 keys][128 B];
+//     16-token blocks, each as HD/64 128-byte-wide TMA boxes) through separate
+//     K and V rings of two stages, in the canonical 128-byte-swizzled layouts:
+//     Q [HD/64][128 rows][128 B], K and V [HD/64][64 keys][128 B]. A K stage
+//     is handed back as soon as S = Q . K^T has read it, a V stage once
+//     P . V has; K of stage j is issued before V of stage j - 1. (With one
+//     barrier pair for K and V together, each K load waited for the P . V of
+//     two stages back, and the kernel ran 1.36x slower.)
 //   * one thread of warp 4 issues the UMMAs: S_j = Q . K_j^T (M 128, N 64,
 //     K-major A and B) into one of two tensor-memory score buffers, then,
 //     once the softmax has written P_j, O += P_j . V_j (M 128, N HD, A K-major
@@ -424,7 +428,8 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
 // buffers at 128 and 192); two CTAs per SM.
 
 constexpr int kTcRows = 128;
-constexpr int kTcStages = 2;
+constexpr int kTcK = 2;  // K stages
+constexpr int kTcV = 2;  // V stages
 constexpr int kTcThreads = 192;
 constexpr uint32_t kTcCols = 256;
 
@@ -432,17 +437,22 @@ template <int HD>
 struct TcSmem {
     static constexpr int kH = HD / 64;                    // 128-byte column blocks of a row
     static constexpr int kQ = 0;                           // Q: kH x [128 rows][128 B]
-    static constexpr int kRing = kQ + kH * kTcRows * 128;
     static constexpr int kKV = kH * 64 * 128;              // K (or V) of one stage: kH x [64 keys][128 B]
-    static constexpr int kStage = 2 * kKV;
-    static constexpr int kBar = kRing + kTcStages * kStage;
-    // q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full, o_done[2], fin
-    static constexpr int kNBar = 1 + 2 * kTcStages + 2 + 2 + 4;
+    static constexpr int kRingK = kQ + kH * kTcRows * 128;
+    static constexpr int kRingV = kRingK + kTcK * kKV;
+    static constexpr int kBar = kRingV + kTcV * kKV;
+    // q_full, k_full[2 kTcK], k_empty[kTcK], v_full[kTcV], v_empty[kTcV], s_full[2], s_free[2], p_full,
+    // o_done[2], fin
+    static constexpr int kNBar = 1 + 3 * kTcK + 2 * kTcV + 2 + 2 + 4;
     static constexpr int kMask = kBar + kNBar * 8;
-    static constexpr int kTmem = kMask + kTcStages * 4;
+    static constexpr int kTmem = kMask + 2 * kTcK * 4;     // block masks of stages j mod 2 kTcK
     static constexpr int kUsed = kTmem + 16;
-    static constexpr int kSlack = 896;                     // the base is aligned up to 1024 B at run time
+    // the base is aligned up to 1024 B at run time; two CTAs per SM leave
+    // 115,712 B each, so the slack is what remains of that (none needed when
+    // the dynamic shared memory starts on a 1024-byte boundary)
+    static constexpr int kSlack = 115712 - kUsed < 896 ? 115712 - kUsed : 896;
     static constexpr int kTotal = kUsed + kSlack;
+    static_assert(kSlack >= 0, "shared memory plan exceeds two CTAs per SM");
 };
 
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
@@ -471,8 +481,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     const int nst = (it.nblk + kStageBlocks - 1) / kStageBlocks;
     const uint32_t bar = sbase + SM::kBar;
-    const uint32_t q_full = bar, kv_full0 = bar + 8, kv_empty0 = bar + 8 + 8 * kTcStages;
-    const uint32_t s_full0 = bar + 8 + 16 * kTcStages, s_free0 = s_full0 + 16, p_full = s_free0 + 16;
+    // K and V of a stage have their own barriers: a K stage is handed back as
+    // soon as S = Q . K^T has read it, a V stage once P . V has. K of stage
+    // j lands on k_full[j mod 2S]: the softmax warps wait on it too (for the
+    // block mask), and with 2S barriers the next phase of the one a warp
+    // waits on needs that warp's own P first, so no wait can see a phase
+    // ahead of the one it means.
+    const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 16 * kTcK;
+    const uint32_t v_full0 = k_empty0 + 8 * kTcK, v_empty0 = v_full0 + 8 * kTcV;
+    const uint32_t s_full0 = v_empty0 + 8 * kTcV, s_free0 = s_full0 + 16, p_full = s_free0 + 16;
     // o_done[b] completes when P . V of a stage with parity b has finished: one
     // barrier per parity keeps every wait within one phase of the barrier,
     // although softmax warps may run a stage apart
@@ -481,9 +498,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(kv_full0 + s * 8, 1);
-            mbar_init(kv_empty0 + s * 8, 1);
+        for (int s = 0; s < 2 * kTcK; ++s) mbar_init(k_full0 + s * 8, 1);
+        for (int s = 0; s < kTcK; ++s) mbar_init(k_empty0 + s * 8, 1);
+        for (int s = 0; s < kTcV; ++s) {
+            mbar_init(v_full0 + s * 8, 1);
+            mbar_init(v_empty0 + s * 8, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full0 + b * 8, 1);
@@ -513,10 +532,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 tma_load_4d(sbase + SM::kQ + hh * kTcRows * 128, &tmq, q_full, 0, hh, it.h * p.G,
                             it.q0 + it.rho0 / p.G, policy);
         }
+        // K of stage j is issued before V of stage j - 1: V is needed a
+        // softmax later than K, and its stage frees up later
+        int pblk = -1;
+        bool pok = false;
+        auto load_v = [&](int jv) -> bool {
+            const int sl = jv % kTcV, u = jv / kTcV;
+            if (!wait_all(v_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) return false;
+            const uint32_t msk = __ballot_sync(0xffffffffu, pok);
+            const uint32_t fb = v_full0 + sl * 8;
+            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
+            __syncwarp();
+            if (pok) {
+                const uint32_t vd = sbase + SM::kRingV + sl * SM::kKV + lane * kBlock * 128;
+                const int row0 = (pblk * p.Hkv + it.h) * kBlock;
+                for (int hh = 0; hh < kH; ++hh) tma_load_3d(vd + hh * 64 * 128, &tmv, fb, 0, hh, row0, policy);
+            }
+            return true;
+        };
+        bool pgood = true;
         for (int j = 0; j < nst; ++j) {
-            const int sl = j % kTcStages, u = j / kTcStages;
-            if (!wait_all(kv_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) {
-                if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            const int sl = j % kTcK, u = j / kTcK;
+            if (!wait_all(k_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) {
+                pgood = false;
                 break;
             }
             const int x = j * kStageBlocks + lane;
@@ -528,21 +566,26 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 if (!ok) raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
             }
             const uint32_t msk = __ballot_sync(0xffffffffu, ok);
-            const uint32_t fb = kv_full0 + sl * 8;
+            const uint32_t fb = k_full0 + (j % (2 * kTcK)) * 8;
             if (lane == 0) {
-                sts32(mask0 + sl * 4, msk);
-                mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * 2u * kH * kBlock * 128u);
+                sts32(mask0 + (j % (2 * kTcK)) * 4, msk);
+                mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
             }
             __syncwarp();
             if (ok) {
-                const uint32_t kd = sbase + SM::kRing + sl * SM::kStage + lane * kBlock * 128;
+                const uint32_t kd = sbase + SM::kRingK + sl * SM::kKV + lane * kBlock * 128;
                 const int row0 = (blk * p.Hkv + it.h) * kBlock;
-                for (int hh = 0; hh < kH; ++hh) {
-                    tma_load_3d(kd + hh * 64 * 128, &tmk, fb, 0, hh, row0, policy);
-                    tma_load_3d(kd + SM::kKV + hh * 64 * 128, &tmv, fb, 0, hh, row0, policy);
-                }
+                for (int hh = 0; hh < kH; ++hh) tma_load_3d(kd + hh * 64 * 128, &tmk, fb, 0, hh, row0, policy);
             }
+            if (j > 0 && !load_v(j - 1)) {
+                pgood = false;
+                break;
+            }
+            pblk = blk;
+            pok = ok;
         }
+        if (pgood && nst > 0 && !load_v(nst - 1)) pgood = false;
+        if (!pgood && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
     } else if (warp == 4) {
         // ------------------------------------------------- MMA issuer ----
         if (lane == 0 && nst > 0) {
@@ -550,8 +593,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             auto issue_s = [&](int jj) {
-                const int sl = jj % kTcStages, b = jj & 1;
-                const uint32_t kbase = sbase + SM::kRing + sl * SM::kStage;
+                const int sl = jj % kTcK, b = jj & 1;
+                const uint32_t kbase = sbase + SM::kRingK + sl * SM::kKV;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;  // 16 bf16 of the 128-byte row
@@ -560,8 +603,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     tc::mma_ss(tbase + 128u + 64u * b, a, bd, idS, kk > 0);
                 }
                 tc::commit(s_full0 + b * 8);
+                tc::commit(k_empty0 + sl * 8);  // S_jj has read its K stage
             };
-            if (ok) ok = mbar_wait_bounded(kv_full0, 0);
+            if (ok) ok = mbar_wait_bounded(k_full0, 0);
             if (ok) {
                 tc::fence_after();
                 issue_s(0);
@@ -569,15 +613,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int j = 0; ok && j < nst; ++j) {
                 if (j + 1 < nst) {
                     const int j1 = j + 1, u1 = j1 >> 1;
-                    ok = mbar_wait_bounded(kv_full0 + (j1 % kTcStages) * 8, (uint32_t)((j1 / kTcStages) & 1));
+                    ok = mbar_wait_bounded(k_full0 + (j1 % (2 * kTcK)) * 8, (uint32_t)((j1 / (2 * kTcK)) & 1));
                     if (ok && u1 >= 1) ok = mbar_wait_bounded(s_free0 + (j1 & 1) * 8, (uint32_t)((u1 - 1) & 1));
                     if (!ok) break;
                     tc::fence_after();
                     issue_s(j1);
                 }
                 if (!(ok = mbar_wait_bounded(p_full, (uint32_t)(j & 1)))) break;
+                if (!(ok = mbar_wait_bounded(v_full0 + (j % kTcV) * 8, (uint32_t)((j / kTcV) & 1)))) break;
                 tc::fence_after();
-                const uint32_t vbase = sbase + SM::kRing + (j % kTcStages) * SM::kStage + SM::kKV;
+                const uint32_t vbase = sbase + SM::kRingV + (j % kTcV) * SM::kKV;
                 // P_j sits in the first 32 columns of its score buffer (bf16 pairs)
                 const uint32_t pcol = tbase + 128u + 64u * (j & 1);
 #pragma unroll
@@ -587,7 +632,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 }
                 tc::commit(o_done0 + (j & 1) * 8);
                 tc::commit(s_free0 + (j & 1) * 8);  // the buffer's P has been read
-                tc::commit(kv_empty0 + (j % kTcStages) * 8);
+                tc::commit(v_empty0 + (j % kTcV) * 8);
             }
             if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             // every MMA issued has finished before tensor memory is released
@@ -609,8 +654,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float mrow = -INFINITY, lrow = 0.f;
         bool ok = true;
         for (int j = 0; j < nst; ++j) {
-            const int sl = j % kTcStages, b = j & 1;
-            ok = wait_all(kv_full0 + sl * 8, (uint32_t)((j / kTcStages) & 1)) &&
+            const int sl = j % kTcV, b = j & 1;  // sl: the V stage
+            ok = wait_all(k_full0 + (j % (2 * kTcK)) * 8, (uint32_t)((j / (2 * kTcK)) & 1)) &&
                  wait_all(s_full0 + b * 8, (uint32_t)((j >> 1) & 1));
             if (!ok) break;
             tc::fence_after();
@@ -618,7 +663,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc::ld32(tl + 128u + 64u * b, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
             tc::ld32(tl + 128u + 64u * b + 32u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
             tc::wait_ld();
-            const uint32_t present = lds_u32(mask0 + sl * 4);
+            const uint32_t present = lds_u32(mask0 + (j % (2 * kTcK)) * 4);
             const int kbase = j * kStageBlocks * kBlock;
             // eight independent partial maxima keep the dependency chains short
             float mp[8];
@@ -689,9 +734,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc::wait_st();
             if (warp == 0) {
                 // V rows of keys outside the context (missing blocks, the
-                // last block's tail) may hold any bits: zero them
-                const uint32_t vbase = sbase + SM::kRing + sl * SM::kStage + SM::kKV;
+                // last block's tail) may hold any bits: zero them, once the
+                // stage's V copies have landed
+                const uint32_t vbase = sbase + SM::kRingV + sl * SM::kKV;
+                bool any = false;
                 for (int l = 0; l < kStageBlocks; ++l) {
+                    const int blk = j * kStageBlocks + l;
+                    any |= !((present >> l) & 1u) || (blk == nb_ctx - 1 && tail < kBlock);
+                }
+                if (any && !(ok = wait_all(v_full0 + sl * 8, (uint32_t)((j / kTcV) & 1)))) break;
+                for (int l = 0; any && l < kStageBlocks; ++l) {
                     const int blk = j * kStageBlocks + l;
                     const int from = !((present >> l) & 1u) ? 0 : (blk == nb_ctx - 1 && tail < kBlock ? tail : kBlock);
                     for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
