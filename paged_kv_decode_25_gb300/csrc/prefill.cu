@@ -665,16 +665,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             tc::wait_ld();
             const uint32_t present = lds_u32(mask0 + (j % (2 * kTcK)) * 4);
             const int kbase = j * kStageBlocks * kBlock;
-            // eight independent partial maxima keep the dependency chains short
+            // eight independent partial maxima keep the dependency chains short.
+            // With a positive scale (the usual case) the max is taken over the
+            // raw scores and the scale folds into the exponent's fma; else the
+            // scores are scaled first.
+            const bool fold = p.sl2 > 0.f;
             float mp[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
             // stages wholly below every row's position with all blocks
             // present need no mask
-            if (__all_sync(0xffffffffu, present == 0xFu && kbase + kStageBlocks * kBlock - 1 <= mpos)) {
+            const bool nomask = __all_sync(0xffffffffu, present == 0xFu && kbase + kStageBlocks * kBlock - 1 <= mpos);
+            if (fold && nomask) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(x[c]));
+            } else if (fold) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float v = __uint_as_float(x[c]) * p.sl2;
+                    const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
+                    const float v = keep ? __uint_as_float(x[c]) : -INFINITY;
                     x[c] = __float_as_uint(v);
                     mp[c & 7] = fmaxf(mp[c & 7], v);
                 }
@@ -687,8 +696,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     mp[c & 7] = fmaxf(mp[c & 7], v);
                 }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+            const float mr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            const float mx = fold ? mr * p.sl2 : mr;
             // Lazy rescaling: the reference max only moves when the new max
             // exceeds it by more than 2^8 (weights stay <= 256); O and l are
             // rescaled together, so the normalised result is unchanged.
@@ -706,12 +716,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
             for (int i = 0; i < 8; ++i) ps[i] = 0.f;
             uint32_t w[32];
+            if (fold) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float e0 = ex2(__uint_as_float(x[2 * c]) - un);
-                const float e1 = ex2(__uint_as_float(x[2 * c + 1]) - un);
-                ps[c & 7] += e0 + e1;
-                w[c] = pack_bf16x2(e0, e1);
+                for (int c = 0; c < 32; ++c) {
+                    const float e0 = ex2(fmaf(__uint_as_float(x[2 * c]), p.sl2, -un));
+                    const float e1 = ex2(fmaf(__uint_as_float(x[2 * c + 1]), p.sl2, -un));
+                    ps[c & 7] += e0 + e1;
+                    w[c] = pack_bf16x2(e0, e1);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float e0 = ex2(__uint_as_float(x[2 * c]) - un);
+                    const float e1 = ex2(__uint_as_float(x[2 * c + 1]) - un);
+                    ps[c & 7] += e0 + e1;
+                    w[c] = pack_bf16x2(e0, e1);
+                }
             }
             const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             lrow = lrow * alpha + psum;
