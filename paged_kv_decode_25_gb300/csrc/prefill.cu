@@ -678,7 +678,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             const bool nomask = __all_sync(0xffffffffu, present == 0xFu && kbase + kStageBlocks * kBlock - 1 <= mpos);
             if (fold && nomask) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(x[c]));
+                for (int c = 0; c < 32; ++c)
+                    mp[c & 7] = tc::max3(mp[c & 7], __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]));
             } else if (fold) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
@@ -717,12 +718,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             for (int i = 0; i < 8; ++i) ps[i] = 0.f;
             uint32_t w[32];
             if (fold) {
+                // exponent arguments and row sums on packed fp32 pairs
+                const uint64_t sc2 = tc::f2(p.sl2, p.sl2), nu2 = tc::f2(-un, -un);
+                uint64_t acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = 0ull;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float e0 = ex2(fmaf(__uint_as_float(x[2 * c]), p.sl2, -un));
-                    const float e1 = ex2(fmaf(__uint_as_float(x[2 * c + 1]), p.sl2, -un));
-                    ps[c & 7] += e0 + e1;
+                    const uint64_t a2 = tc::fma2(tc::f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sc2, nu2);
+                    const float e0 = ex2(tc::f2_lo(a2)), e1 = ex2(tc::f2_hi(a2));
+                    acc[c & 3] = tc::add2(acc[c & 3], tc::f2(e0, e1));
                     w[c] = pack_bf16x2(e0, e1);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ps[2 * i] = tc::f2_lo(acc[i]);
+                    ps[2 * i + 1] = tc::f2_hi(acc[i]);
                 }
             } else {
 #pragma unroll
