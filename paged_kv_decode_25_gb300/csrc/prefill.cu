@@ -413,11 +413,11 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
 //     P . V has; K of stage j is issued before V of stage j - 1. (With one
 //     barrier pair for K and V together, each K load waited for the P . V of
 //     two stages back, and the kernel ran 1.36x slower.)
-//   * one thread of warp 4 issues the UMMAs: S_j = Q . K_j^T (M 128, N 64,
-//     K-major A and B) into one of two tensor-memory score buffers, then,
-//     once the softmax has written P_j, O += P_j . V_j (M 128, N HD, A K-major
-//     from shared memory, B = V MN-major) into the tensor-memory accumulator;
-//     tcgen05.commit signals the mbarriers;
+//   * one thread of warp 4 issues S_j = Q . K_j^T (M 128, N 64, K-major A
+//     and B) into one of two tensor-memory score buffers; one thread of
+//     warp 6, once the softmax has written P_j, issues O += P_j . V_j (M 128,
+//     N HD, A = P from tensor memory, B = V MN-major) into the tensor-memory
+//     accumulator; tcgen05.commit signals the mbarriers;
 //   * warps 0-3 (softmax): thread t owns row t, i.e. tensor-memory lane t. It
 //     loads its 64 scores, masks (causal, missing blocks), updates the
 //     running max and sum, rescales its O row in tensor memory when the max
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
 constexpr int kTcRows = 128;
 constexpr int kTcK = 2;  // K stages
 constexpr int kTcV = 2;  // V stages
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr uint32_t kTcCols = 256;
 
 template <int HD>
@@ -441,9 +441,9 @@ struct TcSmem {
     static constexpr int kRingK = kQ + kH * kTcRows * 128;
     static constexpr int kRingV = kRingK + kTcK * kKV;
     static constexpr int kBar = kRingV + kTcV * kKV;
-    // q_full, k_full[2 kTcK], k_empty[kTcK], v_full[kTcV], v_empty[kTcV], s_full[2], s_free[2], p_full,
-    // o_done[2], fin
-    static constexpr int kNBar = 1 + 3 * kTcK + 2 * kTcV + 2 + 2 + 4;
+    // q_full, k_full[2 kTcK], k_empty[kTcK], v_full[kTcV], v_empty[kTcV], s_full[2], s_free[2], p_full[2],
+    // o_done[2], fin_s, fin_o
+    static constexpr int kNBar = 1 + 3 * kTcK + 2 * kTcV + 2 + 2 + 6;
     static constexpr int kMask = kBar + kNBar * 8;
     static constexpr int kTmem = kMask + 2 * kTcK * 4;     // block masks of stages j mod 2 kTcK
     static constexpr int kUsed = kTmem + 16;
@@ -489,11 +489,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // ahead of the one it means.
     const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 16 * kTcK;
     const uint32_t v_full0 = k_empty0 + 8 * kTcK, v_empty0 = v_full0 + 8 * kTcV;
-    const uint32_t s_full0 = v_empty0 + 8 * kTcV, s_free0 = s_full0 + 16, p_full = s_free0 + 16;
+    const uint32_t s_full0 = v_empty0 + 8 * kTcV, s_free0 = s_full0 + 16, p_full0 = s_free0 + 16;
     // o_done[b] completes when P . V of a stage with parity b has finished: one
     // barrier per parity keeps every wait within one phase of the barrier,
     // although softmax warps may run a stage apart
-    const uint32_t o_done0 = p_full + 8, fin = o_done0 + 16;
+    const uint32_t o_done0 = p_full0 + 16, fin = o_done0 + 16, fin_o = fin + 8;
     const uint32_t mask0 = sbase + SM::kMask;
 
     if (threadIdx.x == 0) {
@@ -508,10 +508,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_init(s_full0 + b * 8, 1);
             mbar_init(s_free0 + b * 8, 1);
         }
-        mbar_init(p_full, 128);
+        // P_j is ready when all 128 softmax threads have arrived on
+        // p_full[j mod 2]: one barrier per stage parity, since a warp may
+        // finish stage j + 1 before another has finished stage j
+        mbar_init(p_full0, 128);
+        mbar_init(p_full0 + 8, 128);
         mbar_init(o_done0, 1);
         mbar_init(o_done0 + 8, 1);
         mbar_init(fin, 1);
+        mbar_init(fin_o, 1);
         fence_mbar_init();
     }
     if (warp == 4) {
@@ -590,7 +595,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ------------------------------------------------- MMA issuer ----
         if (lane == 0 && nst > 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kTcRows, 64, false);
-            constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
             bool ok = mbar_wait_bounded(q_full, 0);
             auto issue_s = [&](int jj) {
                 const int sl = jj % kTcK, b = jj & 1;
@@ -605,21 +609,31 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 tc::commit(s_full0 + b * 8);
                 tc::commit(k_empty0 + sl * 8);  // S_jj has read its K stage
             };
-            if (ok) ok = mbar_wait_bounded(k_full0, 0);
-            if (ok) {
+            // S_j needs K_j and its score buffer back from P . V of stage
+            // j - 2 (P_{j-2} lives there)
+            for (int jj = 0; ok && jj < nst; ++jj) {
+                const int u = jj >> 1;
+                ok = mbar_wait_bounded(k_full0 + (jj % (2 * kTcK)) * 8, (uint32_t)((jj / (2 * kTcK)) & 1));
+                if (ok && u >= 1) ok = mbar_wait_bounded(s_free0 + (jj & 1) * 8, (uint32_t)((u - 1) & 1));
+                if (!ok) break;
                 tc::fence_after();
-                issue_s(0);
+                issue_s(jj);
             }
+            if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            // every MMA issued has finished before tensor memory is released
+            tc::commit(fin);
+            (void)mbar_wait_bounded(fin, 0);
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // --------------------------------------------- P . V issuer ----
+        // A second issuing thread, so that P . V of a stage goes out as soon
+        // as its P is written instead of after the next S has been issued.
+        if (lane == 0 && nst > 0) {
+            constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
+            bool ok = true;
             for (int j = 0; ok && j < nst; ++j) {
-                if (j + 1 < nst) {
-                    const int j1 = j + 1, u1 = j1 >> 1;
-                    ok = mbar_wait_bounded(k_full0 + (j1 % (2 * kTcK)) * 8, (uint32_t)((j1 / (2 * kTcK)) & 1));
-                    if (ok && u1 >= 1) ok = mbar_wait_bounded(s_free0 + (j1 & 1) * 8, (uint32_t)((u1 - 1) & 1));
-                    if (!ok) break;
-                    tc::fence_after();
-                    issue_s(j1);
-                }
-                if (!(ok = mbar_wait_bounded(p_full, (uint32_t)(j & 1)))) break;
+                if (!(ok = mbar_wait_bounded(p_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1)))) break;
                 if (!(ok = mbar_wait_bounded(v_full0 + (j % kTcV) * 8, (uint32_t)((j / kTcV) & 1)))) break;
                 tc::fence_after();
                 const uint32_t vbase = sbase + SM::kRingV + (j % kTcV) * SM::kKV;
@@ -635,9 +649,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 tc::commit(v_empty0 + (j % kTcV) * 8);
             }
             if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
-            // every MMA issued has finished before tensor memory is released
-            tc::commit(fin);
-            (void)mbar_wait_bounded(fin, 0);
+            tc::commit(fin_o);
+            (void)mbar_wait_bounded(fin_o, 0);
         }
         __syncwarp();
     } else {
@@ -785,7 +798,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             fence_proxy_async_smem();
             tc::fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full0 + (j & 1) * 8);
         }
         if (!ok && threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
         if (ok && nst > 0) ok = wait_all(o_done0 + ((nst - 1) & 1) * 8, (uint32_t)(((nst - 1) >> 1) & 1));
