@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -120,10 +121,16 @@ def prefill_flops(w, hist, new):
 
 
 def kernel_source_hash():
+    """Hash of the attention kernel's sources with comments and whitespace
+    removed, so that a recorded traffic figure stays valid across comment
+    edits and is dropped as soon as any code changes."""
     h = hashlib.sha256()
     for f in ("decode.cu", "common.cuh", "tma.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_decode_25_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_decode_25_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,9 +10,10 @@
 //   * A "unit" is one (request b, KV head h) pair; it owns ceil(n_b / 16) KV
 //     blocks. Units are laid end to end in (b, h) order into one flat sequence
 //     of TB blocks.
-//   * A persistent grid (two CTAs per SM) cuts that sequence into equal
-//     contiguous ranges, one per CTA, so every CTA streams the same number of
-//     bytes however skewed the context lengths are.
+//   * A persistent grid (two CTAs per SM, three for e4m3 tiles) cuts that
+//     sequence into equal contiguous ranges, one per CTA, so every CTA
+//     streams the same number of bytes however skewed the context lengths
+//     are.
 //   * Warp specialisation: in each CTA one producer warp walks the block table
 //     and issues 2-D TMA tensor copies (128-byte swizzle, one 4 KB box per K
 //     or V tile) into a ring of shared-memory stages per consumer warp
