@@ -51,6 +51,7 @@ namespace mi {
 namespace {
 
 constexpr int kMaxG = 8;
+constexpr int kUnitCostE4m3 = 24;  // blocks; measured optimum 16-32 on a Qwen3-8B serving step
 constexpr float kNegInf = -INFINITY;
 
 struct AttnParams {
@@ -86,9 +87,12 @@ __device__ __forceinline__ int unit_blocks(const AttnParams& p, int b) {
 // [start, start + len).
 struct Cursor {
     int b, h, len;
-    long long start;
+    long long start;   // first flat block
+    long long cstart;  // cost position: every unit before it costs len + uc
+    int uc;            // per-unit cost of the split, in blocks
     __device__ __forceinline__ void next(const AttnParams& p) {
         start += len;
+        cstart += len + uc;
         if (++h == p.Hkv) {
             h = 0;
             ++b;
@@ -134,19 +138,29 @@ __device__ void block_exclusive_scan(long long v, long long* scratch) {
 // Each thread sums the unit lengths of a contiguous chunk of requests; after
 // the scan, scan[t] is the number of request blocks before chunk t and
 // scan[nt] their total. Returns TB = Hkv * total.
-__device__ __forceinline__ long long plan_scan(const AttnParams& p, long long* scan) {
+// With uc > 0 the same for the unit costs (len + uc per unit) into cscan, and
+// TC = their total; with uc = 0 cscan aliases scan and TC = TB.
+__device__ __forceinline__ long long plan_scan(const AttnParams& p, int uc, long long* scan, long long* cscan,
+                                               long long& TC) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (p.B + nt - 1) / nt;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
-    long long s = 0;
-    for (int b = b0; b < b1; ++b) s += unit_blocks(p, b);
+    long long s = 0, c = 0;
+    for (int b = b0; b < b1; ++b) {
+        const int L = unit_blocks(p, b);
+        s += L;
+        c += L > 0 ? L + uc : 0;
+    }
     block_exclusive_scan(s, scan);
+    if (uc > 0) block_exclusive_scan(c, cscan);
+    TC = (uc > 0 ? cscan[nt] : scan[nt]) * p.Hkv;
     return scan[nt] * p.Hkv;
 }
 
 // The unit holding flat block x (0 <= x < TB), by one thread: binary search
 // of the chunk sums, then a walk through that chunk's requests.
-__device__ Cursor locate(const AttnParams& p, const long long* scan, int nt, long long x) {
+__device__ Cursor locate(const AttnParams& p, int uc, const long long* scan, const long long* cscan, int nt,
+                         long long x) {
     int lo = 0, hi = nt;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -154,10 +168,11 @@ __device__ Cursor locate(const AttnParams& p, const long long* scan, int nt, lon
     }
     const int per = (p.B + nt - 1) / nt;
     int b = lo * per;
-    long long acc = scan[lo];
+    long long acc = scan[lo], cacc = uc > 0 ? cscan[lo] : scan[lo];
     int L = unit_blocks(p, b);
     while (x >= (acc + L) * p.Hkv) {
         acc += L;
+        cacc += L > 0 ? L + uc : 0;
         L = unit_blocks(p, ++b);
     }
     Cursor c;
@@ -165,7 +180,38 @@ __device__ Cursor locate(const AttnParams& p, const long long* scan, int nt, lon
     c.len = L;
     c.h = (int)((x - acc * p.Hkv) / L);
     c.start = acc * p.Hkv + (long long)c.h * L;
+    c.cstart = cacc * p.Hkv + (long long)c.h * (L + uc);
+    c.uc = uc;
     return c;
+}
+
+// The flat block at cost position y (0 <= y <= TC): units are laid out in
+// cost space as uc of overhead followed by their blocks; a position in a
+// unit's overhead maps to its first block. Monotone in y; the identity when
+// uc = 0.
+__device__ long long block_at_cost(const AttnParams& p, int uc, const long long* scan, const long long* cscan,
+                                   int nt, long long y, long long TC, long long TB) {
+    if (y >= TC) return TB;
+    if (uc == 0) return y;
+    int lo = 0, hi = nt;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cscan[mid] * p.Hkv <= y) lo = mid; else hi = mid;
+    }
+    const int per = (p.B + nt - 1) / nt;
+    int b = lo * per;
+    long long acc = scan[lo], cacc = cscan[lo];
+    int L = unit_blocks(p, b);
+    long long W = L > 0 ? L + uc : 0;
+    while (y >= (cacc + W) * p.Hkv) {
+        acc += L;
+        cacc += W;
+        L = unit_blocks(p, ++b);
+        W = L > 0 ? L + uc : 0;
+    }
+    const long long r = y - cacc * p.Hkv;
+    const long long h = r / W, o = r - h * W - uc;
+    return acc * p.Hkv + h * L + (o > 0 ? o : 0);
 }
 
 // Range of CTA i of P over TB flat blocks.
@@ -173,7 +219,8 @@ __device__ __forceinline__ long long range_start(long long TB, int P, int i) {
     return (long long)(((unsigned long long)TB * (unsigned long long)i) / (unsigned long long)P);
 }
 
-// The CTA whose range holds flat block x (0 <= x < TB).
+// The CTA whose range holds position x (0 <= x < TB); used on cost positions
+// with TB = TC.
 __device__ __forceinline__ int cta_of(long long TB, int P, long long x) {
     int c = (int)(((unsigned long long)x * (unsigned long long)P) / (unsigned long long)TB);
     while (c > 0 && range_start(TB, P, c) > x) --c;
@@ -195,7 +242,7 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, fac, flag, total;
+    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, cscan, fac, flag, total;
 };
 
 // W consumer warps plus one producer warp; S stages per consumer warp. The
@@ -214,6 +261,7 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.xbuf = off;  off += fma ? W * (kBlock * kMaxG + kMaxG) * 4 : 0;
     off = (off + 15) & ~15;
     s.scan = off;  off += ((W + 1) * 32 + 1 + 32) * 8;
+    s.cscan = off; off += eb == 1 ? ((W + 1) * 32 + 1 + 32) * 8 : 0;  // cost scan of the e4m3 tile
     s.flag = off;  off += 16;
     s.total = off + 1024;  // slack to align the tiles to 1024 bytes
     return s;
@@ -658,6 +706,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     uint8_t* base = smem_raw + pad;
     const uint32_t sbase = raw + pad;
     long long* scan = reinterpret_cast<long long*>(base + sp.scan);
+    long long* cscan = reinterpret_cast<long long*>(base + sp.cscan);
     constexpr int kTile = Tile<HD, elem_bytes(VAR)>::kBytes;
     const uint32_t full0 = sbase + sp.full, empty0 = sbase + sp.empty;
 
@@ -670,18 +719,25 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     pdl_wait();
     pdl_trigger();
 
-    const long long TB = plan_scan(p, scan);  // (ends with a barrier of all warps)
+    // The e4m3 tile splits by cost: a unit weighs its blocks plus a fixed
+    // kUnitCostE4m3 blocks (per-unit work: q, merges, the pipeline restart at
+    // its boundary), which weigh more against its half-size blocks.
+    constexpr int uc = VAR == kVarFp8 ? kUnitCostE4m3 : 0;
+    long long TC = 0;
+    const long long TB = plan_scan(p, uc, scan, cscan, TC);  // (ends with a barrier of all warps)
     const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
     const int cta = blockIdx.x;
-    const long long ra = cta < P ? range_start(TB, P, cta) : 0;
-    const long long rb = cta < P ? range_start(TB, P, cta + 1) : 0;
+    // ranges are equal in cost (equal in blocks when uc = 0)
+    const long long ra = cta < P ? block_at_cost(p, uc, scan, cscan, blockDim.x, range_start(TC, P, cta), TC, TB) : 0;
+    const long long rb =
+        cta < P ? block_at_cost(p, uc, scan, cscan, blockDim.x, range_start(TC, P, cta + 1), TC, TB) : 0;
     // The range's last unit, when it starts inside the range and continues
     // past rb, is streamed first ("part 0" = [sl, rb), then "part 1" =
     // [ra, sl)): both pieces of every cut unit are then written early and
     // their merge does not land at the end of the kernel.
     long long sl = rb;
     if (rb > ra) {
-        const Cursor cl = locate(p, scan, blockDim.x, rb - 1);
+        const Cursor cl = locate(p, uc, scan, cscan, blockDim.x, rb - 1);
         if (cl.start > ra && cl.start + cl.len > rb) sl = cl.start;
     }
 
@@ -713,7 +769,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
         const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
         long long x = ps + lane;
         if (x >= pe) continue;
-        Cursor cu = locate(p, scan, blockDim.x, x);
+        Cursor cu = locate(p, uc, scan, cscan, blockDim.x, x);
         for (; x < pe; x += W) {
             if (!mbar_wait_bounded(my_empty + stg * 8, ph)) {
                 // the consumer stopped taking stages (it timed out itself)
@@ -762,7 +818,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     for (int part = 0; part < 2; ++part) {
     const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
     if (ps >= pe) continue;
-    Cursor cu = locate(p, scan, blockDim.x, ps);
+    Cursor cu = locate(p, uc, scan, cscan, blockDim.x, ps);
     while (cu.start < pe && cu.b < p.B) {
         const long long sa = cu.start > ps ? cu.start : ps;
         const long long se = (cu.start + cu.len) < pe ? (cu.start + cu.len) : pe;
@@ -849,10 +905,13 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
             }
         }
         if (!whole) {
-            // pieces of this unit: CTAs cf..cl; the first one's slot is 1 when
-            // the unit starts inside its range, every other piece is slot 0
-            const int cf = cta_of(TB, P, cu.start), cl = cta_of(TB, P, cu.start + cu.len - 1);
-            const int fs = (cu.start == range_start(TB, P, cf)) ? 0 : 1;
+            // pieces of this unit: CTAs cf..cl, found by cost position (the
+            // unit's first block sits at cstart + uc, its last at cstart + uc
+            // + len - 1); the first piece's slot is 1 when the unit starts
+            // inside that CTA's range, every other piece is slot 0
+            const long long c0 = cu.cstart + uc;
+            const int cf = cta_of(TC, P, c0), cl = cta_of(TC, P, c0 + cu.len - 1);
+            const int fs = (range_start(TC, P, cf) >= cu.cstart) ? 0 : 1;
             const int ns = cl - cf + 1;
             volatile int* mflag = reinterpret_cast<volatile int*>(base + sp.flag);
             consumer_sync(nc);  // this CTA's partial is stored
