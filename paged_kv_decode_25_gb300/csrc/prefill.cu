@@ -420,10 +420,11 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
 //     accumulator; tcgen05.commit signals the mbarriers;
 //   * warps 0-3 (softmax): thread t owns row t, i.e. tensor-memory lane t. It
 //     loads its 64 scores, masks (causal, missing blocks), updates the
-//     running max and sum, rescales its O row in tensor memory when the max
-//     moved, and writes its probabilities as bf16 into the P tile; warp 0
-//     zeroes V rows of keys that are not in the context. After the last
-//     stage each thread reads its O row, normalises it and stores it.
+//     running max and sum (on packed fp32 pairs), rescales its O row in
+//     tensor memory when the max moved by more than 2^8, and writes its
+//     probabilities as bf16 pairs over the consumed scores; warp 0 zeroes V
+//     rows of keys that are not in the context. After the last stage each
+//     thread reads its O row, normalises it and stores it.
 // Tensor memory: 256 columns per CTA (O in columns 0..HD-1, the two score
 // buffers at 128 and 192); two CTAs per SM.
 
