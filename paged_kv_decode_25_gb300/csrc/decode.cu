@@ -886,18 +886,28 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
         const bool whole = (sa == cu.start) && (se == cu.start + cu.len);
         const int slot = (sa == ra) ? 0 : 1;
         float* part = p.part + ((long long)cta * 2 + slot) * p.slot_floats;
-        for (int idx = tid; idx < p.G * HD; idx += nc) {
+        // four consecutive outputs per thread (16-byte shared and global accesses)
+        for (int idx = 4 * tid; idx < p.G * HD; idx += 4 * nc) {
             const int g = idx / HD, dcol = idx - g * HD;
-            float acc = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int w = 0; w < W; ++w) {
                 const float f = fac[w * kMaxG + g];
-                if (f != 0.f) acc += f * obuf[(w * p.G + g) * HD + dcol];
+                if (f != 0.f) {
+                    const float4 o = *reinterpret_cast<const float4*>(obuf + (w * p.G + g) * HD + dcol);
+                    acc.x += f * o.x;
+                    acc.y += f * o.y;
+                    acc.z += f * o.z;
+                    acc.w += f * o.w;
+                }
             }
-            const float v = acc * res[g];
+            const float r = res[g];
+            const float4 v = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
             if (whole) {
-                p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + dcol] = f32_to_bf16(v);
+                *reinterpret_cast<uint2*>(p.out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + dcol) =
+                    make_uint2((uint32_t)f32_to_bf16(v.x) | ((uint32_t)f32_to_bf16(v.y) << 16),
+                               (uint32_t)f32_to_bf16(v.z) | ((uint32_t)f32_to_bf16(v.w) << 16));
             } else {
-                part[idx] = v;
+                *reinterpret_cast<float4*>(part + idx) = v;
                 if (dcol == 0) {
                     const float L = res[2 * kMaxG + g];
                     part[p.G * HD + g] = L > 0.f ? res[kMaxG + g] + log2f(L) : kNegInf;
@@ -956,13 +966,23 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                         res[tid] = den > 0.f ? 1.f / den : 0.f;
                     }
                     consumer_sync(nc);
-                    for (int idx = tid; idx < p.G * HD; idx += nc) {
+                    for (int idx = 4 * tid; idx < p.G * HD; idx += 4 * nc) {
                         const int g = idx / HD;
-                        float num = 0.f;
+                        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-                        for (int c = 0; c < ns; ++c) num += wts[c * p.G + g] * __ldcg(slot_of(cf + c) + idx);
-                        p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + (idx - g * HD)] =
-                            f32_to_bf16(num * res[g]);
+                        for (int c = 0; c < ns; ++c) {
+                            const float wg = wts[c * p.G + g];
+                            const float4 x = __ldcg(reinterpret_cast<const float4*>(slot_of(cf + c) + idx));
+                            num.x += wg * x.x;
+                            num.y += wg * x.y;
+                            num.z += wg * x.z;
+                            num.w += wg * x.w;
+                        }
+                        const float r = res[g];
+                        *reinterpret_cast<uint2*>(p.out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD +
+                                                  (idx - g * HD)) =
+                            make_uint2((uint32_t)f32_to_bf16(num.x * r) | ((uint32_t)f32_to_bf16(num.y * r) << 16),
+                                       (uint32_t)f32_to_bf16(num.z * r) | ((uint32_t)f32_to_bf16(num.w * r) << 16));
                     }
                 } else {
                     // more pieces than the weight buffer holds: two passes per output
