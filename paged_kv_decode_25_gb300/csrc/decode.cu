@@ -242,7 +242,7 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, cscan, fac, flag, total;
+    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, cscan, flag, total;
 };
 
 // W consumer warps plus one producer warp; S stages per consumer warp. The
@@ -256,7 +256,6 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.okf = off;   off += W * S * 4;  // per stage: 1 when its block id was valid and copied
     s.mbuf = off;  off += W * kMaxG * 4;
     s.lbuf = off;  off += W * kMaxG * 4;
-    s.fac = off;   off += (W + 3) * kMaxG * 4;
     s.obuf = off;  off += W * G * HD * 4;
     s.xbuf = off;  off += fma ? W * (kBlock * kMaxG + kMaxG) * 4 : 0;
     off = (off + 15) & ~15;
@@ -805,8 +804,6 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     if (cta >= P) return;
     float* mbuf = reinterpret_cast<float*>(base + sp.mbuf);
     float* lbuf = reinterpret_cast<float*>(base + sp.lbuf);
-    float* fac = reinterpret_cast<float*>(base + sp.fac);
-    float* res = fac + W * kMaxG;  // rows: 1/L, M, L per head
     float* obuf = reinterpret_cast<float*>(base + sp.obuf);
     float* xbuf = reinterpret_cast<float*>(base + sp.xbuf) + warp * (kBlock * kMaxG + kMaxG);
     const int nc = W * 32;
@@ -869,29 +866,24 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
         // it stores its initial state: max -inf, sum 0, output 0)
         st.store(mbuf + warp * kMaxG, lbuf + warp * kMaxG, obuf + warp * p.G * HD, p.G, lane);
         consumer_sync(nc);
-        if (tid < p.G) {
-            float M = kNegInf;
-            for (int w = 0; w < W; ++w) M = fmaxf(M, mbuf[w * kMaxG + tid]);
-            float L = 0.f;
-            for (int w = 0; w < W; ++w) {
-                const float f = (M == kNegInf) ? 0.f : exp2f(mbuf[w * kMaxG + tid] - M);
-                fac[w * kMaxG + tid] = f;
-                L += f * lbuf[w * kMaxG + tid];
-            }
-            res[tid] = L > 0.f ? 1.f / L : 0.f;
-            res[kMaxG + tid] = M;
-            res[2 * kMaxG + tid] = L;
-        }
-        consumer_sync(nc);
         const bool whole = (sa == cu.start) && (se == cu.start + cu.len);
         const int slot = (sa == ra) ? 0 : 1;
         float* part = p.part + ((long long)cta * 2 + slot) * p.slot_floats;
-        // four consecutive outputs per thread (16-byte shared and global accesses)
+        // four consecutive outputs per thread (16-byte shared and global
+        // accesses); each thread weighs the warps' states of its head itself
         for (int idx = 4 * tid; idx < p.G * HD; idx += 4 * nc) {
             const int g = idx / HD, dcol = idx - g * HD;
+            float M = kNegInf;
+            for (int w = 0; w < W; ++w) M = fmaxf(M, mbuf[w * kMaxG + g]);
+            float fw[W];
+            float L = 0.f;
+            for (int w = 0; w < W; ++w) {
+                fw[w] = (M == kNegInf) ? 0.f : exp2f(mbuf[w * kMaxG + g] - M);
+                L += fw[w] * lbuf[w * kMaxG + g];
+            }
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int w = 0; w < W; ++w) {
-                const float f = fac[w * kMaxG + g];
+                const float f = fw[w];
                 if (f != 0.f) {
                     const float4 o = *reinterpret_cast<const float4*>(obuf + (w * p.G + g) * HD + dcol);
                     acc.x += f * o.x;
@@ -900,7 +892,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                     acc.w += f * o.w;
                 }
             }
-            const float r = res[g];
+            const float r = L > 0.f ? 1.f / L : 0.f;
             const float4 v = make_float4(acc.x * r, acc.y * r, acc.z * r, acc.w * r);
             if (whole) {
                 *reinterpret_cast<uint2*>(p.out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + dcol) =
@@ -908,10 +900,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                                (uint32_t)f32_to_bf16(v.z) | ((uint32_t)f32_to_bf16(v.w) << 16));
             } else {
                 *reinterpret_cast<float4*>(part + idx) = v;
-                if (dcol == 0) {
-                    const float L = res[2 * kMaxG + g];
-                    part[p.G * HD + g] = L > 0.f ? res[kMaxG + g] + log2f(L) : kNegInf;
-                }
+                if (dcol == 0) part[p.G * HD + g] = L > 0.f ? M + log2f(L) : kNegInf;
             }
         }
         if (!whole) {
@@ -945,61 +934,34 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
             }
             consumer_sync(nc);
             if (*mflag) {
-                // M = max lse, out = sum 2^(lse-M) o / sum 2^(lse-M), pieces in order
                 auto slot_of = [&](int c) {
                     return p.part + ((long long)c * 2 + (c == cf ? fs : 0)) * p.slot_floats;
                 };
-                if (ns <= W * HD) {
-                    float* wts = obuf;  // [ns][G] log-sum-exps, then weights
-                    for (int i = tid; i < ns * p.G; i += nc)
-                        wts[i] = __ldcg(slot_of(cf + i / p.G) + p.G * HD + i % p.G);
-                    consumer_sync(nc);
-                    if (tid < p.G) {
-                        float M = kNegInf;
-                        for (int c = 0; c < ns; ++c) M = fmaxf(M, wts[c * p.G + tid]);
-                        float den = 0.f;
-                        for (int c = 0; c < ns; ++c) {
-                            const float wgt = M == kNegInf ? 0.f : exp2f(wts[c * p.G + tid] - M);
-                            wts[c * p.G + tid] = wgt;
-                            den += wgt;
-                        }
-                        res[tid] = den > 0.f ? 1.f / den : 0.f;
-                    }
-                    consumer_sync(nc);
-                    for (int idx = 4 * tid; idx < p.G * HD; idx += 4 * nc) {
-                        const int g = idx / HD;
-                        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+                // each thread weighs the pieces for its head itself: M = max
+                // lse, out = sum 2^(lse-M) o / sum 2^(lse-M), pieces in order
+                for (int idx = 4 * tid; idx < p.G * HD; idx += 4 * nc) {
+                    const int g = idx / HD;
+                    float M = kNegInf;
+                    for (int c = cf; c <= cl; ++c) M = fmaxf(M, __ldcg(slot_of(c) + p.G * HD + g));
+                    float den = 0.f;
+                    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (M != kNegInf) {
 #pragma unroll 4
-                        for (int c = 0; c < ns; ++c) {
-                            const float wg = wts[c * p.G + g];
-                            const float4 x = __ldcg(reinterpret_cast<const float4*>(slot_of(cf + c) + idx));
+                        for (int c = cf; c <= cl; ++c) {
+                            const float wg = exp2f(__ldcg(slot_of(c) + p.G * HD + g) - M);
+                            const float4 x = __ldcg(reinterpret_cast<const float4*>(slot_of(c) + idx));
+                            den += wg;
                             num.x += wg * x.x;
                             num.y += wg * x.y;
                             num.z += wg * x.z;
                             num.w += wg * x.w;
                         }
-                        const float r = res[g];
-                        *reinterpret_cast<uint2*>(p.out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD +
-                                                  (idx - g * HD)) =
-                            make_uint2((uint32_t)f32_to_bf16(num.x * r) | ((uint32_t)f32_to_bf16(num.y * r) << 16),
-                                       (uint32_t)f32_to_bf16(num.z * r) | ((uint32_t)f32_to_bf16(num.w * r) << 16));
                     }
-                } else {
-                    // more pieces than the weight buffer holds: two passes per output
-                    for (int idx = tid; idx < p.G * HD; idx += nc) {
-                        const int g = idx / HD;
-                        float M = kNegInf;
-                        for (int c = cf; c <= cl; ++c) M = fmaxf(M, __ldcg(slot_of(c) + p.G * HD + g));
-                        float num = 0.f, den = 0.f;
-                        if (M != kNegInf)
-                            for (int c = cf; c <= cl; ++c) {
-                                const float wgt = exp2f(__ldcg(slot_of(c) + p.G * HD + g) - M);
-                                num += wgt * __ldcg(slot_of(c) + idx);
-                                den += wgt;
-                            }
-                        p.out[((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD + (idx - g * HD)] =
-                            f32_to_bf16(den > 0.f ? num / den : 0.f);
-                    }
+                    const float r = den > 0.f ? 1.f / den : 0.f;
+                    *reinterpret_cast<uint2*>(p.out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD +
+                                              (idx - g * HD)) =
+                        make_uint2((uint32_t)f32_to_bf16(num.x * r) | ((uint32_t)f32_to_bf16(num.y * r) << 16),
+                                   (uint32_t)f32_to_bf16(num.z * r) | ((uint32_t)f32_to_bf16(num.w * r) << 16));
                 }
             }
         }
