@@ -352,10 +352,10 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
 /* Kernel of mi_paged_prefill_attention_variant:
  *   MI_PREFILL_MMA      warp-level mma.sync tiles (64 rows per CTA; any G),
  *   MI_PREFILL_TCGEN05  fifth-generation tensor cores (tcgen05.mma with
- *                       tensor-memory accumulators, 128 rows per CTA; G must
- *                       divide 128, else MI_ERR_UNSUPPORTED).
- * MI_PREFILL_DEFAULT takes the tcgen05 kernel when G divides 128, else the
- * mma.sync one. Both compute the same definition within the same tolerance. */
+ *                       tensor-memory accumulators; 128 / G whole tokens,
+ *                       i.e. (128 / G) * G rows, per CTA; any G up to 8).
+ * MI_PREFILL_DEFAULT takes the tcgen05 kernel. Both compute the same
+ * definition within the same tolerance. */
 #define MI_PREFILL_DEFAULT 0
 #define MI_PREFILL_MMA 1
 #define MI_PREFILL_TCGEN05 2

@@ -474,8 +474,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     pdl_wait();
     pdl_trigger();
 
+    // a tile holds whole tokens: 128 / G of them, G rows each (the UMMA rows
+    // past tile_rows compute on stale shared memory and are never stored)
+    const int tile_rows = (kTcRows / p.G) * p.G;
     Item it;
-    if (!work_item(p, kTcRows, it)) return;
+    if (!work_item(p, tile_rows, it)) return;
     if (sbase - raw > (uint32_t)SM::kSlack) {  // no room to align the tiles
         if (threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_INTERNAL);
         return;
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ------------------------------------------------ producer warp --
         const uint64_t policy = l2_policy_evict_normal();
         if (lane == 0 && nst > 0) {
-            mbar_arrive_expect_tx(q_full, kH * kTcRows * 128);
+            mbar_arrive_expect_tx(q_full, kH * tile_rows * 128);
             for (int hh = 0; hh < kH; ++hh)
                 tma_load_4d(sbase + SM::kQ + hh * kTcRows * 128, &tmq, q_full, 0, hh, it.h * p.G,
                             it.q0 + it.rho0 / p.G, policy);
@@ -658,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ---------------------------------------------------- softmax ----
         const int t = threadIdx.x;  // row of the tile, tensor-memory lane
         const int rr = it.rho0 + t;
-        const bool vrow = rr < it.nrows;
+        const bool vrow = t < tile_rows && rr < it.nrows;
         const int tok = rr / p.G;
         const int pos = vrow ? it.first + tok : it.p_hi;
         const int mpos = pos < 0 ? 0 : pos;
@@ -895,10 +898,9 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         D.Hq / D.Hkv > kMaxGroup)
         return MI_ERR_UNSUPPORTED;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
-    // the tcgen05 tile stacks 128 / G tokens of a group: G must divide 128
-    const bool tc_ok = (kTcRows % G) == 0;
-    if (variant == MI_PREFILL_TCGEN05 && !tc_ok) return MI_ERR_UNSUPPORTED;
-    const bool use_tc = variant == MI_PREFILL_TCGEN05 || (variant == MI_PREFILL_DEFAULT && tc_ok);
+    // the tcgen05 tile stacks 128 / G whole tokens of a group (G <= 8)
+    const bool use_tc = variant == MI_PREFILL_TCGEN05 || variant == MI_PREFILL_DEFAULT;
+    const int tc_rows = (kTcRows / G) * G;
     if ((long long)D.num_blocks * D.Hkv * kBlock * (D.head_dim / 64) > 0x7FFFFFFFLL ||
         (long long)D.max_blocks_per_seq * kBlock > 0x7FFFFFFFLL || (long long)total_q * D.Hq > 0x7FFFFFFFLL ||
         (long long)max_query_len * D.Hq > 0x7FFFFFFFLL)
@@ -909,7 +911,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         return MI_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return MI_ERR_INVALID_ARG;
-    const int rows_per_tile = use_tc ? kTcRows : kPRows;
+    const int rows_per_tile = use_tc ? tc_rows : kPRows;
     const long long tiles_max = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
     const long long grid = (tiles_max + kTileGroup - 1) / kTileGroup * kTileGroup * D.B * D.Hkv;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
@@ -936,7 +938,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
     if (use_tc) {
         if (!(HD == 64 ? prepare_tc<64>() : prepare_tc<128>())) return MI_ERR_CUDA;
         CUtensorMap tq, tk, tv;
-        if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, kTcRows) ||
+        if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, tc_rows) ||
             !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_halves(&tv, v_cache, rows, HD))
             return MI_ERR_CUDA;
         e = HD == 64 ? launch_pdl(prefill_tc_kernel<64>, (int)grid, kTcThreads, TcSmem<64>::kTotal, st, tq, tk, tv, p)

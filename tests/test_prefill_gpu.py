@@ -162,7 +162,8 @@ def _attend(device, q, kc, vc, bt, n, qs, scale, max_q=None, variant=0):
     return from_dev_u16(out)[:T], int(err.item())
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 64), (8, 4, 128), (8, 2, 64), (16, 2, 128), (32, 8, 128)])
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 64), (8, 4, 128), (8, 2, 64), (16, 2, 128), (32, 8, 128),
+                                       (28, 4, 128), (12, 4, 64), (24, 4, 128), (20, 4, 128)])
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_prefill_group_and_head_dim(cuda_device, Hq, Hkv, d, variant):
     hist = [0, 5, 64, 200, 31, 0]

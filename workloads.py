@@ -313,6 +313,11 @@ PREFILL_WORKLOADS = {
     "qwen3_8b_prefill": PrefillWorkload("qwen3_8b_prefill", 7, Hq=32, Hkv=8, head_dim=128,
                                         num_blocks=4096, kind="mixed",
                                         args=(8, 512, 2048, 8, 1024, 8192, 512)),
+    # the same kind of request mix at the Qwen2.5-7B layer shape (Hq 28, Hkv 4: G = 7,
+    # which does not divide a 128-row tile)
+    "qwen25_7b_prefill": PrefillWorkload("qwen25_7b_prefill", 8, Hq=28, Hkv=4, head_dim=128,
+                                         num_blocks=4096, kind="mixed",
+                                         args=(8, 512, 2048, 8, 1024, 8192, 512)),
 }
 
 
