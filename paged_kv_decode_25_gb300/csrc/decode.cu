@@ -51,7 +51,11 @@ namespace mi {
 namespace {
 
 constexpr int kMaxG = 8;
-constexpr int kUnitCostE4m3 = 24;  // blocks; measured optimum 16-32 on a Qwen3-8B serving step
+// Per-unit cost of the split, in blocks (measured optima: e4m3 8-24 on a
+// Qwen3-8B serving step; bf16 8 on a batch of one long and 255 short
+// contexts, neutral on the serving step)
+constexpr int kUnitCostE4m3 = 24;
+constexpr int kUnitCostBf16 = 8;
 constexpr float kNegInf = -INFINITY;
 
 struct AttnParams {
@@ -135,13 +139,22 @@ __device__ void block_exclusive_scan(long long v, long long* scratch) {
     __syncthreads();
 }
 
-// Each thread sums the unit lengths of a contiguous chunk of requests; after
-// the scan, scan[t] is the number of request blocks before chunk t and
-// scan[nt] their total. Returns TB = Hkv * total.
-// With uc > 0 the same for the unit costs (len + uc per unit) into cscan, and
-// TC = their total; with uc = 0 cscan aliases scan and TC = TB.
-__device__ __forceinline__ long long plan_scan(const AttnParams& p, int uc, long long* scan, long long* cscan,
-                                               long long& TC) {
+// The scan packs two sums in one word: flat blocks in the low kCntShift bits,
+// the number of requests with at least one block above them (B < 2^17 and
+// B * max_blocks_per_seq < 2^46, so neither field spills into the other).
+constexpr int kCntShift = 46;
+constexpr long long kBlkMask = (1LL << kCntShift) - 1;
+__device__ __forceinline__ long long sc_blocks(long long v) { return v & kBlkMask; }
+// cost = blocks + uc per unit with blocks (per KV head: multiply by Hkv)
+__device__ __forceinline__ long long sc_cost(long long v, int uc) {
+    return (v & kBlkMask) + (long long)uc * (v >> kCntShift);
+}
+
+// Each thread sums the unit lengths (and counts the non-empty requests) of a
+// contiguous chunk of requests; after the scan, scan[t] holds the sums before
+// chunk t and scan[nt] the totals. Returns TB = Hkv * total blocks and sets
+// TC = Hkv * total cost, a unit costing its blocks plus uc.
+__device__ __forceinline__ long long plan_scan(const AttnParams& p, int uc, long long* scan, long long& TC) {
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (p.B + nt - 1) / nt;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
@@ -149,26 +162,24 @@ __device__ __forceinline__ long long plan_scan(const AttnParams& p, int uc, long
     for (int b = b0; b < b1; ++b) {
         const int L = unit_blocks(p, b);
         s += L;
-        c += L > 0 ? L + uc : 0;
+        c += L > 0 ? 1 : 0;
     }
-    block_exclusive_scan(s, scan);
-    if (uc > 0) block_exclusive_scan(c, cscan);
-    TC = (uc > 0 ? cscan[nt] : scan[nt]) * p.Hkv;
-    return scan[nt] * p.Hkv;
+    block_exclusive_scan(s | (c << kCntShift), scan);
+    TC = sc_cost(scan[nt], uc) * p.Hkv;
+    return sc_blocks(scan[nt]) * p.Hkv;
 }
 
 // The unit holding flat block x (0 <= x < TB), by one thread: binary search
 // of the chunk sums, then a walk through that chunk's requests.
-__device__ Cursor locate(const AttnParams& p, int uc, const long long* scan, const long long* cscan, int nt,
-                         long long x) {
+__device__ Cursor locate(const AttnParams& p, int uc, const long long* scan, int nt, long long x) {
     int lo = 0, hi = nt;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (scan[mid] * p.Hkv <= x) lo = mid; else hi = mid;
+        if (sc_blocks(scan[mid]) * p.Hkv <= x) lo = mid; else hi = mid;
     }
     const int per = (p.B + nt - 1) / nt;
     int b = lo * per;
-    long long acc = scan[lo], cacc = uc > 0 ? cscan[lo] : scan[lo];
+    long long acc = sc_blocks(scan[lo]), cacc = sc_cost(scan[lo], uc);
     int L = unit_blocks(p, b);
     while (x >= (acc + L) * p.Hkv) {
         acc += L;
@@ -189,18 +200,18 @@ __device__ Cursor locate(const AttnParams& p, int uc, const long long* scan, con
 // cost space as uc of overhead followed by their blocks; a position in a
 // unit's overhead maps to its first block. Monotone in y; the identity when
 // uc = 0.
-__device__ long long block_at_cost(const AttnParams& p, int uc, const long long* scan, const long long* cscan,
-                                   int nt, long long y, long long TC, long long TB) {
+__device__ long long block_at_cost(const AttnParams& p, int uc, const long long* scan, int nt, long long y,
+                                   long long TC, long long TB) {
     if (y >= TC) return TB;
     if (uc == 0) return y;
     int lo = 0, hi = nt;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (cscan[mid] * p.Hkv <= y) lo = mid; else hi = mid;
+        if (sc_cost(scan[mid], uc) * p.Hkv <= y) lo = mid; else hi = mid;
     }
     const int per = (p.B + nt - 1) / nt;
     int b = lo * per;
-    long long acc = scan[lo], cacc = cscan[lo];
+    long long acc = sc_blocks(scan[lo]), cacc = sc_cost(scan[lo], uc);
     int L = unit_blocks(p, b);
     long long W = L > 0 ? L + uc : 0;
     while (y >= (cacc + W) * p.Hkv) {
@@ -242,7 +253,7 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, cscan, flag, total;
+    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, flag, total;
 };
 
 // W consumer warps plus one producer warp; S stages per consumer warp. The
@@ -260,7 +271,6 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.xbuf = off;  off += fma ? W * (kBlock * kMaxG + kMaxG) * 4 : 0;
     off = (off + 15) & ~15;
     s.scan = off;  off += ((W + 1) * 32 + 1 + 32) * 8;
-    s.cscan = off; off += eb == 1 ? ((W + 1) * 32 + 1 + 32) * 8 : 0;  // cost scan of the e4m3 tile
     s.flag = off;  off += 16;
     s.total = off + 1024;  // slack to align the tiles to 1024 bytes
     return s;
@@ -705,7 +715,6 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     uint8_t* base = smem_raw + pad;
     const uint32_t sbase = raw + pad;
     long long* scan = reinterpret_cast<long long*>(base + sp.scan);
-    long long* cscan = reinterpret_cast<long long*>(base + sp.cscan);
     constexpr int kTile = Tile<HD, elem_bytes(VAR)>::kBytes;
     const uint32_t full0 = sbase + sp.full, empty0 = sbase + sp.empty;
 
@@ -718,25 +727,24 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     pdl_wait();
     pdl_trigger();
 
-    // The e4m3 tile splits by cost: a unit weighs its blocks plus a fixed
-    // kUnitCostE4m3 blocks (per-unit work: q, merges, the pipeline restart at
-    // its boundary), which weigh more against its half-size blocks.
-    constexpr int uc = VAR == kVarFp8 ? kUnitCostE4m3 : 0;
+    // Ranges are cut by cost: a unit weighs its blocks plus a fixed number of
+    // blocks for its per-unit work (q, the merge, the pipeline restart at its
+    // boundary), which weighs more against the half-size e4m3 blocks.
+    constexpr int uc = VAR == kVarFp8 ? kUnitCostE4m3 : kUnitCostBf16;
     long long TC = 0;
-    const long long TB = plan_scan(p, uc, scan, cscan, TC);  // (ends with a barrier of all warps)
+    const long long TB = plan_scan(p, uc, scan, TC);  // (ends with a barrier of all warps)
     const int P = (int)(TB < (long long)gridDim.x ? TB : (long long)gridDim.x);
     const int cta = blockIdx.x;
-    // ranges are equal in cost (equal in blocks when uc = 0)
-    const long long ra = cta < P ? block_at_cost(p, uc, scan, cscan, blockDim.x, range_start(TC, P, cta), TC, TB) : 0;
-    const long long rb =
-        cta < P ? block_at_cost(p, uc, scan, cscan, blockDim.x, range_start(TC, P, cta + 1), TC, TB) : 0;
+    // ranges of equal cost
+    const long long ra = cta < P ? block_at_cost(p, uc, scan, blockDim.x, range_start(TC, P, cta), TC, TB) : 0;
+    const long long rb = cta < P ? block_at_cost(p, uc, scan, blockDim.x, range_start(TC, P, cta + 1), TC, TB) : 0;
     // The range's last unit, when it starts inside the range and continues
     // past rb, is streamed first ("part 0" = [sl, rb), then "part 1" =
     // [ra, sl)): both pieces of every cut unit are then written early and
     // their merge does not land at the end of the kernel.
     long long sl = rb;
     if (rb > ra) {
-        const Cursor cl = locate(p, uc, scan, cscan, blockDim.x, rb - 1);
+        const Cursor cl = locate(p, uc, scan, blockDim.x, rb - 1);
         if (cl.start > ra && cl.start + cl.len > rb) sl = cl.start;
     }
 
@@ -768,7 +776,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
         const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
         long long x = ps + lane;
         if (x >= pe) continue;
-        Cursor cu = locate(p, uc, scan, cscan, blockDim.x, x);
+        Cursor cu = locate(p, uc, scan, blockDim.x, x);
         for (; x < pe; x += W) {
             if (!mbar_wait_bounded(my_empty + stg * 8, ph)) {
                 // the consumer stopped taking stages (it timed out itself)
@@ -815,7 +823,7 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     for (int part = 0; part < 2; ++part) {
     const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
     if (ps >= pe) continue;
-    Cursor cu = locate(p, uc, scan, cscan, blockDim.x, ps);
+    Cursor cu = locate(p, uc, scan, blockDim.x, ps);
     while (cu.start < pe && cu.b < p.B) {
         const long long sa = cu.start > ps ? cu.start : ps;
         const long long se = (cu.start + cu.len) < pe ? (cu.start + cu.len) : pe;
