@@ -91,9 +91,10 @@ def test_prefill_small_full_parity(cuda_device, variant):
         assert np.array_equal(got[0, j], x["v_new"][0, j // G])
 
 
+@pytest.mark.parametrize("name", ["qwen3_8b_prefill", "qwen25_7b_prefill"])
 @pytest.mark.parametrize("variant", VARIANTS)
-def test_prefill_qwen3_8b_sampled(cuda_device, variant):
-    w = PREFILL_WORKLOADS["qwen3_8b_prefill"]
+def test_prefill_full_size_sampled(cuda_device, variant, name):
+    w = PREFILL_WORKLOADS[name]
     x = _run_prefill(w, cuda_device, variant=variant)
     # append: the new tokens' rows and slots, bit-exact
     assert np.array_equal(from_dev_u16(x["qo_d"]), x["q_ref"])
@@ -113,7 +114,7 @@ def test_prefill_qwen3_8b_sampled(cuda_device, variant):
     ref = oracle.paged_prefill_attention(x["q_ref"][rows], x["kc"], x["vc"], np.stack(tabs),
                                          np.array(lens, np.int32), qs1, w.scale, nthreads=16)
     got = from_dev_u16(x["out_d"])[rows]
-    assert_attention_close(got, ref, "qwen3_8b_prefill sampled rows")
+    assert_attention_close(got, ref, f"{name} sampled rows")
     assert np.all(np.isfinite(oracle.bf16_to_f64(from_dev_u16(x["out_d"]))))
 
 
