@@ -39,33 +39,33 @@ __device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double 
 }
 
 // RN_bf16(RN_double(a*b + c*d)) for bf16 a, c and fp32 b, d, in single
-// precision when that decides it. Both products are split exactly (the fma
-// recovers each rounding error, exact above the underflow range) and their sum
-// is split exactly (two-sum), so exact = s + t + pe + qe with s the rounded
-// sum. When no bf16 rounding boundary (a midpoint between neighbouring bf16
-// values, or one across a binade below) lies within the bound on |exact - s|
-// plus the double rounding's 2^-52 |s| of s, the answer is RN_bf16(s).
+// precision when that decides it. q = RN(c*d) and its rounding error qe (an
+// fma recovers it exactly above the underflow range) give c*d = q + qe; the
+// fma s = RN(a*b + q) rounds the exact a*b + q once, so |exact - s| <=
+// ulp(s)/2 + |qe|. When no bf16 rounding boundary (a midpoint between
+// neighbouring bf16 values, or one across a binade below) lies within that
+// bound plus the double rounding's 2^-50 |s| of s, the answer is RN_bf16(s).
 // Otherwise (a boundary within reach, zero, tiny, infinite or NaN values)
-// `slow` is set and the caller takes the double-precision route.
-// The _rn intrinsics keep the compiler from contracting the transforms into
-// fused multiply-adds, which would break their exactness.
-__device__ __forceinline__ uint32_t rot_fast(float a, float b, float c, float d, bool& slow) {
-    const float p = __fmul_rn(a, b), q = __fmul_rn(c, d);
-    const float pe = fmaf(a, b, -p), qe = fmaf(c, d, -q);
-    const float s = __fadd_rn(p, q);
-    const float bb = __fsub_rn(s, p);
-    const float t = __fadd_rn(__fsub_rn(p, __fsub_rn(s, bb)), __fsub_rn(q, bb));
-    const float err = __fadd_rn(__fmul_rn(__fadd_rn(__fadd_rn(fabsf(t), fabsf(pe)), fabsf(qe)), 1.0001f),
-                                __fmul_rn(fabsf(s), 0x1p-50f));
+// `slow` is set and the caller takes the double-precision route. Returns s;
+// the caller rounds pairs of them to bf16 with the hardware conversion (the
+// same nearest-even result for the finite, normal s this path keeps).
+// The _rn intrinsics keep the compiler from contracting c*d into an fma,
+// which would break the split.
+__device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bool& slow) {
+    const float q = __fmul_rn(c, d);
+    const float qe = fmaf(c, d, -q);
+    const float s = fmaf(a, b, q);
     const uint32_t S = __float_as_uint(fabsf(s));
     const int L = (int)(S & 0xFFFFu);
     const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L) - 2;
     const float ulp = __uint_as_float((S & 0x7F800000u) - (23u << 23));
+    const float err = __fadd_rn(__fadd_rn(__fmul_rn(fabsf(qe), 1.0001f), __fmul_rn(fabsf(s), 0x1p-50f)),
+                                __fmul_rn(ulp, 0.5f));
     const float tiny = 0x1p-100f;
-    const bool ok = isfinite(s) && (p == 0.f || fabsf(p) >= tiny) && (q == 0.f || fabsf(q) >= tiny) &&
-                    fabsf(s) >= tiny && err < __fmul_rn((float)dist, ulp);
+    const bool ok = isfinite(s) && (q == 0.f || fabsf(q) >= tiny) && fabsf(s) >= tiny &&
+                    err < __fmul_rn((float)dist, ulp);
     slow |= !ok;
-    return f32_to_bf16(s);
+    return s;
 }
 
 struct AppendParams {
@@ -113,11 +113,22 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     const long long n_rot = (long long)B * (a.Hq + a.Hkv) * groups;
     const long long n_cpy = (long long)B * a.Hkv * (a.d / 8);
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    // d is 64 or 128: groups (d/16) and chunks (d/8) are powers of two, and
+    // the remaining divisions run in 32 bits whenever the quotient range fits
+    const int lgg = a.d == 128 ? 3 : 2, lgc = lgg + 1;
     if (t < n_rot) {
-        const int grp = (int)(t % groups);
-        const long long bh = t / groups;
-        const int head = (int)(bh % (a.Hq + a.Hkv));
-        const int b = (int)(bh / (a.Hq + a.Hkv));
+        const int grp = (int)(t & (groups - 1));
+        const long long bh = t >> lgg;
+        const int HH = a.Hq + a.Hkv;
+        int head, b;
+        if (bh <= 0xFFFFFFFFLL) {
+            const uint32_t u = (uint32_t)bh;
+            head = (int)(u % (uint32_t)HH);
+            b = (int)(u / (uint32_t)HH);
+        } else {
+            head = (int)(bh % HH);
+            b = (int)(bh / HH);
+        }
         const bool is_q = head < a.Hq;
         const uint16_t* src = is_q ? a.q + ((long long)b * a.Hq + head) * a.d
                                    : a.k + ((long long)b * a.Hkv + (head - a.Hq)) * a.d;
@@ -154,23 +165,21 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
             const float fa0 = bf16_lo(xl[j]), fa1 = bf16_hi(xl[j]);
             const float fb0 = bf16_lo(xh[j]), fb1 = bf16_hi(xh[j]);
             bool slow = false;
-            uint32_t r0 = rot_fast(fa0, cs[j].x, -fb0, cs[j].y, slow);
-            uint32_t r1 = rot_fast(fa1, cs[j].z, -fb1, cs[j].w, slow);
-            uint32_t r2 = rot_fast(fb0, cs[j].x, fa0, cs[j].y, slow);
-            uint32_t r3 = rot_fast(fb1, cs[j].z, fa1, cs[j].w, slow);
+            const float s0 = rot_fast(fa0, cs[j].x, -fb0, cs[j].y, slow);
+            const float s1 = rot_fast(fa1, cs[j].z, -fb1, cs[j].w, slow);
+            const float s2 = rot_fast(fb0, cs[j].x, fa0, cs[j].y, slow);
+            const float s3 = rot_fast(fb1, cs[j].z, fa1, cs[j].w, slow);
+            yl[j] = pack_bf16x2(s0, s1);
+            yh[j] = pack_bf16x2(s2, s3);
             if (slow) {
                 // rare: the exact products and one double rounding decide it
                 const double a0 = bf16_bits_to_f64(xl[j] & 0xFFFFu), a1 = bf16_bits_to_f64(xl[j] >> 16);
                 const double b0 = bf16_bits_to_f64(xh[j] & 0xFFFFu), b1 = bf16_bits_to_f64(xh[j] >> 16);
-                const double c0 = f32_to_f64_bits(cs[j].x), s0 = f32_to_f64_bits(cs[j].y);
-                const double c1 = f32_to_f64_bits(cs[j].z), s1 = f32_to_f64_bits(cs[j].w);
-                r0 = rot_lo(a0, c0, b0, s0);
-                r1 = rot_lo(a1, c1, b1, s1);
-                r2 = rot_hi(b0, c0, a0, s0);
-                r3 = rot_hi(b1, c1, a1, s1);
+                const double c0 = f32_to_f64_bits(cs[j].x), sn0 = f32_to_f64_bits(cs[j].y);
+                const double c1 = f32_to_f64_bits(cs[j].z), sn1 = f32_to_f64_bits(cs[j].w);
+                yl[j] = rot_lo(a0, c0, b0, sn0) | (rot_lo(a1, c1, b1, sn1) << 16);
+                yh[j] = rot_hi(b0, c0, a0, sn0) | (rot_hi(b1, c1, a1, sn1) << 16);
             }
-            yl[j] = r0 | (r1 << 16);
-            yh[j] = r2 | (r3 << 16);
         }
         if (FP8 && !is_q) {
             const float ks = a.k_scale[head - a.Hq];
@@ -191,10 +200,17 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     const long long c = t - n_rot;
     if (c >= n_cpy) return;
     const int chunks = a.d / 8;
-    const int ch = (int)(c % chunks);
-    const long long bh = c / chunks;
-    const int h = (int)(bh % a.Hkv);
-    const int b = (int)(bh / a.Hkv);
+    const int ch = (int)(c & (chunks - 1));
+    const long long bh = c >> lgc;
+    int h, b;
+    if (bh <= 0xFFFFFFFFLL) {
+        const uint32_t u = (uint32_t)bh;
+        h = (int)(u % (uint32_t)a.Hkv);
+        b = (int)(u / (uint32_t)a.Hkv);
+    } else {
+        h = (int)(bh % a.Hkv);
+        b = (int)(bh / a.Hkv);
+    }
     const int p = a.positions[b];
     const int slot = a.slot_mapping[b];
     if (p < 0 || p >= a.max_pos || slot < 0 || slot >= a.num_blocks * kBlock) return;
