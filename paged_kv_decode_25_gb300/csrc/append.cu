@@ -98,24 +98,56 @@ __device__ __forceinline__ uint2 quantize8(const uint32_t (&x)[4], float scale) 
 
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.f && s <= 3.0e38f; }
 
-// One thread per (request, head, group of 8 rotation pairs): heads 0..Hq-1 are
-// query heads (to q_out), heads Hq..Hq+Hkv-1 key heads (to the cache). Each
-// thread loads its two 16-byte halves and its 8 (cos, sin) pairs before it
+// Words of NJ bf16 pairs (NJ = 4: 16 bytes, NJ = 1: 4 bytes).
+template <int NJ>
+__device__ __forceinline__ void load_words(const uint16_t* src, uint32_t (&x)[NJ]) {
+    if constexpr (NJ == 4) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src);
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+    } else {
+        x[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+}
+template <int NJ>
+__device__ __forceinline__ void store_words(uint16_t* dst, const uint32_t (&y)[NJ]) {
+    if constexpr (NJ == 4) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(y[0], y[1], y[2], y[3]);
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = y[0];
+    }
+}
+template <int NJ>
+__device__ __forceinline__ void store_e4m3(uint8_t* dst, const uint32_t (&y)[NJ], float scale) {
+    if constexpr (NJ == 4) {
+        *reinterpret_cast<uint2*>(dst) = quantize8(y, scale);
+    } else {
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(y[0]), scale),
+                                                                      __fdiv_rn(bf16_hi(y[0]), scale));
+    }
+}
+
+// One thread per (request, head, group of PPT rotation pairs): heads 0..Hq-1
+// are query heads (to q_out), heads Hq..Hq+Hkv-1 key heads (to the cache).
+// Each thread loads its two halves and its PPT (cos, sin) pairs before it
 // computes or stores anything, so q_out may alias q. Threads past the
-// rotation items copy 16-byte chunks of v into the cache.
-template <bool FP8>
+// rotation items copy 16-byte chunks of v into the cache. PPT = 8 for many
+// rows (prefill), 2 for a decode batch (more threads, shorter chains).
+template <bool FP8, int PPT>
 __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     // inputs may come from the kernel just before this one in the stream
     pdl_wait();
     pdl_trigger();
+    constexpr int NJ = PPT / 2;  // 32-bit words (bf16 pairs) per half
     const int half = a.d / 2;
-    const int groups = half / 8;  // 8-pair groups per head
+    const int groups = half / PPT;  // PPT-pair groups per head
     const long long n_rot = (long long)B * (a.Hq + a.Hkv) * groups;
     const long long n_cpy = (long long)B * a.Hkv * (a.d / 8);
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    // d is 64 or 128: groups (d/16) and chunks (d/8) are powers of two, and
-    // the remaining divisions run in 32 bits whenever the quotient range fits
-    const int lgg = a.d == 128 ? 3 : 2, lgc = lgg + 1;
+    // d is 64 or 128: groups (d/2/PPT) and chunks (d/8) are powers of two,
+    // and the remaining divisions run in 32 bits whenever the quotient range
+    // fits
+    const int lgc = a.d == 128 ? 4 : 3;
+    const int lgg = lgc + 2 - (PPT == 8 ? 3 : 1);
     if (t < n_rot) {
         const int grp = (int)(t & (groups - 1));
         const long long bh = t >> lgg;
@@ -132,10 +164,11 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
         const bool is_q = head < a.Hq;
         const uint16_t* src = is_q ? a.q + ((long long)b * a.Hq + head) * a.d
                                    : a.k + ((long long)b * a.Hkv + (head - a.Hq)) * a.d;
-        const int i0 = grp * 8;
+        const int i0 = grp * PPT;
         // issue the independent loads first
-        const uint4 lo = *reinterpret_cast<const uint4*>(src + i0);
-        const uint4 hi = *reinterpret_cast<const uint4*>(src + i0 + half);
+        uint32_t xl[NJ], xh[NJ];
+        load_words<NJ>(src + i0, xl);
+        load_words<NJ>(src + i0 + half, xh);
         const int p = a.positions[b];
         const int slot = is_q ? 0 : a.slot_mapping[b];
         if (p < 0 || p >= a.max_pos) {
@@ -153,14 +186,12 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
             dst_off = (((long long)(slot / kBlock) * a.Hkv + (head - a.Hq)) * kBlock + slot % kBlock) * a.d;
         }
         const float4* cs4 = reinterpret_cast<const float4*>(a.rope + (long long)p * half + i0);
-        float4 cs[4];
+        float4 cs[NJ];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cs[j] = cs4[j];
-        const uint32_t xl[4] = {lo.x, lo.y, lo.z, lo.w};
-        const uint32_t xh[4] = {hi.x, hi.y, hi.z, hi.w};
-        uint32_t yl[4], yh[4];
+        for (int j = 0; j < NJ; ++j) cs[j] = cs4[j];
+        uint32_t yl[NJ], yh[NJ];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             // pairs 2j and 2j+1 of the group: (cos, sin) = cs[j].xy and cs[j].zw
             const float fa0 = bf16_lo(xl[j]), fa1 = bf16_hi(xl[j]);
             const float fb0 = bf16_lo(xh[j]), fb1 = bf16_hi(xh[j]);
@@ -188,13 +219,13 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
                 return;
             }
             uint8_t* dst8 = a.k_cache8 + dst_off;
-            *reinterpret_cast<uint2*>(dst8 + i0) = quantize8(yl, ks);
-            *reinterpret_cast<uint2*>(dst8 + i0 + half) = quantize8(yh, ks);
+            store_e4m3<NJ>(dst8 + i0, yl, ks);
+            store_e4m3<NJ>(dst8 + i0 + half, yh, ks);
             return;
         }
         uint16_t* dst = (is_q ? a.q_out : a.k_cache) + dst_off;
-        *reinterpret_cast<uint4*>(dst + i0) = make_uint4(yl[0], yl[1], yl[2], yl[3]);
-        *reinterpret_cast<uint4*>(dst + i0 + half) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
+        store_words<NJ>(dst + i0, yl);
+        store_words<NJ>(dst + i0 + half, yh);
         return;
     }
     const long long c = t - n_rot;
@@ -272,12 +303,20 @@ mi_status append(const mi_dims* dims, const void* q, const void* k, const void* 
     a.d = D.head_dim;
     a.num_blocks = D.num_blocks;
     a.max_pos = max_pos;
-    const long long threads = (long long)D.B * (D.Hq + D.Hkv) * (D.head_dim / 16) +
+    // few rows (a decode batch): two pairs per thread, else eight
+    const int ppt = D.B <= 256 ? 2 : 8;
+    const long long threads = (long long)D.B * (D.Hq + D.Hkv) * (D.head_dim / 2 / ppt) +
                               (long long)D.B * D.Hkv * (D.head_dim / 8);
     const long long grid = (threads + 127) / 128;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
-    const cudaError_t e = fp8 ? launch_pdl(append_kernel<true>, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B)
-                              : launch_pdl(append_kernel<false>, (int)grid, 128, 0, (cudaStream_t)stream, a, (int)D.B);
+    const cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (ppt == 2)
+        e = fp8 ? launch_pdl(append_kernel<true, 2>, (int)grid, 128, 0, st, a, (int)D.B)
+                : launch_pdl(append_kernel<false, 2>, (int)grid, 128, 0, st, a, (int)D.B);
+    else
+        e = fp8 ? launch_pdl(append_kernel<true, 8>, (int)grid, 128, 0, st, a, (int)D.B)
+                : launch_pdl(append_kernel<false, 8>, (int)grid, 128, 0, st, a, (int)D.B);
     return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }
 

@@ -190,16 +190,18 @@ def test_append_bit_exact_on_extreme_values(cuda_device):
     assert np.array_equal(from_dev_u16(vc_d), vc_ref)
 
 
-def test_append_rotation_bit_exact_on_wide_values(cuda_device):
-    """4,096 rows of q (32 heads) and k (8 heads) at positions spread over a
-    32k table, values over many binades (with zeros of both signs and the
-    bf16 extremes): every rotated output equals the oracle's bit for bit,
+@pytest.mark.parametrize("B,d", [(4096, 128), (256, 128), (200, 64)])
+def test_append_rotation_bit_exact_on_wide_values(cuda_device, B, d):
+    """Rows of q (32 heads) and k (8 heads) at positions spread over a 32k
+    table, values over many binades (with zeros of both signs and the bf16
+    extremes): every rotated output equals the oracle's bit for bit,
     whichever internal route (single precision with exact transforms, or
-    double) a kernel thread takes."""
+    double) a kernel thread takes. 4,096 rows run the eight-pairs-per-thread
+    kernel, a few hundred the two-pairs one."""
     import torch
     mi = _mi()
-    r = np.random.Generator(np.random.PCG64(31))
-    B, Hq, Hkv, d, max_pos, nb = 4096, 32, 8, 128, 32768, 300
+    r = np.random.Generator(np.random.PCG64(31 + B + d))
+    Hq, Hkv, max_pos, nb = 32, 8, 32768, 300
     def wide(shape):
         x = r.standard_normal(shape) * 2.0 ** r.integers(-40, 40, shape)
         x[r.random(shape) < 0.01] = 0.0
