@@ -1,0 +1,94 @@
+// Exact RoPE rotation of one bf16 pair element: RN_bf16(RN_f64(a*b + c*d))
+// for bf16 a, c and fp32 table values b, d (each product exact in double),
+// computed in single precision when that provably gives the same bits, else
+// in double. Shared by the append kernel and the fused decode step, so both
+// write the same bits.
+#pragma once
+
+#include "common.cuh"
+
+namespace mi {
+
+// Exact widening to double built from the bit fields (integer work only);
+// zero, subnormal, infinite and NaN inputs take the hardware conversion.
+__device__ __forceinline__ double bf16_bits_to_f64(uint32_t h) {
+    const uint32_t e = (h >> 7) & 0xFFu;
+    if (e == 0u || e == 0xFFu) return (double)__uint_as_float(h << 16);
+    const uint32_t hi = ((h & 0x8000u) << 16) | ((e + 896u) << 20) | ((h & 0x7Fu) << 13);
+    return __hiloint2double((int)hi, 0);
+}
+
+__device__ __forceinline__ double f32_to_f64_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t e = (u >> 23) & 0xFFu;
+    if (e == 0u || e == 0xFFu) return (double)f;
+    const uint32_t m = u & 0x7FFFFFu;
+    const uint32_t hi = (u & 0x80000000u) | ((e + 896u) << 20) | (m >> 3);
+    return __hiloint2double((int)hi, (int)(m << 29));
+}
+
+// y = RN_bf16(RN_double(a*b - c*d)) with every product exact in double: the
+// fma forms a*b - (c*d) exactly and rounds once, as the two-step form does.
+__device__ __forceinline__ uint32_t rot_lo(double a, double b, double c, double d) {
+    return f64_to_bf16(fma(a, b, -(c * d)));
+}
+__device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double d) {
+    return f64_to_bf16(fma(a, b, c * d));
+}
+
+// RN_bf16(RN_double(a*b + c*d)) for bf16 a, c and fp32 b, d, in single
+// precision when that decides it. q = RN(c*d) and its rounding error qe (an
+// fma recovers it exactly above the underflow range) give c*d = q + qe; the
+// fma s = RN(a*b + q) rounds the exact a*b + q once, so |exact - s| <=
+// ulp(s)/2 + |qe|. When no bf16 rounding boundary (a midpoint between
+// neighbouring bf16 values, or one across a binade below) lies within that
+// bound plus the double rounding's 2^-50 |s| of s, the answer is RN_bf16(s).
+// Otherwise (a boundary within reach, zero, tiny, infinite or NaN values)
+// `slow` is set and the caller takes the double-precision route. Returns s;
+// the caller rounds pairs of them to bf16 with the hardware conversion (the
+// same nearest-even result for the finite, normal s this path keeps).
+// The _rn intrinsics keep the compiler from contracting c*d into an fma,
+// which would break the split.
+__device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bool& slow) {
+    const float q = __fmul_rn(c, d);
+    const float qe = fmaf(c, d, -q);
+    const float s = fmaf(a, b, q);
+    const uint32_t S = __float_as_uint(fabsf(s));
+    const int L = (int)(S & 0xFFFFu);
+    const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L) - 2;
+    const float ulp = __uint_as_float((S & 0x7F800000u) - (23u << 23));
+    const float err = __fadd_rn(__fadd_rn(__fmul_rn(fabsf(qe), 1.0001f), __fmul_rn(fabsf(s), 0x1p-50f)),
+                                __fmul_rn(ulp, 0.5f));
+    const float tiny = 0x1p-100f;
+    const bool ok = isfinite(s) && (q == 0.f || fabsf(q) >= tiny) && fabsf(s) >= tiny &&
+                    err < __fmul_rn((float)dist, ulp);
+    slow |= !ok;
+    return s;
+}
+
+// Rotated bf16 pairs of one group: element k of the first half (lo) and of
+// the second half (hi) of a head, two adjacent pairs per word:
+// ylo = x_lo * cos - x_hi * sin, yhi = x_hi * cos + x_lo * sin,
+// cs = (cos, sin) of pair 2j and (cos, sin) of pair 2j + 1.
+__device__ __forceinline__ void rotate_word(uint32_t xl, uint32_t xh, float4 cs, uint32_t& yl, uint32_t& yh) {
+    const float fa0 = bf16_lo(xl), fa1 = bf16_hi(xl);
+    const float fb0 = bf16_lo(xh), fb1 = bf16_hi(xh);
+    bool slow = false;
+    const float s0 = rot_fast(fa0, cs.x, -fb0, cs.y, slow);
+    const float s1 = rot_fast(fa1, cs.z, -fb1, cs.w, slow);
+    const float s2 = rot_fast(fb0, cs.x, fa0, cs.y, slow);
+    const float s3 = rot_fast(fb1, cs.z, fa1, cs.w, slow);
+    yl = pack_bf16x2(s0, s1);
+    yh = pack_bf16x2(s2, s3);
+    if (slow) {
+        // rare: the exact products and one double rounding decide it
+        const double a0 = bf16_bits_to_f64(xl & 0xFFFFu), a1 = bf16_bits_to_f64(xl >> 16);
+        const double b0 = bf16_bits_to_f64(xh & 0xFFFFu), b1 = bf16_bits_to_f64(xh >> 16);
+        const double c0 = f32_to_f64_bits(cs.x), sn0 = f32_to_f64_bits(cs.y);
+        const double c1 = f32_to_f64_bits(cs.z), sn1 = f32_to_f64_bits(cs.w);
+        yl = rot_lo(a0, c0, b0, sn0) | (rot_lo(a1, c1, b1, sn1) << 16);
+        yh = rot_hi(b0, c0, a0, sn0) | (rot_hi(b1, c1, a1, sn1) << 16);
+    }
+}
+
+}  // namespace mi
