@@ -267,6 +267,25 @@ mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const vo
                                     void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                     mi_stream_t stream);
 
+/* One decode step of a layer in one launch: exactly mi_paged_kv_append with
+ * positions[b] = n - 1 and slot_mapping[b] = block_tables[b][(n-1)/16] * 16 +
+ * (n-1) % 16 (n = context_lens[b], the length after the append), followed by
+ * mi_paged_decode_attention on its outputs; q_out, the new cache rows and out
+ * get the same bits as those two calls. Inside the attention kernel, every
+ * CTA streaming a piece of request b's KV head h rotates that head group's q
+ * itself, and the warp that streams the block holding the new token rotates
+ * its k, writes k and v into that row of the staged tiles and of the cache,
+ * and writes the rotated q to q_out. bf16 caches, the MMA tile.
+ * Device buffers as for the two calls; q is the raw (unrotated) q and must
+ * not overlap q_out (MI_ERR_INVALID_ARG). Requests with n <= 0 append nothing
+ * and get zero rows; n - 1 >= max_pos sets MI_DEVERR_BAD_POS and leaves that
+ * request's q zero. */
+mi_status mi_paged_decode_step(const mi_dims* dims, const void* q, const void* k, const void* v,
+                               const float* rope_cos_sin, int32_t max_pos, const int32_t* block_tables,
+                               const int32_t* context_lens, float scale, void* q_out, void* k_cache,
+                               void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_err, mi_stream_t stream);
+
 /* Kernel variant used by mi_paged_decode_attention_variant:
  *   MI_ATTN_MMA  bf16 tensor-core tiles (mma.sync m16n8k16: 16 tokens x 8 heads),
  *   MI_ATTN_FMA  fp32 CUDA-core FMA tiles.

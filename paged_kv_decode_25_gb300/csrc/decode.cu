@@ -45,6 +45,7 @@
 #include <random>
 
 #include "common.cuh"
+#include "rope.cuh"
 #include "tma.cuh"
 
 namespace mi {
@@ -72,6 +73,16 @@ struct AttnParams {
     float sl2;                     // scale * log2(e)
     const float* k_scale;          // [Hkv] e4m3 caches: per-head dequantisation scales
     const float* v_scale;          // [Hkv]
+    // fused decode step only: the new token's raw q / k / v, the RoPE table,
+    // q_out and the caches to write the new row into
+    const uint16_t* qraw;          // [B][Hq][HD]
+    const uint16_t* knew;          // [B][Hkv][HD]
+    const uint16_t* vnew;          // [B][Hkv][HD]
+    const float2* rope;            // [max_pos][HD/2] (cos, sin)
+    uint16_t* q_out;               // [B][Hq][HD]
+    uint16_t* kc;                  // [num_blocks][Hkv][16][HD]
+    uint16_t* vc;
+    int max_pos;
 };
 
 // ------------------------------------------------------------- the plan ---
@@ -303,6 +314,50 @@ struct MmaState {
         for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m[0] = m[1] = kNegInf;
         l[0] = l[1] = 0.f;
+    }
+
+    // The fused decode step: q of the unit's heads rotated here from the raw
+    // q at position pos (the same exact rotation as mi_paged_kv_append). Dims
+    // d and d + HD/2 of a RoPE pair sit in k-slices kk and kk + kK/2 of the
+    // same lane. pos < 0 leaves q zero.
+    __device__ __forceinline__ void begin_unit_rot(const AttnParams& p, int b, int h, int lane, int pos) {
+        const int n = lane >> 2;
+        const bool ok = n < p.G && pos >= 0;
+        const uint16_t* qrow = p.qraw + ((long long)b * p.Hq + (long long)h * p.G + (ok ? n : 0)) * HD;
+        const float2* cs = p.rope + (long long)(pos >= 0 ? pos : 0) * (HD / 2);
+#pragma unroll
+        for (int kk = 0; kk < kK / 2; ++kk) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int dcol = kk * 16 + (lane & 3) * 2 + e * 8;
+                uint32_t lo = 0u, hi = 0u;
+                if (ok) {
+                    const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol));
+                    const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol + HD / 2));
+                    const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + dcol));
+                    rotate_word(xl, xh, c4, lo, hi);
+                }
+                qb[kk][e] = lo;
+                qb[kk + kK / 2][e] = hi;
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
+    }
+
+    // The rotated q of the unit's heads to q_out (lanes of heads < G).
+    __device__ __forceinline__ void store_q(const AttnParams& p, int b, int h, int lane) const {
+        const int n = lane >> 2;
+        if (n >= p.G) return;
+        uint16_t* qrow = p.q_out + ((long long)b * p.Hq + (long long)h * p.G + n) * HD;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const int dcol = kk * 16 + (lane & 3) * 2;
+            *reinterpret_cast<uint32_t*>(qrow + dcol) = qb[kk][0];
+            *reinterpret_cast<uint32_t*>(qrow + dcol + 8) = qb[kk][1];
+        }
     }
 
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float sl2, int lane) {
@@ -702,10 +757,15 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // runs three CTAs per SM (its per-block conversions make it latency-bound,
 // so more resident warps pay; its tiles are half the size, so the stages
 // still fit), the others two.
-template <int HD, int VAR, int GP, int W>
+// FUSED (MMA tile only): the decode step of mi_paged_decode_step. Each unit's
+// q is rotated where the unit starts; the warp that streams the block holding
+// the new token rotates its k, writes k and v into that row of the staged
+// tiles and of the cache, and writes the unit's rotated q to q_out.
+template <int HD, int VAR, int GP, int W, bool FUSED = false>
 __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
+    static_assert(!FUSED || VAR == kVarMma, "the fused step runs the MMA tile");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
@@ -828,7 +888,20 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
         const long long sa = cu.start > ps ? cu.start : ps;
         const long long se = (cu.start + cu.len) < pe ? (cu.start + cu.len) : pe;
         const int nvalid = ctx_clamped(p, cu.b);
-        st.begin_unit(p, cu.b, cu.h, lane);
+        // fused step: the new token sits at position nvalid - 1, in block jnew
+        int pos = -1, jnew = -1;
+        if constexpr (FUSED) {
+            pos = nvalid - 1;
+            jnew = pos / kBlock;
+            if (pos >= p.max_pos) {
+                if (lane == 0 && warp == 0) raise_err(p.dev_err, MI_DEVERR_BAD_POS);
+                pos = -1;
+                jnew = -1;
+            }
+            st.begin_unit_rot(p, cu.b, cu.h, lane, pos);
+        } else {
+            st.begin_unit(p, cu.b, cu.h, lane);
+        }
         long long x = sa + (((warp - (sa - ps)) % W) + W) % W;
         for (; x < se; x += W) {
             const uint32_t si = (uint32_t)(warp * S) + cstage;
@@ -852,6 +925,35 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                         st_shared_zero16(vt + (VAR == kVarFp8 ? swz8<HD>(row, ch) : swz<HD>(row, ch)));
                     }
                     __syncwarp();
+                }
+                if constexpr (FUSED) {
+                    if (j == jnew) {
+                        // the new token: rotate k, write k and v into row
+                        // valid - 1 of the staged tiles and of the cache, q to q_out
+                        const int row = valid - 1;
+                        const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
+                        const long long rofs = (((long long)blk * p.Hkv + cu.h) * kBlock + row) * HD;
+                        const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
+                        for (int i = 2 * lane; i < HD / 2; i += 64) {
+                            const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + i));
+                            const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + i + HD / 2));
+                            const float4 c4 =
+                                __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + i));
+                            uint32_t yl, yh;
+                            rotate_word(xl, xh, c4, yl, yh);
+                            sts32(kt + swz<HD>(row, i >> 3) + (i & 7) * 2, yl);
+                            sts32(kt + swz<HD>(row, (i + HD / 2) >> 3) + ((i + HD / 2) & 7) * 2, yh);
+                            *reinterpret_cast<uint32_t*>(p.kc + rofs + i) = yl;
+                            *reinterpret_cast<uint32_t*>(p.kc + rofs + i + HD / 2) = yh;
+                        }
+                        for (int i = 2 * lane; i < HD; i += 64) {
+                            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + i));
+                            sts32(vt + swz<HD>(row, i >> 3) + (i & 7) * 2, w);
+                            *reinterpret_cast<uint32_t*>(p.vc + rofs + i) = w;
+                        }
+                        st.store_q(p, cu.b, cu.h, lane);
+                        __syncwarp();
+                    }
                 }
                 if constexpr (VAR != kVarFma) {
                     st.block(kt, vt, valid, p.sl2, lane);
@@ -1139,12 +1241,23 @@ extern "C" size_t mi_paged_decode_workspace_bytes(const mi_dims* dims) {
 namespace mi {
 namespace {
 
+// The new token's inputs of the fused decode step.
+struct StepArgs {
+    const void* k;
+    const void* v;
+    const float* rope;
+    int32_t max_pos;
+    void* q_out;
+};
+
 // Checks, plans and launches one attention call of variant `var` (bf16 caches
-// for kVarMma / kVarFma, e4m3 caches with per-head scales for kVarFp8).
+// for kVarMma / kVarFma, e4m3 caches with per-head scales for kVarFp8); with
+// `step`, the fused decode step (q is then the raw q; MMA tile).
 mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, const void* v_cache,
                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
                     const int32_t* context_lens, float scale, void* out, void* workspace,
-                    size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream, int var, int32_t ctas) {
+                    size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream, int var, int32_t ctas,
+                    const StepArgs* step = nullptr) {
     const mi_status ds = check_dims(dims);
     if (ds != MI_OK) return ds;
     const mi_dims D = *dims;
@@ -1157,6 +1270,17 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
         return MI_ERR_INVALID_ARG;
     if (ctas < 0 || !std::isfinite(scale)) return MI_ERR_INVALID_ARG;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
+    if (step) {
+        if (var != kVarMma || !step->k || !step->v || !step->rope || !step->q_out || step->max_pos < 1)
+            return MI_ERR_INVALID_ARG;
+        if (!aligned16(step->k) || !aligned16(step->v) || !aligned16(step->rope) || !aligned16(step->q_out))
+            return MI_ERR_INVALID_ARG;
+        // q is read by every CTA holding a piece of a unit, q_out written by
+        // one of them: they must not overlap
+        const uintptr_t qa = reinterpret_cast<uintptr_t>(q), oa = reinterpret_cast<uintptr_t>(step->q_out);
+        const uintptr_t qbytes = (uintptr_t)D.B * D.Hq * HD * 2;
+        if (qa < oa + qbytes && oa < qa + qbytes) return MI_ERR_INVALID_ARG;
+    }
     const int S = pick_stages(HD, G, var);
     const int smem = smem_of(HD, G, var);
     // the workspace is sized for the widest grid of any variant; this
@@ -1164,7 +1288,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     const int gmax = max_grid(D);
     if (gmax <= 0) return MI_ERR_CUDA;
     if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
-    KernelFn fn = pick_kernel(HD, var, G);
+    KernelFn fn = step ? (HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps, true> : attn_kernel<128, kVarMma, 8, kWarps, true>)
+                       : pick_kernel(HD, var, G);
     const int gown = grid_for(fn, smem);
     if (gown <= 0 || gown > gmax) return MI_ERR_CUDA;
     const int grid = ctas > 0 && ctas < gown ? ctas : gown;
@@ -1196,6 +1321,14 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.sl2 = scale * 1.4426950408889634f;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.qraw = static_cast<const uint16_t*>(q);
+    p.knew = step ? static_cast<const uint16_t*>(step->k) : nullptr;
+    p.vnew = step ? static_cast<const uint16_t*>(step->v) : nullptr;
+    p.rope = step ? reinterpret_cast<const float2*>(step->rope) : nullptr;
+    p.q_out = step ? static_cast<uint16_t*>(step->q_out) : nullptr;
+    p.kc = static_cast<uint16_t*>(const_cast<void*>(k_cache));
+    p.vc = static_cast<uint16_t*>(const_cast<void*>(v_cache));
+    p.max_pos = step ? step->max_pos : 0;
 
     cudaStream_t s = (cudaStream_t)stream;
     return launch_pdl(fn, grid, (kWarps + 1) * 32, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
@@ -1218,6 +1351,18 @@ extern "C" mi_status mi_paged_decode_attention_variant(const mi_dims* dims, cons
     return attention(dims, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale, out,
                      workspace, workspace_bytes, dev_err, stream, variant == MI_ATTN_FMA ? kVarFma : kVarMma,
                      ctas);
+}
+
+extern "C" mi_status mi_paged_decode_step(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                        const float* rope_cos_sin, int32_t max_pos,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        float scale, void* q_out, void* k_cache, void* v_cache, void* out,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                        mi_stream_t stream) {
+    using namespace mi;
+    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out};
+    return attention(dims, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, dev_err, stream, kVarMma, 0, &step);
 }
 
 extern "C" mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, const void* k_cache,
