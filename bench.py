@@ -678,6 +678,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b",
                     choices=list(WORKLOADS) + list(PREFILL_WORKLOADS) + ["qwen3_8b_swap"])
     ap.add_argument("--variant", default="default", choices=["default", "mma", "fma"])
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode: time append and attention as two calls instead of the fused step")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache element type of the decode step (fp8: e4m3 with per-head scales)")
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -761,9 +763,23 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(ev=None):
+    # bf16 caches on the MMA tile: the fused step (append + attention in one
+    # launch per layer) is the timed path; the two calls are timed after it
+    # to report append and attention separately
+    fused = (not fp8) and variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA) and not args.unfused
+
+    def step(ev=None, fuse=False):
         for layer in range(w.layers):
             kc, vc = caches[layer]
+            if fuse:
+                if ev is not None:
+                    ev[layer][0].record(stream)
+                mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos, bt_d,
+                                                 cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
+                                                 dev_err=err, stream=stream), "decode step")
+                if ev is not None:
+                    ev[layer][1].record(stream)
+                continue
             if fp8:
                 mi.check(mi.mi_paged_kv_append_fp8(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
                                                    max_pos, qo_all[layer], kc, vc, ks_d, vs_d, err, stream),
@@ -784,9 +800,10 @@ def main():
             if ev is not None:
                 ev[layer][1].record(stream)
 
-    # ---- device-timed steps (fixed step replayed; inputs resident)
+    # ---- device-timed steps (fixed step replayed; inputs resident). Every
+    # step rewrites the same new-token rows, so replays see the same inputs.
     for _ in range(args.warmup):
-        step()
+        step(fuse=fused)
     torch.cuda.synchronize()
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
            for _ in range(args.steps)]
@@ -799,7 +816,7 @@ def main():
     torch.cuda.synchronize()
     t_start.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step(evs[s], fuse=fused)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -807,19 +824,43 @@ def main():
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
     step_ms_local = t_start.elapsed_time(t_end) / args.steps
     step_ms = max_over_ranks(step_ms_local, world, device)
-    attn_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
+    kern_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
                for layer in range(w.layers)]
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    # append of layer l runs between the end of layer l-1's attention and its own end event
-    app_ms = [evs[s][layer - 1][1].elapsed_time(evs[s][layer][0]) for s in range(args.steps)
-              for layer in range(1, w.layers)]
-    app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
     a_bytes = attention_bytes(w, cl, kvb)
     step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
     value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
     peak, peak_kind = measured_peak()
-    achieved = a_bytes / (attn_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name + ("_fp8" if fp8 else ""))
+    # the dominant kernel: the fused step (its bytes include the append's), or the attention
+    k_bytes = a_bytes + (append_bytes(w, kvb) if fused else 0)
+    achieved = k_bytes / (kern_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name + ("_fp8" if fp8 else "") + ("_step" if fused else ""))
+
+    # append and attention timed separately (the two calls), for the split
+    split_steps = max(3, min(args.steps, 10)) if fused else 0
+    if fused:
+        evs2 = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
+                for _ in range(split_steps)]
+        for _ in range(2):
+            step()
+        t2a, t2b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t2a.record(stream)
+        for s in range(split_steps):
+            step(evs2[s])
+        t2b.record(stream)
+        torch.cuda.synchronize()
+        two_call_step_ms = t2a.elapsed_time(t2b) / split_steps
+    else:
+        evs2, two_call_step_ms = evs, step_ms
+        split_steps = args.steps
+    attn_ms = [evs2[s][layer][0].elapsed_time(evs2[s][layer][1]) for s in range(split_steps)
+               for layer in range(w.layers)]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    # append of layer l runs between the end of layer l-1's attention and its own end event
+    app_ms = [evs2[s][layer - 1][1].elapsed_time(evs2[s][layer][0]) for s in range(split_steps)
+              for layer in range(1, w.layers)]
+    app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
 
     # ---- end to end: real decode steps from host buffers through the C ABI
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
@@ -843,10 +884,11 @@ def main():
                                                 h_cl.numpy(), h_sl.numpy())
         mi.check(st_, "batch_meta")
         h_pos.numpy()[:] = h_cl.numpy() - 1
-        for src, dst in ((h_bt, bt_d), (h_cl, cl_d), (h_sl, sl_d), (h_pos, pos_d), (h_q, q_all), (h_k, k_all),
-                         (h_v, v_all)):
+        copies = ((h_bt, bt_d), (h_cl, cl_d)) + (() if fused else ((h_sl, sl_d), (h_pos, pos_d))) + \
+            ((h_q, q_all), (h_k, k_all), (h_v, v_all))
+        for src, dst in copies:
             dst.copy_(src, non_blocking=True)
-        step()
+        step(fuse=fused)
         h_out.copy_(out_all, non_blocking=True)
         torch.cuda.synchronize()
         e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy(), kvb) + append_bytes(w, kvb))
@@ -860,7 +902,8 @@ def main():
         e2e_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
-    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_cl, h_sl, h_pos, h_q, h_k, h_v))
+    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_cl, h_q, h_k, h_v)) + \
+        (0 if fused else sum(t.numel() * t.element_size() for t in (h_sl, h_pos)))
     d2h = h_out.numel() * h_out.element_size()
     e2e_val = world * (e2e_bytes / e2e_steps) / (e2e_s / e2e_steps) / 1e9
 
@@ -878,16 +921,21 @@ def main():
                        kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16"),
         "steps_per_s": 1e3 / step_ms * world,
         "hbm_frac_step": value / world / peak,
-        "per_layer_ms": {"append": app_avg_ms, "attention": attn_avg_ms, "append+attention": step_ms / w.layers,
+        "per_layer_ms": {"step": step_ms / w.layers, "fused_step_kernel": kern_avg_ms if fused else None,
+                         "append": app_avg_ms, "attention": attn_avg_ms,
+                         "append+attention (two calls)": two_call_step_ms / w.layers,
                          "append_bytes": append_bytes(w, kvb), "attention_bytes": a_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "paged decode attention (split-KV kernel with the LSE combine of cut units fused), per layer",
-                     "algorithmic_bytes_per_launch": a_bytes, "avg_launch_ms": attn_avg_ms},
+                     "kernel": ("fused decode step (RoPE + cache write of the new token, split-KV attention, "
+                                "LSE combine), per layer" if fused else
+                                "paged decode attention (split-KV kernel with the LSE combine of cut units fused), "
+                                "per layer"),
+                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": kern_avg_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
-        "gpu_launches": args.steps * w.layers * 2,  # append + attention per layer
+        "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

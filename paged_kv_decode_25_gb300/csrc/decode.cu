@@ -264,12 +264,15 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, flag, total;
+    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, flag, qring, qbar, total;
 };
 
-// W consumer warps plus one producer warp; S stages per consumer warp. The
-// weight-exchange buffer is only needed by the CUDA-core tile.
-__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma, int eb = 2) {
+// W consumer warps plus one producer warp (and, for the fused step, one RoPE
+// warp); S stages per consumer warp. The weight-exchange buffer is only needed
+// by the CUDA-core tile; the fused step adds a two-slot ring of rotated q rows
+// ([G][HD] bf16 each) with full / empty barriers.
+__host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma, int eb = 2,
+                                             bool fused = false) {
     SmemPlan s;
     int off = 0;
     s.tiles = off; off += W * S * 2 * kBlock * HD * eb;
@@ -281,8 +284,10 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.obuf = off;  off += W * G * HD * 4;
     s.xbuf = off;  off += fma ? W * (kBlock * kMaxG + kMaxG) * 4 : 0;
     off = (off + 15) & ~15;
-    s.scan = off;  off += ((W + 1) * 32 + 1 + 32) * 8;
+    s.scan = off;  off += ((W + (fused ? 2 : 1)) * 32 + 1 + 32) * 8;
     s.flag = off;  off += 16;
+    s.qring = off; off += fused ? 2 * (G + 2) * HD * 2 : 0;  // per slot: q rows [G][HD], new k row, new v row
+    s.qbar = off;  off += fused ? 4 * 8 : 0;
     s.total = off + 1024;  // slack to align the tiles to 1024 bytes
     return s;
 }
@@ -316,48 +321,22 @@ struct MmaState {
         l[0] = l[1] = 0.f;
     }
 
-    // The fused decode step: q of the unit's heads rotated here from the raw
-    // q at position pos (the same exact rotation as mi_paged_kv_append). Dims
-    // d and d + HD/2 of a RoPE pair sit in k-slices kk and kk + kK/2 of the
-    // same lane. pos < 0 leaves q zero.
-    __device__ __forceinline__ void begin_unit_rot(const AttnParams& p, int b, int h, int lane, int pos) {
+    // The fused decode step: q of the unit's heads from rotated rows [G][HD]
+    // bf16 in shared memory (the RoPE warp's ring slot).
+    __device__ __forceinline__ void begin_unit_from(const uint16_t* qrows, const AttnParams& p, int lane) {
         const int n = lane >> 2;
-        const bool ok = n < p.G && pos >= 0;
-        const uint16_t* qrow = p.qraw + ((long long)b * p.Hq + (long long)h * p.G + (ok ? n : 0)) * HD;
-        const float2* cs = p.rope + (long long)(pos >= 0 ? pos : 0) * (HD / 2);
+        const bool ok = n < p.G;
+        const uint16_t* qrow = qrows + (ok ? n : 0) * HD;
 #pragma unroll
-        for (int kk = 0; kk < kK / 2; ++kk) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int dcol = kk * 16 + (lane & 3) * 2 + e * 8;
-                uint32_t lo = 0u, hi = 0u;
-                if (ok) {
-                    const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol));
-                    const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(qrow + dcol + HD / 2));
-                    const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + dcol));
-                    rotate_word(xl, xh, c4, lo, hi);
-                }
-                qb[kk][e] = lo;
-                qb[kk + kK / 2][e] = hi;
-            }
+        for (int kk = 0; kk < kK; ++kk) {
+            const int dcol = kk * 16 + (lane & 3) * 2;
+            qb[kk][0] = ok ? *reinterpret_cast<const uint32_t*>(qrow + dcol) : 0u;
+            qb[kk][1] = ok ? *reinterpret_cast<const uint32_t*>(qrow + dcol + 8) : 0u;
         }
 #pragma unroll
         for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m[0] = m[1] = kNegInf;
         l[0] = l[1] = 0.f;
-    }
-
-    // The rotated q of the unit's heads to q_out (lanes of heads < G).
-    __device__ __forceinline__ void store_q(const AttnParams& p, int b, int h, int lane) const {
-        const int n = lane >> 2;
-        if (n >= p.G) return;
-        uint16_t* qrow = p.q_out + ((long long)b * p.Hq + (long long)h * p.G + n) * HD;
-#pragma unroll
-        for (int kk = 0; kk < kK; ++kk) {
-            const int dcol = kk * 16 + (lane & 3) * 2;
-            *reinterpret_cast<uint32_t*>(qrow + dcol) = qb[kk][0];
-            *reinterpret_cast<uint32_t*>(qrow + dcol + 8) = qb[kk][1];
-        }
     }
 
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, float sl2, int lane) {
@@ -747,6 +726,11 @@ struct StateOf<HD, kVarFma, GP> { using T = FmaState<HD, GP>; };
 template <int HD, int GP>
 struct StateOf<HD, kVarFp8, GP> { using T = Fp8State<HD>; };
 
+// A bounded wait by every lane of a warp; true when all of them saw the phase.
+__device__ __forceinline__ bool wait_all_warp(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
 __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -757,19 +741,22 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // runs three CTAs per SM (its per-block conversions make it latency-bound,
 // so more resident warps pay; its tiles are half the size, so the stages
 // still fit), the others two.
-// FUSED (MMA tile only): the decode step of mi_paged_decode_step. Each unit's
-// q is rotated where the unit starts; the warp that streams the block holding
-// the new token rotates its k, writes k and v into that row of the staged
-// tiles and of the cache, and writes the unit's rotated q to q_out.
+// FUSED (MMA tile only): the decode step of mi_paged_decode_step. An extra
+// RoPE warp walks the CTA's units in the consumers' order and, ahead of them,
+// fills a two-slot ring with each unit's rotated q rows and the new token's
+// rotated k row and v row; when the block holding the new token is in this
+// CTA's range it also writes that row of the cache and the unit's q_out. The
+// consumer warp that streams that block copies the two rows into its staged
+// tiles.
 template <int HD, int VAR, int GP, int W, bool FUSED = false>
-__global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
+__global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
     static_assert(!FUSED || VAR == kVarMma, "the fused step runs the MMA tile");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
-    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma, elem_bytes(VAR));
+    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma, elem_bytes(VAR), FUSED);
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t* base = smem_raw + pad;
@@ -781,6 +768,11 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     if (tid < W * S) {
         mbar_init(full0 + tid * 8, 1);
         mbar_init(empty0 + tid * 8, 1);
+    }
+    const uint32_t qfull0 = sbase + sp.qbar, qempty0 = qfull0 + 16;  // fused step: q ring
+    if (FUSED && tid < 2) {
+        mbar_init(qfull0 + tid * 8, 1);
+        mbar_init(qempty0 + tid * 8, W);
     }
     fence_mbar_init();
     // Inputs may come from the kernel just before this one in the stream.
@@ -806,6 +798,82 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     if (rb > ra) {
         const Cursor cl = locate(p, uc, scan, blockDim.x, rb - 1);
         if (cl.start > ra && cl.start + cl.len > rb) sl = cl.start;
+    }
+
+    if (FUSED && warp == W + 1) {
+        // --------------------------------------------------- RoPE warp --
+        // the consumers' unit order: part 0 = [sl, rb), then part 1 = [ra, sl)
+        if (cta >= P) return;
+        uint16_t* ring = reinterpret_cast<uint16_t*>(base + sp.qring);
+        int u = 0;
+        bool good = true;
+        for (int part = 0; good && part < 2; ++part) {
+            const long long ps = part == 0 ? sl : ra, pe = part == 0 ? rb : sl;
+            if (ps >= pe) continue;
+            Cursor cu = locate(p, uc, scan, blockDim.x, ps);
+            for (; good && cu.start < pe && cu.b < p.B; cu.next(p), ++u) {
+                const int slot = u & 1;
+                if (!wait_all_warp(qempty0 + slot * 8, (uint32_t)(((u >> 1) & 1) ^ 1))) {
+                    if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+                    good = false;
+                    break;
+                }
+                int pos = ctx_clamped(p, cu.b) - 1;
+                if (pos >= p.max_pos) pos = -1;
+                uint16_t* qrows = ring + slot * (p.G + 2) * HD;
+                uint16_t* krow = qrows + p.G * HD;
+                uint16_t* vrow = krow + HD;
+                for (int w = lane; w < p.G * HD / 4; w += 32) {
+                    const int g = w / (HD / 4), k = (w % (HD / 4)) * 2;
+                    uint32_t yl = 0u, yh = 0u;
+                    if (pos >= 0) {
+                        const uint16_t* qr = p.qraw + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD;
+                        const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(qr + k));
+                        const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(qr + k + HD / 2));
+                        const float4 c4 = __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + k));
+                        rotate_word(xl, xh, c4, yl, yh);
+                    }
+                    *reinterpret_cast<uint32_t*>(qrows + g * HD + k) = yl;
+                    *reinterpret_cast<uint32_t*>(qrows + g * HD + k + HD / 2) = yh;
+                }
+                if (pos >= 0) {
+                    const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
+                    for (int k = 2 * lane; k < HD / 2; k += 64) {
+                        const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + k));
+                        const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + k + HD / 2));
+                        const float4 c4 = __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + k));
+                        uint32_t yl, yh;
+                        rotate_word(xl, xh, c4, yl, yh);
+                        *reinterpret_cast<uint32_t*>(krow + k) = yl;
+                        *reinterpret_cast<uint32_t*>(krow + k + HD / 2) = yh;
+                    }
+                    for (int k = 2 * lane; k < HD; k += 64)
+                        *reinterpret_cast<uint32_t*>(vrow + k) = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + k));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qfull0 + slot * 8);
+                if (pos >= 0) {
+                    // the block holding the new token is streamed here: this
+                    // CTA writes the cache row and the unit's q_out
+                    const int jnew = pos / kBlock;
+                    const long long jx = cu.start + jnew;
+                    if (jx >= ra && jx < rb) {
+                        const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + jnew);
+                        if (blk >= 0 && blk < p.num_blocks) {
+                            const long long rofs = (((long long)blk * p.Hkv + cu.h) * kBlock + pos % kBlock) * HD;
+                            for (int k = 2 * lane; k < HD; k += 64) {
+                                *reinterpret_cast<uint32_t*>(p.kc + rofs + k) = *reinterpret_cast<const uint32_t*>(krow + k);
+                                *reinterpret_cast<uint32_t*>(p.vc + rofs + k) = *reinterpret_cast<const uint32_t*>(vrow + k);
+                            }
+                        }
+                        uint16_t* qo = p.q_out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G) * HD;
+                        for (int w = lane; w < p.G * HD / 2; w += 32)
+                            reinterpret_cast<uint32_t*>(qo)[w] = reinterpret_cast<const uint32_t*>(qrows)[w];
+                    }
+                }
+            }
+        }
+        return;
     }
 
     if (warp == W) {
@@ -877,6 +945,8 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
     const int nc = W * 32;
     using State = typename StateOf<HD, VAR, GP>::T;
     State st;
+    int unit_no = 0;  // fused step: units begun so far (q ring slot and phase)
+    const uint16_t* qslot = nullptr;  // fused step: this unit's ring slot
     bool dead = false;  // a wait timed out: stop touching the pipeline
     uint32_t cstage = 0, cphase = 0;
 
@@ -898,7 +968,14 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                 pos = -1;
                 jnew = -1;
             }
-            st.begin_unit_rot(p, cu.b, cu.h, lane, pos);
+            // this unit's rotated q from the RoPE warp's ring
+            const int slot = unit_no & 1;
+            if (!dead && !wait_all_warp(qfull0 + slot * 8, (uint32_t)((unit_no >> 1) & 1))) {
+                dead = true;
+                if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            }
+            qslot = reinterpret_cast<const uint16_t*>(base + sp.qring) + slot * (p.G + 2) * HD;
+            st.begin_unit_from(qslot, p, lane);
         } else {
             st.begin_unit(p, cu.b, cu.h, lane);
         }
@@ -928,30 +1005,15 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                 }
                 if constexpr (FUSED) {
                     if (j == jnew) {
-                        // the new token: rotate k, write k and v into row
-                        // valid - 1 of the staged tiles and of the cache, q to q_out
+                        // the new token: its rotated k and its v (from the
+                        // RoPE warp's ring slot) into row valid - 1 of the tiles
                         const int row = valid - 1;
-                        const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + j);
-                        const long long rofs = (((long long)blk * p.Hkv + cu.h) * kBlock + row) * HD;
-                        const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
-                        for (int i = 2 * lane; i < HD / 2; i += 64) {
-                            const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + i));
-                            const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + i + HD / 2));
-                            const float4 c4 =
-                                __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + i));
-                            uint32_t yl, yh;
-                            rotate_word(xl, xh, c4, yl, yh);
-                            sts32(kt + swz<HD>(row, i >> 3) + (i & 7) * 2, yl);
-                            sts32(kt + swz<HD>(row, (i + HD / 2) >> 3) + ((i + HD / 2) & 7) * 2, yh);
-                            *reinterpret_cast<uint32_t*>(p.kc + rofs + i) = yl;
-                            *reinterpret_cast<uint32_t*>(p.kc + rofs + i + HD / 2) = yh;
-                        }
+                        const uint16_t* krow = qslot + p.G * HD;
+                        const uint16_t* vrow = krow + HD;
                         for (int i = 2 * lane; i < HD; i += 64) {
-                            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + i));
-                            sts32(vt + swz<HD>(row, i >> 3) + (i & 7) * 2, w);
-                            *reinterpret_cast<uint32_t*>(p.vc + rofs + i) = w;
+                            sts32(kt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(krow + i));
+                            sts32(vt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(vrow + i));
                         }
-                        st.store_q(p, cu.b, cu.h, lane);
                         __syncwarp();
                     }
                 }
@@ -971,6 +1033,12 @@ __global__ void __launch_bounds__((W + 1) * 32, VAR == kVarFp8 ? 3 : 2)
                 cstage = 0;
                 cphase ^= 1u;
             }
+        }
+        if constexpr (FUSED) {
+            // this warp is done with the unit's ring slot
+            __syncwarp();
+            if (lane == 0 && !dead) mbar_arrive(qempty0 + (unit_no & 1) * 8);
+            ++unit_no;
         }
         // merge the warps' states for this unit (a warp without a block in
         // it stores its initial state: max -inf, sum 0, output 0)
@@ -1101,21 +1169,21 @@ constexpr int kSmemThreePerSm = 76800;    // per CTA so that three fit
 // wide GQA groups) as many as fit one CTA. e4m3 tiles are half the size, so
 // they take up to twice the stages, and first try for three CTAs per SM with
 // at least two stages each.
-int pick_stages(int HD, int G, int var) {
+int pick_stages(int HD, int G, int var, bool fused = false) {
     const bool fma = var == kVarFma;
     const int eb = elem_bytes(var), top = kMaxStages * 2 / eb;
     if (var == kVarFp8)
         for (int S = top; S >= 2; --S)
-            if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemThreePerSm) return S;
+            if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemThreePerSm) return S;
     for (int S = top; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemTwoPerSm) return S;
+        if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemTwoPerSm) return S;
     for (int S = top; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma, eb).total <= kSmemLimit) return S;
+        if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemLimit) return S;
     return 0;
 }
 
-int smem_of(int HD, int G, int var) {
-    return smem_plan(kWarps, pick_stages(HD, G, var), HD, G, var == kVarFma, elem_bytes(var)).total;
+int smem_of(int HD, int G, int var, bool fused = false) {
+    return smem_plan(kWarps, pick_stages(HD, G, var, fused), HD, G, var == kVarFma, elem_bytes(var), fused).total;
 }
 
 int gp_of(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : 8); }
@@ -1148,7 +1216,7 @@ struct GridKey {
 // The first query for a (device, kernel) raises the kernel's dynamic
 // shared-memory limit to the largest plan any shape uses, so a launch never
 // depends on which shape was seen last; the grid is cached per smem size.
-int grid_for(KernelFn fn, int smem) {
+int grid_for(KernelFn fn, int smem, int threads = (kWarps + 1) * 32) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     static std::mutex mu;
@@ -1164,8 +1232,8 @@ int grid_for(KernelFn fn, int smem) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), (kWarps + 1) * 32,
-                                                      smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reinterpret_cast<const void*>(fn), threads, smem) !=
+        cudaSuccess)
         return 0;
     const int g = sms * (occ > 0 ? occ : 1);
     if (nkeys < 128) {
@@ -1281,8 +1349,11 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
         const uintptr_t qbytes = (uintptr_t)D.B * D.Hq * HD * 2;
         if (qa < oa + qbytes && oa < qa + qbytes) return MI_ERR_INVALID_ARG;
     }
-    const int S = pick_stages(HD, G, var);
-    const int smem = smem_of(HD, G, var);
+    const bool fused = step != nullptr;
+    const int S = pick_stages(HD, G, var, fused);
+    const int smem = smem_of(HD, G, var, fused);
+    const int threads = (kWarps + (fused ? 2 : 1)) * 32;
+    if (S <= 0) return MI_ERR_UNSUPPORTED;
     // the workspace is sized for the widest grid of any variant; this
     // kernel's own persistent grid is its SMs x resident CTAs
     const int gmax = max_grid(D);
@@ -1290,7 +1361,7 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
     KernelFn fn = step ? (HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps, true> : attn_kernel<128, kVarMma, 8, kWarps, true>)
                        : pick_kernel(HD, var, G);
-    const int gown = grid_for(fn, smem);
+    const int gown = grid_for(fn, smem, threads);
     if (gown <= 0 || gown > gmax) return MI_ERR_CUDA;
     const int grid = ctas > 0 && ctas < gown ? ctas : gown;
 
@@ -1331,7 +1402,7 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.max_pos = step ? step->max_pos : 0;
 
     cudaStream_t s = (cudaStream_t)stream;
-    return launch_pdl(fn, grid, (kWarps + 1) * 32, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+    return launch_pdl(fn, grid, threads, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }
 
 }  // namespace
