@@ -287,7 +287,7 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.scan = off;  off += ((W + (fused ? 2 : 1)) * 32 + 1 + 32) * 8;
     s.flag = off;  off += 16;
     s.qring = off; off += fused ? 2 * (G + 2) * HD * 2 : 0;  // per slot: q rows [G][HD], new k row, new v row
-    s.qbar = off;  off += fused ? 4 * 8 : 0;
+    s.qbar = off;  off += fused ? 6 * 8 : 0;  // q full [2], empty [2], k/v rows full [2]
     s.total = off + 1024;  // slack to align the tiles to 1024 bytes
     return s;
 }
@@ -769,10 +769,11 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
         mbar_init(full0 + tid * 8, 1);
         mbar_init(empty0 + tid * 8, 1);
     }
-    const uint32_t qfull0 = sbase + sp.qbar, qempty0 = qfull0 + 16;  // fused step: q ring
+    const uint32_t qfull0 = sbase + sp.qbar, qempty0 = qfull0 + 16, kvfull0 = qfull0 + 32;  // fused step: ring
     if (FUSED && tid < 2) {
         mbar_init(qfull0 + tid * 8, 1);
         mbar_init(qempty0 + tid * 8, W);
+        mbar_init(kvfull0 + tid * 8, 1);
     }
     fence_mbar_init();
     // Inputs may come from the kernel just before this one in the stream.
@@ -836,6 +837,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                     *reinterpret_cast<uint32_t*>(qrows + g * HD + k) = yl;
                     *reinterpret_cast<uint32_t*>(qrows + g * HD + k + HD / 2) = yh;
                 }
+                // q first: the consumers need it where the unit starts, the
+                // new token's rows only at its last block
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qfull0 + slot * 8);
                 if (pos >= 0) {
                     const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
                     for (int k = 2 * lane; k < HD / 2; k += 64) {
@@ -851,7 +856,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                         *reinterpret_cast<uint32_t*>(vrow + k) = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + k));
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(qfull0 + slot * 8);
+                if (lane == 0) mbar_arrive(kvfull0 + slot * 8);
                 if (pos >= 0) {
                     // the block holding the new token is streamed here: this
                     // CTA writes the cache row and the unit's q_out
@@ -1008,6 +1013,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                         // the new token: its rotated k and its v (from the
                         // RoPE warp's ring slot) into row valid - 1 of the tiles
                         const int row = valid - 1;
+                        if (!wait_all_warp(kvfull0 + (unit_no & 1) * 8, (uint32_t)((unit_no >> 1) & 1))) {
+                            dead = true;
+                            if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+                        }
                         const uint16_t* krow = qslot + p.G * HD;
                         const uint16_t* vrow = krow + HD;
                         for (int i = 2 * lane; i < HD; i += 64) {
