@@ -169,9 +169,9 @@ def test_step_bad_position_and_overlap(cuda_device):
     import torch
     mi = _mi()
     r = np.random.Generator(np.random.PCG64(3))
-    B, Hq, Hkv, dh, nb = 2, 4, 2, 64, 8
-    cl = np.array([5, 40], np.int32)
-    bt = np.array([[0, -1, -1], [1, 2, 3]], np.int32)
+    B, Hq, Hkv, dh, nb = 3, 4, 2, 64, 8
+    cl = np.array([5, 40, 0], np.int32)  # request 2 is empty: no append, a zero row
+    bt = np.array([[0, -1, -1], [1, 2, 3], [-1, -1, -1]], np.int32)
     kc = bf16_normal(r, (nb, Hkv, 16, dh))
     vc = bf16_normal(r, (nb, Hkv, 16, dh))
     q, k, v = bf16_normal(r, (B, Hq, dh)), bf16_normal(r, (B, Hkv, dh)), bf16_normal(r, (B, Hkv, dh))
@@ -189,6 +189,8 @@ def test_step_bad_position_and_overlap(cuda_device):
     assert mi.mi_paged_decode_step(d, q_d, *args, qo_d, kc_d, vc_d, out, ws, dev_err=err) == 0
     torch.cuda.synchronize()
     assert int(err.item()) & mi.MI_DEVERR_BAD_POS
-    assert np.all(np.isfinite(oracle.bf16_to_f64(from_dev_u16(out))))
+    got = from_dev_u16(out)
+    assert np.all(np.isfinite(oracle.bf16_to_f64(got)))
+    assert np.all(got[2] == 0)
     # q_out over q (in place) is refused: other CTAs may still read q
     assert mi.mi_paged_decode_step(d, q_d, *args, q_d, kc_d, vc_d, out, ws, dev_err=err) == mi.MI_ERR_INVALID_ARG
