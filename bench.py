@@ -761,14 +761,15 @@ def main():
     bt_d, cl_d, sl_d, pos_d = i32(bt), i32(cl), i32(sl), i32(pos)
     ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
-    stream = torch.cuda.current_stream(device)
+    stream = stream0 = torch.cuda.current_stream(device)
 
     # bf16 caches on the MMA tile: the fused step (append + attention in one
     # launch per layer) is the timed path; the two calls are timed after it
     # to report append and attention separately
     fused = (not fp8) and variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA) and not args.unfused
 
-    def step(ev=None, fuse=False):
+    def step(ev=None, fuse=False, st=None):
+        stream = st if st is not None else stream0
         for layer in range(w.layers):
             kc, vc = caches[layer]
             if fuse:
@@ -862,6 +863,28 @@ def main():
     app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
 
+    # the timed step captured once in a CUDA graph and replayed (launches of
+    # the whole step queued by one call; same kernels, same arguments)
+    graph_steps = max(3, min(args.steps, 20))
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(fuse=fused, st=torch.cuda.current_stream(device))
+        for _ in range(2):
+            g.replay()
+        tga, tgb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tga.record(stream)
+        for _ in range(graph_steps):
+            g.replay()
+        tgb.record(stream)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+        graph = {"ms_per_step": tga.elapsed_time(tgb) / graph_steps, "steps": graph_steps,
+                 "what": "the same step captured once in a CUDA graph and replayed"}
+        del g
+    except RuntimeError as e:  # capture refused by this torch / driver: report, keep the stream numbers
+        graph = {"unavailable": str(e).splitlines()[0][:200]}
+
     # ---- end to end: real decode steps from host buffers through the C ABI
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
     ctx_now = cl.copy()
@@ -936,6 +959,7 @@ def main():
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
+        "cuda_graph": graph,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

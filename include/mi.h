@@ -260,7 +260,11 @@ size_t mi_paged_decode_workspace_bytes(const mi_dims* dims);
  * dev_err int32 or NULL. Only the first ceil(n/16) entries of a table row are
  * read. Tokens past n in the last block are never used (they may hold any bits,
  * NaN included). Results are bitwise independent of where blocks sit in the
- * cache. */
+ * cache. The call may be captured in a CUDA graph and the graph replayed any
+ * number of times over the same workspace (each launch hands back its merge
+ * counters zeroed); after a launch that set MI_DEVERR_TIMEOUT, zero the
+ * workspace before the next replay. The same holds for the e4m3, fused
+ * step and no-allocation variants below. */
 mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* block_tables,
                                     const int32_t* context_lens, float scale, void* out,

@@ -29,8 +29,8 @@
 //     bf16 output; a unit cut by range edges leaves a normalised fp32 partial
 //     and its log-sum-exp per piece in the workspace, then bumps the unit's
 //     counter word (tagged with the call's epoch, so it never needs clearing);
-//     the CTA that stores the last piece merges the unit (log-sum-exp
-//     combine). Each CTA streams the cut unit at its range end first, so
+//     the CTA that stores the last piece zeroes the word and merges the unit
+//     (log-sum-exp combine). Each CTA streams the cut unit at its range end first, so
 //     these merges happen early rather than at the end of the kernel.
 // The split depends only on the context lengths and the grid size, so results
 // are bitwise independent of which physical blocks a request holds.
@@ -1104,9 +1104,9 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
             if (tid == 0) {
                 // one counter word per cut unit, at its first piece's CTA:
                 // high 48 bits = the call's epoch, low 16 = pieces stored. A
-                // word from another call counts as zero, so nothing needs
-                // clearing. acq_rel: this CTA's partial is published before
-                // the count, the others' partials are visible after it.
+                // word from another call counts as zero, so the buffer needs
+                // no clearing. acq_rel: this CTA's partial is published
+                // before the count, the others' partials are visible after it.
                 unsigned long long* wd = p.unit_word + cf;
                 const unsigned long long e48 = p.epoch & 0xFFFFFFFFFFFFull;
                 unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(wd), nw, got;
@@ -1117,7 +1117,12 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                     if (got == old) break;
                     old = got;
                 }
-                *mflag = (int)(nw & 0xFFFFull) == ns;
+                const bool last = (int)(nw & 0xFFFFull) == ns;
+                // The last piece hands the word back as zero (epochs are
+                // never zero), so a replay of the same launch (a captured
+                // graph keeps its epoch) starts every count afresh.
+                if (last) *reinterpret_cast<volatile unsigned long long*>(wd) = 0ull;
+                *mflag = last;
             }
             consumer_sync(nc);
             if (*mflag) {
@@ -1281,8 +1286,9 @@ int max_grid(const mi_dims& D) {
 }
 
 // Workspace: [unit counter words, one per CTA | partial slots, two per CTA].
-// The words carry the epoch of the call that wrote them, so nothing needs
-// clearing between calls.
+// A word carries the epoch of the call that wrote it and is zeroed by the
+// unit's last piece, so nothing needs clearing between calls and a captured
+// launch can be replayed with its one epoch.
 size_t word_bytes(int grid) { return (((size_t)grid * 8) + 255) / 256 * 256; }
 
 size_t workspace_for(const mi_dims& D, int grid) {
@@ -1291,7 +1297,8 @@ size_t workspace_for(const mi_dims& D, int grid) {
 
 // A distinct value per call (in this process): a random start, then a
 // counter, so a word left by earlier work in the buffer is never mistaken for
-// this call's (the kernel compares the low 48 bits).
+// this call's (the kernel compares the low 48 bits). The low bit is set, so an
+// epoch is never the zero a finished unit leaves behind.
 unsigned long long next_epoch() {
     static std::atomic<unsigned long long> ctr{0};
     static const unsigned long long start = [] {
@@ -1299,7 +1306,7 @@ unsigned long long next_epoch() {
         return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd() ^
                (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
     }();
-    return start + 2 * ctr.fetch_add(1) + 1;
+    return (start + 2 * ctr.fetch_add(1)) | 1ull;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
