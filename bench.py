@@ -803,11 +803,37 @@ def main():
 
     # ---- device-timed steps (fixed step replayed; inputs resident). Every
     # step rewrites the same new-token rows, so replays see the same inputs.
-    for _ in range(args.warmup):
-        step(fuse=fused)
+    # The timed region is one replay of a CUDA graph that holds the K steps
+    # (the launches a serving loop captures once), with a CUDA event captured
+    # before and after every timed kernel; where this torch cannot record
+    # events inside a graph, the K steps are launched on the stream instead.
+    def new_events(n, **kw):
+        return [[[torch.cuda.Event(enable_timing=True, **kw) for _ in range(2)] for _ in range(w.layers)]
+                for _ in range(n)]
+
+    step(fuse=fused)  # first launches (kernel attributes, tensor maps) happen outside any capture
     torch.cuda.synchronize()
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
-           for _ in range(args.steps)]
+    g_warm = g_timed = None
+    try:
+        evs = new_events(args.steps, external=True)
+        g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_warm):
+            step(fuse=fused, st=torch.cuda.current_stream(device))
+        with torch.cuda.graph(g_timed):
+            cap = torch.cuda.current_stream(device)
+            for s in range(args.steps):
+                step(evs[s], fuse=fused, st=cap)
+        launch_mode = "cuda graph of the K steps, replayed once"
+    except (TypeError, RuntimeError) as e:  # no events inside graphs on this torch
+        g_warm = g_timed = None
+        evs = new_events(args.steps)
+        launch_mode = "stream launches (%s)" % str(e).splitlines()[0][:120]
+    for _ in range(args.warmup):
+        if g_warm is not None:
+            g_warm.replay()
+        else:
+            step(fuse=fused)
+    torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     clocks = ClockSampler(int(vis[local]) if len(vis) > local and vis[local].isdigit() else local)
@@ -816,8 +842,11 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     t_start.record(stream)
-    for s in range(args.steps):
-        step(evs[s], fuse=fused)
+    if g_timed is not None:
+        g_timed.replay()
+    else:
+        for s in range(args.steps):
+            step(evs[s], fuse=fused)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -828,6 +857,22 @@ def main():
     kern_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
                for layer in range(w.layers)]
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    del g_warm, g_timed
+
+    # the same steps launched one by one on the stream (per-kernel events
+    # between the launches), for comparison with the graph
+    stream_steps = max(3, min(args.steps, 10))
+    evs_s = new_events(stream_steps)
+    tsa, tsb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tsa.record(stream)
+    for s in range(stream_steps):
+        step(evs_s[s], fuse=fused)
+    tsb.record(stream)
+    torch.cuda.synchronize()
+    stream_launch = {"ms_per_step": tsa.elapsed_time(tsb) / stream_steps, "steps": stream_steps,
+                     "timed_kernel_ms": sum(evs_s[s][layer][0].elapsed_time(evs_s[s][layer][1])
+                                            for s in range(stream_steps) for layer in range(w.layers))
+                     / (stream_steps * w.layers)}
     a_bytes = attention_bytes(w, cl, kvb)
     step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
     value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
@@ -863,27 +908,6 @@ def main():
     app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
 
-    # the timed step captured once in a CUDA graph and replayed (launches of
-    # the whole step queued by one call; same kernels, same arguments)
-    graph_steps = max(3, min(args.steps, 20))
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step(fuse=fused, st=torch.cuda.current_stream(device))
-        for _ in range(2):
-            g.replay()
-        tga, tgb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        tga.record(stream)
-        for _ in range(graph_steps):
-            g.replay()
-        tgb.record(stream)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0, "device error word %#x" % int(err.item())
-        graph = {"ms_per_step": tga.elapsed_time(tgb) / graph_steps, "steps": graph_steps,
-                 "what": "the same step captured once in a CUDA graph and replayed"}
-        del g
-    except RuntimeError as e:  # capture refused by this torch / driver: report, keep the stream numbers
-        graph = {"unavailable": str(e).splitlines()[0][:200]}
 
     # ---- end to end: real decode steps from host buffers through the C ABI
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
@@ -959,7 +983,8 @@ def main():
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
-        "cuda_graph": graph,
+        "launch": launch_mode,
+        "stream_launch": stream_launch,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
