@@ -804,30 +804,31 @@ def main():
     # ---- device-timed steps (fixed step replayed; inputs resident). Every
     # step rewrites the same new-token rows, so replays see the same inputs.
     # The timed region is one replay of a CUDA graph that holds the K steps
-    # (the launches a serving loop captures once), with a CUDA event captured
-    # before and after every timed kernel; where this torch cannot record
-    # events inside a graph, the K steps are launched on the stream instead.
+    # (the launches a serving loop captures once and replays). Events between
+    # the kernels would serialise the graph's launches, so per-kernel times
+    # come from separate passes after it: the same steps as a graph with an
+    # event captured around every timed kernel, and launched on the stream.
     def new_events(n, **kw):
         return [[[torch.cuda.Event(enable_timing=True, **kw) for _ in range(2)] for _ in range(w.layers)]
                 for _ in range(n)]
 
+    def capture(n, evs=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream(device)
+            for s in range(n):
+                step(None if evs is None else evs[s], fuse=fused, st=cap)
+        return g
+
     step(fuse=fused)  # first launches (kernel attributes, tensor maps) happen outside any capture
     torch.cuda.synchronize()
-    g_warm = g_timed = None
     try:
-        evs = new_events(args.steps, external=True)
-        g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_warm):
-            step(fuse=fused, st=torch.cuda.current_stream(device))
-        with torch.cuda.graph(g_timed):
-            cap = torch.cuda.current_stream(device)
-            for s in range(args.steps):
-                step(evs[s], fuse=fused, st=cap)
+        g_warm, g_timed = capture(1), capture(args.steps)
         launch_mode = "cuda graph of the K steps, replayed once"
-    except (TypeError, RuntimeError) as e:  # no events inside graphs on this torch
+    except RuntimeError as e:  # capture refused: time stream launches instead
         g_warm = g_timed = None
-        evs = new_events(args.steps)
         launch_mode = "stream launches (%s)" % str(e).splitlines()[0][:120]
+    evs_t = new_events(args.steps) if g_timed is None else None
     for _ in range(args.warmup):
         if g_warm is not None:
             g_warm.replay()
@@ -846,7 +847,7 @@ def main():
         g_timed.replay()
     else:
         for s in range(args.steps):
-            step(evs[s], fuse=fused)
+            step(evs_t[s], fuse=fused)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -854,25 +855,46 @@ def main():
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
     step_ms_local = t_start.elapsed_time(t_end) / args.steps
     step_ms = max_over_ranks(step_ms_local, world, device)
-    kern_ms = [evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(args.steps)
-               for layer in range(w.layers)]
-    kern_avg_ms = sum(kern_ms) / len(kern_ms)
     del g_warm, g_timed
 
-    # the same steps launched one by one on the stream (per-kernel events
-    # between the launches), for comparison with the graph
-    stream_steps = max(3, min(args.steps, 10))
-    evs_s = new_events(stream_steps)
+    def kernel_avg(evs, n):
+        return sum(evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(n)
+                   for layer in range(w.layers)) / (n * w.layers)
+
+    # per-kernel events: the steps as a graph with events around every timed
+    # kernel (where this torch records events inside graphs), and on the stream
+    ev_steps = max(3, min(args.steps, 10))
+    try:
+        evs_g = new_events(ev_steps, external=True)
+        g_ev = capture(ev_steps, evs_g)
+        g_ev.replay()
+        torch.cuda.synchronize()
+        del g_ev
+        graph_events = {"ms_per_timed_kernel": kernel_avg(evs_g, ev_steps), "steps": ev_steps}
+    except (TypeError, RuntimeError) as e:
+        evs_g, graph_events = None, {"unavailable": str(e).splitlines()[0][:120]}
+    evs_s = new_events(ev_steps)
     tsa, tsb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tsa.record(stream)
-    for s in range(stream_steps):
+    for s in range(ev_steps):
         step(evs_s[s], fuse=fused)
     tsb.record(stream)
     torch.cuda.synchronize()
-    stream_launch = {"ms_per_step": tsa.elapsed_time(tsb) / stream_steps, "steps": stream_steps,
-                     "timed_kernel_ms": sum(evs_s[s][layer][0].elapsed_time(evs_s[s][layer][1])
-                                            for s in range(stream_steps) for layer in range(w.layers))
-                     / (stream_steps * w.layers)}
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    stream_launch = {"ms_per_step": tsa.elapsed_time(tsb) / ev_steps, "steps": ev_steps,
+                     "ms_per_timed_kernel": kernel_avg(evs_s, ev_steps)}
+    # the dominant kernel's average launch: the fused step is the only launch
+    # of a layer, so the timed region per launch bounds it from above (gaps
+    # between launches included); otherwise the attention launch's events
+    if evs_t is not None:
+        kern_avg_ms, kern_src = kernel_avg(evs_t, args.steps), "events around each launch in the timed region"
+    elif fused:
+        kern_avg_ms = step_ms / w.layers
+        kern_src = "timed region / launches (one launch per layer; gaps between launches included)"
+    elif evs_g is not None:
+        kern_avg_ms, kern_src = graph_events["ms_per_timed_kernel"], "events around each launch, captured in a graph"
+    else:
+        kern_avg_ms, kern_src = stream_launch["ms_per_timed_kernel"], "events around each stream launch"
     a_bytes = attention_bytes(w, cl, kvb)
     step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
     value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
@@ -883,10 +905,9 @@ def main():
     traffic = recorded_traffic(w.name + ("_fp8" if fp8 else "") + ("_step" if fused else ""))
 
     # append and attention timed separately (the two calls), for the split
-    split_steps = max(3, min(args.steps, 10)) if fused else 0
     if fused:
-        evs2 = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(w.layers)]
-                for _ in range(split_steps)]
+        split_steps = ev_steps
+        evs2 = new_events(split_steps)
         for _ in range(2):
             step()
         t2a, t2b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -897,12 +918,11 @@ def main():
         torch.cuda.synchronize()
         two_call_step_ms = t2a.elapsed_time(t2b) / split_steps
     else:
-        evs2, two_call_step_ms = evs, step_ms
-        split_steps = args.steps
-    attn_ms = [evs2[s][layer][0].elapsed_time(evs2[s][layer][1]) for s in range(split_steps)
-               for layer in range(w.layers)]
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    # append of layer l runs between the end of layer l-1's attention and its own end event
+        split_steps = ev_steps if evs_t is None else args.steps
+        evs2 = evs_t if evs_t is not None else (evs_g if evs_g is not None else evs_s)
+        two_call_step_ms = step_ms
+    attn_avg_ms = kernel_avg(evs2, split_steps)
+    # append of layer l runs between the end of layer l-1's attention and its own start event
     app_ms = [evs2[s][layer - 1][1].elapsed_time(evs2[s][layer][0]) for s in range(split_steps)
               for layer in range(1, w.layers)]
     app_avg_ms = sum(app_ms) / len(app_ms) if app_ms else None
@@ -978,12 +998,14 @@ def main():
                                 "LSE combine), per layer" if fused else
                                 "paged decode attention (split-KV kernel with the LSE combine of cut units fused), "
                                 "per layer"),
-                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": kern_avg_ms},
+                     "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": kern_avg_ms,
+                     "avg_launch_source": kern_src},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
         "launch": launch_mode,
+        "graph_with_kernel_events": graph_events,
         "stream_launch": stream_launch,
         "clocks": clk,
     }
