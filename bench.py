@@ -803,11 +803,12 @@ def main():
 
     # ---- device-timed steps (fixed step replayed; inputs resident). Every
     # step rewrites the same new-token rows, so replays see the same inputs.
-    # The timed region is one replay of a CUDA graph that holds the K steps
-    # (the launches a serving loop captures once and replays). Events between
-    # the kernels would serialise the graph's launches, so per-kernel times
-    # come from separate passes after it: the same steps as a graph with an
-    # event captured around every timed kernel, and launched on the stream.
+    # The timed region replays K times a CUDA graph that holds one step (the
+    # launches a serving loop captures once), with a CUDA event between the
+    # replays (the per-step times give the median). Events between the
+    # kernels would serialise the graph's launches, so per-kernel times come
+    # from separate passes after it: the steps as a graph with an event
+    # captured around every timed kernel, and launched on the stream.
     def new_events(n, **kw):
         return [[[torch.cuda.Event(enable_timing=True, **kw) for _ in range(2)] for _ in range(w.layers)]
                 for _ in range(n)]
@@ -823,39 +824,40 @@ def main():
     step(fuse=fused)  # first launches (kernel attributes, tensor maps) happen outside any capture
     torch.cuda.synchronize()
     try:
-        g_warm, g_timed = capture(1), capture(args.steps)
-        launch_mode = "cuda graph of the K steps, replayed once"
+        g_step = capture(1)
+        launch_mode = "cuda graph of one step, replayed K times"
     except RuntimeError as e:  # capture refused: time stream launches instead
-        g_warm = g_timed = None
+        g_step = None
         launch_mode = "stream launches (%s)" % str(e).splitlines()[0][:120]
-    evs_t = new_events(args.steps) if g_timed is None else None
+    evs_t = new_events(args.steps) if g_step is None else None
     for _ in range(args.warmup):
-        if g_warm is not None:
-            g_warm.replay()
+        if g_step is not None:
+            g_step.replay()
         else:
             step(fuse=fused)
     torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     clocks = ClockSampler(int(vis[local]) if len(vis) > local and vis[local].isdigit() else local)
     clocks.start()
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    t_start.record(stream)
-    if g_timed is not None:
-        g_timed.replay()
-    else:
-        for s in range(args.steps):
+    t_ev[0].record(stream)
+    for s in range(args.steps):
+        if g_step is not None:
+            g_step.replay()
+        else:
             step(evs_t[s], fuse=fused)
-    t_end.record(stream)
+        t_ev[s + 1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
-    step_ms_local = t_start.elapsed_time(t_end) / args.steps
+    step_ms_local = t_ev[0].elapsed_time(t_ev[args.steps]) / args.steps
     step_ms = max_over_ranks(step_ms_local, world, device)
-    del g_warm, g_timed
+    median_step_ms = statistics.median(t_ev[s].elapsed_time(t_ev[s + 1]) for s in range(args.steps))
+    del g_step
 
     def kernel_avg(evs, n):
         return sum(evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(n)
@@ -982,7 +984,8 @@ def main():
         cpu = time_oracle(w)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": median_step_ms,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8e4m3 KV, bf16 q/out" if fp8 else "bf16", "data": "synthetic",
         "config": dict(describe(w), variant=args.variant if not fp8 else "fp8 tensor-core tile",
                        kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16"),
