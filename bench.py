@@ -933,6 +933,11 @@ def main():
 
     # ---- end to end: real decode steps from host buffers through the C ABI
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
+    e2e_warm = min(args.warmup, 2)
+    # each e2e step grows every context by one token: stay within the tables
+    headroom = int(w.max_blocks_per_seq * BLOCK - int(np.max(cl)))
+    e2e_steps = max(1, min(e2e_steps, headroom - e2e_warm))
+    e2e_warm = min(e2e_warm, headroom - e2e_steps)
     ctx_now = cl.copy()
     h_bt = torch.empty((w.B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory()
     h_cl = torch.empty(w.B, dtype=torch.int32).pin_memory()
@@ -962,7 +967,7 @@ def main():
         torch.cuda.synchronize()
         e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy(), kvb) + append_bytes(w, kvb))
 
-    for _ in range(min(args.warmup, 2)):
+    for _ in range(e2e_warm):
         e2e_step()
     e2e_bytes = 0.0
     barrier(world)
