@@ -806,6 +806,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
         // the consumers' unit order: part 0 = [sl, rb), then part 1 = [ra, sl)
         if (cta >= P) return;
         uint16_t* ring = reinterpret_cast<uint16_t*>(base + sp.qring);
+        constexpr int kQW = kMaxG * HD / 4 / 32;   // q words per lane and half row, at most (one per head at d 128)
+        constexpr int kVW = HD / 64;               // v words per lane
+        const int kc = 2 * (lane % (HD / 4));      // this lane's column pair, the same in every head
+        const bool klane = lane < HD / 4;          // lanes that rotate the new k (kc = 2 * lane there)
         int u = 0;
         bool good = true;
         for (int part = 0; good && part < 2; ++part) {
@@ -814,46 +818,67 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
             Cursor cu = locate(p, uc, scan, blockDim.x, ps);
             for (; good && cu.start < pe && cu.b < p.B; cu.next(p), ++u) {
                 const int slot = u & 1;
+                int pos = ctx_clamped(p, cu.b) - 1;
+                if (pos >= p.max_pos) pos = -1;
+                // Every load of the unit is issued at once, ahead of the wait
+                // for its slot: q (this lane's column pair in each head), the
+                // new k and v rows and one cos/sin vector that serves both.
+                uint32_t xl[kQW] = {}, xh[kQW] = {}, vv[kVW] = {}, kl = 0u, kh = 0u;
+                float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (pos >= 0) {
+                    c4 = __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + kc));
+                    const uint16_t* q0 = p.qraw + ((long long)cu.b * p.Hq + (long long)cu.h * p.G) * HD + kc;
+#pragma unroll
+                    for (int i = 0; i < kQW; ++i) {
+                        const int w = lane + 32 * i;
+                        if (w < p.G * HD / 4) {
+                            const uint16_t* qr = q0 + (w / (HD / 4)) * HD;
+                            xl[i] = __ldg(reinterpret_cast<const uint32_t*>(qr));
+                            xh[i] = __ldg(reinterpret_cast<const uint32_t*>(qr + HD / 2));
+                        }
+                    }
+                    const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
+                    if (klane) {
+                        kl = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + kc));
+                        kh = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + kc + HD / 2));
+                    }
+#pragma unroll
+                    for (int j = 0; j < kVW; ++j)
+                        vv[j] = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + 2 * lane + 64 * j));
+                }
                 if (!wait_all_warp(qempty0 + slot * 8, (uint32_t)(((u >> 1) & 1) ^ 1))) {
                     if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                     good = false;
                     break;
                 }
-                int pos = ctx_clamped(p, cu.b) - 1;
-                if (pos >= p.max_pos) pos = -1;
                 uint16_t* qrows = ring + slot * (p.G + 2) * HD;
                 uint16_t* krow = qrows + p.G * HD;
                 uint16_t* vrow = krow + HD;
-                for (int w = lane; w < p.G * HD / 4; w += 32) {
-                    const int g = w / (HD / 4), k = (w % (HD / 4)) * 2;
-                    uint32_t yl = 0u, yh = 0u;
-                    if (pos >= 0) {
-                        const uint16_t* qr = p.qraw + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + g) * HD;
-                        const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(qr + k));
-                        const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(qr + k + HD / 2));
-                        const float4 c4 = __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + k));
-                        rotate_word(xl, xh, c4, yl, yh);
+#pragma unroll
+                for (int i = 0; i < kQW; ++i) {
+                    const int w = lane + 32 * i;
+                    if (w < p.G * HD / 4) {
+                        uint32_t yl = 0u, yh = 0u;
+                        if (pos >= 0) rotate_word(xl[i], xh[i], c4, yl, yh);
+                        uint16_t* qd = qrows + (w / (HD / 4)) * HD + kc;
+                        *reinterpret_cast<uint32_t*>(qd) = yl;
+                        *reinterpret_cast<uint32_t*>(qd + HD / 2) = yh;
                     }
-                    *reinterpret_cast<uint32_t*>(qrows + g * HD + k) = yl;
-                    *reinterpret_cast<uint32_t*>(qrows + g * HD + k + HD / 2) = yh;
                 }
                 // q first: the consumers need it where the unit starts, the
                 // new token's rows only at its last block
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qfull0 + slot * 8);
                 if (pos >= 0) {
-                    const long long nofs = ((long long)cu.b * p.Hkv + cu.h) * HD;
-                    for (int k = 2 * lane; k < HD / 2; k += 64) {
-                        const uint32_t xl = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + k));
-                        const uint32_t xh = __ldg(reinterpret_cast<const uint32_t*>(p.knew + nofs + k + HD / 2));
-                        const float4 c4 = __ldg(reinterpret_cast<const float4*>(p.rope + (long long)pos * (HD / 2) + k));
+                    if (klane) {
                         uint32_t yl, yh;
-                        rotate_word(xl, xh, c4, yl, yh);
-                        *reinterpret_cast<uint32_t*>(krow + k) = yl;
-                        *reinterpret_cast<uint32_t*>(krow + k + HD / 2) = yh;
+                        rotate_word(kl, kh, c4, yl, yh);
+                        *reinterpret_cast<uint32_t*>(krow + kc) = yl;
+                        *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = yh;
                     }
-                    for (int k = 2 * lane; k < HD; k += 64)
-                        *reinterpret_cast<uint32_t*>(vrow + k) = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + k));
+#pragma unroll
+                    for (int j = 0; j < kVW; ++j)
+                        *reinterpret_cast<uint32_t*>(vrow + 2 * lane + 64 * j) = vv[j];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(kvfull0 + slot * 8);
