@@ -222,9 +222,9 @@ def oracle_sample(w, nthreads, rank_seed=0):
     table = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
     pos = (cl - 1).astype(np.int32)
 
-    def run():
+    def run(nt=nthreads):
         q_out, _ = oracle.append(q, k, v, pos, sl, table, kc, vc)
-        oracle.paged_attention(q_out, kc, vc, bt, cl, w.scale, nthreads=nthreads)
+        oracle.paged_attention(q_out, kc, vc, bt, cl, w.scale, nthreads=nt)
         return oracle.paged_attention.threads_used
 
     return run, attention_bytes(w, cl) + append_bytes(w)
@@ -240,10 +240,15 @@ def time_oracle(w, budget_s=12.0):
         run()
         n += 1
     dt = (time.perf_counter() - t0) / n
+    # the same layer on one thread (rows are independent, so the threads do
+    # not change the results, only the time)
+    t1 = time.perf_counter()
+    run(1)
+    dt1 = time.perf_counter() - t1
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": int(used), "kind": "oracle",
             "sample": f"one layer of the step (append + attention, all {w.B} requests, {w.Hq} heads), "
                       f"repeated {n}x, fp64 C on {used} POSIX threads; seconds per layer {dt:.3f}",
-            "s_per_layer": dt}
+            "s_per_layer": dt, "single_thread": {"s_per_layer": dt1, "value": nbytes / dt1 / 1e9}}
 
 
 def prefill_oracle_sample(w, nthreads, rows_per_request=2):
