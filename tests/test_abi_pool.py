@@ -158,6 +158,30 @@ def test_device_entry_points_reject_bad_args_without_a_gpu(mi):
                                  stream=0) == mi.MI_OK
 
 
+def test_step_rejects_bad_args_without_a_gpu(mi):
+    """mi_paged_decode_step refuses bad arguments before any CUDA call: the
+    addresses below are never dereferenced."""
+    d = mi.dims(2, 4, 2, 64, 8, 4)
+    a = {n: (i + 1) << 20 for i, n in enumerate(("q", "k", "v", "rope", "bt", "cl", "qo", "kc", "vc", "out", "ws"))}
+
+    def step(dims=d, max_pos=64, **over):
+        x = dict(a, **over)
+        return mi.mi_paged_decode_step(dims, x["q"], x["k"], x["v"], x["rope"], max_pos, x["bt"], x["cl"], 0.125,
+                                       x["qo"], x["kc"], x["vc"], x["out"], x["ws"], workspace_bytes=1 << 20,
+                                       stream=0)
+    assert step(dims=mi.dims(2, 4, 3, 64, 8, 4)) == mi.MI_ERR_UNSUPPORTED  # Hq % Hkv != 0
+    for name in ("q", "k", "v", "rope", "bt", "cl", "qo", "kc", "vc", "out", "ws"):
+        assert step(**{name: None}) == mi.MI_ERR_INVALID_ARG, name
+    for name in ("q", "k", "v", "rope", "qo", "kc", "vc", "out", "ws"):
+        assert step(**{name: a[name] + 8}) == mi.MI_ERR_INVALID_ARG, name  # not 16-byte aligned
+    assert step(max_pos=0) == mi.MI_ERR_INVALID_ARG
+    # q and q_out overlap (any shared byte of the B x Hq x d bf16 rows)
+    assert step(qo=a["q"] + 16) == mi.MI_ERR_INVALID_ARG
+    assert step(qo=a["q"] - 2 * 4 * 64 * 2 + 16) == mi.MI_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    assert step(dims=mi.dims(0, 4, 2, 64, 8, 4)) == mi.MI_OK
+
+
 def test_token_slots_match_model_after_churn(mi):
     from workloads import PREFILL_WORKLOADS, prefill_setup_pool
     w = WORKLOADS["qwen3_8b"]
