@@ -182,6 +182,28 @@ def test_step_rejects_bad_args_without_a_gpu(mi):
     assert step(dims=mi.dims(0, 4, 2, 64, 8, 4)) == mi.MI_OK
 
 
+def test_fp8_entry_points_reject_bad_args_without_a_gpu(mi):
+    """The e4m3 append and attention refuse missing scales, misaligned
+    buffers and unsupported shapes before any CUDA call."""
+    d = mi.dims(2, 4, 2, 64, 8, 4)
+    A = 1 << 20
+
+    def app(dims=d, ks=9 * A, vs=10 * A, kc=7 * A):
+        return mi.mi_paged_kv_append_fp8(dims, A, 2 * A, 3 * A, 4 * A, 5 * A, 6 * A, 64, 11 * A, kc, 8 * A, ks, vs,
+                                          stream=0)
+
+    def att(dims=d, ks=9 * A, vs=10 * A, kc=7 * A):
+        return mi.mi_paged_decode_attention_fp8(dims, A, kc, 8 * A, ks, vs, 4 * A, 5 * A, 0.125, 11 * A, 12 * A,
+                                                workspace_bytes=1 << 20, stream=0)
+    for call in (app, att):
+        assert call(ks=None) == mi.MI_ERR_INVALID_ARG
+        assert call(vs=None) == mi.MI_ERR_INVALID_ARG
+        assert call(kc=7 * A + 8) == mi.MI_ERR_INVALID_ARG
+        assert call(dims=mi.dims(2, 4, 3, 64, 8, 4)) == mi.MI_ERR_UNSUPPORTED
+        assert call(dims=mi.dims(0, 4, 2, 64, 8, 4)) == mi.MI_OK
+    assert app(dims=mi.dims(2, 4, 2, 96, 8, 4)) == mi.MI_ERR_UNSUPPORTED
+
+
 def test_token_slots_match_model_after_churn(mi):
     from workloads import PREFILL_WORKLOADS, prefill_setup_pool
     w = WORKLOADS["qwen3_8b"]
