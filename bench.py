@@ -101,6 +101,14 @@ def describe(w):
             "parallelism": "replicas"}
 
 
+def arm_config(w, args):
+    """The `config` object of a decode line; the GPU arm and the reference
+    arm print the same one."""
+    fp8 = args.kv == "fp8"
+    return dict(describe(w), variant=args.variant if not fp8 else "fp8 tensor-core tile",
+                kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16")
+
+
 def measured_peak(key="hbm_gbs"):
     fallback = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
@@ -291,9 +299,306 @@ def prefill_oracle_sample(w, nthreads, rows_per_request=2):
     return run, flops, len(rows)
 
 
+# ----------------------------------------------------- the other configs ----
+
+def l2_flush_buffer(device):
+    """A device buffer of twice the L2 size: writing it evicts whatever a step
+    left in L2, so the next step starts cold."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)) or (129 << 20)
+    return torch.empty(2 * l2 // 4, dtype=torch.float32, device=device)
+
+
+def _median_event_ms(fn, stream, reps, warm, flush=None):
+    """Median device time of fn() over `reps` runs after `warm` untimed ones,
+    events on `stream` around each run; with `flush`, the buffer is written
+    before every run, outside the events."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def _time_oracle_layer(run, budget_s):
+    """Runs the oracle sample `run` (returns the threads it used) until
+    budget_s has passed (at least once); returns (seconds per run, runs, threads)."""
+    t0 = time.perf_counter()
+    used = run()
+    n = 1
+    while time.perf_counter() - t0 < budget_s and n < 20:
+        run()
+        n += 1
+    return (time.perf_counter() - t0) / n, n, int(used)
+
+
+def measure_one_layer_config(mi, device, stream, w, peak, flush, reps, warm, oracle_budget_s):
+    """One decode layer of workload w (pool history, one appended token per
+    request): the fused step and the two calls (append, attention), each the
+    median of `reps` event-timed launches; with `flush`, L2 is flushed before
+    every launch. The oracle's append + attention of the same layer is timed on
+    the host cores over the same blocks (copied back from the device)."""
+    import torch
+    import oracle
+    ctx = context_lengths(w)
+    pool = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+    setup_pool(w, pool, ctx)
+    for b in range(w.B):
+        mi.check(pool.alloc(b, int(ctx[b]) + 1), "alloc")
+    bt, cl, sl = pool.batch_meta(range(w.B))
+    pos = (cl - 1).astype(np.int32)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    device_fill_cache(w, 0, kc, vc)
+    q, k, v = new_token_values(w, 0)
+    u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
+    q_d, k_d, v_d = u16(q), u16(k), u16(v)
+    qo_d, out_d = torch.empty_like(q_d), torch.empty_like(q_d)
+    bt_d, cl_d, sl_d, pos_d = i32(bt), i32(cl), i32(sl), i32(pos)
+    st, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    mi.check(st, "rope table")
+    rope = torch.from_numpy(table).to(device)
+    ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def fused():
+        mi.check(mi.mi_paged_decode_step(d, q_d, k_d, v_d, rope, w.max_pos, bt_d, cl_d, w.scale, qo_d, kc, vc,
+                                         out_d, ws, dev_err=err, stream=stream), "decode step")
+
+    def two_calls():
+        mi.check(mi.mi_paged_kv_append(d, q_d, k_d, v_d, pos_d, sl_d, rope, w.max_pos, qo_d, kc, vc, err, stream),
+                 "append")
+        mi.check(mi.mi_paged_decode_attention(d, qo_d, kc, vc, bt_d, cl_d, w.scale, out_d, ws, dev_err=err,
+                                              stream=stream), "attention")
+
+    t_fused = _median_event_ms(fused, stream, reps, warm, flush)
+    t_two = _median_event_ms(two_calls, stream, reps, warm, flush)
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    nbytes = attention_bytes(w, cl) + append_bytes(w)
+    gbs = nbytes / (t_fused * 1e-3) / 1e9
+    rec = {"workload": w.name, "layers": 1, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.head_dim,
+           "path": "fused step (mi_paged_decode_step)", "median_ms": t_fused, "steps_per_s": 1e3 / t_fused,
+           "gbs": gbs, "frac": gbs / peak, "algorithmic_bytes_per_step": nbytes,
+           "two_calls": {"median_ms": t_two, "gbs": nbytes / (t_two * 1e-3) / 1e9},
+           "launches_per_step": 1, "reps": reps,
+           "l2": ("flushed before every step (2x L2 written), flush outside the events; launch-bound: the "
+                  "step's bytes fit in L2 and take a few microseconds at HBM speed")
+           if flush is not None else "no flush: the layer's K/V are larger than L2"}
+    # the oracle on the host cores: the same layer over the same blocks
+    kc_s, vc_s, bt_s, _ = gather_blocks_to_host(kc, vc, bt, cl)
+    table_ref = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    sl_s = oracle.slot_mapping(bt_s, pos)
+    nthreads = os.cpu_count() or 1
+
+    def run():
+        q_ref, _ = oracle.append(q, k, v, pos, sl_s, table_ref, kc_s, vc_s)
+        oracle.paged_attention(q_ref, kc_s, vc_s, bt_s, cl, w.scale, nthreads=nthreads)
+        return oracle.paged_attention.threads_used
+
+    dt, n, used = _time_oracle_layer(run, oracle_budget_s)
+    rec["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+                           "sample": f"the whole layer (append + attention, all {w.B} requests, {w.Hq} heads), "
+                                     f"fp64 C, repeated {n}x; seconds per layer {dt:.4f}"}
+    return rec
+
+
+def measure_sweep_config(mi, device, stream, w, peak, flush, oracle_budget_s):
+    """The decode sweep of workload w: from a history of ctx tokens per
+    request, w.sweep_steps decode steps over w.layers layers. Each step grows
+    the host pool by one token per request, builds the block tables and
+    lengths (mi_kv_pool_batch_meta) into pinned buffers, copies them and the
+    new q/k/v of every layer to the device, and replays a CUDA graph of the
+    layers' fused steps. Timed twice: with L2 flushed before every step (the
+    flush outside each step's events; steps/s = steps / the summed step
+    times) and back to back without a flush (steps / the whole sweep)."""
+    import torch
+    import oracle
+    from oracle.pool import PoolModel
+    ctx = context_lengths(w)
+    B, L, S = w.B, w.layers, w.sweep_steps
+    seqs = list(range(B))
+    d = mi.dims(B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    caches = []
+    for layer in range(L):
+        kc = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        vc = torch.empty_like(kc)
+        device_fill_cache(w, layer, kc, vc)
+        caches.append((kc, vc))
+    st, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    mi.check(st, "rope table")
+    rope = torch.from_numpy(table).to(device)
+    u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    vals = [new_token_values(w, layer) for layer in range(L)]
+    h_q = torch.stack([u16(x[0]) for x in vals]).pin_memory()
+    h_k = torch.stack([u16(x[1]) for x in vals]).pin_memory()
+    h_v = torch.stack([u16(x[2]) for x in vals]).pin_memory()
+    q_all, k_all, v_all = h_q.to(device), h_k.to(device), h_v.to(device)
+    qo_all, out_all = torch.empty_like(q_all), torch.empty_like(q_all)
+    bt_d = torch.empty((B, w.max_blocks_per_seq), dtype=torch.int32, device=device)
+    cl_d = torch.empty(B, dtype=torch.int32, device=device)
+    # two sets of pinned metadata buffers, each reused only once the copies
+    # out of it have run (an event per set)
+    meta = [(torch.empty((B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory(),
+             torch.empty(B, dtype=torch.int32).pin_memory(), np.empty(B, np.int32), torch.cuda.Event())
+            for _ in range(2)]
+    ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def layers(st_):
+        for layer in range(L):
+            kc, vc = caches[layer]
+            mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, w.max_pos, bt_d,
+                                             cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
+                                             dev_err=err, stream=st_), "decode step")
+
+    def host_step(pool, s, buf):
+        h_bt, h_cl, h_sl, ev = meta[buf]
+        ev.synchronize()  # the copies out of this set (two steps ago) have run
+        for b in seqs:
+            mi.check(pool.alloc(b, int(ctx[b]) + s + 1), "alloc")
+        st_, _, _, _ = mi.mi_kv_pool_batch_meta(pool.handle, seqs, w.max_blocks_per_seq, h_bt.numpy(),
+                                                h_cl.numpy(), h_sl)
+        mi.check(st_, "batch_meta")
+        bt_d.copy_(h_bt, non_blocking=True)
+        cl_d.copy_(h_cl, non_blocking=True)
+        ev.record(stream)
+        q_all.copy_(h_q, non_blocking=True)
+        k_all.copy_(h_k, non_blocking=True)
+        v_all.copy_(h_v, non_blocking=True)
+        return L * (attention_bytes(w, h_cl.numpy()) + append_bytes(w))
+
+    def fresh_pool():
+        pool = mi.Pool(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+        setup_pool(w, pool, ctx)
+        return pool
+
+    # first step eagerly (kernel attributes, tensor maps), then capture the layers
+    pool = fresh_pool()
+    host_step(pool, 0, 0)
+    layers(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layers(torch.cuda.current_stream(device))
+    torch.cuda.synchronize()
+
+    def sweep(flushed):
+        pool = fresh_pool()
+        nbytes = 0
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(S)]
+        for s in range(S):
+            if flushed:
+                flush.zero_()
+            evs[s][0].record(stream)
+            nbytes += host_step(pool, s, s & 1)
+            g.replay()
+            evs[s][1].record(stream)
+        torch.cuda.synchronize()
+        per = [e0.elapsed_time(e1) for e0, e1 in evs]
+        return nbytes, sum(per), evs[0][0].elapsed_time(evs[-1][1])
+
+    sweep(True)  # warm-up sweep
+    runs = [sweep(True) for _ in range(3)]
+    warm_runs = [sweep(False) for _ in range(3)]
+    assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    nbytes = runs[0][0]
+    t_flushed = statistics.median(r[1] for r in runs)
+    t_warm = statistics.median(r[2] for r in warm_runs)
+    gbs = nbytes / (t_flushed * 1e-3) / 1e9
+    rec = {"workload": w.name, "layers": L, "batch": B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.head_dim,
+           "sweep_steps": S, "contexts": f"{int(ctx[0]) + 1} -> {int(ctx[0]) + S} tokens per request",
+           "path": ("per step: host pool growth + mi_kv_pool_batch_meta, H2D of tables, lengths and every "
+                    "layer's new q/k/v from pinned memory, then a CUDA graph of the layers' fused steps"),
+           "sweep_ms": t_flushed, "steps_per_s": S / (t_flushed * 1e-3), "median_ms": t_flushed / S,
+           "gbs": gbs, "frac": gbs / peak, "algorithmic_bytes_per_sweep": nbytes,
+           "l2_warm": {"sweep_ms": t_warm, "steps_per_s": S / (t_warm * 1e-3),
+                       "note": "steps back to back without a flush: a step's K/V (about 91 MB) stay in L2"},
+           "launches_per_step": L, "sweeps_timed": len(runs),
+           "l2": ("flushed before every step (2x L2 written), flush outside the step's events; launch-bound: "
+                  "each layer's K/V is a few MB")}
+    # the oracle on the host cores: layer 0 followed through the whole sweep
+    # (its own pool model, append and attention), extrapolated to all layers
+    kc_h = caches[0][0].view(torch.int16).cpu().numpy().view(np.uint16).copy()
+    vc_h = caches[0][1].view(torch.int16).cpu().numpy().view(np.uint16).copy()
+    q0, k0, v0 = vals[0]
+    table_ref = oracle.rope_table(w.theta, w.head_dim, w.max_pos)
+    nthreads = os.cpu_count() or 1
+
+    def run():
+        model = PoolModel(w.num_blocks, w.max_seqs, w.max_blocks_per_seq, initial_free_order(w))
+        setup_pool(w, model, ctx)
+        for s in range(S):
+            for b in seqs:
+                assert model.alloc(b, int(ctx[b]) + s + 1) == 0
+            bt_m, cl_m, sl_m = model.batch_meta(seqs)
+            q_ref, _ = oracle.append(q0, k0, v0, (cl_m - 1).astype(np.int32), sl_m, table_ref, kc_h, vc_h)
+            oracle.paged_attention(q_ref, kc_h, vc_h, bt_m, cl_m, w.scale, nthreads=nthreads)
+        return oracle.paged_attention.threads_used
+
+    dt, n, used = _time_oracle_layer(run, oracle_budget_s)
+    rec["cpu_baseline"] = {"value": S / (dt * L), "unit": "steps/s", "cores": used, "kind": "oracle",
+                           "gbs": nbytes / (dt * L) / 1e9, "extrapolated": True,
+                           "sample": f"layer 0 through all {S} steps (pool model, append, attention), fp64 C, "
+                                     f"repeated {n}x, {dt:.3f} s per pass; x{L} layers for a sweep"}
+    return rec
+
+
+def gather_blocks_to_host(kc_d, vc_d, bt, cl):
+    """Host copies of the blocks the requests use, renumbered 0..n-1, with
+    their tables rewritten to the new numbers (data movement only)."""
+    import torch
+    live = [bt[b, :-(-max(int(cl[b]), 0) // BLOCK)] for b in range(len(cl))]
+    used = sorted({int(x) for row in live for x in row})
+    remap = np.full(max(used) + 1, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    idx = torch.tensor(used, dtype=torch.int64, device=kc_d.device)
+    kc = kc_d[idx].view(torch.int16).cpu().numpy().view(np.uint16)
+    vc = vc_d[idx].view(torch.int16).cpu().numpy().view(np.uint16)
+    bt_s = np.full(bt.shape, -1, np.int32)
+    for i, row in enumerate(live):
+        bt_s[i, :len(row)] = remap[row]
+    return kc, vc, bt_s, used
+
+
+def measure_configs(mi, device, peak, oracle_budget_s=3.0):
+    """The workloads other than the headline, one GPU: the Qwen3-1.7B-shaped
+    layer and the Qwen2.5-7B-shaped 128-step sweep (both L2-flushed before
+    every step), and the skewed batch of one 32k and 255 short contexts."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    flush = l2_flush_buffer(device)
+    out = {}
+    out["qwen3_1p7b"] = measure_one_layer_config(mi, device, stream, WORKLOADS["qwen3_1p7b"], peak, flush,
+                                                 reps=50, warm=5, oracle_budget_s=oracle_budget_s)
+    out["qwen25_7b_sweep"] = measure_sweep_config(mi, device, stream, WORKLOADS["qwen25_7b_sweep"], peak, flush,
+                                                  oracle_budget_s=oracle_budget_s)
+    del flush
+    torch.cuda.empty_cache()
+    out["skewed"] = measure_one_layer_config(mi, device, stream, WORKLOADS["skewed"], peak, None,
+                                             reps=50, warm=5, oracle_budget_s=oracle_budget_s)
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ reference ----
 
 def run_reference(args, w, rank, world):
+    """The reference arm: the oracle as it stands, on the host cores, one
+    layer of the step (append + attention, every request and head) per timed
+    step; ms_per_step is that layer's time x the step's layers (an
+    extrapolation, said so in the line)."""
     if rank != 0:
         return
     nthreads = os.cpu_count() or 1
@@ -306,12 +611,15 @@ def run_reference(args, w, rank, world):
         used = run()
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     val = nbytes / dt / 1e9
+    sample = (f"one of the {w.layers} layers per step (append + attention, all {w.B} requests, {w.Hq} heads), "
+              f"fp64 C; the step time is {w.layers} x the layer's")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 * w.layers,
+            "extrapolated": True, "ms_per_layer": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(describe(w), sample="one of the 36 layers per step (append + attention)"),
-            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": int(used), "kind": "oracle",
-                             "sample": "one layer per step: append + attention, all requests and heads"},
+            "config": arm_config(w, args),
+            "steps_per_s": 1.0 / (dt * w.layers),
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": int(used), "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -691,6 +999,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default: the workload's); fewer only for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' records (Qwen3-1.7B layer, Qwen2.5-7B sweep, skewed batch)")
     args = ap.parse_args()
     assert args.warmup >= 0 and args.steps >= 1
     rank, world, local = dist_setup(args)
@@ -862,7 +1172,6 @@ def main():
     step_ms_local = t_ev[0].elapsed_time(t_ev[args.steps]) / args.steps
     step_ms = max_over_ranks(step_ms_local, world, device)
     median_step_ms = statistics.median(t_ev[s].elapsed_time(t_ev[s + 1]) for s in range(args.steps))
-    del g_step
 
     def kernel_avg(evs, n):
         return sum(evs[s][layer][0].elapsed_time(evs[s][layer][1]) for s in range(n)
@@ -967,7 +1276,12 @@ def main():
             ((h_q, q_all), (h_k, k_all), (h_v, v_all))
         for src, dst in copies:
             dst.copy_(src, non_blocking=True)
-        step(fuse=fused)
+        # the same captured one-step graph as the timed region (it reads the
+        # tables, lengths and new rows from the device buffers just copied)
+        if g_step is not None:
+            g_step.replay()
+        else:
+            step(fuse=fused)
         h_out.copy_(out_all, non_blocking=True)
         torch.cuda.synchronize()
         e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy(), kvb) + append_bytes(w, kvb))
@@ -981,6 +1295,7 @@ def main():
         e2e_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    del g_step
     h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_cl, h_q, h_k, h_v)) + \
         (0 if fused else sum(t.numel() * t.element_size() for t in (h_sl, h_pos)))
     d2h = h_out.numel() * h_out.element_size()
@@ -992,13 +1307,15 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = time_oracle(w)
+    per_config = None
+    if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_config:
+        per_config = measure_configs(mi, device, peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": median_step_ms,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8e4m3 KV, bf16 q/out" if fp8 else "bf16", "data": "synthetic",
-        "config": dict(describe(w), variant=args.variant if not fp8 else "fp8 tensor-core tile",
-                       kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16"),
+        "config": arm_config(w, args),
         "steps_per_s": 1e3 / step_ms * world,
         "hbm_frac_step": value / world / peak,
         "per_layer_ms": {"step": step_ms / w.layers, "fused_step_kernel": kern_avg_ms if fused else None,
@@ -1015,7 +1332,11 @@ def main():
                      "avg_launch_source": kern_src},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
+                "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3,
+                "path": ("per step: host pool growth and mi_kv_pool_batch_meta, H2D from pinned memory, "
+                         + ("the timed region's one-step CUDA graph" if launch_mode.startswith("cuda graph")
+                            else "stream launches") + ", D2H of every layer's output, synchronise")},
+        "per_config": per_config,
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
         "launch": launch_mode,
         "graph_with_kernel_events": graph_events,

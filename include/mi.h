@@ -263,8 +263,8 @@ size_t mi_paged_decode_workspace_bytes(const mi_dims* dims);
  * cache. The call may be captured in a CUDA graph and the graph replayed any
  * number of times over the same workspace (each launch hands back its merge
  * counters zeroed); after a launch that set MI_DEVERR_TIMEOUT, zero the
- * workspace before the next replay. The same holds for the e4m3, fused
- * step and no-allocation variants below. */
+ * workspace before the next replay. The same holds for the e4m3 and fused
+ * step variants below. */
 mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* block_tables,
                                     const int32_t* context_lens, float scale, void* out,
@@ -428,10 +428,14 @@ mi_status mi_kv_copy_blocks(const mi_dims* dims, const void* src_k, const void* 
  * MI_NOALLOC_SCRATCH_BYTES), before anything is queued.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. Every call on a device shares the one array and
- * it keeps the last call's contents (nothing in it needs to start at zero):
- * calls whose work overlaps on the GPU (other streams, other threads) race on
- * it, so order them, e.g. on one stream. */
+ * before any stream capture. The address is looked up again when the
+ * device's context has changed (after a device reset, which also clears the
+ * array). Every call on a device shares the one array and it keeps the last
+ * call's contents; nothing in it needs to start at zero: each call tags the
+ * merge counters it writes with its own epoch, so a counter left half-counted
+ * by an earlier call (one that set MI_DEVERR_TIMEOUT) is ignored by the next.
+ * Calls whose work overlaps on the GPU (other streams, other threads) race on
+ * the array, so order them, e.g. on one stream. */
 mi_status mi_paged_decode_attention_noalloc(const mi_dims* dims, const void* q,
                                             const void* k_cache, const void* v_cache,
                                             const int32_t* block_tables,

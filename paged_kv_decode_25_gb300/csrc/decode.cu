@@ -1247,14 +1247,16 @@ KernelFn pick_kernel(int HD, int var, int G) {
 
 struct GridKey {
     int dev;
+    CUcontext ctx;
     KernelFn fn;
     int smem;
 };
 
 // Persistent grid: SMs x resident CTAs of this kernel at this smem size.
-// The first query for a (device, kernel) raises the kernel's dynamic
+// The first query for a (device, context, kernel) raises the kernel's dynamic
 // shared-memory limit to the largest plan any shape uses, so a launch never
-// depends on which shape was seen last; the grid is cached per smem size.
+// depends on which shape was seen last; the grid is cached per smem size. A
+// new context on the device (after a device reset) starts afresh.
 int grid_for(KernelFn fn, int smem, int threads = (kWarps + 1) * 32) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1263,11 +1265,14 @@ int grid_for(KernelFn fn, int smem, int threads = (kWarps + 1) * 32) {
     static int vals[128];
     static int nkeys = 0;
     std::lock_guard<std::mutex> lk(mu);
+    const CUcontext ctx0 = current_context();
     for (int i = 0; i < nkeys; ++i)
-        if (keys[i].dev == dev && keys[i].fn == fn && keys[i].smem == smem) return vals[i];
+        if (ctx0 && keys[i].dev == dev && keys[i].ctx == ctx0 && keys[i].fn == fn && keys[i].smem == smem)
+            return vals[i];
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemLimit) != cudaSuccess)
         return 0;
+    const CUcontext ctx = current_context();  // made current by the call above if it was not yet
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     int occ = 0;
@@ -1275,10 +1280,13 @@ int grid_for(KernelFn fn, int smem, int threads = (kWarps + 1) * 32) {
         cudaSuccess)
         return 0;
     const int g = sms * (occ > 0 ? occ : 1);
-    if (nkeys < 128) {
-        keys[nkeys] = GridKey{dev, fn, smem};
-        vals[nkeys] = g;
-        ++nkeys;
+    int slot = -1;
+    for (int i = 0; i < nkeys && slot < 0; ++i)
+        if (keys[i].dev == dev && keys[i].fn == fn && keys[i].smem == smem) slot = i;  // a stale context's entry
+    if (slot < 0 && nkeys < 128) slot = nkeys++;
+    if (slot >= 0 && ctx) {
+        keys[slot] = GridKey{dev, ctx, fn, smem};
+        vals[slot] = g;
     }
     return g;
 }

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "mi.h"
+#include "tma.cuh"
 
 namespace {
 
@@ -22,25 +23,30 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MI_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 256;
 
-// Device address of the array, looked up once per device with that device
-// current. In host code `g_noalloc_scratch` names a host-side stand-in, never
-// the device memory, so only the looked-up address is passed on.
+// Device address of the array, looked up with the device current on the
+// first call there and again whenever the device's context has changed (a
+// device reset gives the array a new address). In host code
+// `g_noalloc_scratch` names a host-side stand-in, never the device memory,
+// so only the looked-up address is passed on.
 void* scratch_on_current_device(mi_status* st) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static CUcontext ctx_of[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *st = MI_ERR_CUDA;
         return nullptr;
     }
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    const CUcontext ctx = mi::current_context();
+    if (!addr[dev] || !ctx || ctx != ctx_of[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             *st = MI_ERR_CUDA;
             return nullptr;
         }
         addr[dev] = p;
+        ctx_of[dev] = mi::current_context();  // current now, if it was not before the lookup
     }
     *st = MI_OK;
     return addr[dev];

@@ -844,38 +844,32 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-template <int HD>
-bool prepare_tc() {
-    static std::mutex mu;
-    static bool done[256] = {};
+// Raise a kernel's dynamic shared-memory limit once per device and context
+// (a device reset makes a new context, which needs it again).
+bool raise_smem_once(const void* fn, int smem, CUcontext* done, std::mutex& mu) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return false;
     std::lock_guard<std::mutex> lk(mu);
-    if (!done[dev]) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(prefill_tc_kernel<HD>),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<HD>::kTotal) != cudaSuccess)
-            return false;
-        done[dev] = true;
-    }
+    const CUcontext ctx0 = current_context();
+    if (ctx0 && done[dev] == ctx0) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+    done[dev] = current_context();
     return true;
 }
 
 template <int HD>
-bool prepare(int* smem) {
-    // raise the kernel's dynamic shared-memory limit once per device
+bool prepare_tc() {
     static std::mutex mu;
-    static bool done[256] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return false;
+    static CUcontext done[256] = {};
+    return raise_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<HD>), TcSmem<HD>::kTotal, done, mu);
+}
+
+template <int HD>
+bool prepare(int* smem) {
+    static std::mutex mu;
+    static CUcontext done[256] = {};
     *smem = PrefillSmem<HD>::kTotal;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!done[dev]) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(prefill_kernel<HD>),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, *smem) != cudaSuccess)
-            return false;
-        done[dev] = true;
-    }
-    return true;
+    return raise_smem_once(reinterpret_cast<const void*>(prefill_kernel<HD>), *smem, done, mu);
 }
 
 }  // namespace

@@ -50,6 +50,26 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// The calling thread's current CUDA context (cuCtxGetCurrent through the
+// runtime's driver entry point), or nullptr when there is none yet. Caches of
+// per-device set-up (kernel attributes, symbol addresses) are keyed by it: a
+// device reset makes a new context, and the set-up is then done again.
+inline CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult qr;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
 // 2-D map over a cache viewed as 128-byte lines: [rows * HD/64][64] bf16,
 // box = one 16-token tile (16 * HD/64 lines x 64 columns), 128-byte swizzle.
 // `rows` counts token rows of all blocks and KV heads (num_blocks * Hkv * 16).

@@ -60,3 +60,21 @@ def assert_attention_close(gpu_bits, ref, what=""):
     assert np.all(np.isfinite(oracle.bf16_to_f64(gpu_bits))), what
     assert mx <= MAX_ABS_TOL and mean <= MEAN_ABS_TOL, f"{what}: max {mx:.3e} mean {mean:.3e}"
     return mx, mean
+
+
+def gather_used_blocks(kc_d, vc_d, bt, cl, rows=None):
+    """Host copies of the cache blocks that requests `rows` (default: all) use
+    within their first ceil(cl/16) table entries, renumbered 0..n-1, and their
+    tables rewritten to the new numbers (-1 elsewhere). Only moves data: the
+    oracle, not this helper, computes results over it."""
+    import torch
+    rows = list(range(len(cl))) if rows is None else list(rows)
+    live = [bt[b, :-(-max(int(cl[b]), 0) // 16)] for b in rows]
+    used = sorted({int(x) for row in live for x in row})
+    remap = {blk: i for i, blk in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.int64, device=kc_d.device)
+    kc, vc = from_dev_u16(kc_d[idx]), from_dev_u16(vc_d[idx])
+    bt_s = np.full((len(rows), bt.shape[1]), -1, np.int32)
+    for i, row in enumerate(live):
+        bt_s[i, :len(row)] = [remap[int(x)] for x in row]
+    return kc, vc, bt_s, used

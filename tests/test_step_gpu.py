@@ -3,14 +3,16 @@ layer: its q_out, the new cache rows and the attention output carry the same
 bits as mi_paged_kv_append followed by mi_paged_decode_attention (both pinned
 to the oracle elsewhere), and the output is within the attention tolerance of
 the fp64 oracle's append + attention. Covered: the small workloads in full,
-the Qwen3-8B-shaped serving layer at full size, edge context lengths, head
+the Qwen3-8B-shaped serving layer at full size (every request and head
+against the oracle), edge context lengths, head
 dims 64 and 128 and several GQA groups, NaN in unused cache rows, a position
 past the RoPE table, and the overlap check on q / q_out."""
 import numpy as np
 import pytest
 
 import oracle
-from helpers import assert_attention_close, from_dev_u16, grow, pools_for, to_dev_i32, to_dev_u16
+from helpers import (assert_attention_close, from_dev_u16, gather_used_blocks, grow, pools_for, to_dev_i32,
+                     to_dev_u16)
 from workloads import BLOCK, WORKLOADS, bf16_normal, device_fill_cache, history_cache, new_token_values
 
 pytestmark = pytest.mark.gpu
@@ -85,8 +87,12 @@ def test_step_matches_two_calls_and_oracle(cuda_device, name):
 
 def test_step_full_size_serving_layer(cuda_device):
     """Qwen3-8B serving layer (B = 64, contexts up to 8k, fragmented pool,
-    device-filled caches): the fused step equals the two calls bit for bit
-    (q_out, both whole caches, the output)."""
+    device-filled caches), in the launch configuration the benchmark times:
+    the fused step equals the two calls bit for bit (q_out, both whole
+    caches, the output), and equals the oracle's own append (q_out and every
+    cache block the requests use, bit for bit) followed by its attention
+    (every request and head, within the tolerance)."""
+    import os
     import torch
     mi = _mi()
     w = WORKLOADS["qwen3_8b"]
@@ -107,6 +113,8 @@ def test_step_full_size_serving_layer(cuda_device):
     pos = (cl - 1).astype(np.int32)
     sl = np.array([bt[b, (cl[b] - 1) // 16] * 16 + (cl[b] - 1) % 16 for b in range(w.B)], np.int32)
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    # the oracle's inputs: every block the requests use, before the step
+    kc_s, vc_s, bt_s, used = gather_used_blocks(kc0, vc0, bt, cl)
     # two calls
     kc_a, vc_a = kc0.clone(), vc0.clone()
     qo_a, out_a = torch.empty_like(q_d), torch.empty_like(q_d)
@@ -123,6 +131,17 @@ def test_step_full_size_serving_layer(cuda_device):
     assert torch.equal(kc_a.view(torch.int16), kc0.view(torch.int16))
     assert torch.equal(vc_a.view(torch.int16), vc0.view(torch.int16))
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    # the oracle's append (slots from its own slot mapping over the renumbered
+    # tables) and attention over the same blocks
+    q_ref, st = oracle.append(q, k, v, pos, oracle.slot_mapping(bt_s, pos),
+                              oracle.rope_table(w.theta, w.head_dim, w.max_pos), kc_s, vc_s)
+    assert st == 0
+    assert np.array_equal(from_dev_u16(qo_b), q_ref)
+    kc_f, vc_f, _, used_f = gather_used_blocks(kc0, vc0, bt, cl)
+    assert used_f == used
+    assert np.array_equal(kc_f, kc_s) and np.array_equal(vc_f, vc_s)
+    ref = oracle.paged_attention(q_ref, kc_s, vc_s, bt_s, cl, w.scale, nthreads=os.cpu_count() or 8)
+    assert_attention_close(from_dev_u16(out_b), ref, "qwen3_8b fused step")
 
 
 @pytest.mark.parametrize("d_head,Hq,Hkv", [(128, 8, 2), (64, 4, 2), (128, 7, 1), (64, 8, 8), (128, 16, 2)])
