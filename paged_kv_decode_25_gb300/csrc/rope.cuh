@@ -66,6 +66,19 @@ __device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bo
     return s;
 }
 
+// The double-precision route of rotate_word: the exact products and one
+// double rounding decide the bits. Kept out of line: it is rarely taken, and
+// inlined into every unrolled rotation it would make the code several times
+// larger (cold instruction fetches then dominate a short kernel's start).
+static __device__ __noinline__ uint2 rotate_word_exact(uint32_t xl, uint32_t xh, float4 cs) {
+    const double a0 = bf16_bits_to_f64(xl & 0xFFFFu), a1 = bf16_bits_to_f64(xl >> 16);
+    const double b0 = bf16_bits_to_f64(xh & 0xFFFFu), b1 = bf16_bits_to_f64(xh >> 16);
+    const double c0 = f32_to_f64_bits(cs.x), sn0 = f32_to_f64_bits(cs.y);
+    const double c1 = f32_to_f64_bits(cs.z), sn1 = f32_to_f64_bits(cs.w);
+    return make_uint2(rot_lo(a0, c0, b0, sn0) | (rot_lo(a1, c1, b1, sn1) << 16),
+                      rot_hi(b0, c0, a0, sn0) | (rot_hi(b1, c1, a1, sn1) << 16));
+}
+
 // Rotated bf16 pairs of one group: element k of the first half (lo) and of
 // the second half (hi) of a head, two adjacent pairs per word:
 // ylo = x_lo * cos - x_hi * sin, yhi = x_hi * cos + x_lo * sin,
@@ -82,12 +95,9 @@ __device__ __forceinline__ void rotate_word(uint32_t xl, uint32_t xh, float4 cs,
     yh = pack_bf16x2(s2, s3);
     if (slow) {
         // rare: the exact products and one double rounding decide it
-        const double a0 = bf16_bits_to_f64(xl & 0xFFFFu), a1 = bf16_bits_to_f64(xl >> 16);
-        const double b0 = bf16_bits_to_f64(xh & 0xFFFFu), b1 = bf16_bits_to_f64(xh >> 16);
-        const double c0 = f32_to_f64_bits(cs.x), sn0 = f32_to_f64_bits(cs.y);
-        const double c1 = f32_to_f64_bits(cs.z), sn1 = f32_to_f64_bits(cs.w);
-        yl = rot_lo(a0, c0, b0, sn0) | (rot_lo(a1, c1, b1, sn1) << 16);
-        yh = rot_hi(b0, c0, a0, sn0) | (rot_hi(b1, c1, a1, sn1) << 16);
+        const uint2 y = rotate_word_exact(xl, xh, cs);
+        yl = y.x;
+        yh = y.y;
     }
 }
 

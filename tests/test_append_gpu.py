@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from helpers import from_dev_u16, grow, pools_for, to_dev_i32, to_dev_u16
-from workloads import WORKLOADS, device_fill_cache, history_cache, new_token_values
+from workloads import WORKLOADS, bf16_normal, device_fill_cache, history_cache, new_token_values
 
 pytestmark = pytest.mark.gpu
 
@@ -227,6 +227,106 @@ def test_append_rotation_bit_exact_on_wide_values(cuda_device, B, d):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     q_ref, st = oracle.append(q, k, v, pos, slots, table_ref, kc, vc)
+    assert st == 0
+    assert np.array_equal(from_dev_u16(qo_d), q_ref)
+    assert np.array_equal(from_dev_u16(kc_d), kc)
+    assert np.array_equal(from_dev_u16(vc_d), vc)
+
+
+NEAR_TIE_POSITIONS = [1, 3, 17, 100, 255, 1000, 2047, 4095]
+
+
+@pytest.fixture(scope="module")
+def near_tie_sets():
+    """Near-tie rotation pairs for every table entry of the positions above
+    (d = 128, theta = 1e6), from the oracle's table."""
+    from near_ties import near_tie_sets as sets_for
+    table = oracle.rope_table(1e6, 128, 4096)
+    return table, sets_for(table, NEAR_TIE_POSITIONS, seed=2024)
+
+
+@pytest.mark.parametrize("rows_per_position", [3, 40])  # 24 rows: two pairs per thread; 320: eight
+def test_append_bit_exact_at_near_ties(cuda_device, near_tie_sets, rows_per_position):
+    """Every rotation pair of every q and k head holds a pair whose exact
+    rotated value lies within 4 fp32 ulps of a bf16 rounding midpoint or of
+    a power of two (over 10^4 distinct such pairs): the places where a
+    single-precision rotation could round differently. q_out and the cache
+    rows equal the oracle's bit for bit through both thread layouts of the
+    append (decode-sized and prefill-sized batches)."""
+    import torch
+    from near_ties import near_tie_rows
+    mi = _mi()
+    table_ref, sets = near_tie_sets
+    Hq, Hkv, dh = 8, 2, 128
+    rows, pos, distinct, kinds = near_tie_rows(sets, NEAR_TIE_POSITIONS, rows_per_position, Hq + Hkv)
+    assert distinct >= 10_000 and kinds[0] > 0 and kinds[1] > 0, (distinct, kinds)
+    B = rows.shape[0]
+    q, k = np.ascontiguousarray(rows[:, :Hq]), np.ascontiguousarray(rows[:, Hq:])
+    v = bf16_normal(np.random.Generator(np.random.PCG64(11)), (B, Hkv, dh))
+    nb = B
+    sl = (np.arange(B) * 16 + np.arange(B) % 16).astype(np.int32)  # block b, a different row in each
+    kc = np.full((nb, Hkv, 16, dh), 0x7FA5, np.uint16)
+    vc = kc.copy()
+    _, table = mi.mi_rope_table(1e6, dh, 4096)
+    assert np.array_equal(table, table_ref)
+    d = mi.dims(B, Hq, Hkv, dh, nb, 1)
+    q_d = to_dev_u16(q, cuda_device)
+    qo_d = torch.empty_like(q_d)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(vc, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    assert mi.mi_paged_kv_append(d, q_d, to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                 to_dev_i32(pos, cuda_device), to_dev_i32(sl, cuda_device),
+                                 torch.from_numpy(table).to(cuda_device), 4096, qo_d, kc_d, vc_d, err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q_ref, st = oracle.append(q, k, v, pos, sl, table_ref, kc, vc)
+    assert st == 0
+    assert np.array_equal(from_dev_u16(qo_d), q_ref)
+    assert np.array_equal(from_dev_u16(kc_d), kc)
+    assert np.array_equal(from_dev_u16(vc_d), vc)
+
+
+def test_step_bit_exact_at_near_ties(cuda_device, near_tie_sets):
+    """The fused decode step rotates q and the new k with the same exact
+    rule: on near-tie inputs its q_out and the new cache rows equal the
+    oracle's append bit for bit (the attention output is not compared here:
+    the near-tie values span 2^-30 .. 2^30)."""
+    import torch
+    from near_ties import near_tie_rows
+    mi = _mi()
+    table_ref, sets = near_tie_sets
+    Hq, Hkv, dh = 8, 2, 128
+    rows, pos, distinct, _ = near_tie_rows(sets, NEAR_TIE_POSITIONS, 3, Hq + Hkv)
+    B = rows.shape[0]
+    q, k = np.ascontiguousarray(rows[:, :Hq]), np.ascontiguousarray(rows[:, Hq:])
+    r = np.random.Generator(np.random.PCG64(12))
+    v = bf16_normal(r, (B, Hkv, dh))
+    cl = (pos + 1).astype(np.int32)            # the new token sits at position cl - 1
+    nblk = -(-cl // 16)
+    nb = int(nblk.sum())
+    mbps = int(nblk.max())
+    perm = r.permutation(nb)
+    bt = np.full((B, mbps), -1, np.int32)
+    i = 0
+    for b in range(B):
+        bt[b, :nblk[b]] = perm[i:i + nblk[b]]
+        i += nblk[b]
+    kc = bf16_normal(r, (nb, Hkv, 16, dh))
+    vc = bf16_normal(r, (nb, Hkv, 16, dh))
+    _, table = mi.mi_rope_table(1e6, dh, 4096)
+    d = mi.dims(B, Hq, Hkv, dh, nb, mbps)
+    ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=cuda_device)
+    q_d = to_dev_u16(q, cuda_device)
+    qo_d, out = torch.empty_like(q_d), torch.empty_like(q_d)
+    kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(vc, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    assert mi.mi_paged_decode_step(d, q_d, to_dev_u16(k, cuda_device), to_dev_u16(v, cuda_device),
+                                   torch.from_numpy(table).to(cuda_device), 4096, to_dev_i32(bt, cuda_device),
+                                   to_dev_i32(cl, cuda_device), 1.0 / np.sqrt(dh), qo_d, kc_d, vc_d, out, ws,
+                                   dev_err=err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q_ref, st = oracle.append(q, k, v, pos, oracle.slot_mapping(bt, pos), table_ref, kc, vc)
     assert st == 0
     assert np.array_equal(from_dev_u16(qo_d), q_ref)
     assert np.array_equal(from_dev_u16(kc_d), kc)
