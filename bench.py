@@ -512,6 +512,15 @@ def measure_sweep_config(mi, device, stream, w, peak, flush, oracle_budget_s):
     sweep(True)  # warm-up sweep
     runs = [sweep(True) for _ in range(3)]
     warm_runs = [sweep(False) for _ in range(3)]
+    # the device side alone: the graph of the layers replayed on the last
+    # step's inputs, back to back (no host work, no copies)
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record(stream)
+    for _ in range(20):
+        g.replay()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = ga.elapsed_time(gb) / 20
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
     nbytes = runs[0][0]
     t_flushed = statistics.median(r[1] for r in runs)
@@ -525,6 +534,7 @@ def measure_sweep_config(mi, device, stream, w, peak, flush, oracle_budget_s):
            "gbs": gbs, "frac": gbs / peak, "algorithmic_bytes_per_sweep": nbytes,
            "l2_warm": {"sweep_ms": t_warm, "steps_per_s": S / (t_warm * 1e-3),
                        "note": "steps back to back without a flush: a step's K/V (about 91 MB) stay in L2"},
+           "graph_only_ms_per_step": graph_ms,
            "launches_per_step": L, "sweeps_timed": len(runs),
            "l2": ("flushed before every step (2x L2 written), flush outside the step's events; launch-bound: "
                   "each layer's K/V is a few MB")}

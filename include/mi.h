@@ -442,6 +442,30 @@ mi_status mi_paged_decode_attention_noalloc(const mi_dims* dims, const void* q,
                                             const int32_t* context_lens, float scale, void* out,
                                             int32_t* dev_err, mi_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Failure-detection test hooks. Every mbarrier wait in the attention kernels
+ * is bounded: when a staged copy or a partner warp does not arrive in time
+ * the kernel ORs MI_DEVERR_TIMEOUT into *dev_err and returns instead of
+ * hanging. These two process-wide settings let a test make such a wait run
+ * out without faulting anything: they apply to every launch queued after the
+ * call (not to launches already queued or captured), and a serving process
+ * leaves them at their defaults. Not thread-safe against launches on other
+ * host threads. */
+
+/* Bound on each wait of later launches, in nanoseconds: 1 .. 2e9; 0 restores
+ * the default (2 s). Waits for the launch's own copies or MMAs to finish
+ * before it releases its memory keep a floor of 10 ms. MI_ERR_INVALID_ARG
+ * outside 0 .. 2e9. */
+mi_status mi_test_set_wait_limit(int64_t ns);
+
+/* enable != 0: in later decode attention / fused step launches (bf16 and
+ * e4m3), every CTA's producer neither copies nor announces the first block it
+ * stages; in later tcgen05 prefill launches, every CTA's producer does so for
+ * its first K stage. The waits on those stages then run out (set
+ * MI_DEVERR_TIMEOUT) and the affected outputs are not valid. No copy is left
+ * in flight. enable = 0 turns it off. Always MI_OK. */
+mi_status mi_test_withhold_copy(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif

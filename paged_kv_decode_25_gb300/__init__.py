@@ -41,7 +41,7 @@ EXPORTS = (
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
     "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
     "mi_paged_prefill_attention", "mi_paged_prefill_attention_variant", "mi_paged_decode_attention_noalloc",
-    "mi_paged_decode_step",
+    "mi_paged_decode_step", "mi_test_set_wait_limit", "mi_test_withhold_copy",
 )
 MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -99,6 +99,8 @@ def load():
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
             "mi_paged_decode_step": (
                 [dims_p, P, P, P, P, i32, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
+            "mi_test_set_wait_limit": ([ctypes.c_int64], i32),
+            "mi_test_withhold_copy": ([i32], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -395,3 +397,14 @@ def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tabl
     return load().mi_paged_decode_attention_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                     _ptr(block_tables), _ptr(context_lens), float(scale),
                                                     _ptr(out), _ptr(dev_err), _stream(stream))
+
+
+def mi_test_set_wait_limit(ns):
+    """Bound on each device wait of later launches (ns; 0 = the 2 s default)."""
+    return load().mi_test_set_wait_limit(int(ns))
+
+
+def mi_test_withhold_copy(enable):
+    """Failure-detection test hook: later attention launches withhold one
+    staged copy, so a bounded wait runs out (see include/mi.h)."""
+    return load().mi_test_withhold_copy(1 if enable else 0)

@@ -12,6 +12,21 @@ namespace mi {
 
 constexpr int kBlock = 16;               // tokens per KV block
 constexpr long long kWaitLimitNs = 2000000000LL;  // 2 s bound on any mbarrier wait
+// Waits for asynchronous work a kernel has itself issued (its copies landing,
+// its MMAs finishing) before it releases shared or tensor memory use at
+// least this bound, however short a test makes the launch's wait limit.
+constexpr long long kDrainMinNs = 10000000LL;     // 10 ms
+
+__host__ __device__ inline long long drain_limit(long long wait_ns) {
+    return wait_ns > kDrainMinNs ? wait_ns : kDrainMinNs;
+}
+
+// Failure-detection test settings (mi_test_set_wait_limit,
+// mi_test_withhold_copy), read on the host when a launch's parameters are
+// built: the launch's wait limit, and whether its producer withholds one
+// staged copy.
+long long test_wait_limit_ns();
+bool test_withhold_copy();
 
 // ------------------------------------------------------------------ bf16 ---
 
@@ -118,15 +133,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier to complete, for at most
-// kWaitLimitNs. Returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier to complete, for at most limit_ns
+// (the launch's wait limit: kWaitLimitNs unless a test shortened it).
+// Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if ((long long)(globaltimer() - t0) > kWaitLimitNs) return false;
+        if ((long long)(globaltimer() - t0) > limit_ns) return false;
     }
 }
 

@@ -87,6 +87,8 @@ struct AttnParams {
     uint16_t* kc;                  // [num_blocks][Hkv][16][HD]
     uint16_t* vc;
     int max_pos;
+    long long wait_ns;             // bound on every mbarrier wait of the launch
+    int withhold;                  // failure-detection test: each producer withholds its first copy
 };
 
 // ------------------------------------------------------------- the plan ---
@@ -803,8 +805,8 @@ template <int HD, int GP>
 struct StateOf<HD, kVarFp8, GP> { using T = Fp8State<HD>; };
 
 // A bounded wait by every lane of a warp; true when all of them saw the phase.
-__device__ __forceinline__ bool wait_all_warp(uint32_t bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+__device__ __forceinline__ bool wait_all_warp(uint32_t bar, uint32_t parity, long long limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, limit_ns));
 }
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
@@ -929,7 +931,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                     for (int j = 0; j < kVW; ++j)
                         vv[j] = __ldg(reinterpret_cast<const uint32_t*>(p.vnew + nofs + 2 * lane + 64 * j));
                 }
-                if (!wait_all_warp(qempty0 + slot * 8, (uint32_t)(((u >> 1) & 1) ^ 1))) {
+                if (!wait_all_warp(qempty0 + slot * 8, (uint32_t)(((u >> 1) & 1) ^ 1), p.wait_ns)) {
                     if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                     good = false;
                     break;
@@ -1011,6 +1013,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
         // the two copies.
         const uint64_t policy = l2_policy_evict_first();
         uint32_t stg = 0, ph = 1;  // a fresh barrier reads as having completed the phase before 0
+        // failure-detection test: in every CTA, lane 0 neither copies nor
+        // arrives for its first block, so consumer warp 0's wait on that
+        // stage runs out (some CTAs may have no blocks at all)
+        bool withhold = p.withhold != 0 && lane == 0;
         const uint32_t my_full = full0 + (uint32_t)(lane * S) * 8, my_empty = empty0 + (uint32_t)(lane * S) * 8;
         const uint32_t my_tiles = sbase + sp.tiles + (uint32_t)(lane * S) * (2 * kTile);
         for (int part = 0; part < 2; ++part) {
@@ -1019,7 +1025,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
         if (x >= pe) continue;
         Cursor cu = part == 0 ? rp->c0 : rp->c1;  // advanced to each block below
         for (; x < pe; x += W) {
-            if (!mbar_wait_bounded(my_empty + stg * 8, ph)) {
+            if (!mbar_wait_bounded(my_empty + stg * 8, ph, p.wait_ns)) {
                 // the consumer stopped taking stages (it timed out itself)
                 raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                 return;
@@ -1028,7 +1034,9 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
             const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
             const uint32_t bar = my_full + stg * 8;
             const uint32_t okf = sbase + sp.okf + ((uint32_t)(lane * S) + stg) * 4;
-            if (blk < 0 || blk >= p.num_blocks) {
+            if (withhold) {
+                withhold = false;  // nothing is copied into this stage and nothing arrives on it
+            } else if (blk < 0 || blk >= p.num_blocks) {
                 raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
                 sts32(okf, 0u);
                 mbar_arrive(bar);  // the consumer skips the block
@@ -1083,7 +1091,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
             }
             // this unit's rotated q from the RoPE warp's ring
             const int slot = unit_no & 1;
-            if (!dead && !wait_all_warp(qfull0 + slot * 8, (uint32_t)((unit_no >> 1) & 1))) {
+            if (!dead && !wait_all_warp(qfull0 + slot * 8, (uint32_t)((unit_no >> 1) & 1), p.wait_ns)) {
                 dead = true;
                 if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             }
@@ -1096,7 +1104,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
         for (; x < se; x += W) {
             const uint32_t si = (uint32_t)(warp * S) + cstage;
             if (!dead) {
-                const bool okw = mbar_wait_bounded(full0 + si * 8, cphase);
+                const bool okw = mbar_wait_bounded(full0 + si * 8, cphase, p.wait_ns);
                 if (__any_sync(0xffffffffu, !okw)) {
                     dead = true;
                     if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
@@ -1121,7 +1129,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                         // the new token: its rotated k and its v (from the
                         // RoPE warp's ring slot) into row valid - 1 of the tiles
                         const int row = valid - 1;
-                        if (!wait_all_warp(kvfull0 + (unit_no & 1) * 8, (uint32_t)((unit_no >> 1) & 1))) {
+                        if (!wait_all_warp(kvfull0 + (unit_no & 1) * 8, (uint32_t)((unit_no >> 1) & 1), p.wait_ns)) {
                             dead = true;
                             if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                         }
@@ -1274,7 +1282,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
     if (dead && lane == 0) {
         for (int s2 = 0; s2 < S; ++s2) {
             const uint32_t si = (uint32_t)(warp * S) + (uint32_t)s2;
-            (void)mbar_wait_bounded(full0 + si * 8, s2 < (int)cstage ? cphase ^ 1u : cphase);
+            (void)mbar_wait_bounded(full0 + si * 8, s2 < (int)cstage ? cphase ^ 1u : cphase, drain_limit(p.wait_ns));
         }
     }
 }
@@ -1427,8 +1435,30 @@ unsigned long long next_epoch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<long long> g_test_wait_ns{0};  // 0: the default kWaitLimitNs
+std::atomic<int> g_test_withhold{0};
+
 }  // namespace
+
+long long test_wait_limit_ns() {
+    const long long v = g_test_wait_ns.load(std::memory_order_relaxed);
+    return v > 0 ? v : kWaitLimitNs;
+}
+
+bool test_withhold_copy() { return g_test_withhold.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace mi
+
+extern "C" mi_status mi_test_set_wait_limit(int64_t ns) {
+    if (ns < 0 || ns > mi::kWaitLimitNs) return MI_ERR_INVALID_ARG;
+    mi::g_test_wait_ns.store((long long)ns, std::memory_order_relaxed);
+    return MI_OK;
+}
+
+extern "C" mi_status mi_test_withhold_copy(int32_t enable) {
+    mi::g_test_withhold.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return MI_OK;
+}
 
 extern "C" size_t mi_paged_decode_workspace_bytes(const mi_dims* dims) {
     using namespace mi;
@@ -1532,6 +1562,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.kc = static_cast<uint16_t*>(const_cast<void*>(k_cache));
     p.vc = static_cast<uint16_t*>(const_cast<void*>(v_cache));
     p.max_pos = step ? step->max_pos : 0;
+    p.wait_ns = test_wait_limit_ns();
+    p.withhold = test_withhold_copy() ? 1 : 0;
 
     cudaStream_t s = (cudaStream_t)stream;
     return launch_pdl(fn, grid, threads, smem, s, tk, tv, p) == cudaSuccess ? MI_OK : MI_ERR_CUDA;

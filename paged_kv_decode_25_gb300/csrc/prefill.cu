@@ -56,6 +56,8 @@ struct PrefillParams {
     int32_t* dev_err;
     int R, Hq, Hkv, G, num_blocks, mbps, T, max_q;
     float sl2;                     // scale * log2(e)
+    long long wait_ns;             // bound on every mbarrier wait of the launch
+    int withhold;                  // failure-detection test: each producer withholds its first K copy
 };
 
 // The work item of a CTA: row tile k (counted from the request's end) of
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
         for (int j = 0; j < nst; ++j) {
             // every lane waits; the warp gives up together if any lane ran out of
             // time (a consumer stopped taking stages: it timed out itself)
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + stg * 8, ph))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + stg * 8, ph, p.wait_ns))) {
                 if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                 break;
             }
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
         if (lane == 0) {
             for (int s = 0; s < kPStages && s < issued; ++s) {
                 const int fills = (issued - s + kPStages - 1) / kPStages;
-                (void)mbar_wait_bounded(full0 + s * 8, (uint32_t)((fills - 1) & 1));
+                (void)mbar_wait_bounded(full0 + s * 8, (uint32_t)((fills - 1) & 1), drain_limit(p.wait_ns));
             }
         }
         return;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__((kPWarps + 1) * 32, kMT == 1 ? 2 : 1)
     uint32_t stg = 0, ph = 0;
     bool dead = false;
     for (int j = 0; j < nst; ++j) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + stg * 8, ph))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + stg * 8, ph, p.wait_ns))) {
             if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             dead = true;
             break;
@@ -456,8 +458,8 @@ struct TcSmem {
     static_assert(kSlack >= 0, "shared memory plan exceeds two CTAs per SM");
 };
 
-__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, long long limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, limit_ns));
 }
 
 template <int HD>
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         bool pok = false;
         auto load_v = [&](int jv) -> bool {
             const int sl = jv % kTcV, u = jv / kTcV;
-            if (!wait_all(v_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) return false;
+            if (!wait_all(v_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1), p.wait_ns)) return false;
             const uint32_t msk = __ballot_sync(0xffffffffu, pok);
             const uint32_t fb = v_full0 + sl * 8;
             if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         bool pgood = true;
         for (int j = 0; j < nst; ++j) {
             const int sl = j % kTcK, u = j / kTcK;
-            if (!wait_all(k_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1))) {
+            if (!wait_all(k_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1), p.wait_ns)) {
                 pgood = false;
                 break;
             }
@@ -576,12 +578,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             const uint32_t msk = __ballot_sync(0xffffffffu, ok);
             const uint32_t fb = k_full0 + (j % (2 * kTcK)) * 8;
-            if (lane == 0) {
+            // failure-detection test: stage 0's K is neither copied nor
+            // announced, so every wait on it runs out
+            const bool held = p.withhold != 0 && j == 0;
+            if (lane == 0 && !held) {
                 sts32(mask0 + (j % (2 * kTcK)) * 4, msk);
                 mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
             }
             __syncwarp();
-            if (ok) {
+            if (ok && !held) {
                 const uint32_t kd = sbase + SM::kRingK + sl * SM::kKV + lane * kBlock * 128;
                 const int row0 = (blk * p.Hkv + it.h) * kBlock;
                 for (int hh = 0; hh < kH; ++hh) tma_load_3d(kd + hh * 64 * 128, &tmk, fb, 0, hh, row0, policy);
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         // ------------------------------------------------- MMA issuer ----
         if (lane == 0 && nst > 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kTcRows, 64, false);
-            bool ok = mbar_wait_bounded(q_full, 0);
+            bool ok = mbar_wait_bounded(q_full, 0, p.wait_ns);
             auto issue_s = [&](int jj) {
                 const int sl = jj % kTcK, b = jj & 1;
                 const uint32_t kbase = sbase + SM::kRingK + sl * SM::kKV;
@@ -617,8 +622,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             // j - 2 (P_{j-2} lives there)
             for (int jj = 0; ok && jj < nst; ++jj) {
                 const int u = jj >> 1;
-                ok = mbar_wait_bounded(k_full0 + (jj % (2 * kTcK)) * 8, (uint32_t)((jj / (2 * kTcK)) & 1));
-                if (ok && u >= 1) ok = mbar_wait_bounded(s_free0 + (jj & 1) * 8, (uint32_t)((u - 1) & 1));
+                ok = mbar_wait_bounded(k_full0 + (jj % (2 * kTcK)) * 8, (uint32_t)((jj / (2 * kTcK)) & 1), p.wait_ns);
+                if (ok && u >= 1) ok = mbar_wait_bounded(s_free0 + (jj & 1) * 8, (uint32_t)((u - 1) & 1), p.wait_ns);
                 if (!ok) break;
                 tc::fence_after();
                 issue_s(jj);
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             // every MMA issued has finished before tensor memory is released
             tc::commit(fin);
-            (void)mbar_wait_bounded(fin, 0);
+            (void)mbar_wait_bounded(fin, 0, drain_limit(p.wait_ns));
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -637,8 +642,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
             bool ok = true;
             for (int j = 0; ok && j < nst; ++j) {
-                if (!(ok = mbar_wait_bounded(p_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1)))) break;
-                if (!(ok = mbar_wait_bounded(v_full0 + (j % kTcV) * 8, (uint32_t)((j / kTcV) & 1)))) break;
+                if (!(ok = mbar_wait_bounded(p_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns))) break;
+                if (!(ok = mbar_wait_bounded(v_full0 + (j % kTcV) * 8, (uint32_t)((j / kTcV) & 1), p.wait_ns))) break;
                 tc::fence_after();
                 const uint32_t vbase = sbase + SM::kRingV + (j % kTcV) * SM::kKV;
                 // P_j sits in the first 32 columns of its score buffer (bf16 pairs)
@@ -654,7 +659,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
             if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             tc::commit(fin_o);
-            (void)mbar_wait_bounded(fin_o, 0);
+            (void)mbar_wait_bounded(fin_o, 0, drain_limit(p.wait_ns));
         }
         __syncwarp();
     } else {
@@ -672,8 +677,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         bool ok = true;
         for (int j = 0; j < nst; ++j) {
             const int sl = j % kTcV, b = j & 1;  // sl: the V stage
-            ok = wait_all(k_full0 + (j % (2 * kTcK)) * 8, (uint32_t)((j / (2 * kTcK)) & 1)) &&
-                 wait_all(s_full0 + b * 8, (uint32_t)((j >> 1) & 1));
+            ok = wait_all(k_full0 + (j % (2 * kTcK)) * 8, (uint32_t)((j / (2 * kTcK)) & 1), p.wait_ns) &&
+                 wait_all(s_full0 + b * 8, (uint32_t)((j >> 1) & 1), p.wait_ns);
             if (!ok) break;
             tc::fence_after();
             uint32_t x[64];
@@ -765,7 +770,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             lrow = lrow * alpha + psum;
             if (__any_sync(0xffffffffu, need)) {
                 // O may be touched once the previous P . V has finished
-                if (!(ok = wait_all(o_done0 + ((j - 1) & 1) * 8, (uint32_t)(((j - 1) >> 1) & 1)))) break;
+                if (!(ok = wait_all(o_done0 + ((j - 1) & 1) * 8, (uint32_t)(((j - 1) >> 1) & 1), p.wait_ns))) break;
                 tc::fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < HD / 32; ++ch) {
@@ -790,7 +795,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     const int blk = j * kStageBlocks + l;
                     any |= !((present >> l) & 1u) || (blk == nb_ctx - 1 && tail < kBlock);
                 }
-                if (any && !(ok = wait_all(v_full0 + sl * 8, (uint32_t)((j / kTcV) & 1)))) break;
+                if (any && !(ok = wait_all(v_full0 + sl * 8, (uint32_t)((j / kTcV) & 1), p.wait_ns))) break;
                 for (int l = 0; any && l < kStageBlocks; ++l) {
                     const int blk = j * kStageBlocks + l;
                     const int from = !((present >> l) & 1u) ? 0 : (blk == nb_ctx - 1 && tail < kBlock ? tail : kBlock);
@@ -805,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             mbar_arrive(p_full0 + (j & 1) * 8);
         }
         if (!ok && threadIdx.x == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
-        if (ok && nst > 0) ok = wait_all(o_done0 + ((nst - 1) & 1) * 8, (uint32_t)(((nst - 1) >> 1) & 1));
+        if (ok && nst > 0) ok = wait_all(o_done0 + ((nst - 1) & 1) * 8, (uint32_t)(((nst - 1) >> 1) & 1), p.wait_ns);
         tc::fence_after();
         const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
         const uint32_t keep = pos >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
@@ -926,6 +931,8 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
     p.T = total_q;
     p.max_q = max_query_len;
     p.sl2 = scale * 1.4426950408889634f;
+    p.wait_ns = test_wait_limit_ns();
+    p.withhold = use_tc && test_withhold_copy() ? 1 : 0;  // (the tcgen05 kernel's test hook)
     const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
