@@ -70,6 +70,39 @@ __device__ __forceinline__ void store_e4m3(uint8_t* dst, const uint32_t (&y)[NJ]
     }
 }
 
+// The rare second pass of a thread's rotation: each word flagged in `need`
+// is rotated again by the exact route and stored over the fast result (bf16
+// words at lo / hi, or, with E4M3, its two e4m3 pairs quantised with
+// `scale`). The inputs stay in registers (q_out may alias q, so the source
+// cannot be re-read); a rolled loop with a select keeps this pass compact
+// and keeps the out-of-line call away from the main rotation.
+template <int NJ, bool E4M3, typename T>
+__device__ __forceinline__ void exact_words(unsigned need, const uint32_t (&xl)[NJ], const uint32_t (&xh)[NJ],
+                                         const float4 (&cs)[NJ], T* lo, T* hi, float scale) {
+#pragma unroll 1
+    for (int j = 0; j < NJ; ++j) {
+        if (!((need >> j) & 1u)) continue;
+        uint32_t wl = xl[0], wh = xh[0];
+        float4 c = cs[0];
+#pragma unroll
+        for (int jj = 1; jj < NJ; ++jj)
+            if (j == jj) {
+                wl = xl[jj];
+                wh = xh[jj];
+                c = cs[jj];
+            }
+        const uint2 y = rotate_word_exact(wl, wh, c);
+        if constexpr (E4M3) {
+            const uint32_t yl1[1] = {y.x}, yh1[1] = {y.y};
+            store_e4m3<1>(reinterpret_cast<uint8_t*>(lo) + 2 * j, yl1, scale);
+            store_e4m3<1>(reinterpret_cast<uint8_t*>(hi) + 2 * j, yh1, scale);
+        } else {
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(lo) + 2 * j) = y.x;
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(hi) + 2 * j) = y.y;
+        }
+    }
+}
+
 // One thread per (request, head, group of PPT rotation pairs): heads 0..Hq-1
 // are query heads (to q_out), heads Hq..Hq+Hkv-1 key heads (to the cache).
 // Each thread loads its two halves and its PPT (cos, sin) pairs before it
@@ -134,8 +167,9 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
 #pragma unroll
         for (int j = 0; j < NJ; ++j) cs[j] = cs4[j];
         uint32_t yl[NJ], yh[NJ];
+        unsigned need = 0;  // words whose values need the exact route
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) rotate_word(xl[j], xh[j], cs[j], yl[j], yh[j]);
+        for (int j = 0; j < NJ; ++j) need |= (unsigned)rotate_word_fast(xl[j], xh[j], cs[j], yl[j], yh[j]) << j;
         if (FP8 && !is_q) {
             const float ks = a.k_scale[head - a.Hq];
             if (!scale_ok(ks)) {
@@ -145,11 +179,13 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
             uint8_t* dst8 = a.k_cache8 + dst_off;
             store_e4m3<NJ>(dst8 + i0, yl, ks);
             store_e4m3<NJ>(dst8 + i0 + half, yh, ks);
+            if (need) exact_words<NJ, true>(need, xl, xh, cs, dst8 + i0, dst8 + i0 + half, ks);
             return;
         }
         uint16_t* dst = (is_q ? a.q_out : a.k_cache) + dst_off;
         store_words<NJ>(dst + i0, yl);
         store_words<NJ>(dst + i0 + half, yh);
+        if (need) exact_words<NJ, false>(need, xl, xh, cs, dst + i0, dst + i0 + half, 0.f);
         return;
     }
     const long long c = t - n_rot;

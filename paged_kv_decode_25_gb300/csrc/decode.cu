@@ -52,11 +52,12 @@ namespace mi {
 namespace {
 
 constexpr int kMaxG = 8;
-// Per-unit cost of the split, in blocks (measured optima: e4m3 8-24 on a
-// Qwen3-8B serving step; bf16 8 on a batch of one long and 255 short
-// contexts, neutral on the serving step)
-constexpr int kUnitCostE4m3 = 24;
-constexpr int kUnitCostBf16 = 8;
+// Per-unit cost of the split, in blocks (measured: e4m3 best at 12 on a
+// Qwen3-8B layer and at 8 on a batch of one 32k and 255 short contexts;
+// bf16 flat from 4 to 16 on the Qwen3-8B layer, best at 4-8 on the skewed
+// batch)
+constexpr int kUnitCostE4m3 = 10;
+constexpr int kUnitCostBf16 = 6;
 // Fewest blocks a CTA's range is cut to (measured on one layer of 8 requests
 // of 200 tokens, 4 KV heads: 11 us with 32 CTAs against 17 us on all 304;
 // larger batches keep the whole grid).
@@ -87,6 +88,9 @@ struct AttnParams {
     uint16_t* kc;                  // [num_blocks][Hkv][16][HD]
     uint16_t* vc;
     int max_pos;
+    unsigned char* plan_cache;     // [grid] entries of plan_stride bytes, or null (see PlanEntry)
+    int plan_stride;
+    int plan_kind;                 // which kernel the plans are for (variant, fused step)
     long long wait_ns;             // bound on every mbarrier wait of the launch
     int withhold;                  // failure-detection test: each producer withholds its first copy
 };
@@ -275,6 +279,24 @@ struct RangePlan {
     long long ra, rb, sl;
     Cursor c0, c1;
 };
+
+// A CTA's plan kept in the workspace for the next launch: the split depends
+// only on the context lengths, the dims, the grid and the kernel, and every
+// layer of a decode step has the same lengths, so each later layer's CTA
+// finds its range here instead of recomputing the scan. An entry is used only
+// when its key and its copy of all B lengths equal the launch's exactly (a
+// stale or uninitialised entry then cannot match), and a CTA reads and writes
+// only its own entry. The lengths follow the header: int32 lens[B].
+struct PlanEntry {
+    int32_t key[8];                // kPlanMagic, kind, B, Hkv, mbps, grid, uc, P
+    long long TB, TC;
+    RangePlan rp;
+};
+constexpr int32_t kPlanMagic = 0x6E616C50;  // "Plan"
+constexpr int kPlanMaxB = 1024;               // larger batches always compute their plan
+__host__ __device__ inline int plan_stride_for(int B) {
+    return B > kPlanMaxB ? 0 : (int)((sizeof(PlanEntry) + 4 * (size_t)B + 127) / 128 * 128);
+}
 
 // Every thread of the CTA calls this after plan_scan. The ranges are of equal
 // cost (range_start over TC); each end is resolved by the one thread whose
@@ -873,17 +895,65 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
     // blocks for its per-unit work (q, the merge, the pipeline restart at its
     // boundary), which weighs more against the half-size e4m3 blocks.
     constexpr int uc = VAR == kVarFp8 ? kUnitCostE4m3 : kUnitCostBf16;
-    long long TC = 0;
-    const long long TB = plan_scan(p, uc, scan, TC);  // (ends with a barrier of all warps)
-    // CTAs that take part: the whole grid, unless that leaves fewer than
-    // kMinBlocksPerCta blocks each (a small batch): every CTA's fixed cost
-    // (the plan, the first copies, a merge) then outweighs its share of
-    // streaming, and fewer, longer ranges finish sooner.
-    const long long Pw = (TB + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
-    const int P = (int)(Pw < (long long)gridDim.x ? Pw : (long long)gridDim.x);
     const int cta = blockIdx.x;
     RangePlan* rp = reinterpret_cast<RangePlan*>(base + sp.rplan);
-    plan_ranges(p, uc, scan, TB, TC, P, rp);  // (ends with a barrier of all warps)
+    long long TB = 0, TC = 0;
+    int P = 0;
+    // this CTA's plan from an earlier launch with the same lengths, if any
+    PlanEntry* pe = p.plan_cache ? reinterpret_cast<PlanEntry*>(p.plan_cache + (long long)cta * p.plan_stride)
+                                 : nullptr;
+    const int32_t key[6] = {kPlanMagic, p.plan_kind, p.B, p.Hkv, p.mbps, (int32_t)gridDim.x};
+    bool hit = false;
+    if (pe) {
+        bool same = true;
+        if (tid < 6) same = __ldcg(pe->key + tid) == key[tid];
+        if (tid == 6) same = __ldcg(pe->key + 6) == uc;
+        const int32_t* lens = reinterpret_cast<const int32_t*>(pe + 1);
+        for (int b = tid; b < p.B; b += blockDim.x) same &= __ldcg(lens + b) == __ldg(p.context_lens + b);
+        hit = __syncthreads_and(same) != 0;
+    }
+    if (hit) {
+        if (tid == 0) {
+            TB = __ldcg(&pe->TB);
+            TC = __ldcg(&pe->TC);
+            P = __ldcg(pe->key + 7);
+            scan[0] = TB;
+            scan[1] = TC;
+            scan[2] = P;
+        }
+        const int nw = (int)(sizeof(RangePlan) / 4);
+        for (int i = tid; i < nw; i += blockDim.x)
+            reinterpret_cast<int32_t*>(rp)[i] = __ldcg(reinterpret_cast<const int32_t*>(&pe->rp) + i);
+        __syncthreads();
+        TB = scan[0];
+        TC = scan[1];
+        P = (int)scan[2];
+    } else {
+        TB = plan_scan(p, uc, scan, TC);  // (ends with a barrier of all warps)
+        // CTAs that take part: the whole grid, unless that leaves fewer than
+        // kMinBlocksPerCta blocks each (a small batch): every CTA's fixed cost
+        // (the plan, the first copies, a merge) then outweighs its share of
+        // streaming, and fewer, longer ranges finish sooner.
+        const long long Pw = (TB + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
+        P = (int)(Pw < (long long)gridDim.x ? Pw : (long long)gridDim.x);
+        plan_ranges(p, uc, scan, TB, TC, P, rp);  // (ends with a barrier of all warps)
+        if (pe) {
+            // the plan first, the lengths, then the key: an entry is
+            // complete when its key matches
+            int32_t* lens = reinterpret_cast<int32_t*>(pe + 1);
+            for (int b = tid; b < p.B; b += blockDim.x) lens[b] = __ldg(p.context_lens + b);
+            const int nw = (int)(sizeof(RangePlan) / 4);
+            for (int i = tid; i < nw; i += blockDim.x)
+                reinterpret_cast<int32_t*>(&pe->rp)[i] = reinterpret_cast<const int32_t*>(rp)[i];
+            if (tid == 0) {
+                pe->TB = TB;
+                pe->TC = TC;
+                pe->key[7] = P;
+                pe->key[6] = uc;
+                for (int i = 0; i < 6; ++i) pe->key[i] = key[i];
+            }
+        }
+    }
     const long long ra = rp->ra, rb = rp->rb, sl = rp->sl;
 
     if (FUSED && warp == W + 1) {
@@ -939,15 +1009,32 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                 uint16_t* qrows = ring + slot * (p.G + 2) * HD;
                 uint16_t* krow = qrows + p.G * HD;
                 uint16_t* vrow = krow + HD;
+                unsigned need = 0;  // q words whose values need the exact route
 #pragma unroll
                 for (int i = 0; i < kQW; ++i) {
                     const int w = lane + 32 * i;
                     if (w < p.G * HD / 4) {
                         uint32_t yl = 0u, yh = 0u;
-                        if (pos >= 0) rotate_word(xl[i], xh[i], c4, yl, yh);
+                        if (pos >= 0) need |= (unsigned)rotate_word_fast(xl[i], xh[i], c4, yl, yh) << i;
                         uint16_t* qd = qrows + (w / (HD / 4)) * HD + kc;
                         *reinterpret_cast<uint32_t*>(qd) = yl;
                         *reinterpret_cast<uint32_t*>(qd + HD / 2) = yh;
+                    }
+                }
+                if (need) {
+                    // rare: those words again by the exact route (the raw q
+                    // is never written by this kernel, so it is re-read)
+#pragma unroll 1
+                    for (int i = 0; i < kQW; ++i) {
+                        if (!((need >> i) & 1u)) continue;
+                        const int row = (lane + 32 * i) / (HD / 4);
+                        const uint16_t* qr =
+                            p.qraw + ((long long)cu.b * p.Hq + (long long)cu.h * p.G + row) * HD + kc;
+                        const uint2 y = rotate_word_exact(__ldg(reinterpret_cast<const uint32_t*>(qr)),
+                                                          __ldg(reinterpret_cast<const uint32_t*>(qr + HD / 2)), c4);
+                        uint16_t* qd = qrows + row * HD + kc;
+                        *reinterpret_cast<uint32_t*>(qd) = y.x;
+                        *reinterpret_cast<uint32_t*>(qd + HD / 2) = y.y;
                     }
                 }
                 // q first: the consumers need it where the unit starts, the
@@ -957,9 +1044,14 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                 if (pos >= 0) {
                     if (klane) {
                         uint32_t yl, yh;
-                        rotate_word(kl, kh, c4, yl, yh);
+                        const bool kneed = rotate_word_fast(kl, kh, c4, yl, yh);
                         *reinterpret_cast<uint32_t*>(krow + kc) = yl;
                         *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = yh;
+                        if (kneed) {  // rare: the exact route over it
+                            const uint2 y = rotate_word_exact(kl, kh, c4);
+                            *reinterpret_cast<uint32_t*>(krow + kc) = y.x;
+                            *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = y.y;
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < kVW; ++j)
@@ -1409,14 +1501,17 @@ int max_grid(const mi_dims& D) {
     return g;
 }
 
-// Workspace: [unit counter words, one per CTA | partial slots, two per CTA].
-// A word carries the epoch of the call that wrote it and is zeroed by the
-// unit's last piece, so nothing needs clearing between calls and a captured
-// launch can be replayed with its one epoch.
+// Unit counter words, one per CTA. A word carries the epoch of the call that
+// wrote it and is zeroed by the unit's last piece, so nothing needs clearing
+// between calls and a captured launch can be replayed with its one epoch.
 size_t word_bytes(int grid) { return (((size_t)grid * 8) + 255) / 256 * 256; }
 
+size_t partial_bytes(const mi_dims& D, int grid) { return (size_t)grid * 2 * (size_t)slot_floats(D) * sizeof(float); }
+
+// Workspace: [unit counter words | partial slots | plan entries, one per CTA
+// (none for batches above kPlanMaxB)].
 size_t workspace_for(const mi_dims& D, int grid) {
-    return word_bytes(grid) + (size_t)grid * 2 * (size_t)slot_floats(D) * sizeof(float);
+    return word_bytes(grid) + (partial_bytes(D, grid) + 127) / 128 * 128 + (size_t)grid * plan_stride_for(D.B);
 }
 
 // A distinct value per call (in this process): a random start, then a
@@ -1540,6 +1635,11 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.out = static_cast<uint16_t*>(out);
     p.unit_word = static_cast<unsigned long long*>(workspace);
     p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + word_bytes(gmax));
+    p.plan_stride = plan_stride_for(D.B);
+    p.plan_cache = p.plan_stride > 0 ? static_cast<uint8_t*>(workspace) + word_bytes(gmax) +
+                                           (partial_bytes(D, gmax) + 127) / 128 * 128
+                                     : nullptr;
+    p.plan_kind = var * 2 + (step ? 1 : 0);
     p.epoch = next_epoch();
     p.dev_err = dev_err;
     p.B = D.B;

@@ -40,36 +40,46 @@ __device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double 
 // precision when that decides it. q = RN(c*d) and its rounding error qe (an
 // fma recovers it exactly above the underflow range) give c*d = q + qe; the
 // fma s = RN(a*b + q) rounds the exact a*b + q once, so |exact - s| <=
-// ulp(s)/2 + |qe|. When no bf16 rounding boundary (a midpoint between
-// neighbouring bf16 values, or one across a binade below) lies within that
-// bound plus the double rounding's 2^-50 |s| of s, the answer is RN_bf16(s).
-// Otherwise (a boundary within reach, zero, tiny, infinite or NaN values)
-// `slow` is set and the caller takes the double-precision route. Returns s;
-// the caller rounds pairs of them to bf16 with the hardware conversion (the
-// same nearest-even result for the finite, normal s this path keeps).
-// The _rn intrinsics keep the compiler from contracting c*d into an fma,
-// which would break the split.
+// |qe| + ulp(s)/2. The decision is taken on the bit patterns alone:
+//  * s sits L = (its low 16 bits) fp32 ulps above the bf16 value below it,
+//    so the nearest bf16 rounding boundary (the midpoint at L = 0x8000, the
+//    next one up at 0x18000, and, across the binade edge below, the one at
+//    -0x4000) is dist = min(|L - 0x8000|, L + 0x4000, 0x18000 - L) ulps away;
+//  * |qe| < 2^(e(qe) - e(s) + 24) ulp(s) from the biased exponents;
+//  * so no boundary lies within reach when dist >= 2 (|qe| below an ulp) or
+//    dist >= 2^k + 2 (k = e(qe) - e(s) + 24 >= 0), which also leaves room
+//    for the double rounding's 2^-53 relative.
+// Otherwise (a boundary within reach, s zero, tiny (below 2^-100), infinite
+// or NaN, q tiny but not zero) `slow` is set and the caller takes the
+// double-precision route. Returns s; the caller rounds pairs of them to bf16
+// with the hardware conversion (the same nearest-even result for the
+// finite, normal s this path keeps). The _rn intrinsics keep the compiler
+// from contracting c*d into an fma, which would break the split. (The same
+// test written with float products, a conversion of dist and float
+// compares took ~40 times longer per word.)
 __device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bool& slow) {
     const float q = __fmul_rn(c, d);
     const float qe = fmaf(c, d, -q);
     const float s = fmaf(a, b, q);
-    const uint32_t S = __float_as_uint(fabsf(s));
+    const uint32_t S = __float_as_uint(s) & 0x7FFFFFFFu;
+    const uint32_t Q = __float_as_uint(q) & 0x7FFFFFFFu;
+    const int es = (int)(S >> 23), eq = (int)(Q >> 23);
+    const int eqe = max((int)((__float_as_uint(qe) & 0x7FFFFFFFu) >> 23), 1);
     const int L = (int)(S & 0xFFFFu);
-    const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L) - 2;
-    const float ulp = __uint_as_float((S & 0x7F800000u) - (23u << 23));
-    const float err = __fadd_rn(__fadd_rn(__fmul_rn(fabsf(qe), 1.0001f), __fmul_rn(fabsf(s), 0x1p-50f)),
-                                __fmul_rn(ulp, 0.5f));
-    const float tiny = 0x1p-100f;
-    const bool ok = isfinite(s) && (q == 0.f || fabsf(q) >= tiny) && fabsf(s) >= tiny &&
-                    err < __fmul_rn((float)dist, ulp);
+    const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L);
+    const int k = eqe - es + 24;
+    const int need = k < 0 ? 2 : (k < 16 ? (1 << k) + 2 : 0x20000);
+    const bool ok = es >= 27 && es <= 254 && (Q == 0u || eq >= 27) && dist >= need;
     slow |= !ok;
     return s;
 }
 
-// The double-precision route of rotate_word: the exact products and one
-// double rounding decide the bits. Kept out of line: it is rarely taken, and
-// inlined into every unrolled rotation it would make the code several times
-// larger (cold instruction fetches then dominate a short kernel's start).
+// The double-precision route of a rotated word: the exact products and one
+// double rounding decide the bits. Out of line and called only from a
+// separate pass after a caller's rotation loop (rotate_word_fast flags the
+// words that need it): a call site inside the loop, even untaken, cost ~650
+// cycles per word, and the route inlined there made the code several times
+// larger.
 static __device__ __noinline__ uint2 rotate_word_exact(uint32_t xl, uint32_t xh, float4 cs) {
     const double a0 = bf16_bits_to_f64(xl & 0xFFFFu), a1 = bf16_bits_to_f64(xl >> 16);
     const double b0 = bf16_bits_to_f64(xh & 0xFFFFu), b1 = bf16_bits_to_f64(xh >> 16);
@@ -83,7 +93,11 @@ static __device__ __noinline__ uint2 rotate_word_exact(uint32_t xl, uint32_t xh,
 // the second half (hi) of a head, two adjacent pairs per word:
 // ylo = x_lo * cos - x_hi * sin, yhi = x_hi * cos + x_lo * sin,
 // cs = (cos, sin) of pair 2j and (cos, sin) of pair 2j + 1.
-__device__ __forceinline__ void rotate_word(uint32_t xl, uint32_t xh, float4 cs, uint32_t& yl, uint32_t& yh) {
+// Single precision only; returns true when one of the four values needs
+// the exact route, in which case the caller replaces (yl, yh) by
+// rotate_word_exact(xl, xh, cs).
+__device__ __forceinline__ bool rotate_word_fast(uint32_t xl, uint32_t xh, float4 cs, uint32_t& yl,
+                                                 uint32_t& yh) {
     const float fa0 = bf16_lo(xl), fa1 = bf16_hi(xl);
     const float fb0 = bf16_lo(xh), fb1 = bf16_hi(xh);
     bool slow = false;
@@ -93,12 +107,7 @@ __device__ __forceinline__ void rotate_word(uint32_t xl, uint32_t xh, float4 cs,
     const float s3 = rot_fast(fb1, cs.z, fa1, cs.w, slow);
     yl = pack_bf16x2(s0, s1);
     yh = pack_bf16x2(s2, s3);
-    if (slow) {
-        // rare: the exact products and one double rounding decide it
-        const uint2 y = rotate_word_exact(xl, xh, cs);
-        yl = y.x;
-        yh = y.y;
-    }
+    return slow;
 }
 
 }  // namespace mi
