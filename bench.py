@@ -129,11 +129,11 @@ def prefill_flops(w, hist, new):
 
 
 def kernel_source_hash():
-    """Hash of the attention kernel's sources with comments and whitespace
-    removed, so that a recorded traffic figure stays valid across comment
+    """Hash of the attention kernel's sources (decode.cu and the headers it
+    includes) with comments and whitespace removed, so that a recorded traffic figure stays valid across comment
     edits and is dropped as soon as any code changes."""
     h = hashlib.sha256()
-    for f in ("decode.cu", "common.cuh", "tma.cuh"):
+    for f in ("decode.cu", "common.cuh", "tma.cuh", "rope.cuh"):
         with open(os.path.join(ROOT, "paged_kv_decode_25_gb300", "csrc", f), encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
