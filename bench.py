@@ -15,7 +15,10 @@ metadata, H2D of metadata and new q/k/v from pinned memory, 36 layers, D2H of
 the outputs. ``roofline`` = the attention call (split-KV kernel + LSE combine)
 against the measured HBM copy bandwidth (one kernel per layer: the log-sum-exp
 combine of split units runs inside it). ``cpu_baseline`` = the fp64 oracle on
-the host cores on a bounded sample.
+the host cores on a bounded sample. The default run adds ``per_config`` (the
+Qwen3-1.7B layer, the Qwen2.5-7B 128-step sweep and the skewed batch, each
+with the oracle on the host cores) and ``per_variant.fp8`` (the same step
+over e4m3 caches, run as ``--kv fp8`` in a child process).
 
 ``--impl reference`` times the oracle alone (the reference arm).
 """
@@ -99,6 +102,27 @@ def describe(w):
             "pool": "fragmented by seeded alloc/free churn" if w.churn else "seeded permutation",
             "l2": "no flush: every layer reads its own K/V (> L2) once per step",
             "parallelism": "replicas"}
+
+
+def fp8_variant_record(args):
+    """The same serving step over e4m3 caches (the fused e4m3 decode step),
+    run as `bench.py --kv fp8` in a child process with this run's steps and
+    warm-up; its headline figures, for the default line."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--kv", "fp8", "--steps", str(args.steps), "--warmup",
+           str(args.warmup), "--no-cpu-baseline", "--e2e-steps", "3"]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")][-1]
+        d = json.loads(line)
+    except Exception as e:  # reported, not fatal: the bf16 line stands on its own
+        return {"unavailable": ("%s: %s" % (type(e).__name__, e))[:200]}
+    rf = d["roofline"]
+    return {"metric": d["metric"], "value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+            "steps_per_s": d["steps_per_s"], "dtype": d["dtype"], "kv_cache": d["config"]["kv_cache"],
+            "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel",
+                                            "avg_launch_ms", "avg_launch_source")},
+            "per_layer_ms": d["per_layer_ms"], "e2e": d["e2e"], "clocks": d["clocks"],
+            "command": " ".join(["python", "bench.py"] + cmd[2:])}
 
 
 def arm_config(w, args):
@@ -1009,6 +1033,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default: the workload's); fewer only for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-variant", action="store_true",
+                    help="skip the e4m3-cache run of the same step in the default line")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other workloads' records (Qwen3-1.7B layer, Qwen2.5-7B sweep, skewed batch)")
     args = ap.parse_args()
@@ -1088,10 +1114,10 @@ def main():
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = stream0 = torch.cuda.current_stream(device)
 
-    # bf16 caches on the MMA tile: the fused step (append + attention in one
-    # launch per layer) is the timed path; the two calls are timed after it
-    # to report append and attention separately
-    fused = (not fp8) and variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA) and not args.unfused
+    # the fused step (append + attention in one launch per layer; bf16 caches
+    # on the MMA tile, or e4m3 caches) is the timed path; the two calls are
+    # timed after it to report append and attention separately
+    fused = (fp8 or variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA)) and not args.unfused
 
     def step(ev=None, fuse=False, st=None):
         stream = st if st is not None else stream0
@@ -1100,9 +1126,15 @@ def main():
             if fuse:
                 if ev is not None:
                     ev[layer][0].record(stream)
-                mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos, bt_d,
-                                                 cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
-                                                 dev_err=err, stream=stream), "decode step")
+                if fp8:
+                    mi.check(mi.mi_paged_decode_step_fp8(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos,
+                                                         bt_d, cl_d, ks_d, vs_d, w.scale, qo_all[layer], kc, vc,
+                                                         out_all[layer], ws, dev_err=err, stream=stream),
+                             "decode step (e4m3)")
+                else:
+                    mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos,
+                                                     bt_d, cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
+                                                     dev_err=err, stream=stream), "decode step")
                 if ev is not None:
                     ev[layer][1].record(stream)
                 continue
@@ -1320,6 +1352,9 @@ def main():
     per_config = None
     if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_config:
         per_config = measure_configs(mi, device, peak)
+    per_variant = None
+    if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_variant:
+        per_variant = {"fp8": fp8_variant_record(args)}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": median_step_ms,
@@ -1334,8 +1369,8 @@ def main():
                          "append_bytes": append_bytes(w, kvb), "attention_bytes": a_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": ("fused decode step (RoPE + cache write of the new token, split-KV attention, "
-                                "LSE combine), per layer" if fused else
+                     "kernel": ("fused decode step (RoPE + cache write of the new token%s, split-KV attention, "
+                                "LSE combine), per layer" % (" quantised to e4m3" if fp8 else "") if fused else
                                 "paged decode attention (split-KV kernel with the LSE combine of cut units fused), "
                                 "per layer"),
                      "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": kern_avg_ms,
@@ -1347,6 +1382,7 @@ def main():
                          + ("the timed region's one-step CUDA graph" if launch_mode.startswith("cuda graph")
                             else "stream launches") + ", D2H of every layer's output, synchronise")},
         "per_config": per_config,
+        "per_variant": per_variant,
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention
         "launch": launch_mode,
         "graph_with_kernel_events": graph_events,

@@ -324,7 +324,7 @@ mi_status mi_paged_decode_attention_variant(const mi_dims* dims, const void* q,
  * quotient is an IEEE single-precision division, and e4m3() rounds to nearest
  * with ties to even, values beyond +-448 saturating to +-448. A scale that is
  * not a positive finite number skips that head's cache writes
- * (MI_DEVERR_BAD_SCALE). */
+ * (MI_DEVERR_BAD_SCALE; a bad V scale likewise skips its V rows). */
 mi_status mi_paged_kv_append_fp8(const mi_dims* dims, const void* q, const void* k, const void* v,
                                  const int32_t* positions, const int32_t* slot_mapping,
                                  const float* rope_cos_sin, int32_t max_pos, void* q_out, void* k_cache,
@@ -342,6 +342,23 @@ mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, cons
                                         const int32_t* block_tables, const int32_t* context_lens,
                                         float scale, void* out, void* workspace, size_t workspace_bytes,
                                         int32_t* dev_err, mi_stream_t stream);
+
+/* One decode step of a layer over FP8 caches in one launch: exactly
+ * mi_paged_kv_append_fp8 with positions[b] = n - 1 and slot_mapping[b] =
+ * block_tables[b][(n-1)/16] * 16 + (n-1) % 16 (n = context_lens[b], the
+ * length after the append), followed by mi_paged_decode_attention_fp8 on its
+ * outputs; q_out and the new cache rows (quantised as the FP8 append
+ * quantises them) get the same bits as those two calls, and out is within
+ * the attention's fp32 rounding of theirs (this kernel runs two CTAs per SM
+ * where the e4m3 attention runs three, so the split differs). A K
+ * or V scale that is not a positive finite number leaves that row of the
+ * cache as it was (MI_DEVERR_BAD_SCALE). Other arguments, errors and
+ * guarantees as mi_paged_decode_step; q must not overlap q_out. */
+mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                   const float* rope_cos_sin, int32_t max_pos, const int32_t* block_tables,
+                                   const int32_t* context_lens, const float* k_scale, const float* v_scale,
+                                   float scale, void* q_out, void* k_cache, void* v_cache, void* out,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream);
 
 /* Causal paged GQA attention for a prefill or chunked-prefill batch (NJU
  * course brief §2.1, the prefill stage of the prefill + decode loop; mini-infer

@@ -41,7 +41,7 @@ EXPORTS = (
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
     "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
     "mi_paged_prefill_attention", "mi_paged_prefill_attention_variant", "mi_paged_decode_attention_noalloc",
-    "mi_paged_decode_step", "mi_test_set_wait_limit", "mi_test_withhold_copy",
+    "mi_paged_decode_step", "mi_paged_decode_step_fp8", "mi_test_set_wait_limit", "mi_test_withhold_copy",
 )
 MI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -99,6 +99,8 @@ def load():
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
             "mi_paged_decode_step": (
                 [dims_p, P, P, P, P, i32, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
+            "mi_paged_decode_step_fp8": (
+                [dims_p, P, P, P, P, i32, P, P, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
             "mi_test_set_wait_limit": ([ctypes.c_int64], i32),
             "mi_test_withhold_copy": ([i32], i32),
         }
@@ -397,6 +399,16 @@ def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tabl
     return load().mi_paged_decode_attention_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                     _ptr(block_tables), _ptr(context_lens), float(scale),
                                                     _ptr(out), _ptr(dev_err), _stream(stream))
+
+
+def mi_paged_decode_step_fp8(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, k_scale,
+                             v_scale, scale, q_out, k_cache, v_cache, out, workspace, workspace_bytes=None,
+                             dev_err=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return load().mi_paged_decode_step_fp8(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
+                                           int(max_pos), _ptr(block_tables), _ptr(context_lens), _ptr(k_scale),
+                                           _ptr(v_scale), float(scale), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream))
 
 
 def mi_test_set_wait_limit(ns):

@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(128) append_kernel(AppendParams a, int B) {
     const long long row = (((long long)(slot / kBlock) * a.Hkv + h) * kBlock + slot % kBlock) * a.d;
     if (FP8) {
         const float vs = a.v_scale[h];
-        if (!scale_ok(vs)) return;  // reported by the key threads
+        if (!scale_ok(vs)) {
+            if (ch == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SCALE);
+            return;
+        }
         const uint32_t x[4] = {val.x, val.y, val.z, val.w};
         reinterpret_cast<uint2*>(a.v_cache8 + row)[ch] = quantize8(x, vs);
     } else {

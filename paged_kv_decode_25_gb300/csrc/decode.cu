@@ -64,6 +64,9 @@ constexpr int kUnitCostBf16 = 6;
 constexpr long long kMinBlocksPerCta = 12;
 constexpr float kNegInf = -INFINITY;
 
+// An e4m3 scale the FP8 append accepts: positive and finite.
+__device__ __forceinline__ bool fp8_scale_ok(float s) { return s > 0.f && s <= 3.0e38f; }
+
 struct AttnParams {
     const uint16_t* q;             // [B][Hq][HD]
     const int32_t* block_tables;   // [B][mbps]
@@ -423,7 +426,8 @@ struct MmaState {
 
     // The fused decode step: q of the unit's heads from rotated rows [G][HD]
     // bf16 in shared memory (the RoPE warp's ring slot).
-    __device__ __forceinline__ void begin_unit_from(const uint16_t* qrows, const AttnParams& p, int lane) {
+    __device__ __forceinline__ void begin_unit_from(const uint16_t* qrows, const AttnParams& p, int /*h*/,
+                                                    int lane) {
         const int n = lane >> 2;
         const bool ok = n < p.G;
         const uint16_t* qrow = qrows + (ok ? n : 0) * HD;
@@ -557,6 +561,26 @@ struct Fp8State {
             const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c)) : make_uint2(0, 0);
             qb[kk][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));  // dims 4c, 4c+1
             qb[kk][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));  // dims 4c+2, 4c+3
+        }
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
+        sl2 = p.sl2 * __ldg(p.k_scale + h);
+        vsc = __ldg(p.v_scale + h);
+    }
+
+    // The fused decode step: q of the unit's heads from rotated rows [G][HD]
+    // bf16 in shared memory (the RoPE warp's ring slot), in the same order.
+    __device__ __forceinline__ void begin_unit_from(const uint16_t* qrows, const AttnParams& p, int h, int lane) {
+        const int n = lane >> 2, c = lane & 3;
+        const bool ok = n < p.G;
+        const uint16_t* qrow = qrows + (ok ? n : 0) * HD;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const uint2 w = ok ? *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c) : make_uint2(0, 0);
+            qb[kk][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+            qb[kk][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
         }
 #pragma unroll
         for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -849,10 +873,10 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // consumer warp that streams that block copies the two rows into its staged
 // tiles.
 template <int HD, int VAR, int GP, int W, bool FUSED = false>
-__global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3 : 2)
+__global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && !FUSED ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
-    static_assert(!FUSED || VAR == kVarMma, "the fused step runs the MMA tile");
+    static_assert(!FUSED || VAR == kVarMma || VAR == kVarFp8, "the fused step runs the MMA or e4m3 tile");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
@@ -1041,22 +1065,50 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                 // new token's rows only at its last block
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qfull0 + slot * 8);
+                // e4m3 caches: the rows are stored quantised with the head's
+                // scales, as the FP8 append stores them; a row whose scale is
+                // not a positive finite number is not written (a flag word in
+                // the slot tells the consumers which rows to place)
+                bool k_ok = true, v_ok = true;
+                float ks = 1.f, vs = 1.f;
+                if constexpr (VAR == kVarFp8) {
+                    ks = __ldg(p.k_scale + cu.h);
+                    vs = __ldg(p.v_scale + cu.h);
+                    k_ok = fp8_scale_ok(ks);
+                    v_ok = fp8_scale_ok(vs);
+                    if (pos >= 0 && !(k_ok && v_ok) && lane == 0) raise_err(p.dev_err, MI_DEVERR_BAD_SCALE);
+                }
                 if (pos >= 0) {
                     if (klane) {
                         uint32_t yl, yh;
-                        const bool kneed = rotate_word_fast(kl, kh, c4, yl, yh);
-                        *reinterpret_cast<uint32_t*>(krow + kc) = yl;
-                        *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = yh;
-                        if (kneed) {  // rare: the exact route over it
+                        if (rotate_word_fast(kl, kh, c4, yl, yh)) {  // rare: the exact route
                             const uint2 y = rotate_word_exact(kl, kh, c4);
-                            *reinterpret_cast<uint32_t*>(krow + kc) = y.x;
-                            *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = y.y;
+                            yl = y.x;
+                            yh = y.y;
+                        }
+                        if constexpr (VAR == kVarFp8) {
+                            uint8_t* k8 = reinterpret_cast<uint8_t*>(krow);
+                            *reinterpret_cast<uint16_t*>(k8 + kc) =
+                                (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(yl), ks), __fdiv_rn(bf16_hi(yl), ks));
+                            *reinterpret_cast<uint16_t*>(k8 + kc + HD / 2) =
+                                (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(yh), ks), __fdiv_rn(bf16_hi(yh), ks));
+                        } else {
+                            *reinterpret_cast<uint32_t*>(krow + kc) = yl;
+                            *reinterpret_cast<uint32_t*>(krow + kc + HD / 2) = yh;
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < kVW; ++j)
-                        *reinterpret_cast<uint32_t*>(vrow + 2 * lane + 64 * j) = vv[j];
+                    for (int j = 0; j < kVW; ++j) {
+                        if constexpr (VAR == kVarFp8) {
+                            *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(vrow) + 2 * lane + 64 * j) =
+                                (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(vv[j]), vs), __fdiv_rn(bf16_hi(vv[j]), vs));
+                        } else {
+                            *reinterpret_cast<uint32_t*>(vrow + 2 * lane + 64 * j) = vv[j];
+                        }
+                    }
                 }
+                if (VAR == kVarFp8 && lane == 0)
+                    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(krow) + HD) = (k_ok ? 1u : 0u) | (v_ok ? 2u : 0u);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(kvfull0 + slot * 8);
                 if (pos >= 0) {
@@ -1068,9 +1120,22 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                         const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + jnew);
                         if (blk >= 0 && blk < p.num_blocks) {
                             const long long rofs = (((long long)blk * p.Hkv + cu.h) * kBlock + pos % kBlock) * HD;
-                            for (int k = 2 * lane; k < HD; k += 64) {
-                                *reinterpret_cast<uint32_t*>(p.kc + rofs + k) = *reinterpret_cast<const uint32_t*>(krow + k);
-                                *reinterpret_cast<uint32_t*>(p.vc + rofs + k) = *reinterpret_cast<const uint32_t*>(vrow + k);
+                            if constexpr (VAR == kVarFp8) {
+                                uint8_t* kc8 = reinterpret_cast<uint8_t*>(p.kc);
+                                uint8_t* vc8 = reinterpret_cast<uint8_t*>(p.vc);
+                                for (int k = 4 * lane; k < HD; k += 128) {
+                                    if (k_ok)
+                                        *reinterpret_cast<uint32_t*>(kc8 + rofs + k) =
+                                            *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(krow) + k);
+                                    if (v_ok)
+                                        *reinterpret_cast<uint32_t*>(vc8 + rofs + k) =
+                                            *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(vrow) + k);
+                                }
+                            } else {
+                                for (int k = 2 * lane; k < HD; k += 64) {
+                                    *reinterpret_cast<uint32_t*>(p.kc + rofs + k) = *reinterpret_cast<const uint32_t*>(krow + k);
+                                    *reinterpret_cast<uint32_t*>(p.vc + rofs + k) = *reinterpret_cast<const uint32_t*>(vrow + k);
+                                }
                             }
                         }
                         uint16_t* qo = p.q_out + ((long long)cu.b * p.Hq + (long long)cu.h * p.G) * HD;
@@ -1188,7 +1253,7 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                 if (lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             }
             qslot = reinterpret_cast<const uint16_t*>(base + sp.qring) + slot * (p.G + 2) * HD;
-            st.begin_unit_from(qslot, p, lane);
+            st.begin_unit_from(qslot, p, cu.h, lane);
         } else {
             st.begin_unit(p, cu.b, cu.h, lane);
         }
@@ -1227,9 +1292,21 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 ? 3
                         }
                         const uint16_t* krow = qslot + p.G * HD;
                         const uint16_t* vrow = krow + HD;
-                        for (int i = 2 * lane; i < HD; i += 64) {
-                            sts32(kt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(krow + i));
-                            sts32(vt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(vrow + i));
+                        if constexpr (VAR == kVarFp8) {
+                            const uint8_t* k8 = reinterpret_cast<const uint8_t*>(krow);
+                            const uint8_t* v8 = reinterpret_cast<const uint8_t*>(vrow);
+                            const uint32_t which = *reinterpret_cast<const uint32_t*>(k8 + HD);
+                            for (int i = 4 * lane; i < HD; i += 128) {
+                                if (which & 1u)
+                                    sts32(kt + swz8<HD>(row, i >> 4) + (i & 15), *reinterpret_cast<const uint32_t*>(k8 + i));
+                                if (which & 2u)
+                                    sts32(vt + swz8<HD>(row, i >> 4) + (i & 15), *reinterpret_cast<const uint32_t*>(v8 + i));
+                            }
+                        } else {
+                            for (int i = 2 * lane; i < HD; i += 64) {
+                                sts32(kt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(krow + i));
+                                sts32(vt + swz<HD>(row, i >> 3) + (i & 7) * 2, *reinterpret_cast<const uint32_t*>(vrow + i));
+                            }
                         }
                         __syncwarp();
                     }
@@ -1394,7 +1471,7 @@ constexpr int kSmemThreePerSm = 76800;    // per CTA so that three fit
 int pick_stages(int HD, int G, int var, bool fused = false) {
     const bool fma = var == kVarFma;
     const int eb = elem_bytes(var), top = kMaxStages * 2 / eb;
-    if (var == kVarFp8)
+    if (var == kVarFp8 && !fused)
         for (int S = top; S >= 2; --S)
             if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemThreePerSm) return S;
     for (int S = top; S >= 1; --S)
@@ -1596,7 +1673,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     if (ctas < 0 || !std::isfinite(scale)) return MI_ERR_INVALID_ARG;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     if (step) {
-        if (var != kVarMma || !step->k || !step->v || !step->rope || !step->q_out || step->max_pos < 1)
+        if ((var != kVarMma && var != kVarFp8) || !step->k || !step->v || !step->rope || !step->q_out ||
+            step->max_pos < 1)
             return MI_ERR_INVALID_ARG;
         if (!aligned16(step->k) || !aligned16(step->v) || !aligned16(step->rope) || !aligned16(step->q_out))
             return MI_ERR_INVALID_ARG;
@@ -1616,8 +1694,11 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     const int gmax = max_grid(D);
     if (gmax <= 0) return MI_ERR_CUDA;
     if (workspace_bytes < workspace_for(D, gmax)) return MI_ERR_INVALID_ARG;
-    KernelFn fn = step ? (HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps, true> : attn_kernel<128, kVarMma, 8, kWarps, true>)
-                       : pick_kernel(HD, var, G);
+    KernelFn fn = !step ? pick_kernel(HD, var, G)
+                : var == kVarFp8 ? (HD == 64 ? attn_kernel<64, kVarFp8, 8, kWarps, true>
+                                             : attn_kernel<128, kVarFp8, 8, kWarps, true>)
+                                 : (HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps, true>
+                                             : attn_kernel<128, kVarMma, 8, kWarps, true>);
     const int gown = grid_for(fn, smem, threads);
     if (gown <= 0 || gown > gmax) return MI_ERR_CUDA;
     const int grid = ctas > 0 && ctas < gown ? ctas : gown;
@@ -1698,6 +1779,18 @@ extern "C" mi_status mi_paged_decode_step(const mi_dims* dims, const void* q, co
     const StepArgs step{k, v, rope_cos_sin, max_pos, q_out};
     return attention(dims, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale, out,
                      workspace, workspace_bytes, dev_err, stream, kVarMma, 0, &step);
+}
+
+extern "C" mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                            const float* rope_cos_sin, int32_t max_pos,
+                                            const int32_t* block_tables, const int32_t* context_lens,
+                                            const float* k_scale, const float* v_scale, float scale, void* q_out,
+                                            void* k_cache, void* v_cache, void* out, void* workspace,
+                                            size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream) {
+    using namespace mi;
+    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out};
+    return attention(dims, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, dev_err, stream, kVarFp8, 0, &step);
 }
 
 extern "C" mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, const void* k_cache,
