@@ -394,11 +394,15 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
  *   MI_PREFILL_TCGEN05  fifth-generation tensor cores (tcgen05.mma with
  *                       tensor-memory accumulators; 128 / G whole tokens,
  *                       i.e. (128 / G) * G rows, per CTA; any G up to 8).
- * MI_PREFILL_DEFAULT takes the tcgen05 kernel. Both compute the same
+ *   MI_PREFILL_TCGEN05_PAIR  tcgen05 with two 128-row Q tiles per CTA
+ *                       (one CTA per SM) sharing 128-key K / V stages,
+ *                       one issuing thread alternating the tiles.
+ * MI_PREFILL_DEFAULT takes the tcgen05 kernel. All compute the same
  * definition within the same tolerance. */
 #define MI_PREFILL_DEFAULT 0
 #define MI_PREFILL_MMA 1
 #define MI_PREFILL_TCGEN05 2
+#define MI_PREFILL_TCGEN05_PAIR 3
 mi_status mi_paged_prefill_attention_variant(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
                                              const void* q, const void* k_cache, const void* v_cache,
                                              const int32_t* block_tables, const int32_t* context_lens,

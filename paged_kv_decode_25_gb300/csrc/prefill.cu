@@ -847,6 +847,399 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
 }
 
+// ----------------------------------------- tcgen05 prefill, two Q tiles --
+//
+// One CTA per SM holds two 128-row Q tiles of the same (request, KV head)
+// (the second tile's rows are later positions) and streams 128-key stages
+// that both tiles consume, so each K / V byte is staged once for 256 rows and
+// each S = Q . K^T instruction is 128 x 128 (half the Q operand traffic per
+// key of a 128 x 64 one). Tensor memory (512 columns): O_t at 256 t, S_t at
+// 256 t + 128 (P_t, the bf16 probabilities, over the first 64 of its
+// columns). One thread issues every MMA, alternating the tiles so that one
+// tile's softmax runs under the other tile's MMAs:
+//   S_0(0), S_1(0); for each stage j: O_0 += P_0(j) V(j), S_0(j+1),
+//   O_1 += P_1(j) V(j), S_1(j+1).
+// S_t(j+1) overwrites P_t(j) after O_t += P_t(j) V(j) has read it: MMAs one
+// thread issues run in issue order. Warps 0-3 (tile 0) and 4-7 (tile 1) run
+// the softmax of their tile (thread = row = tensor-memory lane, 128 scores
+// per stage in registers); warp 8 issues the MMAs and owns the tensor
+// memory; warp 9 loads Q once and streams K and V (two stages each, K of
+// stage j before V of stage j - 1).
+
+constexpr int kT2Keys = 128;                 // keys per stage
+constexpr int kT2Blocks = kT2Keys / kBlock;  // 16-token blocks per stage
+constexpr int kT2Threads = 320;
+constexpr uint32_t kT2Cols = 512;
+
+template <int HD>
+struct Tc2Smem {
+    static constexpr int kH = HD / 64;
+    static constexpr int kQT = kH * kTcRows * 128;            // one Q tile: kH x [128 rows][128 B]
+    static constexpr int kKV = kH * kT2Keys * 128;            // one K (or V) stage: kH x [128 keys][128 B]
+    static constexpr int kQ = 0;
+    static constexpr int kRingK = kQ + 2 * kQT;
+    static constexpr int kRingV = kRingK + 2 * kKV;
+    static constexpr int kBar = kRingV + 2 * kKV;
+    // q_full, k_full[4], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin
+    static constexpr int kNBar = 1 + 4 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    static constexpr int kMask = kBar + kNBar * 8;
+    static constexpr int kTmem = kMask + 4 * 4;
+    static constexpr int kTotal = kTmem + 16 + 1024;  // slack to align the base to 1024 B
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kT2Threads, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, PrefillParams p) {
+    using SM = Tc2Smem<HD>;
+    constexpr int kH = SM::kH;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    pdl_wait();
+    pdl_trigger();
+
+    // a Q tile holds whole tokens: 128 / G of them, G rows each; the CTA's
+    // two tiles are consecutive, tr rows apart
+    const int tr = (kTcRows / p.G) * p.G;
+    Item it;
+    if (!work_item(p, 2 * tr, it)) return;
+    const int nst = (it.nblk + kT2Blocks - 1) / kT2Blocks;
+    const uint32_t bar = sbase + SM::kBar;
+    const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 32, v_full0 = k_empty0 + 16;
+    const uint32_t v_empty0 = v_full0 + 16, s_full0 = v_empty0 + 16, p_full0 = s_full0 + 16;
+    const uint32_t o_done0 = p_full0 + 16, fin = o_done0 + 16;
+    const uint32_t mask0 = sbase + SM::kMask;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(k_full0 + i * 8, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(k_empty0 + i * 8, 1);
+            mbar_init(v_full0 + i * 8, 1);
+            mbar_init(v_empty0 + i * 8, 1);
+            mbar_init(s_full0 + i * 8, 1);
+            mbar_init(p_full0 + i * 8, 128);
+            mbar_init(o_done0 + i * 8, 1);
+        }
+        mbar_init(fin, 1);
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tc::alloc(sbase + SM::kTmem, kT2Cols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tbase = lds_u32(sbase + SM::kTmem);
+
+    if (warp == 9) {
+        // ------------------------------------------------ producer warp --
+        const uint64_t policy = l2_policy_evict_normal();
+        if (lane == 0 && nst > 0) {
+            mbar_arrive_expect_tx(q_full, 2u * kH * (uint32_t)tr * 128u);
+            for (int t = 0; t < 2; ++t)
+                for (int hh = 0; hh < kH; ++hh)
+                    tma_load_4d(sbase + SM::kQ + t * SM::kQT + hh * kTcRows * 128, &tmq, q_full, 0, hh, it.h * p.G,
+                                it.q0 + (it.rho0 + t * tr) / p.G, policy);
+        }
+        int pblk = -1;
+        bool pok = false;
+        auto load_v = [&](int jv) -> bool {
+            const int sl = jv & 1, u = jv >> 1;
+            if (!wait_all(v_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1), p.wait_ns)) return false;
+            const uint32_t msk = __ballot_sync(0xffffffffu, pok);
+            const uint32_t fb = v_full0 + sl * 8;
+            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
+            __syncwarp();
+            if (pok) {
+                const uint32_t vd = sbase + SM::kRingV + sl * SM::kKV + lane * kBlock * 128;
+                const int row0 = (pblk * p.Hkv + it.h) * kBlock;
+                for (int hh = 0; hh < kH; ++hh) tma_load_3d(vd + hh * kT2Keys * 128, &tmv, fb, 0, hh, row0, policy);
+            }
+            return true;
+        };
+        bool pgood = true;
+        for (int j = 0; j < nst; ++j) {
+            const int sl = j & 1, u = j >> 1;
+            if (!wait_all(k_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1), p.wait_ns)) {
+                pgood = false;
+                break;
+            }
+            const int x = j * kT2Blocks + lane;
+            int blk = -1;
+            bool ok = false;
+            if (lane < kT2Blocks && x < it.nblk) {
+                blk = __ldg(p.block_tables + (long long)it.r * p.mbps + x);
+                ok = blk >= 0 && blk < p.num_blocks;
+                if (!ok) raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
+            }
+            const uint32_t msk = __ballot_sync(0xffffffffu, ok);
+            const uint32_t fb = k_full0 + (j & 3) * 8;
+            // failure-detection test: stage 0's K is neither copied nor
+            // announced, so every wait on it runs out
+            const bool held = p.withhold != 0 && j == 0;
+            if (lane == 0 && !held) {
+                sts32(mask0 + (j & 3) * 4, msk);
+                mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
+            }
+            __syncwarp();
+            if (ok && !held) {
+                const uint32_t kd = sbase + SM::kRingK + sl * SM::kKV + lane * kBlock * 128;
+                const int row0 = (blk * p.Hkv + it.h) * kBlock;
+                for (int hh = 0; hh < kH; ++hh) tma_load_3d(kd + hh * kT2Keys * 128, &tmk, fb, 0, hh, row0, policy);
+            }
+            if (j > 0 && !load_v(j - 1)) {
+                pgood = false;
+                break;
+            }
+            pblk = blk;
+            pok = ok;
+        }
+        if (pgood && nst > 0 && !load_v(nst - 1)) pgood = false;
+        if (!pgood && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+    } else if (warp == 8) {
+        // -------------------------------------------------- MMA issuer --
+        if (lane == 0 && nst > 0) {
+            constexpr uint32_t idS = tc::idesc_bf16(kTcRows, kT2Keys, false);
+            constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
+            auto issue_s = [&](int t, int j) {
+                const uint32_t kbase = sbase + SM::kRingK + (j & 1) * SM::kKV;
+                const uint32_t qbase = sbase + SM::kQ + t * SM::kQT;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;  // 16 bf16 of the 128-byte row
+                    const uint64_t a = tc::sdesc_sw128(qbase + (kk >> 2) * kTcRows * 128 + off, 16, 1024);
+                    const uint64_t bd = tc::sdesc_sw128(kbase + (kk >> 2) * kT2Keys * 128 + off, 16, 1024);
+                    tc::mma_ss(tbase + 256u * t + 128u, a, bd, idS, kk > 0);
+                }
+                tc::commit(s_full0 + t * 8);
+            };
+            auto issue_o = [&](int t, int j) {
+                const uint32_t vbase = sbase + SM::kRingV + (j & 1) * SM::kKV;
+                const uint32_t pcol = tbase + 256u * t + 128u;  // P_t(j): bf16 pairs over S_t's first 64 columns
+#pragma unroll
+                for (int l = 0; l < kT2Blocks; ++l) {
+                    const uint64_t bd = tc::sdesc_sw128(vbase + l * kBlock * 128, kT2Keys * 128, 1024);
+                    tc::mma_ts(tbase + 256u * t, pcol + 8u * l, bd, idO, j > 0 || l > 0);
+                }
+                tc::commit(o_done0 + t * 8);
+            };
+            bool ok = mbar_wait_bounded(q_full, 0, p.wait_ns) &&
+                      mbar_wait_bounded(k_full0, 0, p.wait_ns);
+            if (ok) {
+                tc::fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                tc::commit(k_empty0);  // K(0) read by both tiles
+            }
+            for (int j = 0; ok && j < nst; ++j) {
+                const uint32_t ph = (uint32_t)(j & 1);
+                ok = mbar_wait_bounded(p_full0, ph, p.wait_ns) &&
+                     mbar_wait_bounded(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns);
+                if (!ok) break;
+                tc::fence_after();
+                issue_o(0, j);
+                const bool more = j + 1 < nst;
+                if (more) {
+                    if (!(ok = mbar_wait_bounded(k_full0 + ((j + 1) & 3) * 8, (uint32_t)(((j + 1) >> 2) & 1),
+                                                 p.wait_ns)))
+                        break;
+                    tc::fence_after();
+                    issue_s(0, j + 1);
+                }
+                if (!(ok = mbar_wait_bounded(p_full0 + 8, ph, p.wait_ns))) break;
+                tc::fence_after();
+                issue_o(1, j);
+                tc::commit(v_empty0 + (j & 1) * 8);  // V(j) read by both tiles
+                if (more) {
+                    issue_s(1, j + 1);
+                    tc::commit(k_empty0 + ((j + 1) & 1) * 8);
+                }
+            }
+            if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            // every MMA issued has finished before tensor memory is released
+            tc::commit(fin);
+            (void)mbar_wait_bounded(fin, 0, drain_limit(p.wait_ns));
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- softmax ----
+        const int t = warp >> 2;                      // tile
+        const int rl = threadIdx.x & 127;             // row of the tile, tensor-memory lane
+        const int rr = it.rho0 + t * tr + rl;         // row of the request
+        const bool vrow = rl < tr && rr < it.nrows;
+        const int tok = rr / p.G;
+        const int pos = vrow ? it.first + tok : it.p_hi;
+        const int mpos = pos < 0 ? 0 : pos;
+        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + 256u * t;  // O_t of this lane
+        const uint32_t ts = tl + 128u;                                                // S_t / P_t
+        const int nb_ctx = (it.n + kBlock - 1) / kBlock;
+        const int tail = it.n - (nb_ctx - 1) * kBlock;
+        const bool fold = p.sl2 > 0.f;
+        float mrow = -INFINITY, lrow = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nst; ++j) {
+            ok = wait_all(k_full0 + (j & 3) * 8, (uint32_t)((j >> 2) & 1), p.wait_ns) &&
+                 wait_all(s_full0 + t * 8, (uint32_t)(j & 1), p.wait_ns);
+            if (!ok) break;
+            tc::fence_after();
+            uint32_t x[kT2Keys];
+#pragma unroll
+            for (int c = 0; c < kT2Keys / 32; ++c)
+                tc::ld32(ts + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+            tc::wait_ld();
+            const uint32_t present = lds_u32(mask0 + (j & 3) * 4);
+            const int kbase = j * kT2Keys;
+            float mp[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+            const bool nomask = __all_sync(0xffffffffu, present == (1u << kT2Blocks) - 1u &&
+                                                            kbase + kT2Keys - 1 <= mpos);
+            if (fold && nomask) {
+#pragma unroll
+                for (int c = 0; c < kT2Keys / 2; ++c)
+                    mp[c & 7] = tc::max3(mp[c & 7], __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < kT2Keys; ++c) {
+                    const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
+                    const float v = keep ? (fold ? __uint_as_float(x[c]) : __uint_as_float(x[c]) * p.sl2)
+                                         : -INFINITY;
+                    x[c] = __float_as_uint(v);
+                    mp[c & 7] = fmaxf(mp[c & 7], v);
+                }
+            }
+            const float mr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            const float mx = fold ? mr * p.sl2 : mr;
+            // lazy rescaling: the reference max moves only when the new max
+            // exceeds it by more than 2^8; O and l are rescaled together
+            float alpha = 1.f;
+            bool need = false;
+            if (mrow == -INFINITY) {
+                mrow = mx;
+            } else if (mx > mrow + 8.f) {
+                alpha = exp2f(mrow - mx);
+                mrow = mx;
+                need = true;
+            }
+            const float un = mrow == -INFINITY ? 0.f : mrow;
+            float ps[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+            if (fold) {
+                const uint64_t sc2 = tc::f2(p.sl2, p.sl2), nu2 = tc::f2(-un, -un);
+                uint64_t acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = 0ull;
+#pragma unroll
+                for (int c = 0; c < kT2Keys / 2; ++c) {
+                    const uint64_t a2 = tc::fma2(tc::f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])),
+                                                 sc2, nu2);
+                    const float e0 = ex2(tc::f2_lo(a2)), e1 = ex2(tc::f2_hi(a2));
+                    acc[c & 3] = tc::add2(acc[c & 3], tc::f2(e0, e1));
+                    x[c] = pack_bf16x2(e0, e1);  // P over the consumed scores (x[c] is no longer needed)
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ps[2 * i] = tc::f2_lo(acc[i]);
+                    ps[2 * i + 1] = tc::f2_hi(acc[i]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kT2Keys / 2; ++c) {
+                    const float e0 = ex2(__uint_as_float(x[2 * c]) - un);
+                    const float e1 = ex2(__uint_as_float(x[2 * c + 1]) - un);
+                    ps[c & 7] += e0 + e1;
+                    x[c] = pack_bf16x2(e0, e1);
+                }
+            }
+            const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            lrow = lrow * alpha + psum;
+            if (__any_sync(0xffffffffu, need)) {
+                // O_t may be touched once its previous P . V has finished
+                if (!(ok = wait_all(o_done0 + t * 8, (uint32_t)((j - 1) & 1), p.wait_ns))) break;
+                tc::fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    uint32_t y[32];
+                    tc::ld32(tl + 32u * ch, y);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
+                    tc::st32(tl + 32u * ch, y);
+                }
+            }
+            // P_t(j): the A operand of O_t += P_t(j) . V(j)
+            tc::st32(ts, *reinterpret_cast<const uint32_t(*)[32]>(&x[0]));
+            tc::st32(ts + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&x[32]));
+            tc::wait_st();
+            if (warp == 0) {
+                // V rows of keys outside the context (missing blocks, the
+                // last block's tail) may hold any bits: zero them once the
+                // stage's V copies have landed, before tile 0's P . V (tile
+                // 1's is issued after it)
+                const uint32_t vbase = sbase + SM::kRingV + (j & 1) * SM::kKV;
+                bool any = false;
+                for (int l = 0; l < kT2Blocks; ++l) {
+                    const int blk = j * kT2Blocks + l;
+                    any |= !((present >> l) & 1u) || (blk == nb_ctx - 1 && tail < kBlock);
+                }
+                if (any && !(ok = wait_all(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns))) break;
+                for (int l = 0; any && l < kT2Blocks; ++l) {
+                    const int blk = j * kT2Blocks + l;
+                    const int from = !((present >> l) & 1u) ? 0 : (blk == nb_ctx - 1 && tail < kBlock ? tail : kBlock);
+                    for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
+                        const int key = l * kBlock + from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
+                        st_shared_zero16(vbase + hh * kT2Keys * 128 + key * 128 + ch * 16);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before();
+            mbar_arrive(p_full0 + t * 8);
+        }
+        if (!ok && (threadIdx.x & 127) == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+        if (ok && nst > 0) ok = wait_all(o_done0 + t * 8, (uint32_t)((nst - 1) & 1), p.wait_ns);
+        tc::fence_after();
+        const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+        const uint32_t keep = pos >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
+        uint16_t* orow = p.out + ((long long)(it.q0 + tok) * p.Hq + (long long)it.h * p.G + rr % p.G) * HD;
+#pragma unroll 1
+        for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t y[32];
+            if (nst > 0 && ok) {
+                tc::ld32(tl + 32u * ch, y);
+                tc::wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) y[i] = 0u;
+            }
+            if (vrow && ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pk[i] = pack_bf16x2(__uint_as_float(y[8 * q4 + 2 * i]) * inv,
+                                            __uint_as_float(y[8 * q4 + 2 * i + 1]) * inv) & keep;
+                    dst[q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc::fence_after();
+        tc::dealloc(tbase, kT2Cols);
+    }
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 // Raise a kernel's dynamic shared-memory limit once per device and context
@@ -870,6 +1263,13 @@ bool prepare_tc() {
 }
 
 template <int HD>
+bool prepare_tc2() {
+    static std::mutex mu;
+    static CUcontext done[256] = {};
+    return raise_smem_once(reinterpret_cast<const void*>(prefill_tc2_kernel<HD>), Tc2Smem<HD>::kTotal, done, mu);
+}
+
+template <int HD>
 bool prepare(int* smem) {
     static std::mutex mu;
     static CUcontext done[256] = {};
@@ -888,7 +1288,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
                   const int32_t* query_start, float scale, void* out, int32_t* dev_err, mi_stream_t stream,
                   int32_t variant) {
     if (!dims) return MI_ERR_INVALID_ARG;
-    if (variant < MI_PREFILL_DEFAULT || variant > MI_PREFILL_TCGEN05) return MI_ERR_INVALID_ARG;
+    if (variant < MI_PREFILL_DEFAULT || variant > MI_PREFILL_TCGEN05_PAIR) return MI_ERR_INVALID_ARG;
     const mi_dims D = *dims;
     if (D.B < 0 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1 || total_q < 0 ||
         max_query_len < 0)
@@ -898,7 +1298,8 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         return MI_ERR_UNSUPPORTED;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     // the tcgen05 tile stacks 128 / G whole tokens of a group (G <= 8)
-    const bool use_tc = variant == MI_PREFILL_TCGEN05 || variant == MI_PREFILL_DEFAULT;
+    const bool use_tc2 = variant == MI_PREFILL_TCGEN05_PAIR;
+    const bool use_tc = variant == MI_PREFILL_TCGEN05 || variant == MI_PREFILL_DEFAULT || use_tc2;
     const int tc_rows = (kTcRows / G) * G;
     if ((long long)D.num_blocks * D.Hkv * kBlock * (D.head_dim / 64) > 0x7FFFFFFFLL ||
         (long long)D.max_blocks_per_seq * kBlock > 0x7FFFFFFFLL || (long long)total_q * D.Hq > 0x7FFFFFFFLL ||
@@ -910,7 +1311,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         return MI_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return MI_ERR_INVALID_ARG;
-    const int rows_per_tile = use_tc ? tc_rows : kPRows;
+    const int rows_per_tile = use_tc2 ? 2 * tc_rows : (use_tc ? tc_rows : kPRows);
     const long long tiles_max = ((long long)max_query_len * G + rows_per_tile - 1) / rows_per_tile;
     const long long grid = (tiles_max + kTileGroup - 1) / kTileGroup * kTileGroup * D.B * D.Hkv;
     if (grid > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
@@ -936,7 +1337,16 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
     const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
-    if (use_tc) {
+    if (use_tc2) {
+        if (!(HD == 64 ? prepare_tc2<64>() : prepare_tc2<128>())) return MI_ERR_CUDA;
+        CUtensorMap tq, tk, tv;
+        if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, tc_rows) ||
+            !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_halves(&tv, v_cache, rows, HD))
+            return MI_ERR_CUDA;
+        e = HD == 64 ? launch_pdl(prefill_tc2_kernel<64>, (int)grid, kT2Threads, Tc2Smem<64>::kTotal, st, tq, tk, tv, p)
+                     : launch_pdl(prefill_tc2_kernel<128>, (int)grid, kT2Threads, Tc2Smem<128>::kTotal, st, tq, tk,
+                                  tv, p);
+    } else if (use_tc) {
         if (!(HD == 64 ? prepare_tc<64>() : prepare_tc<128>())) return MI_ERR_CUDA;
         CUtensorMap tq, tk, tv;
         if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, tc_rows) ||

@@ -139,8 +139,9 @@ def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
     assert_attention_close(from_dev_u16(out), ref, f"{kind} after a timed-out launch")
 
 
-def test_prefill_wait_runs_out_then_recovers(cuda_device):
-    """The tcgen05 prefill kernel: every CTA's first K stage is withheld, so
+@pytest.mark.parametrize("variant", [2, 3])  # MI_PREFILL_TCGEN05, MI_PREFILL_TCGEN05_PAIR
+def test_prefill_wait_runs_out_then_recovers(cuda_device, variant):
+    """The tcgen05 prefill kernels: every CTA's first K stage is withheld, so
     its MMA, softmax and P.V waits run out; no MMA is left running and the
     tensor memory is released (the next launch allocates it again); the next
     call is correct."""
@@ -148,7 +149,7 @@ def test_prefill_wait_runs_out_then_recovers(cuda_device):
     from test_prefill_gpu import _run_prefill
     mi = _mi()
     w = PREFILL_WORKLOADS["prefill_small"]
-    x = _run_prefill(w, cuda_device, order_seed=3, variant=mi.MI_PREFILL_TCGEN05)
+    x = _run_prefill(w, cuda_device, order_seed=3, variant=variant)
     R = w.B
     d_att = mi.dims(R, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
     bt_d, n_d, qs_d = (to_dev_i32(a, cuda_device) for a in (x["bt"], x["n"], x["qs"]))
@@ -158,7 +159,7 @@ def test_prefill_wait_runs_out_then_recovers(cuda_device):
         t0 = time.perf_counter()
         assert mi.mi_paged_prefill_attention_variant(d_att, x["T"], max_q, x["qo_d"], x["kc_d"], x["vc_d"], bt_d,
                                                      n_d, qs_d, w.scale, torch.empty_like(x["qo_d"]),
-                                                     variant=mi.MI_PREFILL_TCGEN05, dev_err=err) == mi.MI_OK
+                                                     variant=variant, dev_err=err) == mi.MI_OK
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
     assert int(err.item()) & mi.MI_DEVERR_TIMEOUT
@@ -166,7 +167,7 @@ def test_prefill_wait_runs_out_then_recovers(cuda_device):
     err.zero_()
     out = torch.full_like(x["qo_d"], float("nan"))
     assert mi.mi_paged_prefill_attention_variant(d_att, x["T"], max_q, x["qo_d"], x["kc_d"], x["vc_d"], bt_d, n_d,
-                                                 qs_d, w.scale, out, variant=mi.MI_PREFILL_TCGEN05,
+                                                 qs_d, w.scale, out, variant=variant,
                                                  dev_err=err) == mi.MI_OK
     torch.cuda.synchronize()
     assert int(err.item()) == 0
