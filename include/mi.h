@@ -396,8 +396,9 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
  *                       i.e. (128 / G) * G rows, per CTA; any G up to 8).
  *   MI_PREFILL_TCGEN05_PAIR  tcgen05 with two 128-row Q tiles per CTA
  *                       (one CTA per SM) sharing 128-key K / V stages,
- *                       one issuing thread alternating the tiles.
- * MI_PREFILL_DEFAULT takes the tcgen05 kernel. All compute the same
+ *                       one issuing thread alternating the tiles, 16
+ *                       softmax warps (each lane: two rows, 32 keys).
+ * MI_PREFILL_DEFAULT takes the pair kernel. All compute the same
  * definition within the same tolerance. */
 #define MI_PREFILL_DEFAULT 0
 #define MI_PREFILL_MMA 1

@@ -868,7 +868,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 
 constexpr int kT2Keys = 128;                 // keys per stage
 constexpr int kT2Blocks = kT2Keys / kBlock;  // 16-token blocks per stage
-constexpr int kT2Threads = 320;
+constexpr int kT2MmaWarp = 16;                           // warps 0-15 softmax, 16 MMA, 17 producer
+constexpr int kT2Threads = (kT2MmaWarp + 2) * 32;
 constexpr uint32_t kT2Cols = 512;
 
 template <int HD>
@@ -920,13 +921,13 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(v_full0 + i * 8, 1);
             mbar_init(v_empty0 + i * 8, 1);
             mbar_init(s_full0 + i * 8, 1);
-            mbar_init(p_full0 + i * 8, 128);
+            mbar_init(p_full0 + i * 8, 256);  // every softmax thread of the tile
             mbar_init(o_done0 + i * 8, 1);
         }
         mbar_init(fin, 1);
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == kT2MmaWarp) {
         tc::alloc(sbase + SM::kTmem, kT2Cols);
         tc::relinquish();
     }
@@ -935,7 +936,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     tc::fence_after();
     const uint32_t tbase = lds_u32(sbase + SM::kTmem);
 
-    if (warp == 9) {
+    if (warp == kT2MmaWarp + 1) {
         // ------------------------------------------------ producer warp --
         const uint64_t policy = l2_policy_evict_normal();
         if (lane == 0 && nst > 0) {
@@ -1000,7 +1001,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
         if (pgood && nst > 0 && !load_v(nst - 1)) pgood = false;
         if (!pgood && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
-    } else if (warp == 8) {
+    } else if (warp == kT2MmaWarp) {
         // -------------------------------------------------- MMA issuer --
         if (lane == 0 && nst > 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kTcRows, kT2Keys, false);
@@ -1067,174 +1068,220 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------- softmax ----
-        const int t = warp >> 2;                      // tile
-        const int rl = threadIdx.x & 127;             // row of the tile, tensor-memory lane
-        const int rr = it.rho0 + t * tr + rl;         // row of the request
-        const bool vrow = rl < tr && rr < it.nrows;
-        const int tok = rr / p.G;
-        const int pos = vrow ? it.first + tok : it.p_hi;
-        const int mpos = pos < 0 ? 0 : pos;
-        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + 256u * t;  // O_t of this lane
-        const uint32_t ts = tl + 128u;                                                // S_t / P_t
+        // Eight warps per tile. Warp w reads tensor-memory lanes lb ... lb + 15
+        // (lb = 32 (w mod 4) + 16 (w / 8)) with the 16-lane shapes: lane i
+        // holds rows a = lb + i/4 and b = a + 8, keys 8k + 2 (i mod 4) and the
+        // next one of each 8-key group k, so a quad of lanes shares two rows'
+        // scores (32 keys each per lane) and reduces them with shuffles.
+        const int t = (warp >> 2) & 1;  // tile
+        const int c4 = lane & 3;
+        const int lb = (warp & 3) * 32 + (warp >> 3) * 16;
+        const int rla = lb + (lane >> 2), rlb = rla + 8;  // rows of the tile
+        const int rra = it.rho0 + t * tr + rla, rrb = it.rho0 + t * tr + rlb;
+        const bool va = rla < tr && rra < it.nrows, vb = rlb < tr && rrb < it.nrows;
+        const int toka = rra / p.G, tokb = rrb / p.G;
+        const int posa = va ? it.first + toka : it.p_hi, posb = vb ? it.first + tokb : it.p_hi;
+        const int mposa = posa < 0 ? 0 : posa, mposb = posb < 0 ? 0 : posb;
+        const uint32_t tl = tbase + ((uint32_t)lb << 16) + 256u * t;  // O_t of these lanes
+        const uint32_t ts = tl + 128u;                                // S_t / P_t
         const int nb_ctx = (it.n + kBlock - 1) / kBlock;
         const int tail = it.n - (nb_ctx - 1) * kBlock;
         const bool fold = p.sl2 > 0.f;
-        float mrow = -INFINITY, lrow = 0.f;
+        float mra_run = -INFINITY, mrb_run = -INFINITY, lra = 0.f, lrb = 0.f;  // per lane: its 32 keys of the row
         bool ok = true;
         for (int j = 0; j < nst; ++j) {
             ok = wait_all(k_full0 + (j & 3) * 8, (uint32_t)((j >> 2) & 1), p.wait_ns) &&
                  wait_all(s_full0 + t * 8, (uint32_t)(j & 1), p.wait_ns);
             if (!ok) break;
             tc::fence_after();
-            uint32_t x[kT2Keys];
-#pragma unroll
-            for (int c = 0; c < kT2Keys / 32; ++c)
-                tc::ld32(ts + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+            uint32_t x[2 * kT2Keys / 4];  // x[4k + e]: e = 0, 1 row a; e = 2, 3 row b
+            tc::ld16x256_x8(ts, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tc::ld16x256_x8(ts + 64u, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
             tc::wait_ld();
             const uint32_t present = lds_u32(mask0 + (j & 3) * 4);
             const int kbase = j * kT2Keys;
-            float mp[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
             const bool nomask = __all_sync(0xffffffffu, present == (1u << kT2Blocks) - 1u &&
-                                                            kbase + kT2Keys - 1 <= mpos);
+                                                            kbase + kT2Keys - 1 <= min(mposa, mposb));
+            float alpha_a = 1.f, alpha_b = 1.f, psa, psb;
+            bool need = false;
+            float ma[4], mb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ma[i] = mb[i] = -INFINITY;
             if (fold && nomask) {
 #pragma unroll
-                for (int c = 0; c < kT2Keys / 2; ++c)
-                    mp[c & 7] = tc::max3(mp[c & 7], __uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]));
+                for (int k = 0; k < kT2Keys / 8; ++k) {
+                    ma[k & 3] = tc::max3(ma[k & 3], __uint_as_float(x[4 * k]), __uint_as_float(x[4 * k + 1]));
+                    mb[k & 3] = tc::max3(mb[k & 3], __uint_as_float(x[4 * k + 2]), __uint_as_float(x[4 * k + 3]));
+                }
             } else {
 #pragma unroll
-                for (int c = 0; c < kT2Keys; ++c) {
-                    const bool keep = ((present >> (c >> 4)) & 1u) && kbase + c <= mpos;
-                    const float v = keep ? (fold ? __uint_as_float(x[c]) : __uint_as_float(x[c]) * p.sl2)
-                                         : -INFINITY;
-                    x[c] = __float_as_uint(v);
-                    mp[c & 7] = fmaxf(mp[c & 7], v);
+                for (int k = 0; k < kT2Keys / 8; ++k) {
+                    const bool blk = (present >> (k >> 1)) & 1u;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = kbase + 8 * k + 2 * c4 + (e & 1);
+                        const bool keep = blk && key <= (e < 2 ? mposa : mposb);
+                        const float v = keep ? (fold ? __uint_as_float(x[4 * k + e])
+                                                     : __uint_as_float(x[4 * k + e]) * p.sl2)
+                                             : -INFINITY;
+                        x[4 * k + e] = __float_as_uint(v);
+                        if (e < 2)
+                            ma[k & 3] = fmaxf(ma[k & 3], v);
+                        else
+                            mb[k & 3] = fmaxf(mb[k & 3], v);
+                    }
                 }
             }
-            const float mr = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-            const float mx = fold ? mr * p.sl2 : mr;
-            // lazy rescaling: the reference max moves only when the new max
-            // exceeds it by more than 2^8; O and l are rescaled together
-            float alpha = 1.f;
-            bool need = false;
-            if (mrow == -INFINITY) {
-                mrow = mx;
-            } else if (mx > mrow + 8.f) {
-                alpha = exp2f(mrow - mx);
-                mrow = mx;
+            float mxa = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3]));
+            float mxb = fmaxf(fmaxf(mb[0], mb[1]), fmaxf(mb[2], mb[3]));
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+            if (fold) {
+                mxa *= p.sl2;
+                mxb *= p.sl2;
+            }
+            // lazy rescaling, per row: the reference max moves only when the
+            // new max exceeds it by more than 2^8; O and l are rescaled
+            // together (the four lanes of a quad take the same decision)
+            if (mra_run == -INFINITY) {
+                mra_run = mxa;
+            } else if (mxa > mra_run + 8.f) {
+                alpha_a = exp2f(mra_run - mxa);
+                mra_run = mxa;
                 need = true;
             }
-            const float un = mrow == -INFINITY ? 0.f : mrow;
-            float ps[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
-            if (fold) {
-                const uint64_t sc2 = tc::f2(p.sl2, p.sl2), nu2 = tc::f2(-un, -un);
-                uint64_t acc[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = 0ull;
-#pragma unroll
-                for (int c = 0; c < kT2Keys / 2; ++c) {
-                    const uint64_t a2 = tc::fma2(tc::f2(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])),
-                                                 sc2, nu2);
-                    const float e0 = ex2(tc::f2_lo(a2)), e1 = ex2(tc::f2_hi(a2));
-                    acc[c & 3] = tc::add2(acc[c & 3], tc::f2(e0, e1));
-                    x[c] = pack_bf16x2(e0, e1);  // P over the consumed scores (x[c] is no longer needed)
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    ps[2 * i] = tc::f2_lo(acc[i]);
-                    ps[2 * i + 1] = tc::f2_hi(acc[i]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kT2Keys / 2; ++c) {
-                    const float e0 = ex2(__uint_as_float(x[2 * c]) - un);
-                    const float e1 = ex2(__uint_as_float(x[2 * c + 1]) - un);
-                    ps[c & 7] += e0 + e1;
-                    x[c] = pack_bf16x2(e0, e1);
-                }
+            if (mrb_run == -INFINITY) {
+                mrb_run = mxb;
+            } else if (mxb > mrb_run + 8.f) {
+                alpha_b = exp2f(mrb_run - mxb);
+                mrb_run = mxb;
+                need = true;
             }
-            const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            lrow = lrow * alpha + psum;
+            const float una = mra_run == -INFINITY ? 0.f : mra_run;
+            const float unb = mrb_run == -INFINITY ? 0.f : mrb_run;
+            if (fold) {
+                const uint64_t sc2 = tc::f2(p.sl2, p.sl2);
+                const uint64_t nua = tc::f2(-una, -una), nub = tc::f2(-unb, -unb);
+                uint64_t acca[2] = {0ull, 0ull}, accb[2] = {0ull, 0ull};
+#pragma unroll
+                for (int k = 0; k < kT2Keys / 8; ++k) {
+                    const uint64_t a2 = tc::fma2(tc::f2(__uint_as_float(x[4 * k]), __uint_as_float(x[4 * k + 1])),
+                                                 sc2, nua);
+                    const uint64_t b2 = tc::fma2(
+                        tc::f2(__uint_as_float(x[4 * k + 2]), __uint_as_float(x[4 * k + 3])), sc2, nub);
+                    const float ea0 = ex2(tc::f2_lo(a2)), ea1 = ex2(tc::f2_hi(a2));
+                    const float eb0 = ex2(tc::f2_lo(b2)), eb1 = ex2(tc::f2_hi(b2));
+                    acca[k & 1] = tc::add2(acca[k & 1], tc::f2(ea0, ea1));
+                    accb[k & 1] = tc::add2(accb[k & 1], tc::f2(eb0, eb1));
+                    // P words (column 4k + i mod 4 of rows a and b) over the
+                    // consumed scores
+                    x[2 * k] = pack_bf16x2(ea0, ea1);
+                    x[2 * k + 1] = pack_bf16x2(eb0, eb1);
+                }
+                const uint64_t sa = tc::add2(acca[0], acca[1]), sb = tc::add2(accb[0], accb[1]);
+                psa = tc::f2_lo(sa) + tc::f2_hi(sa);
+                psb = tc::f2_lo(sb) + tc::f2_hi(sb);
+            } else {
+                float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < kT2Keys / 8; ++k) {
+                    const float ea0 = ex2(__uint_as_float(x[4 * k]) - una);
+                    const float ea1 = ex2(__uint_as_float(x[4 * k + 1]) - una);
+                    const float eb0 = ex2(__uint_as_float(x[4 * k + 2]) - unb);
+                    const float eb1 = ex2(__uint_as_float(x[4 * k + 3]) - unb);
+                    pa[k & 1] += ea0 + ea1;
+                    pb[k & 1] += eb0 + eb1;
+                    x[2 * k] = pack_bf16x2(ea0, ea1);
+                    x[2 * k + 1] = pack_bf16x2(eb0, eb1);
+                }
+                psa = pa[0] + pa[1];
+                psb = pb[0] + pb[1];
+            }
+            lra = lra * alpha_a + psa;
+            lrb = lrb * alpha_b + psb;
             if (__any_sync(0xffffffffu, need)) {
                 // O_t may be touched once its previous P . V has finished
                 if (!(ok = wait_all(o_done0 + t * 8, (uint32_t)((j - 1) & 1), p.wait_ns))) break;
                 tc::fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < HD / 32; ++ch) {
-                    uint32_t y[32];
-                    tc::ld32(tl + 32u * ch, y);
+                    uint32_t y[16];
+                    tc::ld16x256_x4(tl + 32u * ch, y);
                     tc::wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * alpha);
-                    tc::st32(tl + 32u * ch, y);
+                    for (int i = 0; i < 16; ++i)
+                        y[i] = __float_as_uint(__uint_as_float(y[i]) * ((i & 2) ? alpha_b : alpha_a));
+                    tc::st16x256_x4(tl + 32u * ch, y);
                 }
             }
             // P_t(j): the A operand of O_t += P_t(j) . V(j)
-            tc::st32(ts, *reinterpret_cast<const uint32_t(*)[32]>(&x[0]));
-            tc::st32(ts + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&x[32]));
+            tc::st16x128_x16(ts, *reinterpret_cast<const uint32_t(*)[32]>(&x[0]));
             tc::wait_st();
-            if (warp == 0) {
+            if (warp == 1) {
                 // V rows of keys outside the context (missing blocks, the
                 // last block's tail) may hold any bits: zero them once the
                 // stage's V copies have landed, before tile 0's P . V (tile
-                // 1's is issued after it)
-                const uint32_t vbase = sbase + SM::kRingV + (j & 1) * SM::kKV;
-                bool any = false;
-                for (int l = 0; l < kT2Blocks; ++l) {
-                    const int blk = j * kT2Blocks + l;
-                    any |= !((present >> l) & 1u) || (blk == nb_ctx - 1 && tail < kBlock);
-                }
-                if (any && !(ok = wait_all(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns))) break;
-                for (int l = 0; any && l < kT2Blocks; ++l) {
-                    const int blk = j * kT2Blocks + l;
-                    const int from = !((present >> l) & 1u) ? 0 : (blk == nb_ctx - 1 && tail < kBlock ? tail : kBlock);
-                    for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
-                        const int key = l * kBlock + from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
-                        st_shared_zero16(vbase + hh * kT2Keys * 128 + key * 128 + ch * 16);
+                // 1's is issued after it). A warp of tile 0 off the MMA
+                // warp's scheduler does it.
+                const int last = nb_ctx - 1 - j * kT2Blocks;  // the context's last block, stage-local
+                const bool any = present != (1u << kT2Blocks) - 1u || (last < kT2Blocks && tail < kBlock);
+                if (any) {
+                    if (!(ok = wait_all(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns))) break;
+                    const uint32_t vbase = sbase + SM::kRingV + (j & 1) * SM::kKV;
+                    for (int l = 0; l < kT2Blocks; ++l) {
+                        const int from = !((present >> l) & 1u) ? 0 : (l == last && tail < kBlock ? tail : kBlock);
+                        for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
+                            const int key = l * kBlock + from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
+                            st_shared_zero16(vbase + hh * kT2Keys * 128 + key * 128 + ch * 16);
+                        }
                     }
+                    fence_proxy_async_smem();  // generic-proxy writes read by the tensor cores
                 }
             }
-            fence_proxy_async_smem();
             tc::fence_before();
             mbar_arrive(p_full0 + t * 8);
         }
-        if (!ok && (threadIdx.x & 127) == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+        if (!ok && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
         if (ok && nst > 0) ok = wait_all(o_done0 + t * 8, (uint32_t)((nst - 1) & 1), p.wait_ns);
         tc::fence_after();
-        const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-        const uint32_t keep = pos >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
-        uint16_t* orow = p.out + ((long long)(it.q0 + tok) * p.Hq + (long long)it.h * p.G + rr % p.G) * HD;
+        lra += __shfl_xor_sync(0xffffffffu, lra, 1);
+        lrb += __shfl_xor_sync(0xffffffffu, lrb, 1);
+        lra += __shfl_xor_sync(0xffffffffu, lra, 2);
+        lrb += __shfl_xor_sync(0xffffffffu, lrb, 2);
+        const float inva = lra > 0.f ? 1.f / lra : 0.f, invb = lrb > 0.f ? 1.f / lrb : 0.f;
+        const uint32_t keepa = posa >= 0 ? 0xFFFFFFFFu : 0u, keepb = posb >= 0 ? 0xFFFFFFFFu : 0u;  // rows before position 0 are +0
+        uint16_t* orowa = p.out + ((long long)(it.q0 + toka) * p.Hq + (long long)it.h * p.G + rra % p.G) * HD;
+        uint16_t* orowb = p.out + ((long long)(it.q0 + tokb) * p.Hq + (long long)it.h * p.G + rrb % p.G) * HD;
 #pragma unroll 1
         for (int ch = 0; ch < HD / 32; ++ch) {
-            uint32_t y[32];
+            uint32_t y[16];
             if (nst > 0 && ok) {
-                tc::ld32(tl + 32u * ch, y);
+                tc::ld16x256_x4(tl + 32u * ch, y);
                 tc::wait_ld();
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) y[i] = 0u;
+                for (int i = 0; i < 16; ++i) y[i] = 0u;
             }
-            if (vrow && ok) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+            if (ok) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(y[8 * q4 + 2 * i]) * inv,
-                                            __uint_as_float(y[8 * q4 + 2 * i + 1]) * inv) & keep;
-                    dst[q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int k = 0; k < 4; ++k) {
+                    const int col = 32 * ch + 8 * k + 2 * c4;
+                    if (va)
+                        *reinterpret_cast<uint32_t*>(orowa + col) =
+                            pack_bf16x2(__uint_as_float(y[4 * k]) * inva, __uint_as_float(y[4 * k + 1]) * inva) & keepa;
+                    if (vb)
+                        *reinterpret_cast<uint32_t*>(orowb + col) =
+                            pack_bf16x2(__uint_as_float(y[4 * k + 2]) * invb, __uint_as_float(y[4 * k + 3]) * invb) &
+                            keepb;
                 }
             }
         }
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kT2MmaWarp) {
         tc::fence_after();
         tc::dealloc(tbase, kT2Cols);
     }
@@ -1298,8 +1345,8 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         return MI_ERR_UNSUPPORTED;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     // the tcgen05 tile stacks 128 / G whole tokens of a group (G <= 8)
-    const bool use_tc2 = variant == MI_PREFILL_TCGEN05_PAIR;
-    const bool use_tc = variant == MI_PREFILL_TCGEN05 || variant == MI_PREFILL_DEFAULT || use_tc2;
+    const bool use_tc2 = variant == MI_PREFILL_TCGEN05_PAIR || variant == MI_PREFILL_DEFAULT;
+    const bool use_tc = variant == MI_PREFILL_TCGEN05 || use_tc2;
     const int tc_rows = (kTcRows / G) * G;
     if ((long long)D.num_blocks * D.Hkv * kBlock * (D.head_dim / 64) > 0x7FFFFFFFLL ||
         (long long)D.max_blocks_per_seq * kBlock > 0x7FFFFFFFLL || (long long)total_q * D.Hq > 0x7FFFFFFFLL ||

@@ -126,6 +126,47 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
+// 16-lane shapes. From tensor-memory lane L (a multiple of 16 inside the
+// warp's quarter), lane i of the warp holds rows L + i/4 and L + 8 + i/4:
+//  * 16x256b, repetition k (8 columns): r[4k] and r[4k+1] = columns
+//    8k + 2(i mod 4) and the next one of row L + i/4, r[4k+2] and r[4k+3] the
+//    same columns of row L + 8 + i/4;
+//  * 16x128b, repetition k (4 columns): r[2k] = column 4k + (i mod 4) of row
+//    L + i/4, r[2k+1] the same column of row L + 8 + i/4.
+#define MI_TC_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), \
+                    "=r"(r[b + 6]), "=r"(r[b + 7])
+#define MI_TC_W8(b) "r"(r[b]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), "r"(r[b + 4]), "r"(r[b + 5]), \
+                    "r"(r[b + 6]), "r"(r[b + 7])
+__device__ __forceinline__ void ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : MI_TC_R8(0), MI_TC_R8(8), MI_TC_R8(16), MI_TC_R8(24)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : MI_TC_R8(0), MI_TC_R8(8)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void st16x256_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr), MI_TC_W8(0), MI_TC_W8(8)
+        : "memory");
+}
+__device__ __forceinline__ void st16x128_x16(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        MI_TC_W8(0), MI_TC_W8(8), MI_TC_W8(16), MI_TC_W8(24)
+        : "memory");
+}
+#undef MI_TC_R8
+#undef MI_TC_W8
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
