@@ -133,15 +133,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Like mbar_try_wait, with a suspend-time hint: a thread whose phase has not
+// completed may sleep up to hint_ns before the call returns false, and
+// wakes when the phase completes. A waiting warp then polls rarely and
+// leaves its scheduler's issue slots to the warps that work (a warp issuing
+// tensor-core MMAs among busy warps gets few of them).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kWaitSleepNs = 50000;  // longest sleep of one poll; the limit is checked between polls
+
 // Wait for phase `parity` of the barrier to complete, for at most limit_ns
-// (the launch's wait limit: kWaitLimitNs unless a test shortened it).
-// Returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
+// (the launch's wait limit: kWaitLimitNs unless a test shortened it), plus
+// one poll's sleep when sleep_ns > 0 (each poll may then sleep that long;
+// with 0 the thread polls without a hint). Returns false when the limit ran
+// out. Which is faster depends on the kernel: measured per kernel.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns,
+                                                  uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (sleep_ns > 0) {
+            if (mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
+        } else {
+            for (int i = 0; i < 64; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+        }
         if ((long long)(globaltimer() - t0) > limit_ns) return false;
     }
 }
