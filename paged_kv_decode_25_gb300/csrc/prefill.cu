@@ -1011,7 +1011,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if (!pgood && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
     } else if (warp == kT2MmaWarp) {
         // -------------------------------------------------- MMA issuer --
-        if (lane == 0 && nst > 0) {
+        // The whole warp runs the loop; one elected lane issues each MMA
+        // and commit.
+        if (nst > 0) {
             constexpr uint32_t idS = tc::idesc_bf16(kTcRows, kT2Keys, false);
             constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
             auto issue_s = [&](int t, int j) {
@@ -1022,9 +1024,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                     const uint32_t off = (kk & 3) * 32;  // 16 bf16 of the 128-byte row
                     const uint64_t a = tc::sdesc_sw128(qbase + (kk >> 2) * kTcRows * 128 + off, 16, 1024);
                     const uint64_t bd = tc::sdesc_sw128(kbase + (kk >> 2) * kT2Keys * 128 + off, 16, 1024);
-                    tc::mma_ss(tbase + 256u * t + 128u, a, bd, idS, kk > 0);
+                    tc::mma_ss_elect(tbase + 256u * t + 128u, a, bd, idS, kk > 0);
                 }
-                tc::commit(s_full0 + t * 8);
+                tc::commit_elect(s_full0 + t * 8);
             };
             auto issue_o = [&](int t, int j) {
                 const uint32_t vbase = sbase + SM::kRingV + (j & 1) * SM::kKV;
@@ -1032,46 +1034,44 @@ __global__ void __launch_bounds__(kT2Threads, 1)
 #pragma unroll
                 for (int l = 0; l < kT2Blocks; ++l) {
                     const uint64_t bd = tc::sdesc_sw128(vbase + l * kBlock * 128, kT2Keys * 128, 1024);
-                    tc::mma_ts(tbase + 256u * t, pcol + 8u * l, bd, idO, j > 0 || l > 0);
+                    tc::mma_ts_elect(tbase + 256u * t, pcol + 8u * l, bd, idO, j > 0 || l > 0);
                 }
-                tc::commit(o_done0 + t * 8);
+                tc::commit_elect(o_done0 + t * 8);
             };
-            bool ok = wait_pf(q_full, 0, p.wait_ns) &&
-                      wait_pf(k_full0, 0, p.wait_ns);
+            bool ok = wait_all(q_full, 0, p.wait_ns) && wait_all(k_full0, 0, p.wait_ns);
             if (ok) {
                 tc::fence_after();
                 issue_s(0, 0);
                 issue_s(1, 0);
-                tc::commit(k_empty0);  // K(0) read by both tiles
+                tc::commit_elect(k_empty0);  // K(0) read by both tiles
             }
             for (int j = 0; ok && j < nst; ++j) {
                 const uint32_t ph = (uint32_t)(j & 1);
-                ok = wait_pf(p_full0, ph, p.wait_ns) &&
-                     wait_pf(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns);
+                ok = wait_all(p_full0, ph, p.wait_ns) &&
+                     wait_all(v_full0 + (j & 1) * 8, (uint32_t)((j >> 1) & 1), p.wait_ns);
                 if (!ok) break;
                 tc::fence_after();
                 issue_o(0, j);
                 const bool more = j + 1 < nst;
                 if (more) {
-                    if (!(ok = wait_pf(k_full0 + ((j + 1) & 3) * 8, (uint32_t)(((j + 1) >> 2) & 1),
-                                                 p.wait_ns)))
+                    if (!(ok = wait_all(k_full0 + ((j + 1) & 3) * 8, (uint32_t)(((j + 1) >> 2) & 1), p.wait_ns)))
                         break;
                     tc::fence_after();
                     issue_s(0, j + 1);
                 }
-                if (!(ok = wait_pf(p_full0 + 8, ph, p.wait_ns))) break;
+                if (!(ok = wait_all(p_full0 + 8, ph, p.wait_ns))) break;
                 tc::fence_after();
                 issue_o(1, j);
-                tc::commit(v_empty0 + (j & 1) * 8);  // V(j) read by both tiles
+                tc::commit_elect(v_empty0 + (j & 1) * 8);  // V(j) read by both tiles
                 if (more) {
                     issue_s(1, j + 1);
-                    tc::commit(k_empty0 + ((j + 1) & 1) * 8);
+                    tc::commit_elect(k_empty0 + ((j + 1) & 1) * 8);
                 }
             }
-            if (!ok) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
+            if (!ok && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
             // every MMA issued has finished before tensor memory is released
-            tc::commit(fin);
-            (void)wait_pf(fin, 0, drain_limit(p.wait_ns));
+            tc::commit_elect(fin);
+            (void)wait_all(fin, 0, drain_limit(p.wait_ns));
         }
         __syncwarp();
     } else {
