@@ -879,6 +879,7 @@ constexpr int kT2Blocks = kT2Keys / kBlock;  // 16-token blocks per stage
 constexpr int kT2MmaWarp = 16;                           // warps 0-15 softmax, 16 MMA, 17 producer
 constexpr int kT2Threads = (kT2MmaWarp + 2) * 32;
 constexpr uint32_t kT2Cols = 512;
+constexpr int kT2KSlots = 2;  // K ring depth (V: two); three measured no faster (0.389 against 0.386 ms)
 
 template <int HD>
 struct Tc2Smem {
@@ -887,10 +888,10 @@ struct Tc2Smem {
     static constexpr int kKV = kH * kT2Keys * 128;            // one K (or V) stage: kH x [128 keys][128 B]
     static constexpr int kQ = 0;
     static constexpr int kRingK = kQ + 2 * kQT;
-    static constexpr int kRingV = kRingK + 2 * kKV;
+    static constexpr int kRingV = kRingK + kT2KSlots * kKV;
     static constexpr int kBar = kRingV + 2 * kKV;
-    // q_full, k_full[4], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin
-    static constexpr int kNBar = 1 + 4 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    // q_full, k_full[4], k_empty[kT2KSlots], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], fin
+    static constexpr int kNBar = 1 + 4 + kT2KSlots + 2 + 2 + 2 + 2 + 2 + 1;
     static constexpr int kMask = kBar + kNBar * 8;
     static constexpr int kTmem = kMask + 4 * 4;
     static constexpr int kTotal = kTmem + 16 + 1024;  // slack to align the base to 1024 B
@@ -916,7 +917,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if (!work_item(p, 2 * tr, it)) return;
     const int nst = (it.nblk + kT2Blocks - 1) / kT2Blocks;
     const uint32_t bar = sbase + SM::kBar;
-    const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 32, v_full0 = k_empty0 + 16;
+    const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 32, v_full0 = k_empty0 + 8 * kT2KSlots;
     const uint32_t v_empty0 = v_full0 + 16, s_full0 = v_empty0 + 16, p_full0 = s_full0 + 16;
     const uint32_t o_done0 = p_full0 + 16, fin = o_done0 + 16;
     const uint32_t mask0 = sbase + SM::kMask;
@@ -924,8 +925,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int i = 0; i < 4; ++i) mbar_init(k_full0 + i * 8, 1);
+        for (int i = 0; i < kT2KSlots; ++i) mbar_init(k_empty0 + i * 8, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(k_empty0 + i * 8, 1);
             mbar_init(v_full0 + i * 8, 1);
             mbar_init(v_empty0 + i * 8, 1);
             mbar_init(s_full0 + i * 8, 1);
@@ -971,17 +972,24 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             return true;
         };
         bool pgood = true;
+        // block-table entries are read a stage ahead, before the wait for
+        // the slot, so their load latency is hidden
+        auto table_entry = [&](int jj) -> int {
+            const int x = jj * kT2Blocks + lane;
+            return (lane < kT2Blocks && x < it.nblk) ? __ldg(p.block_tables + (long long)it.r * p.mbps + x) : -1;
+        };
+        int nblk_next = table_entry(0);
         for (int j = 0; j < nst; ++j) {
-            const int sl = j & 1, u = j >> 1;
+            const int sl = j % kT2KSlots, u = j / kT2KSlots;
+            const int x = j * kT2Blocks + lane;
+            const int blk = nblk_next;
+            if (j + 1 < nst) nblk_next = table_entry(j + 1);
             if (!wait_all(k_empty0 + sl * 8, (uint32_t)((u & 1) ^ 1), p.wait_ns)) {
                 pgood = false;
                 break;
             }
-            const int x = j * kT2Blocks + lane;
-            int blk = -1;
             bool ok = false;
             if (lane < kT2Blocks && x < it.nblk) {
-                blk = __ldg(p.block_tables + (long long)it.r * p.mbps + x);
                 ok = blk >= 0 && blk < p.num_blocks;
                 if (!ok) raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
             }
@@ -1017,7 +1025,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             constexpr uint32_t idS = tc::idesc_bf16(kTcRows, kT2Keys, false);
             constexpr uint32_t idO = tc::idesc_bf16(kTcRows, HD, true);
             auto issue_s = [&](int t, int j) {
-                const uint32_t kbase = sbase + SM::kRingK + (j & 1) * SM::kKV;
+                const uint32_t kbase = sbase + SM::kRingK + (j % kT2KSlots) * SM::kKV;
                 const uint32_t qbase = sbase + SM::kQ + t * SM::kQT;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
@@ -1065,7 +1073,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 tc::commit_elect(v_empty0 + (j & 1) * 8);  // V(j) read by both tiles
                 if (more) {
                     issue_s(1, j + 1);
-                    tc::commit_elect(k_empty0 + ((j + 1) & 1) * 8);
+                    tc::commit_elect(k_empty0 + ((j + 1) % kT2KSlots) * 8);
                 }
             }
             if (!ok && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
