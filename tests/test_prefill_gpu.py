@@ -214,6 +214,62 @@ def test_prefill_edge_lengths(cuda_device, variant):
     assert_attention_close(got, ref, "edge lengths")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.09])
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_nonpositive_scale(cuda_device, scale, variant):
+    """A scale of zero or below takes the softmax path that scales every
+    score before the row max (the fast path folds a positive scale into the
+    exponent); with scale 0 every row is the mean of V over its causal
+    window."""
+    hist, new = [0, 37, 300], [70, 140, 9]
+    q, kc, vc, bt, n, qs = _random_case(21, 16, 4, 128, hist, new)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, scale, variant=variant)
+    assert err == 0
+    ref = oracle.paged_prefill_attention(q, kc, vc, bt, n, qs, scale, nthreads=8)
+    assert_attention_close(got, ref, f"scale {scale}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_growing_scores_rescale(cuda_device, variant):
+    """Keys whose magnitude grows along the context (block j of every request
+    scaled by 1 + j / 2) push each row's running max up by far more than 2^8
+    (base 2) many times over: the kernels' lazy rescaling of O and l has to
+    give the oracle's result."""
+    hist, new = [400, 900], [64, 130]
+    q, kc, vc, bt, n, qs = _random_case(22, 8, 2, 128, hist, new)
+    k64 = oracle.bf16_to_f64(kc)
+    for b in range(len(n)):
+        for j in range(-(-int(n[b]) // BLOCK)):
+            k64[bt[b, j]] *= 1.0 + j / 2.0
+    kc = oracle.f64_to_bf16(k64)
+    scale = 1.0 / np.sqrt(128)
+    got, err = _attend(cuda_device, q, kc, vc, bt, n, qs, scale, variant=variant)
+    assert err == 0
+    ref = oracle.paged_prefill_attention(q, kc, vc, bt, n, qs, scale, nthreads=8)
+    # the input does what it is for: for the last new token of request 1
+    # (query head 0, KV head 0) the running max of its base-2 scores over
+    # 128-key stages grows by more than 8 at least three times
+    b, row = 1, int(qs[2]) - 1
+    keys = np.stack([oracle.bf16_to_f64(kc[bt[b, t // BLOCK], 0, t % BLOCK]) for t in range(int(n[b]))])
+    s2 = keys @ oracle.bf16_to_f64(q[row, 0]) * scale * np.log2(np.e)
+    stage_max = np.maximum.accumulate([s2[i:i + 128].max() for i in range(0, len(s2), 128)])
+    assert int(np.sum(np.diff(stage_max) > 8.0)) >= 3
+    # Rows here are nearly one-hot, so outputs are about as large as V (up to
+    # ~4) and the fixed absolute tolerance of the other tests does not apply.
+    # The kernels round each weight p_i to bf16 for the P.V product (relative
+    # error <= 2^-9) and the output to bf16 (<= 2^-9 |o|); scores, sums and
+    # O are fp32. So per element |got - ref| <= 2^-9 (sum_i p_i |v_i| + |ref|),
+    # checked with a factor 2 of margin; sum_i p_i |v_i| is the oracle's
+    # attention over |V|.
+    vabs = np.where(np.isnan(oracle.bf16_to_f64(vc)), vc, vc & np.uint16(0x7FFF)).astype(np.uint16)
+    ref_abs = oracle.paged_prefill_attention(q, kc, vabs, bt, n, qs, scale, nthreads=8)
+    g = oracle.bf16_to_f64(got)
+    assert np.all(np.isfinite(g))
+    bound = 2.0 ** -8 * (ref_abs + np.abs(ref))
+    worst = float(np.max(np.abs(g - ref) / bound))
+    assert worst <= 1.0, f"growing scores: error {worst:.2f} x the bound"
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_prefill_error_bits(cuda_device, variant):
     mi = _mi()
