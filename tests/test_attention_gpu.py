@@ -226,6 +226,40 @@ def test_attention_edge_lengths(cuda_device, d_head, Hq, Hkv):
             assert np.all(out[empty] == 0)
 
 
+def test_attention_growing_scores(cuda_device):
+    """Keys whose magnitude grows along the context (block j scaled by
+    1 + j / 2): each row's max moves by far more than 2^8 (base 2) from block
+    to block, and at small grids the split-KV pieces merged at the end carry
+    very different maxima. Rows are nearly one-hot, so outputs are as large
+    as V; the bound is the bf16 rounding of each weight and of the output
+    (2^-9 relative each, factor 2 margin): |got - ref| <= 2^-8 (sum_i p_i
+    |v_i| + |ref|), sum_i p_i |v_i| being the oracle's attention over |V|."""
+    mi = _mi()
+    q, kc, vc, bt, lens, mbps, nb = _edge_case(cuda_device, 128, [1500, 700, 33, 4000], Hq=8, Hkv=2)
+    k64 = oracle.bf16_to_f64(kc)
+    for b in range(len(lens)):
+        for j in range(-(-int(lens[b]) // BLOCK)):
+            k64[bt[b, j]] *= 1.0 + j / 2.0
+    kc = oracle.f64_to_bf16(k64)
+    scale = 1.0 / np.sqrt(128)
+    ref = oracle.paged_attention(q, kc, vc, bt, lens, scale, nthreads=8)
+    vabs = np.where(np.isnan(oracle.bf16_to_f64(vc)), vc, vc & np.uint16(0x7FFF)).astype(np.uint16)
+    ref_abs = oracle.paged_attention(q, kc, vabs, bt, lens, scale, nthreads=8)
+    bound = 2.0 ** -8 * (ref_abs + np.abs(ref))
+    d = mi.dims(len(lens), 8, 2, 128, nb, mbps)
+    q_d, kc_d, vc_d = (to_dev_u16(a, cuda_device) for a in (q, kc, vc))
+    bt_d, cl_d = to_dev_i32(bt, cuda_device), to_dev_i32(lens, cuda_device)
+    ws = _workspace(mi, d, cuda_device)
+    for var in VARIANTS:
+        for ctas in (0, 1, 3, 13, 100):
+            out, err = _run(mi, d, q_d, kc_d, vc_d, bt_d, cl_d, scale, ws, var, ctas, cuda_device)
+            assert err == 0
+            g = oracle.bf16_to_f64(out)
+            assert np.all(np.isfinite(g))
+            worst = float(np.max(np.abs(g - ref) / bound))
+            assert worst <= 1.0, f"var {var} ctas {ctas}: error {worst:.2f} x the bound"
+
+
 def test_one_token_context_returns_v_exactly(cuda_device):
     mi = _mi()
     q, kc, vc, bt, lens, mbps, nb = _edge_case(cuda_device, 128, [1, 1, 1], Hq=8, Hkv=2)
