@@ -885,7 +885,8 @@ template <int HD>
 struct Tc2Smem {
     static constexpr int kH = HD / 64;
     static constexpr int kQT = kH * kTcRows * 128;            // one Q tile: kH x [128 rows][128 B]
-    static constexpr int kKV = kH * kT2Keys * 128;            // one K (or V) stage: kH x [128 keys][128 B]
+    // one K or V stage: K as kH x [128 keys][128 B], V as 8 blocks x kH x [16 keys][128 B]
+    static constexpr int kKV = kH * kT2Keys * 128;
     static constexpr int kQ = 0;
     static constexpr int kRingK = kQ + 2 * kQT;
     static constexpr int kRingV = kRingK + kT2KSlots * kKV;
@@ -965,9 +966,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
             __syncwarp();
             if (pok) {
-                const uint32_t vd = sbase + SM::kRingV + sl * SM::kKV + lane * kBlock * 128;
+                // one copy per block: both 128-byte halves of its 16 rows
+                const uint32_t vd = sbase + SM::kRingV + sl * SM::kKV + lane * kH * kBlock * 128;
                 const int row0 = (pblk * p.Hkv + it.h) * kBlock;
-                for (int hh = 0; hh < kH; ++hh) tma_load_3d(vd + hh * kT2Keys * 128, &tmv, fb, 0, hh, row0, policy);
+                tma_load_3d(vd, &tmv, fb, 0, row0, 0, policy);
             }
             return true;
         };
@@ -1041,7 +1043,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 const uint32_t pcol = tbase + 256u * t + 128u;  // P_t(j): bf16 pairs over S_t's first 64 columns
 #pragma unroll
                 for (int l = 0; l < kT2Blocks; ++l) {
-                    const uint64_t bd = tc::sdesc_sw128(vbase + l * kBlock * 128, kT2Keys * 128, 1024);
+                    // block l: [kH][16 keys][128 B]; the 64-column halves of V
+                    // are kBlock * 128 bytes apart
+                    const uint64_t bd = tc::sdesc_sw128(vbase + l * kH * kBlock * 128, kBlock * 128, 1024);
                     tc::mma_ts_elect(tbase + 256u * t, pcol + 8u * l, bd, idO, j > 0 || l > 0);
                 }
                 tc::commit_elect(o_done0 + t * 8);
@@ -1249,8 +1253,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                     for (int l = 0; l < kT2Blocks; ++l) {
                         const int from = !((present >> l) & 1u) ? 0 : (l == last && tail < kBlock ? tail : kBlock);
                         for (int i = lane; i < (kBlock - from) * kH * 8; i += 32) {
-                            const int key = l * kBlock + from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
-                            st_shared_zero16(vbase + hh * kT2Keys * 128 + key * 128 + ch * 16);
+                            const int r = from + i / (kH * 8), hh = (i / 8) % kH, ch = i % 8;
+                            st_shared_zero16(vbase + (l * kH + hh) * kBlock * 128 + r * 128 + ch * 16);
                         }
                     }
                     fence_proxy_async_smem();  // generic-proxy writes read by the tensor cores
@@ -1404,7 +1408,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         if (!(HD == 64 ? prepare_tc2<64>() : prepare_tc2<128>())) return MI_ERR_CUDA;
         CUtensorMap tq, tk, tv;
         if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, tc_rows) ||
-            !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_halves(&tv, v_cache, rows, HD))
+            !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_blocks(&tv, v_cache, rows, HD))
             return MI_ERR_CUDA;
         e = HD == 64 ? launch_pdl(prefill_tc2_kernel<64>, (int)grid, kT2Threads, Tc2Smem<64>::kTotal, st, tq, tk, tv, p)
                      : launch_pdl(prefill_tc2_kernel<128>, (int)grid, kT2Threads, Tc2Smem<128>::kTotal, st, tq, tk,

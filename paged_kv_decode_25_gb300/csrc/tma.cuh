@@ -118,6 +118,23 @@ inline bool make_tmap_kv_halves(CUtensorMap* m, const void* base, long long rows
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a bf16 cache for whole blocks: dims {64, rows, HD/64} (the
+// 128-byte halves of a token row as the outer dimension), box {64, 16,
+// HD/64}: all of a block's 16 token rows in one copy, landing as
+// [HD/64][16][128 B] with 128-byte swizzle (each half's 16 rows together).
+inline bool make_tmap_kv_blocks(CUtensorMap* m, const void* base, long long rows, int HD) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(HD / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)HD * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kBlock, (cuuint32_t)(HD / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 4-D map over q [T][Hq][HD] bf16: dims {64, HD/64, Hq, T}, box {64, 1, G,
 // rows / G}: one 128-byte half of `rows` (token, head) rows of a GQA group,
 // landing as [rows][128 B] with 128-byte swizzle; tokens past T read as zero.
