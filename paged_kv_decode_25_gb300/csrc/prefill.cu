@@ -6,7 +6,12 @@
 // context positions, n_r - m_r .. n_r - 1, and token n_r - m_r + i attends to
 // cached tokens 0 .. n_r - m_r + i.
 //
-// Work decomposition:
+// Three kernels compute it: the two-tile tcgen05 kernel (the default,
+// prefill_tc2_kernel), the single-tile tcgen05 kernel (prefill_tc_kernel) and
+// the mma.sync kernel below (prefill_kernel), whose layout follows; the two
+// tcgen05 kernels describe theirs where they are defined.
+//
+// mma.sync work decomposition:
 //   * Rows are (new token i, query head g of the GQA group) pairs, row index
 //     i * G + g, so one staged K/V tile serves every head of the group. A CTA
 //     owns 64 consecutive rows of one (request, KV head); its 4 consumer warps
@@ -863,20 +868,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 // each S = Q . K^T instruction is 128 x 128 (half the Q operand traffic per
 // key of a 128 x 64 one). Tensor memory (512 columns): O_t at 256 t, S_t at
 // 256 t + 128 (P_t, the bf16 probabilities, over the first 64 of its
-// columns). One thread issues every MMA, alternating the tiles so that one
-// tile's softmax runs under the other tile's MMAs:
+// columns). One warp issues every MMA (converged, one elected lane),
+// alternating the tiles so that one tile's softmax runs under the other
+// tile's MMAs:
 //   S_0(0), S_1(0); for each stage j: O_0 += P_0(j) V(j), S_0(j+1),
 //   O_1 += P_1(j) V(j), S_1(j+1).
 // S_t(j+1) overwrites P_t(j) after O_t += P_t(j) V(j) has read it: MMAs one
-// thread issues run in issue order. Warps 0-3 (tile 0) and 4-7 (tile 1) run
-// the softmax of their tile (thread = row = tensor-memory lane, 128 scores
-// per stage in registers); warp 8 issues the MMAs and owns the tensor
-// memory; warp 9 loads Q once and streams K and V (two stages each, K of
-// stage j before V of stage j - 1).
+// thread issues run in issue order. Warps 0-15 run the softmax, eight per
+// tile: warp w reads tensor-memory lanes 32 (w mod 4) + 16 (w / 8) ... + 15
+// with the 16-lane shapes, each lane holding two rows x 32 keys of a stage;
+// warp 16 issues the MMAs and owns the tensor memory; warp 17 loads Q once
+// and streams K (two stages, a 2 KB copy per block half) and V (two stages,
+// a 4 KB copy per block), K of stage j before V of stage j - 1.
 
 constexpr int kT2Keys = 128;                 // keys per stage
 constexpr int kT2Blocks = kT2Keys / kBlock;  // 16-token blocks per stage
-constexpr int kT2MmaWarp = 16;                           // warps 0-15 softmax, 16 MMA, 17 producer
+constexpr int kT2MmaWarp = 16;  // warps 0-15 softmax, 16 MMA, 17 producer
 constexpr int kT2Threads = (kT2MmaWarp + 2) * 32;
 constexpr uint32_t kT2Cols = 512;
 constexpr int kT2KSlots = 2;  // K ring depth (V: two); three measured no faster (0.389 against 0.386 ms)
