@@ -731,12 +731,11 @@ def run_prefill(args, w, rank, world):
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
     max_q = int(m.max())
-    pvar = {"mma": mi.MI_PREFILL_MMA, "single": mi.MI_PREFILL_TCGEN05, "pair": mi.MI_PREFILL_TCGEN05_PAIR,
-            "cluster": mi.MI_PREFILL_TCGEN05_CLUSTER}.get(args.variant, mi.MI_PREFILL_DEFAULT)
+    pvar = {"mma": mi.MI_PREFILL_MMA, "single": mi.MI_PREFILL_TCGEN05,
+            "pair": mi.MI_PREFILL_TCGEN05_PAIR}.get(args.variant, mi.MI_PREFILL_DEFAULT)
     kernel_name = {"mma": "paged prefill attention (mma.sync m16n8k16 bf16), per layer",
-                   "single": "paged prefill attention (tcgen05.mma, one Q tile per CTA, two CTAs per SM), per layer",
-                   "cluster": "paged prefill attention (tcgen05.mma, two Q tiles per CTA, CTA pairs sharing K/V stages "
-                              "by TMA multicast), per layer"}.get(args.variant, "paged prefill attention (tcgen05.mma, two Q tiles per CTA sharing 128-key "
+                   "single": "paged prefill attention (tcgen05.mma, one Q tile per CTA, two CTAs per SM), per layer"
+                   }.get(args.variant, "paged prefill attention (tcgen05.mma, two Q tiles per CTA sharing 128-key "
                                        "stages, 16 softmax warps), per layer")
 
     def step(ev=None):
@@ -1028,7 +1027,7 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="qwen3_8b",
                     choices=list(WORKLOADS) + list(PREFILL_WORKLOADS) + ["qwen3_8b_swap"])
-    ap.add_argument("--variant", default="default", choices=["default", "mma", "fma", "pair", "single", "cluster"],
+    ap.add_argument("--variant", default="default", choices=["default", "mma", "fma", "pair", "single"],
                     help="decode: attention tile (mma, fma); prefill: mma (mma.sync), single (tcgen05, one Q tile "
                          "per CTA) or pair (the default: two Q tiles per CTA)")
     ap.add_argument("--unfused", action="store_true",

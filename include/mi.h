@@ -398,17 +398,12 @@ mi_status mi_paged_prefill_attention(const mi_dims* dims, int32_t total_q, int32
  *                       (one CTA per SM) sharing 128-key K / V stages,
  *                       one issuing thread alternating the tiles, 16
  *                       softmax warps (each lane: two rows, 32 keys).
- *   MI_PREFILL_TCGEN05_CLUSTER  the pair kernel in clusters of two CTAs
- *                       (adjacent row tiles of one request and KV head)
- *                       that copy the K / V stages both read once, by TMA
- *                       multicast into both.
  * MI_PREFILL_DEFAULT takes the pair kernel. All compute the same
  * definition within the same tolerance. */
 #define MI_PREFILL_DEFAULT 0
 #define MI_PREFILL_MMA 1
 #define MI_PREFILL_TCGEN05 2
 #define MI_PREFILL_TCGEN05_PAIR 3
-#define MI_PREFILL_TCGEN05_CLUSTER 4
 mi_status mi_paged_prefill_attention_variant(const mi_dims* dims, int32_t total_q, int32_t max_query_len,
                                              const void* q, const void* k_cache, const void* v_cache,
                                              const int32_t* block_tables, const int32_t* context_lens,

@@ -28,7 +28,6 @@ MI_ATTN_DEFAULT, MI_ATTN_MMA, MI_ATTN_FMA = 0, 1, 2
 MI_ADMIT_PROCEED, MI_ADMIT_SOFT_BRAKE, MI_ADMIT_HARD_BRAKE = 0, 1, 2
 MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
 MI_PREFILL_DEFAULT, MI_PREFILL_MMA, MI_PREFILL_TCGEN05, MI_PREFILL_TCGEN05_PAIR = 0, 1, 2, 3
-MI_PREFILL_TCGEN05_CLUSTER = 4
 MI_DEVERR_INTERNAL = 0x80
 
 # every symbol include/mi.h declares

@@ -192,35 +192,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// tma_load_3d delivered to the same shared-memory offset, and completing on
-// the barrier at the same offset, in every CTA of the cluster named in
-// cta_mask (bit i = cluster rank i).
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z,
-                                               uint64_t policy, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
-// This CTA's rank in its cluster.
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// One arrival, with release semantics at cluster scope, on the mbarrier at
-// shared-memory offset `bar` of the cluster's CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t rank) {
-    asm volatile(
-        "{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(bar),
-        "r"(rank)
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z,
                                             int w, uint64_t policy) {
     asm volatile(
@@ -341,27 +312,6 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
 // that kernel may write, and pdl_trigger() to let the next kernel start.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// launch_pdl for a kernel launched in clusters of `cluster` CTAs along x.
-template <typename... Args>
-inline cudaError_t launch_pdl_cluster(void (*fn)(Args...), int grid, int block, int smem, int cluster,
-                                      cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fn, args...);
-}
 
 template <typename... Args>
 inline cudaError_t launch_pdl(void (*fn)(Args...), int grid, int block, int smem, cudaStream_t s,

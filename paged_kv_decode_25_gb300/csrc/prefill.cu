@@ -73,16 +73,14 @@ struct Item {
     int r, h, q0, m, n, first, nrows, rho0, rows_here, p_hi, nblk;
 };
 
-__device__ __forceinline__ bool work_item(const PrefillParams& p, int tile_rows, Item& it, int bid = -1) {
-    const bool own = bid < 0;  // another CTA's item (bid >= 0) is worked out without error reports
-    if (own) bid = (int)blockIdx.x;
-    const int kw = bid % kTileGroup;
-    const int rest0 = bid / kTileGroup;
+__device__ __forceinline__ bool work_item(const PrefillParams& p, int tile_rows, Item& it) {
+    const int kw = blockIdx.x % kTileGroup;
+    const int rest0 = blockIdx.x / kTileGroup;
     it.h = rest0 % p.Hkv;
     const int rest = rest0 / p.Hkv;
     it.r = rest % p.R;
     const int k = (rest / p.R) * kTileGroup + kw;
-    const bool reporter = own && k == 0 && it.h == 0 && threadIdx.x == 0;  // one error report per request
+    const bool reporter = k == 0 && it.h == 0 && threadIdx.x == 0;  // one error report per request
     it.q0 = __ldg(p.query_start + it.r);
     const int q1 = __ldg(p.query_start + it.r + 1);
     it.m = q1 - it.q0;
@@ -138,13 +136,6 @@ __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
 // mbarrier.try_wait): their waiting warps share schedulers with the warps
 // issuing MMAs and computing the softmax. 0.403 ms per Qwen3-8B layer
 // against 0.412 ms polling.
-// Every thread of every CTA in the cluster arrives, then waits for all of
-// them (memory before the arrive is visible to the cluster after the wait).
-// Unbounded: each caller reaches it from every thread of both CTAs.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 __device__ __forceinline__ bool wait_pf(uint32_t bar, uint32_t parity, long long limit_ns) {
     return mbar_wait_bounded(bar, parity, limit_ns, kWaitSleepNs);
 }
@@ -914,12 +905,7 @@ struct Tc2Smem {
     static constexpr int kTotal = kTmem + 16 + 1024;  // slack to align the base to 1024 B
 };
 
-// MC: CTAs run in clusters of two (row tiles k and k + 1 of the same
-// request and KV head) and share the K/V stages both need: each CTA copies
-// half of every such stage's blocks into both CTAs' shared memory (TMA
-// multicast), and a stage's slot goes back once both CTAs' MMAs have read it
-// (their commits arrive on both CTAs' barriers).
-template <int HD, bool MC>
+template <int HD>
 __global__ void __launch_bounds__(kT2Threads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, PrefillParams p) {
@@ -936,22 +922,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     // two tiles are consecutive, tr rows apart
     const int tr = (kTcRows / p.G) * p.G;
     Item it;
-    const bool valid = work_item(p, 2 * tr, it);
-    if (!MC && !valid) return;
-    const int nst = valid ? (it.nblk + kT2Blocks - 1) / kT2Blocks : 0;
-    // stages [0, shared) are the two CTAs' common ones (the peer, with the
-    // earlier rows, reads a prefix of this CTA's blocks or this CTA of its)
-    int shared = 0, nblk_both = 0;  // nblk_both: blocks either CTA reads (the copies of shared stages)
-    uint32_t rank = 0;
-    if (MC) {
-        rank = cluster_rank();
-        Item pit;
-        if (valid && work_item(p, 2 * tr, pit, (int)(blockIdx.x ^ 1u))) {
-            shared = min(nst, (pit.nblk + kT2Blocks - 1) / kT2Blocks);
-            nblk_both = max(it.nblk, pit.nblk);
-        }
-    }
-    const bool dbl = shared > 0;  // slots are released by both CTAs: two arrivals each
+    if (!work_item(p, 2 * tr, it)) return;
+    const int nst = (it.nblk + kT2Blocks - 1) / kT2Blocks;
     const uint32_t bar = sbase + SM::kBar;
     const uint32_t q_full = bar, k_full0 = bar + 8, k_empty0 = k_full0 + 32, v_full0 = k_empty0 + 8 * kT2KSlots;
     const uint32_t v_empty0 = v_full0 + 16, s_full0 = v_empty0 + 16, p_full0 = s_full0 + 16;
@@ -961,22 +933,16 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int i = 0; i < 4; ++i) mbar_init(k_full0 + i * 8, 1);
-        for (int i = 0; i < kT2KSlots; ++i) mbar_init(k_empty0 + i * 8, dbl ? 2 : 1);
+        for (int i = 0; i < kT2KSlots; ++i) mbar_init(k_empty0 + i * 8, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(v_full0 + i * 8, 1);
-            mbar_init(v_empty0 + i * 8, dbl ? 2 : 1);
+            mbar_init(v_empty0 + i * 8, 1);
             mbar_init(s_full0 + i * 8, 1);
             mbar_init(p_full0 + i * 8, 256);  // every softmax thread of the tile
             mbar_init(o_done0 + i * 8, 1);
         }
         mbar_init(fin, 1);
         fence_mbar_init();
-    }
-    if (MC) {
-        // the peer's copies and commits may target this CTA's barriers only
-        // once they are initialised; every thread of both CTAs comes here
-        cluster_sync();
-        if (!valid) return;
     }
     if (warp == kT2MmaWarp) {
         tc::alloc(sbase + SM::kTmem, kT2Cols);
@@ -1006,31 +972,20 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             const uint32_t fb = v_full0 + sl * 8;
             if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
             __syncwarp();
-            // a stage both CTAs read: this CTA copies the blocks of its
-            // parity into both
-            const bool mc = MC && jv < shared;
-            if (pok && (!mc || (uint32_t)(lane & 1) == rank)) {
+            if (pok) {
                 // one copy per block: both 128-byte halves of its 16 rows
                 const uint32_t vd = sbase + SM::kRingV + sl * SM::kKV + lane * kH * kBlock * 128;
                 const int row0 = (pblk * p.Hkv + it.h) * kBlock;
-                if (mc)
-                    tma_load_3d_mc(vd, &tmv, fb, 0, row0, 0, policy, (uint16_t)3);
-                else
-                    tma_load_3d(vd, &tmv, fb, 0, row0, 0, policy);
+                tma_load_3d(vd, &tmv, fb, 0, row0, 0, policy);
             }
             return true;
         };
         bool pgood = true;
         // block-table entries are read a stage ahead, before the wait for
         // the slot, so their load latency is hidden
-        // blocks copied in stage jj: in a stage both CTAs read, every block
-        // either needs (both copy and expect the same bytes; each masks its
-        // own causal limit)
-        auto nblk_of = [&](int jj) { return (MC && jj < shared) ? nblk_both : it.nblk; };
         auto table_entry = [&](int jj) -> int {
             const int x = jj * kT2Blocks + lane;
-            return (lane < kT2Blocks && x < nblk_of(jj)) ? __ldg(p.block_tables + (long long)it.r * p.mbps + x)
-                                                          : -1;
+            return (lane < kT2Blocks && x < it.nblk) ? __ldg(p.block_tables + (long long)it.r * p.mbps + x) : -1;
         };
         int nblk_next = table_entry(0);
         for (int j = 0; j < nst; ++j) {
@@ -1042,33 +997,25 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 pgood = false;
                 break;
             }
-            bool ok = false;  // block `lane` is copied into this stage
-            if (lane < kT2Blocks && x < nblk_of(j)) {
+            bool ok = false;
+            if (lane < kT2Blocks && x < it.nblk) {
                 ok = blk >= 0 && blk < p.num_blocks;
                 if (!ok) raise_err(p.dev_err, MI_DEVERR_BAD_BLOCK);
             }
             const uint32_t msk = __ballot_sync(0xffffffffu, ok);
-            // the blocks this CTA's rows read (its softmax masks the rest)
-            const uint32_t own = __ballot_sync(0xffffffffu, ok && x < it.nblk);
             const uint32_t fb = k_full0 + (j & 3) * 8;
             // failure-detection test: stage 0's K is neither copied nor
             // announced, so every wait on it runs out
             const bool held = p.withhold != 0 && j == 0;
             if (lane == 0 && !held) {
-                sts32(mask0 + (j & 3) * 4, own);
+                sts32(mask0 + (j & 3) * 4, msk);
                 mbar_arrive_expect_tx(fb, (uint32_t)__popc(msk) * kH * kBlock * 128u);
             }
             __syncwarp();
-            const bool mc = MC && j < shared;
-            if (ok && !held && (!mc || (uint32_t)(lane & 1) == rank)) {
+            if (ok && !held) {
                 const uint32_t kd = sbase + SM::kRingK + sl * SM::kKV + lane * kBlock * 128;
                 const int row0 = (blk * p.Hkv + it.h) * kBlock;
-                for (int hh = 0; hh < kH; ++hh) {
-                    if (mc)
-                        tma_load_3d_mc(kd + hh * kT2Keys * 128, &tmk, fb, 0, hh, row0, policy, (uint16_t)3);
-                    else
-                        tma_load_3d(kd + hh * kT2Keys * 128, &tmk, fb, 0, hh, row0, policy);
-                }
+                for (int hh = 0; hh < kH; ++hh) tma_load_3d(kd + hh * kT2Keys * 128, &tmk, fb, 0, hh, row0, policy);
             }
             if (j > 0 && !load_v(j - 1)) {
                 pgood = false;
@@ -1110,23 +1057,12 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 }
                 tc::commit_elect(o_done0 + t * 8);
             };
-            // hand a K or V slot back: in a stage both CTAs read, on both
-            // CTAs' barriers; otherwise twice on this CTA's when the slots
-            // count two arrivals
-            auto release = [&](uint32_t b, int stage) {
-                if (MC && stage < shared) {
-                    tc::commit_elect_mc(b, (uint16_t)3);
-                } else {
-                    tc::commit_elect(b);
-                    if (dbl) tc::commit_elect(b);
-                }
-            };
             bool ok = wait_all(q_full, 0, p.wait_ns) && wait_all(k_full0, 0, p.wait_ns);
             if (ok) {
                 tc::fence_after();
                 issue_s(0, 0);
                 issue_s(1, 0);
-                release(k_empty0, 0);  // K(0) read by both tiles
+                tc::commit_elect(k_empty0);  // K(0) read by both tiles
             }
             for (int j = 0; ok && j < nst; ++j) {
                 const uint32_t ph = (uint32_t)(j & 1);
@@ -1145,10 +1081,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
                 if (!(ok = wait_all(p_full0 + 8, ph, p.wait_ns))) break;
                 tc::fence_after();
                 issue_o(1, j);
-                release(v_empty0 + (j & 1) * 8, j);  // V(j) read by both tiles
+                tc::commit_elect(v_empty0 + (j & 1) * 8);  // V(j) read by both tiles
                 if (more) {
                     issue_s(1, j + 1);
-                    release(k_empty0 + ((j + 1) % kT2KSlots) * 8, j + 1);
+                    tc::commit_elect(k_empty0 + ((j + 1) % kT2KSlots) * 8);
                 }
             }
             if (!ok && lane == 0) raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
@@ -1371,9 +1307,6 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
     }
     tc::fence_before();
-    // the peer's copies into and commits onto this CTA are over once both
-    // CTAs have drained their MMAs (every thread of both comes here)
-    if (MC && dbl) cluster_sync();
     __syncthreads();
     if (warp == kT2MmaWarp) {
         tc::fence_after();
@@ -1403,11 +1336,11 @@ bool prepare_tc() {
     return raise_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<HD>), TcSmem<HD>::kTotal, done, mu);
 }
 
-template <int HD, bool MC>
+template <int HD>
 bool prepare_tc2() {
     static std::mutex mu;
     static CUcontext done[256] = {};
-    return raise_smem_once(reinterpret_cast<const void*>(prefill_tc2_kernel<HD, MC>), Tc2Smem<HD>::kTotal, done, mu);
+    return raise_smem_once(reinterpret_cast<const void*>(prefill_tc2_kernel<HD>), Tc2Smem<HD>::kTotal, done, mu);
 }
 
 template <int HD>
@@ -1429,7 +1362,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
                   const int32_t* query_start, float scale, void* out, int32_t* dev_err, mi_stream_t stream,
                   int32_t variant) {
     if (!dims) return MI_ERR_INVALID_ARG;
-    if (variant < MI_PREFILL_DEFAULT || variant > MI_PREFILL_TCGEN05_CLUSTER) return MI_ERR_INVALID_ARG;
+    if (variant < MI_PREFILL_DEFAULT || variant > MI_PREFILL_TCGEN05_PAIR) return MI_ERR_INVALID_ARG;
     const mi_dims D = *dims;
     if (D.B < 0 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1 || total_q < 0 ||
         max_query_len < 0)
@@ -1439,8 +1372,7 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
         return MI_ERR_UNSUPPORTED;
     const int G = D.Hq / D.Hkv, HD = D.head_dim;
     // the tcgen05 tile stacks 128 / G whole tokens of a group (G <= 8)
-    const bool use_mc = variant == MI_PREFILL_TCGEN05_CLUSTER;
-    const bool use_tc2 = variant == MI_PREFILL_TCGEN05_PAIR || variant == MI_PREFILL_DEFAULT || use_mc;
+    const bool use_tc2 = variant == MI_PREFILL_TCGEN05_PAIR || variant == MI_PREFILL_DEFAULT;
     const bool use_tc = variant == MI_PREFILL_TCGEN05 || use_tc2;
     const int tc_rows = (kTcRows / G) * G;
     if ((long long)D.num_blocks * D.Hkv * kBlock * (D.head_dim / 64) > 0x7FFFFFFFLL ||
@@ -1480,23 +1412,14 @@ mi_status prefill(const mi_dims* dims, int32_t total_q, int32_t max_query_len, c
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
     if (use_tc2) {
-        const bool prepared = use_mc ? (HD == 64 ? prepare_tc2<64, true>() : prepare_tc2<128, true>())
-                                     : (HD == 64 ? prepare_tc2<64, false>() : prepare_tc2<128, false>());
-        if (!prepared) return MI_ERR_CUDA;
+        if (!(HD == 64 ? prepare_tc2<64>() : prepare_tc2<128>())) return MI_ERR_CUDA;
         CUtensorMap tq, tk, tv;
         if (!make_tmap_q_group(&tq, q, total_q, D.Hq, HD, G, tc_rows) ||
             !make_tmap_kv_halves(&tk, k_cache, rows, HD) || !make_tmap_kv_blocks(&tv, v_cache, rows, HD))
             return MI_ERR_CUDA;
-        if (use_mc)  // clusters of two CTAs; the grid is a multiple of kTileGroup
-            e = HD == 64 ? launch_pdl_cluster(prefill_tc2_kernel<64, true>, (int)grid, kT2Threads, Tc2Smem<64>::kTotal,
-                                              2, st, tq, tk, tv, p)
-                         : launch_pdl_cluster(prefill_tc2_kernel<128, true>, (int)grid, kT2Threads,
-                                              Tc2Smem<128>::kTotal, 2, st, tq, tk, tv, p);
-        else
-            e = HD == 64 ? launch_pdl(prefill_tc2_kernel<64, false>, (int)grid, kT2Threads, Tc2Smem<64>::kTotal, st, tq,
-                                      tk, tv, p)
-                         : launch_pdl(prefill_tc2_kernel<128, false>, (int)grid, kT2Threads, Tc2Smem<128>::kTotal, st,
-                                      tq, tk, tv, p);
+        e = HD == 64 ? launch_pdl(prefill_tc2_kernel<64>, (int)grid, kT2Threads, Tc2Smem<64>::kTotal, st, tq, tk, tv, p)
+                     : launch_pdl(prefill_tc2_kernel<128>, (int)grid, kT2Threads, Tc2Smem<128>::kTotal, st, tq, tk,
+                                  tv, p);
     } else if (use_tc) {
         if (!(HD == 64 ? prepare_tc<64>() : prepare_tc<128>())) return MI_ERR_CUDA;
         CUtensorMap tq, tk, tv;

@@ -99,16 +99,6 @@ __device__ __forceinline__ void commit_elect(uint32_t mbar) {
         : "memory");
 }
 
-// commit_elect arriving on the barrier at the same offset in every CTA of
-// the cluster named in cta_mask.
-__device__ __forceinline__ void commit_elect_mc(uint32_t mbar, uint16_t cta_mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-        ::"r"(mbar), "h"(cta_mask)
-        : "memory");
-}
-
 // Arrive once on the mbarrier when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void commit(uint32_t mbar) {

@@ -16,9 +16,7 @@ from workloads import (BLOCK, PREFILL_WORKLOADS, bf16_normal, history_cache,
 
 pytestmark = pytest.mark.gpu
 
-# MI_PREFILL_MMA (mma.sync tiles), MI_PREFILL_TCGEN05 (tcgen05 + tensor memory), MI_PREFILL_TCGEN05_PAIR,
-# MI_PREFILL_TCGEN05_CLUSTER
-VARIANTS = [1, 2, 3, 4]
+VARIANTS = [1, 2, 3]  # MI_PREFILL_MMA (mma.sync tiles), MI_PREFILL_TCGEN05 (tcgen05 + tensor memory), MI_PREFILL_TCGEN05_PAIR
 
 
 def _mi():

@@ -139,7 +139,7 @@ def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
     assert_attention_close(from_dev_u16(out), ref, f"{kind} after a timed-out launch")
 
 
-@pytest.mark.parametrize("variant", [2, 3, 4])  # MI_PREFILL_TCGEN05, _PAIR, _CLUSTER
+@pytest.mark.parametrize("variant", [2, 3])  # MI_PREFILL_TCGEN05, MI_PREFILL_TCGEN05_PAIR
 def test_prefill_wait_runs_out_then_recovers(cuda_device, variant):
     """The tcgen05 prefill kernels: every CTA's first K stage is withheld, so
     its MMA, softmax and P.V waits run out; no MMA is left running and the
