@@ -1,10 +1,11 @@
-"""CUDA-graph capture of the decode calls: a captured launch keeps the kernel
-arguments of the capture, the split-KV merge's epoch included, and is replayed
-many times over one workspace. Each replay must give the bits of an eager
-call. Covered on the Qwen3-8B-shaped serving layer (B = 64, contexts up to
-8k, a fragmented pool, hundreds of units cut across CTAs): the bf16 and the
-e4m3 attention and the fused step, each replayed three times, and two
-launches captured back to back on one workspace."""
+"""CUDA-graph capture of the decode and prefill calls: a captured launch
+keeps the kernel arguments of the capture, the split-KV merge's epoch
+included, and is replayed many times over one workspace. Each replay must
+give the bits of an eager call. Covered on the Qwen3-8B-shaped serving layer
+(B = 64, contexts up to 8k, a fragmented pool, hundreds of units cut across
+CTAs): the bf16 and the e4m3 attention and the bf16 and e4m3 fused steps,
+each replayed three times, and two launches captured back to back on one
+workspace; and the causal prefill attention with each of its kernels."""
 import pytest
 
 from helpers import grow, pools_for, to_dev_i32, to_dev_u16
@@ -131,3 +132,63 @@ def test_graph_replay_step(cuda_device):
     _replay_and_check(step, [qo, out], [qo_ref, out_ref], err)
     assert torch.equal(_bits(lay["kc"]), _bits(kc_ref))
     assert torch.equal(_bits(lay["vc"]), _bits(vc_ref))
+
+
+def test_graph_replay_step_fp8(cuda_device):
+    """The fused e4m3 step captured once and replayed: each replay writes the
+    same quantised cache rows and q_out and gives the eager step's output."""
+    import torch
+    mi = _mi()
+    lay = _layer(cuda_device)
+    w, d = lay["w"], lay["d"]
+    _, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    tab = torch.from_numpy(table).to(cuda_device)
+    ks = torch.full((w.Hkv,), 1.0 / 64, dtype=torch.float32, device=cuda_device)
+    vs = torch.full((w.Hkv,), 1.0 / 32, dtype=torch.float32, device=cuda_device)
+    kc = (lay["kc"].float() * 64).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc = (lay["vc"].float() * 32).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    kc_ref, vc_ref = kc.clone(), vc.clone()
+    qo_ref, out_ref = torch.empty_like(lay["q"]), torch.empty_like(lay["q"])
+    assert mi.mi_paged_decode_step_fp8(d, lay["q"], lay["k"], lay["v"], tab, w.max_pos, lay["bt"], lay["cl"], ks, vs,
+                                       w.scale, qo_ref, kc_ref, vc_ref, out_ref, _workspace(mi, d, cuda_device),
+                                       dev_err=err) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ws = _workspace(mi, d, cuda_device)
+    qo, out = torch.empty_like(qo_ref), torch.empty_like(out_ref)
+
+    def step():
+        assert mi.mi_paged_decode_step_fp8(d, lay["q"], lay["k"], lay["v"], tab, w.max_pos, lay["bt"], lay["cl"], ks,
+                                           vs, w.scale, qo, kc, vc, out, ws, dev_err=err) == 0
+    _replay_and_check(step, [qo, out], [qo_ref, out_ref], err)
+    assert torch.equal(kc, kc_ref)
+    assert torch.equal(vc, vc_ref)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])  # default (two-tile), mma.sync, single-tile tcgen05, two-tile
+def test_graph_replay_prefill(cuda_device, variant):
+    """Causal prefill attention captured once and replayed (requests with and
+    without history, G = 4): each replay gives the eager call's bits."""
+    import numpy as np
+    import torch
+    from test_prefill_gpu import _random_case
+    mi = _mi()
+    q, kc, vc, bt, n, qs = _random_case(31, 16, 4, 128, [0, 300, 1000, 5], [200, 64, 333, 1])
+    T, Hq, dh = q.shape
+    d = mi.dims(len(n), Hq, kc.shape[1], dh, kc.shape[0], bt.shape[1])
+    q_d, kc_d, vc_d = (to_dev_u16(a, cuda_device) for a in (q, kc, vc))
+    bt_d, n_d, qs_d = (to_dev_i32(a, cuda_device) for a in (bt, n, qs))
+    max_q = int(np.diff(qs).max())
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    scale = 1.0 / np.sqrt(dh)
+
+    def call(out):
+        assert mi.mi_paged_prefill_attention_variant(d, T, max_q, q_d, kc_d, vc_d, bt_d, n_d, qs_d, scale, out,
+                                                     variant=variant, dev_err=err) == 0
+    ref = torch.empty_like(q_d)
+    call(ref)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    out = torch.empty_like(ref)
+    _replay_and_check(lambda: call(out), [out], [ref], err)
