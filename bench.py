@@ -17,8 +17,10 @@ against the measured HBM copy bandwidth (one kernel per layer: the log-sum-exp
 combine of split units runs inside it). ``cpu_baseline`` = the fp64 oracle on
 the host cores on a bounded sample. The default run adds ``per_config`` (the
 Qwen3-1.7B layer, the Qwen2.5-7B 128-step sweep and the skewed batch, each
-with the oracle on the host cores) and ``per_variant.fp8`` (the same step
-over e4m3 caches, run as ``--kv fp8`` in a child process).
+with the oracle on the host cores) and ``per_variant`` records: ``fp8``
+(the same step over e4m3 caches, run as ``--kv fp8`` in a child process) and
+``prefill`` (the Qwen3-8B-shaped prefill step on the default prefill kernel,
+run as ``--workload qwen3_8b_prefill`` in a child process).
 
 ``--impl reference`` times the oracle alone (the reference arm).
 """
@@ -123,6 +125,27 @@ def fp8_variant_record(args):
                                             "avg_launch_ms", "avg_launch_source")},
             "per_layer_ms": d["per_layer_ms"], "e2e": d["e2e"], "clocks": d["clocks"],
             "command": " ".join(["python", "bench.py"] + cmd[2:])}
+
+
+def prefill_variant_record(args):
+    """The Qwen3-8B-shaped prefill step (36 layers of chunked append + causal
+    prefill attention on the default kernel), run as `bench.py --workload
+    qwen3_8b_prefill` in a child process; its headline figures, for the
+    default line."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", "qwen3_8b_prefill", "--steps",
+           str(min(args.steps, 20)), "--warmup", str(args.warmup), "--no-cpu-baseline", "--e2e-steps", "1"]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")][-1]
+        d = json.loads(line)
+    except Exception as e:  # reported, not fatal: the decode line stands on its own
+        return {"unavailable": ("%s: %s" % (type(e).__name__, e))[:200]}
+    rf = d["roofline"]
+    return {"metric": d["metric"], "value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+            "dtype": d["dtype"], "workload": d["config"]["workload"],
+            "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "kernel",
+                                            "algorithmic_flops_per_launch", "avg_launch_ms")},
+            "e2e": d["e2e"], "clocks": d["clocks"], "command": " ".join(["python", "bench.py"] + cmd[2:])}
 
 
 def arm_config(w, args):
@@ -1359,7 +1382,7 @@ def main():
         per_config = measure_configs(mi, device, peak)
     per_variant = None
     if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_variant:
-        per_variant = {"fp8": fp8_variant_record(args)}
+        per_variant = {"fp8": fp8_variant_record(args), "prefill": prefill_variant_record(args)}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": median_step_ms,
