@@ -1138,6 +1138,7 @@ def main():
     out_all = torch.empty_like(q_all)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
     bt_d, cl_d, sl_d, pos_d = i32(bt), i32(cl), i32(sl), i32(pos)
+    dev_bufs = (q_all, k_all, v_all, qo_all, out_all, bt_d, cl_d, sl_d, pos_d)
     ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = stream0 = torch.cuda.current_stream(device)
@@ -1147,8 +1148,9 @@ def main():
     # timed after it to report append and attention separately
     fused = (fp8 or variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA)) and not args.unfused
 
-    def step(ev=None, fuse=False, st=None):
+    def step(ev=None, fuse=False, st=None, bufs=None):
         stream = st if st is not None else stream0
+        q_all, k_all, v_all, qo_all, out_all, bt_d, cl_d, sl_d, pos_d = bufs if bufs is not None else dev_bufs
         for layer in range(w.layers):
             kc, vc = caches[layer]
             if fuse:
@@ -1323,52 +1325,100 @@ def main():
     e2e_steps = max(1, min(e2e_steps, headroom - e2e_warm))
     e2e_warm = min(e2e_warm, headroom - e2e_steps)
     ctx_now = cl.copy()
-    h_bt = torch.empty((w.B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory()
-    h_cl = torch.empty(w.B, dtype=torch.int32).pin_memory()
-    h_sl = torch.empty(w.B, dtype=torch.int32).pin_memory()
-    h_pos = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    seq_arr = np.asarray(seqs, np.int32)
+    # Two sets, each with pinned host buffers (tables, lengths, the step's
+    # result) and device buffers (tables, lengths, every layer's new rows and
+    # outputs) and its own captured one-step graph: step s uses set s % 2.
+    # Copies in run on one stream, the steps on another, copies out on a
+    # third, so step s + 1's inputs go in and step s - 1's result comes out
+    # while step s computes; the host fills a set once its step two back is
+    # done (copies and result).
+    def dev_set():
+        return tuple(torch.empty_like(t) for t in dev_bufs)
+
+    sets = [dict(bt=torch.empty((w.B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory(),
+                 cl=torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                 sl=torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                 pos=torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                 out=torch.empty(out_all.shape, dtype=torch.bfloat16).pin_memory(),
+                 dev=dev_set(), done=torch.cuda.Event(), inp=torch.cuda.Event(), comp=torch.cuda.Event())
+            for _ in range(2)]
     h_q = torch.stack([u16(x[0]) for x in qkv_host]).pin_memory()
     h_k = torch.stack([u16(x[1]) for x in qkv_host]).pin_memory()
     h_v = torch.stack([u16(x[2]) for x in qkv_host]).pin_memory()
-    h_out = torch.empty(out_all.shape, dtype=torch.bfloat16).pin_memory()
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    for hs in sets:  # the sets' device buffers start from the resident step's contents
+        for dst, src in zip(hs["dev"], dev_bufs):
+            dst.copy_(src)
+    torch.cuda.synchronize()
+    e2e_graphs = None
+    if g_step is not None:
+        e2e_graphs = []
+        for hs in sets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(fuse=fused, st=torch.cuda.current_stream(device), bufs=hs["dev"])
+            e2e_graphs.append(g)
     e2e_bytes = 0.0
+    e2e_no = 0
 
     def e2e_step():
-        nonlocal ctx_now, e2e_bytes
+        nonlocal ctx_now, e2e_bytes, e2e_no
+        k = e2e_no & 1
+        hs = sets[k]
+        e2e_no += 1
+        hs["done"].synchronize()  # the step two back (same set): copies done, result read
         ctx_now = ctx_now + 1
-        for b in seqs:
-            mi.check(pool.alloc(b, int(ctx_now[b])), "alloc")
-        st_, _, _, _ = mi.mi_kv_pool_batch_meta(pool.handle, seqs, w.max_blocks_per_seq, h_bt.numpy(),
-                                                h_cl.numpy(), h_sl.numpy())
+        mi.check(pool.alloc_batch(seq_arr, ctx_now.astype(np.int32)), "alloc_batch")
+        st_, _, _, _ = mi.mi_kv_pool_batch_meta(pool.handle, seqs, w.max_blocks_per_seq, hs["bt"].numpy(),
+                                                hs["cl"].numpy(), hs["sl"].numpy())
         mi.check(st_, "batch_meta")
-        h_pos.numpy()[:] = h_cl.numpy() - 1
-        copies = ((h_bt, bt_d), (h_cl, cl_d)) + (() if fused else ((h_sl, sl_d), (h_pos, pos_d))) + \
-            ((h_q, q_all), (h_k, k_all), (h_v, v_all))
-        for src, dst in copies:
-            dst.copy_(src, non_blocking=True)
-        # the same captured one-step graph as the timed region (it reads the
-        # tables, lengths and new rows from the device buffers just copied)
-        if g_step is not None:
-            g_step.replay()
+        hs["pos"].numpy()[:] = hs["cl"].numpy() - 1
+        q_d, k_d, v_d, qo_d, out_d, bt_e, cl_e, sl_e, pos_e = hs["dev"]
+        copies = ((hs["bt"], bt_e), (hs["cl"], cl_e)) + (() if fused else ((hs["sl"], sl_e), (hs["pos"], pos_e))) + \
+            ((h_q, q_d), (h_k, k_d), (h_v, v_d))
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(hs["comp"])  # the set's step two back has read its inputs
+            for src, dst in copies:
+                dst.copy_(src, non_blocking=True)
+            hs["inp"].record(s_in)
+        stream.wait_event(hs["inp"])
+        if e2e_graphs is not None:
+            e2e_graphs[k].replay()
         else:
-            step(fuse=fused)
-        h_out.copy_(out_all, non_blocking=True)
-        torch.cuda.synchronize()
-        e2e_bytes += w.layers * (attention_bytes(w, h_cl.numpy(), kvb) + append_bytes(w, kvb))
+            step(fuse=fused, bufs=hs["dev"])
+        hs["comp"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(hs["comp"])
+            hs["out"].copy_(out_d, non_blocking=True)
+            hs["done"].record(s_out)
+        e2e_bytes += w.layers * (attention_bytes(w, hs["cl"].numpy(), kvb) + append_bytes(w, kvb))
 
     for _ in range(e2e_warm):
         e2e_step()
+    torch.cuda.synchronize()
     e2e_bytes = 0.0
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
+    torch.cuda.synchronize()  # the last step's result is on the host
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    # the pipeline read back what the step computed: the same step again,
+    # eagerly, over the last set's inputs (it rewrites the same new rows)
+    # gives the host copy's bits
+    last = sets[(e2e_no - 1) & 1]
+    check_out = torch.empty_like(last["dev"][4])
+    step(fuse=fused, bufs=last["dev"][:4] + (check_out,) + last["dev"][5:])
+    torch.cuda.synchronize()
+    assert torch.equal(check_out.cpu().view(torch.int16), last["out"].view(torch.int16)), \
+        "end-to-end result differs from the step recomputed on its inputs"
     del g_step
-    h2d = sum(t.numel() * t.element_size() for t in (h_bt, h_cl, h_q, h_k, h_v)) + \
-        (0 if fused else sum(t.numel() * t.element_size() for t in (h_sl, h_pos)))
-    d2h = h_out.numel() * h_out.element_size()
+    hs = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in (hs["bt"], hs["cl"], h_q, h_k, h_v)) + \
+        (0 if fused else sum(t.numel() * t.element_size() for t in (hs["sl"], hs["pos"])))
+    d2h = hs["out"].numel() * hs["out"].element_size()
     e2e_val = world * (e2e_bytes / e2e_steps) / (e2e_s / e2e_steps) / 1e9
 
     if rank != 0:
@@ -1406,9 +1456,15 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3,
-                "path": ("per step: host pool growth and mi_kv_pool_batch_meta, H2D from pinned memory, "
-                         + ("the timed region's one-step CUDA graph" if launch_mode.startswith("cuda graph")
-                            else "stream launches") + ", D2H of every layer's output, synchronise")},
+                "path": ("per step: host pool growth (mi_kv_pool_alloc_batch) and mi_kv_pool_batch_meta into one "
+                         "of two pinned buffer sets, H2D of tables, lengths and every layer's new q/k/v from "
+                         "pinned memory, "
+                         + ("a captured one-step CUDA graph" if launch_mode.startswith("cuda graph")
+                            else "stream launches") + ", D2H of every layer's output; two sets of host and "
+                         "device buffers (a graph each), copies in and out on their own streams, so step s + 1's "
+                         "inputs go in and step s - 1's result comes out while step s computes, and the host "
+                         "prepares a set once its step two back is done; timed from the first step's host work to "
+                         "the last step's result on the host")},
         "per_config": per_config,
         "per_variant": per_variant,
         "gpu_launches": args.steps * w.layers * (1 if fused else 2),  # fused step, or append + attention

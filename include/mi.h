@@ -103,6 +103,16 @@ void mi_kv_pool_destroy(mi_kv_pool* pool);
  * MI_ERR_OUT_OF_BLOCKS: not enough free blocks; the pool is unchanged. */
 mi_status mi_kv_pool_alloc(mi_kv_pool* pool, int32_t seq_id, int32_t num_tokens);
 
+/* mi_kv_pool_alloc for a whole batch (a decode step grows every request by
+ * one token): entry i grows seq_ids[i] to num_tokens[i] tokens, in order, as
+ * count calls of mi_kv_pool_alloc would (the same tables and use order), but
+ * all or nothing: the batch is checked first, and on any error
+ * (MI_ERR_INVALID_ARG for an entry mi_kv_pool_alloc would reject,
+ * MI_ERR_OUT_OF_BLOCKS when the batch needs more blocks than are free) the
+ * pool is unchanged. Host arrays of count entries; count 0 does nothing. */
+mi_status mi_kv_pool_alloc_batch(mi_kv_pool* pool, const int32_t* seq_ids, const int32_t* num_tokens,
+                                 int32_t count);
+
 /* Return all blocks of seq_id to the free list. MI_ERR_UNKNOWN_SEQ if seq_id
  * holds no allocation. */
 mi_status mi_kv_pool_free(mi_kv_pool* pool, int32_t seq_id);

@@ -32,7 +32,7 @@ MI_DEVERR_INTERNAL = 0x80
 
 # every symbol include/mi.h declares
 EXPORTS = (
-    "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc",
+    "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc", "mi_kv_pool_alloc_batch",
     "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_token_slots",
     "mi_kv_pool_admission", "mi_kv_pool_touch", "mi_kv_pool_lru_victim", "mi_kv_pool_swap_out",
     "mi_kv_pool_swap_in", "mi_kv_copy_blocks",
@@ -74,6 +74,7 @@ def load():
             "mi_kv_pool_create": ([i32, i32, i32, i32, P, ctypes.POINTER(P)], i32),
             "mi_kv_pool_destroy": ([P], None),
             "mi_kv_pool_alloc": ([P, i32, i32], i32),
+            "mi_kv_pool_alloc_batch": ([P, P, P, i32], i32),
             "mi_kv_pool_free": ([P, i32], i32),
             "mi_kv_pool_num_free": ([P], i32),
             "mi_kv_pool_batch_meta": ([P, P, i32, P, P, P], i32),
@@ -171,6 +172,14 @@ def mi_kv_pool_alloc(handle, seq_id, num_tokens):
     return load().mi_kv_pool_alloc(handle, int(seq_id), int(num_tokens))
 
 
+def mi_kv_pool_alloc_batch(handle, seq_ids, num_tokens):
+    """seq_ids, num_tokens: sequences of ints of equal length (host)."""
+    sids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    ntok = np.ascontiguousarray(num_tokens, dtype=np.int32)
+    assert sids.shape == ntok.shape and sids.ndim == 1
+    return load().mi_kv_pool_alloc_batch(handle, _ptr(sids), _ptr(ntok), int(sids.size))
+
+
 def mi_kv_pool_free(handle, seq_id):
     return load().mi_kv_pool_free(handle, int(seq_id))
 
@@ -255,6 +264,9 @@ class Pool:
 
     def alloc(self, seq, num_tokens):
         return mi_kv_pool_alloc(self.handle, seq, num_tokens)
+
+    def alloc_batch(self, seqs, num_tokens):
+        return mi_kv_pool_alloc_batch(self.handle, seqs, num_tokens)
 
     def free(self, seq):
         return mi_kv_pool_free(self.handle, seq)

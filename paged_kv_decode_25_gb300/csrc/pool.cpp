@@ -105,6 +105,35 @@ extern "C" mi_status mi_kv_pool_alloc(mi_kv_pool* p, int32_t seq, int32_t num_to
     return MI_OK;
 }
 
+extern "C" mi_status mi_kv_pool_alloc_batch(mi_kv_pool* p, const int32_t* seq_ids, const int32_t* num_tokens,
+                                            int32_t count) {
+    if (!p || count < 0 || (count > 0 && (!seq_ids || !num_tokens))) return MI_ERR_INVALID_ARG;
+    // check the whole batch first, earlier entries applied on a copy of the
+    // state they touch, so that either every entry is made or none
+    std::vector<int64_t> size(p->tables.size(), -1), toks(p->tables.size(), -1);
+    int64_t extra_total = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        const int32_t seq = seq_ids[i], n = num_tokens[i];
+        if (seq < 0 || (size_t)seq >= p->tables.size() || n < 0) return MI_ERR_INVALID_ARG;
+        if (p->swapped[(size_t)seq]) return MI_ERR_INVALID_ARG;
+        const bool live = p->live[(size_t)seq] || size[(size_t)seq] >= 0;
+        const int64_t have = size[(size_t)seq] >= 0 ? size[(size_t)seq] : (int64_t)p->tables[(size_t)seq].size();
+        const int64_t held = toks[(size_t)seq] >= 0 ? toks[(size_t)seq] : p->tokens[(size_t)seq];
+        if (live && n < held) return MI_ERR_INVALID_ARG;
+        const int64_t need = ((int64_t)n + p->block_size - 1) / p->block_size;
+        if (need > p->max_blocks_per_seq) return MI_ERR_INVALID_ARG;
+        if (need > have) extra_total += need - have;
+        size[(size_t)seq] = need > have ? need : have;
+        toks[(size_t)seq] = n;
+    }
+    if (extra_total > (int64_t)p->free_stack.size()) return MI_ERR_OUT_OF_BLOCKS;
+    for (int32_t i = 0; i < count; ++i) {
+        const mi_status st = mi_kv_pool_alloc(p, seq_ids[i], num_tokens[i]);
+        if (st != MI_OK) return st;  // not reached: the batch was checked above
+    }
+    return MI_OK;
+}
+
 extern "C" mi_status mi_kv_pool_free(mi_kv_pool* p, int32_t seq) {
     if (!p) return MI_ERR_INVALID_ARG;
     if (seq >= 0 && (size_t)seq < p->tables.size() && p->swapped[(size_t)seq]) {

@@ -126,6 +126,64 @@ def test_pool_exhaustion_is_all_or_nothing(mi):
     assert mi.mi_kv_pool_seq_blocks(lib.handle, 1) is None
 
 
+def _state(mi, lib, S):
+    """Every sequence's table, the free count and the LRU order (victims
+    taken one after another)."""
+    tables = [None if (t := mi.mi_kv_pool_seq_blocks(lib.handle, s)) is None else t.tolist() for s in range(S)]
+    order, ex = [], []
+    while (v := mi.mi_kv_pool_lru_victim(lib.handle, ex)) >= 0:
+        order.append(v)
+        ex.append(v)
+    return tables, lib.num_free(), order
+
+
+def test_pool_alloc_batch_equals_sequential_allocs(mi):
+    """A batch grows its sequences exactly as the same allocs one by one:
+    tables, free count and use order, repeated ids included (the pool is
+    large enough that every batch fits)."""
+    r = np.random.Generator(np.random.PCG64(41))
+    S, W = 24, 32
+    N = S * W
+    order = r.permutation(N)
+    a, b = mi.Pool(N, S, W, order), mi.Pool(N, S, W, order)
+    tok = np.zeros(S, np.int64)
+    for it in range(300):
+        if r.random() < 0.2:
+            s = int(r.integers(0, S))
+            assert a.free(s) == b.free(s)
+            tok[s] = 0
+            continue
+        k = int(r.integers(1, 9))
+        seqs = r.integers(0, S, size=k)
+        ntok = []
+        for s in seqs:  # growing; repeated ids grow again
+            tok[s] = min(int(tok[s]) + int(r.integers(0, 40)), W * 16)
+            ntok.append(int(tok[s]))
+        assert a.alloc_batch(seqs, ntok) == mi.MI_OK
+        assert all(b.alloc(int(s), n) == mi.MI_OK for s, n in zip(seqs, ntok))
+        assert _state(mi, a, S) == _state(mi, b, S)
+
+
+def test_pool_alloc_batch_is_all_or_nothing(mi):
+    lib = mi.Pool(10, 4, 8)
+    assert lib.alloc_batch([0, 1], [16, 16]) == mi.MI_OK
+    before = _state(mi, lib, 4)
+    # more blocks than are free: nothing changes
+    assert lib.alloc_batch([2, 3, 0], [16 * 3, 16 * 3, 16 * 4]) == mi.MI_ERR_OUT_OF_BLOCKS  # 9 of 8 free
+    assert _state(mi, lib, 4) == before
+    # a bad entry after good ones: nothing changes
+    for seqs, ntok in (([2, 0], [16, 8]),        # shrinking sequence 0
+                       ([2, 4], [16, 16]),       # id out of range
+                       ([2, 3], [16, -1]),       # negative count
+                       ([2, 3], [16, 16 * 9]),   # wider than a table row
+                       ([2, 2], [32, 16])):      # shrinking within the batch
+        assert lib.alloc_batch(seqs, ntok) == mi.MI_ERR_INVALID_ARG
+        assert _state(mi, lib, 4) == before
+    assert lib.alloc_batch([], []) == mi.MI_OK
+    assert lib.alloc_batch([2, 2], [16, 48]) == mi.MI_OK
+    assert mi.mi_kv_pool_seq_blocks(lib.handle, 2).size == 3
+
+
 @pytest.mark.parametrize("d,theta,max_pos", [(64, 1e6, 100), (128, 1e6, 9000), (128, 1e4, 33)])
 def test_rope_table_matches_oracle_bits(mi, d, theta, max_pos):
     st, t = mi.mi_rope_table(theta, d, max_pos)
