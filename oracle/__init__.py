@@ -70,6 +70,15 @@ def _load():
             lib.or_append_fp8.restype = i32
             lib.or_paged_attention_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, i32, P, f64, P, i32]
             lib.or_paged_attention_fp8.restype = i32
+            lib.or_int8_quantize.argtypes = [P, i64, P]
+            lib.or_int8_quantize.restype = ctypes.c_float
+            lib.or_int8_from_bf16_cache.argtypes = [i32, i32, i32, i32, P, P, P, i32, P, P, i32, P, P, P, P, P, P]
+            lib.or_int8_from_bf16_cache.restype = i32
+            lib.or_append_int8.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, i32, P, i32, P, P, i32,
+                                           P, P, P, P, P, P, P]
+            lib.or_append_int8.restype = i32
+            lib.or_paged_attention_int8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, i32, P, f64, P, i32]
+            lib.or_paged_attention_int8.restype = i32
             _lib = lib
     return _lib
 
@@ -241,4 +250,77 @@ def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, con
     used = _load().or_paged_attention_fp8(B, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
                                           bt.shape[1], _p(cl), float(scale), _p(out), int(nthreads))
     paged_attention_fp8.threads_used = used
+    return out
+
+
+# ------------------------------------------------------------ INT8 KV ------
+
+GROUP = 64  # tokens per quantisation group
+
+
+def int8_quantize(x) -> tuple:
+    """One group of bf16 values (uint16 bits, any shape) -> (int8 codes of
+    the same shape, m = max |x| as a float)."""
+    x = _c(x, np.uint16)
+    codes = np.empty(x.shape, np.int8)
+    m = _load().or_int8_quantize(_p(x), x.size, _p(codes))
+    return codes, float(m)
+
+
+def int8_state(num_blocks: int, Hkv: int, d: int, num_slots: int) -> dict:
+    """Zeroed INT8 cache state: int8 caches [nb][Hkv][16][d], fp32 group
+    maxima [nb][Hkv], bf16 open-group buffers [slots][Hkv][64][d]."""
+    return {
+        "k8": np.zeros((num_blocks, Hkv, 16, d), np.int8), "v8": np.zeros((num_blocks, Hkv, 16, d), np.int8),
+        "k_amax": np.zeros((num_blocks, Hkv), np.float32), "v_amax": np.zeros((num_blocks, Hkv), np.float32),
+        "k_open": np.zeros((num_slots, Hkv, GROUP, d), np.uint16),
+        "v_open": np.zeros((num_slots, Hkv, GROUP, d), np.uint16),
+    }
+
+
+def _state_args(st):
+    for key in ("k8", "v8", "k_amax", "v_amax", "k_open", "v_open"):
+        assert st[key].flags.c_contiguous
+    return (_p(st["k8"]), _p(st["v8"]), _p(st["k_amax"]), _p(st["v_amax"]), _p(st["k_open"]), _p(st["v_open"]))
+
+
+def int8_from_bf16_cache(k_cache, v_cache, block_tables, context_lens, open_slots, st) -> int:
+    """Fill the INT8 state `st` (from int8_state) from the first
+    context_lens[b] tokens of each request held in bf16 caches (uint16
+    [nb][Hkv][16][d]) at the same slots. Returns the status."""
+    kc = _c(k_cache, np.uint16); vc = _c(v_cache, np.uint16)
+    nb, Hkv, _, d = kc.shape
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32); sl = _c(open_slots, np.int32)
+    return _load().or_int8_from_bf16_cache(cl.shape[0], Hkv, d, nb, _p(kc), _p(vc), _p(bt), bt.shape[1], _p(cl),
+                                           _p(sl), st["k_open"].shape[0], *_state_args(st))
+
+
+def append_int8(q, k, v, table, block_tables, context_lens, open_slots, st):
+    """Append one token per request (position context_lens[b] - 1) into the
+    INT8 state `st`, in place. Returns (q_out, status)."""
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k.shape[1]
+    table = _c(table, np.float32)
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32); sl = _c(open_slots, np.int32)
+    q_out = np.zeros_like(q)
+    status = _load().or_append_int8(B, Hq, Hkv, d, st["k8"].shape[0], _p(q), _p(k), _p(v), _p(table), table.shape[0],
+                                    _p(bt), bt.shape[1], _p(cl), _p(sl), st["k_open"].shape[0], _p(q_out),
+                                    *_state_args(st))
+    return q_out, status
+
+
+def paged_attention_int8(q, k8, v8, k_amax, v_amax, block_tables, context_lens, scale, nthreads=1):
+    """q uint16 [B][Hq][d]; int8 caches [nb][Hkv][16][d]; fp32 group maxima
+    [nb][Hkv]; returns float64 [B][Hq][d]."""
+    q = _c(q, np.uint16)
+    B, Hq, d = q.shape
+    Hkv = k8.shape[1]
+    kc = _c(k8, np.int8); vc = _c(v8, np.int8)
+    ka = _c(k_amax, np.float32); va = _c(v_amax, np.float32)
+    bt = _c(block_tables, np.int32); cl = _c(context_lens, np.int32)
+    out = np.empty((B, Hq, d), np.float64)
+    used = _load().or_paged_attention_int8(B, Hq, Hkv, d, _p(q), _p(kc), _p(vc), _p(ka), _p(va), _p(bt),
+                                           bt.shape[1], _p(cl), float(scale), _p(out), int(nthreads))
+    paged_attention_int8.threads_used = used
     return out

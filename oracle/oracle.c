@@ -587,3 +587,250 @@ int32_t or_paged_attention_fp8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, co
     free(jobs);
     return nthreads;
 }
+
+/* ------------------------------------------------------------ INT8 KV ---- */
+/* INT8 KV cache (nxmr.cn article, §2.2 "量化压缩的实战选择": the KV cache held
+ * in 8 bits, quantised in groups of 64 tokens rather than per token,
+ * symmetric (no zero point) with scale = 127 / max|x|, the scaled values
+ * clamped to [-128, 127] and converted to int8; per head where heads' ranges
+ * differ). Readings taken here:
+ *  - a group is 64 consecutive tokens (64g .. 64g+63) of one request and one
+ *    KV head, over all d dims; K and V are quantised separately;
+ *  - x is the bf16 value the bf16 cache would hold (after RoPE for K);
+ *  - m = max |x| over the group's tokens; s = 127 / m divided in IEEE single
+ *    precision; y = x * s multiplied in single precision; y clamped to
+ *    [-128, 127] and converted to int8 toward zero (the article's tensor
+ *    cast); m = 0 gives code 0 for every value;
+ *  - a code stands for the value code * m / 127;
+ *  - a request's last group may hold fewer than 64 tokens; it is quantised
+ *    over the tokens it holds, and again over all of them, from their
+ *    original values, whenever a token joins it (so a full group ends up
+ *    quantised over its 64 tokens, the article's definition).
+ * Storage: codes in int8 caches [num_blocks][Hkv][16][d]; m (a bf16 value
+ * held as fp32) at amax[blk][h] for every block blk the group's tokens lie
+ * in; the original bf16 rows of each request's last group in an open-group
+ * buffer [slots][Hkv][64][d] at the request's slot. Inputs are finite. */
+
+#define OR_GROUP 64
+
+/* Codes of one group of `count` bf16 values; returns m. */
+float or_int8_quantize(const uint16_t* x, int64_t count, int8_t* codes) {
+    double m = 0.0;
+    for (int64_t i = 0; i < count; ++i) {
+        const double a = fabs(or_double_from_bf16(x[i]));
+        if (a > m) m = a;
+    }
+    if (m == 0.0) {
+        memset(codes, 0, (size_t)count);
+        return 0.0f;
+    }
+    const float s = 127.0f / (float)m;  /* m is a bf16 value: exact in float */
+    for (int64_t i = 0; i < count; ++i) {
+        float y = (float)or_double_from_bf16(x[i]) * s;
+        if (y > 127.0f) y = 127.0f;
+        if (y < -128.0f) y = -128.0f;
+        codes[i] = (int8_t)(int)y;      /* C's float -> int conversion truncates toward zero */
+    }
+    return (float)m;
+}
+
+/* The group holding tokens t0 .. t0+ntok-1 of one request and head h, from
+ * its bf16 rows [ntok][d]: codes to the tokens' cache slots through the
+ * request's block table row, m to amax of every block those tokens lie in.
+ * Returns -1 (and writes nothing) if a block id is out of range. */
+static int32_t int8_group(const uint16_t* rows, int32_t ntok, int32_t d, int32_t Hkv, int32_t h,
+                          const int32_t* bt_row, int32_t t0, int32_t num_blocks, int8_t* cache, float* amax,
+                          int8_t* tmp) {
+    for (int32_t t = 0; t < ntok; ++t) {
+        const int32_t blk = bt_row[(t0 + t) / OR_BLOCK];
+        if (blk < 0 || blk >= num_blocks) return -1;
+    }
+    const float m = or_int8_quantize(rows, (int64_t)ntok * d, tmp);
+    for (int32_t t = 0; t < ntok; ++t) {
+        const int64_t blk = bt_row[(t0 + t) / OR_BLOCK], off = (t0 + t) % OR_BLOCK;
+        memcpy(cache + ((blk * Hkv + h) * OR_BLOCK + off) * d, tmp + (int64_t)t * d, (size_t)d);
+        amax[blk * Hkv + h] = m;
+    }
+    return 0;
+}
+
+/* INT8 caches of B requests whose first context_lens[b] tokens are held in
+ * bf16 caches (layout [num_blocks][Hkv][16][d]) at the same slots: every
+ * group quantised over the tokens it holds, and each request's last group
+ * copied to its open-group slot. Returns 0, or -1 if a block id or a slot is
+ * out of range (that request is skipped). */
+int32_t or_int8_from_bf16_cache(int32_t B, int32_t Hkv, int32_t d, int32_t num_blocks,
+                                const uint16_t* k_cache, const uint16_t* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* open_slots, int32_t num_slots,
+                                int8_t* k8, int8_t* v8, float* k_amax, float* v_amax,
+                                uint16_t* k_open, uint16_t* v_open) {
+    int32_t status = 0;
+    uint16_t* rk = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)OR_GROUP * d);
+    uint16_t* rv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)OR_GROUP * d);
+    int8_t* tmp = (int8_t*)malloc((size_t)OR_GROUP * d);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = context_lens[b];
+        if (n <= 0) continue;
+        const int32_t slot = open_slots[b];
+        const int32_t* bt = block_tables + (int64_t)b * max_blocks_per_seq;
+        int bad = slot < 0 || slot >= num_slots;
+        for (int32_t t = 0; t < n && !bad; t += OR_BLOCK) bad = bt[t / OR_BLOCK] < 0 || bt[t / OR_BLOCK] >= num_blocks;
+        if (bad) { status = -1; continue; }
+        for (int32_t h = 0; h < Hkv; ++h) {
+            for (int32_t t0 = 0; t0 < n; t0 += OR_GROUP) {
+                const int32_t ntok = n - t0 < OR_GROUP ? n - t0 : OR_GROUP;
+                for (int32_t t = 0; t < ntok; ++t) {
+                    const int64_t blk = bt[(t0 + t) / OR_BLOCK], off = (t0 + t) % OR_BLOCK;
+                    const int64_t src = ((blk * Hkv + h) * OR_BLOCK + off) * d;
+                    memcpy(rk + (int64_t)t * d, k_cache + src, sizeof(uint16_t) * (size_t)d);
+                    memcpy(rv + (int64_t)t * d, v_cache + src, sizeof(uint16_t) * (size_t)d);
+                }
+                (void)int8_group(rk, ntok, d, Hkv, h, bt, t0, num_blocks, k8, k_amax, tmp);
+                (void)int8_group(rv, ntok, d, Hkv, h, bt, t0, num_blocks, v8, v_amax, tmp);
+                if (t0 + OR_GROUP >= n) {  /* the last group: its rows to the open-group slot */
+                    const int64_t o = ((int64_t)slot * Hkv + h) * OR_GROUP * d;
+                    memcpy(k_open + o, rk, sizeof(uint16_t) * (size_t)ntok * d);
+                    memcpy(v_open + o, rv, sizeof(uint16_t) * (size_t)ntok * d);
+                }
+            }
+        }
+    }
+    free(rk);
+    free(rv);
+    free(tmp);
+    return status;
+}
+
+/* Append one new token per request into INT8 caches: n = context_lens[b]
+ * (the length after the append; n <= 0 appends nothing), position p = n - 1,
+ * group g = p / 64, offset o = p % 64.
+ *   q_out[b][j] = RoPE(q[b][j], p);
+ *   open[slot][h][o] = RoPE(k[b][h], p) for K, v[b][h] for V;
+ *   the group is quantised over open[slot][h][0 .. o] and its codes and m
+ *   written to tokens 64g .. p through the block table.
+ * Returns 0, or -1 if some position, slot or block id is out of range (that
+ * request's cache writes are skipped; q_out is written when p is valid). */
+int32_t or_append_int8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t num_blocks,
+                       const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const float* table, int32_t max_pos,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       const int32_t* open_slots, int32_t num_slots,
+                       uint16_t* q_out, int8_t* k8, int8_t* v8, float* k_amax, float* v_amax,
+                       uint16_t* k_open, uint16_t* v_open) {
+    int32_t status = 0;
+    int8_t* tmp = (int8_t*)malloc((size_t)OR_GROUP * d);
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t n = context_lens[b];
+        if (n <= 0) continue;
+        const int32_t p = n - 1;
+        if (p >= max_pos || n > max_blocks_per_seq * OR_BLOCK) { status = -1; continue; }
+        or_rope_rotate(q + (int64_t)b * Hq * d, Hq, d, table, p, q_out + (int64_t)b * Hq * d);
+        const int32_t slot = open_slots[b];
+        if (slot < 0 || slot >= num_slots) { status = -1; continue; }
+        const int32_t* bt = block_tables + (int64_t)b * max_blocks_per_seq;
+        const int32_t t0 = p / OR_GROUP * OR_GROUP, o = p % OR_GROUP;
+        int bad = 0;
+        for (int32_t t = t0; t <= p; t += OR_BLOCK) bad |= bt[t / OR_BLOCK] < 0 || bt[t / OR_BLOCK] >= num_blocks;
+        if (bad) { status = -1; continue; }
+        for (int32_t h = 0; h < Hkv; ++h) {
+            uint16_t* ko = k_open + ((int64_t)slot * Hkv + h) * OR_GROUP * d;
+            uint16_t* vo = v_open + ((int64_t)slot * Hkv + h) * OR_GROUP * d;
+            or_rope_rotate(k + ((int64_t)b * Hkv + h) * d, 1, d, table, p, ko + (int64_t)o * d);
+            memcpy(vo + (int64_t)o * d, v + ((int64_t)b * Hkv + h) * d, sizeof(uint16_t) * (size_t)d);
+            (void)int8_group(ko, o + 1, d, Hkv, h, bt, t0, num_blocks, k8, k_amax, tmp);
+            (void)int8_group(vo, o + 1, d, Hkv, h, bt, t0, num_blocks, v8, v_amax, tmp);
+        }
+    }
+    free(tmp);
+    return status;
+}
+
+typedef struct {
+    int32_t B, Hq, Hkv, d, max_blocks_per_seq;
+    const uint16_t* q;
+    const int8_t* k8;
+    const int8_t* v8;
+    const float* k_amax;
+    const float* v_amax;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    double scale;
+    double* out;
+    int64_t row_begin, row_end;
+} or_attn_i8_job;
+
+/* Decode attention over INT8 caches: the definition of attn_row with
+ * K_t = code * amax_k[blk][h] / 127 and V_t = code * amax_v[blk][h] / 127,
+ * blk = table[b][t/16], in double. */
+static void attn_i8_row(const or_attn_i8_job* a, int32_t b, int32_t j, double* s) {
+    const int32_t d = a->d, G = a->Hq / a->Hkv, h = j / G;
+    double* o = a->out + ((int64_t)b * a->Hq + j) * d;
+    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+    const int32_t n = a->context_lens[b];
+    if (n <= 0) return;
+    const uint16_t* qr = a->q + ((int64_t)b * a->Hq + j) * d;
+    double m = -INFINITY;
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const int8_t* kt = a->k8 + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        const double am = (double)a->k_amax[blk * a->Hkv + h];
+        double acc = 0.0;
+        for (int32_t i = 0; i < d; ++i) acc += or_double_from_bf16(qr[i]) * ((double)kt[i] * am / 127.0);
+        s[t] = a->scale * acc;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int32_t t = 0; t < n; ++t) {
+        const double w = exp(s[t] - m);
+        l += w;
+        const int64_t blk = a->block_tables[(int64_t)b * a->max_blocks_per_seq + t / OR_BLOCK];
+        const int8_t* vt = a->v8 + ((blk * a->Hkv + h) * OR_BLOCK + t % OR_BLOCK) * d;
+        const double am = (double)a->v_amax[blk * a->Hkv + h];
+        for (int32_t i = 0; i < d; ++i) o[i] += w * ((double)vt[i] * am / 127.0);
+    }
+    for (int32_t i = 0; i < d; ++i) o[i] /= l;
+}
+
+static void* attn_i8_worker(void* arg) {
+    const or_attn_i8_job* a = (const or_attn_i8_job*)arg;
+    int32_t nmax = 1;
+    for (int32_t b = 0; b < a->B; ++b)
+        if (a->context_lens[b] > nmax) nmax = a->context_lens[b];
+    double* s = (double*)malloc(sizeof(double) * (size_t)nmax);
+    for (int64_t r = a->row_begin; r < a->row_end; ++r)
+        attn_i8_row(a, (int32_t)(r / a->Hq), (int32_t)(r % a->Hq), s);
+    free(s);
+    return NULL;
+}
+
+/* INT8 paged decode attention, rows (b, j) on nthreads POSIX threads as in
+ * or_paged_attention. Returns the number of threads used. */
+int32_t or_paged_attention_int8(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, const uint16_t* q,
+                                const int8_t* k8, const int8_t* v8, const float* k_amax, const float* v_amax,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, double scale, double* out, int32_t nthreads) {
+    const int64_t rows = (int64_t)B * Hq;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = (int32_t)(rows > 0 ? rows : 1);
+    or_attn_i8_job* jobs = (or_attn_i8_job*)malloc(sizeof(or_attn_i8_job) * (size_t)nthreads);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int32_t t = 0; t < nthreads; ++t) {
+        or_attn_i8_job* a = &jobs[t];
+        a->B = B; a->Hq = Hq; a->Hkv = Hkv; a->d = d; a->max_blocks_per_seq = max_blocks_per_seq;
+        a->q = q; a->k8 = k8; a->v8 = v8; a->k_amax = k_amax; a->v_amax = v_amax;
+        a->block_tables = block_tables; a->context_lens = context_lens;
+        a->scale = scale; a->out = out;
+        a->row_begin = rows * t / nthreads;
+        a->row_end = rows * (t + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        attn_i8_worker(&jobs[0]);
+    } else {
+        for (int32_t t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, attn_i8_worker, &jobs[t]);
+        for (int32_t t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    }
+    free(th);
+    free(jobs);
+    return nthreads;
+}
