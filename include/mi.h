@@ -370,6 +370,63 @@ mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q, const voi
                                    float scale, void* q_out, void* k_cache, void* v_cache, void* out,
                                    void* workspace, size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream);
 
+/* ---- INT8 KV cache in 64-token groups (nxmr.cn article, §2.2
+ * "量化压缩的实战选择": 8-bit KV quantised per group of 64 tokens rather than
+ * per token, symmetric, scale = 127 / max|x|, the scaled values clamped to
+ * [-128, 127] and cast to int8; per head).
+ * A group is tokens 64g .. 64g+63 of one request and one KV head, over all
+ * head_dim values; K and V are quantised separately. With m = max |x| over
+ * the group's tokens (x the bf16 value the bf16 cache would hold, after RoPE
+ * for K), a value is stored as the code
+ *   c = trunc(clamp(fp32(x * fp32(127 / m)), -128, 127))
+ * (both operations IEEE single precision, truncation toward zero; m = 0 gives
+ * 0) and stands for c * m / 127. Buffers (device):
+ *   k_cache, v_cache  int8 [num_blocks][Hkv][16][head_dim], 16-byte aligned;
+ *   k_amax, v_amax    fp32 [num_blocks][Hkv]: m of the group each block's
+ *                     tokens belong to (every block of a group holds it),
+ *                     16-byte aligned, allocated to a multiple of 4 floats
+ *                     (num_blocks * Hkv rounded up: the attention copies the
+ *                     16-byte group holding a block's entry);
+ *   k_open, v_open    bf16 [num_open_slots][Hkv][64][head_dim]: the original
+ *                     values of each sequence's last, still open group, at
+ *                     the sequence's slot (open_slots[b] for request b).
+ * A group that has fewer than 64 tokens (a sequence's last) is quantised over
+ * the tokens it holds, and again from the open buffer whenever a token joins
+ * it, so a full group ends up quantised over its 64 tokens. */
+
+/* Decode append into INT8 caches, one new token per request: with n =
+ * context_lens[b] (the length after the append; n <= 0 appends nothing) and
+ * p = n - 1, q_out[b] = RoPE(q[b], p) as mi_paged_kv_append computes it; the
+ * rotated k and the v of the new token go to row p % 64 of the request's open
+ * slot, and the group of p (tokens 64(p/64) .. p) gets its codes and its m
+ * as defined above, written through block_tables[b] (its blocks must be
+ * allocated). Device errors: p >= max_pos (MI_DEVERR_BAD_POS) or n above
+ * max_blocks_per_seq * 16 (MI_DEVERR_BAD_CONTEXT) skip the request; a slot
+ * outside [0, num_open_slots) (MI_DEVERR_BAD_SLOT) or a block id of the
+ * group out of range (MI_DEVERR_BAD_BLOCK) skip its cache writes. q, k, v,
+ * q_out, rope_cos_sin and the open buffers 16-byte aligned; q_out may alias
+ * q. */
+mi_status mi_paged_kv_append_int8(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                  const float* rope_cos_sin, int32_t max_pos, const int32_t* block_tables,
+                                  const int32_t* context_lens, const int32_t* open_slots,
+                                  int32_t num_open_slots, void* q_out, void* k_cache, void* v_cache,
+                                  float* k_amax, float* v_amax, void* k_open, void* v_open, int32_t* dev_err,
+                                  mi_stream_t stream);
+
+/* mi_paged_decode_attention over INT8 caches: the same definition with
+ * K_t = c_t * k_amax[blk][h] / 127 and V_t = c_t * v_amax[blk][h] / 127,
+ * blk = block_tables[b][t / 16]. The products run on tensor cores in f16
+ * (every code is an f16 value; q is converted to f16 with one rounding, so
+ * |q| must stay below 65504), with an fp32 online softmax; each block's V
+ * factor scales the f16 probabilities relative to the largest factor seen so
+ * far in the piece. Same workspace (mi_paged_decode_workspace_bytes), errors
+ * and guarantees as mi_paged_decode_attention. */
+mi_status mi_paged_decode_attention_int8(const mi_dims* dims, const void* q, const void* k_cache,
+                                         const void* v_cache, const float* k_amax, const float* v_amax,
+                                         const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                         void* out, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                         mi_stream_t stream);
+
 /* Causal paged GQA attention for a prefill or chunked-prefill batch (NJU
  * course brief §2.1, the prefill stage of the prefill + decode loop; mini-infer
  * README "项目概述", prefill as its own pass). dims.B = R requests. Request r

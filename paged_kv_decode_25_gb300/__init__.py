@@ -40,6 +40,7 @@ EXPORTS = (
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
     "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
+    "mi_paged_kv_append_int8", "mi_paged_decode_attention_int8",
     "mi_paged_prefill_attention", "mi_paged_prefill_attention_variant", "mi_paged_decode_attention_noalloc",
     "mi_paged_decode_step", "mi_paged_decode_step_fp8", "mi_test_set_wait_limit", "mi_test_withhold_copy",
 )
@@ -98,6 +99,10 @@ def load():
             "mi_paged_decode_attention_fp8": (
                 [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
+            "mi_paged_kv_append_int8": (
+                [dims_p, P, P, P, P, i32, P, P, P, i32, P, P, P, P, P, P, P, P, P], i32),
+            "mi_paged_decode_attention_int8": (
+                [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_step": (
                 [dims_p, P, P, P, P, i32, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_step_fp8": (
@@ -378,6 +383,32 @@ def mi_paged_decode_attention_fp8(d: MiDims, q, k_cache, v_cache, k_scale, v_sca
                                                 _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
                                                 _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
                                                 int(wb), _ptr(dev_err), _stream(stream))
+
+
+def mi_paged_kv_append_int8(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, open_slots,
+                            q_out, k_cache, v_cache, k_amax, v_amax, k_open, v_open, dev_err=None, stream=None):
+    """The INT8 decode append; the open buffers' first dimension is the number
+    of open-group slots."""
+    return load().mi_paged_kv_append_int8(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
+                                          int(max_pos), _ptr(block_tables), _ptr(context_lens), _ptr(open_slots),
+                                          int(k_open.shape[0]), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_amax), _ptr(v_amax), _ptr(k_open), _ptr(v_open), _ptr(dev_err),
+                                          _stream(stream))
+
+
+def mi_paged_decode_attention_int8(d: MiDims, q, k_cache, v_cache, k_amax, v_amax, block_tables, context_lens,
+                                   scale, out, workspace, workspace_bytes=None, dev_err=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return load().mi_paged_decode_attention_int8(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                 _ptr(k_amax), _ptr(v_amax), _ptr(block_tables),
+                                                 _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
+                                                 int(wb), _ptr(dev_err), _stream(stream))
+
+
+def amax_floats(num_blocks: int, Hkv: int) -> int:
+    """Floats to allocate for a group-maxima array: num_blocks * Hkv rounded
+    up to a multiple of 4 (the attention copies 16-byte groups)."""
+    return (num_blocks * Hkv + 3) // 4 * 4
 
 
 def mi_paged_prefill_attention(d: MiDims, total_q, max_query_len, q, k_cache, v_cache, block_tables,

@@ -23,7 +23,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-ffp-contract=off",
               "-I" + INCLUDE] + ARCH
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-I" + INCLUDE]
-CU_SOURCES = ["append.cu", "decode.cu", "noalloc.cu", "prefill.cu", "swap.cu"]
+CU_SOURCES = ["append.cu", "decode.cu", "int8.cu", "noalloc.cu", "prefill.cu", "swap.cu"]
 CPP_SOURCES = ["pool.cpp"]
 
 

@@ -201,6 +201,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -255,6 +263,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     uint32_t r;
     const unsigned short h = (unsigned short)(two & 0xFFFFu);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
+// ----------------------------------------------------------------- int8 ---
+
+// Two int8 codes -> f16x2 (low half first), exact. `u` holds four codes with
+// their sign bits flipped (code + 128, offset binary); `sel` picks bytes 0-1
+// (0x4140) or 2-3 (0x4342). Each byte goes under 0x64, giving the f16 value
+// 1024 + (code + 128); subtracting 1152 leaves the code, an integer f16
+// holds exactly.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t u, uint32_t sel) {
+    const uint32_t x = __byte_perm(u, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64806480u));
     return r;
 }
 

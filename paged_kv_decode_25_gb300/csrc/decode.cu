@@ -81,6 +81,8 @@ struct AttnParams {
     float sl2;                     // scale * log2(e)
     const float* k_scale;          // [Hkv] e4m3 caches: per-head dequantisation scales
     const float* v_scale;          // [Hkv]
+    const float* k_amax;           // [num_blocks][Hkv] INT8 caches: each block's 64-token group maximum
+    const float* v_amax;           // (held in arrays of a multiple of 4 floats: copied 16 bytes at a time)
     // fused decode step only: the new token's raw q / k / v, the RoPE table,
     // q_out and the caches to write the new row into
     const uint16_t* qraw;          // [B][Hq][HD]
@@ -355,10 +357,10 @@ __device__ __forceinline__ void prefetch_share(const void* base, long long bytes
 
 // ------------------------------------------------------- smem layout ------
 
-enum { kVarMma = 1, kVarFma = 2, kVarFp8 = 3 };
+enum { kVarMma = 1, kVarFma = 2, kVarFp8 = 3, kVarInt8 = 4 };
 
-// Bytes of one cache element: bf16, or e4m3 for the FP8 variant.
-__host__ __device__ constexpr int elem_bytes(int var) { return var == kVarFp8 ? 1 : 2; }
+// Bytes of one cache element: bf16, or one byte for the e4m3 and INT8 variants.
+__host__ __device__ constexpr int elem_bytes(int var) { return var == kVarFp8 || var == kVarInt8 ? 1 : 2; }
 
 template <int HD, int EB>
 struct Tile {
@@ -366,21 +368,24 @@ struct Tile {
 };
 
 struct SmemPlan {
-    int tiles, full, empty, okf, mbuf, lbuf, obuf, xbuf, scan, flag, rplan, qring, qbar, total;
+    int tiles, full, empty, okf, amx, mbuf, lbuf, obuf, xbuf, scan, flag, rplan, qring, qbar, total;
 };
 
 // W consumer warps plus one producer warp (and, for the fused step, one RoPE
 // warp); S stages per consumer warp. The weight-exchange buffer is only needed
 // by the CUDA-core tile; the fused step adds a two-slot ring of rotated q rows
-// ([G][HD] bf16 each) with full / empty barriers.
+// ([G][HD] bf16 each) with full / empty barriers. INT8 tiles add, per stage,
+// the 16-byte groups of the K and V maxima arrays that hold the block's.
 __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma, int eb = 2,
-                                             bool fused = false) {
+                                             bool fused = false, bool amx = false) {
     SmemPlan s;
     int off = 0;
     s.tiles = off; off += W * S * 2 * kBlock * HD * eb;
     s.full = off;  off += W * S * 8;
     s.empty = off; off += W * S * 8;
-    s.okf = off;   off += W * S * 4;  // per stage: 1 when its block id was valid and copied
+    s.okf = off;   off += W * S * 4;  // per stage: nonzero when its block id was valid and copied
+    off = (off + 15) & ~15;
+    s.amx = off;   off += amx ? W * S * 32 : 0;
     s.mbuf = off;  off += W * kMaxG * 4;
     s.lbuf = off;  off += W * kMaxG * 4;
     s.obuf = off;  off += W * G * HD * 4;
@@ -690,6 +695,167 @@ struct Fp8State {
     }
 };
 
+// Tensor-core tile over INT8 K/V tiles quantised in 64-token groups: the e4m3
+// tile's data movement and fragment orders, with each code turned into an
+// f16 value exactly (i8x2_to_f16x2). A block's codes stand for code * a / 127,
+// a the maximum of its group (one per block and head, staged with the tile):
+// K's factor multiplies the block's scores; V's factor is taken relative to
+// a reference factor of the warp (the first block's, raised, with a rescale
+// of O, when a block's factor exceeds it 256-fold) and multiplies the f16
+// probabilities of the block (at most 256, so within f16's range), while the
+// running sum keeps the unscaled ones. O times the reference is the output.
+template <int HD>
+struct Int8State {
+    static constexpr int kK = HD / 16;
+    static constexpr uint32_t kFlip = 0x80808080u;  // sign bits: codes to offset binary
+    static constexpr uint32_t kLo = 0x4140u, kHi = 0x4342u;
+    uint32_t qb[kK][2];
+    float o[kK][4];
+    float m[2], l[2];
+    float sl2, vref, rvref;
+
+    __device__ __forceinline__ void reset(const AttnParams& p) {
+#pragma unroll
+        for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
+        sl2 = p.sl2 * (1.f / 127.f);
+        vref = 0.f;
+        rvref = 0.f;
+    }
+
+    __device__ __forceinline__ void begin_unit(const AttnParams& p, int b, int h, int lane) {
+        const int n = lane >> 2, c = lane & 3;
+        const bool ok = n < p.G;
+        const uint16_t* qrow = p.q + ((long long)b * p.Hq + (long long)h * p.G + (ok ? n : 0)) * HD;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk) {
+            const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c)) : make_uint2(0, 0);
+            qb[kk][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));  // dims 4c, 4c+1
+            qb[kk][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));  // dims 4c+2, 4c+3
+        }
+        reset(p);
+    }
+
+    __device__ __forceinline__ void begin_unit_from(const uint16_t*, const AttnParams& p, int, int) { reset(p); }
+
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, int lane, float ak, float av) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            float c1[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulation chain (odd k-slices)
+            const int mi = lane >> 3;
+            const int tok = (lane & 7) + (mi & 1) * 8;
+#pragma unroll
+            for (int kp = 0; kp < kK / 2; ++kp) {
+                uint32_t r0, r1, r2, r3;  // tokens g / g+8 of k-slices 2kp / 2kp+1
+                ldsm_x4(kt + swz8<HD>(tok, 2 * kp + (mi >> 1)), r0, r1, r2, r3);
+                r0 ^= kFlip;
+                r1 ^= kFlip;
+                r2 ^= kFlip;
+                r3 ^= kFlip;
+                mma_f16_16816(c, i8x2_to_f16x2(r0, kLo), i8x2_to_f16x2(r1, kLo), i8x2_to_f16x2(r0, kHi),
+                              i8x2_to_f16x2(r1, kHi), qb[2 * kp][0], qb[2 * kp][1]);
+                mma_f16_16816(c1, i8x2_to_f16x2(r2, kLo), i8x2_to_f16x2(r3, kLo), i8x2_to_f16x2(r2, kHi),
+                              i8x2_to_f16x2(r3, kHi), qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] += c1[i];
+        }
+        const float ks = sl2 * ak;  // scale * log2(e) * a_k / 127
+        const int t0 = lane >> 2, t1 = t0 + 8;
+        float s0 = t0 < valid ? c[0] * ks : kNegInf;
+        float s1 = t0 < valid ? c[1] * ks : kNegInf;
+        float s2 = t1 < valid ? c[2] * ks : kNegInf;
+        float s3 = t1 < valid ? c[3] * ks : kNegInf;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float r0 = mn0 == kNegInf ? 0.f : mn0, r1 = mn1 == kNegInf ? 0.f : mn1;
+        float al0 = ex2(m[0] - r0), al1 = ex2(m[1] - r1);
+        m[0] = mn0;
+        m[1] = mn1;
+        const float p0 = ex2(s0 - r0), p1 = ex2(s1 - r1), p2 = ex2(s2 - r0), p3 = ex2(s3 - r1);
+        l[0] = l[0] * al0 + (p0 + p2);
+        l[1] = l[1] * al1 + (p1 + p3);
+        // V's factor relative to the reference (the same for every lane)
+        const float fv = av * (1.f / 127.f);
+        float ov0 = al0, ov1 = al1;  // O's factors for this block
+        if (fv > vref * 256.f) {
+            const float f = vref * (1.f / fv);  // 0 for the first nonzero factor (O is still 0)
+            ov0 *= f;
+            ov1 *= f;
+            vref = fv;
+            rvref = 1.f / fv;
+        }
+        const float rel = fv * rvref;
+        const uint32_t x0 = pack_f16x2(p0 * rel, p1 * rel);
+        const uint32_t x1 = pack_f16x2(p2 * rel, p3 * rel);
+        if (__any_sync(0xffffffffu, ov0 != 1.f || ov1 != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < kK; ++mt) {
+                o[mt][0] *= ov0;
+                o[mt][1] *= ov1;
+                o[mt][2] *= ov0;
+                o[mt][3] *= ov1;
+            }
+        }
+        const uint32_t b0 = movmatrix_trans(x0), b1 = movmatrix_trans(x1);
+        {
+            const int g = lane >> 2, cc = lane & 3;
+#pragma unroll
+            for (int t = 0; t < kK / 2; ++t) {
+                // dims 4j .. 4j+3, j = 8t + g, of token rows 2cc, 2cc+1, 2cc+8, 2cc+9
+                const int chunk = 2 * t + (g >> 2), inb = (g & 3) * 4;
+                const uint32_t w0 = lds32(vt + swz8<HD>(2 * cc, chunk) + inb);
+                const uint32_t w1 = lds32(vt + swz8<HD>(2 * cc + 1, chunk) + inb);
+                const uint32_t w2 = lds32(vt + swz8<HD>(2 * cc + 8, chunk) + inb);
+                const uint32_t w3 = lds32(vt + swz8<HD>(2 * cc + 9, chunk) + inb);
+                const uint32_t lo01 = __byte_perm(w0, w1, 0x5140) ^ kFlip, hi01 = __byte_perm(w0, w1, 0x7362) ^ kFlip;
+                const uint32_t lo89 = __byte_perm(w2, w3, 0x5140) ^ kFlip, hi89 = __byte_perm(w2, w3, 0x7362) ^ kFlip;
+                mma_f16_16816(o[2 * t], i8x2_to_f16x2(lo01, kLo), i8x2_to_f16x2(lo01, kHi), i8x2_to_f16x2(lo89, kLo),
+                              i8x2_to_f16x2(lo89, kHi), b0, b1);
+                mma_f16_16816(o[2 * t + 1], i8x2_to_f16x2(hi01, kLo), i8x2_to_f16x2(hi01, kHi),
+                              i8x2_to_f16x2(hi89, kLo), i8x2_to_f16x2(hi89, kHi), b0, b1);
+            }
+        }
+    }
+
+    // Reduce the per-thread sums and write (m, l, O * reference) of this warp to smem.
+    __device__ __forceinline__ void store(float* mbuf, float* lbuf, float* obuf, int G, int lane) {
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], sh);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], sh);
+        }
+        const int h0 = (lane & 3) * 2, h1 = h0 + 1;
+        if (lane < 4) {
+            if (h0 < G) { mbuf[h0] = m[0]; lbuf[h0] = l[0]; }
+            if (h1 < G) { mbuf[h1] = m[1]; lbuf[h1] = l[1]; }
+        }
+        const int r = lane >> 2;
+#pragma unroll
+        for (int t = 0; t < kK / 2; ++t) {
+            const int d0 = 4 * (8 * t + r);
+            if (h0 < G) {
+                obuf[h0 * HD + d0] = o[2 * t][0] * vref;
+                obuf[h0 * HD + d0 + 1] = o[2 * t][2] * vref;
+                obuf[h0 * HD + d0 + 2] = o[2 * t + 1][0] * vref;
+                obuf[h0 * HD + d0 + 3] = o[2 * t + 1][2] * vref;
+            }
+            if (h1 < G) {
+                obuf[h1 * HD + d0] = o[2 * t][1] * vref;
+                obuf[h1 * HD + d0 + 1] = o[2 * t][3] * vref;
+                obuf[h1 * HD + d0 + 2] = o[2 * t + 1][1] * vref;
+                obuf[h1 * HD + d0 + 3] = o[2 * t + 1][3] * vref;
+            }
+        }
+    }
+};
+
 // CUDA-core tile. Lane (r, c): c = lane % LPR picks a 16-byte chunk (8 dims)
 // of a K/V row, r = lane / LPR a row group; the lane handles tokens r + RG*i.
 // Partial dot products (TPL tokens x GP heads per lane) are summed over the
@@ -849,6 +1015,8 @@ template <int HD, int GP>
 struct StateOf<HD, kVarFma, GP> { using T = FmaState<HD, GP>; };
 template <int HD, int GP>
 struct StateOf<HD, kVarFp8, GP> { using T = Fp8State<HD>; };
+template <int HD, int GP>
+struct StateOf<HD, kVarInt8, GP> { using T = Int8State<HD>; };
 
 // A bounded wait by every lane of a warp; true when all of them saw the phase.
 __device__ __forceinline__ bool wait_all_warp(uint32_t bar, uint32_t parity, long long limit_ns,
@@ -874,18 +1042,19 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // consumer warp that streams that block copies the two rows into its staged
 // tiles.
 template <int HD, int VAR, int GP, int W, bool FUSED = false>
-__global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && !FUSED ? 3 : 2)
+__global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 || VAR == kVarInt8) && !FUSED ? 3 : 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
-    // e4m3 waits sleep between polls (the hint of mbarrier.try_wait), bf16
-    // ones poll: 2.415 against 2.440 ms per e4m3 step, 4.02 against 3.98
-    // ms per bf16 step
-    constexpr uint32_t kSleep = VAR == kVarFp8 ? kWaitSleepNs : 0u;
+    // e4m3 (and INT8) waits sleep between polls (the hint of
+    // mbarrier.try_wait), bf16 ones poll: 2.415 against 2.440 ms per e4m3
+    // step, 4.02 against 3.98 ms per bf16 step
+    constexpr bool kOneByte = VAR == kVarFp8 || VAR == kVarInt8;
+    constexpr uint32_t kSleep = kOneByte ? kWaitSleepNs : 0u;
     static_assert(!FUSED || VAR == kVarMma || VAR == kVarFp8, "the fused step runs the MMA or e4m3 tile");
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = p.stages;
-    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma, elem_bytes(VAR), FUSED);
+    const SmemPlan sp = smem_plan(W, S, HD, p.G, VAR == kVarFma, elem_bytes(VAR), FUSED, VAR == kVarInt8);
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     uint8_t* base = smem_raw + pad;
@@ -922,8 +1091,8 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && 
 
     // Ranges are cut by cost: a unit weighs its blocks plus a fixed number of
     // blocks for its per-unit work (q, the merge, the pipeline restart at its
-    // boundary), which weighs more against the half-size e4m3 blocks.
-    constexpr int uc = VAR == kVarFp8 ? kUnitCostE4m3 : kUnitCostBf16;
+    // boundary), which weighs more against the half-size one-byte blocks.
+    constexpr int uc = kOneByte ? kUnitCostE4m3 : kUnitCostBf16;
     const int cta = blockIdx.x;
     RangePlan* rp = reinterpret_cast<RangePlan*>(base + sp.rplan);
     long long TB = 0, TC = 0;
@@ -1204,11 +1373,25 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && 
                 mbar_arrive(bar);  // the consumer skips the block
             } else {
                 const uint32_t dst = my_tiles + stg * (2 * kTile);
-                sts32(okf, 1u);
-                mbar_arrive_expect_tx(bar, 2 * kTile);
-                const int y = (blk * p.Hkv + cu.h) * (kTile / 128);  // the tile's first 128-byte line
-                tma_load_2d(dst, &tmk, bar, 0, y, policy);
-                tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
+                const int e = blk * p.Hkv + cu.h;
+                const int y = e * (kTile / 128);  // the tile's first 128-byte line
+                if constexpr (VAR == kVarInt8) {
+                    // with the tiles, the 16-byte groups of the maxima
+                    // arrays holding this block's (the flag says which of
+                    // the four it is)
+                    const uint32_t am = sbase + sp.amx + ((uint32_t)(lane * S) + stg) * 32;
+                    sts32(okf, 1u + (uint32_t)(e & 3));
+                    mbar_arrive_expect_tx(bar, 2 * kTile + 32);
+                    tma_load_2d(dst, &tmk, bar, 0, y, policy);
+                    tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
+                    bulk_load(am, p.k_amax + (e & ~3), 16, bar);
+                    bulk_load(am + 16, p.v_amax + (e & ~3), 16, bar);
+                } else {
+                    sts32(okf, 1u);
+                    mbar_arrive_expect_tx(bar, 2 * kTile);
+                    tma_load_2d(dst, &tmk, bar, 0, y, policy);
+                    tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
+                }
             }
             if (++stg == (uint32_t)S) {
                 stg = 0;
@@ -1275,10 +1458,13 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && 
             const int j = (int)(x - cu.start);
             const int valid = min(kBlock, nvalid - j * kBlock);
             // the producer's flag (published by its arrive) says whether the block was copied
-            if (!dead && lds32(sbase + sp.okf + si * 4) != 0u) {
+            const uint32_t okv = dead ? 0u : lds32(sbase + sp.okf + si * 4);
+            if (okv != 0u) {
                 const uint32_t kt = sbase + sp.tiles + si * (2 * kTile), vt = kt + kTile;
-                if (VAR != kVarFma && valid < kBlock) {
-                    // rows past the context may hold any bits: zero V there
+                // rows past the context may hold any bits: zero V there (they
+                // meet zero weights, which clear every finite value; INT8
+                // codes always are)
+                if (VAR != kVarFma && VAR != kVarInt8 && valid < kBlock) {
                     constexpr int kChunks = HD * elem_bytes(VAR) / 16;  // 16-byte chunks per token row
                     for (int i = lane; i < (kBlock - valid) * kChunks; i += 32) {
                         const int row = valid + i / kChunks, ch = i % kChunks;
@@ -1316,7 +1502,11 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, VAR == kVarFp8 && 
                         __syncwarp();
                     }
                 }
-                if constexpr (VAR != kVarFma) {
+                if constexpr (VAR == kVarInt8) {
+                    // the block's K and V group maxima, staged with the tiles
+                    const uint32_t am = sbase + sp.amx + si * 32 + (okv - 1u) * 4;
+                    st.block(kt, vt, valid, lane, __uint_as_float(lds32(am)), __uint_as_float(lds32(am + 16)));
+                } else if constexpr (VAR != kVarFma) {
                     st.block(kt, vt, valid, p.sl2, lane);
                 } else {
                     st.block(kt, vt, valid, p.sl2, lane, xbuf, p.G);
@@ -1470,24 +1660,26 @@ constexpr int kSmemTwoPerSm = 115712;     // per CTA so that two fit in an SM's 
 constexpr int kSmemThreePerSm = 76800;    // per CTA so that three fit
 
 // Stages per consumer warp: as many as fit with two CTAs per SM, else (very
-// wide GQA groups) as many as fit one CTA. e4m3 tiles are half the size, so
-// they take up to twice the stages, and first try for three CTAs per SM with
-// at least two stages each.
+// wide GQA groups) as many as fit one CTA. One-byte (e4m3, INT8) tiles are
+// half the size, so they take up to twice the stages, and first try for
+// three CTAs per SM with at least two stages each.
 int pick_stages(int HD, int G, int var, bool fused = false) {
-    const bool fma = var == kVarFma;
+    const bool fma = var == kVarFma, amx = var == kVarInt8;
     const int eb = elem_bytes(var), top = kMaxStages * 2 / eb;
-    if (var == kVarFp8 && !fused)
+    if ((var == kVarFp8 || var == kVarInt8) && !fused)
         for (int S = top; S >= 2; --S)
-            if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemThreePerSm) return S;
+            if (smem_plan(kWarps, S, HD, G, fma, eb, fused, amx).total <= kSmemThreePerSm) return S;
     for (int S = top; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemTwoPerSm) return S;
+        if (smem_plan(kWarps, S, HD, G, fma, eb, fused, amx).total <= kSmemTwoPerSm) return S;
     for (int S = top; S >= 1; --S)
-        if (smem_plan(kWarps, S, HD, G, fma, eb, fused).total <= kSmemLimit) return S;
+        if (smem_plan(kWarps, S, HD, G, fma, eb, fused, amx).total <= kSmemLimit) return S;
     return 0;
 }
 
 int smem_of(int HD, int G, int var, bool fused = false) {
-    return smem_plan(kWarps, pick_stages(HD, G, var, fused), HD, G, var == kVarFma, elem_bytes(var), fused).total;
+    return smem_plan(kWarps, pick_stages(HD, G, var, fused), HD, G, var == kVarFma, elem_bytes(var), fused,
+                     var == kVarInt8)
+        .total;
 }
 
 int gp_of(int G) { return G <= 2 ? 2 : (G <= 4 ? 4 : 8); }
@@ -1507,6 +1699,8 @@ KernelFn pick_kernel(int HD, int var, int G) {
     // the MMA tiles always span 8 head columns; the FMA tile is sized to G
     if (var == kVarMma) return HD == 64 ? attn_kernel<64, kVarMma, 8, kWarps> : attn_kernel<128, kVarMma, 8, kWarps>;
     if (var == kVarFp8) return HD == 64 ? attn_kernel<64, kVarFp8, 8, kWarps> : attn_kernel<128, kVarFp8, 8, kWarps>;
+    if (var == kVarInt8)
+        return HD == 64 ? attn_kernel<64, kVarInt8, 8, kWarps> : attn_kernel<128, kVarInt8, 8, kWarps>;
     return HD == 64 ? fma_kernel_for<64>(gp_of(G)) : fma_kernel_for<128>(gp_of(G));
 }
 
@@ -1574,7 +1768,7 @@ int slot_floats(const mi_dims& D) { return (D.Hq / D.Hkv) * D.head_dim + 8; }
 int max_grid(const mi_dims& D) {
     const int G = D.Hq / D.Hkv;
     int g = 0;
-    for (int var : {kVarMma, kVarFma, kVarFp8}) {
+    for (int var : {kVarMma, kVarFma, kVarFp8, kVarInt8}) {
         if (!pick_stages(D.head_dim, G, var)) return 0;
         const int n = grid_for(pick_kernel(D.head_dim, var, G), smem_of(D.head_dim, G, var));
         if (n <= 0) return 0;
@@ -1658,8 +1852,9 @@ struct StepArgs {
 };
 
 // Checks, plans and launches one attention call of variant `var` (bf16 caches
-// for kVarMma / kVarFma, e4m3 caches with per-head scales for kVarFp8); with
-// `step`, the fused decode step (q is then the raw q; MMA tile).
+// for kVarMma / kVarFma, e4m3 caches with per-head scales for kVarFp8, INT8
+// caches with per-block group maxima in k_scale / v_scale for kVarInt8);
+// with `step`, the fused decode step (q is then the raw q; MMA tile).
 mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, const void* v_cache,
                     const float* k_scale, const float* v_scale, const int32_t* block_tables,
                     const int32_t* context_lens, float scale, void* out, void* workspace,
@@ -1671,7 +1866,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     if (D.B == 0) return MI_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return MI_ERR_INVALID_ARG;
-    if (var == kVarFp8 && (!k_scale || !v_scale)) return MI_ERR_INVALID_ARG;
+    if ((var == kVarFp8 || var == kVarInt8) && (!k_scale || !v_scale)) return MI_ERR_INVALID_ARG;
+    if (var == kVarInt8 && (!aligned16(k_scale) || !aligned16(v_scale))) return MI_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
         !aligned16(workspace))
         return MI_ERR_INVALID_ARG;
@@ -1710,8 +1906,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
 
     CUtensorMap tk, tv;
     const long long rows = (long long)D.num_blocks * D.Hkv * kBlock;
-    const bool maps = var == kVarFp8 ? make_tmap8(&tk, k_cache, rows, HD) && make_tmap8(&tv, v_cache, rows, HD)
-                                     : make_tmap(&tk, k_cache, rows, HD) && make_tmap(&tv, v_cache, rows, HD);
+    const bool maps = elem_bytes(var) == 1 ? make_tmap8(&tk, k_cache, rows, HD) && make_tmap8(&tv, v_cache, rows, HD)
+                                           : make_tmap(&tk, k_cache, rows, HD) && make_tmap(&tv, v_cache, rows, HD);
     if (!maps) return MI_ERR_CUDA;
 
     AttnParams p;
@@ -1738,8 +1934,10 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.slot_floats = slot_floats(D);
     p.grid = grid;
     p.sl2 = scale * 1.4426950408889634f;
-    p.k_scale = k_scale;
-    p.v_scale = v_scale;
+    p.k_scale = var == kVarFp8 ? k_scale : nullptr;
+    p.v_scale = var == kVarFp8 ? v_scale : nullptr;
+    p.k_amax = var == kVarInt8 ? k_scale : nullptr;
+    p.v_amax = var == kVarInt8 ? v_scale : nullptr;
     p.qraw = static_cast<const uint16_t*>(q);
     p.knew = step ? static_cast<const uint16_t*>(step->k) : nullptr;
     p.vnew = step ? static_cast<const uint16_t*>(step->v) : nullptr;
@@ -1817,4 +2015,14 @@ extern "C" mi_status mi_paged_decode_attention(const mi_dims* dims, const void* 
     return mi_paged_decode_attention_variant(dims, q, k_cache, v_cache, block_tables, context_lens, scale,
                                              out, workspace, workspace_bytes, dev_err, stream,
                                              MI_ATTN_DEFAULT, 0);
+}
+
+extern "C" mi_status mi_paged_decode_attention_int8(const mi_dims* dims, const void* q, const void* k_cache,
+                                                    const void* v_cache, const float* k_amax, const float* v_amax,
+                                                    const int32_t* block_tables, const int32_t* context_lens,
+                                                    float scale, void* out, void* workspace,
+                                                    size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream) {
+    using namespace mi;
+    return attention(dims, q, k_cache, v_cache, k_amax, v_amax, block_tables, context_lens, scale, out,
+                     workspace, workspace_bytes, dev_err, stream, kVarInt8, 0);
 }

@@ -1,0 +1,238 @@
+// mi_paged_kv_append_int8: the decode append into INT8 KV caches quantised in
+// groups of 64 tokens (nxmr.cn article, §2.2 "量化压缩的实战选择": 8-bit KV,
+// quantised per 64-token group rather than per token, symmetric, scale =
+// 127 / max|x|, the scaled values clamped to [-128, 127] and cast to int8,
+// a cast that truncates toward zero; per head).
+//
+// A group is 64 consecutive tokens of one request and one KV head, over all
+// dims, with K and V quantised separately. Its maximum m = max|x| (a bf16
+// value, kept as fp32) is stored for every block of the group at
+// amax[block][head]; a code c stands for c * m / 127. The last group of a
+// request is open: its tokens keep their bf16 values in an open-group buffer
+// [slot][Hkv][64][d] (one slot per sequence), and each new token is quantised
+// with the group's current maximum. When the new row raises the maximum,
+// every row of the group is quantised again from that buffer; otherwise only
+// the new row is (with an unchanged maximum the other rows' codes come out
+// the same), so a full group ends up quantised over its 64 tokens.
+//
+// One CTA per request: all its threads rotate the request's q heads (RoPE as
+// mi_paged_kv_append computes it, the same bits), then each warp takes (KV
+// head, K or V) items: the new row (k rotated, v as given) into the open
+// buffer, the row maximum by a warp reduction, and the codes of the new row
+// or of the whole group.
+#include "common.cuh"
+#include "rope.cuh"
+
+namespace mi {
+namespace {
+
+constexpr int kGroup = 64;
+constexpr int kAppendThreads = 256;
+
+struct Int8AppendParams {
+    const uint16_t* q;             // [B][Hq][d] raw
+    const uint16_t* k;             // [B][Hkv][d] raw
+    const uint16_t* v;             // [B][Hkv][d]
+    const float2* rope;            // [max_pos][d/2] (cos, sin)
+    const int32_t* block_tables;   // [B][mbps]
+    const int32_t* context_lens;   // [B], length after the append
+    const int32_t* open_slots;     // [B]
+    uint16_t* q_out;               // [B][Hq][d]
+    int8_t* kc;                    // [num_blocks][Hkv][16][d]
+    int8_t* vc;
+    float* k_amax;                 // [num_blocks][Hkv]
+    float* v_amax;
+    uint16_t* k_open;              // [num_slots][Hkv][64][d]
+    uint16_t* v_open;
+    int32_t* dev_err;
+    int Hq, Hkv, d, num_blocks, mbps, max_pos, num_slots;
+};
+
+// Code of one value with s = 127 / m: x * s in single precision, clamped to
+// [-128, 127], truncated toward zero.
+__device__ __forceinline__ uint32_t code_of(float x, float s) {
+    const float y = fminf(fmaxf(__fmul_rn(x, s), -128.f), 127.f);
+    return (uint32_t)__float2int_rz(y) & 0xFFu;
+}
+
+// Codes of a bf16 pair (one 32-bit word), first value in the low byte.
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, float s) {
+    return code_of(bf16_lo(w), s) | (code_of(bf16_hi(w), s) << 8);
+}
+
+__device__ __forceinline__ float absmax_pair(uint32_t w) {
+    return fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)));
+}
+
+__global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendParams a) {
+    // inputs may come from the kernel just before this one in the stream
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = a.d, half = d / 2, words = d / 4;  // words: 32-bit words per half row
+    const int n = __ldg(a.context_lens + b);
+    if (n <= 0) return;  // nothing to append
+    const int p = n - 1;
+    if (p >= a.max_pos || n > a.mbps * kBlock) {
+        if (tid == 0) raise_err(a.dev_err, p >= a.max_pos ? MI_DEVERR_BAD_POS : MI_DEVERR_BAD_CONTEXT);
+        return;
+    }
+    const float2* cs_row = a.rope + (long long)p * half;
+
+    // q heads: each item is one word of the first half and the matching word
+    // of the second half of a head; both are loaded before anything is
+    // stored, so q_out may alias q
+    for (int i = tid; i < a.Hq * words; i += blockDim.x) {
+        const int head = i / words, w = i - head * words;
+        const uint16_t* src = a.q + ((long long)b * a.Hq + head) * d;
+        const uint32_t xl = *reinterpret_cast<const uint32_t*>(src + 2 * w);
+        const uint32_t xh = *reinterpret_cast<const uint32_t*>(src + 2 * w + half);
+        const float4 cs = *reinterpret_cast<const float4*>(cs_row + 2 * w);
+        uint32_t yl, yh;
+        if (rotate_word_fast(xl, xh, cs, yl, yh)) {
+            const uint2 y = rotate_word_exact(xl, xh, cs);
+            yl = y.x;
+            yh = y.y;
+        }
+        uint16_t* dst = a.q_out + ((long long)b * a.Hq + head) * d;
+        *reinterpret_cast<uint32_t*>(dst + 2 * w) = yl;
+        *reinterpret_cast<uint32_t*>(dst + 2 * w + half) = yh;
+    }
+
+    const int slot = __ldg(a.open_slots + b);
+    if (slot < 0 || slot >= a.num_slots) {
+        if (tid == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SLOT);
+        return;
+    }
+    const int t0 = p / kGroup * kGroup, o = p - t0;  // the group's first token, the new token's offset
+    const int j0 = t0 / kBlock, jp = p / kBlock;      // the group's first block, the new token's block
+    const int32_t* bt = a.block_tables + (long long)b * a.mbps;
+    bool ok = true;
+    for (int j = j0; j <= jp; ++j) {
+        const int blk = __ldg(bt + j);
+        ok &= blk >= 0 && blk < a.num_blocks;
+    }
+    if (!ok) {
+        if (tid == 0) raise_err(a.dev_err, MI_DEVERR_BAD_BLOCK);
+        return;
+    }
+
+    // lane l owns words l (dims 2l, 2l+1) and l + words (dims half + 2l, +1)
+    // of every row; lanes past `words` (d = 64) own nothing
+    const bool own = lane < words;
+    const int nw = blockDim.x >> 5;
+    for (int item = warp; item < 2 * a.Hkv; item += nw) {
+        const int h = item >> 1;
+        const bool is_v = (item & 1) != 0;
+        const long long nofs = ((long long)b * a.Hkv + h) * d;
+        uint32_t yl = 0u, yh = 0u;
+        if (own) {
+            const uint16_t* src = (is_v ? a.v : a.k) + nofs;
+            const uint32_t xl = *reinterpret_cast<const uint32_t*>(src + 2 * lane);
+            const uint32_t xh = *reinterpret_cast<const uint32_t*>(src + 2 * lane + half);
+            if (is_v) {
+                yl = xl;
+                yh = xh;
+            } else {
+                const float4 cs = *reinterpret_cast<const float4*>(cs_row + 2 * lane);
+                if (rotate_word_fast(xl, xh, cs, yl, yh)) {
+                    const uint2 y = rotate_word_exact(xl, xh, cs);
+                    yl = y.x;
+                    yh = y.y;
+                }
+            }
+        }
+        uint16_t* grp = (is_v ? a.v_open : a.k_open) + ((long long)slot * a.Hkv + h) * kGroup * d;
+        if (own) {
+            *reinterpret_cast<uint32_t*>(grp + (long long)o * d + 2 * lane) = yl;
+            *reinterpret_cast<uint32_t*>(grp + (long long)o * d + 2 * lane + half) = yh;
+        }
+        float rmax = own ? fmaxf(absmax_pair(yl), absmax_pair(yh)) : 0.f;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, sh));
+        float* amax = is_v ? a.v_amax : a.k_amax;
+        int8_t* cache = is_v ? a.vc : a.kc;
+        // the group's maximum so far (held by its first block), none for a new group
+        const float m_old = o > 0 ? __ldcg(amax + (long long)__ldg(bt + j0) * a.Hkv + h) : 0.f;
+        const float m = fmaxf(m_old, rmax);
+        const float s = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;  // m = 0: every code is 0
+        if (o > 0 && m > m_old) {
+            // the maximum grew: the whole group again, from its bf16 rows
+            __syncwarp();
+            for (int t = 0; t <= o; ++t) {
+                const int blk = __ldg(bt + (t0 + t) / kBlock);
+                int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + (t0 + t) % kBlock) * d;
+                if (own) {
+                    const uint32_t wl = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane);
+                    const uint32_t wh = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane + half);
+                    *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(wl, s);
+                    *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(wh, s);
+                }
+            }
+            for (int j = j0 + lane; j <= jp; j += 32) amax[(long long)__ldg(bt + j) * a.Hkv + h] = m;
+        } else {
+            const int blk = __ldg(bt + jp);
+            int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + p % kBlock) * d;
+            if (own) {
+                *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(yl, s);
+                *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(yh, s);
+            }
+            if (lane == 0) amax[(long long)blk * a.Hkv + h] = m;  // a new block of the group gets m too
+        }
+    }
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+}  // namespace
+}  // namespace mi
+
+extern "C" mi_status mi_paged_kv_append_int8(const mi_dims* dims, const void* q, const void* k, const void* v,
+                                             const float* rope_cos_sin, int32_t max_pos,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             const int32_t* open_slots, int32_t num_open_slots, void* q_out,
+                                             void* k_cache, void* v_cache, float* k_amax, float* v_amax,
+                                             void* k_open, void* v_open, int32_t* dev_err, mi_stream_t stream) {
+    using namespace mi;
+    if (!dims) return MI_ERR_INVALID_ARG;
+    const mi_dims D = *dims;
+    if (D.B < 0 || D.B > 0x7FFFFFFF || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1 ||
+        max_pos < 1 || num_open_slots < 1)
+        return MI_ERR_INVALID_ARG;
+    if (D.block_size != kBlock || (D.head_dim != 64 && D.head_dim != 128) || D.Hq % D.Hkv != 0)
+        return MI_ERR_UNSUPPORTED;
+    if ((long long)D.num_blocks * D.Hkv * kBlock * D.head_dim > (1LL << 46)) return MI_ERR_INVALID_ARG;
+    if (D.B == 0) return MI_OK;
+    if (!q || !k || !v || !rope_cos_sin || !block_tables || !context_lens || !open_slots || !q_out || !k_cache ||
+        !v_cache || !k_amax || !v_amax || !k_open || !v_open)
+        return MI_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) || !aligned(rope_cos_sin, 16) ||
+        !aligned(k_open, 16) || !aligned(v_open, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_amax, 4) || !aligned(v_amax, 4))
+        return MI_ERR_INVALID_ARG;
+    Int8AppendParams a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.rope = reinterpret_cast<const float2*>(rope_cos_sin);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.open_slots = open_slots;
+    a.q_out = static_cast<uint16_t*>(q_out);
+    a.kc = static_cast<int8_t*>(k_cache);
+    a.vc = static_cast<int8_t*>(v_cache);
+    a.k_amax = k_amax;
+    a.v_amax = v_amax;
+    a.k_open = static_cast<uint16_t*>(k_open);
+    a.v_open = static_cast<uint16_t*>(v_open);
+    a.dev_err = dev_err;
+    a.Hq = D.Hq;
+    a.Hkv = D.Hkv;
+    a.d = D.head_dim;
+    a.num_blocks = D.num_blocks;
+    a.mbps = D.max_blocks_per_seq;
+    a.max_pos = max_pos;
+    a.num_slots = num_open_slots;
+    const cudaError_t e = launch_pdl(append_int8_kernel, (int)D.B, kAppendThreads, 0, (cudaStream_t)stream, a);
+    return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}

@@ -321,6 +321,33 @@ PREFILL_WORKLOADS = {
 }
 
 
+def device_int8_cache(w: Workload, layer: int, device):
+    """INT8 caches of one layer on the device, as a decode over INT8 caches
+    sees them: codes round(N(0,1) * 127 / 4) clamped to [-127, 127], and for
+    every block and KV head a group maximum uniform in [3.5, 4.5] (what a
+    64-token group of N(0,1) values gives), in arrays of num_blocks * Hkv
+    floats rounded up to a multiple of 4. Seeded torch CUDA generator.
+    Returns (k_codes, v_codes, k_amax, v_amax)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed * 1000 + 500 + layer)
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    n_amax = (w.num_blocks * w.Hkv + 3) // 4 * 4
+    out = []
+    for _ in range(2):
+        c = torch.empty(shape, dtype=torch.int8, device=device)
+        flat = c.view(-1)
+        chunk = 1 << 28
+        for s0 in range(0, flat.numel(), chunk):
+            e = min(flat.numel(), s0 + chunk)
+            x = torch.randn(e - s0, generator=g, device=device) * (127.0 / 4.0)
+            flat[s0:e].copy_(x.round_().clamp_(-127, 127).to(torch.int8))
+        out.append(c)
+    for _ in range(2):
+        out.append(3.5 + torch.rand(n_amax, generator=g, device=device))
+    return tuple(out)
+
+
 def prefill_setup_pool(w: PrefillWorkload, pool) -> None:
     """Give request r (sequence id r) history[r] + new[r] tokens, in order."""
     h, n = w.lengths()
