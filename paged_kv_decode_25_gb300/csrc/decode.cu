@@ -289,11 +289,19 @@ struct RangePlan {
 // only on the context lengths, the dims, the grid and the kernel, and every
 // layer of a decode step has the same lengths, so each later layer's CTA
 // finds its range here instead of recomputing the scan. An entry is used only
-// when its key and its copy of all B lengths equal the launch's exactly (a
-// stale or uninitialised entry then cannot match), and a CTA reads and writes
-// only its own entry. The lengths follow the header: int32 lens[B].
+// when its key (which names the CTA) and its copy of all B lengths equal the
+// launch's exactly and its hash matches its plan words, and a CTA reads and
+// writes only its own entry. The CTA in the key matters when a workspace is
+// given at another address over memory that still holds entries (a buffer
+// freed and handed out again at a shifted offset): the entry found at a
+// CTA's position may then be another CTA's. The hash catches an entry whose
+// plan words were overwritten (the same memory used as the workspace of
+// other dims) while its key and lengths survived. The lengths follow the
+// header: int32 lens[B].
 struct PlanEntry {
-    int32_t key[8];                // kPlanMagic, kind, B, Hkv, mbps, grid, uc, P
+    int32_t key[8];                // kPlanMagic, kind, B, Hkv, mbps, grid, uc, CTA
+    int32_t P;
+    uint32_t sum;                  // plan_sum of (P, TB, TC, rp)
     long long TB, TC;
     RangePlan rp;
 };
@@ -301,6 +309,31 @@ constexpr int32_t kPlanMagic = 0x6E616C50;  // "Plan"
 constexpr int kPlanMaxB = 1024;               // larger batches always compute their plan
 __host__ __device__ inline int plan_stride_for(int B) {
     return B > kPlanMaxB ? 0 : (int)((sizeof(PlanEntry) + 4 * (size_t)B + 127) / 128 * 128);
+}
+
+// Hash of an entry's plan words (P, TB, TC, then the range plan as 32-bit
+// words, rp in shared memory), each mixed with its position; every lane of
+// the calling warp gets the same value.
+__device__ uint32_t plan_sum(int P, long long TB, long long TC, const RangePlan* rp, int lane) {
+    constexpr int nrp = (int)(sizeof(RangePlan) / 4);
+    uint32_t h = 0;
+    for (int i = lane; i < 5 + nrp; i += 32) {
+        uint32_t v;
+        if (i == 0)
+            v = (uint32_t)P;
+        else if (i < 3)
+            v = (uint32_t)((unsigned long long)TB >> (32 * (i - 1)));
+        else if (i < 5)
+            v = (uint32_t)((unsigned long long)TC >> (32 * (i - 3)));
+        else
+            v = reinterpret_cast<const uint32_t*>(rp)[i - 5];
+        uint32_t x = (v ^ (0x9E3779B9u * (uint32_t)(i + 1))) * 0x85EBCA6Bu;
+        x ^= x >> 15;
+        h ^= x * 0xC2B2AE35u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) h ^= __shfl_xor_sync(0xffffffffu, h, o);
+    return h;
 }
 
 // Every thread of the CTA calls this after plan_scan. The ranges are of equal
@@ -1100,24 +1133,21 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
     // this CTA's plan from an earlier launch with the same lengths, if any
     PlanEntry* pe = p.plan_cache ? reinterpret_cast<PlanEntry*>(p.plan_cache + (long long)cta * p.plan_stride)
                                  : nullptr;
-    const int32_t key[6] = {kPlanMagic, p.plan_kind, p.B, p.Hkv, p.mbps, (int32_t)gridDim.x};
+    const int32_t key[8] = {kPlanMagic, p.plan_kind, p.B, p.Hkv, p.mbps, (int32_t)gridDim.x, uc, cta};
     bool hit = false;
     if (pe) {
         bool same = true;
-        if (tid < 6) same = __ldcg(pe->key + tid) == key[tid];
-        if (tid == 6) same = __ldcg(pe->key + 6) == uc;
+        if (tid < 8) same = __ldcg(pe->key + tid) == key[tid];
         const int32_t* lens = reinterpret_cast<const int32_t*>(pe + 1);
         for (int b = tid; b < p.B; b += blockDim.x) same &= __ldcg(lens + b) == __ldg(p.context_lens + b);
         hit = __syncthreads_and(same) != 0;
     }
     if (hit) {
         if (tid == 0) {
-            TB = __ldcg(&pe->TB);
-            TC = __ldcg(&pe->TC);
-            P = __ldcg(pe->key + 7);
-            scan[0] = TB;
-            scan[1] = TC;
-            scan[2] = P;
+            scan[0] = __ldcg(&pe->TB);
+            scan[1] = __ldcg(&pe->TC);
+            scan[2] = __ldcg(&pe->P);
+            scan[3] = (long long)__ldcg(&pe->sum);
         }
         const int nw = (int)(sizeof(RangePlan) / 4);
         for (int i = tid; i < nw; i += blockDim.x)
@@ -1126,7 +1156,14 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
         TB = scan[0];
         TC = scan[1];
         P = (int)scan[2];
-    } else {
+        if (warp == 0) {
+            const uint32_t h = plan_sum(P, TB, TC, rp, lane);
+            if (lane == 0) scan[4] = h == (uint32_t)scan[3] ? 1 : 0;
+        }
+        __syncthreads();
+        hit = scan[4] != 0;  // a damaged entry: the plan is computed below
+    }
+    if (!hit) {
         TB = plan_scan(p, uc, scan, TC);  // (ends with a barrier of all warps)
         // CTAs that take part: the whole grid, unless that leaves fewer than
         // kMinBlocksPerCta blocks each (a small batch): every CTA's fixed cost
@@ -1143,12 +1180,15 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
             const int nw = (int)(sizeof(RangePlan) / 4);
             for (int i = tid; i < nw; i += blockDim.x)
                 reinterpret_cast<int32_t*>(&pe->rp)[i] = reinterpret_cast<const int32_t*>(rp)[i];
-            if (tid == 0) {
-                pe->TB = TB;
-                pe->TC = TC;
-                pe->key[7] = P;
-                pe->key[6] = uc;
-                for (int i = 0; i < 6; ++i) pe->key[i] = key[i];
+            if (warp == 0) {
+                const uint32_t h = plan_sum(P, TB, TC, rp, lane);
+                if (lane == 0) {
+                    pe->TB = TB;
+                    pe->TC = TC;
+                    pe->P = P;
+                    pe->sum = h;
+                    for (int i = 0; i < 8; ++i) pe->key[i] = key[i];
+                }
             }
         }
     }
