@@ -44,6 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import (BLOCK, PREFILL_WORKLOADS, WORKLOADS, context_lengths, device_fill_cache,  # noqa: E402
+                       device_int8_cache,
                        history_cache, initial_free_order, new_token_values, prefill_new_values,
                        prefill_setup_pool, setup_pool)
 
@@ -72,6 +73,32 @@ def append_bytes(w, kvb=2):
     written = w.B * w.Hq * w.head_dim * 2 + w.B * 2 * w.Hkv * w.head_dim * kvb
     rope_rows = w.B * (w.head_dim // 2) * 8
     return new + written + rope_rows + 8 * w.B
+
+
+def int8_extra_attention_bytes(w, lens):
+    """The INT8 attention's bytes beyond its one-byte K/V tiles: the K and V
+    group maxima of every block and KV head it reads (4 bytes each)."""
+    lens = np.maximum(np.asarray(lens, np.int64), 0)
+    return 8 * int(np.sum(-(-lens // BLOCK))) * w.Hkv
+
+
+def int8_extra_append_bytes(w):
+    """The INT8 append's bytes beyond append_bytes(w, 1): the new k and v rows
+    also written in bf16 to the open-group buffer, the group maxima read and
+    written, the open slots read. (When a new row raises its group's maximum,
+    the group's earlier rows are read back and quantised again: data
+    dependent, not counted.)"""
+    return w.B * 2 * w.Hkv * w.head_dim * 2 + w.B * 2 * w.Hkv * 8 + 4 * w.B
+
+
+def step_kv_bytes(w, lens, kv):
+    """Algorithmic bytes of one layer of the decode step (append + attention)
+    for KV cache type kv ("bf16", "fp8", "int8")."""
+    kvb = 2 if kv == "bf16" else 1
+    b = attention_bytes(w, lens, kvb) + append_bytes(w, kvb)
+    if kv == "int8":
+        b += int8_extra_attention_bytes(w, lens) + int8_extra_append_bytes(w)
+    return b
 
 
 def fp8_scales(w):
@@ -106,11 +133,12 @@ def describe(w):
             "parallelism": "replicas"}
 
 
-def fp8_variant_record(args):
-    """The same serving step over e4m3 caches (the fused e4m3 decode step),
-    run as `bench.py --kv fp8` in a child process with this run's steps and
-    warm-up; its headline figures, for the default line."""
-    cmd = [sys.executable, os.path.abspath(__file__), "--kv", "fp8", "--steps", str(args.steps), "--warmup",
+def kv_variant_record(args, kv):
+    """The same serving step over one-byte caches (kv "fp8": the fused e4m3
+    decode step; "int8": the INT8 append and attention), run as `bench.py
+    --kv <kv>` in a child process with this run's steps and warm-up; its
+    headline figures, for the default line."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--kv", kv, "--steps", str(args.steps), "--warmup",
            str(args.warmup), "--no-cpu-baseline", "--e2e-steps", "3"]
     try:
         r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
@@ -151,9 +179,12 @@ def prefill_variant_record(args):
 def arm_config(w, args):
     """The `config` object of a decode line; the GPU arm and the reference
     arm print the same one."""
-    fp8 = args.kv == "fp8"
-    return dict(describe(w), variant=args.variant if not fp8 else "fp8 tensor-core tile",
-                kv_cache="e4m3, per-KV-head fp32 scales" if fp8 else "bf16")
+    if args.kv == "fp8":
+        return dict(describe(w), variant="fp8 tensor-core tile", kv_cache="e4m3, per-KV-head fp32 scales")
+    if args.kv == "int8":
+        return dict(describe(w), variant="int8 tensor-core tile",
+                    kv_cache="int8, symmetric per 64-token group and KV head (group maxima per block)")
+    return dict(describe(w), variant=args.variant, kv_cache="bf16")
 
 
 def measured_peak(key="hbm_gbs"):
@@ -1055,8 +1086,9 @@ def main():
                          "per CTA) or pair (the default: two Q tiles per CTA)")
     ap.add_argument("--unfused", action="store_true",
                     help="decode: time append and attention as two calls instead of the fused step")
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
-                    help="KV cache element type of the decode step (fp8: e4m3 with per-head scales)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8", "int8"],
+                    help="KV cache element type of the decode step (fp8: e4m3 with per-head scales; int8: "
+                         "symmetric 64-token groups)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default: the workload's); fewer only for small profiling runs")
@@ -1091,10 +1123,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     variant = {"default": mi.MI_ATTN_DEFAULT, "mma": mi.MI_ATTN_MMA, "fma": mi.MI_ATTN_FMA}[args.variant]
-    fp8 = args.kv == "fp8"
-    kvb = 1 if fp8 else 2
-    if fp8 and not w.device_fill:
-        raise SystemExit("--kv fp8 is measured on the device-filled serving workload")
+    fp8, int8 = args.kv == "fp8", args.kv == "int8"
+    kvb = 1 if (fp8 or int8) else 2
+    if (fp8 or int8) and not w.device_fill:
+        raise SystemExit("--kv %s is measured on the device-filled serving workload" % args.kv)
 
     # ---- workload: pool history, caches, new-token values (one replica per rank)
     ctx = context_lengths(w)
@@ -1111,6 +1143,12 @@ def main():
     ks_h, vs_h = fp8_scales(w)
     ks_d, vs_d = torch.from_numpy(ks_h).to(device), torch.from_numpy(vs_h).to(device)
     for layer in range(w.layers):
+        if int8:
+            # codes, group maxima and each sequence's open-group rows (slot b)
+            k8, v8, ka, va = device_int8_cache(w, layer + 1000 * rank, device)
+            ko = torch.zeros((w.B, w.Hkv, 64, w.head_dim), dtype=torch.bfloat16, device=device)
+            caches.append((k8, v8, ka, va, ko, torch.zeros_like(ko)))
+            continue
         kc = torch.empty(shape, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
         vc = torch.empty_like(kc)
         if fp8:
@@ -1138,6 +1176,7 @@ def main():
     out_all = torch.empty_like(q_all)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(device)  # noqa: E731
     bt_d, cl_d, sl_d, pos_d = i32(bt), i32(cl), i32(sl), i32(pos)
+    open_slots_d = i32(np.arange(w.B))
     dev_bufs = (q_all, k_all, v_all, qo_all, out_all, bt_d, cl_d, sl_d, pos_d)
     ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
@@ -1146,13 +1185,13 @@ def main():
     # the fused step (append + attention in one launch per layer; bf16 caches
     # on the MMA tile, or e4m3 caches) is the timed path; the two calls are
     # timed after it to report append and attention separately
-    fused = (fp8 or variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA)) and not args.unfused
+    fused = (fp8 or variant in (mi.MI_ATTN_DEFAULT, mi.MI_ATTN_MMA)) and not args.unfused and not int8
 
     def step(ev=None, fuse=False, st=None, bufs=None):
         stream = st if st is not None else stream0
         q_all, k_all, v_all, qo_all, out_all, bt_d, cl_d, sl_d, pos_d = bufs if bufs is not None else dev_bufs
         for layer in range(w.layers):
-            kc, vc = caches[layer]
+            kc, vc = caches[layer][:2]
             if fuse:
                 if ev is not None:
                     ev[layer][0].record(stream)
@@ -1168,7 +1207,12 @@ def main():
                 if ev is not None:
                     ev[layer][1].record(stream)
                 continue
-            if fp8:
+            if int8:
+                _, _, ka, va, ko, vo = caches[layer]
+                mi.check(mi.mi_paged_kv_append_int8(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos,
+                                                    bt_d, cl_d, open_slots_d, qo_all[layer], kc, vc, ka, va, ko, vo,
+                                                    err, stream), "append (int8)")
+            elif fp8:
                 mi.check(mi.mi_paged_kv_append_fp8(d, q_all[layer], k_all[layer], v_all[layer], pos_d, sl_d, rope,
                                                    max_pos, qo_all[layer], kc, vc, ks_d, vs_d, err, stream),
                          "append")
@@ -1177,7 +1221,11 @@ def main():
                                                max_pos, qo_all[layer], kc, vc, err, stream), "append")
             if ev is not None:
                 ev[layer][0].record(stream)
-            if fp8:
+            if int8:
+                mi.check(mi.mi_paged_decode_attention_int8(d, qo_all[layer], kc, vc, ka, va, bt_d, cl_d, w.scale,
+                                                           out_all[layer], ws, dev_err=err, stream=stream),
+                         "attention (int8)")
+            elif fp8:
                 mi.check(mi.mi_paged_decode_attention_fp8(d, qo_all[layer], kc, vc, ks_d, vs_d, bt_d, cl_d, w.scale,
                                                           out_all[layer], ws, dev_err=err, stream=stream),
                          "attention")
@@ -1283,14 +1331,15 @@ def main():
         kern_avg_ms, kern_src = graph_events["ms_per_timed_kernel"], "events around each launch, captured in a graph"
     else:
         kern_avg_ms, kern_src = stream_launch["ms_per_timed_kernel"], "events around each stream launch"
-    a_bytes = attention_bytes(w, cl, kvb)
-    step_bytes = w.layers * (a_bytes + append_bytes(w, kvb))
+    a_bytes = attention_bytes(w, cl, kvb) + (int8_extra_attention_bytes(w, cl) if int8 else 0)
+    ap_bytes = append_bytes(w, kvb) + (int8_extra_append_bytes(w) if int8 else 0)
+    step_bytes = w.layers * step_kv_bytes(w, cl, args.kv)
     value = whole_job_rate(step_bytes, step_ms * 1e-3, world) / 1e9
     peak, peak_kind = measured_peak()
     # the dominant kernel: the fused step (its bytes include the append's), or the attention
-    k_bytes = a_bytes + (append_bytes(w, kvb) if fused else 0)
+    k_bytes = a_bytes + (ap_bytes if fused else 0)
     achieved = k_bytes / (kern_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(w.name + ("_fp8" if fp8 else "") + ("_step" if fused else ""))
+    traffic = recorded_traffic(w.name + ("_fp8" if fp8 else "_int8" if int8 else "") + ("_step" if fused else ""))
 
     # append and attention timed separately (the two calls), for the split
     if fused:
@@ -1375,7 +1424,7 @@ def main():
         mi.check(st_, "batch_meta")
         hs["pos"].numpy()[:] = hs["cl"].numpy() - 1
         q_d, k_d, v_d, qo_d, out_d, bt_e, cl_e, sl_e, pos_e = hs["dev"]
-        copies = ((hs["bt"], bt_e), (hs["cl"], cl_e)) + (() if fused else ((hs["sl"], sl_e), (hs["pos"], pos_e))) + \
+        copies = ((hs["bt"], bt_e), (hs["cl"], cl_e)) + (() if fused or int8 else ((hs["sl"], sl_e), (hs["pos"], pos_e))) + \
             ((h_q, q_d), (h_k, k_d), (h_v, v_d))
         with torch.cuda.stream(s_in):
             s_in.wait_event(hs["comp"])  # the set's step two back has read its inputs
@@ -1392,7 +1441,7 @@ def main():
             s_out.wait_event(hs["comp"])
             hs["out"].copy_(out_d, non_blocking=True)
             hs["done"].record(s_out)
-        e2e_bytes += w.layers * (attention_bytes(w, hs["cl"].numpy(), kvb) + append_bytes(w, kvb))
+        e2e_bytes += w.layers * step_kv_bytes(w, hs["cl"].numpy(), args.kv)
 
     for _ in range(e2e_warm):
         e2e_step()
@@ -1417,7 +1466,7 @@ def main():
     del g_step
     hs = sets[0]
     h2d = sum(t.numel() * t.element_size() for t in (hs["bt"], hs["cl"], h_q, h_k, h_v)) + \
-        (0 if fused else sum(t.numel() * t.element_size() for t in (hs["sl"], hs["pos"])))
+        (0 if fused or int8 else sum(t.numel() * t.element_size() for t in (hs["sl"], hs["pos"])))
     d2h = hs["out"].numel() * hs["out"].element_size()
     e2e_val = world * (e2e_bytes / e2e_steps) / (e2e_s / e2e_steps) / 1e9
 
@@ -1428,29 +1477,32 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = time_oracle(w)
     per_config = None
-    if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_config:
+    if world == 1 and w.name == "qwen3_8b" and args.kv == "bf16" and not args.no_per_config:
         per_config = measure_configs(mi, device, peak)
     per_variant = None
-    if world == 1 and w.name == "qwen3_8b" and not fp8 and not args.no_per_variant:
-        per_variant = {"fp8": fp8_variant_record(args), "prefill": prefill_variant_record(args)}
+    if world == 1 and w.name == "qwen3_8b" and args.kv == "bf16" and not args.no_per_variant:
+        per_variant = {"fp8": kv_variant_record(args, "fp8"), "int8": kv_variant_record(args, "int8"),
+                       "prefill": prefill_variant_record(args)}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "median_ms_per_step": median_step_ms,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8e4m3 KV, bf16 q/out" if fp8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("fp8e4m3 KV, bf16 q/out" if fp8 else "int8 KV, bf16 q/out" if int8 else "bf16"),
+        "data": "synthetic",
         "config": arm_config(w, args),
         "steps_per_s": 1e3 / step_ms * world,
         "hbm_frac_step": value / world / peak,
         "per_layer_ms": {"step": step_ms / w.layers, "fused_step_kernel": kern_avg_ms if fused else None,
                          "append": app_avg_ms, "attention": attn_avg_ms,
                          "append+attention (two calls)": two_call_step_ms / w.layers,
-                         "append_bytes": append_bytes(w, kvb), "attention_bytes": a_bytes},
+                         "append_bytes": ap_bytes, "attention_bytes": a_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": ("fused decode step (RoPE + cache write of the new token%s, split-KV attention, "
                                 "LSE combine), per layer" % (" quantised to e4m3" if fp8 else "") if fused else
-                                "paged decode attention (split-KV kernel with the LSE combine of cut units fused), "
-                                "per layer"),
+                                "paged decode attention%s (split-KV kernel with the LSE combine of cut units fused), "
+                                "per layer" % (" over INT8 caches (group maxima staged with each block)" if int8
+                                               else "")),
                      "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": kern_avg_ms,
                      "avg_launch_source": kern_src},
         "cpu_baseline": cpu,

@@ -384,9 +384,7 @@ mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q, const voi
  *   k_cache, v_cache  int8 [num_blocks][Hkv][16][head_dim], 16-byte aligned;
  *   k_amax, v_amax    fp32 [num_blocks][Hkv]: m of the group each block's
  *                     tokens belong to (every block of a group holds it),
- *                     16-byte aligned, allocated to a multiple of 4 floats
- *                     (num_blocks * Hkv rounded up: the attention copies the
- *                     16-byte group holding a block's entry);
+ *                     4-byte aligned;
  *   k_open, v_open    bf16 [num_open_slots][Hkv][64][head_dim]: the original
  *                     values of each sequence's last, still open group, at
  *                     the sequence's slot (open_slots[b] for request b).

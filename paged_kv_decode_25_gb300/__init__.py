@@ -406,9 +406,8 @@ def mi_paged_decode_attention_int8(d: MiDims, q, k_cache, v_cache, k_amax, v_ama
 
 
 def amax_floats(num_blocks: int, Hkv: int) -> int:
-    """Floats to allocate for a group-maxima array: num_blocks * Hkv rounded
-    up to a multiple of 4 (the attention copies 16-byte groups)."""
-    return (num_blocks * Hkv + 3) // 4 * 4
+    """Floats of a group-maxima array: one per block and KV head."""
+    return num_blocks * Hkv
 
 
 def mi_paged_prefill_attention(d: MiDims, total_q, max_query_len, q, k_cache, v_cache, block_tables,

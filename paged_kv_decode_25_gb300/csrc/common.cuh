@@ -117,6 +117,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Raises the barrier's expected transaction bytes without arriving (the
+// caller arrives later, after writes the waiters must see).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -201,14 +207,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned) from global to shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -278,6 +276,13 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t u, uint32_t sel) {
     uint32_t r;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64806480u));
     return r;
+}
+
+// The same pair without the subtraction: f16 values 1152 + code, exact. A
+// caller that multiplies them on tensor cores takes 1152 times the other
+// operand's sum back off the result.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2_biased(uint32_t u, uint32_t sel) {
+    return __byte_perm(u, 0x64646464u, sel);
 }
 
 // Two fp32 -> e4m3 codes (lo in the low byte), nearest-even, saturating to

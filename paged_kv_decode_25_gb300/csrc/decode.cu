@@ -82,7 +82,7 @@ struct AttnParams {
     const float* k_scale;          // [Hkv] e4m3 caches: per-head dequantisation scales
     const float* v_scale;          // [Hkv]
     const float* k_amax;           // [num_blocks][Hkv] INT8 caches: each block's 64-token group maximum
-    const float* v_amax;           // (held in arrays of a multiple of 4 floats: copied 16 bytes at a time)
+    const float* v_amax;
     // fused decode step only: the new token's raw q / k / v, the RoPE table,
     // q_out and the caches to write the new row into
     const uint16_t* qraw;          // [B][Hq][HD]
@@ -408,7 +408,7 @@ struct SmemPlan {
 // warp); S stages per consumer warp. The weight-exchange buffer is only needed
 // by the CUDA-core tile; the fused step adds a two-slot ring of rotated q rows
 // ([G][HD] bf16 each) with full / empty barriers. INT8 tiles add, per stage,
-// the 16-byte groups of the K and V maxima arrays that hold the block's.
+// the block's K and V group maxima.
 __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool fma, int eb = 2,
                                              bool fused = false, bool amx = false) {
     SmemPlan s;
@@ -418,7 +418,7 @@ __host__ __device__ inline SmemPlan smem_plan(int W, int S, int HD, int G, bool 
     s.empty = off; off += W * S * 8;
     s.okf = off;   off += W * S * 4;  // per stage: nonzero when its block id was valid and copied
     off = (off + 15) & ~15;
-    s.amx = off;   off += amx ? W * S * 32 : 0;
+    s.amx = off;   off += amx ? W * S * 8 : 0;
     s.mbuf = off;  off += W * kMaxG * 4;
     s.lbuf = off;  off += W * kMaxG * 4;
     s.obuf = off;  off += W * G * HD * 4;
@@ -729,32 +729,52 @@ struct Fp8State {
 };
 
 // Tensor-core tile over INT8 K/V tiles quantised in 64-token groups: the e4m3
-// tile's data movement and fragment orders, with each code turned into an
-// f16 value exactly (i8x2_to_f16x2). A block's codes stand for code * a / 127,
-// a the maximum of its group (one per block and head, staged with the tile):
-// K's factor multiplies the block's scores; V's factor is taken relative to
-// a reference factor of the warp (the first block's, raised, with a rescale
-// of O, when a block's factor exceeds it 256-fold) and multiplies the f16
-// probabilities of the block (at most 256, so within f16's range), while the
-// running sum keeps the unscaled ones. O times the reference is the output.
+// tile's data movement and fragment orders. Each code enters the MMAs as the
+// f16 value 1152 + code (a byte permute, exact), and the bias is taken back
+// off the results: from the scores, 1152 times the sum of the head's q (a
+// constant per head, folded into the scaling FMA); from O, 1152 times the
+// sum of the f16 probabilities that went into the PV products (summed per
+// lane like the running sum and subtracted once, at the store). A block's
+// codes stand for code * a / 127, a the maximum of its group (one per block
+// and head, staged with the tile): K's factor multiplies the block's scores;
+// V's factor is taken relative to a reference factor of the warp (the first
+// block's, raised, with a rescale of O, when a block's factor exceeds it
+// 256-fold) and multiplies the f16 probabilities of the block (at most 256,
+// so within f16's range), while the running sum keeps the unscaled ones. O
+// times the reference is the output.
 template <int HD>
 struct Int8State {
     static constexpr int kK = HD / 16;
     static constexpr uint32_t kFlip = 0x80808080u;  // sign bits: codes to offset binary
     static constexpr uint32_t kLo = 0x4140u, kHi = 0x4342u;
+    static constexpr float kBias = 1152.f;
     uint32_t qb[kK][2];
     float o[kK][4];
     float m[2], l[2];
+    float koff[2];  // kBias * sum of q over the dims, for this lane's two heads
+    float sp[2];    // this lane's sum of the f16 probabilities fed to the PV products
     float sl2, vref, rvref;
 
-    __device__ __forceinline__ void reset(const AttnParams& p) {
+    __device__ __forceinline__ void reset(const AttnParams& p, int lane) {
 #pragma unroll
         for (int mt = 0; mt < kK; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m[0] = m[1] = kNegInf;
         l[0] = l[1] = 0.f;
+        sp[0] = sp[1] = 0.f;
         sl2 = p.sl2 * (1.f / 127.f);
         vref = 0.f;
         rvref = 0.f;
+        // q's sum per head: lane (n, c) holds dims 4c..4c+3 of every 16-dim
+        // slice of head n; the quad reduces, then each lane takes the sums of
+        // the heads its score columns hold (2c and 2c + 1)
+        float qs = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kK; ++kk)
+            qs += (f16_lo(qb[kk][0]) + f16_hi(qb[kk][0])) + (f16_lo(qb[kk][1]) + f16_hi(qb[kk][1]));
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        koff[0] = kBias * __shfl_sync(0xffffffffu, qs, 8 * (lane & 3));
+        koff[1] = kBias * __shfl_sync(0xffffffffu, qs, 8 * (lane & 3) + 4);
     }
 
     __device__ __forceinline__ void begin_unit(const AttnParams& p, int b, int h, int lane) {
@@ -767,10 +787,12 @@ struct Int8State {
             qb[kk][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));  // dims 4c, 4c+1
             qb[kk][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));  // dims 4c+2, 4c+3
         }
-        reset(p);
+        reset(p, lane);
     }
 
-    __device__ __forceinline__ void begin_unit_from(const uint16_t*, const AttnParams& p, int, int) { reset(p); }
+    __device__ __forceinline__ void begin_unit_from(const uint16_t*, const AttnParams& p, int, int lane) {
+        reset(p, lane);
+    }
 
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int valid, int lane, float ak, float av) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -786,20 +808,23 @@ struct Int8State {
                 r1 ^= kFlip;
                 r2 ^= kFlip;
                 r3 ^= kFlip;
-                mma_f16_16816(c, i8x2_to_f16x2(r0, kLo), i8x2_to_f16x2(r1, kLo), i8x2_to_f16x2(r0, kHi),
-                              i8x2_to_f16x2(r1, kHi), qb[2 * kp][0], qb[2 * kp][1]);
-                mma_f16_16816(c1, i8x2_to_f16x2(r2, kLo), i8x2_to_f16x2(r3, kLo), i8x2_to_f16x2(r2, kHi),
-                              i8x2_to_f16x2(r3, kHi), qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+                mma_f16_16816(c, i8x2_to_f16x2_biased(r0, kLo), i8x2_to_f16x2_biased(r1, kLo),
+                              i8x2_to_f16x2_biased(r0, kHi), i8x2_to_f16x2_biased(r1, kHi), qb[2 * kp][0],
+                              qb[2 * kp][1]);
+                mma_f16_16816(c1, i8x2_to_f16x2_biased(r2, kLo), i8x2_to_f16x2_biased(r3, kLo),
+                              i8x2_to_f16x2_biased(r2, kHi), i8x2_to_f16x2_biased(r3, kHi), qb[2 * kp + 1][0],
+                              qb[2 * kp + 1][1]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[i] += c1[i];
         }
         const float ks = sl2 * ak;  // scale * log2(e) * a_k / 127
+        const float kb0 = ks * koff[0], kb1 = ks * koff[1];
         const int t0 = lane >> 2, t1 = t0 + 8;
-        float s0 = t0 < valid ? c[0] * ks : kNegInf;
-        float s1 = t0 < valid ? c[1] * ks : kNegInf;
-        float s2 = t1 < valid ? c[2] * ks : kNegInf;
-        float s3 = t1 < valid ? c[3] * ks : kNegInf;
+        float s0 = t0 < valid ? fmaf(c[0], ks, -kb0) : kNegInf;
+        float s1 = t0 < valid ? fmaf(c[1], ks, -kb1) : kNegInf;
+        float s2 = t1 < valid ? fmaf(c[2], ks, -kb0) : kNegInf;
+        float s3 = t1 < valid ? fmaf(c[3], ks, -kb1) : kNegInf;
         float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
@@ -827,6 +852,8 @@ struct Int8State {
         const float rel = fv * rvref;
         const uint32_t x0 = pack_f16x2(p0 * rel, p1 * rel);
         const uint32_t x1 = pack_f16x2(p2 * rel, p3 * rel);
+        sp[0] = sp[0] * ov0 + (f16_lo(x0) + f16_lo(x1));
+        sp[1] = sp[1] * ov1 + (f16_hi(x0) + f16_hi(x1));
         if (__any_sync(0xffffffffu, ov0 != 1.f || ov1 != 1.f)) {
 #pragma unroll
             for (int mt = 0; mt < kK; ++mt) {
@@ -849,41 +876,45 @@ struct Int8State {
                 const uint32_t w3 = lds32(vt + swz8<HD>(2 * cc + 9, chunk) + inb);
                 const uint32_t lo01 = __byte_perm(w0, w1, 0x5140) ^ kFlip, hi01 = __byte_perm(w0, w1, 0x7362) ^ kFlip;
                 const uint32_t lo89 = __byte_perm(w2, w3, 0x5140) ^ kFlip, hi89 = __byte_perm(w2, w3, 0x7362) ^ kFlip;
-                mma_f16_16816(o[2 * t], i8x2_to_f16x2(lo01, kLo), i8x2_to_f16x2(lo01, kHi), i8x2_to_f16x2(lo89, kLo),
-                              i8x2_to_f16x2(lo89, kHi), b0, b1);
-                mma_f16_16816(o[2 * t + 1], i8x2_to_f16x2(hi01, kLo), i8x2_to_f16x2(hi01, kHi),
-                              i8x2_to_f16x2(hi89, kLo), i8x2_to_f16x2(hi89, kHi), b0, b1);
+                mma_f16_16816(o[2 * t], i8x2_to_f16x2_biased(lo01, kLo), i8x2_to_f16x2_biased(lo01, kHi),
+                              i8x2_to_f16x2_biased(lo89, kLo), i8x2_to_f16x2_biased(lo89, kHi), b0, b1);
+                mma_f16_16816(o[2 * t + 1], i8x2_to_f16x2_biased(hi01, kLo), i8x2_to_f16x2_biased(hi01, kHi),
+                              i8x2_to_f16x2_biased(hi89, kLo), i8x2_to_f16x2_biased(hi89, kHi), b0, b1);
             }
         }
     }
 
-    // Reduce the per-thread sums and write (m, l, O * reference) of this warp to smem.
+    // Reduce the per-thread sums and write (m, l, (O - bias * probability
+    // sum) * reference) of this warp to smem.
     __device__ __forceinline__ void store(float* mbuf, float* lbuf, float* obuf, int G, int lane) {
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
             l[0] += __shfl_xor_sync(0xffffffffu, l[0], sh);
             l[1] += __shfl_xor_sync(0xffffffffu, l[1], sh);
+            sp[0] += __shfl_xor_sync(0xffffffffu, sp[0], sh);
+            sp[1] += __shfl_xor_sync(0xffffffffu, sp[1], sh);
         }
         const int h0 = (lane & 3) * 2, h1 = h0 + 1;
         if (lane < 4) {
             if (h0 < G) { mbuf[h0] = m[0]; lbuf[h0] = l[0]; }
             if (h1 < G) { mbuf[h1] = m[1]; lbuf[h1] = l[1]; }
         }
+        const float b0 = kBias * sp[0], b1 = kBias * sp[1];
         const int r = lane >> 2;
 #pragma unroll
         for (int t = 0; t < kK / 2; ++t) {
             const int d0 = 4 * (8 * t + r);
             if (h0 < G) {
-                obuf[h0 * HD + d0] = o[2 * t][0] * vref;
-                obuf[h0 * HD + d0 + 1] = o[2 * t][2] * vref;
-                obuf[h0 * HD + d0 + 2] = o[2 * t + 1][0] * vref;
-                obuf[h0 * HD + d0 + 3] = o[2 * t + 1][2] * vref;
+                obuf[h0 * HD + d0] = (o[2 * t][0] - b0) * vref;
+                obuf[h0 * HD + d0 + 1] = (o[2 * t][2] - b0) * vref;
+                obuf[h0 * HD + d0 + 2] = (o[2 * t + 1][0] - b0) * vref;
+                obuf[h0 * HD + d0 + 3] = (o[2 * t + 1][2] - b0) * vref;
             }
             if (h1 < G) {
-                obuf[h1 * HD + d0] = o[2 * t][1] * vref;
-                obuf[h1 * HD + d0 + 1] = o[2 * t][3] * vref;
-                obuf[h1 * HD + d0 + 2] = o[2 * t + 1][1] * vref;
-                obuf[h1 * HD + d0 + 3] = o[2 * t + 1][3] * vref;
+                obuf[h1 * HD + d0] = (o[2 * t][1] - b1) * vref;
+                obuf[h1 * HD + d0 + 1] = (o[2 * t][3] - b1) * vref;
+                obuf[h1 * HD + d0 + 2] = (o[2 * t + 1][1] - b1) * vref;
+                obuf[h1 * HD + d0 + 3] = (o[2 * t + 1][3] - b1) * vref;
             }
         }
     }
@@ -1395,14 +1426,48 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
         long long x = ps + lane;
         if (x >= pe) continue;
         Cursor cu = part == 0 ? rp->c0 : rp->c1;  // advanced to each block below
+        // INT8 tiles: each block's table entry and group maxima are read one
+        // block ahead, before the wait for its stage, so that the loads of
+        // the maxima (which need the block id) stay off the issue path
+        int nblk = 0, nh = 0;
+        float nak = 0.f, nav = 0.f;
+        if constexpr (VAR == kVarInt8) {
+            cu.advance_to(p, x);
+            nblk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
+            nh = cu.h;
+            if (nblk >= 0 && nblk < p.num_blocks) {
+                nak = __ldg(p.k_amax + (long long)nblk * p.Hkv + nh);
+                nav = __ldg(p.v_amax + (long long)nblk * p.Hkv + nh);
+            }
+        }
         for (; x < pe; x += W) {
+            int blk = 0, hh = 0;
+            float ak = 0.f, av = 0.f;
+            if constexpr (VAR == kVarInt8) {
+                blk = nblk;
+                hh = nh;
+                ak = nak;
+                av = nav;
+                if (x + W < pe) {
+                    cu.advance_to(p, x + W);
+                    nblk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x + W - cu.start));
+                    nh = cu.h;
+                    if (nblk >= 0 && nblk < p.num_blocks) {
+                        nak = __ldg(p.k_amax + (long long)nblk * p.Hkv + nh);
+                        nav = __ldg(p.v_amax + (long long)nblk * p.Hkv + nh);
+                    }
+                }
+            }
             if (!mbar_wait_bounded(my_empty + stg * 8, ph, p.wait_ns, kSleep)) {
                 // the consumer stopped taking stages (it timed out itself)
                 raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
                 return;
             }
-            cu.advance_to(p, x);
-            const int blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
+            if constexpr (VAR != kVarInt8) {
+                cu.advance_to(p, x);
+                blk = __ldg(p.block_tables + (long long)cu.b * p.mbps + (x - cu.start));
+                hh = cu.h;
+            }
             const uint32_t bar = my_full + stg * 8;
             const uint32_t okf = sbase + sp.okf + ((uint32_t)(lane * S) + stg) * 4;
             if (withhold) {
@@ -1413,19 +1478,22 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
                 mbar_arrive(bar);  // the consumer skips the block
             } else {
                 const uint32_t dst = my_tiles + stg * (2 * kTile);
-                const int e = blk * p.Hkv + cu.h;
+                const int e = blk * p.Hkv + hh;
                 const int y = e * (kTile / 128);  // the tile's first 128-byte line
                 if constexpr (VAR == kVarInt8) {
-                    // with the tiles, the 16-byte groups of the maxima
-                    // arrays holding this block's (the flag says which of
-                    // the four it is)
-                    const uint32_t am = sbase + sp.amx + ((uint32_t)(lane * S) + stg) * 32;
-                    sts32(okf, 1u + (uint32_t)(e & 3));
-                    mbar_arrive_expect_tx(bar, 2 * kTile + 32);
+                    // the tiles, then the block's K and V group maxima (read
+                    // a block ahead; two more bulk copies per stage cost ~5
+                    // us per Qwen3-8B layer) into the stage's slot; the
+                    // arrive comes after them, so its release publishes them
+                    // with the flag
+                    const uint32_t am = sbase + sp.amx + ((uint32_t)(lane * S) + stg) * 8;
+                    mbar_expect_tx(bar, 2 * kTile);
                     tma_load_2d(dst, &tmk, bar, 0, y, policy);
                     tma_load_2d(dst + kTile, &tmv, bar, 0, y, policy);
-                    bulk_load(am, p.k_amax + (e & ~3), 16, bar);
-                    bulk_load(am + 16, p.v_amax + (e & ~3), 16, bar);
+                    sts32(am, __float_as_uint(ak));
+                    sts32(am + 4, __float_as_uint(av));
+                    sts32(okf, 1u);
+                    mbar_arrive(bar);
                 } else {
                     sts32(okf, 1u);
                     mbar_arrive_expect_tx(bar, 2 * kTile);
@@ -1544,8 +1612,8 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
                 }
                 if constexpr (VAR == kVarInt8) {
                     // the block's K and V group maxima, staged with the tiles
-                    const uint32_t am = sbase + sp.amx + si * 32 + (okv - 1u) * 4;
-                    st.block(kt, vt, valid, lane, __uint_as_float(lds32(am)), __uint_as_float(lds32(am + 16)));
+                    const uint32_t am = sbase + sp.amx + si * 8;
+                    st.block(kt, vt, valid, lane, __uint_as_float(lds32(am)), __uint_as_float(lds32(am + 4)));
                 } else if constexpr (VAR != kVarFma) {
                     st.block(kt, vt, valid, p.sl2, lane);
                 } else {
@@ -1907,7 +1975,8 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return MI_ERR_INVALID_ARG;
     if ((var == kVarFp8 || var == kVarInt8) && (!k_scale || !v_scale)) return MI_ERR_INVALID_ARG;
-    if (var == kVarInt8 && (!aligned16(k_scale) || !aligned16(v_scale))) return MI_ERR_INVALID_ARG;
+    if (var == kVarInt8 && ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u))
+        return MI_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
         !aligned16(workspace))
         return MI_ERR_INVALID_ARG;

@@ -32,8 +32,7 @@ def _workspace(mi, d, device):
 
 
 class DevState:
-    """Device copies of an oracle INT8 state (oracle.int8_state layout); the
-    maxima arrays padded to a multiple of 4 floats."""
+    """Device copies of an oracle INT8 state (oracle.int8_state layout)."""
 
     def __init__(self, st, device):
         import torch

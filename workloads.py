@@ -326,13 +326,13 @@ def device_int8_cache(w: Workload, layer: int, device):
     sees them: codes round(N(0,1) * 127 / 4) clamped to [-127, 127], and for
     every block and KV head a group maximum uniform in [3.5, 4.5] (what a
     64-token group of N(0,1) values gives), in arrays of num_blocks * Hkv
-    floats rounded up to a multiple of 4. Seeded torch CUDA generator.
+    floats. Seeded torch CUDA generator.
     Returns (k_codes, v_codes, k_amax, v_amax)."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(w.seed * 1000 + 500 + layer)
     shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
-    n_amax = (w.num_blocks * w.Hkv + 3) // 4 * 4
+    n_amax = w.num_blocks * w.Hkv
     out = []
     for _ in range(2):
         c = torch.empty(shape, dtype=torch.int8, device=device)
