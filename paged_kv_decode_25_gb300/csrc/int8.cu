@@ -15,11 +15,15 @@
 // the new row is (with an unchanged maximum the other rows' codes come out
 // the same), so a full group ends up quantised over its 64 tokens.
 //
-// One CTA per request: all its threads rotate the request's q heads (RoPE as
-// mi_paged_kv_append computes it, the same bits), then each warp takes (KV
-// head, K or V) items: the new row (k rotated, v as given) into the open
-// buffer, the row maximum by a warp reduction, and the codes of the new row
-// or of the whole group.
+// One CTA per request, one warp per (KV head, K or V) item (8 to 16 warps;
+// a warp takes a second item past 16):
+// all threads rotate the request's q heads (RoPE as mi_paged_kv_append
+// computes it, the same bits; each thread loads all its words before it
+// stores any, so the loads overlap and q_out may alias q), then each warp
+// takes its item: the new row (k rotated, v as given) into the open buffer,
+// the row maximum by a warp reduction, and the codes of the new row or of
+// the whole group. The open slot and the group's table entries are read
+// before the q work, so their latency overlaps it.
 #include "common.cuh"
 #include "rope.cuh"
 
@@ -27,7 +31,8 @@ namespace mi {
 namespace {
 
 constexpr int kGroup = 64;
-constexpr int kAppendThreads = 256;
+constexpr int kMaxThreads = 512;
+constexpr int kQWords = 8;  // q words a thread holds at once
 
 struct Int8AppendParams {
     const uint16_t* q;             // [B][Hq][d] raw
@@ -64,7 +69,12 @@ __device__ __forceinline__ float absmax_pair(uint32_t w) {
     return fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)));
 }
 
-__global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendParams a) {
+// g[j] for a run-time j < 4, without indexing the array in local memory.
+__device__ __forceinline__ int pick4(const int (&g)[4], int j) {
+    return j == 0 ? g[0] : (j == 1 ? g[1] : (j == 2 ? g[2] : g[3]));
+}
+
+__global__ void __launch_bounds__(kMaxThreads) append_int8_kernel(Int8AppendParams a) {
     // inputs may come from the kernel just before this one in the stream
     pdl_wait();
     pdl_trigger();
@@ -78,19 +88,57 @@ __global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendP
         return;
     }
     const float2* cs_row = a.rope + (long long)p * half;
+    // read now, used after the q work
+    const int slot = __ldg(a.open_slots + b);
+    const int t0 = p / kGroup * kGroup, o = p - t0;  // the group's first token, the new token's offset
+    const int j0 = t0 / kBlock, jp = p / kBlock;      // the group's first block, the new token's block
+    const int32_t* bt = a.block_tables + (long long)b * a.mbps;
+    int gblk[kGroup / kBlock];                        // the group's blocks so far
+#pragma unroll
+    for (int j = 0; j < kGroup / kBlock; ++j) gblk[j] = j0 + j <= jp ? __ldg(bt + j0 + j) : 0;
 
-    // q heads: each item is one word of the first half and the matching word
-    // of the second half of a head; both are loaded before anything is
-    // stored, so q_out may alias q
-    for (int i = tid; i < a.Hq * words; i += blockDim.x) {
+    // q heads: each word is one word of the first half and the matching word
+    // of the second half of a head
+    const int nq = a.Hq * words, nthr = blockDim.x;
+    uint32_t xl[kQWords], xh[kQWords];
+    float4 cs[kQWords];
+#pragma unroll
+    for (int k = 0; k < kQWords; ++k) {
+        const int i = tid + k * nthr;
+        if (i < nq) {
+            const int head = i / words, w = i - head * words;
+            const uint16_t* src = a.q + ((long long)b * a.Hq + head) * d;
+            xl[k] = *reinterpret_cast<const uint32_t*>(src + 2 * w);
+            xh[k] = *reinterpret_cast<const uint32_t*>(src + 2 * w + half);
+            cs[k] = *reinterpret_cast<const float4*>(cs_row + 2 * w);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kQWords; ++k) {
+        const int i = tid + k * nthr;
+        if (i < nq) {
+            const int head = i / words, w = i - head * words;
+            uint32_t yl, yh;
+            if (rotate_word_fast(xl[k], xh[k], cs[k], yl, yh)) {
+                const uint2 y = rotate_word_exact(xl[k], xh[k], cs[k]);
+                yl = y.x;
+                yh = y.y;
+            }
+            uint16_t* dst = a.q_out + ((long long)b * a.Hq + head) * d;
+            *reinterpret_cast<uint32_t*>(dst + 2 * w) = yl;
+            *reinterpret_cast<uint32_t*>(dst + 2 * w + half) = yh;
+        }
+    }
+    // more q words than the threads hold at once (very wide heads): one at a time
+    for (int i = tid + kQWords * nthr; i < nq; i += nthr) {
         const int head = i / words, w = i - head * words;
         const uint16_t* src = a.q + ((long long)b * a.Hq + head) * d;
-        const uint32_t xl = *reinterpret_cast<const uint32_t*>(src + 2 * w);
-        const uint32_t xh = *reinterpret_cast<const uint32_t*>(src + 2 * w + half);
-        const float4 cs = *reinterpret_cast<const float4*>(cs_row + 2 * w);
+        const uint32_t wl = *reinterpret_cast<const uint32_t*>(src + 2 * w);
+        const uint32_t wh = *reinterpret_cast<const uint32_t*>(src + 2 * w + half);
+        const float4 c4 = *reinterpret_cast<const float4*>(cs_row + 2 * w);
         uint32_t yl, yh;
-        if (rotate_word_fast(xl, xh, cs, yl, yh)) {
-            const uint2 y = rotate_word_exact(xl, xh, cs);
+        if (rotate_word_fast(wl, wh, c4, yl, yh)) {
+            const uint2 y = rotate_word_exact(wl, wh, c4);
             yl = y.x;
             yh = y.y;
         }
@@ -99,19 +147,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendP
         *reinterpret_cast<uint32_t*>(dst + 2 * w + half) = yh;
     }
 
-    const int slot = __ldg(a.open_slots + b);
     if (slot < 0 || slot >= a.num_slots) {
         if (tid == 0) raise_err(a.dev_err, MI_DEVERR_BAD_SLOT);
         return;
     }
-    const int t0 = p / kGroup * kGroup, o = p - t0;  // the group's first token, the new token's offset
-    const int j0 = t0 / kBlock, jp = p / kBlock;      // the group's first block, the new token's block
-    const int32_t* bt = a.block_tables + (long long)b * a.mbps;
     bool ok = true;
-    for (int j = j0; j <= jp; ++j) {
-        const int blk = __ldg(bt + j);
-        ok &= blk >= 0 && blk < a.num_blocks;
-    }
+#pragma unroll
+    for (int j = 0; j < kGroup / kBlock; ++j) ok &= j0 + j > jp || (gblk[j] >= 0 && gblk[j] < a.num_blocks);
     if (!ok) {
         if (tid == 0) raise_err(a.dev_err, MI_DEVERR_BAD_BLOCK);
         return;
@@ -142,6 +184,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendP
                 }
             }
         }
+        float* amax = is_v ? a.v_amax : a.k_amax;
+        // the group's maximum so far (held by its first block), none for a new group
+        const float m_old = o > 0 ? __ldcg(amax + (long long)gblk[0] * a.Hkv + h) : 0.f;
         uint16_t* grp = (is_v ? a.v_open : a.k_open) + ((long long)slot * a.Hkv + h) * kGroup * d;
         if (own) {
             *reinterpret_cast<uint32_t*>(grp + (long long)o * d + 2 * lane) = yl;
@@ -150,17 +195,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendP
         float rmax = own ? fmaxf(absmax_pair(yl), absmax_pair(yh)) : 0.f;
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, sh));
-        float* amax = is_v ? a.v_amax : a.k_amax;
         int8_t* cache = is_v ? a.vc : a.kc;
-        // the group's maximum so far (held by its first block), none for a new group
-        const float m_old = o > 0 ? __ldcg(amax + (long long)__ldg(bt + j0) * a.Hkv + h) : 0.f;
         const float m = fmaxf(m_old, rmax);
         const float s = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;  // m = 0: every code is 0
         if (o > 0 && m > m_old) {
             // the maximum grew: the whole group again, from its bf16 rows
             __syncwarp();
             for (int t = 0; t <= o; ++t) {
-                const int blk = __ldg(bt + (t0 + t) / kBlock);
+                const int blk = pick4(gblk, t / kBlock);
                 int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + (t0 + t) % kBlock) * d;
                 if (own) {
                     const uint32_t wl = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane);
@@ -169,9 +211,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_int8_kernel(Int8AppendP
                     *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(wh, s);
                 }
             }
-            for (int j = j0 + lane; j <= jp; j += 32) amax[(long long)__ldg(bt + j) * a.Hkv + h] = m;
+#pragma unroll
+            for (int j = 0; j < kGroup / kBlock; ++j)
+                if (lane == j && j0 + j <= jp) amax[(long long)gblk[j] * a.Hkv + h] = m;
         } else {
-            const int blk = __ldg(bt + jp);
+            const int blk = pick4(gblk, jp - j0);
             int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + p % kBlock) * d;
             if (own) {
                 *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(yl, s);
@@ -233,6 +277,9 @@ extern "C" mi_status mi_paged_kv_append_int8(const mi_dims* dims, const void* q,
     a.mbps = D.max_blocks_per_seq;
     a.max_pos = max_pos;
     a.num_slots = num_open_slots;
-    const cudaError_t e = launch_pdl(append_int8_kernel, (int)D.B, kAppendThreads, 0, (cudaStream_t)stream, a);
+    // one warp per (KV head, K or V) item, at least 8 warps for the q work,
+    // at most 16
+    const int warps = 2 * D.Hkv < 8 ? 8 : (2 * D.Hkv > kMaxThreads / 32 ? kMaxThreads / 32 : 2 * D.Hkv);
+    const cudaError_t e = launch_pdl(append_int8_kernel, (int)D.B, warps * 32, 0, (cudaStream_t)stream, a);
     return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }

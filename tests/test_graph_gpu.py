@@ -3,9 +3,11 @@ keeps the kernel arguments of the capture, the split-KV merge's epoch
 included, and is replayed many times over one workspace. Each replay must
 give the bits of an eager call. Covered on the Qwen3-8B-shaped serving layer
 (B = 64, contexts up to 8k, a fragmented pool, hundreds of units cut across
-CTAs): the bf16 and the e4m3 attention and the bf16 and e4m3 fused steps,
-each replayed three times, and two launches captured back to back on one
-workspace; and the causal prefill attention with each of its kernels."""
+CTAs): the bf16, e4m3 and INT8 attention, the bf16 and e4m3 fused steps and
+the INT8 append + attention, each replayed three times, and two launches
+captured back to back on one workspace; and the causal prefill attention
+with each of its kernels."""
+import numpy as np
 import pytest
 
 from helpers import grow, pools_for, to_dev_i32, to_dev_u16
@@ -69,7 +71,7 @@ def _replay_and_check(launch, outs, refs, err):
             assert torch.equal(_bits(o), _bits(r))
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
 def test_graph_replay_attention(cuda_device, kv):
     import torch
     mi = _mi()
@@ -91,6 +93,17 @@ def test_graph_replay_attention(cuda_device, kv):
         def call(out, ws):
             assert mi.mi_paged_decode_attention_fp8(d, lay["q"], kc, vc, ks, vs, lay["bt"], lay["cl"], w.scale, out,
                                                     ws, dev_err=err) == 0
+    if kv == "int8":
+        kc = (lay["kc"].float() * 32).round_().clamp_(-127, 127).to(torch.int8)
+        vc = (lay["vc"].float() * 32).round_().clamp_(-127, 127).to(torch.int8)
+        g = torch.Generator(device=cuda_device)
+        g.manual_seed(3)
+        ka = 3.5 + torch.rand(w.num_blocks * w.Hkv, generator=g, device=cuda_device)
+        va = 3.5 + torch.rand(w.num_blocks * w.Hkv, generator=g, device=cuda_device)
+
+        def call(out, ws):
+            assert mi.mi_paged_decode_attention_int8(d, lay["q"], kc, vc, ka, va, lay["bt"], lay["cl"], w.scale, out,
+                                                     ws, dev_err=err) == 0
     ref = torch.empty_like(lay["q"])
     call(ref, _workspace(mi, d, cuda_device))
     torch.cuda.synchronize()
@@ -192,3 +205,50 @@ def test_graph_replay_prefill(cuda_device, variant):
     assert int(err.item()) == 0
     out = torch.empty_like(ref)
     _replay_and_check(lambda: call(out), [out], [ref], err)
+
+
+def test_graph_replay_int8_step(cuda_device):
+    """The INT8 append (RoPE, the open group's bf16 rows, the group's codes
+    and maxima) then the INT8 attention, captured once and replayed: the
+    append of the same token is idempotent (the maximum it raised is the one
+    it finds again), so every replay gives the same bits in q_out, codes,
+    maxima, open rows and output."""
+    import torch
+    mi = _mi()
+    lay = _layer(cuda_device)
+    w, d = lay["w"], lay["d"]
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    k8 = (lay["kc"].float() * 32).round_().clamp_(-127, 127).to(torch.int8)
+    v8 = (lay["vc"].float() * 32).round_().clamp_(-127, 127).to(torch.int8)
+    ka = torch.full((w.num_blocks * w.Hkv,), 4.0, dtype=torch.float32, device=cuda_device)
+    va = torch.full_like(ka, 4.0)
+    ko = torch.zeros((w.B, w.Hkv, 64, w.head_dim), dtype=torch.bfloat16, device=cuda_device)
+    vo = torch.zeros_like(ko)
+    slots = to_dev_i32(np.arange(w.B, dtype=np.int32), cuda_device)
+    _, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    rope = torch.from_numpy(table).to(cuda_device)
+    ws = _workspace(mi, d, cuda_device)
+    qo, out = torch.empty_like(lay["q"]), torch.empty_like(lay["q"])
+
+    def launch():
+        assert mi.mi_paged_kv_append_int8(d, lay["q"], lay["k"], lay["v"], rope, w.max_pos, lay["bt"], lay["cl"],
+                                          slots, qo, k8, v8, ka, va, ko, vo, err) == 0
+        assert mi.mi_paged_decode_attention_int8(d, qo, k8, v8, ka, va, lay["bt"], lay["cl"], w.scale, out, ws,
+                                                 dev_err=err) == 0
+    launch()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    refs = [t.clone() for t in (qo, out, k8, v8, ka, va, ko, vo)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch()
+    for _ in range(REPLAYS):
+        qo.fill_(float("nan"))
+        out.fill_(float("nan"))
+        err.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for t, r in zip((qo, out, k8, v8, ka, va, ko, vo), refs):
+            assert torch.equal(_bits(t) if t.dtype != torch.float32 else t.view(torch.int32),
+                               _bits(r) if r.dtype != torch.float32 else r.view(torch.int32))

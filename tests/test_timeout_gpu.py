@@ -69,7 +69,7 @@ def test_hook_arguments_checked():
     assert mi.mi_test_set_wait_limit(0) == mi.MI_OK
 
 
-@pytest.mark.parametrize("kind", ["attention", "fp8", "step"])
+@pytest.mark.parametrize("kind", ["attention", "fp8", "int8", "step"])
 def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
     """A decode launch whose first staged block never arrives sets the timeout
     bit and returns within milliseconds; after the workspace is zeroed the
@@ -93,6 +93,13 @@ def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
         vc8 = oracle.e4m3_from_f64(oracle.bf16_to_f64(vc) / ks[None, :, None, None].astype(np.float64))
         kc_d = torch.from_numpy(kc8).to(cuda_device)
         vc_d = torch.from_numpy(vc8).to(cuda_device)
+    elif kind == "int8":
+        # INT8 codes and group maxima of the same history (the oracle's quantiser)
+        st8 = oracle.int8_state(nb, Hkv, d, B)
+        assert oracle.int8_from_bf16_cache(kc, vc, bt, lens, np.arange(B, dtype=np.int32), st8) == 0
+        kc_d, vc_d = torch.from_numpy(st8["k8"]).to(cuda_device), torch.from_numpy(st8["v8"]).to(cuda_device)
+        ka_d = torch.from_numpy(st8["k_amax"].ravel()).to(cuda_device)
+        va_d = torch.from_numpy(st8["v_amax"].ravel()).to(cuda_device)
     else:
         kc_d, vc_d = to_dev_u16(kc, cuda_device), to_dev_u16(vc, cuda_device)
     q_d, k_d, v_d = (to_dev_u16(a, cuda_device) for a in (q, k, v))
@@ -103,6 +110,9 @@ def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
         if kind == "fp8":
             return mi.mi_paged_decode_attention_fp8(dims, q_d, kc_d, vc_d, ks_d, ks_d, bt_d, cl_d, scale, out, ws,
                                                     dev_err=err)
+        if kind == "int8":
+            return mi.mi_paged_decode_attention_int8(dims, q_d, kc_d, vc_d, ka_d, va_d, bt_d, cl_d, scale, out, ws,
+                                                     dev_err=err)
         return mi.mi_paged_decode_step(dims, q_d, k_d, v_d, rope_d, 4096, bt_d, cl_d, scale, qo, kc_d, vc_d, out,
                                        ws, dev_err=err)
 
@@ -134,6 +144,9 @@ def test_decode_wait_runs_out_then_recovers(cuda_device, kind):
         ref = oracle.paged_attention(q_ref, kc_h, vc_h, bt, lens, scale, nthreads=8)
     elif kind == "fp8":
         ref = oracle.paged_attention_fp8(q, kc8, vc8, ks, ks, bt, lens, scale, nthreads=8)
+    elif kind == "int8":
+        ref = oracle.paged_attention_int8(q, st8["k8"], st8["v8"], st8["k_amax"], st8["v_amax"], bt, lens, scale,
+                                          nthreads=8)
     else:
         ref = oracle.paged_attention(q, kc, vc, bt, lens, scale, nthreads=8)
     assert_attention_close(from_dev_u16(out), ref, f"{kind} after a timed-out launch")
