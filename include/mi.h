@@ -495,6 +495,21 @@ mi_status mi_kv_copy_blocks(const mi_dims* dims, const void* src_k, const void* 
                             int32_t dst_num_blocks, const int32_t* dst_blocks, int32_t n,
                             int32_t* dev_err, mi_stream_t stream);
 
+/* Copy n rows of row_bytes bytes each: row src_ids[i] of src (src_count rows
+ * of row_bytes, back to back) to row dst_ids[i] of dst (dst_count rows).
+ * The general form of mi_kv_copy_blocks for KV state whose rows are not
+ * bf16 blocks: the blocks of one-byte (e4m3, INT8) caches (row =
+ * Hkv * 16 * head_dim bytes), the INT8 group maxima of a block (row = Hkv
+ * floats) and a sequence's INT8 open-group rows (row = Hkv * 64 * head_dim
+ * bf16). row_bytes a positive multiple of 4, src and dst 4-byte aligned
+ * (16-byte vectors are used when both are 16-byte aligned and row_bytes is
+ * a multiple of 16). Memory, id arrays, overlap rules, errors
+ * (MI_DEVERR_BAD_BLOCK for an id out of range, the pair skipped) and
+ * streams as mi_kv_copy_blocks; one kernel launch. */
+mi_status mi_kv_copy_rows(const void* src, int64_t src_count, const int32_t* src_ids, void* dst,
+                          int64_t dst_count, const int32_t* dst_ids, int32_t n, int64_t row_bytes,
+                          int32_t* dev_err, mi_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Allocation-free attention. The pages have no counterpart to this entry
  * point: it serves callers of this library that cannot call cudaMalloc (a

@@ -35,7 +35,7 @@ EXPORTS = (
     "mi_status_string", "mi_kv_pool_create", "mi_kv_pool_destroy", "mi_kv_pool_alloc", "mi_kv_pool_alloc_batch",
     "mi_kv_pool_free", "mi_kv_pool_num_free", "mi_kv_pool_batch_meta", "mi_kv_pool_token_slots",
     "mi_kv_pool_admission", "mi_kv_pool_touch", "mi_kv_pool_lru_victim", "mi_kv_pool_swap_out",
-    "mi_kv_pool_swap_in", "mi_kv_copy_blocks",
+    "mi_kv_pool_swap_in", "mi_kv_copy_blocks", "mi_kv_copy_rows",
     "mi_kv_pool_seq_blocks",
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
@@ -99,6 +99,7 @@ def load():
             "mi_paged_decode_attention_fp8": (
                 [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_attention_noalloc": ([dims_p, P, P, P, P, P, f32, P, P, P], i32),
+            "mi_kv_copy_rows": ([P, ctypes.c_int64, P, P, ctypes.c_int64, P, i32, ctypes.c_int64, P, P], i32),
             "mi_paged_kv_append_int8": (
                 [dims_p, P, P, P, P, i32, P, P, P, i32, P, P, P, P, P, P, P, P, P], i32),
             "mi_paged_decode_attention_int8": (
@@ -403,6 +404,12 @@ def mi_paged_decode_attention_int8(d: MiDims, q, k_cache, v_cache, k_amax, v_ama
                                                  _ptr(k_amax), _ptr(v_amax), _ptr(block_tables),
                                                  _ptr(context_lens), float(scale), _ptr(out), _ptr(workspace),
                                                  int(wb), _ptr(dev_err), _stream(stream))
+
+
+def mi_kv_copy_rows(src, src_count, src_ids, dst, dst_count, dst_ids, n, row_bytes, dev_err=None, stream=None):
+    """Copy n rows of row_bytes: src row src_ids[i] to dst row dst_ids[i]."""
+    return load().mi_kv_copy_rows(_ptr(src), int(src_count), _ptr(src_ids), _ptr(dst), int(dst_count),
+                                  _ptr(dst_ids), int(n), int(row_bytes), _ptr(dev_err), _stream(stream))
 
 
 def amax_floats(num_blocks: int, Hkv: int) -> int:
