@@ -411,6 +411,30 @@ mi_status mi_paged_kv_append_int8(const mi_dims* dims, const void* q, const void
                                   float* k_amax, float* v_amax, void* k_open, void* v_open, int32_t* dev_err,
                                   mi_stream_t stream);
 
+/* The INT8 append for many new tokens per request (a prompt, or a chunk of
+ * one): dims.B = R requests; request r's m_r = query_start[r+1] -
+ * query_start[r] new tokens are rows query_start[r] .. query_start[r+1]-1 of
+ * q [T][Hq][d], k and v [T][Hkv][d] (T = total_tokens = query_start[R]),
+ * at positions n_r - m_r .. n_r - 1 (n_r = context_lens[r], counting them).
+ * The result is exactly that of m_r calls of mi_paged_kv_append_int8, one
+ * token each, in order: q_out rows rotated, every group the new tokens touch
+ * quantised over all its tokens (the open group's earlier ones from the open
+ * buffer), its maxima written to all its blocks, and the last group's new
+ * rows added to the open buffer (rows of a slot past its open group's tokens
+ * are unspecified, and no call reads them). Device errors: query_start out of order or
+ * past T, or m_r > n_r (MI_DEVERR_BAD_QUERY), n_r above max_blocks_per_seq *
+ * 16 (MI_DEVERR_BAD_CONTEXT) or n_r - 1 >= max_pos (MI_DEVERR_BAD_POS) skip
+ * the request; a bad open slot (MI_DEVERR_BAD_SLOT) or a bad block id of a
+ * touched group (MI_DEVERR_BAD_BLOCK) skip its cache writes. Buffers and
+ * alignment as mi_paged_kv_append_int8. */
+mi_status mi_paged_kv_append_int8_tokens(const mi_dims* dims, int32_t total_tokens, const void* q, const void* k,
+                                         const void* v, const float* rope_cos_sin, int32_t max_pos,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         const int32_t* query_start, const int32_t* open_slots,
+                                         int32_t num_open_slots, void* q_out, void* k_cache, void* v_cache,
+                                         float* k_amax, float* v_amax, void* k_open, void* v_open, int32_t* dev_err,
+                                         mi_stream_t stream);
+
 /* mi_paged_decode_attention over INT8 caches: the same definition with
  * K_t = c_t * k_amax[blk][h] / 127 and V_t = c_t * v_amax[blk][h] / 127,
  * blk = block_tables[b][t / 16]. The products run on tensor cores in f16

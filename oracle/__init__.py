@@ -310,6 +310,29 @@ def append_int8(q, k, v, table, block_tables, context_lens, open_slots, st):
     return q_out, status
 
 
+def append_int8_tokens(q, k, v, table, block_tables, context_lens, query_start, open_slots, st):
+    """Many new tokens per request: request r's rows query_start[r] ..
+    query_start[r+1]-1 of q [T][Hq][d], k and v [T][Hkv][d], at positions
+    n_r - m_r .. n_r - 1, appended one token at a time with append_int8 (the
+    definition). Returns (q_out [T][Hq][d], status)."""
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    qs = _c(query_start, np.int32); cl = _c(context_lens, np.int32)
+    R = cl.shape[0]
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    m = qs[1:] - qs[:-1]
+    q_out = np.zeros_like(q)
+    status = 0
+    for i in range(int(m.max()) if R else 0):
+        live = m > i
+        cl_i = np.where(live, cl - m + i + 1, 0).astype(np.int32)
+        rows = np.where(live, qs[:-1] + i, 0)
+        qo, st_i = append_int8(q[rows], k[rows], v[rows], table, block_tables, cl_i, open_slots, st)
+        status = min(status, st_i)
+        q_out[rows[live]] = qo[live]
+    return q_out, status
+
+
 def paged_attention_int8(q, k8, v8, k_amax, v_amax, block_tables, context_lens, scale, nthreads=1):
     """q uint16 [B][Hq][d]; int8 caches [nb][Hkv][16][d]; fp32 group maxima
     [nb][Hkv]; returns float64 [B][Hq][d]."""

@@ -40,7 +40,7 @@ EXPORTS = (
     "mi_rope_table", "mi_paged_kv_append", "mi_paged_decode_workspace_bytes",
     "mi_paged_decode_attention", "mi_paged_decode_attention_variant",
     "mi_paged_kv_append_fp8", "mi_paged_decode_attention_fp8",
-    "mi_paged_kv_append_int8", "mi_paged_decode_attention_int8",
+    "mi_paged_kv_append_int8", "mi_paged_decode_attention_int8", "mi_paged_kv_append_int8_tokens",
     "mi_paged_prefill_attention", "mi_paged_prefill_attention_variant", "mi_paged_decode_attention_noalloc",
     "mi_paged_decode_step", "mi_paged_decode_step_fp8", "mi_test_set_wait_limit", "mi_test_withhold_copy",
 )
@@ -102,6 +102,8 @@ def load():
             "mi_kv_copy_rows": ([P, ctypes.c_int64, P, P, ctypes.c_int64, P, i32, ctypes.c_int64, P, P], i32),
             "mi_paged_kv_append_int8": (
                 [dims_p, P, P, P, P, i32, P, P, P, i32, P, P, P, P, P, P, P, P, P], i32),
+            "mi_paged_kv_append_int8_tokens": (
+                [dims_p, i32, P, P, P, P, i32, P, P, P, P, i32, P, P, P, P, P, P, P, P, P], i32),
             "mi_paged_decode_attention_int8": (
                 [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_step": (
@@ -395,6 +397,19 @@ def mi_paged_kv_append_int8(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tab
                                           int(k_open.shape[0]), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(k_amax), _ptr(v_amax), _ptr(k_open), _ptr(v_open), _ptr(dev_err),
                                           _stream(stream))
+
+
+def mi_paged_kv_append_int8_tokens(d: MiDims, total_tokens, q, k, v, rope_cos_sin, max_pos, block_tables,
+                                   context_lens, query_start, open_slots, q_out, k_cache, v_cache, k_amax, v_amax,
+                                   k_open, v_open, dev_err=None, stream=None):
+    """The INT8 append of many new tokens per request (rows query_start[r] ..
+    query_start[r+1]-1); the open buffers' first dimension is the number of
+    open-group slots."""
+    return load().mi_paged_kv_append_int8_tokens(
+        ctypes.byref(d), int(total_tokens), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin), int(max_pos),
+        _ptr(block_tables), _ptr(context_lens), _ptr(query_start), _ptr(open_slots), int(k_open.shape[0]),
+        _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(k_amax), _ptr(v_amax), _ptr(k_open), _ptr(v_open),
+        _ptr(dev_err), _stream(stream))
 
 
 def mi_paged_decode_attention_int8(d: MiDims, q, k_cache, v_cache, k_amax, v_amax, block_tables, context_lens,

@@ -226,6 +226,189 @@ __global__ void __launch_bounds__(kMaxThreads) append_int8_kernel(Int8AppendPara
     }
 }
 
+// ------------------------------------------------- many tokens per request --
+// mi_paged_kv_append_int8_tokens: request r's m = query_start[r+1] -
+// query_start[r] new tokens at positions n - m .. n - 1 (n = context_lens[r],
+// counting them), with the result of m decode appends in order: every group
+// the new tokens touch is quantised over all its tokens (the open group's
+// earlier ones from the open buffer), and the last group's new rows join the
+// open buffer. One CTA per (request, KV head, K or V), eight warps; the G
+// query heads of the KV head are rotated by its K and V CTAs, half each.
+
+constexpr int kTokThreads = 256;
+constexpr int kTokWarps = kTokThreads / 32;
+constexpr int kRowsPerWarp = kGroup / kTokWarps;  // rows of a group per warp
+constexpr int kQBatch = 8;                          // q words a thread loads before it stores
+
+struct Int8TokParams {
+    const uint16_t* q;             // [T][Hq][d] raw
+    const uint16_t* k;             // [T][Hkv][d] raw
+    const uint16_t* v;             // [T][Hkv][d]
+    const float2* rope;
+    const int32_t* block_tables;   // [R][mbps]
+    const int32_t* context_lens;   // [R]
+    const int32_t* query_start;    // [R + 1]
+    const int32_t* open_slots;     // [R]
+    uint16_t* q_out;               // [T][Hq][d]
+    int8_t* kc;
+    int8_t* vc;
+    float* k_amax;
+    float* v_amax;
+    uint16_t* k_open;
+    uint16_t* v_open;
+    int32_t* dev_err;
+    int Hq, Hkv, d, num_blocks, mbps, max_pos, num_slots, T;
+};
+
+__global__ void __launch_bounds__(kTokThreads) append_int8_tokens_kernel(Int8TokParams a) {
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x / (2 * a.Hkv), h = (blockIdx.x >> 1) % a.Hkv;
+    const bool is_v = (blockIdx.x & 1) != 0;
+    const bool reporter = tid == 0 && blockIdx.x % (2 * a.Hkv) == 0;  // one error report per request
+    const int d = a.d, half = d / 2, words = d / 4;
+    const int n = __ldg(a.context_lens + r);
+    const int q0 = __ldg(a.query_start + r), q1 = __ldg(a.query_start + r + 1);
+    const int m = q1 - q0;
+    if (q0 < 0 || q1 < q0 || q1 > a.T || m > (n > 0 ? n : 0)) {
+        if (reporter) raise_err(a.dev_err, MI_DEVERR_BAD_QUERY);
+        return;
+    }
+    if (m == 0) return;  // nothing to append
+    if (n > a.mbps * kBlock || n - 1 >= a.max_pos) {
+        if (reporter) raise_err(a.dev_err, n - 1 >= a.max_pos ? MI_DEVERR_BAD_POS : MI_DEVERR_BAD_CONTEXT);
+        return;
+    }
+    const int p0 = n - m;
+
+    // q rows of this CTA's share of the KV head's query heads, a batch of
+    // words loaded per thread before any is stored (q_out may alias q)
+    const int G = a.Hq / a.Hkv, gk = (G + 1) / 2;
+    const int hq0 = h * G + (is_v ? gk : 0), nh = is_v ? G - gk : gk;
+    const long long nqw = (long long)m * nh * words;
+    for (long long i0 = tid; i0 < nqw; i0 += (long long)kQBatch * kTokThreads) {
+        uint32_t xl[kQBatch], xh[kQBatch];
+        float4 cs[kQBatch];
+        long long ofs[kQBatch];
+#pragma unroll
+        for (int u = 0; u < kQBatch; ++u) {
+            const long long i = i0 + (long long)u * kTokThreads;
+            ofs[u] = -1;
+            if (i < nqw) {
+                const int w = (int)(i % words);
+                const long long rest = i / words;
+                const int hh = (int)(rest % nh), tok = (int)(rest / nh);
+                ofs[u] = ((long long)(q0 + tok) * a.Hq + hq0 + hh) * d + 2 * w;
+                xl[u] = *reinterpret_cast<const uint32_t*>(a.q + ofs[u]);
+                xh[u] = *reinterpret_cast<const uint32_t*>(a.q + ofs[u] + half);
+                cs[u] = *reinterpret_cast<const float4*>(a.rope + (long long)(p0 + tok) * half + 2 * w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kQBatch; ++u) {
+            if (ofs[u] < 0) continue;
+            uint32_t yl, yh;
+            if (rotate_word_fast(xl[u], xh[u], cs[u], yl, yh)) {
+                const uint2 y = rotate_word_exact(xl[u], xh[u], cs[u]);
+                yl = y.x;
+                yh = y.y;
+            }
+            *reinterpret_cast<uint32_t*>(a.q_out + ofs[u]) = yl;
+            *reinterpret_cast<uint32_t*>(a.q_out + ofs[u] + half) = yh;
+        }
+    }
+
+    const int slot = __ldg(a.open_slots + r);
+    if (slot < 0 || slot >= a.num_slots) {
+        if (reporter) raise_err(a.dev_err, MI_DEVERR_BAD_SLOT);
+        return;
+    }
+    const int32_t* bt = a.block_tables + (long long)r * a.mbps;
+    // every block of the groups the new tokens touch must be valid
+    const int jfirst = p0 / kGroup * (kGroup / kBlock), jlast = (n - 1) / kBlock;
+    bool ok = true;
+    for (int j = jfirst + tid; j <= jlast; j += kTokThreads) {
+        const int blk = __ldg(bt + j);
+        ok &= blk >= 0 && blk < a.num_blocks;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (reporter) raise_err(a.dev_err, MI_DEVERR_BAD_BLOCK);
+        return;
+    }
+
+    __shared__ float wmax[kTokWarps];
+    uint16_t* grp = (is_v ? a.v_open : a.k_open) + ((long long)slot * a.Hkv + h) * kGroup * d;
+    const uint16_t* in = is_v ? a.v : a.k;
+    float* amax = is_v ? a.v_amax : a.k_amax;
+    int8_t* cache = is_v ? a.vc : a.kc;
+    const bool own = lane < words;  // lane l owns words l and l + words of every row
+    for (int g = p0 / kGroup; g <= (n - 1) / kGroup; ++g) {
+        const int t0 = g * kGroup, te = min(t0 + kGroup, n);
+        uint32_t xl[kRowsPerWarp], xh[kRowsPerWarp];
+        float lmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int t = t0 + warp + kTokWarps * i;
+            xl[i] = xh[i] = 0u;
+            if (t < te && own) {
+                if (t < p0) {
+                    // a token of the open group from before this call: its bf16 row
+                    const uint16_t* row = grp + (long long)(t - t0) * d;
+                    xl[i] = *reinterpret_cast<const uint32_t*>(row + 2 * lane);
+                    xh[i] = *reinterpret_cast<const uint32_t*>(row + 2 * lane + half);
+                } else {
+                    const uint16_t* row = in + ((long long)(q0 + t - p0) * a.Hkv + h) * d;
+                    const uint32_t wl = *reinterpret_cast<const uint32_t*>(row + 2 * lane);
+                    const uint32_t wh = *reinterpret_cast<const uint32_t*>(row + 2 * lane + half);
+                    if (is_v) {
+                        xl[i] = wl;
+                        xh[i] = wh;
+                    } else {
+                        const float4 c4 = *reinterpret_cast<const float4*>(a.rope + (long long)t * half + 2 * lane);
+                        uint32_t yl, yh;
+                        if (rotate_word_fast(wl, wh, c4, yl, yh)) {
+                            const uint2 y = rotate_word_exact(wl, wh, c4);
+                            yl = y.x;
+                            yh = y.y;
+                        }
+                        xl[i] = yl;
+                        xh[i] = yh;
+                    }
+                }
+                lmax = fmaxf(lmax, fmaxf(absmax_pair(xl[i]), absmax_pair(xh[i])));
+            }
+        }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, sh));
+        if (lane == 0) wmax[warp] = lmax;
+        __syncthreads();
+        float mx = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTokWarps; ++w) mx = fmaxf(mx, wmax[w]);
+        const float sc = mx > 0.f ? __fdiv_rn(127.f, mx) : 0.f;  // m = 0: every code is 0
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int t = t0 + warp + kTokWarps * i;
+            if (t < te && own) {
+                const int blk = __ldg(bt + t / kBlock);
+                int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + t % kBlock) * d;
+                *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(xl[i], sc);
+                *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(xh[i], sc);
+                if (te == n && t >= p0) {
+                    // the request's last group stays open: its new rows join the buffer
+                    uint16_t* orow = grp + (long long)(t - t0) * d;
+                    *reinterpret_cast<uint32_t*>(orow + 2 * lane) = xl[i];
+                    *reinterpret_cast<uint32_t*>(orow + 2 * lane + half) = xh[i];
+                }
+            }
+        }
+        for (int j = t0 / kBlock + tid; j <= (te - 1) / kBlock; j += kTokThreads)
+            amax[(long long)__ldg(bt + j) * a.Hkv + h] = mx;
+        __syncthreads();  // wmax and the buffer rows are reused by the next group
+    }
+}
+
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
 }  // namespace
@@ -281,5 +464,60 @@ extern "C" mi_status mi_paged_kv_append_int8(const mi_dims* dims, const void* q,
     // at most 16
     const int warps = 2 * D.Hkv < 8 ? 8 : (2 * D.Hkv > kMaxThreads / 32 ? kMaxThreads / 32 : 2 * D.Hkv);
     const cudaError_t e = launch_pdl(append_int8_kernel, (int)D.B, warps * 32, 0, (cudaStream_t)stream, a);
+    return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
+}
+
+extern "C" mi_status mi_paged_kv_append_int8_tokens(const mi_dims* dims, int32_t total_tokens, const void* q,
+                                                    const void* k, const void* v, const float* rope_cos_sin,
+                                                    int32_t max_pos, const int32_t* block_tables,
+                                                    const int32_t* context_lens, const int32_t* query_start,
+                                                    const int32_t* open_slots, int32_t num_open_slots, void* q_out,
+                                                    void* k_cache, void* v_cache, float* k_amax, float* v_amax,
+                                                    void* k_open, void* v_open, int32_t* dev_err,
+                                                    mi_stream_t stream) {
+    using namespace mi;
+    if (!dims) return MI_ERR_INVALID_ARG;
+    const mi_dims D = *dims;
+    if (D.B < 0 || D.Hq < 1 || D.Hkv < 1 || D.num_blocks < 1 || D.max_blocks_per_seq < 1 || max_pos < 1 ||
+        num_open_slots < 1 || total_tokens < 0)
+        return MI_ERR_INVALID_ARG;
+    if (D.block_size != kBlock || (D.head_dim != 64 && D.head_dim != 128) || D.Hq % D.Hkv != 0)
+        return MI_ERR_UNSUPPORTED;
+    if ((long long)D.B * 2 * D.Hkv > 0x7FFFFFFFLL) return MI_ERR_INVALID_ARG;
+    if (D.B == 0 || total_tokens == 0) return MI_OK;
+    if (!q || !k || !v || !rope_cos_sin || !block_tables || !context_lens || !query_start || !open_slots ||
+        !q_out || !k_cache || !v_cache || !k_amax || !v_amax || !k_open || !v_open)
+        return MI_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) || !aligned(rope_cos_sin, 16) ||
+        !aligned(k_open, 16) || !aligned(v_open, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_amax, 4) || !aligned(v_amax, 4))
+        return MI_ERR_INVALID_ARG;
+    Int8TokParams a;
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.rope = reinterpret_cast<const float2*>(rope_cos_sin);
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.open_slots = open_slots;
+    a.q_out = static_cast<uint16_t*>(q_out);
+    a.kc = static_cast<int8_t*>(k_cache);
+    a.vc = static_cast<int8_t*>(v_cache);
+    a.k_amax = k_amax;
+    a.v_amax = v_amax;
+    a.k_open = static_cast<uint16_t*>(k_open);
+    a.v_open = static_cast<uint16_t*>(v_open);
+    a.dev_err = dev_err;
+    a.Hq = D.Hq;
+    a.Hkv = D.Hkv;
+    a.d = D.head_dim;
+    a.num_blocks = D.num_blocks;
+    a.mbps = D.max_blocks_per_seq;
+    a.max_pos = max_pos;
+    a.num_slots = num_open_slots;
+    a.T = total_tokens;
+    const cudaError_t e =
+        launch_pdl(append_int8_tokens_kernel, (int)(D.B * 2 * D.Hkv), kTokThreads, 0, (cudaStream_t)stream, a);
     return e == cudaSuccess ? MI_OK : MI_ERR_CUDA;
 }

@@ -327,3 +327,126 @@ def test_int8_append_errors(cuda_device):
     _assert_state_equal(ds.host(), st, "errors")
     got = ds.host()
     assert got["k8"][0, :, 4].any() and not got["k8"][3:].any()        # only request 0 wrote codes
+
+
+def _tokens_case(seed, hist, m, Hq, Hkv, d_head, spare=4):
+    r = np.random.Generator(np.random.PCG64(seed))
+    final = [h + c for h, c in zip(hist, m)]
+    B = len(hist)
+    nblk = [max(-(-f // BLOCK), 1) for f in final]
+    nb = sum(nblk) + spare
+    perm = r.permutation(nb)
+    bt = np.full((B, max(nblk) + 1), -1, np.int32)
+    i = 0
+    for b in range(B):
+        bt[b, :nblk[b]] = perm[i:i + nblk[b]]
+        i += nblk[b]
+    kc16 = np.zeros((nb, Hkv, BLOCK, d_head), np.uint16)
+    vc16 = np.zeros_like(kc16)
+    for b in range(B):
+        for t in range(hist[b]):
+            kc16[bt[b, t // BLOCK], :, t % BLOCK] = bf16_normal(r, (Hkv, d_head))
+            vc16[bt[b, t // BLOCK], :, t % BLOCK] = bf16_normal(r, (Hkv, d_head))
+    slots = r.permutation(B + 2)[:B].astype(np.int32)
+    st = oracle.int8_state(nb, Hkv, d_head, B + 2)
+    assert oracle.int8_from_bf16_cache(kc16, vc16, bt, np.array(hist, np.int32), slots, st) == 0
+    qs = np.concatenate([[0], np.cumsum(m)]).astype(np.int32)
+    T = int(qs[-1])
+    q = bf16_normal(r, (T, Hq, d_head))
+    # rows at several magnitudes (zero rows included): group maxima grow, stay and restart
+    mag = r.choice([0.0, 0.5, 1.0, 4.0], size=(2, T, Hkv, 1), p=[0.05, 0.25, 0.5, 0.2])
+    k = oracle.f64_to_bf16(oracle.bf16_to_f64(bf16_normal(r, (T, Hkv, d_head))) * mag[0])
+    v = oracle.f64_to_bf16(oracle.bf16_to_f64(bf16_normal(r, (T, Hkv, d_head))) * mag[1])
+    return st, bt, np.array(final, np.int32), qs, slots, q, k, v
+
+
+def _assert_tokens_state_equal(got, want, cl, slots, what=""):
+    """Codes and maxima everywhere; of the open-group buffers, the live rows
+    of each request's last group (rows past them are unspecified after a
+    many-token append: the token-by-token definition leaves an earlier full
+    group's rows there, the kernel leaves the slot's earlier contents)."""
+    for key in ("k8", "v8", "k_amax", "v_amax"):
+        assert np.array_equal(got[key], want[key]), f"{what}: {key} differs"
+    for b, n in enumerate(cl):
+        if n > 0:
+            o = (int(n) - 1) % GRP + 1
+            for key in ("k_open", "v_open"):
+                assert np.array_equal(got[key][slots[b], :, :o], want[key][slots[b], :, :o]), (what, key, b)
+
+
+def _gpu_append_tokens(mi, d, ds, q, k, v, table, max_pos, bt, cl, qs, slots, device):
+    import torch
+    qo_d = torch.zeros((q.shape[0],) + q.shape[1:], dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    st = mi.mi_paged_kv_append_int8_tokens(d, q.shape[0], to_dev_u16(q, device), to_dev_u16(k, device),
+                                           to_dev_u16(v, device), torch.from_numpy(table).to(device), max_pos,
+                                           to_dev_i32(bt, device), to_dev_i32(cl, device), to_dev_i32(qs, device),
+                                           to_dev_i32(slots, device), qo_d, ds.k8, ds.v8, ds.k_amax, ds.v_amax,
+                                           ds.k_open, ds.v_open, err)
+    assert st == 0, mi.status_string(st)
+    torch.cuda.synchronize()
+    return from_dev_u16(qo_d), int(err.item())
+
+
+@pytest.mark.parametrize("d_head,Hq,Hkv", [(128, 8, 2), (64, 4, 4), (128, 7, 1)])
+def test_int8_append_tokens_equals_sequential_appends(cuda_device, d_head, Hq, Hkv):
+    """Prompts and chunks (1 to 300 new tokens, from histories at every phase
+    of a group) through mi_paged_kv_append_int8_tokens: q_out and the whole
+    INT8 state bit for bit as the oracle's token-by-token appends, then the
+    attention over the result within the tolerance."""
+    mi = _mi()
+    hist = [0, 1, 15, 63, 64, 100, 500, 10]
+    m = [300, 1, 70, 2, 129, 28, 64, 0]
+    st, bt, cl, qs, slots, q, k, v = _tokens_case(70 + d_head + Hq, hist, m, Hq, Hkv, d_head)
+    table = oracle.rope_table(1e6, d_head, 1024)
+    d = mi.dims(len(hist), Hq, Hkv, d_head, st["k8"].shape[0], bt.shape[1])
+    ds = DevState(st, cuda_device)
+    q_gpu, err = _gpu_append_tokens(mi, d, ds, q, k, v, table, 1024, bt, cl, qs, slots, cuda_device)
+    assert err == 0
+    q_ref, s = oracle.append_int8_tokens(q, k, v, table, bt, cl, qs, slots, st)
+    assert s == 0
+    assert np.array_equal(q_gpu, q_ref)
+    _assert_tokens_state_equal(ds.host(), st, cl, slots, "tokens")
+    # decode attention over the appended state (the last token's q of each request)
+    last = np.maximum(qs[1:] - 1, 0)
+    qd = q_ref[last]
+    live = cl > 0
+    ref = oracle.paged_attention_int8(qd, st["k8"], st["v8"], st["k_amax"], st["v_amax"], bt, cl, 0.1)
+    out, err = _gpu_attend(mi, d, qd, ds, bt, cl, 0.1, cuda_device)
+    assert err == 0
+    got = oracle.bf16_to_f64(out)
+    vmax = float(st["v_amax"].max())
+    assert np.abs(got[live] - ref[live]).max() <= 1e-2 * max(1.0, vmax / 4)
+
+
+def test_int8_append_tokens_errors(cuda_device):
+    """query_start out of order, more new tokens than the context, a position
+    past max_pos, a bad slot and a bad block id each set their bit and skip
+    what they name; a good request in the same call appends."""
+    mi = _mi()
+    hist = [10, 20, 30, 40, 50, 60]
+    m = [5, 5, 5, 5, 5, 5]
+    st, bt, cl, qs, slots, q, k, v = _tokens_case(80, hist, m, 4, 2, 64)
+    table = oracle.rope_table(1e6, 64, 66)
+    cl = cl.copy(); qs = qs.copy(); slots = slots.copy(); bt = bt.copy()
+    cl[1] = 3                      # 5 new tokens in a context of 3: bad query
+    slots[2] = 99                  # bad slot
+    bt[3, 2] = 10_000              # bad block in the touched group
+    cl[4] = 70                     # last position 69 >= max_pos 66 (request 5 ends at 64)
+    d = mi.dims(len(hist), 4, 2, 64, st["k8"].shape[0], bt.shape[1])
+    ds = DevState(st, cuda_device)
+    q_gpu, err = _gpu_append_tokens(mi, d, ds, q, k, v, table, 66, bt, cl, qs, slots, cuda_device)
+    for bit in (mi.MI_DEVERR_BAD_QUERY, mi.MI_DEVERR_BAD_SLOT, mi.MI_DEVERR_BAD_BLOCK, mi.MI_DEVERR_BAD_POS):
+        assert err & bit, bit
+    got = ds.host()
+    # requests 0 and 5 appended like the oracle's token-by-token appends
+    ref_st = {key: val.copy() for key, val in st.items()}
+    keep = np.array([0, 5])
+    sub_qs = np.array([0, 5, 10], np.int32)
+    rows = np.concatenate([np.arange(qs[b], qs[b + 1]) for b in keep])
+    q_ref, s = oracle.append_int8_tokens(q[rows], k[rows], v[rows], table, bt[keep], cl[keep], sub_qs, slots[keep],
+                                         ref_st)
+    assert s == 0
+    _assert_tokens_state_equal(got, ref_st, cl[keep], slots[keep], "errors")
+    assert np.array_equal(q_gpu[rows], q_ref)
+    assert not q_gpu[qs[4]:qs[5]].any() and not q_gpu[qs[1]:qs[2]].any()   # skipped requests: no q_out

@@ -283,3 +283,45 @@ def test_int8_attention_scaling_by_two_is_exact():
     v0 = v8.copy(); v0[blk] = 0
     assert np.array_equal(oracle.paged_attention_int8(q, k8, v8, ka, va0, bt, cl, 0.02),
                           oracle.paged_attention_int8(q, k8, v0, ka, va, bt, cl, 0.02))
+
+
+def test_int8_append_tokens_equals_history():
+    """Many new tokens per request through the oracle's chunked helper (the
+    token-by-token append in order) give the quantisation of the final
+    history, from every phase of a group, with chunks crossing groups."""
+    r = np.random.Generator(np.random.PCG64(90))
+    Hq, Hkv, d = 4, 2, 32
+    hist = [0, 1, 63, 64, 100, 10]
+    m = [70, 1, 2, 129, 28, 0]
+    final = [h + c for h, c in zip(hist, m)]
+    kc, vc, bt, _, slots, nslot = _history_case(91, [max(f, 1) for f in final], Hkv=Hkv, d=d)
+    nb = kc.shape[0]
+    table = oracle.rope_table(1e6, d, 512)
+    kc16, vc16 = np.zeros_like(kc), np.zeros_like(vc)
+    for b in range(len(hist)):
+        for t in range(hist[b]):
+            kc16[bt[b, t // BS], :, t % BS] = kc[bt[b, t // BS], :, t % BS]
+            vc16[bt[b, t // BS], :, t % BS] = vc[bt[b, t // BS], :, t % BS]
+    st = oracle.int8_state(nb, Hkv, d, nslot)
+    assert oracle.int8_from_bf16_cache(kc16, vc16, bt, np.array(hist, np.int32), slots, st) == 0
+    qs = np.concatenate([[0], np.cumsum(m)]).astype(np.int32)
+    T = int(qs[-1])
+    q, k, v = (bf16_normal(r, (T, H, d)) for H in (Hq, Hkv, Hkv))
+    q_out, s = oracle.append_int8_tokens(q, k, v, table, bt, np.array(final, np.int32), qs, slots, st)
+    assert s == 0
+    # the bf16 history the same tokens make, one bf16 append per token
+    for b in range(len(hist)):
+        for i in range(m[b]):
+            p = hist[b] + i
+            row = qs[b] + i
+            qo, s16 = oracle.append(q[row:row + 1], k[row:row + 1], v[row:row + 1], np.array([p], np.int32),
+                                    oracle.slot_mapping(bt[b:b + 1], np.array([p], np.int32)), table, kc16, vc16)
+            assert s16 == 0 and np.array_equal(qo[0], q_out[row])
+    want = oracle.int8_state(nb, Hkv, d, nslot)
+    assert oracle.int8_from_bf16_cache(kc16, vc16, bt, np.array(final, np.int32), slots, want) == 0
+    for key in ("k8", "v8", "k_amax", "v_amax"):
+        assert np.array_equal(st[key], want[key]), key
+    for b in range(len(hist)):
+        if final[b] > 0:
+            o = (final[b] - 1) % GRP + 1
+            assert np.array_equal(st["k_open"][slots[b], :, :o], want["k_open"][slots[b], :, :o])
