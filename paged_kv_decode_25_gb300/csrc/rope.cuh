@@ -39,37 +39,29 @@ __device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double 
 // RN_bf16(RN_double(a*b + c*d)) for bf16 a, c and fp32 b, d, in single
 // precision when that decides it. q = RN(c*d) and its rounding error qe (an
 // fma recovers it exactly above the underflow range) give c*d = q + qe; the
-// fma s = RN(a*b + q) rounds the exact a*b + q once, so |exact - s| <=
-// |qe| + ulp(s)/2. The decision is taken on the bit patterns alone:
-//  * s sits L = (its low 16 bits) fp32 ulps above the bf16 value below it,
-//    so the nearest bf16 rounding boundary (the midpoint at L = 0x8000, the
-//    next one up at 0x18000, and, across the binade edge below, the one at
-//    -0x4000) is dist = min(|L - 0x8000|, L + 0x4000, 0x18000 - L) ulps away;
-//  * |qe| < 2^(e(qe) - e(s) + 24) ulp(s) from the biased exponents;
-//  * so no boundary lies within reach when dist >= 2 (|qe| below an ulp) or
-//    dist >= 2^k + 2 (k = e(qe) - e(s) + 24 >= 0), which also leaves room
-//    for the double rounding's 2^-53 relative.
-// Otherwise (a boundary within reach, s zero, tiny (below 2^-100), infinite
-// or NaN, q tiny but not zero) `slow` is set and the caller takes the
-// double-precision route. Returns s; the caller rounds pairs of them to bf16
-// with the hardware conversion (the same nearest-even result for the
-// finite, normal s this path keeps). The _rn intrinsics keep the compiler
-// from contracting c*d into an fma, which would break the split. (The same
-// test written with float products, a conversion of dist and float
-// compares took ~40 times longer per word.)
+// fma s = RN(a*b + q) rounds the exact a*b + q once, so
+//   |exact - s| <= |qe| + ulp(s)/2 <= |qe| + |s| 2^-24 <= err,
+// err being that sum (plus 2^-140 for a product c*d that underflowed)
+// rounded upward. lo = s - err rounded down and hi = s + err rounded up
+// enclose the exact value and its double rounding; rounding to bf16 is
+// monotone, so when lo and hi round to the same bf16 (one paired hardware
+// conversion) the exact value does too, and so does s. Otherwise (a
+// boundary within reach, s zero, tiny (below 2^-100), huge or not finite, q
+// tiny but not zero) `slow` is set and the caller takes the double-precision
+// route. Returns s; the caller rounds pairs of them to bf16 with the same
+// conversion. The _rn intrinsics keep the compiler from contracting c*d into
+// an fma, which would break the split. (An earlier test on the bit patterns,
+// about twenty integer operations per value, made the prefill append ALU-
+// bound.)
 __device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bool& slow) {
     const float q = __fmul_rn(c, d);
     const float qe = fmaf(c, d, -q);
     const float s = fmaf(a, b, q);
-    const uint32_t S = __float_as_uint(s) & 0x7FFFFFFFu;
-    const uint32_t Q = __float_as_uint(q) & 0x7FFFFFFFu;
-    const int es = (int)(S >> 23), eq = (int)(Q >> 23);
-    const int eqe = max((int)((__float_as_uint(qe) & 0x7FFFFFFFu) >> 23), 1);
-    const int L = (int)(S & 0xFFFFu);
-    const int dist = min(min(abs(L - 0x8000), L + 0x4000), 0x18000 - L);
-    const int k = eqe - es + 24;
-    const int need = k < 0 ? 2 : (k < 16 ? (1 << k) + 2 : 0x20000);
-    const bool ok = es >= 27 && es <= 254 && (Q == 0u || eq >= 27) && dist >= need;
+    const float as = fabsf(s);
+    const float err = __fmaf_ru(as, 0x1p-24f, __fadd_ru(fabsf(qe), 0x1p-140f));
+    const uint32_t pk = pack_bf16x2(__fsub_rd(s, err), __fadd_ru(s, err));
+    const bool ok = ((pk ^ (pk >> 16)) & 0xFFFFu) == 0u && as >= 0x1p-100f && as < 0x1p127f &&
+                    (fabsf(q) >= 0x1p-100f || q == 0.f);
     slow |= !ok;
     return s;
 }

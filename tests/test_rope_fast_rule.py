@@ -2,12 +2,12 @@
 
 The append and the fused decode step compute each rotated value
 RN_bf16(RN_f64(a*b + c*d)) (a, c bf16; b, d the fp32 table entries) in fp32
-when an integer test on the bit patterns says that no bf16 rounding boundary
-lies within the fp32 result's error bound, and by the exact double route
+when both ends of the fp32 result's error interval round to the same bf16, and by the exact double route
 otherwise. This test restates that decision rule in numpy (fp32 products and
 fma simulated exactly in wider precision) and checks, against the oracle's
 own double-to-bf16 rounding, that every value the rule lets through rounds
-to the same bf16 as the exact definition: on random values over 40 binades
+to the same bf16 as the exact definition (the rule: the fp32 result's error
+interval, widened with directed rounding, rounds to one bf16 at both ends): on random values over 40 binades
 and on inputs whose exact value lies within 4 fp32 ulps of a bf16 midpoint
 or of a power of two. A failure here means the kernels' shortcut is unsound;
 the GPU tests compare the kernels' bits with the oracle directly."""
@@ -21,23 +21,35 @@ def _f32(x):
     return np.asarray(x, np.float64).astype(np.float32)
 
 
+def _round_dir(x, up):
+    """float32 nearest to the long double x in the given direction."""
+    f = np.asarray(x, np.longdouble).astype(np.float32)
+    fl = f.astype(np.longdouble)
+    if up:
+        return np.where(fl < x, np.nextafter(f, np.float32(np.inf)), f)
+    return np.where(fl > x, np.nextafter(f, np.float32(-np.inf)), f)
+
+
+def _bf16_rn(f):
+    """bf16 bits of float32 values, round to nearest even (the hardware conversion)."""
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
 def _rule(a, b, c, d):
     """(bf16 bits of RN_bf16(s), accepted) for the kernel's fast path."""
     q = _f32(c * d)                                     # the product is exact in double
     qe = _f32(c * d - q.astype(np.float64))             # its rounding error, exact above underflow
     s = (np.longdouble(a * b) + np.longdouble(q.astype(np.float64))).astype(np.float32)  # one rounding
-    S = s.view(np.uint32) & 0x7FFFFFFF
-    Q = q.view(np.uint32) & 0x7FFFFFFF
-    es, eq = (S >> 23).astype(np.int64), (Q >> 23).astype(np.int64)
-    eqe = np.maximum(((qe.view(np.uint32) & 0x7FFFFFFF) >> 23).astype(np.int64), 1)
-    L = (S & 0xFFFF).astype(np.int64)
-    dist = np.minimum(np.minimum(np.abs(L - 0x8000), L + 0x4000), 0x18000 - L)
-    k = eqe - es + 24
-    need = np.where(k < 0, 2, np.where(k < 16, (1 << np.clip(k, 0, 15)) + 2, 0x20000))
-    ok = (es >= 27) & (es <= 254) & ((Q == 0) | (eq >= 27)) & (dist >= need)
-    u = s.view(np.uint32).astype(np.uint64)
-    bits = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)  # round to nearest even
-    return bits, ok
+    L = np.longdouble
+    a_s = np.abs(s)
+    t = _round_dir(np.abs(qe).astype(L) + L(2.0) ** -140, up=True)
+    err = _round_dir(a_s.astype(L) * L(2.0) ** -24 + t.astype(L), up=True)
+    lo = _round_dir(s.astype(L) - err.astype(L), up=False)
+    hi = _round_dir(s.astype(L) + err.astype(L), up=True)
+    ok = ((_bf16_rn(lo) == _bf16_rn(hi)) & (a_s >= np.float32(2.0 ** -100)) & (a_s < np.float32(2.0 ** 127)) &
+          ((np.abs(q) >= np.float32(2.0 ** -100)) | (q == 0)))
+    return _bf16_rn(s), ok
 
 
 def _exact(a, b, c, d):
