@@ -44,25 +44,25 @@ __device__ __forceinline__ uint32_t rot_hi(double a, double b, double c, double 
 // err being that sum (plus 2^-140 for a product c*d that underflowed)
 // rounded upward. lo = s - err rounded down and hi = s + err rounded up
 // enclose the exact value and its double rounding; rounding to bf16 is
-// monotone, so when lo and hi round to the same bf16 (one paired hardware
-// conversion) the exact value does too, and so does s. Otherwise (a
-// boundary within reach, s zero, tiny (below 2^-100), huge or not finite, q
-// tiny but not zero) `slow` is set and the caller takes the double-precision
-// route. Returns s; the caller rounds pairs of them to bf16 with the same
-// conversion. The _rn intrinsics keep the compiler from contracting c*d into
-// an fma, which would break the split. (An earlier test on the bit patterns,
-// about twenty integer operations per value, made the prefill append ALU-
-// bound.)
-__device__ __forceinline__ float rot_fast(float a, float b, float c, float d, bool& slow) {
+// monotone, so when lo and hi round to the same bf16 the exact value does
+// too, and so does s. Returns s and sets lo and hi; the caller rounds pairs
+// of values, and of their lo and hi, with the hardware conversion and
+// compares the packed ends a pair at a time. `slow` is set here when s is
+// zero, tiny (below 2^-100), huge or not finite, or q tiny but not zero;
+// the caller then (or when the ends differ) takes the double-precision
+// route. The _rn intrinsics keep the compiler from contracting c*d into an
+// fma, which would break the split. (An earlier test on the bit patterns,
+// about twenty integer operations per value, made the prefill append
+// ALU-bound.)
+__device__ __forceinline__ float rot_fast(float a, float b, float c, float d, float& lo, float& hi, bool& slow) {
     const float q = __fmul_rn(c, d);
     const float qe = fmaf(c, d, -q);
     const float s = fmaf(a, b, q);
     const float as = fabsf(s);
     const float err = __fmaf_ru(as, 0x1p-24f, __fadd_ru(fabsf(qe), 0x1p-140f));
-    const uint32_t pk = pack_bf16x2(__fsub_rd(s, err), __fadd_ru(s, err));
-    const bool ok = ((pk ^ (pk >> 16)) & 0xFFFFu) == 0u && as >= 0x1p-100f && as < 0x1p127f &&
-                    (fabsf(q) >= 0x1p-100f || q == 0.f);
-    slow |= !ok;
+    lo = __fsub_rd(s, err);
+    hi = __fadd_ru(s, err);
+    slow |= !(as >= 0x1p-100f && as < 0x1p127f && (fabsf(q) >= 0x1p-100f || q == 0.f));
     return s;
 }
 
@@ -93,12 +93,15 @@ __device__ __forceinline__ bool rotate_word_fast(uint32_t xl, uint32_t xh, float
     const float fa0 = bf16_lo(xl), fa1 = bf16_hi(xl);
     const float fb0 = bf16_lo(xh), fb1 = bf16_hi(xh);
     bool slow = false;
-    const float s0 = rot_fast(fa0, cs.x, -fb0, cs.y, slow);
-    const float s1 = rot_fast(fa1, cs.z, -fb1, cs.w, slow);
-    const float s2 = rot_fast(fb0, cs.x, fa0, cs.y, slow);
-    const float s3 = rot_fast(fb1, cs.z, fa1, cs.w, slow);
+    float lo0, hi0, lo1, hi1, lo2, hi2, lo3, hi3;
+    const float s0 = rot_fast(fa0, cs.x, -fb0, cs.y, lo0, hi0, slow);
+    const float s1 = rot_fast(fa1, cs.z, -fb1, cs.w, lo1, hi1, slow);
+    const float s2 = rot_fast(fb0, cs.x, fa0, cs.y, lo2, hi2, slow);
+    const float s3 = rot_fast(fb1, cs.z, fa1, cs.w, lo3, hi3, slow);
     yl = pack_bf16x2(s0, s1);
     yh = pack_bf16x2(s2, s3);
+    // both ends of each value's interval round alike: a pair at a time
+    slow |= pack_bf16x2(lo0, lo1) != pack_bf16x2(hi0, hi1) || pack_bf16x2(lo2, lo3) != pack_bf16x2(hi2, hi3);
     return slow;
 }
 
