@@ -531,15 +531,18 @@ def measure_sweep_config(mi, device, stream, w, peak, flush, oracle_budget_s):
     meta = [(torch.empty((B, w.max_blocks_per_seq), dtype=torch.int32).pin_memory(),
              torch.empty(B, dtype=torch.int32).pin_memory(), np.empty(B, np.int32), torch.cuda.Event())
             for _ in range(2)]
-    ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
+    # two workspaces in turn: consecutive layers start early (MI_STEP_EARLY_START)
+    ws = [torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
+          for _ in range(2)]
     err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def layers(st_):
         for layer in range(L):
             kc, vc = caches[layer]
             mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, w.max_pos, bt_d,
-                                             cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
-                                             dev_err=err, stream=st_), "decode step")
+                                             cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws[layer % 2],
+                                             dev_err=err, stream=st_, flags=mi.MI_STEP_EARLY_START),
+                     "decode step")
 
     def host_step(pool, s, buf):
         h_bt, h_cl, h_sl, ev = meta[buf]
@@ -1093,6 +1096,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default: the workload's); fewer only for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-early-start", action="store_true",
+                    help="fused steps wait for the layer before them before planning (no MI_STEP_EARLY_START)")
     ap.add_argument("--no-per-variant", action="store_true",
                     help="skip the e4m3-cache run of the same step in the default line")
     ap.add_argument("--no-per-config", action="store_true",
@@ -1181,6 +1186,12 @@ def main():
     ws = torch.empty(mi.mi_paged_decode_workspace_bytes(d) // 4 + 4, dtype=torch.float32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     stream = stream0 = torch.cuda.current_stream(device)
+    # fused steps start early (each layer's plan and first copies overlap the
+    # layer before): no layer writes another's inputs, and two workspaces in
+    # turn keep each step's plan entries away from the step before it
+    early = not args.no_early_start
+    step_flags = mi.MI_STEP_EARLY_START if early else 0
+    ws_step = (ws, torch.empty_like(ws)) if early else (ws, ws)
 
     # the fused step (append + attention in one launch per layer; bf16 caches
     # on the MMA tile, or e4m3 caches) is the timed path; the two calls are
@@ -1195,15 +1206,16 @@ def main():
             if fuse:
                 if ev is not None:
                     ev[layer][0].record(stream)
+                wsl = ws_step[layer % 2]
                 if fp8:
                     mi.check(mi.mi_paged_decode_step_fp8(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos,
                                                          bt_d, cl_d, ks_d, vs_d, w.scale, qo_all[layer], kc, vc,
-                                                         out_all[layer], ws, dev_err=err, stream=stream),
-                             "decode step (e4m3)")
+                                                         out_all[layer], wsl, dev_err=err, stream=stream,
+                                                         flags=step_flags), "decode step (e4m3)")
                 else:
                     mi.check(mi.mi_paged_decode_step(d, q_all[layer], k_all[layer], v_all[layer], rope, max_pos,
-                                                     bt_d, cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], ws,
-                                                     dev_err=err, stream=stream), "decode step")
+                                                     bt_d, cl_d, w.scale, qo_all[layer], kc, vc, out_all[layer], wsl,
+                                                     dev_err=err, stream=stream, flags=step_flags), "decode step")
                 if ev is not None:
                     ev[layer][1].record(stream)
                 continue
@@ -1264,6 +1276,8 @@ def main():
     except RuntimeError as e:  # capture refused: time stream launches instead
         g_step = None
         launch_mode = "stream launches (%s)" % str(e).splitlines()[0][:120]
+    if fused and early:
+        launch_mode += "; fused steps start early (MI_STEP_EARLY_START, two workspaces in turn)"
     evs_t = new_events(args.steps) if g_step is None else None
     for _ in range(args.warmup):
         if g_step is not None:

@@ -293,12 +293,36 @@ mi_status mi_paged_decode_attention(const mi_dims* dims, const void* q, const vo
  * Device buffers as for the two calls; q is the raw (unrotated) q and must
  * not overlap q_out (MI_ERR_INVALID_ARG). Requests with n <= 0 append nothing
  * and get zero rows; n - 1 >= max_pos sets MI_DEVERR_BAD_POS and leaves that
- * request's q zero. */
+ * request's q zero.
+ * flags: 0, or MI_STEP_EARLY_START (below); any other bit is
+ * MI_ERR_INVALID_ARG. */
 mi_status mi_paged_decode_step(const mi_dims* dims, const void* q, const void* k, const void* v,
                                const float* rope_cos_sin, int32_t max_pos, const int32_t* block_tables,
                                const int32_t* context_lens, float scale, void* q_out, void* k_cache,
                                void* v_cache, void* out, void* workspace, size_t workspace_bytes,
-                               int32_t* dev_err, mi_stream_t stream);
+                               int32_t* dev_err, mi_stream_t stream, uint32_t flags);
+
+/* Early start of a fused step (mi_paged_decode_step, mi_paged_decode_step_fp8).
+ * Every call of this library waits for the kernel launched just before it on
+ * the same stream before it reads anything, though it may be launched while
+ * that kernel is finishing (programmatic dependent launch). With this flag
+ * the step reads context_lens, block_tables, the cache rows of the history
+ * and its plan entries in the workspace before that wait, and may write
+ * those plan entries and report errors into dev_err: in a stack of layers,
+ * each layer's plan and first KV copies then overlap the previous layer's
+ * last CTAs. The results are bit for bit those without the flag.
+ * The caller guarantees that the kernel launched just before the call on
+ * the same stream writes none of this call's context_lens, block_tables,
+ * k_cache and v_cache, does not clear dev_err (the library's own error
+ * reports are atomic ORs, so consecutive steps may share one word), and
+ * neither reads nor writes this call's workspace. So two consecutive
+ * early-start calls take different workspaces (two, used in turn, suffice:
+ * the step lets the next launch start only after its own wait, so a
+ * launch never runs beside the one two before it), and a call directly
+ * after mi_kv_copy_blocks, mi_kv_copy_rows or an append into the same
+ * caches, or after a kernel of the caller's that fills the tables or
+ * lengths, does not set the flag. */
+#define MI_STEP_EARLY_START 1u
 
 /* Kernel variant used by mi_paged_decode_attention_variant:
  *   MI_ATTN_MMA  bf16 tensor-core tiles (mma.sync m16n8k16: 16 tokens x 8 heads),
@@ -363,12 +387,14 @@ mi_status mi_paged_decode_attention_fp8(const mi_dims* dims, const void* q, cons
  * where the e4m3 attention runs three, so the split differs). A K
  * or V scale that is not a positive finite number leaves that row of the
  * cache as it was (MI_DEVERR_BAD_SCALE). Other arguments, errors and
- * guarantees as mi_paged_decode_step; q must not overlap q_out. */
+ * guarantees as mi_paged_decode_step (flags included); q must not overlap
+ * q_out. */
 mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q, const void* k, const void* v,
                                    const float* rope_cos_sin, int32_t max_pos, const int32_t* block_tables,
                                    const int32_t* context_lens, const float* k_scale, const float* v_scale,
                                    float scale, void* q_out, void* k_cache, void* v_cache, void* out,
-                                   void* workspace, size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream);
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream,
+                                   uint32_t flags);
 
 /* ---- INT8 KV cache in 64-token groups (nxmr.cn article, §2.2
  * "量化压缩的实战选择": 8-bit KV quantised per group of 64 tokens rather than

@@ -29,6 +29,7 @@ MI_ADMIT_PROCEED, MI_ADMIT_SOFT_BRAKE, MI_ADMIT_HARD_BRAKE = 0, 1, 2
 MI_ADMIT_HARD_BP_DEFAULT, MI_ADMIT_SOFT_BP_DEFAULT = 1000, 3000
 MI_PREFILL_DEFAULT, MI_PREFILL_MMA, MI_PREFILL_TCGEN05, MI_PREFILL_TCGEN05_PAIR = 0, 1, 2, 3
 MI_DEVERR_INTERNAL = 0x80
+MI_STEP_EARLY_START = 0x1
 
 # every symbol include/mi.h declares
 EXPORTS = (
@@ -107,9 +108,10 @@ def load():
             "mi_paged_decode_attention_int8": (
                 [dims_p, P, P, P, P, P, P, P, f32, P, P, ctypes.c_size_t, P, P], i32),
             "mi_paged_decode_step": (
-                [dims_p, P, P, P, P, i32, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
+                [dims_p, P, P, P, P, i32, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P, ctypes.c_uint32], i32),
             "mi_paged_decode_step_fp8": (
-                [dims_p, P, P, P, P, i32, P, P, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P], i32),
+                [dims_p, P, P, P, P, i32, P, P, P, P, f32, P, P, P, P, P, ctypes.c_size_t, P, P, ctypes.c_uint32],
+                i32),
             "mi_test_set_wait_limit": ([ctypes.c_int64], i32),
             "mi_test_withhold_copy": ([i32], i32),
         }
@@ -363,12 +365,13 @@ def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tabl
 
 
 def mi_paged_decode_step(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, scale, q_out,
-                         k_cache, v_cache, out, workspace, workspace_bytes=None, dev_err=None, stream=None):
+                         k_cache, v_cache, out, workspace, workspace_bytes=None, dev_err=None, stream=None,
+                         flags=0):
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return load().mi_paged_decode_step(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
                                        int(max_pos), _ptr(block_tables), _ptr(context_lens), float(scale),
                                        _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(workspace),
-                                       int(wb), _ptr(dev_err), _stream(stream))
+                                       int(wb), _ptr(dev_err), _stream(stream), int(flags))
 
 
 def mi_paged_kv_append_fp8(d: MiDims, q, k, v, positions, slot_mapping, rope_cos_sin, max_pos, q_out,
@@ -467,12 +470,13 @@ def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tabl
 
 def mi_paged_decode_step_fp8(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, k_scale,
                              v_scale, scale, q_out, k_cache, v_cache, out, workspace, workspace_bytes=None,
-                             dev_err=None, stream=None):
+                             dev_err=None, stream=None, flags=0):
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return load().mi_paged_decode_step_fp8(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
                                            int(max_pos), _ptr(block_tables), _ptr(context_lens), _ptr(k_scale),
                                            _ptr(v_scale), float(scale), _ptr(q_out), _ptr(k_cache), _ptr(v_cache),
-                                           _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream))
+                                           _ptr(out), _ptr(workspace), int(wb), _ptr(dev_err), _stream(stream),
+                                           int(flags))
 
 
 def mi_test_set_wait_limit(ns):

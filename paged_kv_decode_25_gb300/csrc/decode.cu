@@ -97,6 +97,7 @@ struct AttnParams {
     int plan_stride;
     int plan_kind;                 // which kernel the plans are for (variant, fused step)
     long long wait_ns;             // bound on every mbarrier wait of the launch
+    int early;                     // fused step: plan and first copies before the wait on the kernel before
     int withhold;                  // failure-detection test: each producer withholds its first copy
 };
 
@@ -1138,9 +1139,18 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
         mbar_init(kvfull0 + tid * 8, 1);
     }
     fence_mbar_init();
-    // Inputs may come from the kernel just before this one in the stream.
-    pdl_wait();
-    pdl_trigger();
+    // Inputs may come from the kernel just before this one in the stream:
+    // what it wrote is visible only past pdl_wait. An early-start fused step
+    // (the caller promises that kernel writes none of the lengths, the block
+    // tables, the caches, the error word or this call's workspace) plans
+    // and issues each producer lane's first S copies before its wait. Every
+    // thread lets the next launch start only after its own wait has
+    // returned, so that launch never runs beside the one before this.
+    const bool early = FUSED && p.early != 0;
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
     // Warm L2 with this CTA's share of the block tables and of q (and, for
     // the fused step, of the new token's k and v rows): the lookups and loads
     // that follow the plan then hit L2 instead of going to DRAM.
@@ -1224,6 +1234,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
         }
     }
     const long long ra = rp->ra, rb = rp->rb, sl = rp->sl;
+    if (early && !(warp == W && lane < W)) {
+        pdl_wait();
+        pdl_trigger();
+    }
 
     if (FUSED && warp == W + 1) {
         // --------------------------------------------------- RoPE warp --
@@ -1419,6 +1433,8 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
         // arrives for its first block, so consumer warp 0's wait on that
         // stage runs out (some CTAs may have no blocks at all)
         bool withhold = p.withhold != 0 && lane == 0;
+        bool waited = !early;  // early start: this lane waits once its first S copies are issued
+        int issued = 0;
         const uint32_t my_full = full0 + (uint32_t)(lane * S) * 8, my_empty = empty0 + (uint32_t)(lane * S) * 8;
         const uint32_t my_tiles = sbase + sp.tiles + (uint32_t)(lane * S) * (2 * kTile);
         for (int part = 0; part < 2; ++part) {
@@ -1458,6 +1474,12 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
                     }
                 }
             }
+            if (!waited && issued == S) {
+                pdl_wait();
+                pdl_trigger();
+                waited = true;
+            }
+            ++issued;
             if (!mbar_wait_bounded(my_empty + stg * 8, ph, p.wait_ns, kSleep)) {
                 // the consumer stopped taking stages (it timed out itself)
                 raise_err(p.dev_err, MI_DEVERR_TIMEOUT);
@@ -1506,6 +1528,10 @@ __global__ void __launch_bounds__((W + (FUSED ? 2 : 1)) * 32, (VAR == kVarFp8 ||
                 ph ^= 1u;
             }
         }
+        }
+        if (!waited) {
+            pdl_wait();
+            pdl_trigger();
         }
         return;
     }
@@ -1957,6 +1983,7 @@ struct StepArgs {
     const float* rope;
     int32_t max_pos;
     void* q_out;
+    uint32_t flags;  // MI_STEP_* bits
 };
 
 // Checks, plans and launches one attention call of variant `var` (bf16 caches
@@ -2056,6 +2083,7 @@ mi_status attention(const mi_dims* dims, const void* q, const void* k_cache, con
     p.vc = static_cast<uint16_t*>(const_cast<void*>(v_cache));
     p.max_pos = step ? step->max_pos : 0;
     p.wait_ns = test_wait_limit_ns();
+    p.early = step && (step->flags & MI_STEP_EARLY_START) ? 1 : 0;
     p.withhold = test_withhold_copy() ? 1 : 0;
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -2086,9 +2114,10 @@ extern "C" mi_status mi_paged_decode_step(const mi_dims* dims, const void* q, co
                                         const int32_t* block_tables, const int32_t* context_lens,
                                         float scale, void* q_out, void* k_cache, void* v_cache, void* out,
                                         void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                                        mi_stream_t stream) {
+                                        mi_stream_t stream, uint32_t flags) {
     using namespace mi;
-    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out};
+    if (flags & ~MI_STEP_EARLY_START) return MI_ERR_INVALID_ARG;
+    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out, flags};
     return attention(dims, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, scale, out,
                      workspace, workspace_bytes, dev_err, stream, kVarMma, 0, &step);
 }
@@ -2098,9 +2127,11 @@ extern "C" mi_status mi_paged_decode_step_fp8(const mi_dims* dims, const void* q
                                             const int32_t* block_tables, const int32_t* context_lens,
                                             const float* k_scale, const float* v_scale, float scale, void* q_out,
                                             void* k_cache, void* v_cache, void* out, void* workspace,
-                                            size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream) {
+                                            size_t workspace_bytes, int32_t* dev_err, mi_stream_t stream,
+                                            uint32_t flags) {
     using namespace mi;
-    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out};
+    if (flags & ~MI_STEP_EARLY_START) return MI_ERR_INVALID_ARG;
+    const StepArgs step{k, v, rope_cos_sin, max_pos, q_out, flags};
     return attention(dims, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
                      workspace, workspace_bytes, dev_err, stream, kVarFp8, 0, &step);
 }

@@ -44,6 +44,19 @@ def test_library_exports_every_declared_symbol(mi):
     assert declared == set(mi.EXPORTS)
 
 
+def test_header_constants_match_the_binding(mi):
+    """Every numeric #define of the header has the binding's value."""
+    src = open(os.path.join(ROOT, "include", "mi.h")).read()
+    found = 0
+    for name, val in re.findall(r"^#define (MI_\w+)\s+\(?([0-9xXa-fA-F]+)u?", src, flags=re.M):
+        if name == "MI_NOALLOC_SCRATCH_BYTES":
+            continue  # a product, checked below
+        assert getattr(mi, name) == int(val, 0), name
+        found += 1
+    assert found >= 14
+    assert mi.MI_NOALLOC_SCRATCH_BYTES == 16 * 1024 * 1024
+
+
 def _compare(lib, model, seqs, mbps):
     bt1, cl1, sl1 = lib.batch_meta(seqs)
     bt2, cl2, sl2 = model.batch_meta(seqs)
@@ -237,6 +250,15 @@ def test_step_rejects_bad_args_without_a_gpu(mi):
     assert step(qo=a["q"] + 16) == mi.MI_ERR_INVALID_ARG
     assert step(qo=a["q"] - 2 * 4 * 64 * 2 + 16) == mi.MI_ERR_INVALID_ARG
     # an empty batch is a no-op
+    assert step(dims=mi.dims(0, 4, 2, 64, 8, 4)) == mi.MI_OK
+    # flags: only MI_STEP_EARLY_START is defined
+    for bad in (2, 0x80000000, mi.MI_STEP_EARLY_START | 4):
+        assert mi.mi_paged_decode_step(d, a["q"], a["k"], a["v"], a["rope"], 64, a["bt"], a["cl"], 0.125, a["qo"],
+                                       a["kc"], a["vc"], a["out"], a["ws"], workspace_bytes=1 << 20, stream=0,
+                                       flags=bad) == mi.MI_ERR_INVALID_ARG
+        assert mi.mi_paged_decode_step_fp8(d, a["q"], a["k"], a["v"], a["rope"], 64, a["bt"], a["cl"], a["k"],
+                                           a["v"], 0.125, a["qo"], a["kc"], a["vc"], a["out"], a["ws"],
+                                           workspace_bytes=1 << 20, stream=0, flags=bad) == mi.MI_ERR_INVALID_ARG
     assert step(dims=mi.dims(0, 4, 2, 64, 8, 4)) == mi.MI_OK
 
 

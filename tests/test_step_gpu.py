@@ -6,7 +6,8 @@ the fp64 oracle's append + attention. Covered: the small workloads in full,
 the Qwen3-8B-shaped serving layer at full size (every request and head
 against the oracle), edge context lengths, head
 dims 64 and 128 and several GQA groups, NaN in unused cache rows, a position
-past the RoPE table, and the overlap check on q / q_out."""
+past the RoPE table, the overlap check on q / q_out, and early start
+(MI_STEP_EARLY_START) over a stack of layers, eager and graph-replayed."""
 import numpy as np
 import pytest
 
@@ -213,3 +214,93 @@ def test_step_bad_position_and_overlap(cuda_device):
     assert np.all(got[2] == 0)
     # q_out over q (in place) is refused: other CTAs may still read q
     assert mi.mi_paged_decode_step(d, q_d, *args, q_d, kc_d, vc_d, out, ws, dev_err=err) == mi.MI_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_early_start_stack_matches_the_plain_stack(cuda_device, kv):
+    """A stack of fused steps at the Qwen3-8B serving layer's full size
+    (persistent grid, every layer's own caches and q / k / v), called with
+    MI_STEP_EARLY_START and two workspaces in turn, so that no step shares
+    its workspace with the kernel just before it: every layer's q_out, cache
+    and out carry the same bits as the stack called without the flag on one
+    workspace, both eagerly and replayed from a CUDA graph (twice: a replay
+    rewrites the same rows)."""
+    import torch
+    import bench
+    mi = _mi()
+    w = WORKLOADS["qwen3_8b"]
+    L = 3
+    fp8 = kv == "fp8"
+    lib, model, ctx = pools_for(w)
+    grow(lib, w.B, ctx + 1)
+    bt, cl, _ = lib.batch_meta(range(w.B))
+    shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
+    ks, vs = bench.fp8_scales(w)
+    ks_d, vs_d = torch.from_numpy(ks).to(cuda_device), torch.from_numpy(vs).to(cuda_device)
+    caches = []
+    for layer in range(L):
+        kc = torch.empty(shape, dtype=torch.uint8 if fp8 else torch.bfloat16, device=cuda_device)
+        vc = torch.empty_like(kc)
+        if fp8:
+            bench.device_fill_fp8(w, layer, kc, vc, ks, vs)
+        else:
+            device_fill_cache(w, layer, kc, vc)
+        caches.append((kc, vc))
+    qkv = [tuple(to_dev_u16(a, cuda_device) for a in new_token_values(w, layer)) for layer in range(L)]
+    _, table = mi.mi_rope_table(w.theta, w.head_dim, w.max_pos)
+    tab_d = torch.from_numpy(table).to(cuda_device)
+    d = mi.dims(w.B, w.Hq, w.Hkv, w.head_dim, w.num_blocks, w.max_blocks_per_seq)
+    bt_d, cl_d = to_dev_i32(bt, cuda_device), to_dev_i32(cl, cuda_device)
+    wsb = mi.mi_paged_decode_workspace_bytes(d) // 4 + 4
+    ws = [torch.empty(wsb, dtype=torch.float32, device=cuda_device) for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+
+    def run(cs, qo, out, flags):
+        for layer in range(L):
+            q_d, k_d, v_d = qkv[layer]
+            kc, vc = cs[layer]
+            wk = ws[layer % 2] if flags else ws[0]
+            if fp8:
+                st = mi.mi_paged_decode_step_fp8(d, q_d, k_d, v_d, tab_d, w.max_pos, bt_d, cl_d, ks_d, vs_d,
+                                                 w.scale, qo[layer], kc, vc, out[layer], wk, dev_err=err,
+                                                 flags=flags)
+            else:
+                st = mi.mi_paged_decode_step(d, q_d, k_d, v_d, tab_d, w.max_pos, bt_d, cl_d, w.scale, qo[layer], kc,
+                                             vc, out[layer], wk, dev_err=err, flags=flags)
+            assert st == 0, mi.status_string(st)
+
+    def fresh():
+        return ([(kc.clone(), vc.clone()) for kc, vc in caches],
+                [torch.full_like(qkv[0][0], float("nan")) for _ in range(L)],
+                [torch.full_like(qkv[0][0], float("nan")) for _ in range(L)])
+
+    def same(a, b, what):
+        ca, qa, oa = a
+        cb, qb, ob = b
+        for layer in range(L):
+            assert torch.equal(qa[layer].view(torch.int16), qb[layer].view(torch.int16)), f"{what} q_out {layer}"
+            assert torch.equal(oa[layer].view(torch.int16), ob[layer].view(torch.int16)), f"{what} out {layer}"
+            for x, y in zip(ca[layer], cb[layer]):
+                assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), f"{what} cache {layer}"
+
+    plain = fresh()
+    torch.cuda.synchronize()
+    run(*plain, flags=0)
+    torch.cuda.synchronize()
+    for rep in range(2):   # the second pass finds its plans in the workspaces
+        early = fresh()
+        torch.cuda.synchronize()
+        run(*early, flags=mi.MI_STEP_EARLY_START)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        same(plain, early, f"eager pass {rep}")
+    graph_bufs = fresh()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(*graph_bufs, flags=mi.MI_STEP_EARLY_START)
+    for rep in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        same(plain, graph_bufs, f"graph replay {rep}")
