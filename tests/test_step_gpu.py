@@ -217,23 +217,29 @@ def test_step_bad_position_and_overlap(cuda_device):
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_early_start_stack_matches_the_plain_stack(cuda_device, kv):
-    """A stack of fused steps at the Qwen3-8B serving layer's full size
-    (persistent grid, every layer's own caches and q / k / v), called with
-    MI_STEP_EARLY_START and two workspaces in turn, so that no step shares
-    its workspace with the kernel just before it: every layer's q_out, cache
-    and out carry the same bits as the stack called without the flag on one
-    workspace, both eagerly and replayed from a CUDA graph (twice: a replay
-    rewrites the same rows)."""
+@pytest.mark.parametrize("name", ["qwen3_8b", "tiny", "qwen3_1p7b", "skewed", "empty_rows"])
+def test_early_start_stack_matches_the_plain_stack(cuda_device, kv, name):
+    """A stack of fused steps (every layer's own caches and q / k / v),
+    called with MI_STEP_EARLY_START and two workspaces in turn, so that no
+    step shares its workspace with the kernel just before it: every layer's
+    q_out, cache and out carry the same bits as the stack called without the
+    flag on one workspace, both eagerly and replayed from a CUDA graph
+    (twice: a replay rewrites the same rows). Workloads: the Qwen3-8B
+    serving layer at full size (persistent grid), the small ones (a grid
+    cut to fewer CTAs than SMs) and the skewed batch, and the Qwen3-1.7B
+    layer with two requests of length 0 (zero rows, nothing appended)."""
     import torch
     import bench
     mi = _mi()
-    w = WORKLOADS["qwen3_8b"]
+    w = WORKLOADS["qwen3_1p7b" if name == "empty_rows" else name]
     L = 3
     fp8 = kv == "fp8"
     lib, model, ctx = pools_for(w)
     grow(lib, w.B, ctx + 1)
     bt, cl, _ = lib.batch_meta(range(w.B))
+    if name == "empty_rows":
+        cl = cl.copy()
+        cl[[1, 5]] = 0
     shape = (w.num_blocks, w.Hkv, BLOCK, w.head_dim)
     ks, vs = bench.fp8_scales(w)
     ks_d, vs_d = torch.from_numpy(ks).to(cuda_device), torch.from_numpy(vs).to(cuda_device)
