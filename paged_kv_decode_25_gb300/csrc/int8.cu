@@ -33,6 +33,8 @@ namespace {
 constexpr int kGroup = 64;
 constexpr int kMaxThreads = 512;
 constexpr int kQWords = 8;  // q words a thread holds at once
+constexpr int kRequantRows = 16;  // open-buffer rows a lane loads at once when a group is quantised again
+static_assert(kGroup % kRequantRows == 0, "a batch of rows never runs past the group's buffer");
 
 struct Int8AppendParams {
     const uint16_t* q;             // [B][Hq][d] raw
@@ -199,16 +201,33 @@ __global__ void __launch_bounds__(kMaxThreads) append_int8_kernel(Int8AppendPara
         const float m = fmaxf(m_old, rmax);
         const float s = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;  // m = 0: every code is 0
         if (o > 0 && m > m_old) {
-            // the maximum grew: the whole group again, from its bf16 rows
+            // the maximum grew: the whole group again, from its bf16 rows,
+            // kRequantRows rows' loads in flight before their codes are
+            // stored (one row at a time put o + 1 dependent trips to L2 on
+            // the warp's path)
             __syncwarp();
-            for (int t = 0; t <= o; ++t) {
-                const int blk = pick4(gblk, t / kBlock);
-                int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + (t0 + t) % kBlock) * d;
-                if (own) {
-                    const uint32_t wl = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane);
-                    const uint32_t wh = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane + half);
-                    *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(wl, s);
-                    *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(wh, s);
+            for (int tb = 0; tb <= o; tb += kRequantRows) {
+                // rows tb .. tb + kRequantRows - 1 lie inside the group's
+                // 64-row buffer (tb <= o < 64, kRequantRows divides 64), so
+                // they load unconditionally; only rows up to o are stored
+                uint32_t wl[kRequantRows], wh[kRequantRows];
+#pragma unroll
+                for (int u = 0; u < kRequantRows; ++u) {
+                    const int t = tb + u;
+                    if (own) {
+                        wl[u] = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane);
+                        wh[u] = *reinterpret_cast<const uint32_t*>(grp + (long long)t * d + 2 * lane + half);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRequantRows; ++u) {
+                    const int t = tb + u;
+                    if (own && t <= o) {
+                        const int blk = pick4(gblk, t / kBlock);
+                        int8_t* row = cache + (((long long)blk * a.Hkv + h) * kBlock + (t0 + t) % kBlock) * d;
+                        *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)code_pair(wl[u], s);
+                        *reinterpret_cast<uint16_t*>(row + 2 * lane + half) = (uint16_t)code_pair(wh[u], s);
+                    }
                 }
             }
 #pragma unroll
