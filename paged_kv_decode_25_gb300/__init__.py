@@ -367,6 +367,10 @@ def mi_paged_decode_attention_variant(d: MiDims, q, k_cache, v_cache, block_tabl
 def mi_paged_decode_step(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, scale, q_out,
                          k_cache, v_cache, out, workspace, workspace_bytes=None, dev_err=None, stream=None,
                          flags=0):
+    """flags: 0 or MI_STEP_EARLY_START (the step plans and issues its first
+    KV copies before the kernel ahead of it on the stream ends; the caller
+    keeps the contract of include/mi.h, e.g. two workspaces in turn for
+    consecutive early-start calls)."""
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return load().mi_paged_decode_step(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
                                        int(max_pos), _ptr(block_tables), _ptr(context_lens), float(scale),
@@ -471,6 +475,7 @@ def mi_paged_decode_attention_noalloc(d: MiDims, q, k_cache, v_cache, block_tabl
 def mi_paged_decode_step_fp8(d: MiDims, q, k, v, rope_cos_sin, max_pos, block_tables, context_lens, k_scale,
                              v_scale, scale, q_out, k_cache, v_cache, out, workspace, workspace_bytes=None,
                              dev_err=None, stream=None, flags=0):
+    """flags as for mi_paged_decode_step."""
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return load().mi_paged_decode_step_fp8(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(rope_cos_sin),
                                            int(max_pos), _ptr(block_tables), _ptr(context_lens), _ptr(k_scale),
